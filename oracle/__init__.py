@@ -1,0 +1,302 @@
+"""CPU oracle for the sparse MoE expert block -- TEST INFRASTRUCTURE ONLY.
+
+Only the test suite, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The CUDA path (the package
+``mixture_experts_ffn_histogram_gb300``) never imports it, and the two share
+no code: the oracle is ``oracle.c`` compiled with gcc (``-O3 -fopenmp
+-ffp-contract=off``), wrapped here with ctypes over numpy arrays.
+
+bf16 tensors cross this boundary as numpy ``uint16`` arrays of raw bit
+patterns; see ``oracle.h`` for the definitions each function writes out.
+"""
+from __future__ import annotations
+
+import contextlib
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB_PATH = os.path.join(_HERE, "_build", "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+SOFTMAX_TOPK, SIGMOID_NORM, GIVEN = 0, 1, 2
+
+
+def build(force: bool = False, src: str = _SRC, out: str = _LIB_PATH) -> str:
+    """Compile ``oracle.c`` into a shared library with gcc; returns its path."""
+    os.makedirs(os.path.dirname(out), exist_ok=True)
+    if (not force and os.path.exists(out)
+            and os.path.getmtime(out) >= max(os.path.getmtime(src),
+                                              os.path.getmtime(os.path.join(_HERE, "oracle.h")))):
+        return out
+    base = ["gcc", "-std=c11", "-O3", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared",
+            "-I", _HERE, src, "-o", out + ".tmp", "-lm"]
+    try:
+        subprocess.run(base[:1] + ["-fopenmp"] + base[1:], check=True, capture_output=True)
+    except subprocess.CalledProcessError:
+        subprocess.run(base, check=True, capture_output=True)   # no OpenMP runtime: 1 thread
+    os.replace(out + ".tmp", out)
+    return out
+
+
+def load_library(path: str) -> ctypes.CDLL:
+    lib = ctypes.CDLL(path)
+    P = ctypes.c_void_p
+    I = ctypes.c_int
+    sig = {
+        "oracle_f32_to_bf16": ([ctypes.c_float], ctypes.c_uint16),
+        "oracle_bf16_to_f32": ([ctypes.c_uint16], ctypes.c_float),
+        "oracle_route": ([P, P, I, I, I, I, P, P], I),
+        "oracle_histogram": ([P, I, I, I, P, P, P, P], I),
+        "oracle_permute": ([P, P, I, I, I, P], I),
+        "oracle_fc1_swiglu": ([P, P, P, I, I, I, P, P], I),
+        "oracle_fc2": ([P, P, P, I, I, I, P], I),
+        "oracle_combine": ([P, P, P, I, I, I, P], I),
+        "oracle_combine_bwd": ([P, P, P, P, I, I, I, P, P], I),
+        "oracle_fc2_bwd": ([P, P, P, P, P, I, I, I, P, P], I),
+        "oracle_swiglu_bwd": ([P, P, I, I, P], I),
+        "oracle_fc1_bwd": ([P, P, P, P, I, I, I, P, P], I),
+        "oracle_permute_bwd": ([P, P, I, I, I, P], I),
+        "oracle_num_threads": ([], I),
+    }
+    for name, (args, res) in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = res
+    return lib
+
+
+def lib() -> ctypes.CDLL:
+    global _lib
+    with _lock:
+        if _lib is None:
+            _lib = load_library(build())
+        return _lib
+
+
+@contextlib.contextmanager
+def using_library(path: str):
+    """Temporarily route every wrapper through another build of the oracle
+    (used by the test that plants mistakes in copies of ``oracle.c``)."""
+    global _lib
+    other = load_library(path)
+    with _lock:
+        old = _lib
+        _lib = other
+    try:
+        yield
+    finally:
+        with _lock:
+            _lib = old
+
+
+def _p(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _c(a, dtype):
+    return None if a is None else np.ascontiguousarray(a, dtype=dtype)
+
+
+def _check(rc, name):
+    if rc < 0:
+        raise ValueError(f"{name}: bad arguments (rc={rc})")
+    return rc
+
+
+# ----------------------------------------------------------------- wrappers
+def f32_to_bf16(a) -> np.ndarray:
+    """RNE rounding of an fp32 array to bf16 bit patterns (elementwise)."""
+    L = lib()
+    a = np.asarray(a, dtype=np.float32)
+    return np.array([L.oracle_f32_to_bf16(float(v)) for v in a.ravel()],
+                    dtype=np.uint16).reshape(a.shape)
+
+
+def bf16_to_f32(b) -> np.ndarray:
+    """Exact widening of bf16 bit patterns to fp32."""
+    b = np.asarray(b, dtype=np.uint16)
+    return (b.astype(np.uint32) << 16).view(np.float32)
+
+
+def route(logits, bias, mode, T, E, K):
+    ids = np.empty((T, K), np.int32)
+    w = np.empty((T, K), np.float32)
+    logits = _c(logits, np.float32)
+    bias = _c(bias, np.float32)
+    _check(lib().oracle_route(_p(logits), _p(bias), mode, T, E, K, _p(ids), _p(w)), "route")
+    return ids, w
+
+
+def histogram(ids, E):
+    ids = _c(ids, np.int32)
+    T, K = ids.shape
+    gs = np.empty(E, np.int32)
+    off = np.empty(E + 1, np.int32)
+    pos = np.empty((T, K), np.int32)
+    row_src = np.empty(T * K, np.int32)
+    bad = _check(lib().oracle_histogram(_p(ids), T, K, E, _p(gs), _p(off), _p(pos), _p(row_src)),
+                 "histogram")
+    return gs, off, pos, row_src, bad
+
+
+def permute(x, pos):
+    x = _c(x, np.uint16)
+    pos = _c(pos, np.int32)
+    T, D = x.shape
+    K = pos.shape[1]
+    xs = np.zeros((T * K, D), np.uint16)
+    _check(lib().oracle_permute(_p(x), _p(pos), T, K, D, _p(xs)), "permute")
+    return xs
+
+
+def fc1_swiglu(xs, wi, offs, want_z=True):
+    xs = _c(xs, np.uint16)
+    wi = _c(wi, np.uint16)
+    offs = _c(offs, np.int32)
+    E, D, N = wi.shape
+    F = N // 2
+    R = int(offs[E])
+    h = np.zeros((R, F), np.uint16)
+    z = np.zeros((R, N), np.uint16) if want_z else None
+    _check(lib().oracle_fc1_swiglu(_p(xs), _p(wi), _p(offs), E, D, F, _p(h), _p(z)), "fc1")
+    return h, z
+
+
+def fc2(h, wo, offs):
+    h = _c(h, np.uint16)
+    wo = _c(wo, np.uint16)
+    offs = _c(offs, np.int32)
+    E, F, D = wo.shape
+    R = int(offs[E])
+    ys = np.zeros((R, D), np.uint16)
+    _check(lib().oracle_fc2(_p(h), _p(wo), _p(offs), E, F, D, _p(ys)), "fc2")
+    return ys
+
+
+def combine(ys, w, pos, T, D):
+    ys = _c(ys, np.uint16)
+    w = _c(w, np.float32)
+    pos = _c(pos, np.int32)
+    K = pos.shape[1]
+    out = np.zeros((T, D), np.uint16)
+    _check(lib().oracle_combine(_p(ys), _p(w), _p(pos), T, K, D, _p(out)), "combine")
+    return out
+
+
+def combine_bwd(dout, ys, w, pos):
+    dout = _c(dout, np.uint16)
+    ys = _c(ys, np.uint16)
+    w = _c(w, np.float32)
+    pos = _c(pos, np.int32)
+    T, D = dout.shape
+    K = pos.shape[1]
+    dys = np.zeros((ys.shape[0], D), np.uint16)
+    dw = np.zeros((T, K), np.float32)
+    _check(lib().oracle_combine_bwd(_p(dout), _p(ys), _p(w), _p(pos), T, K, D, _p(dys), _p(dw)),
+           "combine_bwd")
+    return dys, dw
+
+
+def fc2_bwd(dys, h, wo, z, offs, want_dlhs=True, want_drhs=True):
+    dys = _c(dys, np.uint16)
+    h = _c(h, np.uint16)
+    wo = _c(wo, np.uint16)
+    z = _c(z, np.uint16)
+    offs = _c(offs, np.int32)
+    E, F, D = wo.shape
+    R = int(offs[E])
+    g = np.zeros((R, 2 * F if z is not None else F), np.uint16) if want_dlhs else None
+    dwo = np.zeros((E, F, D), np.uint16) if want_drhs else None
+    _check(lib().oracle_fc2_bwd(_p(dys), _p(h), _p(wo), _p(z), _p(offs), E, F, D, _p(g), _p(dwo)),
+           "fc2_bwd")
+    return g, dwo
+
+
+def swiglu_bwd(dh, z):
+    dh = _c(dh, np.uint16)
+    z = _c(z, np.uint16)
+    R, F = dh.shape
+    dz = np.zeros((R, 2 * F), np.uint16)
+    _check(lib().oracle_swiglu_bwd(_p(dh), _p(z), R, F, _p(dz)), "swiglu_bwd")
+    return dz
+
+
+def fc1_bwd(dz, xs, wi, offs, want_dlhs=True, want_drhs=True):
+    dz = _c(dz, np.uint16)
+    xs = _c(xs, np.uint16)
+    wi = _c(wi, np.uint16)
+    offs = _c(offs, np.int32)
+    E, D, N = wi.shape
+    F = N // 2
+    R = int(offs[E])
+    dxs = np.zeros((R, D), np.uint16) if want_dlhs else None
+    dwi = np.zeros((E, D, N), np.uint16) if want_drhs else None
+    _check(lib().oracle_fc1_bwd(_p(dz), _p(xs), _p(wi), _p(offs), E, D, F, _p(dxs), _p(dwi)),
+           "fc1_bwd")
+    return dxs, dwi
+
+
+def permute_bwd(dxs, pos, T, D):
+    dxs = _c(dxs, np.uint16)
+    pos = _c(pos, np.int32)
+    K = pos.shape[1]
+    dx = np.zeros((T, D), np.uint16)
+    _check(lib().oracle_permute_bwd(_p(dxs), _p(pos), T, K, D, _p(dx)), "permute_bwd")
+    return dx
+
+
+def num_threads() -> int:
+    return int(lib().oracle_num_threads())
+
+
+# ------------------------------------------------------- whole-block drivers
+def block_forward(inp: dict, want_z: bool = True) -> dict:
+    """Run the forward steps in order on numpy copies of ``inp`` (a dict from
+    ``mixture_experts_ffn_histogram_gb300.inputs.make_inputs`` converted by
+    :func:`to_numpy`).  Returns every intermediate."""
+    wl = inp["workload"]
+    T, D, E, K, F = wl.T, wl.D, wl.E, wl.K, wl.F
+    if wl.score_mode == GIVEN:
+        ids, w = inp["ids"], inp["w"]
+    else:
+        ids, w = route(inp["logits"], inp["bias"], wl.score_mode, T, E, K)
+    gs, off, pos, row_src, bad = histogram(ids, E)
+    xs = permute(inp["x"], pos)
+    h, z = fc1_swiglu(xs, inp["wi"], off, want_z=want_z)
+    ys = fc2(h, inp["wo"], off)
+    out = combine(ys, w, pos, T, D)
+    return dict(ids=ids, w=w, group_sizes=gs, group_offsets=off, pos=pos, row_src=row_src,
+                bad=bad, xs=xs, h=h, z=z, ys=ys, out=out)
+
+
+def block_backward(inp: dict, fwd: dict) -> dict:
+    """The backward steps in order (fused SwiGLU backward inside FC2's)."""
+    wl = inp["workload"]
+    T, D = wl.T, wl.D
+    dys, dw = combine_bwd(inp["dy"], fwd["ys"], fwd["w"], fwd["pos"])
+    dz, dwo = fc2_bwd(dys, fwd["h"], inp["wo"], fwd["z"], fwd["group_offsets"])
+    dxs, dwi = fc1_bwd(dz, fwd["xs"], inp["wi"], fwd["group_offsets"])
+    dx = permute_bwd(dxs, fwd["pos"], T, D)
+    return dict(dys=dys, dw=dw, dz=dz, dwo=dwo, dxs=dxs, dwi=dwi, dx=dx)
+
+
+def to_numpy(inp: dict) -> dict:
+    """Convert the torch tensors of an input dict to numpy (bf16 -> uint16 bits)."""
+    import torch
+    out = {}
+    for k, v in inp.items():
+        if isinstance(v, torch.Tensor):
+            v = v.detach().contiguous().cpu()
+            if v.dtype == torch.bfloat16:
+                v = v.view(torch.int16).numpy().view(np.uint16)
+            else:
+                v = v.numpy()
+        out[k] = v
+    return out

@@ -1,0 +1,397 @@
+/*
+ * CPU oracle for the sparse MoE expert block -- TEST INFRASTRUCTURE ONLY.
+ * (See oracle.h for who may use it and for the conventions.)
+ *
+ * This file writes out the plain definition of each step of the block, one
+ * function per entry point of the CUDA library, in the order and notation of
+ * the pages it follows:
+ *
+ *   [Keep fused]  MaxText "Keep fused MoE weights intact through FSDP gather",
+ *                 Description (updated flow: one grouped GEMM on the prefused
+ *                 [experts, embed, 2*mlp] weight, then split the output
+ *                 activations for SwiGLU).
+ *   [Fused p/c]   MaxText "MoE: fused TensorCore Pallas permute/combine
+ *                 kernels and split-expert wi layout for TPU v6e", Context
+ *                 item 1 and Commits table rows 1-2 (combine = unpermute +
+ *                 top-K weighted sum; its backward = a permutation for dx and
+ *                 a per-slot reduction for dw; permute = gather into expert-
+ *                 sorted order with the group_size histogram computed first;
+ *                 permute backward = combine with unit weights) and Tests
+ *                 (f32 routing weights).
+ *   [Gemma4 L/M]  MaxText "Gemma4 26B MoE on TPU v6e: MaxText layer/model
+ *                 optimizations", Commits table row 6 (top_k_weights and
+ *                 group_size), row 7 and the code-review suggestion
+ *                 (_split_gate_up_bwd: the gate/up gradient is one
+ *                 concatenation [grad_gate, grad_up] along the last axis).
+ *   [TE MoE]      TransformerEngine "[DRAFT][JAX] Optimize MoE block",
+ *                 Flowchart (routing -> grouped FC1 -> activation and
+ *                 grouped FC2 -> combine).
+ *
+ * Readings where the pages are silent (each is also listed in the design
+ * notes):  top-K ties go to the lower expert id; the expert-sorted order is
+ * stable in the flat slot index t*K+k; gate = columns [0,F) of wi's last
+ * axis and up = [F,2F); bf16 rounding exactly where a tensor is stored; the
+ * block is dropless.
+ *
+ * Parity pins: every function here is checked against brute force, library
+ * routines, closed forms, finite differences and invariants by the CPU test
+ * suite; none is "parity unpinned".
+ */
+#include "oracle.h"
+
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+uint16_t oracle_f32_to_bf16(float f) {
+  uint32_t u;
+  memcpy(&u, &f, 4);
+  if ((u & 0x7fffffffu) > 0x7f800000u) return (uint16_t)((u >> 16) | 0x0040u); /* quiet NaN */
+  /* round to nearest, ties to even, on the 16 discarded bits */
+  uint32_t lsb = (u >> 16) & 1u;
+  u += 0x7fffu + lsb;
+  return (uint16_t)(u >> 16);
+}
+
+float oracle_bf16_to_f32(uint16_t b) {
+  uint32_t u = ((uint32_t)b) << 16;
+  float f;
+  memcpy(&f, &u, 4);
+  return f;
+}
+
+#define BF(b) oracle_bf16_to_f32(b)
+#define RN(f) oracle_f32_to_bf16(f)
+
+int oracle_num_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}
+
+static float sigmoidf_(float v) { return 1.0f / (1.0f + expf(-v)); }
+
+/* Step 1, routing [Gemma4 L/M row 6]: per token, the K largest scores in
+ * descending order (ties: lower expert id first), and their weights:
+ *   SOFTMAX_TOPK: w_k = exp(s_k - s_0) / sum_j exp(s_j - s_0) over the K selected;
+ *   SIGMOID_NORM: w_k = sigmoid(s_k) / sum_j sigmoid(s_j) over the K selected;
+ * with s = logit (+ bias[e] when a bias is given).  GIVEN: ids/w are inputs. */
+int oracle_route(const float* logits, const float* bias, int mode, int T, int E, int K,
+                 int32_t* ids, float* w) {
+  if (T < 0 || E <= 0 || K <= 0 || K > E) return -1;
+  if (mode == ORACLE_GIVEN) return 0;
+  if (mode != ORACLE_SOFTMAX_TOPK && mode != ORACLE_SIGMOID_NORM) return -1;
+  int bad = 0;
+#pragma omp parallel for schedule(static)
+  for (int t = 0; t < T; ++t) {
+    float* s = (float*)malloc(sizeof(float) * (size_t)E);
+    unsigned char* taken = (unsigned char*)calloc((size_t)E, 1);
+    for (int e = 0; e < E; ++e) {
+      float v = logits[(size_t)t * E + e];
+      s[e] = bias ? v + bias[e] : v;
+    }
+    for (int k = 0; k < K; ++k) {
+      int best = -1;
+      for (int e = 0; e < E; ++e) {
+        if (taken[e]) continue;
+        if (best < 0 || s[e] > s[best]) best = e;  /* strict: ties keep the lower id */
+      }
+      taken[best] = 1;
+      ids[(size_t)t * K + k] = best;
+    }
+    float sum = 0.0f;
+    float* v = w + (size_t)t * K;
+    if (mode == ORACLE_SOFTMAX_TOPK) {
+      float m = s[ids[(size_t)t * K]];
+      for (int k = 0; k < K; ++k) { v[k] = expf(s[ids[(size_t)t * K + k]] - m); sum = sum + v[k]; }
+    } else {
+      for (int k = 0; k < K; ++k) { v[k] = sigmoidf_(s[ids[(size_t)t * K + k]]); sum = sum + v[k]; }
+    }
+    for (int k = 0; k < K; ++k) v[k] = v[k] / sum;
+    free(s);
+    free(taken);
+  }
+  return bad;
+}
+
+/* Step 2, group_size histogram above the gather [Fused p/c row 2; Gemma4 L/M
+ * row 6]: flatten ids token-major (j = t*K + k);
+ *   group_sizes[e] = #{j : ids[j] = e};  group_offsets = exclusive prefix sum;
+ *   pos[j] = group_offsets[ids[j]] + #{j' < j : ids[j'] = ids[j]}  (stable);
+ *   row_src[pos[j]] = j.
+ * Slots whose id lies outside [0,E) get pos = -1 and are not counted; the
+ * rows left over at the end of row_src are -1.  Returns that slot count. */
+int oracle_histogram(const int32_t* ids, int T, int K, int E, int32_t* group_sizes,
+                     int32_t* group_offsets, int32_t* pos, int32_t* row_src) {
+  if (T < 0 || K <= 0 || E <= 0) return -1;
+  const long R = (long)T * K;
+  int bad = 0;
+  for (int e = 0; e < E; ++e) group_sizes[e] = 0;
+  for (long j = 0; j < R; ++j) {
+    int e = ids[j];
+    if (e < 0 || e >= E) { ++bad; continue; }
+    group_sizes[e] += 1;
+  }
+  group_offsets[0] = 0;
+  for (int e = 0; e < E; ++e) group_offsets[e + 1] = group_offsets[e] + group_sizes[e];
+  int32_t* seen = (int32_t*)calloc((size_t)E, sizeof(int32_t));
+  for (long j = 0; j < R; ++j) row_src[j] = -1;
+  for (long j = 0; j < R; ++j) {
+    int e = ids[j];
+    if (e < 0 || e >= E) { pos[j] = -1; continue; }
+    int p = group_offsets[e] + seen[e];
+    seen[e] += 1;
+    pos[j] = p;
+    row_src[p] = (int32_t)j;
+  }
+  free(seen);
+  return bad;
+}
+
+/* Step 3, permute [Fused p/c Context 1, row 2]: xs[pos[t,k]] = x[t] (exact). */
+int oracle_permute(const uint16_t* x, const int32_t* pos, int T, int K, int D, uint16_t* xs) {
+  if (T < 0 || K <= 0 || D <= 0) return -1;
+#pragma omp parallel for schedule(static)
+  for (int t = 0; t < T; ++t)
+    for (int k = 0; k < K; ++k) {
+      int p = pos[(size_t)t * K + k];
+      if (p < 0) continue;
+      memcpy(xs + (size_t)p * D, x + (size_t)t * D, sizeof(uint16_t) * (size_t)D);
+    }
+  return 0;
+}
+
+/* Step 4, FC1 + SwiGLU [Keep fused, Description; TE MoE, Flowchart]: for
+ * every row r of group e, a[n] = sum_d xs[r,d] * wi[e,d,n] over the whole
+ * prefused weight (n < 2F), then g = a[0:F], u = a[F:2F],
+ *   h[r,f] = bf16(silu(g_f) * u_f),  silu(g) = g * sigmoid(g);
+ *   z[r,n] = bf16(a[n])  (stored for the backward when z != NULL). */
+int oracle_fc1_swiglu(const uint16_t* xs, const uint16_t* wi, const int32_t* offs, int E,
+                      int D, int F, uint16_t* h, uint16_t* z) {
+  if (E <= 0 || D <= 0 || F <= 0) return -1;
+  const int N = 2 * F;
+  const int R = offs[E];
+#pragma omp parallel
+  {
+    float* a = (float*)malloc(sizeof(float) * (size_t)N);
+#pragma omp for schedule(dynamic, 4)
+    for (int r = 0; r < R; ++r) {
+      int e = 0;
+      while (offs[e + 1] <= r) ++e;
+      const uint16_t* W = wi + (size_t)e * D * N;
+      for (int n = 0; n < N; ++n) a[n] = 0.0f;
+      for (int d = 0; d < D; ++d) {
+        float xv = BF(xs[(size_t)r * D + d]);
+        const uint16_t* wr = W + (size_t)d * N;
+        for (int n = 0; n < N; ++n) a[n] = a[n] + xv * BF(wr[n]);
+      }
+      for (int f = 0; f < F; ++f) {
+        float g = a[f], u = a[F + f];
+        h[(size_t)r * F + f] = RN((g * sigmoidf_(g)) * u);
+      }
+      if (z)
+        for (int n = 0; n < N; ++n) z[(size_t)r * N + n] = RN(a[n]);
+    }
+    free(a);
+  }
+  return 0;
+}
+
+/* Step 5, FC2 [TE MoE, Flowchart]: ys[r,:] = bf16(sum_f h[r,f] * wo[e,f,:]). */
+int oracle_fc2(const uint16_t* h, const uint16_t* wo, const int32_t* offs, int E, int F, int D,
+               uint16_t* ys) {
+  if (E <= 0 || D <= 0 || F <= 0) return -1;
+  const int R = offs[E];
+#pragma omp parallel
+  {
+    float* a = (float*)malloc(sizeof(float) * (size_t)D);
+#pragma omp for schedule(dynamic, 4)
+    for (int r = 0; r < R; ++r) {
+      int e = 0;
+      while (offs[e + 1] <= r) ++e;
+      const uint16_t* W = wo + (size_t)e * F * D;
+      for (int d = 0; d < D; ++d) a[d] = 0.0f;
+      for (int f = 0; f < F; ++f) {
+        float hv = BF(h[(size_t)r * F + f]);
+        const uint16_t* wr = W + (size_t)f * D;
+        for (int d = 0; d < D; ++d) a[d] = a[d] + hv * BF(wr[d]);
+      }
+      for (int d = 0; d < D; ++d) ys[(size_t)r * D + d] = RN(a[d]);
+    }
+    free(a);
+  }
+  return 0;
+}
+
+/* Step 6, combine [Fused p/c row 1]: unpermute plus the top-K weighted sum,
+ *   out[t] = bf16(sum_{k ascending} w[t,k] * ys[pos[t,k]]). */
+int oracle_combine(const uint16_t* ys, const float* w, const int32_t* pos, int T, int K, int D,
+                   uint16_t* out) {
+  if (T < 0 || K <= 0 || D <= 0) return -1;
+#pragma omp parallel for schedule(static)
+  for (int t = 0; t < T; ++t)
+    for (int d = 0; d < D; ++d) {
+      float acc = 0.0f;
+      for (int k = 0; k < K; ++k) {
+        int p = pos[(size_t)t * K + k];
+        if (p < 0) continue;
+        float wk = w ? w[(size_t)t * K + k] : 1.0f;
+        acc = acc + wk * BF(ys[(size_t)p * D + d]);
+      }
+      out[(size_t)t * D + d] = RN(acc);
+    }
+  return 0;
+}
+
+/* Backward of the combine [Fused p/c row 1: a permutation for dx and a
+ * per-slot reduction for dw]:
+ *   dys[pos[t,k]] = bf16(w[t,k] * dout[t]);
+ *   dw[t,k] = sum_d dout[t,d] * ys[pos[t,k], d]  (fp32). */
+int oracle_combine_bwd(const uint16_t* dout, const uint16_t* ys, const float* w,
+                       const int32_t* pos, int T, int K, int D, uint16_t* dys, float* dw) {
+  if (T < 0 || K <= 0 || D <= 0) return -1;
+#pragma omp parallel for schedule(static)
+  for (int t = 0; t < T; ++t)
+    for (int k = 0; k < K; ++k) {
+      int p = pos[(size_t)t * K + k];
+      if (p < 0) { dw[(size_t)t * K + k] = 0.0f; continue; }
+      float wk = w[(size_t)t * K + k];
+      float acc = 0.0f;
+      for (int d = 0; d < D; ++d) {
+        float g = BF(dout[(size_t)t * D + d]);
+        dys[(size_t)p * D + d] = RN(wk * g);
+        acc = acc + g * BF(ys[(size_t)p * D + d]);
+      }
+      dw[(size_t)t * K + k] = acc;
+    }
+  return 0;
+}
+
+/* SwiGLU backward at one element [Gemma4 L/M row 7 and review suggestion]:
+ * with s = sigmoid(g), h = g*s*u:
+ *   dgate = dh * u * s * (1 + g*(1 - s)),  dup = dh * g * s,
+ * and dz = [dgate | dup] written as one [R, 2F] tensor (a concatenation). */
+static void swiglu_bwd_one(float dh, float g, float u, float* dgate, float* dup) {
+  float s = sigmoidf_(g);
+  *dgate = ((dh * u) * s) * (1.0f + g * (1.0f - s));
+  *dup = (dh * g) * s;
+}
+
+/* Backward of FC2: dlhs dh[r,f] = sum_d dys[r,d] * wo[e,f,d] (the gradient
+ * against the transposed wo), kept in fp32 and passed through the SwiGLU
+ * backward when z is given (output dz [R,2F]), else stored as bf16 dh [R,F];
+ * drhs dwo[e,f,d] = bf16(sum_{r in group e, ascending} h[r,f] * dys[r,d]),
+ * zero for an empty group. */
+int oracle_fc2_bwd(const uint16_t* dys, const uint16_t* h, const uint16_t* wo,
+                   const uint16_t* z, const int32_t* offs, int E, int F, int D,
+                   uint16_t* dh_or_dz, uint16_t* dwo) {
+  if (E <= 0 || D <= 0 || F <= 0) return -1;
+  const int R = offs[E];
+  if (dh_or_dz) {
+#pragma omp parallel for schedule(dynamic, 4)
+    for (int r = 0; r < R; ++r) {
+      int e = 0;
+      while (offs[e + 1] <= r) ++e;
+      const uint16_t* W = wo + (size_t)e * F * D;
+      for (int f = 0; f < F; ++f) {
+        float acc = 0.0f;
+        for (int d = 0; d < D; ++d) acc = acc + BF(dys[(size_t)r * D + d]) * BF(W[(size_t)f * D + d]);
+        if (z) {
+          float dg, du;
+          swiglu_bwd_one(acc, BF(z[(size_t)r * 2 * F + f]), BF(z[(size_t)r * 2 * F + F + f]), &dg, &du);
+          dh_or_dz[(size_t)r * 2 * F + f] = RN(dg);
+          dh_or_dz[(size_t)r * 2 * F + F + f] = RN(du);
+        } else {
+          dh_or_dz[(size_t)r * F + f] = RN(acc);
+        }
+      }
+    }
+  }
+  if (dwo) {
+#pragma omp parallel
+    {
+      float* a = (float*)malloc(sizeof(float) * (size_t)D);
+#pragma omp for collapse(2) schedule(dynamic, 4)
+      for (int e = 0; e < E; ++e)
+        for (int f = 0; f < F; ++f) {
+          for (int d = 0; d < D; ++d) a[d] = 0.0f;
+          for (int r = offs[e]; r < offs[e + 1]; ++r) {
+            float hv = BF(h[(size_t)r * F + f]);
+            for (int d = 0; d < D; ++d) a[d] = a[d] + hv * BF(dys[(size_t)r * D + d]);
+          }
+          for (int d = 0; d < D; ++d) dwo[((size_t)e * F + f) * D + d] = RN(a[d]);
+        }
+      free(a);
+    }
+  }
+  return 0;
+}
+
+/* The SwiGLU backward on its own, from a stored bf16 dh [R,F] and z [R,2F]. */
+int oracle_swiglu_bwd(const uint16_t* dh, const uint16_t* z, int R, int F, uint16_t* dz) {
+  if (R < 0 || F <= 0) return -1;
+#pragma omp parallel for schedule(static)
+  for (int r = 0; r < R; ++r)
+    for (int f = 0; f < F; ++f) {
+      float dg, du;
+      swiglu_bwd_one(BF(dh[(size_t)r * F + f]), BF(z[(size_t)r * 2 * F + f]),
+                     BF(z[(size_t)r * 2 * F + F + f]), &dg, &du);
+      dz[(size_t)r * 2 * F + f] = RN(dg);
+      dz[(size_t)r * 2 * F + F + f] = RN(du);
+    }
+  return 0;
+}
+
+/* Backward of FC1 against the whole prefused wi: dlhs
+ *   dxs[r,d] = bf16(sum_{n<2F} dz[r,n] * wi[e,d,n])  (the transposed wi),
+ * drhs dwi[e,d,n] = bf16(sum_{r in group e, ascending} xs[r,d] * dz[r,n]),
+ * zero for an empty group. */
+int oracle_fc1_bwd(const uint16_t* dz, const uint16_t* xs, const uint16_t* wi,
+                   const int32_t* offs, int E, int D, int F, uint16_t* dxs, uint16_t* dwi) {
+  if (E <= 0 || D <= 0 || F <= 0) return -1;
+  const int N = 2 * F;
+  const int R = offs[E];
+  if (dxs) {
+#pragma omp parallel for schedule(dynamic, 4)
+    for (int r = 0; r < R; ++r) {
+      int e = 0;
+      while (offs[e + 1] <= r) ++e;
+      const uint16_t* W = wi + (size_t)e * D * N;
+      for (int d = 0; d < D; ++d) {
+        float acc = 0.0f;
+        for (int n = 0; n < N; ++n) acc = acc + BF(dz[(size_t)r * N + n]) * BF(W[(size_t)d * N + n]);
+        dxs[(size_t)r * D + d] = RN(acc);
+      }
+    }
+  }
+  if (dwi) {
+#pragma omp parallel
+    {
+      float* a = (float*)malloc(sizeof(float) * (size_t)N);
+#pragma omp for collapse(2) schedule(dynamic, 4)
+      for (int e = 0; e < E; ++e)
+        for (int d = 0; d < D; ++d) {
+          for (int n = 0; n < N; ++n) a[n] = 0.0f;
+          for (int r = offs[e]; r < offs[e + 1]; ++r) {
+            float xv = BF(xs[(size_t)r * D + d]);
+            for (int n = 0; n < N; ++n) a[n] = a[n] + xv * BF(dz[(size_t)r * N + n]);
+          }
+          for (int n = 0; n < N; ++n) dwi[((size_t)e * D + d) * N + n] = RN(a[n]);
+        }
+      free(a);
+    }
+  }
+  return 0;
+}
+
+/* Backward of the permute [Fused p/c row 2]: the combine with unit weights,
+ *   dx[t] = bf16(sum_{k ascending} dxs[pos[t,k]]). */
+int oracle_permute_bwd(const uint16_t* dxs, const int32_t* pos, int T, int K, int D,
+                       uint16_t* dx) {
+  return oracle_combine(dxs, NULL, pos, T, K, D, dx);
+}
