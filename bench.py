@@ -1,0 +1,546 @@
+"""Benchmark of the sparse MoE expert block on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl ours|reference] [--fwd-only]
+
+A step is one pass of the whole block, forward and backward (routing
+histogram, permute, FC1+SwiGLU, FC2, combine, combine backward, FC2 backward
+with the fused SwiGLU backward, FC1 backward, permute backward) over one
+batch of seeded synthetic input resident in HBM.  The default workload is
+``long_seq_train`` (T=32768 tokens = 2 x 16384, emb 2816, 128 experts,
+top-8, mlp 704, router logits plus a per-expert bias): the training block
+the MaxText Gemma4-26B-A4B pages measure.  Its inputs (xs 1.5 GB, wi 1 GB)
+are larger than the 129 MB L2, so no L2 flush is needed between steps.
+
+Prints one JSON line (rank 0).  Under torchrun every rank runs its own
+replica on its own tokens (weak scaling, no collective on the data path; a
+max-reduction of the timings only).  ``--impl reference`` times the CPU
+oracle on the host cores instead, on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from mixture_experts_ffn_histogram_gb300.inputs import WORKLOADS, make_inputs  # noqa: E402
+
+METRIC = "MoE block tokens/s (fwd+bwd)"
+METRIC_FWD = "MoE block tokens/s (fwd)"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="long_seq_train", choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--fwd-only", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------- distributed
+def dist_setup(n):
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    if ws > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+        return dist, int(os.environ.get("RANK", "0")), ws, int(os.environ.get("LOCAL_RANK", "0"))
+    return None, 0, 1, 0
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def max_over_ranks(dist, v: float) -> float:
+    if dist is None:
+        return v
+    t = torch.tensor([v], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# --------------------------------------------------------- roofline model
+def gemm_flops(kind, R, D, F):
+    return {"fc1": 4, "fc2": 2, "fc2_dlhs": 2, "fc2_drhs": 2, "fc1_dlhs": 4, "fc1_drhs": 4}[kind] * R * D * F
+
+
+def hbm_bytes(kind, T, D, E, K, F):
+    """Algorithmic bytes of each HBM-bound step (what the method must move)."""
+    R = T * K
+    return {
+        "route": 4 * T * E + 4 * E + 8 * T * K + 8 * E + 12 * T * K,
+        "permute": 2 * T * D + 2 * R * D + 4 * T * K,
+        "combine": 2 * R * D + 2 * T * D + 8 * T * K,
+        "combine_bwd": 2 * T * D + 4 * R * D + 12 * T * K,
+        "permute_bwd": 2 * R * D + 2 * T * D + 4 * T * K,
+    }[kind]
+
+
+def gemm_bytes(kind, R, D, E, F, train=True):
+    z = 4 * R * F if train else 0
+    return {
+        "fc1": 2 * R * D + 4 * E * D * F + 2 * R * F + z,
+        "fc2": 2 * R * F + 2 * E * F * D + 2 * R * D,
+        "fc2_dlhs": 2 * R * D + 2 * E * F * D + 8 * R * F,
+        "fc2_drhs": 2 * R * F + 2 * R * D + 2 * E * F * D,
+        "fc1_dlhs": 4 * R * F + 4 * E * D * F + 2 * R * D,
+        "fc1_drhs": 2 * R * D + 4 * R * F + 4 * E * D * F,
+    }[kind]
+
+
+# kernel names as ncu reports them, for the traffic figures under profiles/
+NCU_NAME = {
+    "route": "route_topk_hist", "permute": "permute_kernel", "fc1": "grouped_gemm_kernel<0>",
+    "fc2": "grouped_gemm_kernel<1>", "combine": "combine_kernel", "combine_bwd": "combine_bwd_kernel",
+    "fc2_dlhs": "grouped_gemm_kernel<2>", "fc2_drhs": "grouped_gemm_kernel<4>",
+    "fc1_dlhs": "grouped_gemm_kernel<3>", "fc1_drhs": "grouped_gemm_kernel<5>",
+    "permute_bwd": "combine_kernel",
+}
+
+
+def source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "mixture_experts_ffn_histogram_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(step: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if rec.get("source_hash") != source_hash():
+        return None
+    ent = rec.get("kernels", {}).get(workload, {}).get(step)
+    return None if ent is None else ent.get("dram_bytes_per_launch")
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return dict(hbm=float(p["hbm_gbs"]), bf16=float(p["bf16_tflops"]),
+                    bf16_sustained=float(p["bf16_tflops_sustained"]), source="measured")
+    except (OSError, KeyError, ValueError):
+        return dict(hbm=6800.0, bf16=1900.0, bf16_sustained=1700.0, source="fallback")
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.out = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out = ""
+
+    def summary(self):
+        if not self.out:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax = float(parts[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------- our GPU arm
+class Step:
+    """One forward+backward pass through the C ABI, with a CUDA event pair
+    around every kernel launch (all on the one stream the block runs on)."""
+
+    def __init__(self, wl, inp, fwd_only):
+        from mixture_experts_ffn_histogram_gb300 import binding as B
+        from mixture_experts_ffn_histogram_gb300.block import MoEBlock
+        self.B = B
+        self.wl = wl
+        self.fwd_only = fwd_only
+        self.blk = MoEBlock(wl.T, wl.D, wl.E, wl.K, wl.F, wl.score_mode, train=not fwd_only)
+        self.inp = inp
+        self.names = ["route", "permute", "fc1", "fc2", "combine"]
+        if not fwd_only:
+            self.names += ["combine_bwd", "fc2_dlhs", "fc2_drhs", "fc1_dlhs", "fc1_drhs", "permute_bwd"]
+        self.launches_per_step = 7 + (0 if fwd_only else 6)
+        self.times = {n: [] for n in self.names}
+        self._ev = []
+
+    def run(self, record=False, x=None, logits=None, dy=None):
+        B, b, d, inp = self.B, self.blk, self.blk.d, self.inp
+        x = inp["x"] if x is None else x
+        logits = inp["logits"] if logits is None else logits
+        dy = inp["dy"] if dy is None else dy
+        ev = []
+
+        def mark():
+            if record:
+                e = torch.cuda.Event(enable_timing=True)
+                e.record()
+                ev.append(e)
+
+        if self.wl.score_mode == B.SCORE_GIVEN:
+            b.ids.copy_(inp["ids"])
+            b.w.copy_(inp["w"])
+        mark()
+        B.moe_route_histogram(logits, inp["bias"], b.mode, b.ids, b.w, b.group_sizes,
+                              b.group_offsets, b.pos, b.row_src, b.status, b.ws, d)
+        mark()
+        B.moe_permute(x, b.pos, b.xs, d)
+        mark()
+        B.moe_grouped_gemm_fc1_swiglu(b.xs, inp["wi"], b.group_offsets, b.h, b.z, b.status, b.ws, d)
+        mark()
+        B.moe_grouped_gemm_fc2(b.h, inp["wo"], b.group_offsets, b.ys, b.status, b.ws, d)
+        mark()
+        B.moe_combine(b.ys, b.w, b.pos, b.out, d)
+        mark()
+        if not self.fwd_only:
+            B.moe_combine_bwd(dy, b.ys, b.w, b.pos, b.dys, b.dw, d)
+            mark()
+            B.moe_grouped_gemm_fc2_bwd(b.dys, b.h, inp["wo"], b.z, b.group_offsets, b.dz, None,
+                                       b.status, b.ws, d)
+            mark()
+            B.moe_grouped_gemm_fc2_bwd(b.dys, b.h, inp["wo"], b.z, b.group_offsets, None, b.dwo,
+                                       b.status, b.ws, d)
+            mark()
+            B.moe_grouped_gemm_fc1_swiglu_bwd(b.dz, None, b.xs, inp["wi"], b.group_offsets, b.dxs,
+                                              None, b.status, b.ws, d)
+            mark()
+            B.moe_grouped_gemm_fc1_swiglu_bwd(b.dz, None, b.xs, inp["wi"], b.group_offsets, None,
+                                              b.dwi, b.status, b.ws, d)
+            mark()
+            B.moe_permute_bwd(b.dxs, b.pos, b.dx, d)
+            mark()
+        if record:
+            self._ev.append(ev)
+
+    def collect(self):
+        torch.cuda.synchronize()
+        for ev in self._ev:
+            for i, n in enumerate(self.names):
+                self.times[n].append(ev[i].elapsed_time(ev[i + 1]) * 1e-3)
+        self._ev = []
+
+
+def run_ours(args, dist, rank, world):
+    wl = WORKLOADS[args.workload]
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    from mixture_experts_ffn_histogram_gb300 import _build
+    _build.build()
+    from dataclasses import replace
+    wl_rank = replace(wl, seed=wl.seed + rank)
+    fwd_only = args.fwd_only or not wl.train
+    inp = make_inputs(wl_rank, dev, with_grad=not fwd_only)
+    step = Step(wl_rank, inp, fwd_only)
+    for _ in range(max(args.warmup, 3)):
+        step.run()
+    torch.cuda.synchronize()
+    # ---- timed region: K steps, events around every launch
+    barrier(dist)
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index) as clk:
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        start.record()
+        for _ in range(args.steps):
+            step.run(record=True)
+        end.record()
+        torch.cuda.synchronize()
+    barrier(dist)
+    elapsed = start.elapsed_time(end) * 1e-3
+    elapsed_max = max_over_ranks(dist, elapsed)
+    step.collect()
+    status = int(step.blk.status.item())
+    if status != 0:
+        raise RuntimeError(f"device status {status} after the timed steps")
+
+    # ---- forward-only tokens/s, same inputs (a separate timed loop)
+    fwd_tps = None
+    if not fwd_only:
+        fstep = Step(wl_rank, inp, True)
+        for _ in range(3):
+            fstep.run()
+        torch.cuda.synchronize()
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s0.record()
+        for _ in range(args.steps):
+            fstep.run()
+        s1.record()
+        torch.cuda.synchronize()
+        fwd_tps = wl.T * args.steps / (s0.elapsed_time(s1) * 1e-3)
+        del fstep
+
+    # ---- end to end through the C ABI from pinned host buffers
+    e2e = None
+    if not args.no_e2e:
+        e2e = measure_e2e(step, inp, args, dist, fwd_only)
+
+    T = wl.T
+    value = world * T * args.steps / elapsed_max
+    pk = peaks()
+    per_kernel = {}
+    for n in step.names:
+        ts = step.times[n]
+        avg = sum(ts) / len(ts)
+        per_kernel[n] = {"avg_us": avg * 1e6, "share": sum(ts) / max(1e-12, sum(sum(v) for v in step.times.values()))}
+        if n in ("fc1", "fc2", "fc2_dlhs", "fc2_drhs", "fc1_dlhs", "fc1_drhs"):
+            fl = gemm_flops(n, wl.R, wl.D, wl.F)
+            per_kernel[n]["tflops"] = fl / avg / 1e12
+            per_kernel[n]["frac_tensor"] = fl / avg / 1e12 / pk["bf16_sustained"]
+            per_kernel[n]["hbm_gbs_algorithmic"] = gemm_bytes(n, wl.R, wl.D, wl.E, wl.F, not fwd_only) / avg / 1e9
+        else:
+            by = hbm_bytes(n, wl.T, wl.D, wl.E, wl.K, wl.F)
+            per_kernel[n]["gbs"] = by / avg / 1e9
+            per_kernel[n]["frac_hbm"] = by / avg / 1e9 / pk["hbm"]
+    dom = max(step.names, key=lambda n: sum(step.times[n]))
+    avg = sum(step.times[dom]) / len(step.times[dom])
+    if dom in ("fc1", "fc2", "fc2_dlhs", "fc2_drhs", "fc1_dlhs", "fc1_drhs"):
+        achieved = gemm_flops(dom, wl.R, wl.D, wl.F) / avg / 1e12
+        roof = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": pk["bf16_sustained"],
+                "unit": "TFLOP/s", "frac": achieved / pk["bf16_sustained"],
+                "peak_source": f"{pk['source']} bf16_tflops_sustained"}
+    else:
+        achieved = hbm_bytes(dom, wl.T, wl.D, wl.E, wl.K, wl.F) / avg / 1e9
+        roof = {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": pk["hbm"],
+                "unit": "GB/s", "frac": achieved / pk["hbm"], "peak_source": f"{pk['source']} hbm_gbs"}
+    roof["traffic"] = recorded_traffic(dom, wl.name)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(wl, fwd_only, budget_s=20.0)
+
+    line = {
+        "metric": METRIC_FWD if fwd_only else METRIC,
+        "value": value,
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": elapsed_max / args.steps * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded; N(0,1) activations, N(0,0.02) weights)",
+        "config": {"workload": wl.name, "T": wl.T, "D": wl.D, "E": wl.E, "K": wl.K, "F": wl.F,
+                   "pass": "fwd" if fwd_only else "fwd+bwd",
+                   "l2": "inputs larger than L2 (no flush)" if wl.R * wl.D * 2 > 129e6 else
+                         "inputs smaller than L2 (warm)",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": roof,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": step.launches_per_step * args.steps,
+        "clocks": clk.summary(),
+        "kernels": per_kernel,
+    }
+    if fwd_tps is not None:
+        line["fwd_tokens_per_s"] = world * fwd_tps
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def measure_e2e(step, inp, args, dist, fwd_only):
+    """The same steps with the step's activations copied in from pinned host
+    memory and the block's outputs copied back, inside the timed region."""
+    wl = step.wl
+    host_x = inp["x"].cpu().pin_memory()
+    host_logits = inp["logits"].cpu().pin_memory() if inp["logits"] is not None else None
+    host_dy = inp["dy"].cpu().pin_memory() if not fwd_only else None
+    dx_ = torch.empty_like(inp["x"])
+    dl_ = torch.empty_like(inp["logits"]) if host_logits is not None else None
+    ddy = torch.empty_like(inp["dy"]) if host_dy is not None else None
+    out_h = torch.empty_like(step.blk.out, device="cpu").pin_memory()
+    dx_h = torch.empty_like(step.blk.out, device="cpu").pin_memory() if not fwd_only else None
+    h2d = host_x.numel() * 2 + (host_logits.numel() * 4 if host_logits is not None else 0) + \
+        (host_dy.numel() * 2 if host_dy is not None else 0)
+    d2h = out_h.numel() * 2 + (dx_h.numel() * 2 if dx_h is not None else 0)
+
+    def one():
+        dx_.copy_(host_x, non_blocking=True)
+        if dl_ is not None:
+            dl_.copy_(host_logits, non_blocking=True)
+        if ddy is not None:
+            ddy.copy_(host_dy, non_blocking=True)
+        step.run(x=dx_, logits=dl_, dy=ddy)
+        out_h.copy_(step.blk.out, non_blocking=True)
+        if dx_h is not None:
+            dx_h.copy_(step.blk.dx, non_blocking=True)
+
+    for _ in range(2):
+        one()
+    torch.cuda.synchronize()
+    barrier(dist)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        one()
+    torch.cuda.synchronize()
+    el = max_over_ranks(dist, time.perf_counter() - t0)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    return {"value": world * wl.T * args.steps / el, "unit": "tokens/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+# ------------------------------------------------------ oracle (CPU) arm
+def _sample_workload(wl, T_sample):
+    from dataclasses import replace
+    return replace(wl, T=T_sample)
+
+
+def _oracle_step(wl_s, inp_np, fwd_only):
+    import oracle
+    fwd = oracle.block_forward(inp_np, want_z=not fwd_only)
+    if not fwd_only:
+        oracle.block_backward(inp_np, fwd)
+
+
+def _oracle_inputs(wl_s, fwd_only):
+    import oracle
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    return oracle.to_numpy(make_inputs(wl_s, dev, with_grad=not fwd_only))
+
+
+def cpu_baseline(wl, fwd_only, budget_s=20.0, T_sample=None):
+    """The oracle as it stands on the host cores, on a bounded sample of the
+    workload (the first T_sample tokens' worth of a draw with the same sizes)."""
+    import oracle
+    oracle.build()
+    if T_sample is None:
+        T_sample = 16
+        probe = _oracle_inputs(_sample_workload(wl, T_sample), fwd_only)
+        t0 = time.perf_counter()
+        _oracle_step(None, probe, fwd_only)
+        dt = time.perf_counter() - t0
+        # the weight-gradient part does not shrink with T; scale the token part
+        T_sample = int(max(16, min(wl.T, T_sample * budget_s / max(dt, 1e-3) / 2)))
+    wl_s = _sample_workload(wl, T_sample)
+    inp = _oracle_inputs(wl_s, fwd_only)
+    t0 = time.perf_counter()
+    _oracle_step(wl_s, inp, fwd_only)
+    dt = time.perf_counter() - t0
+    return {"value": T_sample / dt, "unit": "tokens/s", "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": f"{T_sample} of {wl.T} tokens of {wl.name} (same D,E,K,F), "
+                      f"{'fwd' if fwd_only else 'fwd+bwd'}, one pass, {dt:.1f} s"}
+
+
+def run_reference(args, dist, rank, world):
+    if rank != 0:
+        return
+    wl = WORKLOADS[args.workload]
+    fwd_only = args.fwd_only or not wl.train
+    import oracle
+    oracle.build()
+    # size the per-step sample so that warmup+steps end within ~3 minutes
+    steps_total = max(args.warmup, 0) + args.steps
+    per_step = max(2.0, 180.0 / max(1, steps_total))
+    T_sample = 8
+    probe = _oracle_inputs(_sample_workload(wl, T_sample), fwd_only)
+    t0 = time.perf_counter()
+    _oracle_step(None, probe, fwd_only)
+    dt = time.perf_counter() - t0
+    T_sample = int(max(8, min(wl.T, T_sample * per_step / max(dt, 1e-3) / 2)))
+    wl_s = _sample_workload(wl, T_sample)
+    inp = _oracle_inputs(wl_s, fwd_only)
+    for _ in range(args.warmup):
+        _oracle_step(wl_s, inp, fwd_only)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        _oracle_step(wl_s, inp, fwd_only)
+    el = time.perf_counter() - t0
+    value = T_sample * args.steps / el
+    line = {
+        "impl": "reference",
+        "metric": METRIC_FWD if fwd_only else METRIC,
+        "value": value,
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": el / args.steps * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded; N(0,1) activations, N(0,0.02) weights)",
+        "config": {"workload": wl.name, "T": wl.T, "D": wl.D, "E": wl.E, "K": wl.K, "F": wl.F,
+                   "pass": "fwd" if fwd_only else "fwd+bwd", "parallelism": "host cores"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oracle.num_threads(),
+                         "kind": "oracle",
+                         "sample": f"{T_sample} of {wl.T} tokens per step, same D,E,K,F"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    dist, rank, world, _ = dist_setup(args.gpus)
+    try:
+        if args.impl == "reference":
+            run_reference(args, dist, rank, world)
+        else:
+            run_ours(args, dist, rank, world)
+    finally:
+        if dist is not None:
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,241 @@
+/*
+ * moe.h -- C ABI of libmoe.so, the single-GPU sparse mixture-of-experts
+ * expert block for NVIDIA GB300 (sm_103a).
+ *
+ * The block (forward):
+ *   route    -> top-k expert ids and routing weights per token
+ *   histogram-> group_size per expert, expert-sorted position of every slot
+ *   permute  -> xs: tokens gathered into expert-sorted order
+ *   FC1      -> one grouped GEMM against the whole prefused wi [E, emb, 2*mlp],
+ *               SwiGLU applied to its output activations
+ *   FC2      -> grouped GEMM against wo [E, mlp, emb]
+ *   combine  -> unpermute plus the top-k weighted sum
+ * and the backward of every step.
+ *
+ * Sources the operations follow (pages of the MoE optimisation discussions):
+ *   [Keep fused]  MaxText "Keep fused MoE weights intact through FSDP gather",
+ *                 Description: the prefused [experts, embed, 2*mlp] weight goes
+ *                 through one grouped GEMM; only its output is split into gate
+ *                 and up activations for SwiGLU.
+ *   [Fused p/c]   MaxText "MoE: fused TensorCore Pallas permute/combine kernels
+ *                 and split-expert wi layout for TPU v6e", Context item 1 and
+ *                 Commits table rows 1-2: the permute gathers tokens into
+ *                 expert-sorted order without an unsorted [tokens*top_k, emb]
+ *                 copy, with the group_size histogram computed first; its
+ *                 backward is the combine with unit weights; the combine is the
+ *                 unpermute plus the top-K weighted sum, whose backward is a
+ *                 permutation for dx and a per-slot reduction for dw.
+ *   [Gemma4 L/M]  MaxText "Gemma4 26B MoE on TPU v6e: MaxText layer/model
+ *                 optimizations", Commits table row 6 (top_k_weights and
+ *                 group_size) and row 7 (gate/up split backward = one
+ *                 concatenation).
+ *   [TE MoE]      TransformerEngine "[DRAFT][JAX] Optimize MoE block", Changes
+ *                 (group-aware grouped GEMM, no masking pass) and Flowchart.
+ *   [Transposed]  The "transposed-RHS gmm_v2 kernel for the backward dlhs"
+ *                 named under Related PRs of [Fused p/c]: dlhs multiplies by
+ *                 the transposed expert weight.
+ *
+ * Notation: T tokens, D = emb, E experts, K = top_k, F = mlp, R = T*K.
+ * All tensors are dense, row-major, and live in DEVICE memory owned by the
+ * caller (for example PyTorch tensors).  bf16 tensors are raw IEEE bfloat16
+ * bit patterns (moe_bf16).  The library never allocates device memory:
+ * scratch comes from `ws`, at least moe_workspace_bytes(d) bytes.
+ *
+ * Every call is asynchronous and stream-ordered on `stream`; none blocks the
+ * host or reads group sizes back to it.  Host-side argument errors are
+ * returned synchronously before anything is enqueued:
+ *   MOE_ERR_INVALID_ARG  a required pointer is NULL or not 16-byte aligned;
+ *   MOE_ERR_UNSUPPORTED  D % 64 != 0, F % 64 != 0, K < 1, K > E, K > 32,
+ *                        E > 1024, T < 0, or R >= 2^31;
+ *   MOE_ERR_CUDA         a kernel launch failed (cudaGetLastError).
+ * Errors found on the device are written to *dev_status (an int32 in device
+ * memory that the caller zeroes and reads after synchronising; the first
+ * error wins):
+ *   MOE_ERR_DEVICE       an expert id outside [0, E) (its slot is dropped:
+ *                        pos = -1, not counted in group_sizes);
+ *   MOE_ERR_TIMEOUT      a bounded wait inside a kernel gave up (the kernel
+ *                        released its resources and returned).
+ * T = 0 is valid: the calls do nothing but zero group_sizes/group_offsets.
+ * Gradient outputs overwrite their buffers; they never accumulate.
+ * The functions keep no state between calls apart from a per-device cache of
+ * the SM count and of a driver entry point, and are safe to call from several
+ * host threads; calls that share a `ws` must be ordered on one stream.
+ */
+#ifndef MOE_H
+#define MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,
+  MOE_ERR_UNSUPPORTED = 2,
+  MOE_ERR_CUDA = 3,
+  MOE_ERR_DEVICE = 4,
+  MOE_ERR_TIMEOUT = 5
+} moe_status;
+
+typedef struct {
+  int32_t T; /* tokens */
+  int32_t D; /* emb, multiple of 64 */
+  int32_t E; /* experts, 1..1024 */
+  int32_t K; /* top_k, 1..min(E, 32) */
+  int32_t F; /* mlp, multiple of 64 */
+} moe_dims;
+
+typedef enum {
+  MOE_SCORE_SOFTMAX_TOPK = 0, /* w = softmax over the K selected scores */
+  MOE_SCORE_SIGMOID_NORM = 1, /* w = sigmoid(selected) / sum of the K sigmoids */
+  MOE_SCORE_GIVEN = 2         /* ids and w are inputs; only the histogram runs */
+} moe_score_mode;
+
+typedef uint16_t moe_bf16; /* raw bfloat16 bits */
+
+/* Bytes of scratch that every call below may use through `ws` for dims d
+ * (the largest need over all calls). */
+size_t moe_workspace_bytes(moe_dims d);
+
+/* A static English description of a status code. */
+const char* moe_status_string(moe_status s);
+
+/* Version of this ABI (1); lets a loader check the library it opened
+ * without touching a GPU. */
+int moe_abi_version(void);
+
+/*
+ * Routing and group_size histogram [Gemma4 L/M row 6; Fused p/c row 2].
+ *   logits  fp32 [T,E]   router logits (ignored, may be NULL, for GIVEN)
+ *   bias    fp32 [E]     per-expert bias added to the logits, or NULL
+ *   mode    score mode: the score of expert e is s = logit + bias[e]; the K
+ *           largest scores are taken in descending order (equal scores: the
+ *           lower expert id first) and weighted by `mode`
+ *   ids     int32 [T,K]  out (in for GIVEN): expert id of slot (t,k)
+ *   w       fp32 [T,K]   out (in for GIVEN, may then be NULL): routing weight
+ *   group_sizes   int32 [E]    out: rows routed to each expert
+ *   group_offsets int32 [E+1]  out: exclusive prefix sum of group_sizes
+ *   pos     int32 [T,K]  out: expert-sorted row of slot (t,k); the order is
+ *           stable in the flat slot index j = t*K + k
+ *   row_src int32 [R]    out: row_src[pos[j]] = j (rows never filled: -1)
+ *   dev_status int32*    device error word (may be NULL)
+ *   ws      scratch, moe_workspace_bytes(d) bytes
+ */
+moe_status moe_route_histogram(const float* logits, const float* bias, moe_score_mode mode,
+                               int32_t* ids, float* w, int32_t* group_sizes,
+                               int32_t* group_offsets, int32_t* pos, int32_t* row_src,
+                               int32_t* dev_status, void* ws, moe_dims d, cudaStream_t stream);
+
+/*
+ * Permute [Fused p/c Context item 1, row 2]: xs[pos[t,k]] = x[t] for every
+ * slot with pos >= 0 (an exact copy; each x row is read once and written K
+ * times; no unsorted [R, D] copy exists).
+ *   x  bf16 [T,D] in;  pos int32 [T,K] in;  xs bf16 [R,D] out.
+ */
+moe_status moe_permute(const moe_bf16* x, const int32_t* pos, moe_bf16* xs, moe_dims d,
+                       cudaStream_t stream);
+
+/*
+ * Permute backward [Fused p/c row 2] = the combine with unit weights:
+ *   dx[t] = bf16(sum_{k ascending} dxs[pos[t,k]])  (fp32 sum).
+ *   dxs bf16 [R,D] in;  pos int32 [T,K] in;  dx bf16 [T,D] out.
+ */
+moe_status moe_permute_bwd(const moe_bf16* dxs, const int32_t* pos, moe_bf16* dx, moe_dims d,
+                           cudaStream_t stream);
+
+/*
+ * FC1 + SwiGLU [Keep fused, Description; TE MoE, Changes and Flowchart]:
+ * for every row r of group e (rows group_offsets[e] .. group_offsets[e+1]-1)
+ *   a = xs[r] . wi[e]   (fp32 accumulation, N = 2F columns, wi never split)
+ *   h[r,f] = bf16(silu(a[f]) * a[F+f]),  z[r,:] = bf16(a)  (when z != NULL)
+ * Gate = columns [0,F) of wi's last axis, up = [F,2F).
+ *   xs bf16 [R,D];  wi bf16 [E,D,2F];  group_offsets int32 [E+1] (device);
+ *   h bf16 [R,F] out;  z bf16 [R,2F] out or NULL (inference).
+ * Rows at or beyond group_offsets[E] are neither read nor written.
+ */
+moe_status moe_grouped_gemm_fc1_swiglu(const moe_bf16* xs, const moe_bf16* wi,
+                                       const int32_t* group_offsets, moe_bf16* h, moe_bf16* z,
+                                       int32_t* dev_status, void* ws, moe_dims d,
+                                       cudaStream_t stream);
+
+/*
+ * FC1 backward against the whole wi [Transposed; TE MoE]:
+ *   dlhs: dxs[r,d] = bf16(sum_{n<2F} dz[r,n] * wi[e,d,n])
+ *   drhs: dwi[e,d,n] = bf16(sum_{r in group e} xs[r,d] * dz[r,n]); zero for
+ *         an empty group.
+ * grad is dz bf16 [R,2F] when z == NULL.  When z != NULL, grad is dh bf16
+ * [R,F] and the SwiGLU backward [Gemma4 L/M row 7] runs first, writing
+ * dz = [dgate | dup] into ws.  dxs (bf16 [R,D]) or dwi (bf16 [E,D,2F]) may be
+ * NULL to skip that half.
+ */
+moe_status moe_grouped_gemm_fc1_swiglu_bwd(const moe_bf16* grad, const moe_bf16* z,
+                                           const moe_bf16* xs, const moe_bf16* wi,
+                                           const int32_t* group_offsets, moe_bf16* dxs,
+                                           moe_bf16* dwi, int32_t* dev_status, void* ws,
+                                           moe_dims d, cudaStream_t stream);
+
+/*
+ * FC2 [TE MoE, Flowchart "grouped FC2 GEMM"]:
+ *   ys[r,:] = bf16(h[r] . wo[e])  (fp32 accumulation).
+ *   h bf16 [R,F];  wo bf16 [E,F,D];  ys bf16 [R,D] out.
+ */
+moe_status moe_grouped_gemm_fc2(const moe_bf16* h, const moe_bf16* wo,
+                                const int32_t* group_offsets, moe_bf16* ys,
+                                int32_t* dev_status, void* ws, moe_dims d, cudaStream_t stream);
+
+/*
+ * FC2 backward [Transposed; Gemma4 L/M row 7]:
+ *   dlhs: dh[r,f] = sum_d dys[r,d] * wo[e,f,d] in fp32; with z != NULL the
+ *         SwiGLU backward is fused on that fp32 value (s = sigmoid(g),
+ *         g = z[r,f], u = z[r,F+f]):
+ *           dz[r,f]   = bf16(dh * u * s * (1 + g*(1-s)))
+ *           dz[r,F+f] = bf16(dh * g * s)
+ *         and dh_or_dz is dz bf16 [R,2F]; with z == NULL it is dh bf16 [R,F].
+ *   drhs: dwo[e,f,d] = bf16(sum_{r in group e} h[r,f] * dys[r,d]); zero for
+ *         an empty group.
+ * dh_or_dz or dwo may be NULL to skip that half.
+ */
+moe_status moe_grouped_gemm_fc2_bwd(const moe_bf16* dys, const moe_bf16* h, const moe_bf16* wo,
+                                    const moe_bf16* z, const int32_t* group_offsets,
+                                    moe_bf16* dh_or_dz, moe_bf16* dwo, int32_t* dev_status,
+                                    void* ws, moe_dims d, cudaStream_t stream);
+
+/*
+ * Combine [Fused p/c row 1]: unpermute plus the top-K weighted sum,
+ *   out[t] = bf16(sum_{k ascending} w[t,k] * ys[pos[t,k]])  (fp32, each
+ *   product and sum rounded separately, slots with pos < 0 skipped).
+ *   ys bf16 [R,D];  w fp32 [T,K];  pos int32 [T,K];  out bf16 [T,D].
+ */
+moe_status moe_combine(const moe_bf16* ys, const float* w, const int32_t* pos, moe_bf16* out,
+                       moe_dims d, cudaStream_t stream);
+
+/*
+ * Combine backward [Fused p/c row 1]: a permutation for the activation
+ * gradient and a per-slot reduction for the routing-weight gradient,
+ *   dys[pos[t,k]] = bf16(w[t,k] * dout[t])
+ *   dw[t,k] = sum_d dout[t,d] * ys[pos[t,k],d]  (fp32; 0 when pos < 0)
+ *   dout bf16 [T,D];  ys bf16 [R,D];  w fp32 [T,K];  pos int32 [T,K];
+ *   dys bf16 [R,D] out;  dw fp32 [T,K] out.
+ */
+moe_status moe_combine_bwd(const moe_bf16* dout, const moe_bf16* ys, const float* w,
+                           const int32_t* pos, moe_bf16* dys, float* dw, moe_dims d,
+                           cudaStream_t stream);
+
+/*
+ * Self-test of the kernels' bounded waits (no counterpart on the pages):
+ * launches one block that waits on a barrier nothing ever arrives at, with a
+ * limit of `limit_ns` nanoseconds (at most 10^9).  The wait gives up,
+ * MOE_ERR_TIMEOUT is written to *dev_status and the kernel returns normally,
+ * leaving the context usable.
+ */
+moe_status moe_selftest_bounded_wait(int32_t* dev_status, uint64_t limit_ns, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_H */

@@ -1,0 +1,273 @@
+// C entry points of libmoe.so: argument checks, workspace carving, launches.
+// The operations and their sources are documented in include/moe.h.
+#include <atomic>
+#include <cstdint>
+
+#include "kernels.h"
+#include "moe.h"
+
+namespace moe {
+
+int sm_count() {
+  static std::atomic<int> cache[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (dev < 0 || dev >= 64) dev = 0;
+  int v = cache[dev].load(std::memory_order_relaxed);
+  if (v > 0) return v;
+  if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
+    v = 148;
+  cache[dev].store(v, std::memory_order_relaxed);
+  return v;
+}
+
+}  // namespace moe
+
+namespace {
+
+using moe::GemmCall;
+using moe::GemmKind;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool ok_ptr(const void* p) { return p != nullptr && aligned16(p); }
+
+moe_status check_dims(const moe_dims& d) {
+  if (d.T < 0 || d.D <= 0 || d.F <= 0 || d.E <= 0 || d.K <= 0) return MOE_ERR_UNSUPPORTED;
+  if (d.D % 64 != 0 || d.F % 64 != 0) return MOE_ERR_UNSUPPORTED;
+  if (d.K > d.E || d.K > 32 || d.E > 1024) return MOE_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(d.T) * d.K >= (int64_t{1} << 31)) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+moe_status from_cuda(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+int64_t rows(const moe_dims& d) { return static_cast<int64_t>(d.T) * d.K; }
+
+size_t dz_ws_bytes(const moe_dims& d) {
+  return static_cast<size_t>(rows(d)) * 2u * static_cast<size_t>(d.F) * 2u;
+}
+
+}  // namespace
+
+#define MOE_CHECK_DIMS(d)                          \
+  do {                                             \
+    moe_status st_ = check_dims(d);                \
+    if (st_ != MOE_OK) return st_;                 \
+  } while (0)
+#define MOE_REQUIRE(p)                             \
+  do {                                             \
+    if (!ok_ptr(p)) return MOE_ERR_INVALID_ARG;    \
+  } while (0)
+#define MOE_OPTIONAL(p)                                        \
+  do {                                                         \
+    if ((p) != nullptr && !aligned16(p)) return MOE_ERR_INVALID_ARG; \
+  } while (0)
+
+extern "C" {
+
+size_t moe_workspace_bytes(moe_dims d) {
+  if (check_dims(d) != MOE_OK) return 0;
+  size_t need = moe::route_ws_bytes(d);
+  const size_t dz = dz_ws_bytes(d);
+  if (dz > need) need = dz;
+  return (need + 255u) & ~static_cast<size_t>(255u);
+}
+
+const char* moe_status_string(moe_status s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument (null or misaligned pointer)";
+    case MOE_ERR_UNSUPPORTED: return "unsupported dimensions";
+    case MOE_ERR_CUDA: return "CUDA launch error";
+    case MOE_ERR_DEVICE: return "expert id outside [0, E) seen on the device";
+    case MOE_ERR_TIMEOUT: return "a bounded wait inside a kernel timed out";
+  }
+  return "unknown status";
+}
+
+int moe_abi_version(void) { return 1; }
+
+moe_status moe_route_histogram(const float* logits, const float* bias, moe_score_mode mode,
+                               int32_t* ids, float* w, int32_t* group_sizes,
+                               int32_t* group_offsets, int32_t* pos, int32_t* row_src,
+                               int32_t* dev_status, void* ws, moe_dims d, cudaStream_t stream) {
+  MOE_CHECK_DIMS(d);
+  if (mode != MOE_SCORE_SOFTMAX_TOPK && mode != MOE_SCORE_SIGMOID_NORM && mode != MOE_SCORE_GIVEN)
+    return MOE_ERR_INVALID_ARG;
+  MOE_REQUIRE(group_sizes);
+  MOE_REQUIRE(group_offsets);
+  MOE_OPTIONAL(dev_status);
+  MOE_OPTIONAL(bias);
+  if (d.T > 0) {
+    MOE_REQUIRE(ids);
+    MOE_REQUIRE(pos);
+    MOE_REQUIRE(row_src);
+    MOE_REQUIRE(ws);
+    if (mode != MOE_SCORE_GIVEN) {
+      MOE_REQUIRE(logits);
+      MOE_REQUIRE(w);
+    } else {
+      MOE_OPTIONAL(w);
+    }
+  }
+  int32_t* counts = static_cast<int32_t*>(ws);
+  int32_t* chunk_excl =
+      counts + static_cast<size_t>(moe::route_chunks(d.T)) * static_cast<size_t>(d.E);
+  return from_cuda(moe::launch_route_histogram(logits, bias, static_cast<int>(mode), ids, w,
+                                               group_sizes, group_offsets, pos, row_src,
+                                               dev_status, counts, chunk_excl, d, stream));
+}
+
+moe_status moe_permute(const moe_bf16* x, const int32_t* pos, moe_bf16* xs, moe_dims d,
+                       cudaStream_t stream) {
+  MOE_CHECK_DIMS(d);
+  if (d.T == 0) return MOE_OK;
+  MOE_REQUIRE(x);
+  MOE_REQUIRE(pos);
+  MOE_REQUIRE(xs);
+  return from_cuda(moe::launch_permute(x, pos, xs, d, stream));
+}
+
+moe_status moe_permute_bwd(const moe_bf16* dxs, const int32_t* pos, moe_bf16* dx, moe_dims d,
+                           cudaStream_t stream) {
+  MOE_CHECK_DIMS(d);
+  if (d.T == 0) return MOE_OK;
+  MOE_REQUIRE(dxs);
+  MOE_REQUIRE(pos);
+  MOE_REQUIRE(dx);
+  return from_cuda(moe::launch_combine(dxs, nullptr, pos, dx, d, stream));
+}
+
+moe_status moe_combine(const moe_bf16* ys, const float* w, const int32_t* pos, moe_bf16* out,
+                       moe_dims d, cudaStream_t stream) {
+  MOE_CHECK_DIMS(d);
+  if (d.T == 0) return MOE_OK;
+  MOE_REQUIRE(ys);
+  MOE_REQUIRE(w);
+  MOE_REQUIRE(pos);
+  MOE_REQUIRE(out);
+  return from_cuda(moe::launch_combine(ys, w, pos, out, d, stream));
+}
+
+moe_status moe_combine_bwd(const moe_bf16* dout, const moe_bf16* ys, const float* w,
+                           const int32_t* pos, moe_bf16* dys, float* dw, moe_dims d,
+                           cudaStream_t stream) {
+  MOE_CHECK_DIMS(d);
+  if (d.T == 0) return MOE_OK;
+  MOE_REQUIRE(dout);
+  MOE_REQUIRE(ys);
+  MOE_REQUIRE(w);
+  MOE_REQUIRE(pos);
+  MOE_REQUIRE(dys);
+  MOE_REQUIRE(dw);
+  return from_cuda(moe::launch_combine_bwd(dout, ys, w, pos, dys, dw, d, stream));
+}
+
+moe_status moe_grouped_gemm_fc1_swiglu(const moe_bf16* xs, const moe_bf16* wi,
+                                       const int32_t* group_offsets, moe_bf16* h, moe_bf16* z,
+                                       int32_t* dev_status, void* ws, moe_dims d,
+                                       cudaStream_t stream) {
+  (void)ws;
+  MOE_CHECK_DIMS(d);
+  MOE_OPTIONAL(dev_status);
+  MOE_OPTIONAL(z);
+  if (d.T == 0) return MOE_OK;
+  MOE_REQUIRE(xs);
+  MOE_REQUIRE(wi);
+  MOE_REQUIRE(group_offsets);
+  MOE_REQUIRE(h);
+  GemmCall c{GemmKind::kFc1, xs, wi, group_offsets, h, z, nullptr, dev_status, d};
+  return from_cuda(moe::launch_grouped_gemm(c, stream));
+}
+
+moe_status moe_grouped_gemm_fc2(const moe_bf16* h, const moe_bf16* wo,
+                                const int32_t* group_offsets, moe_bf16* ys, int32_t* dev_status,
+                                void* ws, moe_dims d, cudaStream_t stream) {
+  (void)ws;
+  MOE_CHECK_DIMS(d);
+  MOE_OPTIONAL(dev_status);
+  if (d.T == 0) return MOE_OK;
+  MOE_REQUIRE(h);
+  MOE_REQUIRE(wo);
+  MOE_REQUIRE(group_offsets);
+  MOE_REQUIRE(ys);
+  GemmCall c{GemmKind::kFc2, h, wo, group_offsets, ys, nullptr, nullptr, dev_status, d};
+  return from_cuda(moe::launch_grouped_gemm(c, stream));
+}
+
+moe_status moe_grouped_gemm_fc2_bwd(const moe_bf16* dys, const moe_bf16* h, const moe_bf16* wo,
+                                    const moe_bf16* z, const int32_t* group_offsets,
+                                    moe_bf16* dh_or_dz, moe_bf16* dwo, int32_t* dev_status,
+                                    void* ws, moe_dims d, cudaStream_t stream) {
+  (void)ws;
+  MOE_CHECK_DIMS(d);
+  MOE_OPTIONAL(dev_status);
+  MOE_OPTIONAL(z);
+  MOE_OPTIONAL(dh_or_dz);
+  MOE_OPTIONAL(dwo);
+  if (dh_or_dz == nullptr && dwo == nullptr) return MOE_ERR_INVALID_ARG;
+  MOE_REQUIRE(group_offsets);
+  if (d.T > 0) {
+    MOE_REQUIRE(dys);
+    if (dh_or_dz != nullptr) MOE_REQUIRE(wo);
+    if (dwo != nullptr) MOE_REQUIRE(h);
+  }
+  if (dh_or_dz != nullptr && d.T > 0) {
+    GemmCall c{GemmKind::kDlhsFc2, dys, wo, group_offsets, dh_or_dz, nullptr, z, dev_status, d};
+    moe_status st = from_cuda(moe::launch_grouped_gemm(c, stream));
+    if (st != MOE_OK) return st;
+  }
+  if (dwo != nullptr) {
+    GemmCall c{GemmKind::kDrhsFc2, h, dys, group_offsets, dwo, nullptr, nullptr, dev_status, d};
+    moe_status st = from_cuda(moe::launch_grouped_gemm(c, stream));
+    if (st != MOE_OK) return st;
+  }
+  return MOE_OK;
+}
+
+moe_status moe_grouped_gemm_fc1_swiglu_bwd(const moe_bf16* grad, const moe_bf16* z,
+                                           const moe_bf16* xs, const moe_bf16* wi,
+                                           const int32_t* group_offsets, moe_bf16* dxs,
+                                           moe_bf16* dwi, int32_t* dev_status, void* ws,
+                                           moe_dims d, cudaStream_t stream) {
+  MOE_CHECK_DIMS(d);
+  MOE_OPTIONAL(dev_status);
+  MOE_OPTIONAL(z);
+  MOE_OPTIONAL(dxs);
+  MOE_OPTIONAL(dwi);
+  if (dxs == nullptr && dwi == nullptr) return MOE_ERR_INVALID_ARG;
+  MOE_REQUIRE(group_offsets);
+  const moe_bf16* dz = grad;
+  if (d.T > 0) {
+    MOE_REQUIRE(grad);
+    if (dxs != nullptr) MOE_REQUIRE(wi);
+    if (dwi != nullptr) MOE_REQUIRE(xs);
+    if (z != nullptr) {
+      // grad is dh [R,F]: the SwiGLU backward writes dz into the workspace
+      MOE_REQUIRE(ws);
+      moe_bf16* dzw = static_cast<moe_bf16*>(ws);
+      cudaError_t e = moe::launch_swiglu_bwd(grad, z, dzw, rows(d), d.F, stream);
+      if (e != cudaSuccess) return MOE_ERR_CUDA;
+      dz = dzw;
+    }
+  }
+  if (dxs != nullptr && d.T > 0) {
+    GemmCall c{GemmKind::kDlhsFc1, dz, wi, group_offsets, dxs, nullptr, nullptr, dev_status, d};
+    moe_status st = from_cuda(moe::launch_grouped_gemm(c, stream));
+    if (st != MOE_OK) return st;
+  }
+  if (dwi != nullptr) {
+    GemmCall c{GemmKind::kDrhsFc1, xs, dz, group_offsets, dwi, nullptr, nullptr, dev_status, d};
+    moe_status st = from_cuda(moe::launch_grouped_gemm(c, stream));
+    if (st != MOE_OK) return st;
+  }
+  return MOE_OK;
+}
+
+moe_status moe_selftest_bounded_wait(int32_t* dev_status, uint64_t limit_ns, cudaStream_t stream) {
+  MOE_REQUIRE(dev_status);
+  if (limit_ns == 0 || limit_ns > 1000000000ull) return MOE_ERR_INVALID_ARG;
+  return from_cuda(moe::launch_bounded_wait_selftest(dev_status, limit_ns, stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,615 @@
+// Grouped GEMMs of the MoE block on the fifth-generation tensor cores.
+//
+// What is computed (per expert e, rows r of its group):
+//   FC1 + SwiGLU  a = xs[r] . wi[e] over the whole prefused wi [E, D, 2F];
+//                 h = silu(a[:F]) * a[F:], z = a            (MaxText "Keep fused
+//                 MoE weights intact through FSDP gather", Description)
+//   FC2           ys[r] = h[r] . wo[e]                      (TransformerEngine
+//                 "[DRAFT][JAX] Optimize MoE block", Flowchart)
+//   dlhs of FC2   dh[r] = dys[r] . wo[e]^T, with the SwiGLU backward fused
+//                 into the epilogue (dz = [dgate | dup] as one tensor, MaxText
+//                 "Gemma4 26B MoE on TPU v6e", Commits table row 7)
+//   dlhs of FC1   dxs[r] = dz[r] . wi[e]^T                  (the transposed-RHS
+//                 backward named under Related PRs of the MaxText fused
+//                 permute/combine page)
+//   drhs          dwo[e] = h_e^T . dys_e,  dwi[e] = xs_e^T . dz_e
+// The grouped GEMM is group-aware: ragged group edges are handled inside the
+// kernel (row masks in the epilogue, zero-filled reduction tails), never by a
+// separate masking pass (TransformerEngine page, Changes).
+//
+// Design (one persistent CTA per SM, 192 threads):
+//   warp 0     TMA producer: loads 128x64 A tiles and 256x64 B tiles (bf16,
+//              128-byte swizzle) into a 4-stage shared-memory ring; for the
+//              forward and dlhs GEMMs B comes from a 3-D tensor map whose
+//              outer coordinate is the expert.
+//   warp 1     allocates 512 TMEM columns (two 128x256 fp32 accumulators),
+//              and one thread issues tcgen05.mma (M=128, N=256, K=16) and
+//              tcgen05.commit; for drhs it zero-fills the rows of the last
+//              reduction block that belong to the next expert.
+//   warps 2-5  epilogue: tcgen05.ld of the accumulator (one row per thread),
+//              SwiGLU / SwiGLU-backward / bf16 conversion, masked stores; the
+//              second accumulator lets the next tile's MMAs overlap it.
+// Tiles are scheduled on the device from group_offsets (no host sync):
+// forward/dlhs tiles are (expert, 128-row block, N block) with the rows of a
+// block starting at the group's first row; drhs tiles are (expert, M block,
+// N block) with the group's rows as the reduction.
+#include <cuda.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+namespace {
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 64;
+constexpr int kStages = 4;
+constexpr int kUmmaK = 16;
+constexpr int kAStageBytes = BM * BK * 2;  // 16 KB
+constexpr int kBStageBytes = BN * BK * 2;  // 32 KB
+constexpr int kStageBytes = kAStageBytes + kBStageBytes;
+constexpr int kChunkBytes = 64 * BK * 2;  // one 64-wide MN chunk of 64 K rows: 8 KB
+constexpr int kThreads = 192;
+constexpr int kTmemCols = 512;
+constexpr int kMaxExperts = 1024;
+
+struct SmemCtl {
+  uint64_t full[kStages];
+  uint64_t empty[kStages];
+  uint64_t tfull[2];
+  uint64_t tempty[2];
+  uint32_t tmem_base;
+  int abort_flag;
+  int off[kMaxExperts + 1];  // group offsets
+  int mt[kMaxExperts + 1];   // prefix of 128-row blocks per group
+};
+constexpr size_t kSmemBytes = 1024 + static_cast<size_t>(kStages) * kStageBytes + sizeof(SmemCtl);
+
+struct Params {
+  const int32_t* offs;
+  __nv_bfloat16* out0;
+  __nv_bfloat16* out1;
+  const __nv_bfloat16* aux;
+  int32_t* status;
+  uint64_t limit_ns;
+  int E, Kdim, M, N, F;
+  int m_tiles, n_tiles;
+};
+
+template <int KIND>
+struct Traits {
+  static constexpr bool kGroupedK = (KIND == static_cast<int>(GemmKind::kDrhsFc2) ||
+                                     KIND == static_cast<int>(GemmKind::kDrhsFc1));
+  static constexpr bool kAMn = kGroupedK;
+  static constexpr bool kBMn = (KIND == static_cast<int>(GemmKind::kFc1) ||
+                                KIND == static_cast<int>(GemmKind::kFc2) || kGroupedK);
+  static constexpr uint32_t kIdesc = instr_desc_bf16(BM, BN, kAMn, kBMn);
+};
+
+struct Tile {
+  int e;
+  int row0;   // first output row (forward/dlhs) or first group row (drhs)
+  int rows;   // valid rows of the tile (forward/dlhs)
+  int m0;     // drhs: first output row (of F or D)
+  int n0;     // first output column
+  int kb;     // reduction blocks of 64
+  int klen;   // drhs: group rows
+};
+
+template <int KIND>
+__device__ __forceinline__ Tile decode_tile(int t, const Params& p, const SmemCtl& s) {
+  Tile T;
+  if constexpr (!Traits<KIND>::kGroupedK) {
+    const int mt = t / p.n_tiles;
+    const int nt = t - mt * p.n_tiles;
+    int lo = 0, hi = p.E - 1;  // largest e with mt[e] <= mt
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (s.mt[mid] <= mt) lo = mid;
+      else hi = mid - 1;
+    }
+    T.e = lo;
+    T.row0 = s.off[lo] + (mt - s.mt[lo]) * BM;
+    T.rows = min(BM, s.off[lo + 1] - T.row0);
+    T.m0 = 0;
+    T.n0 = nt * (KIND == static_cast<int>(GemmKind::kFc1) ? BN / 2 : BN);
+    T.kb = p.Kdim / BK;
+    T.klen = p.Kdim;
+  } else {
+    const int per_e = p.m_tiles * p.n_tiles;
+    T.e = t / per_e;
+    const int r = t - T.e * per_e;
+    const int mt = r / p.n_tiles;
+    T.m0 = mt * BM;
+    T.n0 = (r - mt * p.n_tiles) * BN;
+    T.row0 = s.off[T.e];
+    T.klen = s.off[T.e + 1] - T.row0;
+    T.rows = BM;
+    T.kb = (T.klen + BK - 1) / BK;
+  }
+  return T;
+}
+
+template <int KIND>
+__device__ __forceinline__ int total_tiles(const Params& p, const SmemCtl& s) {
+  if constexpr (!Traits<KIND>::kGroupedK) return s.mt[p.E] * p.n_tiles;
+  else return p.E * p.m_tiles * p.n_tiles;
+}
+
+template <int KIND>
+__device__ __forceinline__ void issue_loads(const Tile& T, int kb, uint8_t* sa, uint8_t* sb,
+                                            uint64_t* bar, const CUtensorMap* ma,
+                                            const CUtensorMap* mb, const Params& p) {
+  const int k0 = kb * BK;
+  if constexpr (KIND == static_cast<int>(GemmKind::kFc1)) {
+    tma_load_2d(sa, ma, bar, k0, T.row0);
+    tma_load_3d(sb + 0 * kChunkBytes, mb, bar, T.n0, k0, T.e);              // gate
+    tma_load_3d(sb + 1 * kChunkBytes, mb, bar, T.n0 + 64, k0, T.e);
+    tma_load_3d(sb + 2 * kChunkBytes, mb, bar, p.F + T.n0, k0, T.e);        // up
+    tma_load_3d(sb + 3 * kChunkBytes, mb, bar, p.F + T.n0 + 64, k0, T.e);
+  } else if constexpr (KIND == static_cast<int>(GemmKind::kFc2)) {
+    tma_load_2d(sa, ma, bar, k0, T.row0);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) tma_load_3d(sb + j * kChunkBytes, mb, bar, T.n0 + 64 * j, k0, T.e);
+  } else if constexpr (KIND == static_cast<int>(GemmKind::kDlhsFc2) ||
+                       KIND == static_cast<int>(GemmKind::kDlhsFc1)) {
+    tma_load_2d(sa, ma, bar, k0, T.row0);
+    tma_load_3d(sb, mb, bar, k0, T.n0, T.e);  // K-major B: 256 rows x 64
+  } else {
+    const int kr = T.row0 + k0;
+    tma_load_2d(sa, ma, bar, T.m0, kr);
+    tma_load_2d(sa + kChunkBytes, ma, bar, T.m0 + 64, kr);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) tma_load_2d(sb + j * kChunkBytes, mb, bar, T.n0 + 64 * j, kr);
+  }
+}
+
+__device__ __forceinline__ float silu_f(float g) { return g * (1.0f / (1.0f + expf(-g))); }
+
+__device__ __forceinline__ void store32(__nv_bfloat16* dst, const uint32_t (&v)[32]) {
+  uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t* q = v + 8 * i;
+    d[i] = make_uint4(pack_bf16x2(__uint_as_float(q[0]), __uint_as_float(q[1])),
+                      pack_bf16x2(__uint_as_float(q[2]), __uint_as_float(q[3])),
+                      pack_bf16x2(__uint_as_float(q[4]), __uint_as_float(q[5])),
+                      pack_bf16x2(__uint_as_float(q[6]), __uint_as_float(q[7])));
+  }
+}
+
+__device__ __forceinline__ void store32_zero(__nv_bfloat16* dst) {
+  uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) d[i] = make_uint4(0u, 0u, 0u, 0u);
+}
+
+template <int KIND>
+__device__ __forceinline__ void epilogue_tile(const Tile& T, uint32_t tbase, int row_in_tile,
+                                              const Params& p) {
+  uint32_t v[32];
+  if constexpr (KIND == static_cast<int>(GemmKind::kFc1)) {
+    const bool valid = row_in_tile < T.rows;
+    const long r = static_cast<long>(T.row0) + row_in_tile;
+    for (int c = 0; c < 4; ++c) {
+      const int f0 = T.n0 + 32 * c;
+      if (f0 >= p.F) break;
+      uint32_t u[32];
+      tmem_ld_32x32b_x32(tbase + 32 * c, v);
+      tmem_ld_32x32b_x32(tbase + BN / 2 + 32 * c, u);
+      tmem_ld_wait();
+      if (valid) {
+        uint4* hd = reinterpret_cast<uint4*>(p.out0 + r * p.F + f0);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          uint32_t o[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int k = 8 * i + 2 * q;
+            const float h0 = silu_f(__uint_as_float(v[k])) * __uint_as_float(u[k]);
+            const float h1 = silu_f(__uint_as_float(v[k + 1])) * __uint_as_float(u[k + 1]);
+            o[q] = pack_bf16x2(h0, h1);
+          }
+          hd[i] = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+        if (p.out1 != nullptr) {
+          store32(p.out1 + r * 2 * p.F + f0, v);
+          store32(p.out1 + r * 2 * p.F + p.F + f0, u);
+        }
+      }
+    }
+  } else if constexpr (KIND == static_cast<int>(GemmKind::kDlhsFc2)) {
+    const bool valid = row_in_tile < T.rows;
+    const long r = static_cast<long>(T.row0) + row_in_tile;
+    for (int c = 0; c < BN / 32; ++c) {
+      const int f0 = T.n0 + 32 * c;
+      if (f0 >= p.F) break;
+      tmem_ld_32x32b_x32(tbase + 32 * c, v);
+      tmem_ld_wait();
+      if (!valid) continue;
+      if (p.aux != nullptr) {
+        const uint4* zg = reinterpret_cast<const uint4*>(p.aux + r * 2 * p.F + f0);
+        const uint4* zu = reinterpret_cast<const uint4*>(p.aux + r * 2 * p.F + p.F + f0);
+        uint4* dg = reinterpret_cast<uint4*>(p.out0 + r * 2 * p.F + f0);
+        uint4* du = reinterpret_cast<uint4*>(p.out0 + r * 2 * p.F + p.F + f0);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const uint4 gv = __ldg(zg + i), uv = __ldg(zu + i);
+          const uint32_t gq[4] = {gv.x, gv.y, gv.z, gv.w};
+          const uint32_t uq[4] = {uv.x, uv.y, uv.z, uv.w};
+          uint32_t og[4], ou[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            float rg[2], ru[2];
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+              const float dh = __uint_as_float(v[8 * i + 2 * q + hh]);
+              const float g = hh ? bf16hi(gq[q]) : bf16lo(gq[q]);
+              const float u = hh ? bf16hi(uq[q]) : bf16lo(uq[q]);
+              const float sg = 1.0f / (1.0f + expf(-g));
+              rg[hh] = dh * u * sg * (1.0f + g * (1.0f - sg));
+              ru[hh] = dh * g * sg;
+            }
+            og[q] = pack_bf16x2(rg[0], rg[1]);
+            ou[q] = pack_bf16x2(ru[0], ru[1]);
+          }
+          dg[i] = make_uint4(og[0], og[1], og[2], og[3]);
+          du[i] = make_uint4(ou[0], ou[1], ou[2], ou[3]);
+        }
+      } else {
+        store32(p.out0 + r * p.F + f0, v);
+      }
+    }
+  } else {
+    // plain bf16 store: FC2 (N = D), dlhs of FC1 (N = D), drhs (M x N per expert)
+    bool valid;
+    long rowoff;
+    if constexpr (Traits<KIND>::kGroupedK) {
+      valid = (T.m0 + row_in_tile) < p.M;
+      rowoff = (static_cast<long>(T.e) * p.M + T.m0 + row_in_tile) * p.N;
+    } else {
+      valid = row_in_tile < T.rows;
+      rowoff = (static_cast<long>(T.row0) + row_in_tile) * p.N;
+    }
+    for (int c = 0; c < BN / 32; ++c) {
+      const int col = T.n0 + 32 * c;
+      if (col >= p.N) break;
+      tmem_ld_32x32b_x32(tbase + 32 * c, v);
+      tmem_ld_wait();
+      if (valid) store32(p.out0 + rowoff + col, v);
+    }
+  }
+}
+
+template <int KIND>
+__global__ void __launch_bounds__(kThreads, 1)
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
+                        const __grid_constant__ CUtensorMap map_b, const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* ring = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+  SmemCtl& s = *reinterpret_cast<SmemCtl*>(ring + kStages * kStageBytes);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // ---------------------------------------------------------------- set-up
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_map(&map_a);
+    tma_prefetch_map(&map_b);
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&s.full[i], 1);
+      mbar_init(&s.empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s.tfull[i], 1);
+      mbar_init(&s.tempty[i], 4);
+    }
+    s.abort_flag = 0;
+    mbar_fence_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&s.tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == 2) {
+    // group offsets and the prefix of 128-row blocks per group (warp scan)
+    const int E = p.E;
+    const int per = (E + 31) / 32;
+    const int e0 = min(E, lane * per), e1 = min(E, e0 + per);
+    int local = 0;
+    for (int e = e0; e < e1; ++e) {
+      const int a = __ldg(p.offs + e), b = __ldg(p.offs + e + 1);
+      s.off[e] = a;
+      local += (b - a + BM - 1) / BM;
+    }
+    int incl = local;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += v;
+    }
+    int run = incl - local;
+    for (int e = e0; e < e1; ++e) {
+      s.mt[e] = run;
+      run += (__ldg(p.offs + e + 1) - __ldg(p.offs + e) + BM - 1) / BM;
+    }
+    if (lane == 31) {
+      s.mt[E] = incl;
+      s.off[E] = __ldg(p.offs + E);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = s.tmem_base;
+  const WaitCtl wc{&s.abort_flag, p.status, p.limit_ns};
+  const int ntiles = total_tiles<KIND>(p, s);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0;
+      uint32_t fills[kStages] = {0, 0, 0, 0};
+      bool aborted = false;
+      for (int t = blockIdx.x; t < ntiles && !aborted; t += gridDim.x) {
+        const Tile T = decode_tile<KIND>(t, p, s);
+        for (int kb = 0; kb < T.kb; ++kb) {
+          if (!mbar_wait(&s.empty[stage], phase ^ 1u, wc)) { aborted = true; break; }
+          uint8_t* sa = ring + stage * kStageBytes;
+          mbar_arrive_expect_tx(&s.full[stage], kStageBytes);
+          issue_loads<KIND>(T, kb, sa, sa + kAStageBytes, &s.full[stage], &map_a, &map_b, p);
+          ++fills[stage];
+          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        }
+      }
+      if (aborted) {  // let copies already in flight land before the CTA exits
+        for (int i = 0; i < kStages; ++i)
+          if (fills[i] > 0) (void)mbar_wait_drain(&s.full[i], (fills[i] - 1u) & 1u, 100000000ull);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------- MMA
+    uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+    uint32_t commits[kStages] = {0, 0, 0, 0};
+    int last_stage = -1;
+    bool aborted = false;
+    for (int t = blockIdx.x; t < ntiles && !aborted; t += gridDim.x) {
+      const Tile T = decode_tile<KIND>(t, p, s);
+      if (T.kb == 0) continue;
+      if (!mbar_wait(&s.tempty[acc], acc_phase ^ 1u, wc)) { aborted = true; break; }
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + acc * BN;
+      for (int kb = 0; kb < T.kb; ++kb) {
+        if (!mbar_wait(&s.full[stage], phase, wc)) { aborted = true; break; }
+        tc_fence_after();
+        uint8_t* sa = ring + stage * kStageBytes;
+        uint8_t* sb = sa + kAStageBytes;
+        if constexpr (Traits<KIND>::kGroupedK) {
+          const int valid = T.klen - kb * BK;
+          if (valid < BK) {
+            // rows [valid, 64) of every 64-wide chunk belong to the next group
+            // (or lie past the end): zero them in A (2 chunks) and B (4 chunks)
+            const int nrows = BK - valid;
+            const int nvec = 6 * nrows * 8;
+            for (int i = lane; i < nvec; i += 32) {
+              const int line = i >> 3, part = i & 7;
+              const int chunk = line / nrows, j = valid + (line - chunk * nrows);
+              uint8_t* base = chunk < 2 ? sa + chunk * kChunkBytes : sb + (chunk - 2) * kChunkBytes;
+              *reinterpret_cast<uint4*>(base + j * 128 + part * 16) = make_uint4(0u, 0u, 0u, 0u);
+            }
+            fence_proxy_async_smem();
+          }
+        }
+        __syncwarp();
+        if (lane == 0) {
+          const uint32_t a_addr = smem_u32(sa);
+          const uint32_t b_addr = smem_u32(sb);
+#pragma unroll
+          for (int kk = 0; kk < BK / kUmmaK; ++kk) {
+            const uint64_t ad = Traits<KIND>::kAMn
+                                    ? smem_desc_sw128(a_addr + kk * 2048, kChunkBytes, 1024)
+                                    : smem_desc_sw128(a_addr + kk * 32, 16, 1024);
+            const uint64_t bd = Traits<KIND>::kBMn
+                                    ? smem_desc_sw128(b_addr + kk * 2048, kChunkBytes, 1024)
+                                    : smem_desc_sw128(b_addr + kk * 32, 16, 1024);
+            umma_bf16(d_tmem, ad, bd, Traits<KIND>::kIdesc, (kb > 0 || kk > 0) ? 1u : 0u);
+          }
+          umma_commit(&s.empty[stage]);
+        }
+        __syncwarp();
+        ++commits[stage];
+        last_stage = static_cast<int>(stage);
+        if (++stage == kStages) { stage = 0; phase ^= 1u; }
+      }
+      if (aborted) break;
+      if (lane == 0) umma_commit(&s.tfull[acc]);
+      __syncwarp();
+      if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+    }
+    if (aborted && last_stage >= 0) {  // let issued MMAs finish before TMEM is freed
+      (void)mbar_wait_drain(&s.empty[last_stage], (commits[last_stage] - 1u) & 1u, 100000000ull);
+    }
+  } else {
+    // -------------------------------------------------------- epilogue
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int row_in_tile = q * 32 + lane;
+    uint32_t acc = 0, acc_phase = 0;
+    for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
+      const Tile T = decode_tile<KIND>(t, p, s);
+      if (T.kb == 0) {
+        if constexpr (Traits<KIND>::kGroupedK) {
+          // empty group: its weight gradient is zero
+          if (T.m0 + row_in_tile < p.M) {
+            const long rowoff = (static_cast<long>(T.e) * p.M + T.m0 + row_in_tile) * p.N;
+            for (int c = 0; c < BN / 32; ++c) {
+              const int col = T.n0 + 32 * c;
+              if (col >= p.N) break;
+              store32_zero(p.out0 + rowoff + col);
+            }
+          }
+        }
+        continue;
+      }
+      if (!mbar_wait(&s.tfull[acc], acc_phase, wc)) break;
+      tc_fence_after();
+      epilogue_tile<KIND>(T, tmem_base + acc * BN + (static_cast<uint32_t>(q * 32) << 16),
+                          row_in_tile, p);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s.tempty[acc]);
+      if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------ host side
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
+
+// bf16 tensor map, dims innermost first; strides in bytes for dims 1..rank-1.
+bool make_map(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
+              const uint64_t* strides, const uint32_t* box) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t gd[3], gs[2];
+  cuuint32_t bd[3], es[3] = {1, 1, 1};
+  for (int i = 0; i < rank; ++i) { gd[i] = dims[i]; bd[i] = box[i]; }
+  for (int i = 0; i + 1 < rank; ++i) gs[i] = strides[i];
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), gd, gs, bd, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool map2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner,
+           uint32_t box_outer) {
+  const uint64_t dims[2] = {inner, outer};
+  const uint64_t strides[1] = {inner * 2};
+  const uint32_t box[2] = {box_inner, box_outer};
+  return make_map(m, base, 2, dims, strides, box);
+}
+
+bool map3d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t mid, uint64_t outer,
+           uint32_t box_inner, uint32_t box_mid) {
+  const uint64_t dims[3] = {inner, mid, outer};
+  const uint64_t strides[2] = {inner * 2, inner * mid * 2};
+  const uint32_t box[3] = {box_inner, box_mid, 1};
+  return make_map(m, base, 3, dims, strides, box);
+}
+
+template <int KIND>
+cudaError_t launch_kind(const CUtensorMap& ma, const CUtensorMap& mb, const Params& p,
+                        int max_tiles, cudaStream_t s) {
+  auto kern = grouped_gemm_kernel<KIND>;
+  cudaError_t err =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+  if (err != cudaSuccess) return err;
+  int grid = sm_count();
+  if (max_tiles < grid) grid = max_tiles;
+  if (grid <= 0) return cudaSuccess;
+  kern<<<grid, kThreads, kSmemBytes, s>>>(ma, mb, p);
+  return cudaGetLastError();
+}
+
+inline int cdiv(long a, long b) { return static_cast<int>((a + b - 1) / b); }
+
+}  // namespace
+
+cudaError_t launch_grouped_gemm(const GemmCall& c, cudaStream_t s) {
+  const moe_dims& d = c.d;
+  const long R = static_cast<long>(d.T) * d.K;
+  if (R == 0) {
+    // no rows: forward/dlhs outputs are empty; weight gradients are zero
+    if (c.kind == GemmKind::kDrhsFc2)
+      return cudaMemsetAsync(c.out0, 0, static_cast<size_t>(d.E) * d.F * d.D * 2, s);
+    if (c.kind == GemmKind::kDrhsFc1)
+      return cudaMemsetAsync(c.out0, 0, static_cast<size_t>(d.E) * d.D * 2 * d.F * 2, s);
+    return cudaSuccess;
+  }
+  Params p{};
+  p.offs = c.offs;
+  p.out0 = static_cast<__nv_bfloat16*>(c.out0);
+  p.out1 = static_cast<__nv_bfloat16*>(c.out1);
+  p.aux = static_cast<const __nv_bfloat16*>(c.aux);
+  p.status = c.dev_status;
+  p.limit_ns = kDefaultWaitLimitNs;
+  p.E = d.E;
+  p.F = d.F;
+  CUtensorMap ma, mb;
+  bool ok = false;
+  const long rows_tiles_bound = R / BM + d.E;
+  switch (c.kind) {
+    case GemmKind::kFc1:
+      p.Kdim = d.D;
+      p.N = d.F;
+      p.n_tiles = cdiv(d.F, BN / 2);
+      ok = map2d(&ma, c.a, d.D, R, 64, BM) && map3d(&mb, c.b, 2L * d.F, d.D, d.E, 64, 64);
+      if (!ok) return cudaErrorInvalidValue;
+      return launch_kind<0>(ma, mb, p, static_cast<int>(rows_tiles_bound * p.n_tiles), s);
+    case GemmKind::kFc2:
+      p.Kdim = d.F;
+      p.N = d.D;
+      p.n_tiles = cdiv(d.D, BN);
+      ok = map2d(&ma, c.a, d.F, R, 64, BM) && map3d(&mb, c.b, d.D, d.F, d.E, 64, 64);
+      if (!ok) return cudaErrorInvalidValue;
+      return launch_kind<1>(ma, mb, p, static_cast<int>(rows_tiles_bound * p.n_tiles), s);
+    case GemmKind::kDlhsFc2:
+      p.Kdim = d.D;
+      p.N = d.F;
+      p.n_tiles = cdiv(d.F, BN);
+      ok = map2d(&ma, c.a, d.D, R, 64, BM) && map3d(&mb, c.b, d.D, d.F, d.E, 64, BN);
+      if (!ok) return cudaErrorInvalidValue;
+      return launch_kind<2>(ma, mb, p, static_cast<int>(rows_tiles_bound * p.n_tiles), s);
+    case GemmKind::kDlhsFc1:
+      p.Kdim = 2 * d.F;
+      p.N = d.D;
+      p.n_tiles = cdiv(d.D, BN);
+      ok = map2d(&ma, c.a, 2L * d.F, R, 64, BM) && map3d(&mb, c.b, 2L * d.F, d.D, d.E, 64, BN);
+      if (!ok) return cudaErrorInvalidValue;
+      return launch_kind<3>(ma, mb, p, static_cast<int>(rows_tiles_bound * p.n_tiles), s);
+    case GemmKind::kDrhsFc2:
+      p.M = d.F;
+      p.N = d.D;
+      p.m_tiles = cdiv(d.F, BM);
+      p.n_tiles = cdiv(d.D, BN);
+      ok = map2d(&ma, c.a, d.F, R, 64, 64) && map2d(&mb, c.b, d.D, R, 64, 64);
+      if (!ok) return cudaErrorInvalidValue;
+      return launch_kind<4>(ma, mb, p, d.E * p.m_tiles * p.n_tiles, s);
+    case GemmKind::kDrhsFc1:
+      p.M = d.D;
+      p.N = 2 * d.F;
+      p.m_tiles = cdiv(d.D, BM);
+      p.n_tiles = cdiv(2L * d.F, BN);
+      ok = map2d(&ma, c.a, d.D, R, 64, 64) && map2d(&mb, c.b, 2L * d.F, R, 64, 64);
+      if (!ok) return cudaErrorInvalidValue;
+      return launch_kind<5>(ma, mb, p, d.E * p.m_tiles * p.n_tiles, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace moe

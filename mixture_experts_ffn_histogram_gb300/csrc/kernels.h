@@ -1,0 +1,59 @@
+// Internal launchers of libmoe.so (host side).  Each returns the status of
+// its launches; arguments were validated by the C entry points in api.cu.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "moe.h"
+
+namespace moe {
+
+// Routing: tokens handled by one block of the routing kernels.
+constexpr int kRouteTokensPerChunk = 256;
+
+inline int route_chunks(int T) { return (T + kRouteTokensPerChunk - 1) / kRouteTokensPerChunk; }
+// Scratch of the routing/histogram step: per-chunk expert counts and their
+// exclusive prefix over chunks, both int32 [chunks, E].
+inline size_t route_ws_bytes(const moe_dims& d) {
+  return 2ull * static_cast<size_t>(route_chunks(d.T)) * static_cast<size_t>(d.E) * sizeof(int32_t);
+}
+
+cudaError_t launch_route_histogram(const float* logits, const float* bias, int mode, int32_t* ids,
+                                   float* w, int32_t* group_sizes, int32_t* group_offsets,
+                                   int32_t* pos, int32_t* row_src, int32_t* dev_status,
+                                   int32_t* counts, int32_t* chunk_excl, const moe_dims& d,
+                                   cudaStream_t s);
+
+cudaError_t launch_permute(const uint16_t* x, const int32_t* pos, uint16_t* xs, const moe_dims& d,
+                           cudaStream_t s);
+cudaError_t launch_combine(const uint16_t* ys, const float* w, const int32_t* pos, uint16_t* out,
+                           const moe_dims& d, cudaStream_t s);
+cudaError_t launch_combine_bwd(const uint16_t* dout, const uint16_t* ys, const float* w,
+                               const int32_t* pos, uint16_t* dys, float* dw, const moe_dims& d,
+                               cudaStream_t s);
+cudaError_t launch_swiglu_bwd(const uint16_t* dh, const uint16_t* z, uint16_t* dz, long R, int F,
+                              cudaStream_t s);
+cudaError_t launch_bounded_wait_selftest(int32_t* dev_status, uint64_t limit_ns, cudaStream_t s);
+
+// Grouped GEMMs (tcgen05).  `rows` = T*K.
+enum class GemmKind : int { kFc1 = 0, kFc2 = 1, kDlhsFc2 = 2, kDlhsFc1 = 3, kDrhsFc2 = 4, kDrhsFc1 = 5 };
+
+struct GemmCall {
+  GemmKind kind;
+  const void* a;           // left operand base (xs, h, dys, dz, or h/xs for drhs)
+  const void* b;           // right operand base (wi, wo, or dys/dz for drhs)
+  const int32_t* offs;     // group offsets [E+1]
+  void* out0;              // h / ys / dz-or-dh / dxs / dwo / dwi
+  void* out1;              // z (FC1) or nullptr
+  const void* aux;         // z for the fused SwiGLU backward, or nullptr
+  int32_t* dev_status;
+  moe_dims d;
+};
+
+cudaError_t launch_grouped_gemm(const GemmCall& c, cudaStream_t s);
+
+int sm_count();
+
+}  // namespace moe

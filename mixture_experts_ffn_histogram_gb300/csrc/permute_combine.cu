@@ -1,0 +1,285 @@
+// Permute, combine and their backward passes: HBM-bound gathers and
+// scatters of bf16 rows, one warp per token, 16-byte vector accesses.
+//
+// MaxText "MoE: fused TensorCore Pallas permute/combine kernels and
+// split-expert wi layout for TPU v6e", Context item 1 and Commits table rows
+// 1-2:
+//   permute      xs[pos[t,k]] = x[t]: each token row is read once and stored
+//                to its K expert-sorted rows; the unsorted [T*K, D] copy never
+//                exists.
+//   combine      out[t] = sum_k w[t,k] * ys[pos[t,k]] (unpermute + weighted
+//                sum in one pass).
+//   combine_bwd  dys[pos[t,k]] = w[t,k] * dout[t] (a permutation) and
+//                dw[t,k] = <dout[t], ys[pos[t,k]]> (a per-slot reduction).
+//   permute_bwd  the combine with unit weights.
+// In the combine, the permute backward and the dys scatter each product and
+// each sum is rounded separately (no fused multiply-add) in ascending slot
+// order, so those results are reproducible bit for bit; dw is an fp32 dot
+// product accumulated per lane and reduced across the warp.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+namespace {
+
+constexpr int kThreads = 256;  // 8 warps = 8 tokens per block pass
+constexpr int kWarps = kThreads / 32;
+
+__device__ __forceinline__ uint4 ld_stream(const uint4* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+int grid_for_tokens(int T) {
+  const int want = (T + kWarps - 1) / kWarps;
+  const int cap = sm_count() * 16;  // ~8 resident blocks per SM, two waves
+  return want < cap ? want : cap;
+}
+
+template <int VPL>  // 16-byte vectors per lane per pass
+__global__ void __launch_bounds__(kThreads) permute_kernel(const uint4* __restrict__ x,
+                                                           const int32_t* __restrict__ pos,
+                                                           uint4* __restrict__ xs, int T, int K,
+                                                           int Dv) {
+  const int lane = threadIdx.x & 31;
+  for (int t = blockIdx.x * kWarps + (threadIdx.x >> 5); t < T; t += gridDim.x * kWarps) {
+    const int p_lane = (lane < K) ? __ldg(pos + static_cast<long>(t) * K + lane) : -1;
+    const uint4* src = x + static_cast<long>(t) * Dv;
+    for (int v0 = 0; v0 < Dv; v0 += 32 * VPL) {
+      uint4 buf[VPL];
+#pragma unroll
+      for (int i = 0; i < VPL; ++i) {
+        const int idx = v0 + i * 32 + lane;
+        if (idx < Dv) buf[i] = ld_stream(src + idx);
+      }
+      for (int k = 0; k < K; ++k) {
+        const int p = __shfl_sync(0xffffffffu, p_lane, k);
+        if (p < 0) continue;
+        uint4* dst = xs + static_cast<long>(p) * Dv;
+#pragma unroll
+        for (int i = 0; i < VPL; ++i) {
+          const int idx = v0 + i * 32 + lane;
+          if (idx < Dv) dst[idx] = buf[i];
+        }
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void axpy8(float (&acc)[8], float wk, const uint4& v) {
+  const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    acc[2 * q] = __fadd_rn(acc[2 * q], __fmul_rn(wk, bf16lo(u[q])));
+    acc[2 * q + 1] = __fadd_rn(acc[2 * q + 1], __fmul_rn(wk, bf16hi(u[q])));
+  }
+}
+
+// out[t] = bf16(sum_k w[t,k] * ys[pos[t,k]]); w == nullptr means unit weights.
+template <int VPL>
+__global__ void __launch_bounds__(kThreads) combine_kernel(const uint4* __restrict__ ys,
+                                                           const float* __restrict__ w,
+                                                           const int32_t* __restrict__ pos,
+                                                           uint4* __restrict__ out, int T, int K,
+                                                           int Dv) {
+  const int lane = threadIdx.x & 31;
+  for (int t = blockIdx.x * kWarps + (threadIdx.x >> 5); t < T; t += gridDim.x * kWarps) {
+    const long j = static_cast<long>(t) * K + lane;
+    const int p_lane = (lane < K) ? __ldg(pos + j) : -1;
+    const float w_lane = (lane < K) ? (w != nullptr ? __ldg(w + j) : 1.0f) : 0.f;
+    for (int v0 = 0; v0 < Dv; v0 += 32 * VPL) {
+      float acc[VPL][8];
+#pragma unroll
+      for (int i = 0; i < VPL; ++i)
+#pragma unroll
+        for (int q = 0; q < 8; ++q) acc[i][q] = 0.f;
+      for (int k = 0; k < K; ++k) {
+        const int p = __shfl_sync(0xffffffffu, p_lane, k);
+        const float wk = __shfl_sync(0xffffffffu, w_lane, k);
+        if (p < 0) continue;
+        const uint4* src = ys + static_cast<long>(p) * Dv;
+        uint4 v[VPL];
+#pragma unroll
+        for (int i = 0; i < VPL; ++i) {
+          const int idx = v0 + i * 32 + lane;
+          if (idx < Dv) v[i] = ld_stream(src + idx);
+        }
+#pragma unroll
+        for (int i = 0; i < VPL; ++i) axpy8(acc[i], wk, v[i]);
+      }
+#pragma unroll
+      for (int i = 0; i < VPL; ++i) {
+        const int idx = v0 + i * 32 + lane;
+        if (idx < Dv) {
+          uint4 o;
+          o.x = pack_bf16x2(acc[i][0], acc[i][1]);
+          o.y = pack_bf16x2(acc[i][2], acc[i][3]);
+          o.z = pack_bf16x2(acc[i][4], acc[i][5]);
+          o.w = pack_bf16x2(acc[i][6], acc[i][7]);
+          out[static_cast<long>(t) * Dv + idx] = o;
+        }
+      }
+    }
+  }
+}
+
+// dys[pos[t,k]] = bf16(w * dout[t]);  dw[t,k] = <dout[t], ys[pos[t,k]]>.
+template <int VPL>
+__global__ void __launch_bounds__(kThreads) combine_bwd_kernel(
+    const uint4* __restrict__ dout, const uint4* __restrict__ ys, const float* __restrict__ w,
+    const int32_t* __restrict__ pos, uint4* __restrict__ dys, float* __restrict__ dw, int T, int K,
+    int Dv) {
+  const int lane = threadIdx.x & 31;
+  for (int t = blockIdx.x * kWarps + (threadIdx.x >> 5); t < T; t += gridDim.x * kWarps) {
+    const long j = static_cast<long>(t) * K + lane;
+    const int p_lane = (lane < K) ? __ldg(pos + j) : -1;
+    const float w_lane = (lane < K) ? __ldg(w + j) : 0.f;
+    const uint4* g = dout + static_cast<long>(t) * Dv;
+    for (int k = 0; k < K; ++k) {
+      const int p = __shfl_sync(0xffffffffu, p_lane, k);
+      const float wk = __shfl_sync(0xffffffffu, w_lane, k);
+      float dot = 0.f;
+      if (p >= 0) {
+        const uint4* y = ys + static_cast<long>(p) * Dv;
+        uint4* dst = dys + static_cast<long>(p) * Dv;
+        for (int v0 = 0; v0 < Dv; v0 += 32 * VPL) {
+          uint4 gv[VPL], yv[VPL];
+#pragma unroll
+          for (int i = 0; i < VPL; ++i) {
+            const int idx = v0 + i * 32 + lane;
+            if (idx < Dv) {
+              gv[i] = __ldg(g + idx);
+              yv[i] = ld_stream(y + idx);
+            }
+          }
+#pragma unroll
+          for (int i = 0; i < VPL; ++i) {
+            const int idx = v0 + i * 32 + lane;
+            if (idx < Dv) {
+              const uint32_t gu[4] = {gv[i].x, gv[i].y, gv[i].z, gv[i].w};
+              const uint32_t yu[4] = {yv[i].x, yv[i].y, yv[i].z, yv[i].w};
+              uint32_t o[4];
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                const float g0 = bf16lo(gu[q]), g1 = bf16hi(gu[q]);
+                o[q] = pack_bf16x2(__fmul_rn(wk, g0), __fmul_rn(wk, g1));
+                dot = fmaf(g0, bf16lo(yu[q]), dot);
+                dot = fmaf(g1, bf16hi(yu[q]), dot);
+              }
+              dst[idx] = make_uint4(o[0], o[1], o[2], o[3]);
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
+      if (lane == 0) dw[static_cast<long>(t) * K + k] = dot;
+    }
+  }
+}
+
+// dz = [dgate | dup] from a stored bf16 dh [R,F] and z [R,2F] (the SwiGLU
+// backward of MaxText "Gemma4 26B MoE on TPU v6e", Commits table row 7,
+// written as one tensor).  One thread per 8 columns.
+__global__ void __launch_bounds__(kThreads) swiglu_bwd_kernel(const uint4* __restrict__ dh,
+                                                              const uint4* __restrict__ z,
+                                                              uint4* __restrict__ dz, long R,
+                                                              int Fv) {
+  const long n = R * Fv;
+  for (long i = static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += static_cast<long>(gridDim.x) * blockDim.x) {
+    const long r = i / Fv;
+    const int c = static_cast<int>(i - r * Fv);
+    const uint4 hv = __ldg(dh + i);
+    const uint4 gv = __ldg(z + r * 2 * Fv + c);
+    const uint4 uv = __ldg(z + r * 2 * Fv + Fv + c);
+    const uint32_t hu[4] = {hv.x, hv.y, hv.z, hv.w};
+    const uint32_t gu[4] = {gv.x, gv.y, gv.z, gv.w};
+    const uint32_t uu[4] = {uv.x, uv.y, uv.z, uv.w};
+    uint32_t og[4], ou[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      float dg[2], du[2];
+#pragma unroll
+      for (int hcomp = 0; hcomp < 2; ++hcomp) {
+        const float d = hcomp ? bf16hi(hu[q]) : bf16lo(hu[q]);
+        const float g = hcomp ? bf16hi(gu[q]) : bf16lo(gu[q]);
+        const float u = hcomp ? bf16hi(uu[q]) : bf16lo(uu[q]);
+        const float s = 1.0f / (1.0f + expf(-g));
+        dg[hcomp] = d * u * s * (1.0f + g * (1.0f - s));
+        du[hcomp] = d * g * s;
+      }
+      og[q] = pack_bf16x2(dg[0], dg[1]);
+      ou[q] = pack_bf16x2(du[0], du[1]);
+    }
+    dz[r * 2 * Fv + c] = make_uint4(og[0], og[1], og[2], og[3]);
+    dz[r * 2 * Fv + Fv + c] = make_uint4(ou[0], ou[1], ou[2], ou[3]);
+  }
+}
+
+// A block that waits on a barrier nothing arrives at, to exercise the
+// bounded wait: it must give up, record MOE_ERR_TIMEOUT and return.
+__global__ void bounded_wait_selftest_kernel(int32_t* status, uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    mbar_fence_init();
+  }
+  __syncthreads();
+  WaitCtl c{&abort_flag, status, limit_ns};
+  if (threadIdx.x < 32) (void)mbar_wait(&bar, 0, c);
+  __syncthreads();
+}
+
+}  // namespace
+
+cudaError_t launch_permute(const uint16_t* x, const int32_t* pos, uint16_t* xs, const moe_dims& d,
+                           cudaStream_t s) {
+  if (d.T == 0) return cudaSuccess;
+  permute_kernel<4><<<grid_for_tokens(d.T), kThreads, 0, s>>>(
+      reinterpret_cast<const uint4*>(x), pos, reinterpret_cast<uint4*>(xs), d.T, d.K, d.D / 8);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const uint16_t* ys, const float* w, const int32_t* pos, uint16_t* out,
+                           const moe_dims& d, cudaStream_t s) {
+  if (d.T == 0) return cudaSuccess;
+  combine_kernel<2><<<grid_for_tokens(d.T), kThreads, 0, s>>>(
+      reinterpret_cast<const uint4*>(ys), w, pos, reinterpret_cast<uint4*>(out), d.T, d.K, d.D / 8);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine_bwd(const uint16_t* dout, const uint16_t* ys, const float* w,
+                               const int32_t* pos, uint16_t* dys, float* dw, const moe_dims& d,
+                               cudaStream_t s) {
+  if (d.T == 0) return cudaSuccess;
+  combine_bwd_kernel<2><<<grid_for_tokens(d.T), kThreads, 0, s>>>(
+      reinterpret_cast<const uint4*>(dout), reinterpret_cast<const uint4*>(ys), w, pos,
+      reinterpret_cast<uint4*>(dys), dw, d.T, d.K, d.D / 8);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_swiglu_bwd(const uint16_t* dh, const uint16_t* z, uint16_t* dz, long R, int F,
+                              cudaStream_t s) {
+  if (R == 0) return cudaSuccess;
+  const long n = R * (F / 8);
+  long blocks = (n + kThreads - 1) / kThreads;
+  const long cap = static_cast<long>(sm_count()) * 16;
+  if (blocks > cap) blocks = cap;
+  swiglu_bwd_kernel<<<static_cast<int>(blocks), kThreads, 0, s>>>(
+      reinterpret_cast<const uint4*>(dh), reinterpret_cast<const uint4*>(z),
+      reinterpret_cast<uint4*>(dz), R, F / 8);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bounded_wait_selftest(int32_t* dev_status, uint64_t limit_ns, cudaStream_t s) {
+  bounded_wait_selftest_kernel<<<1, 64, 0, s>>>(dev_status, limit_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

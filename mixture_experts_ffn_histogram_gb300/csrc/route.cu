@@ -1,0 +1,276 @@
+// Routing and group_size histogram of the MoE block.
+//
+// MaxText "Gemma4 26B MoE on TPU v6e: MaxText layer/model optimizations",
+// Commits table row 6: top_k_weights and group_size are computed next to the
+// rest of the block; MaxText "MoE: fused TensorCore Pallas permute/combine
+// kernels and split-expert wi layout for TPU v6e", Commits table row 2: the
+// group_size histogram is computed before the token gather.
+//
+// Three launches, all deterministic (no atomic decides an order):
+//   1. route_topk_hist: one warp per token selects the top-K scores by K
+//      rounds of a warp-wide (score desc, id asc) arg-max and computes the
+//      routing weights; each block (one chunk of 256 tokens) also counts its
+//      slots per expert in shared memory -> counts[chunk, E].
+//   2. route_scan: per expert, the exclusive prefix of counts over chunks,
+//      group_sizes, and the exclusive prefix over experts (group_offsets).
+//   3. route_rank: per chunk, each warp ranks its contiguous run of slots
+//      with __match_any_sync; pos = group_offsets[e] + chunk prefix + warp
+//      prefix + rank, i.e. the stable order in the flat slot index t*K+k.
+#include <cfloat>
+#include <climits>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+namespace {
+
+constexpr int kRouteThreads = 256;  // 8 warps
+constexpr int kRouteWarps = kRouteThreads / 32;
+
+__device__ __forceinline__ bool better(float v1, int e1, float v2, int e2) {
+  return v1 > v2 || (v1 == v2 && e1 < e2);
+}
+
+template <int EPL>  // expert scores held per lane: E <= 32 * EPL
+__global__ void __launch_bounds__(kRouteThreads) route_topk_hist(
+    const float* __restrict__ logits, const float* __restrict__ bias, int mode,
+    int32_t* __restrict__ ids, float* __restrict__ w, int32_t* __restrict__ counts, int T, int E,
+    int K, int32_t* status) {
+  extern __shared__ int32_t hist[];  // [E]
+  for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
+  __syncthreads();
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int t_begin = blockIdx.x * kRouteTokensPerChunk;
+  const int t_end = min(T, t_begin + kRouteTokensPerChunk);
+
+  if (mode == MOE_SCORE_GIVEN) {
+    const long j0 = static_cast<long>(t_begin) * K, j1 = static_cast<long>(t_end) * K;
+    for (long j = j0 + threadIdx.x; j < j1; j += blockDim.x) {
+      const int e = ids[j];
+      if (e >= 0 && e < E) atomicAdd(&hist[e], 1);
+      else report(status, MOE_ERR_DEVICE);
+    }
+  } else {
+    for (int t = t_begin + warp; t < t_end; t += kRouteWarps) {
+      float s[EPL];
+      const float* row = logits + static_cast<long>(t) * E;
+#pragma unroll
+      for (int i = 0; i < EPL; ++i) {
+        const int e = lane + 32 * i;
+        if (e < E) {
+          float v = __ldg(row + e);
+          if (bias != nullptr) v = __fadd_rn(v, __ldg(bias + e));
+          s[i] = v;
+        } else {
+          s[i] = -FLT_MAX;
+        }
+      }
+      uint32_t taken = 0;
+      float my_v = 0.f;
+      int my_e = 0;
+      for (int k = 0; k < K; ++k) {
+        float bv = -FLT_MAX;
+        int be = INT_MAX;  // "no candidate" loses to every real expert
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) {
+          const int e = lane + 32 * i;
+          if (e < E && !((taken >> i) & 1u) && better(s[i], e, bv, be)) { bv = s[i]; be = e; }
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+          const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+          const int oe = __shfl_xor_sync(0xffffffffu, be, off);
+          if (better(ov, oe, bv, be)) { bv = ov; be = oe; }
+        }
+        if ((be & 31) == lane) taken |= 1u << (be >> 5);
+        if (lane == k) { my_v = bv; my_e = be; }
+      }
+      // routing weights of the K selected scores (lane k holds slot k)
+      float ex = 0.f;
+      if (mode == MOE_SCORE_SOFTMAX_TOPK) {
+        const float m = __shfl_sync(0xffffffffu, my_v, 0);
+        if (lane < K) ex = expf(my_v - m);
+      } else {
+        if (lane < K) ex = 1.0f / (1.0f + expf(-my_v));
+      }
+      float sum = 0.f;  // ascending slot order
+      for (int k = 0; k < K; ++k) sum = __fadd_rn(sum, __shfl_sync(0xffffffffu, ex, k));
+      if (lane < K) {
+        const long j = static_cast<long>(t) * K + lane;
+        ids[j] = my_e;
+        w[j] = __fdiv_rn(ex, sum);
+        atomicAdd(&hist[my_e], 1);
+      }
+    }
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x)
+    counts[static_cast<long>(blockIdx.x) * E + e] = hist[e];
+}
+
+// One block of 1024 threads: warp w handles experts w, w+32, ...; its lanes
+// split the chunks into contiguous runs.
+__global__ void __launch_bounds__(1024) route_scan(const int32_t* __restrict__ counts,
+                                                   int32_t* __restrict__ chunk_excl, int nchunks,
+                                                   int E, int32_t* __restrict__ group_sizes,
+                                                   int32_t* __restrict__ group_offsets) {
+  __shared__ int32_t tot[1024];
+  __shared__ int32_t warp_sum[32];
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int cpl = (nchunks + 31) / 32;
+  const int c0 = min(nchunks, lane * cpl), c1 = min(nchunks, c0 + cpl);
+  for (int e = warp; e < E; e += 32) {
+    int local = 0;
+    for (int c = c0; c < c1; ++c) local += counts[static_cast<long>(c) * E + e];
+    int incl = local;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += v;
+    }
+    int run = incl - local;
+    for (int c = c0; c < c1; ++c) {
+      const long idx = static_cast<long>(c) * E + e;
+      const int v = counts[idx];
+      chunk_excl[idx] = run;
+      run += v;
+    }
+    const int total = __shfl_sync(0xffffffffu, incl, 31);
+    if (lane == 0) {
+      tot[e] = total;
+      group_sizes[e] = total;
+    }
+  }
+  __syncthreads();
+  // exclusive scan of tot[0..E) over the block
+  const int e = threadIdx.x;
+  const int v = (e < E) ? tot[e] : 0;
+  int incl = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int u = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += u;
+  }
+  if (lane == 31) warp_sum[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const int ws = warp_sum[lane];
+    int wi = ws;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, wi, off);
+      if (lane >= off) wi += u;
+    }
+    warp_sum[lane] = wi - ws;
+  }
+  __syncthreads();
+  const int excl = warp_sum[warp] + incl - v;
+  if (e < E) group_offsets[e] = excl;
+  if (e == E - 1) group_offsets[E] = excl + v;
+  if (E == 0 && e == 0) group_offsets[0] = 0;
+}
+
+// One block per chunk; warp w ranks slots [j0 + w*32K, j0 + (w+1)*32K).
+__global__ void __launch_bounds__(kRouteThreads) route_rank(
+    const int32_t* __restrict__ ids, const int32_t* __restrict__ chunk_excl,
+    const int32_t* __restrict__ group_offsets, int32_t* __restrict__ pos,
+    int32_t* __restrict__ row_src, int T, int K, int E) {
+  extern __shared__ int32_t sm[];
+  int32_t* wrun = sm;                      // [kRouteWarps][E]
+  int32_t* base = sm + kRouteWarps * E;    // [E]
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const long R = static_cast<long>(T) * K;
+  // rows that no valid slot fills (only when some id was out of range)
+  const long filled = group_offsets[E];
+  for (long r = filled + static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x; r < R;
+       r += static_cast<long>(gridDim.x) * blockDim.x)
+    row_src[r] = -1;
+
+  for (int i = threadIdx.x; i < kRouteWarps * E; i += blockDim.x) wrun[i] = 0;
+  __syncthreads();
+  const long chunk_j0 = static_cast<long>(blockIdx.x) * kRouteTokensPerChunk * K;
+  const long per_warp = 32L * K;
+  const long j0 = chunk_j0 + warp * per_warp;
+  const long j1 = min(R, j0 + per_warp);
+  for (long j = j0 + lane; j < j1; j += 32) {
+    const int e = ids[j];
+    if (e >= 0 && e < E) atomicAdd(&wrun[warp * E + e], 1);
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int run = 0;
+    for (int w = 0; w < kRouteWarps; ++w) {
+      const int v = wrun[w * E + e];
+      wrun[w * E + e] = run;
+      run += v;
+    }
+    base[e] = group_offsets[e] + chunk_excl[static_cast<long>(blockIdx.x) * E + e];
+  }
+  __syncthreads();
+  const uint32_t lt_mask = (1u << lane) - 1u;
+  for (long jb = j0; jb < j1; jb += 32) {
+    const long j = jb + lane;
+    int e = (j < j1) ? ids[j] : -1;
+    const bool valid = (e >= 0 && e < E);
+    if (!valid) e = -1;
+    const uint32_t peers = __match_any_sync(0xffffffffu, e);
+    int before = 0;
+    if (valid) before = wrun[warp * E + e];
+    __syncwarp();
+    if (valid) {
+      const int rank = __popc(peers & lt_mask);
+      const int p = base[e] + before + rank;
+      if (lane == __ffs(peers) - 1) wrun[warp * E + e] = before + __popc(peers);
+      pos[j] = p;
+      row_src[p] = static_cast<int32_t>(j);
+    } else if (j < j1) {
+      pos[j] = -1;
+    }
+    __syncwarp();
+  }
+}
+
+template <int EPL>
+cudaError_t launch_topk(const float* logits, const float* bias, int mode, int32_t* ids, float* w,
+                        int32_t* counts, const moe_dims& d, int32_t* status, cudaStream_t s) {
+  const int nchunks = route_chunks(d.T);
+  route_topk_hist<EPL><<<nchunks, kRouteThreads, d.E * sizeof(int32_t), s>>>(
+      logits, bias, mode, ids, w, counts, d.T, d.E, d.K, status);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_route_histogram(const float* logits, const float* bias, int mode, int32_t* ids,
+                                   float* w, int32_t* group_sizes, int32_t* group_offsets,
+                                   int32_t* pos, int32_t* row_src, int32_t* dev_status,
+                                   int32_t* counts, int32_t* chunk_excl, const moe_dims& d,
+                                   cudaStream_t s) {
+  const int nchunks = route_chunks(d.T);
+  cudaError_t err = cudaSuccess;
+  if (nchunks > 0) {
+    const int epl = (d.E + 31) / 32;
+    if (epl <= 1) err = launch_topk<1>(logits, bias, mode, ids, w, counts, d, dev_status, s);
+    else if (epl <= 2) err = launch_topk<2>(logits, bias, mode, ids, w, counts, d, dev_status, s);
+    else if (epl <= 4) err = launch_topk<4>(logits, bias, mode, ids, w, counts, d, dev_status, s);
+    else if (epl <= 8) err = launch_topk<8>(logits, bias, mode, ids, w, counts, d, dev_status, s);
+    else if (epl <= 16) err = launch_topk<16>(logits, bias, mode, ids, w, counts, d, dev_status, s);
+    else err = launch_topk<32>(logits, bias, mode, ids, w, counts, d, dev_status, s);
+    if (err != cudaSuccess) return err;
+  }
+  route_scan<<<1, 1024, 0, s>>>(counts, chunk_excl, nchunks, d.E, group_sizes, group_offsets);
+  if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  if (nchunks > 0) {
+    const size_t smem = static_cast<size_t>(kRouteWarps + 1) * d.E * sizeof(int32_t);
+    route_rank<<<nchunks, kRouteThreads, smem, s>>>(ids, chunk_excl, group_offsets, pos, row_src,
+                                                    d.T, d.K, d.E);
+    err = cudaGetLastError();
+  }
+  return err;
+}
+
+}  // namespace moe
