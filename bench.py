@@ -50,7 +50,25 @@ def parse():
     ap.add_argument("--fwd-only", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--tokens", type=int, default=None,
+                    help="override T (small cases for profiling; not a bench line)")
+    ap.add_argument("--experts", type=int, default=None,
+                    help="override E (small cases for profiling; not a bench line)")
     return ap.parse_args()
+
+
+def selected_workload(args):
+    from dataclasses import replace
+    wl = WORKLOADS[args.workload]
+    kw = {}
+    if args.tokens is not None:
+        kw["T"] = args.tokens
+    if args.experts is not None:
+        kw["E"] = args.experts
+    if kw:
+        tag = ",".join(f"{k}={v}" for k, v in kw.items())
+        wl = replace(wl, name=f"{wl.name}[{tag}]", **kw)
+    return wl
 
 
 # ------------------------------------------------------------- distributed
@@ -152,6 +170,8 @@ def peaks():
 
 # ------------------------------------------------------------------ clocks
 class ClockSampler:
+    """Samples SM clock and throttle reasons with nvidia-smi while the timed
+    region runs (started, and seen producing samples, before the region)."""
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
@@ -159,26 +179,48 @@ class ClockSampler:
     def __init__(self, index: int):
         self.index = index
         self.proc = None
+        self.lines = []
         self.out = None
+        self._thread = None
+        self._active = False
+
+    def _reader(self):
+        for line in self.proc.stdout:
+            if self._active:
+                self.lines.append(line)
+            else:
+                self._seen = True
 
     def __enter__(self):
+        import threading
+        self._seen = False
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
+            return self
+        self._thread = threading.Thread(target=self._reader, daemon=True)
+        self._thread.start()
+        t0 = time.time()
+        while not self._seen and time.time() - t0 < 5.0:
+            time.sleep(0.01)
+        self._active = True
         return self
 
     def __exit__(self, *a):
+        self._active = False
         if self.proc is not None:
             self.proc.terminate()
             try:
-                self.out, _ = self.proc.communicate(timeout=5)
+                self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
-                self.out = ""
+            if self._thread is not None:
+                self._thread.join(timeout=2)
+        self.out = "".join(self.lines)
 
     def summary(self):
         if not self.out:
@@ -278,7 +320,7 @@ class Step:
 
 
 def run_ours(args, dist, rank, world):
-    wl = WORKLOADS[args.workload]
+    wl = selected_workload(args)
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
     torch.cuda.set_device(dev)
     from mixture_experts_ffn_histogram_gb300 import _build
@@ -483,7 +525,7 @@ def cpu_baseline(wl, fwd_only, budget_s=20.0, T_sample=None):
 def run_reference(args, dist, rank, world):
     if rank != 0:
         return
-    wl = WORKLOADS[args.workload]
+    wl = selected_workload(args)
     fwd_only = args.fwd_only or not wl.train
     import oracle
     oracle.build()

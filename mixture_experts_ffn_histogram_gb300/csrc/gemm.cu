@@ -44,21 +44,30 @@ namespace moe {
 namespace {
 
 constexpr int BM = 128;
-constexpr int BN = 256;
 constexpr int BK = 64;
-constexpr int kStages = 4;
 constexpr int kUmmaK = 16;
 constexpr int kAStageBytes = BM * BK * 2;  // 16 KB
-constexpr int kBStageBytes = BN * BK * 2;  // 32 KB
-constexpr int kStageBytes = kAStageBytes + kBStageBytes;
-constexpr int kChunkBytes = 64 * BK * 2;  // one 64-wide MN chunk of 64 K rows: 8 KB
+constexpr int kChunkBytes = 64 * BK * 2;   // one 64-wide MN chunk of 64 K rows: 8 KB
 constexpr int kThreads = 192;
-constexpr int kTmemCols = 512;
 constexpr int kMaxExperts = 1024;
+constexpr int kMaxStages = 8;
+constexpr int kEpiBytes_ = 4 * 4 * 32 * 128;  // epilogue staging (see kEpiBytes)
+
+// Tile shape: 128 x BN output tile per accumulator, `stages`-deep ring.
+template <int BN_, int STAGES_>
+struct Shape {
+  static constexpr int BN = BN_;
+  static constexpr int kStages = STAGES_;
+  static constexpr int kBStageBytes = BN * BK * 2;
+  static constexpr int kStageBytes = kAStageBytes + kBStageBytes;
+  static constexpr int kTmemCols = 2 * BN;  // two accumulators
+  static_assert(BN == 128 || BN == 256, "tile width");
+  static_assert(STAGES_ <= kMaxStages, "stages");
+};
 
 struct SmemCtl {
-  uint64_t full[kStages];
-  uint64_t empty[kStages];
+  uint64_t full[kMaxStages];
+  uint64_t empty[kMaxStages];
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint32_t tmem_base;
@@ -66,7 +75,10 @@ struct SmemCtl {
   int off[kMaxExperts + 1];  // group offsets
   int mt[kMaxExperts + 1];   // prefix of 128-row blocks per group
 };
-constexpr size_t kSmemBytes = 1024 + static_cast<size_t>(kStages) * kStageBytes + sizeof(SmemCtl);
+template <class S>
+constexpr size_t smem_bytes() {
+  return 1024 + static_cast<size_t>(S::kStages) * S::kStageBytes + kEpiBytes_ + sizeof(SmemCtl);
+}
 
 struct Params {
   const int32_t* offs;
@@ -79,7 +91,7 @@ struct Params {
   int m_tiles, n_tiles;
 };
 
-template <int KIND>
+template <int KIND, int BN>
 struct Traits {
   static constexpr bool kGroupedK = (KIND == static_cast<int>(GemmKind::kDrhsFc2) ||
                                      KIND == static_cast<int>(GemmKind::kDrhsFc1));
@@ -99,10 +111,10 @@ struct Tile {
   int klen;   // drhs: group rows
 };
 
-template <int KIND>
+template <int KIND, int BN>
 __device__ __forceinline__ Tile decode_tile(int t, const Params& p, const SmemCtl& s) {
   Tile T;
-  if constexpr (!Traits<KIND>::kGroupedK) {
+  if constexpr (!Traits<KIND, BN>::kGroupedK) {
     const int mt = t / p.n_tiles;
     const int nt = t - mt * p.n_tiles;
     int lo = 0, hi = p.E - 1;  // largest e with mt[e] <= mt
@@ -133,165 +145,337 @@ __device__ __forceinline__ Tile decode_tile(int t, const Params& p, const SmemCt
   return T;
 }
 
-template <int KIND>
+template <int KIND, int BN>
 __device__ __forceinline__ int total_tiles(const Params& p, const SmemCtl& s) {
-  if constexpr (!Traits<KIND>::kGroupedK) return s.mt[p.E] * p.n_tiles;
+  if constexpr (!Traits<KIND, BN>::kGroupedK) return s.mt[p.E] * p.n_tiles;
   else return p.E * p.m_tiles * p.n_tiles;
 }
 
-template <int KIND>
+template <int KIND, int BN>
 __device__ __forceinline__ void issue_loads(const Tile& T, int kb, uint8_t* sa, uint8_t* sb,
                                             uint64_t* bar, const CUtensorMap* ma,
                                             const CUtensorMap* mb, const Params& p) {
   const int k0 = kb * BK;
+  constexpr int kChunks = BN / 64;
   if constexpr (KIND == static_cast<int>(GemmKind::kFc1)) {
+    // gate columns [n0, n0 + BN/2) and up columns [F + n0, F + n0 + BN/2)
     tma_load_2d(sa, ma, bar, k0, T.row0);
-    tma_load_3d(sb + 0 * kChunkBytes, mb, bar, T.n0, k0, T.e);              // gate
-    tma_load_3d(sb + 1 * kChunkBytes, mb, bar, T.n0 + 64, k0, T.e);
-    tma_load_3d(sb + 2 * kChunkBytes, mb, bar, p.F + T.n0, k0, T.e);        // up
-    tma_load_3d(sb + 3 * kChunkBytes, mb, bar, p.F + T.n0 + 64, k0, T.e);
+#pragma unroll
+    for (int j = 0; j < kChunks / 2; ++j) {
+      tma_load_3d(sb + j * kChunkBytes, mb, bar, T.n0 + 64 * j, k0, T.e);
+      tma_load_3d(sb + (kChunks / 2 + j) * kChunkBytes, mb, bar, p.F + T.n0 + 64 * j, k0, T.e);
+    }
   } else if constexpr (KIND == static_cast<int>(GemmKind::kFc2)) {
     tma_load_2d(sa, ma, bar, k0, T.row0);
 #pragma unroll
-    for (int j = 0; j < 4; ++j) tma_load_3d(sb + j * kChunkBytes, mb, bar, T.n0 + 64 * j, k0, T.e);
+    for (int j = 0; j < kChunks; ++j)
+      tma_load_3d(sb + j * kChunkBytes, mb, bar, T.n0 + 64 * j, k0, T.e);
   } else if constexpr (KIND == static_cast<int>(GemmKind::kDlhsFc2) ||
                        KIND == static_cast<int>(GemmKind::kDlhsFc1)) {
     tma_load_2d(sa, ma, bar, k0, T.row0);
-    tma_load_3d(sb, mb, bar, k0, T.n0, T.e);  // K-major B: 256 rows x 64
+    tma_load_3d(sb, mb, bar, k0, T.n0, T.e);  // K-major B: BN rows x 64
   } else {
     const int kr = T.row0 + k0;
     tma_load_2d(sa, ma, bar, T.m0, kr);
     tma_load_2d(sa + kChunkBytes, ma, bar, T.m0 + 64, kr);
 #pragma unroll
-    for (int j = 0; j < 4; ++j) tma_load_2d(sb + j * kChunkBytes, mb, bar, T.n0 + 64 * j, kr);
+    for (int j = 0; j < kChunks; ++j) tma_load_2d(sb + j * kChunkBytes, mb, bar, T.n0 + 64 * j, kr);
   }
 }
 
 __device__ __forceinline__ float silu_f(float g) { return g * (1.0f / (1.0f + expf(-g))); }
 
-__device__ __forceinline__ void store32(__nv_bfloat16* dst, const uint32_t (&v)[32]) {
-  uint4* d = reinterpret_cast<uint4*>(dst);
+// ---------------------------------------------------------------- epilogue
+// Each epilogue warp owns 32 accumulator rows (its TMEM lane quarter) and a
+// ring of kRingBufs staging buffers of 32 rows x 64 bf16 (128-byte rows,
+// 128-byte swizzle).  A 64-column slice of its rows is converted, written to
+// a buffer (lane = row) and sent to global memory by one TMA bulk-tensor
+// store; the store engine writes whole lines, asynchronously.  A warp whose
+// rows straddle the end of a group (forward/dlhs only) stores its valid
+// rows with per-thread stores instead, so that no row of the next group is
+// touched.
+constexpr int kEpiWarps = 4;
+constexpr int kRingBufs = 4;
+constexpr int kBufBytes = 32 * 128;
+constexpr int kEpiBytes = kEpiWarps * kRingBufs * kBufBytes;  // 64 KB
+static_assert(kEpiBytes == kEpiBytes_, "staging size");
+
+struct Ring {
+  uint8_t* base;
+  uint32_t next;
+};
+
+// Take `n` consecutive buffers; the stores that last read them must be done.
+template <int N>
+__device__ __forceinline__ uint8_t* ring_take(Ring& r, int lane) {
+  static_assert(N >= 1 && N <= kRingBufs, "ring");
+  if (lane == 0) bulk_wait_read<kRingBufs - N>();
+  __syncwarp();
+  uint8_t* b = r.base + (r.next % kRingBufs) * kBufBytes;
+  r.next += N;
+  return b;
+}
+__device__ __forceinline__ uint8_t* ring_buf(const Ring& r, uint8_t* first, int i) {
+  const uint32_t idx = static_cast<uint32_t>((first - r.base) / kBufBytes + i) % kRingBufs;
+  return r.base + idx * kBufBytes;
+}
+
+// 16 packed bf16 pairs = 32 columns (half `h` of a 64-column row) of row `lane`.
+__device__ __forceinline__ void put_half(uint8_t* buf, int lane, int h, const uint32_t (&w)[16]) {
+  uint8_t* row = buf + lane * 128;
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const uint32_t* q = v + 8 * i;
-    d[i] = make_uint4(pack_bf16x2(__uint_as_float(q[0]), __uint_as_float(q[1])),
-                      pack_bf16x2(__uint_as_float(q[2]), __uint_as_float(q[3])),
-                      pack_bf16x2(__uint_as_float(q[4]), __uint_as_float(q[5])),
-                      pack_bf16x2(__uint_as_float(q[6]), __uint_as_float(q[7])));
+  for (int j = 0; j < 4; ++j) {
+    const int unit = h * 4 + j;
+    *reinterpret_cast<uint4*>(row + ((unit ^ (lane & 7)) << 4)) =
+        make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
   }
 }
 
-__device__ __forceinline__ void store32_zero(__nv_bfloat16* dst) {
-  uint4* d = reinterpret_cast<uint4*>(dst);
+__device__ __forceinline__ void pack16(const uint32_t (&v)[32], uint32_t (&w)[16]) {
 #pragma unroll
-  for (int i = 0; i < 4; ++i) d[i] = make_uint4(0u, 0u, 0u, 0u);
+  for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
 }
 
-template <int KIND>
-__device__ __forceinline__ void epilogue_tile(const Tile& T, uint32_t tbase, int row_in_tile,
+__device__ __forceinline__ void store_row32(__nv_bfloat16* dst, const uint32_t (&w)[16]) {
+  uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) d[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+}
+
+// Make the buffers' rows visible to the TMA engine, then store them.
+__device__ __forceinline__ void flush_2d(uint8_t* buf, const CUtensorMap* map, int x, int y, int lane) {
+  if (lane == 0) {
+    tma_store_2d(map, buf, x, y);
+    bulk_commit();
+  }
+}
+__device__ __forceinline__ void flush_3d(uint8_t* buf, const CUtensorMap* map, int x, int y, int z,
+                                         int lane) {
+  if (lane == 0) {
+    tma_store_3d(map, buf, x, y, z);
+    bulk_commit();
+  }
+}
+__device__ __forceinline__ void publish(int) {
+  fence_proxy_async_smem();
+  __syncwarp();
+}
+
+struct EpiCtx {
+  const CUtensorMap* map_c;  // out0
+  const CUtensorMap* map_d;  // out1 (z of FC1)
+  Ring ring;
+  int q;                     // lane quarter: rows [32q, 32q+32) of the tile
+  int lane;
+};
+
+template <int KIND, int BN>
+__device__ __forceinline__ void epilogue_tile(const Tile& T, uint32_t tbase, EpiCtx& c,
                                               const Params& p) {
+  const int lane = c.lane;
   uint32_t v[32];
-  if constexpr (KIND == static_cast<int>(GemmKind::kFc1)) {
-    const bool valid = row_in_tile < T.rows;
-    const long r = static_cast<long>(T.row0) + row_in_tile;
-    for (int c = 0; c < 4; ++c) {
-      const int f0 = T.n0 + 32 * c;
-      if (f0 >= p.F) break;
-      uint32_t u[32];
-      tmem_ld_32x32b_x32(tbase + 32 * c, v);
-      tmem_ld_32x32b_x32(tbase + BN / 2 + 32 * c, u);
-      tmem_ld_wait();
-      if (valid) {
-        uint4* hd = reinterpret_cast<uint4*>(p.out0 + r * p.F + f0);
+  uint32_t w[16];
+  if constexpr (Traits<KIND, BN>::kGroupedK) {
+    // weight gradient tile: rows m0+32q.. of expert e; rows >= M are clipped by the 3-D map
+    const int y = T.m0 + 32 * c.q;
+    if (y >= p.M) return;
+    for (int ch = 0; ch < BN / 64; ++ch) {
+      const int col = T.n0 + 64 * ch;
+      if (col >= p.N) break;
+      uint8_t* buf = ring_take<1>(c.ring, lane);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          uint32_t o[4];
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int k = 8 * i + 2 * q;
-            const float h0 = silu_f(__uint_as_float(v[k])) * __uint_as_float(u[k]);
-            const float h1 = silu_f(__uint_as_float(v[k + 1])) * __uint_as_float(u[k + 1]);
-            o[q] = pack_bf16x2(h0, h1);
-          }
-          hd[i] = make_uint4(o[0], o[1], o[2], o[3]);
-        }
-        if (p.out1 != nullptr) {
-          store32(p.out1 + r * 2 * p.F + f0, v);
-          store32(p.out1 + r * 2 * p.F + p.F + f0, u);
-        }
+      for (int h = 0; h < 2; ++h) {
+        tmem_ld_32x32b_x32(tbase + 64 * ch + 32 * h, v);
+        tmem_ld_wait();
+        pack16(v, w);
+        put_half(buf, lane, h, w);
       }
-    }
-  } else if constexpr (KIND == static_cast<int>(GemmKind::kDlhsFc2)) {
-    const bool valid = row_in_tile < T.rows;
-    const long r = static_cast<long>(T.row0) + row_in_tile;
-    for (int c = 0; c < BN / 32; ++c) {
-      const int f0 = T.n0 + 32 * c;
-      if (f0 >= p.F) break;
-      tmem_ld_32x32b_x32(tbase + 32 * c, v);
-      tmem_ld_wait();
-      if (!valid) continue;
-      if (p.aux != nullptr) {
-        const uint4* zg = reinterpret_cast<const uint4*>(p.aux + r * 2 * p.F + f0);
-        const uint4* zu = reinterpret_cast<const uint4*>(p.aux + r * 2 * p.F + p.F + f0);
-        uint4* dg = reinterpret_cast<uint4*>(p.out0 + r * 2 * p.F + f0);
-        uint4* du = reinterpret_cast<uint4*>(p.out0 + r * 2 * p.F + p.F + f0);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const uint4 gv = __ldg(zg + i), uv = __ldg(zu + i);
-          const uint32_t gq[4] = {gv.x, gv.y, gv.z, gv.w};
-          const uint32_t uq[4] = {uv.x, uv.y, uv.z, uv.w};
-          uint32_t og[4], ou[4];
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            float rg[2], ru[2];
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-              const float dh = __uint_as_float(v[8 * i + 2 * q + hh]);
-              const float g = hh ? bf16hi(gq[q]) : bf16lo(gq[q]);
-              const float u = hh ? bf16hi(uq[q]) : bf16lo(uq[q]);
-              const float sg = 1.0f / (1.0f + expf(-g));
-              rg[hh] = dh * u * sg * (1.0f + g * (1.0f - sg));
-              ru[hh] = dh * g * sg;
-            }
-            og[q] = pack_bf16x2(rg[0], rg[1]);
-            ou[q] = pack_bf16x2(ru[0], ru[1]);
-          }
-          dg[i] = make_uint4(og[0], og[1], og[2], og[3]);
-          du[i] = make_uint4(ou[0], ou[1], ou[2], ou[3]);
-        }
-      } else {
-        store32(p.out0 + r * p.F + f0, v);
-      }
+      publish(lane);
+      flush_3d(buf, c.map_c, col, y, T.e, lane);
     }
   } else {
-    // plain bf16 store: FC2 (N = D), dlhs of FC1 (N = D), drhs (M x N per expert)
-    bool valid;
-    long rowoff;
-    if constexpr (Traits<KIND>::kGroupedK) {
-      valid = (T.m0 + row_in_tile) < p.M;
-      rowoff = (static_cast<long>(T.e) * p.M + T.m0 + row_in_tile) * p.N;
+    const int vw = min(32, max(0, T.rows - 32 * c.q));  // valid rows of this warp
+    if (vw == 0) return;
+    const bool full = (vw == 32);
+    const bool row_ok = lane < vw;
+    const int y = T.row0 + 32 * c.q;
+    const long r = static_cast<long>(y) + lane;
+    if constexpr (KIND == static_cast<int>(GemmKind::kFc1)) {
+      const bool with_z = p.out1 != nullptr;
+      for (int ch = 0; ch < BN / 128; ++ch) {
+        const int f0 = T.n0 + 64 * ch;
+        if (f0 >= p.F) break;
+        uint8_t* hb = nullptr;
+        uint8_t* zb = nullptr;
+        if (full) {
+          if (with_z) {
+            hb = ring_take<3>(c.ring, lane);
+            zb = ring_buf(c.ring, hb, 1);
+          } else {
+            hb = ring_take<1>(c.ring, lane);
+          }
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t u[32];
+          tmem_ld_32x32b_x32(tbase + 64 * ch + 32 * h, v);
+          tmem_ld_32x32b_x32(tbase + BN / 2 + 64 * ch + 32 * h, u);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float h0 = silu_f(__uint_as_float(v[2 * i])) * __uint_as_float(u[2 * i]);
+            const float h1 = silu_f(__uint_as_float(v[2 * i + 1])) * __uint_as_float(u[2 * i + 1]);
+            w[i] = pack_bf16x2(h0, h1);
+          }
+          uint32_t wg[16], wu[16];
+          if (with_z) {
+            pack16(v, wg);
+            pack16(u, wu);
+          }
+          if (full) {
+            put_half(hb, lane, h, w);
+            if (with_z) {
+              put_half(zb, lane, h, wg);
+              put_half(ring_buf(c.ring, hb, 2), lane, h, wu);
+            }
+          } else if (row_ok) {
+            store_row32(p.out0 + r * p.F + f0 + 32 * h, w);
+            if (with_z) {
+              store_row32(p.out1 + r * 2 * p.F + f0 + 32 * h, wg);
+              store_row32(p.out1 + r * 2 * p.F + p.F + f0 + 32 * h, wu);
+            }
+          }
+        }
+        if (full) {
+          publish(lane);
+          flush_2d(hb, c.map_c, f0, y, lane);
+          if (with_z) {
+            flush_2d(zb, c.map_d, f0, y, lane);
+            flush_2d(ring_buf(c.ring, hb, 2), c.map_d, p.F + f0, y, lane);
+          }
+        }
+      }
+    } else if constexpr (KIND == static_cast<int>(GemmKind::kDlhsFc2)) {
+      const bool fused = p.aux != nullptr;
+      for (int ch = 0; ch < BN / 64; ++ch) {
+        const int f0 = T.n0 + 64 * ch;
+        if (f0 >= p.F) break;
+        uint8_t* gb = nullptr;
+        if (full) gb = fused ? ring_take<2>(c.ring, lane) : ring_take<1>(c.ring, lane);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int fc = f0 + 32 * h;
+          uint4 zg[4], zu[4];
+          if (fused && row_ok) {
+            const uint4* pg = reinterpret_cast<const uint4*>(p.aux + r * 2 * p.F + fc);
+            const uint4* pu = reinterpret_cast<const uint4*>(p.aux + r * 2 * p.F + p.F + fc);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              zg[i] = __ldg(pg + i);
+              zu[i] = __ldg(pu + i);
+            }
+          }
+          tmem_ld_32x32b_x32(tbase + 64 * ch + 32 * h, v);
+          tmem_ld_wait();
+          if (fused) {
+            uint32_t wg[16], wu[16];
+            if (row_ok) {
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const uint32_t gq[4] = {zg[i].x, zg[i].y, zg[i].z, zg[i].w};
+                const uint32_t uq[4] = {zu[i].x, zu[i].y, zu[i].z, zu[i].w};
+#pragma unroll
+                for (int qq = 0; qq < 4; ++qq) {
+                  float rg[2], ru[2];
+#pragma unroll
+                  for (int hh = 0; hh < 2; ++hh) {
+                    const float dh = __uint_as_float(v[8 * i + 2 * qq + hh]);
+                    const float g = hh ? bf16hi(gq[qq]) : bf16lo(gq[qq]);
+                    const float u = hh ? bf16hi(uq[qq]) : bf16lo(uq[qq]);
+                    const float sg = 1.0f / (1.0f + expf(-g));
+                    rg[hh] = dh * u * sg * (1.0f + g * (1.0f - sg));
+                    ru[hh] = dh * g * sg;
+                  }
+                  wg[4 * i + qq] = pack_bf16x2(rg[0], rg[1]);
+                  wu[4 * i + qq] = pack_bf16x2(ru[0], ru[1]);
+                }
+              }
+            }
+            if (full) {
+              put_half(gb, lane, h, wg);
+              put_half(ring_buf(c.ring, gb, 1), lane, h, wu);
+            } else if (row_ok) {
+              store_row32(p.out0 + r * 2 * p.F + fc, wg);
+              store_row32(p.out0 + r * 2 * p.F + p.F + fc, wu);
+            }
+          } else {
+            pack16(v, w);
+            if (full) put_half(gb, lane, h, w);
+            else if (row_ok) store_row32(p.out0 + r * p.F + fc, w);
+          }
+        }
+        if (full) {
+          publish(lane);
+          flush_2d(gb, c.map_c, f0, y, lane);
+          if (fused) flush_2d(ring_buf(c.ring, gb, 1), c.map_c, p.F + f0, y, lane);
+        }
+      }
     } else {
-      valid = row_in_tile < T.rows;
-      rowoff = (static_cast<long>(T.row0) + row_in_tile) * p.N;
-    }
-    for (int c = 0; c < BN / 32; ++c) {
-      const int col = T.n0 + 32 * c;
-      if (col >= p.N) break;
-      tmem_ld_32x32b_x32(tbase + 32 * c, v);
-      tmem_ld_wait();
-      if (valid) store32(p.out0 + rowoff + col, v);
+      // plain bf16 store: FC2 and the dlhs of FC1 (N = D columns)
+      for (int ch = 0; ch < BN / 64; ++ch) {
+        const int col = T.n0 + 64 * ch;
+        if (col >= p.N) break;
+        uint8_t* buf = full ? ring_take<1>(c.ring, lane) : nullptr;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          tmem_ld_32x32b_x32(tbase + 64 * ch + 32 * h, v);
+          tmem_ld_wait();
+          pack16(v, w);
+          if (full) put_half(buf, lane, h, w);
+          else if (row_ok) store_row32(p.out0 + r * p.N + col + 32 * h, w);
+        }
+        if (full) {
+          publish(lane);
+          flush_2d(buf, c.map_c, col, y, lane);
+        }
+      }
     }
   }
 }
 
-template <int KIND>
+// An empty group's weight-gradient tile is zero.
+template <int BN>
+__device__ __forceinline__ void zero_tile(const Tile& T, EpiCtx& c, const Params& p) {
+  const int y = T.m0 + 32 * c.q;
+  if (y >= p.M) return;
+  for (int ch = 0; ch < BN / 64; ++ch) {
+    const int col = T.n0 + 64 * ch;
+    if (col >= p.N) break;
+    uint8_t* buf = ring_take<1>(c.ring, c.lane);
+    uint4* row = reinterpret_cast<uint4*>(buf + c.lane * 128);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) row[j] = make_uint4(0u, 0u, 0u, 0u);
+    publish(c.lane);
+    flush_3d(buf, c.map_c, col, y, T.e, c.lane);
+  }
+}
+
+template <int KIND, int BN, int STAGES>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
-                        const __grid_constant__ CUtensorMap map_b, const Params p) {
+                        const __grid_constant__ CUtensorMap map_b,
+                        const __grid_constant__ CUtensorMap map_c,
+                        const __grid_constant__ CUtensorMap map_d, const Params p) {
+  using S = Shape<BN, STAGES>;
+  using Tr = Traits<KIND, BN>;
+  constexpr int kStages = S::kStages;
+  constexpr int kStageBytes = S::kStageBytes;
+  constexpr uint32_t kTmemCols = S::kTmemCols;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* ring = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
-  SmemCtl& s = *reinterpret_cast<SmemCtl*>(ring + kStages * kStageBytes);
+  uint8_t* epi = ring + kStages * kStageBytes;  // staging of the epilogue warps
+  SmemCtl& s = *reinterpret_cast<SmemCtl*>(epi + kEpiBytes);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
@@ -299,6 +483,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_map(&map_a);
     tma_prefetch_map(&map_b);
+    tma_prefetch_map(&map_c);
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&s.full[i], 1);
       mbar_init(&s.empty[i], 1);
@@ -346,21 +531,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = s.tmem_base;
   const WaitCtl wc{&s.abort_flag, p.status, p.limit_ns};
-  const int ntiles = total_tiles<KIND>(p, s);
+  const int ntiles = total_tiles<KIND, BN>(p, s);
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       uint32_t stage = 0, phase = 0;
-      uint32_t fills[kStages] = {0, 0, 0, 0};
+      uint32_t fills[kStages];
+#pragma unroll
+      for (int i = 0; i < kStages; ++i) fills[i] = 0;
       bool aborted = false;
       for (int t = blockIdx.x; t < ntiles && !aborted; t += gridDim.x) {
-        const Tile T = decode_tile<KIND>(t, p, s);
+        const Tile T = decode_tile<KIND, BN>(t, p, s);
         for (int kb = 0; kb < T.kb; ++kb) {
           if (!mbar_wait(&s.empty[stage], phase ^ 1u, wc)) { aborted = true; break; }
           uint8_t* sa = ring + stage * kStageBytes;
           mbar_arrive_expect_tx(&s.full[stage], kStageBytes);
-          issue_loads<KIND>(T, kb, sa, sa + kAStageBytes, &s.full[stage], &map_a, &map_b, p);
+          issue_loads<KIND, BN>(T, kb, sa, sa + kAStageBytes, &s.full[stage], &map_a, &map_b, p);
           ++fills[stage];
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
@@ -373,11 +560,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------- MMA
     uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
-    uint32_t commits[kStages] = {0, 0, 0, 0};
+    uint32_t commits[kStages];
+#pragma unroll
+    for (int i = 0; i < kStages; ++i) commits[i] = 0;
     int last_stage = -1;
     bool aborted = false;
     for (int t = blockIdx.x; t < ntiles && !aborted; t += gridDim.x) {
-      const Tile T = decode_tile<KIND>(t, p, s);
+      const Tile T = decode_tile<KIND, BN>(t, p, s);
       if (T.kb == 0) continue;
       if (!mbar_wait(&s.tempty[acc], acc_phase ^ 1u, wc)) { aborted = true; break; }
       tc_fence_after();
@@ -387,13 +576,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         uint8_t* sa = ring + stage * kStageBytes;
         uint8_t* sb = sa + kAStageBytes;
-        if constexpr (Traits<KIND>::kGroupedK) {
+        if constexpr (Tr::kGroupedK) {
           const int valid = T.klen - kb * BK;
           if (valid < BK) {
             // rows [valid, 64) of every 64-wide chunk belong to the next group
             // (or lie past the end): zero them in A (2 chunks) and B (4 chunks)
             const int nrows = BK - valid;
-            const int nvec = 6 * nrows * 8;
+            constexpr int kChunksAB = 2 + BN / 64;
+            const int nvec = kChunksAB * nrows * 8;
             for (int i = lane; i < nvec; i += 32) {
               const int line = i >> 3, part = i & 7;
               const int chunk = line / nrows, j = valid + (line - chunk * nrows);
@@ -409,13 +599,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t b_addr = smem_u32(sb);
 #pragma unroll
           for (int kk = 0; kk < BK / kUmmaK; ++kk) {
-            const uint64_t ad = Traits<KIND>::kAMn
+            const uint64_t ad = Tr::kAMn
                                     ? smem_desc_sw128(a_addr + kk * 2048, kChunkBytes, 1024)
                                     : smem_desc_sw128(a_addr + kk * 32, 16, 1024);
-            const uint64_t bd = Traits<KIND>::kBMn
+            const uint64_t bd = Tr::kBMn
                                     ? smem_desc_sw128(b_addr + kk * 2048, kChunkBytes, 1024)
                                     : smem_desc_sw128(b_addr + kk * 32, 16, 1024);
-            umma_bf16(d_tmem, ad, bd, Traits<KIND>::kIdesc, (kb > 0 || kk > 0) ? 1u : 0u);
+            umma_bf16(d_tmem, ad, bd, Tr::kIdesc, (kb > 0 || kk > 0) ? 1u : 0u);
           }
           umma_commit(&s.empty[stage]);
         }
@@ -435,33 +625,25 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // -------------------------------------------------------- epilogue
     const int q = warp & 3;  // TMEM lane quarter this warp may access
-    const int row_in_tile = q * 32 + lane;
+    EpiCtx ec{&map_c, &map_d, Ring{epi + (warp - 2) * kRingBufs * kBufBytes, 0u}, q, lane};
     uint32_t acc = 0, acc_phase = 0;
     for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
-      const Tile T = decode_tile<KIND>(t, p, s);
+      const Tile T = decode_tile<KIND, BN>(t, p, s);
       if (T.kb == 0) {
-        if constexpr (Traits<KIND>::kGroupedK) {
-          // empty group: its weight gradient is zero
-          if (T.m0 + row_in_tile < p.M) {
-            const long rowoff = (static_cast<long>(T.e) * p.M + T.m0 + row_in_tile) * p.N;
-            for (int c = 0; c < BN / 32; ++c) {
-              const int col = T.n0 + 32 * c;
-              if (col >= p.N) break;
-              store32_zero(p.out0 + rowoff + col);
-            }
-          }
-        }
+        if constexpr (Tr::kGroupedK) zero_tile<BN>(T, ec, p);
         continue;
       }
       if (!mbar_wait(&s.tfull[acc], acc_phase, wc)) break;
       tc_fence_after();
-      epilogue_tile<KIND>(T, tmem_base + acc * BN + (static_cast<uint32_t>(q * 32) << 16),
-                          row_in_tile, p);
+      epilogue_tile<KIND, BN>(T, tmem_base + acc * BN + (static_cast<uint32_t>(q * 32) << 16), ec,
+                              p);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&s.tempty[acc]);
       if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
     }
+    if (lane == 0) bulk_wait_all();  // every store has finished before the CTA exits
+    __syncwarp();
   }
 
   tc_fence_before();
@@ -522,21 +704,100 @@ bool map3d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t mid, uint6
   return make_map(m, base, 3, dims, strides, box);
 }
 
-template <int KIND>
-cudaError_t launch_kind(const CUtensorMap& ma, const CUtensorMap& mb, const Params& p,
-                        int max_tiles, cudaStream_t s) {
-  auto kern = grouped_gemm_kernel<KIND>;
+template <int KIND, int BN, int STAGES>
+cudaError_t launch_kind(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mc,
+                        const CUtensorMap& md, const Params& p, int max_tiles, cudaStream_t s) {
+  auto kern = grouped_gemm_kernel<KIND, BN, STAGES>;
+  constexpr size_t bytes = smem_bytes<Shape<BN, STAGES>>();
+  static_assert(bytes <= 227 * 1024, "shared memory");
   cudaError_t err =
-      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
   if (err != cudaSuccess) return err;
   int grid = sm_count();
   if (max_tiles < grid) grid = max_tiles;
   if (grid <= 0) return cudaSuccess;
-  kern<<<grid, kThreads, kSmemBytes, s>>>(ma, mb, p);
+  kern<<<grid, kThreads, bytes, s>>>(ma, mb, mc, md, p);
   return cudaGetLastError();
 }
 
 inline int cdiv(long a, long b) { return static_cast<int>((a + b - 1) / b); }
+
+template <int BN, int STAGES>
+cudaError_t launch_shape(const GemmCall& c, cudaStream_t s) {
+  const moe_dims& d = c.d;
+  const long R = static_cast<long>(d.T) * d.K;
+  Params p{};
+  p.offs = c.offs;
+  p.out0 = static_cast<__nv_bfloat16*>(c.out0);
+  p.out1 = static_cast<__nv_bfloat16*>(c.out1);
+  p.aux = static_cast<const __nv_bfloat16*>(c.aux);
+  p.status = c.dev_status;
+  p.limit_ns = kDefaultWaitLimitNs;
+  p.E = d.E;
+  p.F = d.F;
+  CUtensorMap ma, mb, mc, md;
+  bool ok = false;
+  const long rows_tiles_bound = R / BM + d.E;
+  const long F2 = 2L * d.F;
+  switch (c.kind) {
+    case GemmKind::kFc1:
+      p.Kdim = d.D;
+      p.N = d.F;
+      p.n_tiles = cdiv(d.F, BN / 2);
+      ok = map2d(&ma, c.a, d.D, R, 64, BM) && map3d(&mb, c.b, F2, d.D, d.E, 64, 64) &&
+           map2d(&mc, c.out0, d.F, R, 64, 32);
+      if (ok) ok = (c.out1 != nullptr) ? map2d(&md, c.out1, F2, R, 64, 32) : (md = mc, true);
+      if (!ok) return cudaErrorInvalidValue;
+      return launch_kind<0, BN, STAGES>(ma, mb, mc, md, p,
+                                        static_cast<int>(rows_tiles_bound * p.n_tiles), s);
+    case GemmKind::kFc2:
+      p.Kdim = d.F;
+      p.N = d.D;
+      p.n_tiles = cdiv(d.D, BN);
+      ok = map2d(&ma, c.a, d.F, R, 64, BM) && map3d(&mb, c.b, d.D, d.F, d.E, 64, 64) &&
+           map2d(&mc, c.out0, d.D, R, 64, 32);
+      if (!ok) return cudaErrorInvalidValue;
+      return launch_kind<1, BN, STAGES>(ma, mb, mc, mc, p,
+                                        static_cast<int>(rows_tiles_bound * p.n_tiles), s);
+    case GemmKind::kDlhsFc2:
+      p.Kdim = d.D;
+      p.N = d.F;
+      p.n_tiles = cdiv(d.F, BN);
+      ok = map2d(&ma, c.a, d.D, R, 64, BM) && map3d(&mb, c.b, d.D, d.F, d.E, 64, BN) &&
+           map2d(&mc, c.out0, c.aux != nullptr ? F2 : d.F, R, 64, 32);
+      if (!ok) return cudaErrorInvalidValue;
+      return launch_kind<2, BN, STAGES>(ma, mb, mc, mc, p,
+                                        static_cast<int>(rows_tiles_bound * p.n_tiles), s);
+    case GemmKind::kDlhsFc1:
+      p.Kdim = 2 * d.F;
+      p.N = d.D;
+      p.n_tiles = cdiv(d.D, BN);
+      ok = map2d(&ma, c.a, F2, R, 64, BM) && map3d(&mb, c.b, F2, d.D, d.E, 64, BN) &&
+           map2d(&mc, c.out0, d.D, R, 64, 32);
+      if (!ok) return cudaErrorInvalidValue;
+      return launch_kind<3, BN, STAGES>(ma, mb, mc, mc, p,
+                                        static_cast<int>(rows_tiles_bound * p.n_tiles), s);
+    case GemmKind::kDrhsFc2:
+      p.M = d.F;
+      p.N = d.D;
+      p.m_tiles = cdiv(d.F, BM);
+      p.n_tiles = cdiv(d.D, BN);
+      ok = map2d(&ma, c.a, d.F, R, 64, 64) && map2d(&mb, c.b, d.D, R, 64, 64) &&
+           map3d(&mc, c.out0, d.D, d.F, d.E, 64, 32);
+      if (!ok) return cudaErrorInvalidValue;
+      return launch_kind<4, BN, STAGES>(ma, mb, mc, mc, p, d.E * p.m_tiles * p.n_tiles, s);
+    case GemmKind::kDrhsFc1:
+      p.M = d.D;
+      p.N = 2 * d.F;
+      p.m_tiles = cdiv(d.D, BM);
+      p.n_tiles = cdiv(F2, BN);
+      ok = map2d(&ma, c.a, d.D, R, 64, 64) && map2d(&mb, c.b, F2, R, 64, 64) &&
+           map3d(&mc, c.out0, F2, d.D, d.E, 64, 32);
+      if (!ok) return cudaErrorInvalidValue;
+      return launch_kind<5, BN, STAGES>(ma, mb, mc, mc, p, d.E * p.m_tiles * p.n_tiles, s);
+  }
+  return cudaErrorInvalidValue;
+}
 
 }  // namespace
 
@@ -551,65 +812,11 @@ cudaError_t launch_grouped_gemm(const GemmCall& c, cudaStream_t s) {
       return cudaMemsetAsync(c.out0, 0, static_cast<size_t>(d.E) * d.D * 2 * d.F * 2, s);
     return cudaSuccess;
   }
-  Params p{};
-  p.offs = c.offs;
-  p.out0 = static_cast<__nv_bfloat16*>(c.out0);
-  p.out1 = static_cast<__nv_bfloat16*>(c.out1);
-  p.aux = static_cast<const __nv_bfloat16*>(c.aux);
-  p.status = c.dev_status;
-  p.limit_ns = kDefaultWaitLimitNs;
-  p.E = d.E;
-  p.F = d.F;
-  CUtensorMap ma, mb;
-  bool ok = false;
-  const long rows_tiles_bound = R / BM + d.E;
-  switch (c.kind) {
-    case GemmKind::kFc1:
-      p.Kdim = d.D;
-      p.N = d.F;
-      p.n_tiles = cdiv(d.F, BN / 2);
-      ok = map2d(&ma, c.a, d.D, R, 64, BM) && map3d(&mb, c.b, 2L * d.F, d.D, d.E, 64, 64);
-      if (!ok) return cudaErrorInvalidValue;
-      return launch_kind<0>(ma, mb, p, static_cast<int>(rows_tiles_bound * p.n_tiles), s);
-    case GemmKind::kFc2:
-      p.Kdim = d.F;
-      p.N = d.D;
-      p.n_tiles = cdiv(d.D, BN);
-      ok = map2d(&ma, c.a, d.F, R, 64, BM) && map3d(&mb, c.b, d.D, d.F, d.E, 64, 64);
-      if (!ok) return cudaErrorInvalidValue;
-      return launch_kind<1>(ma, mb, p, static_cast<int>(rows_tiles_bound * p.n_tiles), s);
-    case GemmKind::kDlhsFc2:
-      p.Kdim = d.D;
-      p.N = d.F;
-      p.n_tiles = cdiv(d.F, BN);
-      ok = map2d(&ma, c.a, d.D, R, 64, BM) && map3d(&mb, c.b, d.D, d.F, d.E, 64, BN);
-      if (!ok) return cudaErrorInvalidValue;
-      return launch_kind<2>(ma, mb, p, static_cast<int>(rows_tiles_bound * p.n_tiles), s);
-    case GemmKind::kDlhsFc1:
-      p.Kdim = 2 * d.F;
-      p.N = d.D;
-      p.n_tiles = cdiv(d.D, BN);
-      ok = map2d(&ma, c.a, 2L * d.F, R, 64, BM) && map3d(&mb, c.b, 2L * d.F, d.D, d.E, 64, BN);
-      if (!ok) return cudaErrorInvalidValue;
-      return launch_kind<3>(ma, mb, p, static_cast<int>(rows_tiles_bound * p.n_tiles), s);
-    case GemmKind::kDrhsFc2:
-      p.M = d.F;
-      p.N = d.D;
-      p.m_tiles = cdiv(d.F, BM);
-      p.n_tiles = cdiv(d.D, BN);
-      ok = map2d(&ma, c.a, d.F, R, 64, 64) && map2d(&mb, c.b, d.D, R, 64, 64);
-      if (!ok) return cudaErrorInvalidValue;
-      return launch_kind<4>(ma, mb, p, d.E * p.m_tiles * p.n_tiles, s);
-    case GemmKind::kDrhsFc1:
-      p.M = d.D;
-      p.N = 2 * d.F;
-      p.m_tiles = cdiv(d.D, BM);
-      p.n_tiles = cdiv(2L * d.F, BN);
-      ok = map2d(&ma, c.a, d.D, R, 64, 64) && map2d(&mb, c.b, 2L * d.F, R, 64, 64);
-      if (!ok) return cudaErrorInvalidValue;
-      return launch_kind<5>(ma, mb, p, d.E * p.m_tiles * p.n_tiles, s);
-  }
-  return cudaErrorInvalidValue;
+#ifndef MOE_GEMM_BN
+#define MOE_GEMM_BN 256
+#define MOE_GEMM_STAGES 3
+#endif
+  return launch_shape<MOE_GEMM_BN, MOE_GEMM_STAGES>(c, s);
 }
 
 }  // namespace moe

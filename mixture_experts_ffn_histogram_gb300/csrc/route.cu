@@ -6,13 +6,15 @@
 // kernels and split-expert wi layout for TPU v6e", Commits table row 2: the
 // group_size histogram is computed before the token gather.
 //
-// Three launches, all deterministic (no atomic decides an order):
-//   1. route_topk_hist: one warp per token selects the top-K scores by K
-//      rounds of a warp-wide (score desc, id asc) arg-max and computes the
-//      routing weights; each block (one chunk of 256 tokens) also counts its
-//      slots per expert in shared memory -> counts[chunk, E].
-//   2. route_scan: per expert, the exclusive prefix of counts over chunks,
-//      group_sizes, and the exclusive prefix over experts (group_offsets).
+// Three kernels, all deterministic (no atomic decides an order; atomics only
+// add up counts):
+//   1. route_topk: one warp per token (grid-stride over all tokens) selects
+//      the top-K scores by K rounds of a warp-wide (score desc, id asc)
+//      arg-max, computes the routing weights, and adds each slot to the
+//      count of its (chunk of 256 tokens, expert) pair in global memory.
+//   2. route_scan: per expert, the exclusive prefix of the counts over
+//      chunks, group_sizes, and the exclusive prefix over experts
+//      (group_offsets); threads are indexed by expert so reads coalesce.
 //   3. route_rank: per chunk, each warp ranks its contiguous run of slots
 //      with __match_any_sync; pos = group_offsets[e] + chunk prefix + warp
 //      prefix + rank, i.e. the stable order in the flat slot index t*K+k.
@@ -33,121 +35,114 @@ __device__ __forceinline__ bool better(float v1, int e1, float v2, int e2) {
 }
 
 template <int EPL>  // expert scores held per lane: E <= 32 * EPL
-__global__ void __launch_bounds__(kRouteThreads) route_topk_hist(
+__global__ void __launch_bounds__(kRouteThreads) route_topk(
     const float* __restrict__ logits, const float* __restrict__ bias, int mode,
     int32_t* __restrict__ ids, float* __restrict__ w, int32_t* __restrict__ counts, int T, int E,
     int K, int32_t* status) {
-  extern __shared__ int32_t hist[];  // [E]
-  for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
-  __syncthreads();
   const int lane = threadIdx.x & 31;
-  const int warp = threadIdx.x >> 5;
-  const int t_begin = blockIdx.x * kRouteTokensPerChunk;
-  const int t_end = min(T, t_begin + kRouteTokensPerChunk);
-
   if (mode == MOE_SCORE_GIVEN) {
-    const long j0 = static_cast<long>(t_begin) * K, j1 = static_cast<long>(t_end) * K;
-    for (long j = j0 + threadIdx.x; j < j1; j += blockDim.x) {
+    const long R = static_cast<long>(T) * K;
+    for (long j = static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x; j < R;
+         j += static_cast<long>(gridDim.x) * blockDim.x) {
       const int e = ids[j];
-      if (e >= 0 && e < E) atomicAdd(&hist[e], 1);
+      const int chunk = static_cast<int>(j / K) / kRouteTokensPerChunk;
+      if (e >= 0 && e < E) atomicAdd(&counts[static_cast<long>(chunk) * E + e], 1);
       else report(status, MOE_ERR_DEVICE);
     }
-  } else {
-    for (int t = t_begin + warp; t < t_end; t += kRouteWarps) {
-      float s[EPL];
-      const float* row = logits + static_cast<long>(t) * E;
+    return;
+  }
+  const int warps_total = gridDim.x * kRouteWarps;
+  for (int t = blockIdx.x * kRouteWarps + (threadIdx.x >> 5); t < T; t += warps_total) {
+    float s[EPL];
+    const float* row = logits + static_cast<long>(t) * E;
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+      const int e = lane + 32 * i;
+      if (e < E) {
+        float v = __ldg(row + e);
+        if (bias != nullptr) v = __fadd_rn(v, __ldg(bias + e));
+        s[i] = v;
+      } else {
+        s[i] = -FLT_MAX;
+      }
+    }
+    uint32_t taken = 0;
+    float my_v = 0.f;
+    int my_e = 0;
+    for (int k = 0; k < K; ++k) {
+      float bv = -FLT_MAX;
+      int be = INT_MAX;  // "no candidate" loses to every real expert
 #pragma unroll
       for (int i = 0; i < EPL; ++i) {
         const int e = lane + 32 * i;
-        if (e < E) {
-          float v = __ldg(row + e);
-          if (bias != nullptr) v = __fadd_rn(v, __ldg(bias + e));
-          s[i] = v;
-        } else {
-          s[i] = -FLT_MAX;
-        }
+        if (e < E && !((taken >> i) & 1u) && better(s[i], e, bv, be)) { bv = s[i]; be = e; }
       }
-      uint32_t taken = 0;
-      float my_v = 0.f;
-      int my_e = 0;
-      for (int k = 0; k < K; ++k) {
-        float bv = -FLT_MAX;
-        int be = INT_MAX;  // "no candidate" loses to every real expert
 #pragma unroll
-        for (int i = 0; i < EPL; ++i) {
-          const int e = lane + 32 * i;
-          if (e < E && !((taken >> i) & 1u) && better(s[i], e, bv, be)) { bv = s[i]; be = e; }
-        }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-          const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-          const int oe = __shfl_xor_sync(0xffffffffu, be, off);
-          if (better(ov, oe, bv, be)) { bv = ov; be = oe; }
-        }
-        if ((be & 31) == lane) taken |= 1u << (be >> 5);
-        if (lane == k) { my_v = bv; my_e = be; }
+      for (int off = 16; off > 0; off >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+        const int oe = __shfl_xor_sync(0xffffffffu, be, off);
+        if (better(ov, oe, bv, be)) { bv = ov; be = oe; }
       }
-      // routing weights of the K selected scores (lane k holds slot k)
-      float ex = 0.f;
-      if (mode == MOE_SCORE_SOFTMAX_TOPK) {
-        const float m = __shfl_sync(0xffffffffu, my_v, 0);
-        if (lane < K) ex = expf(my_v - m);
-      } else {
-        if (lane < K) ex = 1.0f / (1.0f + expf(-my_v));
-      }
-      float sum = 0.f;  // ascending slot order
-      for (int k = 0; k < K; ++k) sum = __fadd_rn(sum, __shfl_sync(0xffffffffu, ex, k));
-      if (lane < K) {
-        const long j = static_cast<long>(t) * K + lane;
-        ids[j] = my_e;
-        w[j] = __fdiv_rn(ex, sum);
-        atomicAdd(&hist[my_e], 1);
-      }
+      if ((be & 31) == lane) taken |= 1u << (be >> 5);
+      if (lane == k) { my_v = bv; my_e = be; }
+    }
+    // routing weights of the K selected scores (lane k holds slot k)
+    float ex = 0.f;
+    if (mode == MOE_SCORE_SOFTMAX_TOPK) {
+      const float m = __shfl_sync(0xffffffffu, my_v, 0);
+      if (lane < K) ex = expf(my_v - m);
+    } else {
+      if (lane < K) ex = 1.0f / (1.0f + expf(-my_v));
+    }
+    float sum = 0.f;  // ascending slot order
+    for (int k = 0; k < K; ++k) sum = __fadd_rn(sum, __shfl_sync(0xffffffffu, ex, k));
+    if (lane < K) {
+      const long j = static_cast<long>(t) * K + lane;
+      ids[j] = my_e;
+      w[j] = __fdiv_rn(ex, sum);
+      atomicAdd(&counts[static_cast<long>(t / kRouteTokensPerChunk) * E + my_e], 1);
     }
   }
-  __syncthreads();
-  for (int e = threadIdx.x; e < E; e += blockDim.x)
-    counts[static_cast<long>(blockIdx.x) * E + e] = hist[e];
 }
 
-// One block of 1024 threads: warp w handles experts w, w+32, ...; its lanes
-// split the chunks into contiguous runs.
+// One block of 1024 threads.  Thread (g, e) = (tid / E, tid % E) covers
+// expert e over chunk group g (a contiguous run of chunks), so that each
+// load of counts[c, 0..E) is coalesced across the threads of a group.
 __global__ void __launch_bounds__(1024) route_scan(const int32_t* __restrict__ counts,
                                                    int32_t* __restrict__ chunk_excl, int nchunks,
                                                    int E, int32_t* __restrict__ group_sizes,
                                                    int32_t* __restrict__ group_offsets) {
+  __shared__ int32_t part[1024];
   __shared__ int32_t tot[1024];
   __shared__ int32_t warp_sum[32];
-  const int lane = threadIdx.x & 31;
-  const int warp = threadIdx.x >> 5;
-  const int cpl = (nchunks + 31) / 32;
-  const int c0 = min(nchunks, lane * cpl), c1 = min(nchunks, c0 + cpl);
-  for (int e = warp; e < E; e += 32) {
+  const int tid = threadIdx.x;
+  const int lane = tid & 31;
+  const int warp = tid >> 5;
+  const int G = max(1, 1024 / E);
+  const int e = tid % E, g = tid / E;
+  const bool active = g < G;
+  const int cpg = (nchunks + G - 1) / G;
+  const int c0 = min(nchunks, g * cpg), c1 = min(nchunks, c0 + cpg);
+  if (active) {
     int local = 0;
+#pragma unroll 4
     for (int c = c0; c < c1; ++c) local += counts[static_cast<long>(c) * E + e];
-    int incl = local;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const int v = __shfl_up_sync(0xffffffffu, incl, off);
-      if (lane >= off) incl += v;
-    }
-    int run = incl - local;
-    for (int c = c0; c < c1; ++c) {
-      const long idx = static_cast<long>(c) * E + e;
-      const int v = counts[idx];
-      chunk_excl[idx] = run;
+    part[g * E + e] = local;
+  }
+  __syncthreads();
+  if (tid < E) {
+    int run = 0;
+    for (int q = 0; q < G; ++q) {
+      const int v = part[q * E + tid];
+      part[q * E + tid] = run;
       run += v;
     }
-    const int total = __shfl_sync(0xffffffffu, incl, 31);
-    if (lane == 0) {
-      tot[e] = total;
-      group_sizes[e] = total;
-    }
+    tot[tid] = run;
+    group_sizes[tid] = run;
   }
   __syncthreads();
   // exclusive scan of tot[0..E) over the block
-  const int e = threadIdx.x;
-  const int v = (e < E) ? tot[e] : 0;
+  const int v = (tid < E) ? tot[tid] : 0;
   int incl = v;
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
@@ -168,9 +163,18 @@ __global__ void __launch_bounds__(1024) route_scan(const int32_t* __restrict__ c
   }
   __syncthreads();
   const int excl = warp_sum[warp] + incl - v;
-  if (e < E) group_offsets[e] = excl;
-  if (e == E - 1) group_offsets[E] = excl + v;
-  if (E == 0 && e == 0) group_offsets[0] = 0;
+  if (tid < E) group_offsets[tid] = excl;
+  if (tid == E - 1) group_offsets[E] = excl + v;
+  if (active) {
+    int run = part[g * E + e];
+#pragma unroll 4
+    for (int c = c0; c < c1; ++c) {
+      const long idx = static_cast<long>(c) * E + e;
+      const int cv = counts[idx];
+      chunk_excl[idx] = run;
+      run += cv;
+    }
+  }
 }
 
 // One block per chunk; warp w ranks slots [j0 + w*32K, j0 + (w+1)*32K).
@@ -237,9 +241,13 @@ __global__ void __launch_bounds__(kRouteThreads) route_rank(
 template <int EPL>
 cudaError_t launch_topk(const float* logits, const float* bias, int mode, int32_t* ids, float* w,
                         int32_t* counts, const moe_dims& d, int32_t* status, cudaStream_t s) {
-  const int nchunks = route_chunks(d.T);
-  route_topk_hist<EPL><<<nchunks, kRouteThreads, d.E * sizeof(int32_t), s>>>(
-      logits, bias, mode, ids, w, counts, d.T, d.E, d.K, status);
+  long blocks;
+  if (mode == MOE_SCORE_GIVEN) blocks = (static_cast<long>(d.T) * d.K + kRouteThreads - 1) / kRouteThreads;
+  else blocks = (d.T + kRouteWarps - 1) / kRouteWarps;
+  const long cap = static_cast<long>(sm_count()) * 8;
+  if (blocks > cap) blocks = cap;
+  route_topk<EPL><<<static_cast<int>(blocks), kRouteThreads, 0, s>>>(logits, bias, mode, ids, w,
+                                                                      counts, d.T, d.E, d.K, status);
   return cudaGetLastError();
 }
 
@@ -253,6 +261,8 @@ cudaError_t launch_route_histogram(const float* logits, const float* bias, int m
   const int nchunks = route_chunks(d.T);
   cudaError_t err = cudaSuccess;
   if (nchunks > 0) {
+    err = cudaMemsetAsync(counts, 0, static_cast<size_t>(nchunks) * d.E * sizeof(int32_t), s);
+    if (err != cudaSuccess) return err;
     const int epl = (d.E + 31) / 32;
     if (epl <= 1) err = launch_topk<1>(logits, bias, mode, ids, w, counts, d, dev_status, s);
     else if (epl <= 2) err = launch_topk<2>(logits, bias, mode, ids, w, counts, d, dev_status, s);
