@@ -17,24 +17,32 @@
 // kernel (row masks in the epilogue, zero-filled reduction tails), never by a
 // separate masking pass (TransformerEngine page, Changes).
 //
-// Design (one persistent CTA per SM, 192 threads):
-//   warp 0     TMA producer: loads 128x64 A tiles and 256x64 B tiles (bf16,
-//              128-byte swizzle) into a 4-stage shared-memory ring; for the
-//              forward and dlhs GEMMs B comes from a 3-D tensor map whose
-//              outer coordinate is the expert.
-//   warp 1     allocates 512 TMEM columns (two 128x256 fp32 accumulators),
-//              and one thread issues tcgen05.mma (M=128, N=256, K=16) and
-//              tcgen05.commit; for drhs it zero-fills the rows of the last
-//              reduction block that belong to the next expert.
-//   warps 2-5  epilogue: tcgen05.ld of the accumulator (one row per thread),
-//              SwiGLU / SwiGLU-backward / bf16 conversion, masked stores; the
-//              second accumulator lets the next tile's MMAs overlap it.
+// Design: persistent warp-specialised kernel, one CTA per SM, 192 threads.
+//   warp 0     TMA producer: 128x64 A tiles and (BN/CG)x64 B tiles (bf16,
+//              128-byte swizzle) into a shared-memory ring; for the forward
+//              and dlhs GEMMs B comes from a 3-D tensor map whose outer
+//              coordinate is the expert.
+//   warp 1     TMEM allocation (two 128xBN fp32 accumulators) and MMA issue:
+//              one thread issues tcgen05.mma (K=16) and tcgen05.commit; for
+//              drhs the warp zero-fills the rows of the last reduction block
+//              that belong to the next group.
+//   warps 2-5  epilogue: tcgen05.ld (one row per thread), SwiGLU / SwiGLU
+//              backward / bf16 conversion, staged in swizzled shared memory
+//              and written by TMA stores; the second accumulator lets the
+//              next tile's MMAs overlap it.
+// CG = 2 runs the CTA pair of a 2-CTA cluster on one 256-row tile: each CTA
+// loads its own 128 A rows and half of the B columns, the even CTA issues
+// tcgen05.mma.cta_group::2 (M = 256) reading both CTAs' shared memory, and
+// each CTA's TMEM holds its 128 rows.  Both CTAs' loads complete on the even
+// CTA's barrier (TMA with .cta_group::2); commits are multicast to both CTAs.
+// This halves the B bytes each SM loads per MMA.
 // Tiles are scheduled on the device from group_offsets (no host sync):
-// forward/dlhs tiles are (expert, 128-row block, N block) with the rows of a
-// block starting at the group's first row; drhs tiles are (expert, M block,
-// N block) with the group's rows as the reduction.
+// forward/dlhs tiles are (expert, 128*CG-row block, N block) with the rows of
+// a block starting at the group's first row; drhs tiles are (expert, M
+// block, N block) with the group's rows as the reduction.
 #include <cuda.h>
 
+#include <cstdlib>
 #include <mutex>
 
 #include "common.cuh"
@@ -51,19 +59,9 @@ constexpr int kChunkBytes = 64 * BK * 2;   // one 64-wide MN chunk of 64 K rows:
 constexpr int kThreads = 192;
 constexpr int kMaxExperts = 1024;
 constexpr int kMaxStages = 8;
-constexpr int kEpiBytes_ = 4 * 4 * 32 * 128;  // epilogue staging (see kEpiBytes)
-
-// Tile shape: 128 x BN output tile per accumulator, `stages`-deep ring.
-template <int BN_, int STAGES_>
-struct Shape {
-  static constexpr int BN = BN_;
-  static constexpr int kStages = STAGES_;
-  static constexpr int kBStageBytes = BN * BK * 2;
-  static constexpr int kStageBytes = kAStageBytes + kBStageBytes;
-  static constexpr int kTmemCols = 2 * BN;  // two accumulators
-  static_assert(BN == 128 || BN == 256, "tile width");
-  static_assert(STAGES_ <= kMaxStages, "stages");
-};
+constexpr int kEpiWarps = 4;
+constexpr int kBufBytes = 32 * 128;  // staging buffer: 32 rows x 64 bf16
+constexpr size_t kSmemLimit = 227 * 1024;
 
 struct SmemCtl {
   uint64_t full[kMaxStages];
@@ -73,12 +71,30 @@ struct SmemCtl {
   uint32_t tmem_base;
   int abort_flag;
   int off[kMaxExperts + 1];  // group offsets
-  int mt[kMaxExperts + 1];   // prefix of 128-row blocks per group
+  int mt[kMaxExperts + 1];   // prefix of (128*CG)-row blocks per group
 };
-template <class S>
-constexpr size_t smem_bytes() {
-  return 1024 + static_cast<size_t>(S::kStages) * S::kStageBytes + kEpiBytes_ + sizeof(SmemCtl);
-}
+
+// Tile shape: 128 x BN accumulator per CTA, CG CTAs per MMA, a `STAGES`-deep
+// operand ring and RING staging buffers per epilogue warp.
+template <int BN_, int STAGES_, int CG_, int RING_>
+struct Shape {
+  static constexpr int BN = BN_;
+  static constexpr int kStages = STAGES_;
+  static constexpr int CG = CG_;
+  static constexpr int kRing = RING_;
+  static constexpr int kBRows = BN / CG;  // B columns held by one CTA
+  static constexpr int kBStageBytes = kBRows * BK * 2;
+  static constexpr int kStageBytes = kAStageBytes + kBStageBytes;
+  static constexpr int kTmemCols = 2 * BN;  // two accumulators
+  static constexpr int kEpiBytes = kEpiWarps * RING_ * kBufBytes;
+  static constexpr size_t kSmemBytes =
+      1024 + static_cast<size_t>(STAGES_) * kStageBytes + kEpiBytes + sizeof(SmemCtl);
+  static_assert(BN == 256, "tile width");
+  static_assert(CG == 1 || CG == 2, "CTA group");
+  static_assert(STAGES_ >= 2 && STAGES_ <= kMaxStages, "stages");
+  static_assert(RING_ >= 1 && RING_ <= 4, "staging ring");
+  static_assert(kSmemBytes <= kSmemLimit, "shared memory");
+};
 
 struct Params {
   const int32_t* offs;
@@ -91,30 +107,30 @@ struct Params {
   int m_tiles, n_tiles;
 };
 
-template <int KIND, int BN>
+template <int KIND, int BN, int CG>
 struct Traits {
   static constexpr bool kGroupedK = (KIND == static_cast<int>(GemmKind::kDrhsFc2) ||
                                      KIND == static_cast<int>(GemmKind::kDrhsFc1));
   static constexpr bool kAMn = kGroupedK;
   static constexpr bool kBMn = (KIND == static_cast<int>(GemmKind::kFc1) ||
                                 KIND == static_cast<int>(GemmKind::kFc2) || kGroupedK);
-  static constexpr uint32_t kIdesc = instr_desc_bf16(BM, BN, kAMn, kBMn);
+  static constexpr uint32_t kIdesc = instr_desc_bf16(BM * CG, BN, kAMn, kBMn);
 };
 
 struct Tile {
   int e;
-  int row0;   // first output row (forward/dlhs) or first group row (drhs)
-  int rows;   // valid rows of the tile (forward/dlhs)
-  int m0;     // drhs: first output row (of F or D)
-  int n0;     // first output column
+  int row0;   // this CTA's first output row (forward/dlhs) or first group row (drhs)
+  int rows;   // valid rows of this CTA's part of the tile (forward/dlhs)
+  int m0;     // drhs: this CTA's first output row (of F or D)
+  int n0;     // first output column of the tile
   int kb;     // reduction blocks of 64
   int klen;   // drhs: group rows
 };
 
-template <int KIND, int BN>
-__device__ __forceinline__ Tile decode_tile(int t, const Params& p, const SmemCtl& s) {
+template <int KIND, int BN, int CG>
+__device__ __forceinline__ Tile decode_tile(int t, int rank, const Params& p, const SmemCtl& s) {
   Tile T;
-  if constexpr (!Traits<KIND, BN>::kGroupedK) {
+  if constexpr (!Traits<KIND, BN, CG>::kGroupedK) {
     const int mt = t / p.n_tiles;
     const int nt = t - mt * p.n_tiles;
     int lo = 0, hi = p.E - 1;  // largest e with mt[e] <= mt
@@ -124,8 +140,8 @@ __device__ __forceinline__ Tile decode_tile(int t, const Params& p, const SmemCt
       else hi = mid - 1;
     }
     T.e = lo;
-    T.row0 = s.off[lo] + (mt - s.mt[lo]) * BM;
-    T.rows = min(BM, s.off[lo + 1] - T.row0);
+    T.row0 = s.off[lo] + (mt - s.mt[lo]) * (BM * CG) + BM * rank;
+    T.rows = max(0, min(BM, s.off[lo + 1] - T.row0));
     T.m0 = 0;
     T.n0 = nt * (KIND == static_cast<int>(GemmKind::kFc1) ? BN / 2 : BN);
     T.kb = p.Kdim / BK;
@@ -135,7 +151,7 @@ __device__ __forceinline__ Tile decode_tile(int t, const Params& p, const SmemCt
     T.e = t / per_e;
     const int r = t - T.e * per_e;
     const int mt = r / p.n_tiles;
-    T.m0 = mt * BM;
+    T.m0 = mt * (BM * CG) + BM * rank;
     T.n0 = (r - mt * p.n_tiles) * BN;
     T.row0 = s.off[T.e];
     T.klen = s.off[T.e + 1] - T.row0;
@@ -145,80 +161,122 @@ __device__ __forceinline__ Tile decode_tile(int t, const Params& p, const SmemCt
   return T;
 }
 
-template <int KIND, int BN>
+template <int KIND, int BN, int CG>
 __device__ __forceinline__ int total_tiles(const Params& p, const SmemCtl& s) {
-  if constexpr (!Traits<KIND, BN>::kGroupedK) return s.mt[p.E] * p.n_tiles;
+  if constexpr (!Traits<KIND, BN, CG>::kGroupedK) return s.mt[p.E] * p.n_tiles;
   else return p.E * p.m_tiles * p.n_tiles;
 }
 
-template <int KIND, int BN>
-__device__ __forceinline__ void issue_loads(const Tile& T, int kb, uint8_t* sa, uint8_t* sb,
-                                            uint64_t* bar, const CUtensorMap* ma,
+// One TMA load of a stage: for a pair, the bytes complete on the even CTA's
+// barrier (`bar` is then its shared::cluster address).
+template <int CG>
+__device__ __forceinline__ void load2(void* dst, const CUtensorMap* map, uint32_t bar, int c0,
+                                      int c1) {
+  if constexpr (CG == 1) tma_load_2d_addr(dst, map, bar, c0, c1);
+  else tma_load_2d_pair(dst, map, bar, c0, c1);
+}
+template <int CG>
+__device__ __forceinline__ void load3(void* dst, const CUtensorMap* map, uint32_t bar, int c0,
+                                      int c1, int c2) {
+  if constexpr (CG == 1) tma_load_3d_addr(dst, map, bar, c0, c1, c2);
+  else tma_load_3d_pair(dst, map, bar, c0, c1, c2);
+}
+
+// TMA loads of one reduction block: this CTA's 128 A rows and its BN/CG B
+// columns (CTA `rank` of the pair takes the rank-th half).
+template <int KIND, int BN, int CG>
+__device__ __forceinline__ void issue_loads(const Tile& T, int kb, int rank, uint8_t* sa,
+                                            uint8_t* sb, uint32_t bar, const CUtensorMap* ma,
                                             const CUtensorMap* mb, const Params& p) {
   const int k0 = kb * BK;
-  constexpr int kChunks = BN / 64;
+  constexpr int kBChunks = BN / 64 / CG;  // 64-wide B chunks held by this CTA
   if constexpr (KIND == static_cast<int>(GemmKind::kFc1)) {
-    // gate columns [n0, n0 + BN/2) and up columns [F + n0, F + n0 + BN/2)
-    tma_load_2d(sa, ma, bar, k0, T.row0);
+    // accumulator columns [0, BN/2) = gate columns n0.., [BN/2, BN) = up columns F + n0..
+    load2<CG>(sa, ma, bar, k0, T.row0);
+    if constexpr (CG == 1) {
 #pragma unroll
-    for (int j = 0; j < kChunks / 2; ++j) {
-      tma_load_3d(sb + j * kChunkBytes, mb, bar, T.n0 + 64 * j, k0, T.e);
-      tma_load_3d(sb + (kChunks / 2 + j) * kChunkBytes, mb, bar, p.F + T.n0 + 64 * j, k0, T.e);
+      for (int j = 0; j < kBChunks / 2; ++j) {
+        load3<CG>(sb + j * kChunkBytes, mb, bar, T.n0 + 64 * j, k0, T.e);
+        load3<CG>(sb + (kBChunks / 2 + j) * kChunkBytes, mb, bar, p.F + T.n0 + 64 * j, k0, T.e);
+      }
+    } else {
+      const int base = rank == 0 ? T.n0 : p.F + T.n0;
+#pragma unroll
+      for (int j = 0; j < kBChunks; ++j)
+        load3<CG>(sb + j * kChunkBytes, mb, bar, base + 64 * j, k0, T.e);
     }
   } else if constexpr (KIND == static_cast<int>(GemmKind::kFc2)) {
-    tma_load_2d(sa, ma, bar, k0, T.row0);
+    load2<CG>(sa, ma, bar, k0, T.row0);
 #pragma unroll
-    for (int j = 0; j < kChunks; ++j)
-      tma_load_3d(sb + j * kChunkBytes, mb, bar, T.n0 + 64 * j, k0, T.e);
+    for (int j = 0; j < kBChunks; ++j)
+      load3<CG>(sb + j * kChunkBytes, mb, bar, T.n0 + (BN / CG) * rank + 64 * j, k0, T.e);
   } else if constexpr (KIND == static_cast<int>(GemmKind::kDlhsFc2) ||
                        KIND == static_cast<int>(GemmKind::kDlhsFc1)) {
-    tma_load_2d(sa, ma, bar, k0, T.row0);
-    tma_load_3d(sb, mb, bar, k0, T.n0, T.e);  // K-major B: BN rows x 64
+    load2<CG>(sa, ma, bar, k0, T.row0);
+    load3<CG>(sb, mb, bar, k0, T.n0 + (BN / CG) * rank, T.e);  // K-major B rows
   } else {
     const int kr = T.row0 + k0;
-    tma_load_2d(sa, ma, bar, T.m0, kr);
-    tma_load_2d(sa + kChunkBytes, ma, bar, T.m0 + 64, kr);
+    load2<CG>(sa, ma, bar, T.m0, kr);
+    load2<CG>(sa + kChunkBytes, ma, bar, T.m0 + 64, kr);
 #pragma unroll
-    for (int j = 0; j < kChunks; ++j) tma_load_2d(sb + j * kChunkBytes, mb, bar, T.n0 + 64 * j, kr);
+    for (int j = 0; j < kBChunks; ++j)
+      load2<CG>(sb + j * kChunkBytes, mb, bar, T.n0 + (BN / CG) * rank + 64 * j, kr);
   }
+}
+
+// Rows [valid, 64) of every 64-wide chunk of a drhs stage belong to the next
+// group (or lie past the end): zero them in A and B, then make the zeros
+// visible to the tensor core (async proxy).
+// For a pair the even CTA's MMA warp zeroes both CTAs' stages (the odd CTA's
+// through the cluster's shared window), since the odd CTA never learns when
+// its bytes have landed.
+template <int BN, int CG>
+__device__ __forceinline__ void zero_tail(uint8_t* sa, uint8_t* sb, int valid, int lane) {
+  const int nrows = BK - valid;
+  constexpr int kChunksAB = 2 + BN / 64 / CG;
+  const int nvec = kChunksAB * nrows * 8;
+  for (int i = lane; i < nvec; i += 32) {
+    const int line = i >> 3, part = i & 7;
+    const int chunk = line / nrows, j = valid + (line - chunk * nrows);
+    uint8_t* base = chunk < 2 ? sa + chunk * kChunkBytes : sb + (chunk - 2) * kChunkBytes;
+    uint8_t* addr = base + j * 128 + part * 16;
+    *reinterpret_cast<uint4*>(addr) = make_uint4(0u, 0u, 0u, 0u);
+    if constexpr (CG == 2) st_cluster_zero16(mapa_shared(smem_u32(addr), 1));
+  }
+  if constexpr (CG == 2) fence_proxy_async_cluster();
+  else fence_proxy_async_smem();
 }
 
 __device__ __forceinline__ float silu_f(float g) { return g * (1.0f / (1.0f + expf(-g))); }
 
 // ---------------------------------------------------------------- epilogue
 // Each epilogue warp owns 32 accumulator rows (its TMEM lane quarter) and a
-// ring of kRingBufs staging buffers of 32 rows x 64 bf16 (128-byte rows,
-// 128-byte swizzle).  A 64-column slice of its rows is converted, written to
-// a buffer (lane = row) and sent to global memory by one TMA bulk-tensor
-// store; the store engine writes whole lines, asynchronously.  A warp whose
-// rows straddle the end of a group (forward/dlhs only) stores its valid
-// rows with per-thread stores instead, so that no row of the next group is
-// touched.
-constexpr int kEpiWarps = 4;
-constexpr int kRingBufs = 4;
-constexpr int kBufBytes = 32 * 128;
-constexpr int kEpiBytes = kEpiWarps * kRingBufs * kBufBytes;  // 64 KB
-static_assert(kEpiBytes == kEpiBytes_, "staging size");
-
+// ring of staging buffers of 32 rows x 64 bf16 (128-byte rows, 128-byte
+// swizzle).  A 64-column slice of its rows is converted, written to a buffer
+// (lane = row) and sent to global memory by one TMA bulk-tensor store; the
+// store engine writes whole lines, asynchronously.  A warp whose rows
+// straddle the end of a group (forward/dlhs only) stores its valid rows with
+// per-thread stores instead, so that no row of the next group is touched.
+template <int RING>
 struct Ring {
   uint8_t* base;
   uint32_t next;
-};
 
-// Take `n` consecutive buffers; the stores that last read them must be done.
-template <int N>
-__device__ __forceinline__ uint8_t* ring_take(Ring& r, int lane) {
-  static_assert(N >= 1 && N <= kRingBufs, "ring");
-  if (lane == 0) bulk_wait_read<kRingBufs - N>();
-  __syncwarp();
-  uint8_t* b = r.base + (r.next % kRingBufs) * kBufBytes;
-  r.next += N;
-  return b;
-}
-__device__ __forceinline__ uint8_t* ring_buf(const Ring& r, uint8_t* first, int i) {
-  const uint32_t idx = static_cast<uint32_t>((first - r.base) / kBufBytes + i) % kRingBufs;
-  return r.base + idx * kBufBytes;
-}
+  // Take `n` consecutive buffers; the stores that last read them are done.
+  template <int N>
+  __device__ __forceinline__ uint8_t* take(int lane) {
+    static_assert(N >= 1 && N <= RING, "ring");
+    if (lane == 0) bulk_wait_read<RING - N>();
+    __syncwarp();
+    uint8_t* b = base + (next % RING) * kBufBytes;
+    next += N;
+    return b;
+  }
+  __device__ __forceinline__ uint8_t* after(uint8_t* first, int i) const {
+    const uint32_t idx = static_cast<uint32_t>((first - base) / kBufBytes + i) % RING;
+    return base + idx * kBufBytes;
+  }
+};
 
 // 16 packed bf16 pairs = 32 columns (half `h` of a 64-column row) of row `lane`.
 __device__ __forceinline__ void put_half(uint8_t* buf, int lane, int h, const uint32_t (&w)[16]) {
@@ -233,7 +291,8 @@ __device__ __forceinline__ void put_half(uint8_t* buf, int lane, int h, const ui
 
 __device__ __forceinline__ void pack16(const uint32_t (&v)[32], uint32_t (&w)[16]) {
 #pragma unroll
-  for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+  for (int i = 0; i < 16; ++i)
+    w[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
 }
 
 __device__ __forceinline__ void store_row32(__nv_bfloat16* dst, const uint32_t (&w)[16]) {
@@ -242,7 +301,12 @@ __device__ __forceinline__ void store_row32(__nv_bfloat16* dst, const uint32_t (
   for (int i = 0; i < 4; ++i) d[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
 }
 
-// Make the buffers' rows visible to the TMA engine, then store them.
+// Make the staged rows visible to the TMA engine (all lanes), then one lane
+// stores buffers.
+__device__ __forceinline__ void publish() {
+  fence_proxy_async_smem();
+  __syncwarp();
+}
 __device__ __forceinline__ void flush_2d(uint8_t* buf, const CUtensorMap* map, int x, int y, int lane) {
   if (lane == 0) {
     tma_store_2d(map, buf, x, y);
@@ -256,33 +320,30 @@ __device__ __forceinline__ void flush_3d(uint8_t* buf, const CUtensorMap* map, i
     bulk_commit();
   }
 }
-__device__ __forceinline__ void publish(int) {
-  fence_proxy_async_smem();
-  __syncwarp();
-}
 
+template <int RING>
 struct EpiCtx {
   const CUtensorMap* map_c;  // out0
   const CUtensorMap* map_d;  // out1 (z of FC1)
-  Ring ring;
-  int q;                     // lane quarter: rows [32q, 32q+32) of the tile
+  Ring<RING> ring;
+  int q;                     // lane quarter: rows [32q, 32q+32) of this CTA's tile
   int lane;
 };
 
-template <int KIND, int BN>
-__device__ __forceinline__ void epilogue_tile(const Tile& T, uint32_t tbase, EpiCtx& c,
+template <int KIND, int BN, int CG, int RING>
+__device__ __forceinline__ void epilogue_tile(const Tile& T, uint32_t tbase, EpiCtx<RING>& c,
                                               const Params& p) {
   const int lane = c.lane;
   uint32_t v[32];
   uint32_t w[16];
-  if constexpr (Traits<KIND, BN>::kGroupedK) {
+  if constexpr (Traits<KIND, BN, CG>::kGroupedK) {
     // weight gradient tile: rows m0+32q.. of expert e; rows >= M are clipped by the 3-D map
     const int y = T.m0 + 32 * c.q;
     if (y >= p.M) return;
     for (int ch = 0; ch < BN / 64; ++ch) {
       const int col = T.n0 + 64 * ch;
       if (col >= p.N) break;
-      uint8_t* buf = ring_take<1>(c.ring, lane);
+      uint8_t* buf = c.ring.template take<1>(lane);
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         tmem_ld_32x32b_x32(tbase + 64 * ch + 32 * h, v);
@@ -290,7 +351,7 @@ __device__ __forceinline__ void epilogue_tile(const Tile& T, uint32_t tbase, Epi
         pack16(v, w);
         put_half(buf, lane, h, w);
       }
-      publish(lane);
+      publish();
       flush_3d(buf, c.map_c, col, y, T.e, lane);
     }
   } else {
@@ -306,15 +367,7 @@ __device__ __forceinline__ void epilogue_tile(const Tile& T, uint32_t tbase, Epi
         const int f0 = T.n0 + 64 * ch;
         if (f0 >= p.F) break;
         uint8_t* hb = nullptr;
-        uint8_t* zb = nullptr;
-        if (full) {
-          if (with_z) {
-            hb = ring_take<3>(c.ring, lane);
-            zb = ring_buf(c.ring, hb, 1);
-          } else {
-            hb = ring_take<1>(c.ring, lane);
-          }
-        }
+        if (full) hb = with_z ? c.ring.template take<3>(lane) : c.ring.template take<1>(lane);
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           uint32_t u[32];
@@ -335,8 +388,8 @@ __device__ __forceinline__ void epilogue_tile(const Tile& T, uint32_t tbase, Epi
           if (full) {
             put_half(hb, lane, h, w);
             if (with_z) {
-              put_half(zb, lane, h, wg);
-              put_half(ring_buf(c.ring, hb, 2), lane, h, wu);
+              put_half(c.ring.after(hb, 1), lane, h, wg);
+              put_half(c.ring.after(hb, 2), lane, h, wu);
             }
           } else if (row_ok) {
             store_row32(p.out0 + r * p.F + f0 + 32 * h, w);
@@ -347,11 +400,11 @@ __device__ __forceinline__ void epilogue_tile(const Tile& T, uint32_t tbase, Epi
           }
         }
         if (full) {
-          publish(lane);
+          publish();
           flush_2d(hb, c.map_c, f0, y, lane);
           if (with_z) {
-            flush_2d(zb, c.map_d, f0, y, lane);
-            flush_2d(ring_buf(c.ring, hb, 2), c.map_d, p.F + f0, y, lane);
+            flush_2d(c.ring.after(hb, 1), c.map_d, f0, y, lane);
+            flush_2d(c.ring.after(hb, 2), c.map_d, p.F + f0, y, lane);
           }
         }
       }
@@ -361,7 +414,7 @@ __device__ __forceinline__ void epilogue_tile(const Tile& T, uint32_t tbase, Epi
         const int f0 = T.n0 + 64 * ch;
         if (f0 >= p.F) break;
         uint8_t* gb = nullptr;
-        if (full) gb = fused ? ring_take<2>(c.ring, lane) : ring_take<1>(c.ring, lane);
+        if (full) gb = fused ? c.ring.template take<2>(lane) : c.ring.template take<1>(lane);
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           const int fc = f0 + 32 * h;
@@ -403,7 +456,7 @@ __device__ __forceinline__ void epilogue_tile(const Tile& T, uint32_t tbase, Epi
             }
             if (full) {
               put_half(gb, lane, h, wg);
-              put_half(ring_buf(c.ring, gb, 1), lane, h, wu);
+              put_half(c.ring.after(gb, 1), lane, h, wu);
             } else if (row_ok) {
               store_row32(p.out0 + r * 2 * p.F + fc, wg);
               store_row32(p.out0 + r * 2 * p.F + p.F + fc, wu);
@@ -415,9 +468,9 @@ __device__ __forceinline__ void epilogue_tile(const Tile& T, uint32_t tbase, Epi
           }
         }
         if (full) {
-          publish(lane);
+          publish();
           flush_2d(gb, c.map_c, f0, y, lane);
-          if (fused) flush_2d(ring_buf(c.ring, gb, 1), c.map_c, p.F + f0, y, lane);
+          if (fused) flush_2d(c.ring.after(gb, 1), c.map_c, p.F + f0, y, lane);
         }
       }
     } else {
@@ -425,7 +478,7 @@ __device__ __forceinline__ void epilogue_tile(const Tile& T, uint32_t tbase, Epi
       for (int ch = 0; ch < BN / 64; ++ch) {
         const int col = T.n0 + 64 * ch;
         if (col >= p.N) break;
-        uint8_t* buf = full ? ring_take<1>(c.ring, lane) : nullptr;
+        uint8_t* buf = full ? c.ring.template take<1>(lane) : nullptr;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           tmem_ld_32x32b_x32(tbase + 64 * ch + 32 * h, v);
@@ -435,7 +488,7 @@ __device__ __forceinline__ void epilogue_tile(const Tile& T, uint32_t tbase, Epi
           else if (row_ok) store_row32(p.out0 + r * p.N + col + 32 * h, w);
         }
         if (full) {
-          publish(lane);
+          publish();
           flush_2d(buf, c.map_c, col, y, lane);
         }
       }
@@ -444,30 +497,33 @@ __device__ __forceinline__ void epilogue_tile(const Tile& T, uint32_t tbase, Epi
 }
 
 // An empty group's weight-gradient tile is zero.
-template <int BN>
-__device__ __forceinline__ void zero_tile(const Tile& T, EpiCtx& c, const Params& p) {
+template <int BN, int RING>
+__device__ __forceinline__ void zero_tile(const Tile& T, EpiCtx<RING>& c, const Params& p) {
   const int y = T.m0 + 32 * c.q;
   if (y >= p.M) return;
   for (int ch = 0; ch < BN / 64; ++ch) {
     const int col = T.n0 + 64 * ch;
     if (col >= p.N) break;
-    uint8_t* buf = ring_take<1>(c.ring, c.lane);
+    uint8_t* buf = c.ring.template take<1>(c.lane);
     uint4* row = reinterpret_cast<uint4*>(buf + c.lane * 128);
 #pragma unroll
     for (int j = 0; j < 8; ++j) row[j] = make_uint4(0u, 0u, 0u, 0u);
-    publish(c.lane);
+    publish();
     flush_3d(buf, c.map_c, col, y, T.e, c.lane);
   }
 }
 
-template <int KIND, int BN, int STAGES>
+// ------------------------------------------------------------------ kernel
+template <int KIND, class S>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                         const __grid_constant__ CUtensorMap map_b,
                         const __grid_constant__ CUtensorMap map_c,
                         const __grid_constant__ CUtensorMap map_d, const Params p) {
-  using S = Shape<BN, STAGES>;
-  using Tr = Traits<KIND, BN>;
+  constexpr int BN = S::BN;
+  constexpr int CG = S::CG;
+  constexpr int RING = S::kRing;
+  using Tr = Traits<KIND, BN, CG>;
   constexpr int kStages = S::kStages;
   constexpr int kStageBytes = S::kStageBytes;
   constexpr uint32_t kTmemCols = S::kTmemCols;
@@ -475,9 +531,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* ring = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
   uint8_t* epi = ring + kStages * kStageBytes;  // staging of the epilogue warps
-  SmemCtl& s = *reinterpret_cast<SmemCtl*>(epi + kEpiBytes);
+  SmemCtl& s = *reinterpret_cast<SmemCtl*>(epi + S::kEpiBytes);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const int rank = (CG == 2) ? static_cast<int>(cluster_ctarank()) : 0;
+  const bool leader = (rank == 0);
+  const int unit = blockIdx.x / CG;  // this CTA's (pair's) index in the schedule
+  const int units = gridDim.x / CG;
 
   // ---------------------------------------------------------------- set-up
   if (warp == 0 && lane == 0) {
@@ -490,17 +550,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s.tfull[i], 1);
-      mbar_init(&s.tempty[i], 4);
+      mbar_init(&s.tempty[i], kEpiWarps * CG);
     }
     s.abort_flag = 0;
     mbar_fence_init();
   }
   if (warp == 1) {
-    tmem_alloc(&s.tmem_base, kTmemCols);
-    tmem_relinquish();
+    tmem_alloc<CG>(&s.tmem_base, kTmemCols);
+    tmem_relinquish<CG>();
   }
   if (warp == 2) {
-    // group offsets and the prefix of 128-row blocks per group (warp scan)
+    // group offsets and the prefix of (128*CG)-row blocks per group (warp scan)
+    constexpr int kRowsPerBlock = BM * CG;
     const int E = p.E;
     const int per = (E + 31) / 32;
     const int e0 = min(E, lane * per), e1 = min(E, e0 + per);
@@ -508,7 +569,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int e = e0; e < e1; ++e) {
       const int a = __ldg(p.offs + e), b = __ldg(p.offs + e + 1);
       s.off[e] = a;
-      local += (b - a + BM - 1) / BM;
+      local += (b - a + kRowsPerBlock - 1) / kRowsPerBlock;
     }
     int incl = local;
 #pragma unroll
@@ -519,7 +580,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int run = incl - local;
     for (int e = e0; e < e1; ++e) {
       s.mt[e] = run;
-      run += (__ldg(p.offs + e + 1) - __ldg(p.offs + e) + BM - 1) / BM;
+      run += (__ldg(p.offs + e + 1) - __ldg(p.offs + e) + kRowsPerBlock - 1) / kRowsPerBlock;
     }
     if (lane == 31) {
       s.mt[E] = incl;
@@ -528,118 +589,122 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  if constexpr (CG == 2) cluster_sync();  // the peer's barriers exist before any remote arrive
   tc_fence_after();
   const uint32_t tmem_base = s.tmem_base;
   const WaitCtl wc{&s.abort_flag, p.status, p.limit_ns};
-  const int ntiles = total_tiles<KIND, BN>(p, s);
+  const int ntiles = total_tiles<KIND, BN, CG>(p, s);
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
+      // For a pair, both CTAs' bytes complete on the even CTA's full barrier,
+      // which the even CTA arms with the bytes of both.
       uint32_t stage = 0, phase = 0;
       uint32_t fills[kStages];
 #pragma unroll
       for (int i = 0; i < kStages; ++i) fills[i] = 0;
+      const uint32_t full0 = (CG == 2) ? mapa_shared(smem_u32(&s.full[0]), 0) : smem_u32(&s.full[0]);
       bool aborted = false;
-      for (int t = blockIdx.x; t < ntiles && !aborted; t += gridDim.x) {
-        const Tile T = decode_tile<KIND, BN>(t, p, s);
+      for (int t = unit; t < ntiles && !aborted; t += units) {
+        const Tile T = decode_tile<KIND, BN, CG>(t, rank, p, s);
         for (int kb = 0; kb < T.kb; ++kb) {
           if (!mbar_wait(&s.empty[stage], phase ^ 1u, wc)) { aborted = true; break; }
           uint8_t* sa = ring + stage * kStageBytes;
-          mbar_arrive_expect_tx(&s.full[stage], kStageBytes);
-          issue_loads<KIND, BN>(T, kb, sa, sa + kAStageBytes, &s.full[stage], &map_a, &map_b, p);
+          if (leader) mbar_arrive_expect_tx(&s.full[stage], kStageBytes * CG);
+          issue_loads<KIND, BN, CG>(T, kb, rank, sa, sa + kAStageBytes,
+                                    full0 + stage * static_cast<uint32_t>(sizeof(uint64_t)),
+                                    &map_a, &map_b, p);
           ++fills[stage];
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
       }
-      if (aborted) {  // let copies already in flight land before the CTA exits
+      if (aborted && leader) {  // let copies already in flight land before the CTA exits
         for (int i = 0; i < kStages; ++i)
           if (fills[i] > 0) (void)mbar_wait_drain(&s.full[i], (fills[i] - 1u) & 1u, 100000000ull);
       }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------- MMA
-    uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
-    uint32_t commits[kStages];
+    if (CG == 1 || leader) {
+      // ----------------------------------------------------------- MMA
+      uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+      uint32_t commits[kStages];
 #pragma unroll
-    for (int i = 0; i < kStages; ++i) commits[i] = 0;
-    int last_stage = -1;
-    bool aborted = false;
-    for (int t = blockIdx.x; t < ntiles && !aborted; t += gridDim.x) {
-      const Tile T = decode_tile<KIND, BN>(t, p, s);
-      if (T.kb == 0) continue;
-      if (!mbar_wait(&s.tempty[acc], acc_phase ^ 1u, wc)) { aborted = true; break; }
-      tc_fence_after();
-      const uint32_t d_tmem = tmem_base + acc * BN;
-      for (int kb = 0; kb < T.kb; ++kb) {
-        if (!mbar_wait(&s.full[stage], phase, wc)) { aborted = true; break; }
+      for (int i = 0; i < kStages; ++i) commits[i] = 0;
+      int last_stage = -1;
+      bool aborted = false;
+      for (int t = unit; t < ntiles && !aborted; t += units) {
+        const Tile T = decode_tile<KIND, BN, CG>(t, rank, p, s);
+        if (T.kb == 0) continue;
+        if (!mbar_wait(&s.tempty[acc], acc_phase ^ 1u, wc)) { aborted = true; break; }
         tc_fence_after();
-        uint8_t* sa = ring + stage * kStageBytes;
-        uint8_t* sb = sa + kAStageBytes;
-        if constexpr (Tr::kGroupedK) {
-          const int valid = T.klen - kb * BK;
-          if (valid < BK) {
-            // rows [valid, 64) of every 64-wide chunk belong to the next group
-            // (or lie past the end): zero them in A (2 chunks) and B (4 chunks)
-            const int nrows = BK - valid;
-            constexpr int kChunksAB = 2 + BN / 64;
-            const int nvec = kChunksAB * nrows * 8;
-            for (int i = lane; i < nvec; i += 32) {
-              const int line = i >> 3, part = i & 7;
-              const int chunk = line / nrows, j = valid + (line - chunk * nrows);
-              uint8_t* base = chunk < 2 ? sa + chunk * kChunkBytes : sb + (chunk - 2) * kChunkBytes;
-              *reinterpret_cast<uint4*>(base + j * 128 + part * 16) = make_uint4(0u, 0u, 0u, 0u);
-            }
-            fence_proxy_async_smem();
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        for (int kb = 0; kb < T.kb; ++kb) {
+          if (!mbar_wait(&s.full[stage], phase, wc)) { aborted = true; break; }
+          tc_fence_after();
+          uint8_t* sa = ring + stage * kStageBytes;
+          uint8_t* sb = sa + kAStageBytes;
+          if constexpr (Tr::kGroupedK) {
+            const int valid = T.klen - kb * BK;
+            if (valid < BK) zero_tail<BN, CG>(sa, sb, valid, lane);
           }
-        }
-        __syncwarp();
-        if (lane == 0) {
-          const uint32_t a_addr = smem_u32(sa);
-          const uint32_t b_addr = smem_u32(sb);
+          __syncwarp();
+          if (lane == 0) {
+            const uint32_t a_addr = smem_u32(sa);
+            const uint32_t b_addr = smem_u32(sb);
 #pragma unroll
-          for (int kk = 0; kk < BK / kUmmaK; ++kk) {
-            const uint64_t ad = Tr::kAMn
-                                    ? smem_desc_sw128(a_addr + kk * 2048, kChunkBytes, 1024)
-                                    : smem_desc_sw128(a_addr + kk * 32, 16, 1024);
-            const uint64_t bd = Tr::kBMn
-                                    ? smem_desc_sw128(b_addr + kk * 2048, kChunkBytes, 1024)
-                                    : smem_desc_sw128(b_addr + kk * 32, 16, 1024);
-            umma_bf16(d_tmem, ad, bd, Tr::kIdesc, (kb > 0 || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < BK / kUmmaK; ++kk) {
+              const uint64_t ad = Tr::kAMn
+                                      ? smem_desc_sw128(a_addr + kk * 2048, kChunkBytes, 1024)
+                                      : smem_desc_sw128(a_addr + kk * 32, 16, 1024);
+              const uint64_t bd = Tr::kBMn
+                                      ? smem_desc_sw128(b_addr + kk * 2048, kChunkBytes, 1024)
+                                      : smem_desc_sw128(b_addr + kk * 32, 16, 1024);
+              umma_bf16<CG>(d_tmem, ad, bd, Tr::kIdesc, (kb > 0 || kk > 0) ? 1u : 0u);
+            }
+            umma_commit<CG>(&s.empty[stage]);
           }
-          umma_commit(&s.empty[stage]);
+          __syncwarp();
+          ++commits[stage];
+          last_stage = static_cast<int>(stage);
+          if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
+        if (aborted) break;
+        if (lane == 0) umma_commit<CG>(&s.tfull[acc]);
         __syncwarp();
-        ++commits[stage];
-        last_stage = static_cast<int>(stage);
-        if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
       }
-      if (aborted) break;
-      if (lane == 0) umma_commit(&s.tfull[acc]);
-      __syncwarp();
-      if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+      if (aborted && last_stage >= 0) {  // let issued MMAs finish before TMEM is freed
+        (void)mbar_wait_drain(&s.empty[last_stage], (commits[last_stage] - 1u) & 1u,
+                              100000000ull);
+      }
     }
-    if (aborted && last_stage >= 0) {  // let issued MMAs finish before TMEM is freed
-      (void)mbar_wait_drain(&s.empty[last_stage], (commits[last_stage] - 1u) & 1u, 100000000ull);
-    }
+    // the odd CTA's MMA warp only takes part in the collective TMEM allocation
   } else {
     // -------------------------------------------------------- epilogue
     const int q = warp & 3;  // TMEM lane quarter this warp may access
-    EpiCtx ec{&map_c, &map_d, Ring{epi + (warp - 2) * kRingBufs * kBufBytes, 0u}, q, lane};
+    EpiCtx<RING> ec{&map_c, &map_d, Ring<RING>{epi + (warp - 2) * RING * kBufBytes, 0u}, q, lane};
+    uint32_t tempty_peer = 0;
+    if constexpr (CG == 2) tempty_peer = mapa_shared(smem_u32(&s.tempty[0]), 0);
     uint32_t acc = 0, acc_phase = 0;
-    for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
-      const Tile T = decode_tile<KIND, BN>(t, p, s);
+    for (int t = unit; t < ntiles; t += units) {
+      const Tile T = decode_tile<KIND, BN, CG>(t, rank, p, s);
       if (T.kb == 0) {
-        if constexpr (Tr::kGroupedK) zero_tile<BN>(T, ec, p);
+        if constexpr (Tr::kGroupedK) zero_tile<BN, RING>(T, ec, p);
         continue;
       }
       if (!mbar_wait(&s.tfull[acc], acc_phase, wc)) break;
       tc_fence_after();
-      epilogue_tile<KIND, BN>(T, tmem_base + acc * BN + (static_cast<uint32_t>(q * 32) << 16), ec,
-                              p);
+      epilogue_tile<KIND, BN, CG, RING>(
+          T, tmem_base + acc * BN + (static_cast<uint32_t>(q * 32) << 16), ec, p);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&s.tempty[acc]);
+      if (lane == 0) {
+        if (CG == 2 && !leader)
+          mbar_arrive_remote(tempty_peer + acc * static_cast<uint32_t>(sizeof(uint64_t)));
+        else
+          mbar_arrive(&s.tempty[acc]);
+      }
       if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
     }
     if (lane == 0) bulk_wait_all();  // every store has finished before the CTA exits
@@ -648,9 +713,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
+  if constexpr (CG == 2) cluster_sync();  // both CTAs are done with each other's memory
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, kTmemCols);
+    tmem_dealloc<CG>(tmem_base, kTmemCols);
   }
 }
 
@@ -681,7 +747,10 @@ bool make_map(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
   if (fn == nullptr) return false;
   cuuint64_t gd[3], gs[2];
   cuuint32_t bd[3], es[3] = {1, 1, 1};
-  for (int i = 0; i < rank; ++i) { gd[i] = dims[i]; bd[i] = box[i]; }
+  for (int i = 0; i < rank; ++i) {
+    gd[i] = dims[i];
+    bd[i] = box[i];
+  }
   for (int i = 0; i + 1 < rank; ++i) gs[i] = strides[i];
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), gd, gs, bd, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -704,26 +773,55 @@ bool map3d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t mid, uint6
   return make_map(m, base, 3, dims, strides, box);
 }
 
-template <int KIND, int BN, int STAGES>
+template <int KIND, class S>
 cudaError_t launch_kind(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mc,
-                        const CUtensorMap& md, const Params& p, int max_tiles, cudaStream_t s) {
-  auto kern = grouped_gemm_kernel<KIND, BN, STAGES>;
-  constexpr size_t bytes = smem_bytes<Shape<BN, STAGES>>();
-  static_assert(bytes <= 227 * 1024, "shared memory");
+                        const CUtensorMap& md, const Params& p, long max_units, cudaStream_t s) {
+  auto kern = grouped_gemm_kernel<KIND, S>;
+  constexpr size_t bytes = S::kSmemBytes;
   cudaError_t err =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
   if (err != cudaSuccess) return err;
-  int grid = sm_count();
-  if (max_tiles < grid) grid = max_tiles;
-  if (grid <= 0) return cudaSuccess;
-  kern<<<grid, kThreads, bytes, s>>>(ma, mb, mc, md, p);
-  return cudaGetLastError();
+  long units = sm_count() / S::CG;
+  if (max_units < units) units = max_units;
+  if (units <= 0) return cudaSuccess;
+  if constexpr (S::CG == 1) {
+    kern<<<static_cast<int>(units), kThreads, bytes, s>>>(ma, mb, mc, md, p);
+    return cudaGetLastError();
+  } else {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = bytes;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    // clusters that can be resident at once (one CTA per SM), cached per kernel
+    static int max_clusters = 0;
+    static std::once_flag once;
+    std::call_once(once, [&] {
+      cfg.gridDim = dim3(static_cast<unsigned>(2 * (sm_count() / 2)), 1, 1);
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) == cudaSuccess && n > 0) max_clusters = n;
+      else max_clusters = sm_count() / 2;
+    });
+    if (units > max_clusters) units = max_clusters;
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * units), 1, 1);
+    return cudaLaunchKernelEx(&cfg, kern, ma, mb, mc, md, p);
+  }
 }
 
-inline int cdiv(long a, long b) { return static_cast<int>((a + b - 1) / b); }
+inline long cdiv(long a, long b) { return (a + b - 1) / b; }
 
-template <int BN, int STAGES>
+// Operand/output maps and tile counts of one grouped GEMM, for CG CTAs per MMA.
+template <class S>
 cudaError_t launch_shape(const GemmCall& c, cudaStream_t s) {
+  constexpr int BN = S::BN;
+  constexpr int CG = S::CG;
+  constexpr uint32_t kBRows = BN / CG;
   const moe_dims& d = c.d;
   const long R = static_cast<long>(d.T) * d.K;
   Params p{};
@@ -737,66 +835,87 @@ cudaError_t launch_shape(const GemmCall& c, cudaStream_t s) {
   p.F = d.F;
   CUtensorMap ma, mb, mc, md;
   bool ok = false;
-  const long rows_tiles_bound = R / BM + d.E;
+  const long row_blocks_bound = R / (BM * CG) + d.E;
   const long F2 = 2L * d.F;
   switch (c.kind) {
     case GemmKind::kFc1:
-      p.Kdim = d.D;
-      p.N = d.F;
-      p.n_tiles = cdiv(d.F, BN / 2);
-      ok = map2d(&ma, c.a, d.D, R, 64, BM) && map3d(&mb, c.b, F2, d.D, d.E, 64, 64) &&
-           map2d(&mc, c.out0, d.F, R, 64, 32);
-      if (ok) ok = (c.out1 != nullptr) ? map2d(&md, c.out1, F2, R, 64, 32) : (md = mc, true);
-      if (!ok) return cudaErrorInvalidValue;
-      return launch_kind<0, BN, STAGES>(ma, mb, mc, md, p,
-                                        static_cast<int>(rows_tiles_bound * p.n_tiles), s);
+      if constexpr (S::kRing >= 3) {  // h, z gate and z up are staged together
+        p.Kdim = d.D;
+        p.N = d.F;
+        p.n_tiles = static_cast<int>(cdiv(d.F, BN / 2));
+        ok = map2d(&ma, c.a, d.D, R, 64, BM) && map3d(&mb, c.b, F2, d.D, d.E, 64, 64) &&
+             map2d(&mc, c.out0, d.F, R, 64, 32);
+        if (ok) ok = (c.out1 != nullptr) ? map2d(&md, c.out1, F2, R, 64, 32) : (md = mc, true);
+        if (!ok) return cudaErrorInvalidValue;
+        return launch_kind<0, S>(ma, mb, mc, md, p, row_blocks_bound * p.n_tiles, s);
+      }
+      return cudaErrorInvalidValue;
     case GemmKind::kFc2:
       p.Kdim = d.F;
       p.N = d.D;
-      p.n_tiles = cdiv(d.D, BN);
+      p.n_tiles = static_cast<int>(cdiv(d.D, BN));
       ok = map2d(&ma, c.a, d.F, R, 64, BM) && map3d(&mb, c.b, d.D, d.F, d.E, 64, 64) &&
            map2d(&mc, c.out0, d.D, R, 64, 32);
       if (!ok) return cudaErrorInvalidValue;
-      return launch_kind<1, BN, STAGES>(ma, mb, mc, mc, p,
-                                        static_cast<int>(rows_tiles_bound * p.n_tiles), s);
+      return launch_kind<1, S>(ma, mb, mc, mc, p, row_blocks_bound * p.n_tiles, s);
     case GemmKind::kDlhsFc2:
       p.Kdim = d.D;
       p.N = d.F;
-      p.n_tiles = cdiv(d.F, BN);
-      ok = map2d(&ma, c.a, d.D, R, 64, BM) && map3d(&mb, c.b, d.D, d.F, d.E, 64, BN) &&
+      p.n_tiles = static_cast<int>(cdiv(d.F, BN));
+      ok = map2d(&ma, c.a, d.D, R, 64, BM) && map3d(&mb, c.b, d.D, d.F, d.E, 64, kBRows) &&
            map2d(&mc, c.out0, c.aux != nullptr ? F2 : d.F, R, 64, 32);
       if (!ok) return cudaErrorInvalidValue;
-      return launch_kind<2, BN, STAGES>(ma, mb, mc, mc, p,
-                                        static_cast<int>(rows_tiles_bound * p.n_tiles), s);
+      return launch_kind<2, S>(ma, mb, mc, mc, p, row_blocks_bound * p.n_tiles, s);
     case GemmKind::kDlhsFc1:
       p.Kdim = 2 * d.F;
       p.N = d.D;
-      p.n_tiles = cdiv(d.D, BN);
-      ok = map2d(&ma, c.a, F2, R, 64, BM) && map3d(&mb, c.b, F2, d.D, d.E, 64, BN) &&
+      p.n_tiles = static_cast<int>(cdiv(d.D, BN));
+      ok = map2d(&ma, c.a, F2, R, 64, BM) && map3d(&mb, c.b, F2, d.D, d.E, 64, kBRows) &&
            map2d(&mc, c.out0, d.D, R, 64, 32);
       if (!ok) return cudaErrorInvalidValue;
-      return launch_kind<3, BN, STAGES>(ma, mb, mc, mc, p,
-                                        static_cast<int>(rows_tiles_bound * p.n_tiles), s);
+      return launch_kind<3, S>(ma, mb, mc, mc, p, row_blocks_bound * p.n_tiles, s);
     case GemmKind::kDrhsFc2:
       p.M = d.F;
       p.N = d.D;
-      p.m_tiles = cdiv(d.F, BM);
-      p.n_tiles = cdiv(d.D, BN);
+      p.m_tiles = static_cast<int>(cdiv(d.F, BM * CG));
+      p.n_tiles = static_cast<int>(cdiv(d.D, BN));
       ok = map2d(&ma, c.a, d.F, R, 64, 64) && map2d(&mb, c.b, d.D, R, 64, 64) &&
            map3d(&mc, c.out0, d.D, d.F, d.E, 64, 32);
       if (!ok) return cudaErrorInvalidValue;
-      return launch_kind<4, BN, STAGES>(ma, mb, mc, mc, p, d.E * p.m_tiles * p.n_tiles, s);
+      return launch_kind<4, S>(ma, mb, mc, mc, p, static_cast<long>(d.E) * p.m_tiles * p.n_tiles,
+                               s);
     case GemmKind::kDrhsFc1:
       p.M = d.D;
       p.N = 2 * d.F;
-      p.m_tiles = cdiv(d.D, BM);
-      p.n_tiles = cdiv(F2, BN);
+      p.m_tiles = static_cast<int>(cdiv(d.D, BM * CG));
+      p.n_tiles = static_cast<int>(cdiv(F2, BN));
       ok = map2d(&ma, c.a, d.D, R, 64, 64) && map2d(&mb, c.b, F2, R, 64, 64) &&
            map3d(&mc, c.out0, F2, d.D, d.E, 64, 32);
       if (!ok) return cudaErrorInvalidValue;
-      return launch_kind<5, BN, STAGES>(ma, mb, mc, mc, p, d.E * p.m_tiles * p.n_tiles, s);
+      return launch_kind<5, S>(ma, mb, mc, mc, p, static_cast<long>(d.E) * p.m_tiles * p.n_tiles,
+                               s);
   }
   return cudaErrorInvalidValue;
+}
+
+// Single-CTA shape: 3 stages of 48 KB and 4 staging buffers per warp.
+using Shape1 = Shape<256, 3, 1, 4>;
+// CTA-pair shapes: stages of 32 KB per CTA.  FC1 stages three buffers at once
+// (h, z gate, z up); the others need at most two.
+using Shape2Fc1 = Shape<256, 4, 2, 4>;
+using Shape2 = Shape<256, 5, 2, 2>;
+
+// Whether a grouped GEMM runs on CTA pairs.  The pair's 256-row block is the
+// unit of rows for the forward and dlhs GEMMs, so pairs pay off when groups
+// are long; drhs tiles are over output rows (F or D), where the pair loses
+// nothing.  MOE_GEMM_PAIR=0/1 forces the choice.
+bool use_pairs(const GemmCall& c) {
+  const char* env = std::getenv("MOE_GEMM_PAIR");
+  if (env != nullptr && env[0] == '0') return false;
+  if (env != nullptr && env[0] == '1') return true;
+  if (c.kind == GemmKind::kDrhsFc2 || c.kind == GemmKind::kDrhsFc1) return true;
+  const long R = static_cast<long>(c.d.T) * c.d.K;
+  return R / c.d.E >= 1024;
 }
 
 }  // namespace
@@ -812,11 +931,9 @@ cudaError_t launch_grouped_gemm(const GemmCall& c, cudaStream_t s) {
       return cudaMemsetAsync(c.out0, 0, static_cast<size_t>(d.E) * d.D * 2 * d.F * 2, s);
     return cudaSuccess;
   }
-#ifndef MOE_GEMM_BN
-#define MOE_GEMM_BN 256
-#define MOE_GEMM_STAGES 3
-#endif
-  return launch_shape<MOE_GEMM_BN, MOE_GEMM_STAGES>(c, s);
+  if (!use_pairs(c)) return launch_shape<Shape1>(c, s);
+  if (c.kind == GemmKind::kFc1) return launch_shape<Shape2Fc1>(c, s);
+  return launch_shape<Shape2>(c, s);
 }
 
 }  // namespace moe

@@ -36,6 +36,18 @@ def _gpu():
     need_gpu()
 
 
+# The grouped GEMMs run either one CTA per tile or on CTA pairs (a 2-CTA
+# cluster sharing one 256-row tile); MOE_GEMM_PAIR forces the path so that
+# both are checked on every shape.
+PAIR_MODES = pytest.mark.parametrize("pair", ["0", "1"], ids=["cta1", "cta2"])
+
+
+@pytest.fixture
+def pair_env(monkeypatch, pair):
+    monkeypatch.setenv("MOE_GEMM_PAIR", pair)
+    return pair
+
+
 def _numpy_inputs(wl):
     inp = make_inputs(wl, "cpu", with_grad=True)
     return oracle.to_numpy(inp)
@@ -117,7 +129,8 @@ def test_permute_and_combine_exact(case):
     assert_close("dw", to_host(dw), bwd["dw"], bf16=False)
 
 
-def test_fc1_swiglu(case):
+@PAIR_MODES
+def test_fc1_swiglu(case, pair_env):
     wl, inp, fwd, _ = case
     d = _dims(wl)
     R = wl.T * wl.K
@@ -135,7 +148,8 @@ def test_fc1_swiglu(case):
     assert_exact("h (no z)", to_host(h2), to_host(h))
 
 
-def test_fc2(case):
+@PAIR_MODES
+def test_fc2(case, pair_env):
     wl, inp, fwd, _ = case
     d = _dims(wl)
     R = wl.T * wl.K
@@ -148,7 +162,8 @@ def test_fc2(case):
     assert_close("ys", to_host(ys), fwd["ys"])
 
 
-def test_fc2_bwd(case):
+@PAIR_MODES
+def test_fc2_bwd(case, pair_env):
     wl, inp, fwd, bwd = case
     d = _dims(wl)
     R, F = wl.T * wl.K, wl.F
@@ -169,7 +184,8 @@ def test_fc2_bwd(case):
     assert_close("dh", to_host(dh), dh_ref)
 
 
-def test_fc1_bwd(case):
+@PAIR_MODES
+def test_fc1_bwd(case, pair_env):
     wl, inp, fwd, bwd = case
     d = _dims(wl)
     R, F = wl.T * wl.K, wl.F
@@ -197,7 +213,8 @@ def test_fc1_bwd(case):
     assert_close("dwi (unfused)", to_host(dwi2), dwi_ref)
 
 
-def test_block_end_to_end(case):
+@PAIR_MODES
+def test_block_end_to_end(case, pair_env):
     from mixture_experts_ffn_histogram_gb300.block import MoEBlock
     wl, inp, fwd, bwd = case
     blk = MoEBlock(wl.T, wl.D, wl.E, wl.K, wl.F, wl.score_mode, train=True)
@@ -223,9 +240,10 @@ def _given_block(T, D, E, K, F, ids, w, seed=0):
     return wl, inp
 
 
+@PAIR_MODES
 @pytest.mark.parametrize("kind", ["empty_experts", "one_expert_all", "groups_of_one", "k1", "k_eq_e",
                                   "t1", "e1"])
-def test_edge_cases(kind):
+def test_edge_cases(kind, pair_env):
     rng = np.random.Generator(np.random.PCG64(5))
     if kind == "empty_experts":      # only experts 1, 4, 5 are used
         T, D, E, K, F = 200, 128, 8, 2, 128
