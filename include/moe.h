@@ -131,6 +131,32 @@ moe_status moe_route_histogram(const float* logits, const float* bias, moe_score
                                int32_t* dev_status, void* ws, moe_dims d, cudaStream_t stream);
 
 /*
+ * moe_route_histogram without a workspace argument.  The pages have no
+ * counterpart: this exists for callers that cannot allocate device memory,
+ * such as code running inside another framework's operator or plugin that
+ * is handed only the buffers its planner sized, or latency-critical code
+ * that must not call cudaMalloc (it can synchronise the device).  It
+ * computes exactly what moe_route_histogram computes, from the same
+ * arguments minus `ws`, and allocates nothing: its scratch (the per-chunk
+ * expert counts and their prefixes) is a fixed array of 262144 int32
+ * (1 MiB) inside the library, held by every GPU that loads the library
+ * until the process exits.
+ *   Limit: 2 * ceil(T/256) * E <= 262144 (e.g. T = 32768 with E <= 1024);
+ *   larger dims return MOE_ERR_UNSUPPORTED without launching anything.
+ *   The first call on a device looks up the array's device address
+ *   (cudaGetSymbolAddress) with that device current; make that first call
+ *   before any stream capture.
+ *   All calls share the one array: each call clears the counts it uses and
+ *   rewrites the prefixes it reads, so earlier calls leave nothing behind,
+ *   but calls that overlap on the GPU (different streams, or several host
+ *   threads) race on it and must be ordered by the caller.
+ */
+moe_status moe_route_histogram_noalloc(const float* logits, const float* bias, moe_score_mode mode,
+                                       int32_t* ids, float* w, int32_t* group_sizes,
+                                       int32_t* group_offsets, int32_t* pos, int32_t* row_src,
+                                       int32_t* dev_status, moe_dims d, cudaStream_t stream);
+
+/*
  * Permute [Fused p/c Context item 1, row 2]: xs[pos[t,k]] = x[t] for every
  * slot with pos >= 0 (an exact copy; each x row is read once and written K
  * times; no unsorted [R, D] copy exists).

@@ -30,8 +30,11 @@ ENTRY_POINTS = (
     "moe_workspace_bytes", "moe_status_string", "moe_abi_version", "moe_route_histogram",
     "moe_permute", "moe_permute_bwd", "moe_grouped_gemm_fc1_swiglu",
     "moe_grouped_gemm_fc1_swiglu_bwd", "moe_grouped_gemm_fc2", "moe_grouped_gemm_fc2_bwd",
-    "moe_combine", "moe_combine_bwd", "moe_selftest_bounded_wait",
+    "moe_combine", "moe_combine_bwd", "moe_selftest_bounded_wait", "moe_route_histogram_noalloc",
 )
+
+# int32 capacity of the fixed scratch behind moe_route_histogram_noalloc
+NOALLOC_ROUTE_SCRATCH_INTS = 262144
 
 
 class MoeDims(ctypes.Structure):
@@ -43,8 +46,8 @@ class MoeDims(ctypes.Structure):
 
 
 class MoeError(RuntimeError):
-    def __init__(self, fn: str, status: int):
-        super().__init__(f"{fn}: {status_string(status)} (status {status})")
+    def __init__(self, fn: str, status: int, detail: str | None = None):
+        super().__init__(f"{fn}: {detail or status_string(status)} (status {status})")
         self.status = status
 
 
@@ -87,6 +90,7 @@ def lib() -> ctypes.CDLL:
             "moe_combine": ([P, P, P, P, D_, P], I),
             "moe_combine_bwd": ([P, P, P, P, P, P, D_, P], I),
             "moe_selftest_bounded_wait": ([P, ctypes.c_uint64, P], I),
+            "moe_route_histogram_noalloc": ([P, P, I, P, P, P, P, P, P, P, D_, P], I),
         }
         for name, (args, res) in sig.items():
             fn = getattr(L, name)
@@ -136,6 +140,23 @@ def moe_route_histogram(logits, bias, mode, ids, w, group_sizes, group_offsets, 
     _ok("moe_route_histogram", lib().moe_route_histogram(
         _p(logits), _p(bias), int(mode), _p(ids), _p(w), _p(group_sizes), _p(group_offsets),
         _p(pos), _p(row_src), _p(dev_status), _p(ws), d, _s(stream)))
+
+
+def moe_route_histogram_noalloc(logits, bias, mode, ids, w, group_sizes, group_offsets, pos,
+                                row_src, dev_status, d: MoeDims, stream=None):
+    """moe_route_histogram with no workspace: for callers that cannot allocate
+    device memory.  Its scratch is a fixed 1 MiB array inside the library,
+    shared by every call (calls that overlap on the GPU race on it)."""
+    st = lib().moe_route_histogram_noalloc(
+        _p(logits), _p(bias), int(mode), _p(ids), _p(w), _p(group_sizes), _p(group_offsets),
+        _p(pos), _p(row_src), _p(dev_status), d, _s(stream))
+    if st == MOE_ERR_UNSUPPORTED:
+        need = 2 * ((d.T + 255) // 256) * d.E
+        if need > NOALLOC_ROUTE_SCRATCH_INTS:
+            raise MoeError("moe_route_histogram_noalloc", st,
+                           f"needs {need} int32 of fixed scratch (2*ceil(T/256)*E) but the "
+                           f"library holds {NOALLOC_ROUTE_SCRATCH_INTS}")
+    _ok("moe_route_histogram_noalloc", st)
 
 
 def moe_permute(x, pos, xs, d: MoeDims, stream=None):

@@ -118,6 +118,35 @@ moe_status moe_route_histogram(const float* logits, const float* bias, moe_score
                                                dev_status, counts, chunk_excl, d, stream));
 }
 
+moe_status moe_route_histogram_noalloc(const float* logits, const float* bias, moe_score_mode mode,
+                                       int32_t* ids, float* w, int32_t* group_sizes,
+                                       int32_t* group_offsets, int32_t* pos, int32_t* row_src,
+                                       int32_t* dev_status, moe_dims d, cudaStream_t stream) {
+  MOE_CHECK_DIMS(d);
+  if (mode != MOE_SCORE_SOFTMAX_TOPK && mode != MOE_SCORE_SIGMOID_NORM && mode != MOE_SCORE_GIVEN)
+    return MOE_ERR_INVALID_ARG;
+  MOE_REQUIRE(group_sizes);
+  MOE_REQUIRE(group_offsets);
+  MOE_OPTIONAL(dev_status);
+  MOE_OPTIONAL(bias);
+  if (d.T > 0) {
+    MOE_REQUIRE(ids);
+    MOE_REQUIRE(pos);
+    MOE_REQUIRE(row_src);
+    if (mode != MOE_SCORE_GIVEN) {
+      MOE_REQUIRE(logits);
+      MOE_REQUIRE(w);
+    } else {
+      MOE_OPTIONAL(w);
+    }
+  }
+  const size_t need = 2u * static_cast<size_t>(moe::route_chunks(d.T)) * static_cast<size_t>(d.E);
+  if (need > moe::kRouteStaticScratchInts) return MOE_ERR_UNSUPPORTED;
+  return from_cuda(moe::launch_route_histogram_static(logits, bias, static_cast<int>(mode), ids, w,
+                                                      group_sizes, group_offsets, pos, row_src,
+                                                      dev_status, d, stream));
+}
+
 moe_status moe_permute(const moe_bf16* x, const int32_t* pos, moe_bf16* xs, moe_dims d,
                        cudaStream_t stream) {
   MOE_CHECK_DIMS(d);

@@ -26,6 +26,14 @@ cudaError_t launch_route_histogram(const float* logits, const float* bias, int m
                                    int32_t* counts, int32_t* chunk_excl, const moe_dims& d,
                                    cudaStream_t s);
 
+// Capacity, in int32, of the fixed scratch of the no-allocation routing
+// call: 2 * ceil(T/256) * E must not exceed it.
+constexpr size_t kRouteStaticScratchInts = 262144;  // 1 MiB
+cudaError_t launch_route_histogram_static(const float* logits, const float* bias, int mode,
+                                          int32_t* ids, float* w, int32_t* group_sizes,
+                                          int32_t* group_offsets, int32_t* pos, int32_t* row_src,
+                                          int32_t* dev_status, const moe_dims& d, cudaStream_t s);
+
 cudaError_t launch_permute(const uint16_t* x, const int32_t* pos, uint16_t* xs, const moe_dims& d,
                            cudaStream_t s);
 cudaError_t launch_combine(const uint16_t* ys, const float* w, const int32_t* pos, uint16_t* out,

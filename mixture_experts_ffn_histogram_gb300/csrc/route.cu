@@ -20,6 +20,7 @@
 //      prefix + rank, i.e. the stable order in the flat slot index t*K+k.
 #include <cfloat>
 #include <climits>
+#include <mutex>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -251,6 +252,11 @@ cudaError_t launch_topk(const float* logits, const float* bias, int mode, int32_
   return cudaGetLastError();
 }
 
+// Scratch of moe_route_histogram_noalloc: the per-chunk expert counts and
+// their prefixes live in this fixed array instead of a caller workspace.
+// Every GPU that loads the library holds it (1 MiB) until the process exits.
+static __device__ __align__(256) int32_t g_route_scratch[kRouteStaticScratchInts];
+
 }  // namespace
 
 cudaError_t launch_route_histogram(const float* logits, const float* bias, int mode, int32_t* ids,
@@ -281,6 +287,38 @@ cudaError_t launch_route_histogram(const float* logits, const float* bias, int m
     err = cudaGetLastError();
   }
   return err;
+}
+
+// The same three kernels with their scratch in g_route_scratch.  The host
+// only knows a stand-in for the array's name; its device address is looked
+// up once per device (with that device current) on the first call.
+cudaError_t launch_route_histogram_static(const float* logits, const float* bias, int mode,
+                                          int32_t* ids, float* w, int32_t* group_sizes,
+                                          int32_t* group_offsets, int32_t* pos, int32_t* row_src,
+                                          int32_t* dev_status, const moe_dims& d,
+                                          cudaStream_t s) {
+  static std::mutex mu;
+  static int32_t* scratch_of_device[64] = {};
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  int32_t* ptr = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (scratch_of_device[dev] == nullptr) {
+      err = cudaGetSymbolAddress((void**)&ptr, g_route_scratch);
+      if (err != cudaSuccess) return err;
+      scratch_of_device[dev] = ptr;
+    }
+    ptr = scratch_of_device[dev];
+  }
+  const size_t per = static_cast<size_t>(route_chunks(d.T)) * static_cast<size_t>(d.E);
+  if (2 * per > kRouteStaticScratchInts) return cudaErrorInvalidValue;
+  // launch_route_histogram clears the counts it uses before counting, and
+  // rewrites every prefix it reads, so nothing left by an earlier call leaks.
+  return launch_route_histogram(logits, bias, mode, ids, w, group_sizes, group_offsets, pos,
+                                row_src, dev_status, ptr, ptr + per, d, s);
 }
 
 }  // namespace moe
