@@ -68,6 +68,7 @@ struct SmemCtl {
   uint64_t empty[kMaxStages];
   uint64_t tfull[2];
   uint64_t tempty[2];
+  uint64_t zbar[kEpiWarps];  // z rows landed in an epilogue warp's buffers
   uint32_t tmem_base;
   int abort_flag;
   int off[kMaxExperts + 1];  // group offsets
@@ -75,20 +76,24 @@ struct SmemCtl {
 };
 
 // Tile shape: 128 x BN accumulator per CTA, CG CTAs per MMA, a `STAGES`-deep
-// operand ring and RING staging buffers per epilogue warp.
-template <int BN_, int STAGES_, int CG_, int RING_>
+// operand ring, RING staging buffers per epilogue warp, and (ZB) two more
+// buffers per epilogue warp into which TMA loads the z rows that the fused
+// SwiGLU backward reads.
+template <int BN_, int STAGES_, int CG_, int RING_, int ZB_ = 0>
 struct Shape {
   static constexpr int BN = BN_;
   static constexpr int kStages = STAGES_;
   static constexpr int CG = CG_;
   static constexpr int kRing = RING_;
+  static constexpr bool kZB = ZB_ != 0;
+  static constexpr int kZBytes = kZB ? kEpiWarps * 2 * kBufBytes : 0;
   static constexpr int kBRows = BN / CG;  // B columns held by one CTA
   static constexpr int kBStageBytes = kBRows * BK * 2;
   static constexpr int kStageBytes = kAStageBytes + kBStageBytes;
   static constexpr int kTmemCols = 2 * BN;  // two accumulators
   static constexpr int kEpiBytes = kEpiWarps * RING_ * kBufBytes;
   static constexpr size_t kSmemBytes =
-      1024 + static_cast<size_t>(STAGES_) * kStageBytes + kEpiBytes + sizeof(SmemCtl);
+      1024 + static_cast<size_t>(STAGES_) * kStageBytes + kEpiBytes + kZBytes + sizeof(SmemCtl);
   static_assert(BN == 256, "tile width");
   static_assert(CG == 1 || CG == 2, "CTA group");
   static_assert(STAGES_ >= 2 && STAGES_ <= kMaxStages, "stages");
@@ -247,7 +252,11 @@ __device__ __forceinline__ void zero_tail(uint8_t* sa, uint8_t* sb, int valid, i
   else fence_proxy_async_smem();
 }
 
-__device__ __forceinline__ float silu_f(float g) { return g * (1.0f / (1.0f + expf(-g))); }
+// silu(g) = g * sigmoid(g) and sigmoid(g) in the epilogues, with the
+// hardware exponential and approximate division (relative error ~1e-6;
+// for large |g| they reach the exact limits 0 and g).
+__device__ __forceinline__ float sigmoid_fast(float g) { return __fdividef(1.0f, 1.0f + __expf(-g)); }
+__device__ __forceinline__ float silu_f(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
 
 // ---------------------------------------------------------------- epilogue
 // Each epilogue warp owns 32 accumulator rows (its TMEM lane quarter) and a
@@ -324,13 +333,37 @@ __device__ __forceinline__ void flush_3d(uint8_t* buf, const CUtensorMap* map, i
 template <int RING>
 struct EpiCtx {
   const CUtensorMap* map_c;  // out0
-  const CUtensorMap* map_d;  // out1 (z of FC1)
+  const CUtensorMap* map_d;  // out1 (z of FC1), or z (input of the fused SwiGLU backward)
   Ring<RING> ring;
   int q;                     // lane quarter: rows [32q, 32q+32) of this CTA's tile
   int lane;
+  uint8_t* zbuf;             // gate and up z rows of one 64-column chunk (TMA-loaded)
+  uint64_t* zbar;
+  uint32_t zphase;
+  const WaitCtl* wc;
 };
 
-template <int KIND, int BN, int CG, int RING>
+// Whether this warp's z rows come by TMA: the fused SwiGLU backward, a shape
+// with z buffers, and all 32 of the warp's rows inside the group.
+template <int KIND, bool ZB, int RING>
+__device__ __forceinline__ bool z_by_tma(const Tile& T, const EpiCtx<RING>& c, const Params& p) {
+  return KIND == static_cast<int>(GemmKind::kDlhsFc2) && ZB && p.aux != nullptr &&
+         T.rows - 32 * c.q >= 32;
+}
+// Request the gate and up z rows of 64-column chunk `ch` of tile T.
+template <int RING>
+__device__ __forceinline__ void z_request(const Tile& T, int ch, EpiCtx<RING>& c, const Params& p) {
+  if (c.lane == 0) {
+    const int f0 = T.n0 + 64 * ch;
+    const int y = T.row0 + 32 * c.q;
+    const uint32_t bar = smem_u32(c.zbar);
+    mbar_arrive_expect_tx(c.zbar, 2 * kBufBytes);
+    tma_load_2d_addr(c.zbuf, c.map_d, bar, f0, y);
+    tma_load_2d_addr(c.zbuf + kBufBytes, c.map_d, bar, p.F + f0, y);
+  }
+}
+
+template <int KIND, int BN, int CG, int RING, bool ZB>
 __device__ __forceinline__ void epilogue_tile(const Tile& T, uint32_t tbase, EpiCtx<RING>& c,
                                               const Params& p) {
   const int lane = c.lane;
@@ -410,6 +443,59 @@ __device__ __forceinline__ void epilogue_tile(const Tile& T, uint32_t tbase, Epi
       }
     } else if constexpr (KIND == static_cast<int>(GemmKind::kDlhsFc2)) {
       const bool fused = p.aux != nullptr;
+      if (z_by_tma<KIND, ZB, RING>(T, c, p)) {
+        // z rows arrive by TMA; chunk 0 was requested before the accumulator wait
+        for (int ch = 0; ch < BN / 64; ++ch) {
+          const int f0 = T.n0 + 64 * ch;
+          if (f0 >= p.F) break;
+          if (!mbar_wait(c.zbar, c.zphase, *c.wc)) return;
+          c.zphase ^= 1u;
+          uint4 zg[8], zu[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int off = lane * 128 + ((j ^ (lane & 7)) << 4);
+            zg[j] = *reinterpret_cast<const uint4*>(c.zbuf + off);
+            zu[j] = *reinterpret_cast<const uint4*>(c.zbuf + kBufBytes + off);
+          }
+          fence_proxy_async_smem();  // the reads are done before TMA refills the buffers
+          __syncwarp();
+          if (ch + 1 < BN / 64 && f0 + 64 < p.F) z_request(T, ch + 1, c, p);
+          uint8_t* gb = c.ring.template take<2>(lane);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            tmem_ld_32x32b_x32(tbase + 64 * ch + 32 * h, v);
+            tmem_ld_wait();
+            uint32_t wg[16], wu[16];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const uint4 gv = zg[4 * h + i], uv = zu[4 * h + i];
+              const uint32_t gq[4] = {gv.x, gv.y, gv.z, gv.w};
+              const uint32_t uq[4] = {uv.x, uv.y, uv.z, uv.w};
+#pragma unroll
+              for (int qq = 0; qq < 4; ++qq) {
+                float rg[2], ru[2];
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                  const float dh = __uint_as_float(v[8 * i + 2 * qq + hh]);
+                  const float g = hh ? bf16hi(gq[qq]) : bf16lo(gq[qq]);
+                  const float u = hh ? bf16hi(uq[qq]) : bf16lo(uq[qq]);
+                  const float sg = sigmoid_fast(g);
+                  rg[hh] = dh * u * sg * (1.0f + g * (1.0f - sg));
+                  ru[hh] = dh * g * sg;
+                }
+                wg[4 * i + qq] = pack_bf16x2(rg[0], rg[1]);
+                wu[4 * i + qq] = pack_bf16x2(ru[0], ru[1]);
+              }
+            }
+            put_half(gb, lane, h, wg);
+            put_half(c.ring.after(gb, 1), lane, h, wu);
+          }
+          publish();
+          flush_2d(gb, c.map_c, f0, y, lane);
+          flush_2d(c.ring.after(gb, 1), c.map_c, p.F + f0, y, lane);
+        }
+        return;
+      }
       for (int ch = 0; ch < BN / 64; ++ch) {
         const int f0 = T.n0 + 64 * ch;
         if (f0 >= p.F) break;
@@ -445,7 +531,7 @@ __device__ __forceinline__ void epilogue_tile(const Tile& T, uint32_t tbase, Epi
                     const float dh = __uint_as_float(v[8 * i + 2 * qq + hh]);
                     const float g = hh ? bf16hi(gq[qq]) : bf16lo(gq[qq]);
                     const float u = hh ? bf16hi(uq[qq]) : bf16lo(uq[qq]);
-                    const float sg = 1.0f / (1.0f + expf(-g));
+                    const float sg = sigmoid_fast(g);
                     rg[hh] = dh * u * sg * (1.0f + g * (1.0f - sg));
                     ru[hh] = dh * g * sg;
                   }
@@ -531,7 +617,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* ring = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
   uint8_t* epi = ring + kStages * kStageBytes;  // staging of the epilogue warps
-  SmemCtl& s = *reinterpret_cast<SmemCtl*>(epi + S::kEpiBytes);
+  uint8_t* zarea = epi + S::kEpiBytes;           // z rows of the fused SwiGLU backward
+  SmemCtl& s = *reinterpret_cast<SmemCtl*>(zarea + S::kZBytes);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int rank = (CG == 2) ? static_cast<int>(cluster_ctarank()) : 0;
@@ -552,6 +639,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&s.tfull[i], 1);
       mbar_init(&s.tempty[i], kEpiWarps * CG);
     }
+    for (int i = 0; i < kEpiWarps; ++i) mbar_init(&s.zbar[i], 1);
     s.abort_flag = 0;
     mbar_fence_init();
   }
@@ -683,7 +771,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // -------------------------------------------------------- epilogue
     const int q = warp & 3;  // TMEM lane quarter this warp may access
-    EpiCtx<RING> ec{&map_c, &map_d, Ring<RING>{epi + (warp - 2) * RING * kBufBytes, 0u}, q, lane};
+    EpiCtx<RING> ec{&map_c, &map_d, Ring<RING>{epi + (warp - 2) * RING * kBufBytes, 0u}, q, lane,
+                    zarea + (warp - 2) * 2 * kBufBytes, &s.zbar[warp - 2], 0u, &wc};
     uint32_t tempty_peer = 0;
     if constexpr (CG == 2) tempty_peer = mapa_shared(smem_u32(&s.tempty[0]), 0);
     uint32_t acc = 0, acc_phase = 0;
@@ -693,9 +782,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if constexpr (Tr::kGroupedK) zero_tile<BN, RING>(T, ec, p);
         continue;
       }
+      if (z_by_tma<KIND, S::kZB, RING>(T, ec, p)) z_request(T, 0, ec, p);
       if (!mbar_wait(&s.tfull[acc], acc_phase, wc)) break;
       tc_fence_after();
-      epilogue_tile<KIND, BN, CG, RING>(
+      epilogue_tile<KIND, BN, CG, RING, S::kZB>(
           T, tmem_base + acc * BN + (static_cast<uint32_t>(q * 32) << 16), ec, p);
       tc_fence_before();
       __syncwarp();
@@ -864,8 +954,9 @@ cudaError_t launch_shape(const GemmCall& c, cudaStream_t s) {
       p.n_tiles = static_cast<int>(cdiv(d.F, BN));
       ok = map2d(&ma, c.a, d.D, R, 64, BM) && map3d(&mb, c.b, d.D, d.F, d.E, 64, kBRows) &&
            map2d(&mc, c.out0, c.aux != nullptr ? F2 : d.F, R, 64, 32);
+      if (ok) ok = (c.aux != nullptr) ? map2d(&md, c.aux, F2, R, 64, 32) : (md = mc, true);
       if (!ok) return cudaErrorInvalidValue;
-      return launch_kind<2, S>(ma, mb, mc, mc, p, row_blocks_bound * p.n_tiles, s);
+      return launch_kind<2, S>(ma, mb, mc, md, p, row_blocks_bound * p.n_tiles, s);
     case GemmKind::kDlhsFc1:
       p.Kdim = 2 * d.F;
       p.N = d.D;
@@ -904,6 +995,9 @@ using Shape1 = Shape<256, 3, 1, 4>;
 // (h, z gate, z up); the others need at most two.
 using Shape2Fc1 = Shape<256, 4, 2, 4>;
 using Shape2 = Shape<256, 5, 2, 2>;
+// The FC2 dlhs with the fused SwiGLU backward also stages z rows.
+using Shape1Dz = Shape<256, 3, 1, 2, 1>;
+using Shape2Dz = Shape<256, 4, 2, 2, 1>;
 
 // Whether a grouped GEMM runs on CTA pairs.  The pair's 256-row block is the
 // unit of rows for the forward and dlhs GEMMs, so pairs pay off when groups
@@ -931,9 +1025,10 @@ cudaError_t launch_grouped_gemm(const GemmCall& c, cudaStream_t s) {
       return cudaMemsetAsync(c.out0, 0, static_cast<size_t>(d.E) * d.D * 2 * d.F * 2, s);
     return cudaSuccess;
   }
-  if (!use_pairs(c)) return launch_shape<Shape1>(c, s);
+  const bool dz = (c.kind == GemmKind::kDlhsFc2 && c.aux != nullptr);
+  if (!use_pairs(c)) return dz ? launch_shape<Shape1Dz>(c, s) : launch_shape<Shape1>(c, s);
   if (c.kind == GemmKind::kFc1) return launch_shape<Shape2Fc1>(c, s);
-  return launch_shape<Shape2>(c, s);
+  return dz ? launch_shape<Shape2Dz>(c, s) : launch_shape<Shape2>(c, s);
 }
 
 }  // namespace moe

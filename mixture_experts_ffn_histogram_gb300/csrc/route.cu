@@ -8,10 +8,11 @@
 //
 // Three kernels, all deterministic (no atomic decides an order; atomics only
 // add up counts):
-//   1. route_topk: one warp per token (grid-stride over all tokens) selects
-//      the top-K scores by K rounds of a warp-wide (score desc, id asc)
-//      arg-max, computes the routing weights, and adds each slot to the
-//      count of its (chunk of 256 tokens, expert) pair in global memory.
+//   1. route_topk: one group of G lanes per token (32/G tokens per warp,
+//      grid-stride over all tokens) selects the top-K scores by K rounds of
+//      a group-wide (score desc, id asc) arg-max, computes the routing
+//      weights, and adds each slot to the count of its (chunk of 256
+//      tokens, expert) pair in global memory.
 //   2. route_scan: per expert, the exclusive prefix of the counts over
 //      chunks, group_sizes, and the exclusive prefix over experts
 //      (group_offsets); threads are indexed by expert so reads coalesce.
@@ -35,11 +36,16 @@ __device__ __forceinline__ bool better(float v1, int e1, float v2, int e2) {
   return v1 > v2 || (v1 == v2 && e1 < e2);
 }
 
-template <int EPL>  // expert scores held per lane: E <= 32 * EPL
+// One group of G lanes per token (G a power of two, G >= K, G * VPL >= E):
+// a warp selects the top-K of 32/G tokens at once.  Lane i of a group holds
+// the scores of experts i, i+G, i+2G, ...; each of the K rounds takes the
+// group-wide (score desc, id asc) arg-max over the experts not yet taken, so
+// slot k is the k-th largest score.
+template <int VPL>
 __global__ void __launch_bounds__(kRouteThreads) route_topk(
     const float* __restrict__ logits, const float* __restrict__ bias, int mode,
     int32_t* __restrict__ ids, float* __restrict__ w, int32_t* __restrict__ counts, int T, int E,
-    int K, int32_t* status) {
+    int K, int G, int32_t* status) {
   const int lane = threadIdx.x & 31;
   if (mode == MOE_SCORE_GIVEN) {
     const long R = static_cast<long>(T) * K;
@@ -52,14 +58,23 @@ __global__ void __launch_bounds__(kRouteThreads) route_topk(
     }
     return;
   }
-  const int warps_total = gridDim.x * kRouteWarps;
-  for (int t = blockIdx.x * kRouteWarps + (threadIdx.x >> 5); t < T; t += warps_total) {
-    float s[EPL];
-    const float* row = logits + static_cast<long>(t) * E;
+  const int gl = lane & (G - 1);   // lane within the group
+  const int gbase = lane - gl;     // first lane of the group
+  const int groups_per_warp = 32 / G;
+  const long groups_total = static_cast<long>(gridDim.x) * kRouteWarps * groups_per_warp;
+  const long first = (static_cast<long>(blockIdx.x) * kRouteWarps + (threadIdx.x >> 5)) *
+                         groups_per_warp + (lane / G);
+  // every lane of a warp runs the same number of iterations (shuffles stay converged)
+  const long warp_first = first - lane / G;
+  for (long base = warp_first; base < T; base += groups_total) {
+    const long t = base + lane / G;
+    const bool live = t < T;
+    float s[VPL];
+    const float* row = logits + t * E;
 #pragma unroll
-    for (int i = 0; i < EPL; ++i) {
-      const int e = lane + 32 * i;
-      if (e < E) {
+    for (int i = 0; i < VPL; ++i) {
+      const int e = gl + G * i;
+      if (live && e < E) {
         float v = __ldg(row + e);
         if (bias != nullptr) v = __fadd_rn(v, __ldg(bias + e));
         s[i] = v;
@@ -74,34 +89,33 @@ __global__ void __launch_bounds__(kRouteThreads) route_topk(
       float bv = -FLT_MAX;
       int be = INT_MAX;  // "no candidate" loses to every real expert
 #pragma unroll
-      for (int i = 0; i < EPL; ++i) {
-        const int e = lane + 32 * i;
+      for (int i = 0; i < VPL; ++i) {
+        const int e = gl + G * i;
         if (e < E && !((taken >> i) & 1u) && better(s[i], e, bv, be)) { bv = s[i]; be = e; }
       }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {
+      for (int off = G >> 1; off > 0; off >>= 1) {
         const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
         const int oe = __shfl_xor_sync(0xffffffffu, be, off);
         if (better(ov, oe, bv, be)) { bv = ov; be = oe; }
       }
-      if ((be & 31) == lane) taken |= 1u << (be >> 5);
-      if (lane == k) { my_v = bv; my_e = be; }
+      if (be != INT_MAX && (be & (G - 1)) == gl) taken |= 1u << (be / G);
+      if (gl == k) { my_v = bv; my_e = be; }
     }
-    // routing weights of the K selected scores (lane k holds slot k)
+    // routing weights of the K selected scores (group lane k holds slot k)
     float ex = 0.f;
     if (mode == MOE_SCORE_SOFTMAX_TOPK) {
-      const float m = __shfl_sync(0xffffffffu, my_v, 0);
-      if (lane < K) ex = expf(my_v - m);
+      const float m = __shfl_sync(0xffffffffu, my_v, gbase);
+      if (gl < K) ex = expf(my_v - m);
     } else {
-      if (lane < K) ex = 1.0f / (1.0f + expf(-my_v));
+      if (gl < K) ex = 1.0f / (1.0f + expf(-my_v));
     }
     float sum = 0.f;  // ascending slot order
-    for (int k = 0; k < K; ++k) sum = __fadd_rn(sum, __shfl_sync(0xffffffffu, ex, k));
-    if (lane < K) {
-      const long j = static_cast<long>(t) * K + lane;
+    for (int k = 0; k < K; ++k) sum = __fadd_rn(sum, __shfl_sync(0xffffffffu, ex, gbase + k));
+    if (live && gl < K) {
+      const long j = t * K + gl;
       ids[j] = my_e;
       w[j] = __fdiv_rn(ex, sum);
-      atomicAdd(&counts[static_cast<long>(t / kRouteTokensPerChunk) * E + my_e], 1);
+      atomicAdd(&counts[(t / kRouteTokensPerChunk) * E + my_e], 1);
     }
   }
 }
@@ -239,16 +253,21 @@ __global__ void __launch_bounds__(kRouteThreads) route_rank(
   }
 }
 
-template <int EPL>
+template <int VPL>
 cudaError_t launch_topk(const float* logits, const float* bias, int mode, int32_t* ids, float* w,
-                        int32_t* counts, const moe_dims& d, int32_t* status, cudaStream_t s) {
+                        int32_t* counts, const moe_dims& d, int G, int32_t* status,
+                        cudaStream_t s) {
   long blocks;
-  if (mode == MOE_SCORE_GIVEN) blocks = (static_cast<long>(d.T) * d.K + kRouteThreads - 1) / kRouteThreads;
-  else blocks = (d.T + kRouteWarps - 1) / kRouteWarps;
+  if (mode == MOE_SCORE_GIVEN) {
+    blocks = (static_cast<long>(d.T) * d.K + kRouteThreads - 1) / kRouteThreads;
+  } else {
+    const long tokens_per_block = static_cast<long>(kRouteWarps) * (32 / G);
+    blocks = (d.T + tokens_per_block - 1) / tokens_per_block;
+  }
   const long cap = static_cast<long>(sm_count()) * 8;
   if (blocks > cap) blocks = cap;
-  route_topk<EPL><<<static_cast<int>(blocks), kRouteThreads, 0, s>>>(logits, bias, mode, ids, w,
-                                                                      counts, d.T, d.E, d.K, status);
+  route_topk<VPL><<<static_cast<int>(blocks), kRouteThreads, 0, s>>>(
+      logits, bias, mode, ids, w, counts, d.T, d.E, d.K, G, status);
   return cudaGetLastError();
 }
 
@@ -269,13 +288,15 @@ cudaError_t launch_route_histogram(const float* logits, const float* bias, int m
   if (nchunks > 0) {
     err = cudaMemsetAsync(counts, 0, static_cast<size_t>(nchunks) * d.E * sizeof(int32_t), s);
     if (err != cudaSuccess) return err;
-    const int epl = (d.E + 31) / 32;
-    if (epl <= 1) err = launch_topk<1>(logits, bias, mode, ids, w, counts, d, dev_status, s);
-    else if (epl <= 2) err = launch_topk<2>(logits, bias, mode, ids, w, counts, d, dev_status, s);
-    else if (epl <= 4) err = launch_topk<4>(logits, bias, mode, ids, w, counts, d, dev_status, s);
-    else if (epl <= 8) err = launch_topk<8>(logits, bias, mode, ids, w, counts, d, dev_status, s);
-    else if (epl <= 16) err = launch_topk<16>(logits, bias, mode, ids, w, counts, d, dev_status, s);
-    else err = launch_topk<32>(logits, bias, mode, ids, w, counts, d, dev_status, s);
+    // G lanes per token: a power of two with G >= K and G * VPL >= E, VPL <= 32
+    int G = 1;
+    while (G < d.K) G <<= 1;
+    while (G * 32 < d.E) G <<= 1;
+    int vpl = (d.E + G - 1) / G;
+    if (vpl <= 4) err = launch_topk<4>(logits, bias, mode, ids, w, counts, d, G, dev_status, s);
+    else if (vpl <= 8) err = launch_topk<8>(logits, bias, mode, ids, w, counts, d, G, dev_status, s);
+    else if (vpl <= 16) err = launch_topk<16>(logits, bias, mode, ids, w, counts, d, G, dev_status, s);
+    else err = launch_topk<32>(logits, bias, mode, ids, w, counts, d, G, dev_status, s);
     if (err != cudaSuccess) return err;
   }
   route_scan<<<1, 1024, 0, s>>>(counts, chunk_excl, nchunks, d.E, group_sizes, group_offsets);
