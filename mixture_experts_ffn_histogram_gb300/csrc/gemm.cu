@@ -229,15 +229,18 @@ __device__ __forceinline__ void issue_loads(const Tile& T, int kb, int rank, uin
   }
 }
 
-// Rows [valid, 64) of every 64-wide chunk of a drhs stage belong to the next
-// group (or lie past the end): zero them in A and B, then make the zeros
-// visible to the tensor core (async proxy).
-// For a pair the even CTA's MMA warp zeroes both CTAs' stages (the odd CTA's
-// through the cluster's shared window), since the odd CTA never learns when
-// its bytes have landed.
+// The last reduction block of a drhs tile holds `valid` rows of the group
+// (1..63); the rest belong to the next group (or lie past the end).  Its MMA
+// K-steps of 16 rows that lie wholly past `valid` are skipped; only the rows
+// [valid, roundup16(valid)) of the step that straddles the end are zeroed, in
+// A and B.  For a pair the even CTA's MMA warp zeroes both CTAs' stages (the
+// odd CTA's through the cluster's shared window), since the odd CTA never
+// learns when its bytes have landed.
 template <int BN, int CG>
 __device__ __forceinline__ void zero_tail(uint8_t* sa, uint8_t* sb, int valid, int lane) {
-  const int nrows = BK - valid;
+  const int end = (valid + kUmmaK - 1) / kUmmaK * kUmmaK;
+  const int nrows = end - valid;
+  if (nrows == 0) return;
   constexpr int kChunksAB = 2 + BN / 64 / CG;
   const int nvec = kChunksAB * nrows * 8;
   for (int i = lane; i < nvec; i += 32) {
@@ -252,9 +255,6 @@ __device__ __forceinline__ void zero_tail(uint8_t* sa, uint8_t* sb, int valid, i
   else fence_proxy_async_smem();
 }
 
-// silu(g) = g * sigmoid(g) and sigmoid(g) in the epilogues, with the
-// hardware exponential and approximate division (relative error ~1e-6;
-// for large |g| they reach the exact limits 0 and g).
 __device__ __forceinline__ float sigmoid_fast(float g) { return __fdividef(1.0f, 1.0f + __expf(-g)); }
 __device__ __forceinline__ float silu_f(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
 
@@ -732,9 +732,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           uint8_t* sa = ring + stage * kStageBytes;
           uint8_t* sb = sa + kAStageBytes;
+          int ksteps = BK / kUmmaK;
           if constexpr (Tr::kGroupedK) {
             const int valid = T.klen - kb * BK;
-            if (valid < BK) zero_tail<BN, CG>(sa, sb, valid, lane);
+            if (valid < BK) {
+              zero_tail<BN, CG>(sa, sb, valid, lane);
+              ksteps = (valid + kUmmaK - 1) / kUmmaK;
+            }
           }
           __syncwarp();
           if (lane == 0) {
@@ -742,6 +746,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t b_addr = smem_u32(sb);
 #pragma unroll
             for (int kk = 0; kk < BK / kUmmaK; ++kk) {
+              if (kk >= ksteps) break;
               const uint64_t ad = Tr::kAMn
                                       ? smem_desc_sw128(a_addr + kk * 2048, kChunkBytes, 1024)
                                       : smem_desc_sw128(a_addr + kk * 32, 16, 1024);
