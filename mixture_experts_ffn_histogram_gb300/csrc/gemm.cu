@@ -79,18 +79,26 @@ struct SmemCtl {
 // operand ring, RING staging buffers per epilogue warp, and (ZB) two more
 // buffers per epilogue warp into which TMA loads the z rows that the fused
 // SwiGLU backward reads.
-template <int BN_, int STAGES_, int CG_, int RING_, int ZB_ = 0>
+//
+// NACC = 2 makes a tile two accumulators wide (2*BN columns per CTA, all 512
+// TMEM columns): each A stage feeds two MMAs, so each SM loads 25% fewer bytes
+// per MMA, at the price of single-buffered accumulators.
+template <int BN_, int STAGES_, int CG_, int RING_, int ZB_ = 0, int NACC_ = 1>
 struct Shape {
   static constexpr int BN = BN_;
   static constexpr int kStages = STAGES_;
   static constexpr int CG = CG_;
   static constexpr int kRing = RING_;
   static constexpr bool kZB = ZB_ != 0;
+  static constexpr int kNacc = NACC_;
   static constexpr int kZBytes = kZB ? kEpiWarps * 2 * kBufBytes : 0;
-  static constexpr int kBRows = BN / CG;  // B columns held by one CTA
-  static constexpr int kBStageBytes = kBRows * BK * 2;
+  static constexpr int kBRows = BN / CG;  // B columns held by one CTA, per accumulator
+  static constexpr int kBStageBytes = NACC_ * kBRows * BK * 2;
   static constexpr int kStageBytes = kAStageBytes + kBStageBytes;
-  static constexpr int kTmemCols = 2 * BN;  // two accumulators
+  static constexpr int kAccSlots = NACC_ == 1 ? 2 : 1;   // double-buffered when 1 wide
+  static constexpr int kAccStride = BN * NACC_;           // TMEM columns per slot
+  static constexpr int kTmemCols = kAccSlots * kAccStride;
+  static_assert(kTmemCols == 512, "TMEM columns");
   static constexpr int kEpiBytes = kEpiWarps * RING_ * kBufBytes;
   static constexpr size_t kSmemBytes =
       1024 + static_cast<size_t>(STAGES_) * kStageBytes + kEpiBytes + kZBytes + sizeof(SmemCtl);
@@ -189,7 +197,7 @@ __device__ __forceinline__ void load3(void* dst, const CUtensorMap* map, uint32_
 
 // TMA loads of one reduction block: this CTA's 128 A rows and its BN/CG B
 // columns (CTA `rank` of the pair takes the rank-th half).
-template <int KIND, int BN, int CG>
+template <int KIND, int BN, int CG, int NACC = 1>
 __device__ __forceinline__ void issue_loads(const Tile& T, int kb, int rank, uint8_t* sa,
                                             uint8_t* sb, uint32_t bar, const CUtensorMap* ma,
                                             const CUtensorMap* mb, const Params& p) {
@@ -224,8 +232,11 @@ __device__ __forceinline__ void issue_loads(const Tile& T, int kb, int rank, uin
     load2<CG>(sa, ma, bar, T.m0, kr);
     load2<CG>(sa + kChunkBytes, ma, bar, T.m0 + 64, kr);
 #pragma unroll
-    for (int j = 0; j < kBChunks; ++j)
-      load2<CG>(sb + j * kChunkBytes, mb, bar, T.n0 + (BN / CG) * rank + 64 * j, kr);
+    for (int a = 0; a < NACC; ++a)
+#pragma unroll
+      for (int j = 0; j < kBChunks; ++j)
+        load2<CG>(sb + (a * kBChunks + j) * kChunkBytes, mb, bar,
+                  T.n0 + a * BN + (BN / CG) * rank + 64 * j, kr);
   }
 }
 
@@ -236,12 +247,12 @@ __device__ __forceinline__ void issue_loads(const Tile& T, int kb, int rank, uin
 // A and B.  For a pair the even CTA's MMA warp zeroes both CTAs' stages (the
 // odd CTA's through the cluster's shared window), since the odd CTA never
 // learns when its bytes have landed.
-template <int BN, int CG>
+template <int BN, int CG, int NACC = 1>
 __device__ __forceinline__ void zero_tail(uint8_t* sa, uint8_t* sb, int valid, int lane) {
   const int end = (valid + kUmmaK - 1) / kUmmaK * kUmmaK;
   const int nrows = end - valid;
   if (nrows == 0) return;
-  constexpr int kChunksAB = 2 + BN / 64 / CG;
+  constexpr int kChunksAB = 2 + NACC * BN / 64 / CG;
   const int nvec = kChunksAB * nrows * 8;
   for (int i = lane; i < nvec; i += 32) {
     const int line = i >> 3, part = i & 7;
@@ -610,6 +621,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int CG = S::CG;
   constexpr int RING = S::kRing;
   using Tr = Traits<KIND, BN, CG>;
+  constexpr int NACC = S::kNacc;
+  constexpr int BNT = BN * NACC;  // tile width in output columns
+  static_assert(NACC == 1 || Tr::kGroupedK, "wide tiles are for drhs");
   constexpr int kStages = S::kStages;
   constexpr int kStageBytes = S::kStageBytes;
   constexpr uint32_t kTmemCols = S::kTmemCols;
@@ -681,7 +695,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = s.tmem_base;
   const WaitCtl wc{&s.abort_flag, p.status, p.limit_ns};
-  const int ntiles = total_tiles<KIND, BN, CG>(p, s);
+  const int ntiles = total_tiles<KIND, BNT, CG>(p, s);
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -695,12 +709,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t full0 = (CG == 2) ? mapa_shared(smem_u32(&s.full[0]), 0) : smem_u32(&s.full[0]);
       bool aborted = false;
       for (int t = unit; t < ntiles && !aborted; t += units) {
-        const Tile T = decode_tile<KIND, BN, CG>(t, rank, p, s);
+        const Tile T = decode_tile<KIND, BNT, CG>(t, rank, p, s);
         for (int kb = 0; kb < T.kb; ++kb) {
           if (!mbar_wait(&s.empty[stage], phase ^ 1u, wc)) { aborted = true; break; }
           uint8_t* sa = ring + stage * kStageBytes;
           if (leader) mbar_arrive_expect_tx(&s.full[stage], kStageBytes * CG);
-          issue_loads<KIND, BN, CG>(T, kb, rank, sa, sa + kAStageBytes,
+          issue_loads<KIND, BN, CG, NACC>(T, kb, rank, sa, sa + kAStageBytes,
                                     full0 + stage * static_cast<uint32_t>(sizeof(uint64_t)),
                                     &map_a, &map_b, p);
           ++fills[stage];
@@ -722,11 +736,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       int last_stage = -1;
       bool aborted = false;
       for (int t = unit; t < ntiles && !aborted; t += units) {
-        const Tile T = decode_tile<KIND, BN, CG>(t, rank, p, s);
+        const Tile T = decode_tile<KIND, BNT, CG>(t, rank, p, s);
         if (T.kb == 0) continue;
         if (!mbar_wait(&s.tempty[acc], acc_phase ^ 1u, wc)) { aborted = true; break; }
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + acc * BN;
+        const uint32_t d_tmem = tmem_base + acc * S::kAccStride;
         for (int kb = 0; kb < T.kb; ++kb) {
           if (!mbar_wait(&s.full[stage], phase, wc)) { aborted = true; break; }
           tc_fence_after();
@@ -736,7 +750,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if constexpr (Tr::kGroupedK) {
             const int valid = T.klen - kb * BK;
             if (valid < BK) {
-              zero_tail<BN, CG>(sa, sb, valid, lane);
+              zero_tail<BN, CG, NACC>(sa, sb, valid, lane);
               ksteps = (valid + kUmmaK - 1) / kUmmaK;
             }
           }
@@ -750,10 +764,14 @@ __global__ void __launch_bounds__(kThreads, 1)
               const uint64_t ad = Tr::kAMn
                                       ? smem_desc_sw128(a_addr + kk * 2048, kChunkBytes, 1024)
                                       : smem_desc_sw128(a_addr + kk * 32, 16, 1024);
-              const uint64_t bd = Tr::kBMn
-                                      ? smem_desc_sw128(b_addr + kk * 2048, kChunkBytes, 1024)
-                                      : smem_desc_sw128(b_addr + kk * 32, 16, 1024);
-              umma_bf16<CG>(d_tmem, ad, bd, Tr::kIdesc, (kb > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+              for (int a = 0; a < NACC; ++a) {
+                const uint32_t b_acc = b_addr + a * (BN / CG) * BK * 2;
+                const uint64_t bd = Tr::kBMn
+                                        ? smem_desc_sw128(b_acc + kk * 2048, kChunkBytes, 1024)
+                                        : smem_desc_sw128(b_acc + kk * 32, 16, 1024);
+                umma_bf16<CG>(d_tmem + a * BN, ad, bd, Tr::kIdesc, (kb > 0 || kk > 0) ? 1u : 0u);
+              }
             }
             umma_commit<CG>(&s.empty[stage]);
           }
@@ -765,7 +783,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (aborted) break;
         if (lane == 0) umma_commit<CG>(&s.tfull[acc]);
         __syncwarp();
-        if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+        if (++acc == S::kAccSlots) { acc = 0; acc_phase ^= 1u; }
       }
       if (aborted && last_stage >= 0) {  // let issued MMAs finish before TMEM is freed
         (void)mbar_wait_drain(&s.empty[last_stage], (commits[last_stage] - 1u) & 1u,
@@ -782,16 +800,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     if constexpr (CG == 2) tempty_peer = mapa_shared(smem_u32(&s.tempty[0]), 0);
     uint32_t acc = 0, acc_phase = 0;
     for (int t = unit; t < ntiles; t += units) {
-      const Tile T = decode_tile<KIND, BN, CG>(t, rank, p, s);
+      const Tile T = decode_tile<KIND, BNT, CG>(t, rank, p, s);
       if (T.kb == 0) {
-        if constexpr (Tr::kGroupedK) zero_tile<BN, RING>(T, ec, p);
+        if constexpr (Tr::kGroupedK) {
+#pragma unroll
+          for (int a = 0; a < NACC; ++a) {
+            Tile Ta = T;
+            Ta.n0 = T.n0 + a * BN;
+            zero_tile<BN, RING>(Ta, ec, p);
+          }
+        }
         continue;
       }
       if (z_by_tma<KIND, S::kZB, RING>(T, ec, p)) z_request(T, 0, ec, p);
       if (!mbar_wait(&s.tfull[acc], acc_phase, wc)) break;
       tc_fence_after();
-      epilogue_tile<KIND, BN, CG, RING, S::kZB>(
-          T, tmem_base + acc * BN + (static_cast<uint32_t>(q * 32) << 16), ec, p);
+#pragma unroll
+      for (int a = 0; a < NACC; ++a) {
+        Tile Ta = T;
+        Ta.n0 = T.n0 + a * BN;
+        epilogue_tile<KIND, BN, CG, RING, S::kZB>(
+            Ta, tmem_base + acc * S::kAccStride + a * BN + (static_cast<uint32_t>(q * 32) << 16),
+            ec, p);
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
@@ -800,7 +831,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         else
           mbar_arrive(&s.tempty[acc]);
       }
-      if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+      if (++acc == S::kAccSlots) { acc = 0; acc_phase ^= 1u; }
     }
     if (lane == 0) bulk_wait_all();  // every store has finished before the CTA exits
     __syncwarp();
@@ -934,47 +965,61 @@ cudaError_t launch_shape(const GemmCall& c, cudaStream_t s) {
   const long F2 = 2L * d.F;
   switch (c.kind) {
     case GemmKind::kFc1:
-      if constexpr (S::kRing >= 3) {  // h, z gate and z up are staged together
-        p.Kdim = d.D;
-        p.N = d.F;
-        p.n_tiles = static_cast<int>(cdiv(d.F, BN / 2));
-        ok = map2d(&ma, c.a, d.D, R, 64, BM) && map3d(&mb, c.b, F2, d.D, d.E, 64, 64) &&
-             map2d(&mc, c.out0, d.F, R, 64, 32);
-        if (ok) ok = (c.out1 != nullptr) ? map2d(&md, c.out1, F2, R, 64, 32) : (md = mc, true);
-        if (!ok) return cudaErrorInvalidValue;
-        return launch_kind<0, S>(ma, mb, mc, md, p, row_blocks_bound * p.n_tiles, s);
+    case GemmKind::kFc2:
+    case GemmKind::kDlhsFc2:
+    case GemmKind::kDlhsFc1:
+      if constexpr (S::kNacc == 1) {
+        switch (c.kind) {
+          case GemmKind::kFc1:
+            if constexpr (S::kRing >= 3) {  // h, z gate and z up are staged together
+              p.Kdim = d.D;
+              p.N = d.F;
+              p.n_tiles = static_cast<int>(cdiv(d.F, BN / 2));
+              ok = map2d(&ma, c.a, d.D, R, 64, BM) && map3d(&mb, c.b, F2, d.D, d.E, 64, 64) &&
+                   map2d(&mc, c.out0, d.F, R, 64, 32);
+              if (ok) ok = (c.out1 != nullptr) ? map2d(&md, c.out1, F2, R, 64, 32) : (md = mc, true);
+              if (!ok) return cudaErrorInvalidValue;
+              return launch_kind<0, S>(ma, mb, mc, md, p, row_blocks_bound * p.n_tiles, s);
+            }
+            return cudaErrorInvalidValue;
+          case GemmKind::kFc2:
+            p.Kdim = d.F;
+            p.N = d.D;
+            p.n_tiles = static_cast<int>(cdiv(d.D, BN));
+            ok = map2d(&ma, c.a, d.F, R, 64, BM) && map3d(&mb, c.b, d.D, d.F, d.E, 64, 64) &&
+                 map2d(&mc, c.out0, d.D, R, 64, 32);
+            if (!ok) return cudaErrorInvalidValue;
+            return launch_kind<1, S>(ma, mb, mc, mc, p, row_blocks_bound * p.n_tiles, s);
+          case GemmKind::kDlhsFc2:
+            if constexpr (S::kRing >= 2) {  // dgate and dup are staged together
+              p.Kdim = d.D;
+              p.N = d.F;
+              p.n_tiles = static_cast<int>(cdiv(d.F, BN));
+              ok = map2d(&ma, c.a, d.D, R, 64, BM) && map3d(&mb, c.b, d.D, d.F, d.E, 64, kBRows) &&
+                   map2d(&mc, c.out0, c.aux != nullptr ? F2 : d.F, R, 64, 32);
+              if (ok) ok = (c.aux != nullptr) ? map2d(&md, c.aux, F2, R, 64, 32) : (md = mc, true);
+              if (!ok) return cudaErrorInvalidValue;
+              return launch_kind<2, S>(ma, mb, mc, md, p, row_blocks_bound * p.n_tiles, s);
+            }
+            return cudaErrorInvalidValue;
+          case GemmKind::kDlhsFc1:
+            p.Kdim = 2 * d.F;
+            p.N = d.D;
+            p.n_tiles = static_cast<int>(cdiv(d.D, BN));
+            ok = map2d(&ma, c.a, F2, R, 64, BM) && map3d(&mb, c.b, F2, d.D, d.E, 64, kBRows) &&
+                 map2d(&mc, c.out0, d.D, R, 64, 32);
+            if (!ok) return cudaErrorInvalidValue;
+            return launch_kind<3, S>(ma, mb, mc, mc, p, row_blocks_bound * p.n_tiles, s);
+          default:
+            break;
+        }
       }
       return cudaErrorInvalidValue;
-    case GemmKind::kFc2:
-      p.Kdim = d.F;
-      p.N = d.D;
-      p.n_tiles = static_cast<int>(cdiv(d.D, BN));
-      ok = map2d(&ma, c.a, d.F, R, 64, BM) && map3d(&mb, c.b, d.D, d.F, d.E, 64, 64) &&
-           map2d(&mc, c.out0, d.D, R, 64, 32);
-      if (!ok) return cudaErrorInvalidValue;
-      return launch_kind<1, S>(ma, mb, mc, mc, p, row_blocks_bound * p.n_tiles, s);
-    case GemmKind::kDlhsFc2:
-      p.Kdim = d.D;
-      p.N = d.F;
-      p.n_tiles = static_cast<int>(cdiv(d.F, BN));
-      ok = map2d(&ma, c.a, d.D, R, 64, BM) && map3d(&mb, c.b, d.D, d.F, d.E, 64, kBRows) &&
-           map2d(&mc, c.out0, c.aux != nullptr ? F2 : d.F, R, 64, 32);
-      if (ok) ok = (c.aux != nullptr) ? map2d(&md, c.aux, F2, R, 64, 32) : (md = mc, true);
-      if (!ok) return cudaErrorInvalidValue;
-      return launch_kind<2, S>(ma, mb, mc, md, p, row_blocks_bound * p.n_tiles, s);
-    case GemmKind::kDlhsFc1:
-      p.Kdim = 2 * d.F;
-      p.N = d.D;
-      p.n_tiles = static_cast<int>(cdiv(d.D, BN));
-      ok = map2d(&ma, c.a, F2, R, 64, BM) && map3d(&mb, c.b, F2, d.D, d.E, 64, kBRows) &&
-           map2d(&mc, c.out0, d.D, R, 64, 32);
-      if (!ok) return cudaErrorInvalidValue;
-      return launch_kind<3, S>(ma, mb, mc, mc, p, row_blocks_bound * p.n_tiles, s);
     case GemmKind::kDrhsFc2:
       p.M = d.F;
       p.N = d.D;
       p.m_tiles = static_cast<int>(cdiv(d.F, BM * CG));
-      p.n_tiles = static_cast<int>(cdiv(d.D, BN));
+      p.n_tiles = static_cast<int>(cdiv(d.D, BN * S::kNacc));
       ok = map2d(&ma, c.a, d.F, R, 64, 64) && map2d(&mb, c.b, d.D, R, 64, 64) &&
            map3d(&mc, c.out0, d.D, d.F, d.E, 64, 32);
       if (!ok) return cudaErrorInvalidValue;
@@ -984,7 +1029,7 @@ cudaError_t launch_shape(const GemmCall& c, cudaStream_t s) {
       p.M = d.D;
       p.N = 2 * d.F;
       p.m_tiles = static_cast<int>(cdiv(d.D, BM * CG));
-      p.n_tiles = static_cast<int>(cdiv(F2, BN));
+      p.n_tiles = static_cast<int>(cdiv(F2, BN * S::kNacc));
       ok = map2d(&ma, c.a, d.D, R, 64, 64) && map2d(&mb, c.b, F2, R, 64, 64) &&
            map3d(&mc, c.out0, F2, d.D, d.E, 64, 32);
       if (!ok) return cudaErrorInvalidValue;
@@ -1000,6 +1045,8 @@ using Shape1 = Shape<256, 3, 1, 4>;
 // (h, z gate, z up); the others need at most two.
 using Shape2Fc1 = Shape<256, 4, 2, 4>;
 using Shape2 = Shape<256, 5, 2, 2>;
+// drhs: tiles two accumulators wide (fewer bytes loaded per MMA).
+using Shape2Drhs = Shape<256, 3, 2, 2, 0, 2>;
 // The FC2 dlhs with the fused SwiGLU backward also stages z rows.
 using Shape1Dz = Shape<256, 3, 1, 2, 1>;
 using Shape2Dz = Shape<256, 4, 2, 2, 1>;
@@ -1032,6 +1079,8 @@ cudaError_t launch_grouped_gemm(const GemmCall& c, cudaStream_t s) {
   }
   const bool dz = (c.kind == GemmKind::kDlhsFc2 && c.aux != nullptr);
   if (!use_pairs(c)) return dz ? launch_shape<Shape1Dz>(c, s) : launch_shape<Shape1>(c, s);
+  if (c.kind == GemmKind::kDrhsFc2 || c.kind == GemmKind::kDrhsFc1)
+    return launch_shape<Shape2Drhs>(c, s);
   if (c.kind == GemmKind::kFc1) return launch_shape<Shape2Fc1>(c, s);
   return dz ? launch_shape<Shape2Dz>(c, s) : launch_shape<Shape2>(c, s);
 }
