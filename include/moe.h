@@ -196,7 +196,9 @@ moe_status moe_grouped_gemm_fc1_swiglu(const moe_bf16* xs, const moe_bf16* wi,
  * grad is dz bf16 [R,2F] when z == NULL.  When z != NULL, grad is dh bf16
  * [R,F] and the SwiGLU backward [Gemma4 L/M row 7] runs first, writing
  * dz = [dgate | dup] into ws.  dxs (bf16 [R,D]) or dwi (bf16 [E,D,2F]) may be
- * NULL to skip that half.
+ * NULL to skip that half.  ws is required when z != NULL or dwi != NULL (the
+ * drhs keeps the counter of its dynamic tile schedule in the first bytes of
+ * ws and resets it itself; ws needs no initial contents).
  */
 moe_status moe_grouped_gemm_fc1_swiglu_bwd(const moe_bf16* grad, const moe_bf16* z,
                                            const moe_bf16* xs, const moe_bf16* wi,
@@ -223,7 +225,9 @@ moe_status moe_grouped_gemm_fc2(const moe_bf16* h, const moe_bf16* wo,
  *         and dh_or_dz is dz bf16 [R,2F]; with z == NULL it is dh bf16 [R,F].
  *   drhs: dwo[e,f,d] = bf16(sum_{r in group e} h[r,f] * dys[r,d]); zero for
  *         an empty group.
- * dh_or_dz or dwo may be NULL to skip that half.
+ * dh_or_dz or dwo may be NULL to skip that half.  ws is required when dwo !=
+ * NULL (the counter of the drhs's dynamic tile schedule; no initial contents
+ * needed).
  */
 moe_status moe_grouped_gemm_fc2_bwd(const moe_bf16* dys, const moe_bf16* h, const moe_bf16* wo,
                                     const moe_bf16* z, const int32_t* group_offsets,

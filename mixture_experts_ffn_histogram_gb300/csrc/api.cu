@@ -68,7 +68,7 @@ extern "C" {
 size_t moe_workspace_bytes(moe_dims d) {
   if (check_dims(d) != MOE_OK) return 0;
   size_t need = moe::route_ws_bytes(d);
-  const size_t dz = dz_ws_bytes(d);
+  const size_t dz = moe::kWsCounterBytes + dz_ws_bytes(d);
   if (dz > need) need = dz;
   return (need + 255u) & ~static_cast<size_t>(255u);
 }
@@ -228,7 +228,6 @@ moe_status moe_grouped_gemm_fc2_bwd(const moe_bf16* dys, const moe_bf16* h, cons
                                     const moe_bf16* z, const int32_t* group_offsets,
                                     moe_bf16* dh_or_dz, moe_bf16* dwo, int32_t* dev_status,
                                     void* ws, moe_dims d, cudaStream_t stream) {
-  (void)ws;
   MOE_CHECK_DIMS(d);
   MOE_OPTIONAL(dev_status);
   MOE_OPTIONAL(z);
@@ -239,7 +238,10 @@ moe_status moe_grouped_gemm_fc2_bwd(const moe_bf16* dys, const moe_bf16* h, cons
   if (d.T > 0) {
     MOE_REQUIRE(dys);
     if (dh_or_dz != nullptr) MOE_REQUIRE(wo);
-    if (dwo != nullptr) MOE_REQUIRE(h);
+    if (dwo != nullptr) {
+      MOE_REQUIRE(h);
+      MOE_REQUIRE(ws);
+    }
   }
   if (dh_or_dz != nullptr && d.T > 0) {
     GemmCall c{GemmKind::kDlhsFc2, dys, wo, group_offsets, dh_or_dz, nullptr, z, dev_status, d};
@@ -248,6 +250,7 @@ moe_status moe_grouped_gemm_fc2_bwd(const moe_bf16* dys, const moe_bf16* h, cons
   }
   if (dwo != nullptr) {
     GemmCall c{GemmKind::kDrhsFc2, h, dys, group_offsets, dwo, nullptr, nullptr, dev_status, d};
+    c.tile_ctr = static_cast<unsigned int*>(ws);
     moe_status st = from_cuda(moe::launch_grouped_gemm(c, stream));
     if (st != MOE_OK) return st;
   }
@@ -270,11 +273,15 @@ moe_status moe_grouped_gemm_fc1_swiglu_bwd(const moe_bf16* grad, const moe_bf16*
   if (d.T > 0) {
     MOE_REQUIRE(grad);
     if (dxs != nullptr) MOE_REQUIRE(wi);
-    if (dwi != nullptr) MOE_REQUIRE(xs);
-    if (z != nullptr) {
-      // grad is dh [R,F]: the SwiGLU backward writes dz into the workspace
+    if (dwi != nullptr) {
+      MOE_REQUIRE(xs);
       MOE_REQUIRE(ws);
-      moe_bf16* dzw = static_cast<moe_bf16*>(ws);
+    }
+    if (z != nullptr) {
+      // grad is dh [R,F]: the SwiGLU backward writes dz into the workspace,
+      // after the bytes of the drhs tile counter
+      MOE_REQUIRE(ws);
+      moe_bf16* dzw = reinterpret_cast<moe_bf16*>(static_cast<char*>(ws) + moe::kWsCounterBytes);
       cudaError_t e = moe::launch_swiglu_bwd(grad, z, dzw, rows(d), d.F, stream);
       if (e != cudaSuccess) return MOE_ERR_CUDA;
       dz = dzw;
@@ -287,6 +294,7 @@ moe_status moe_grouped_gemm_fc1_swiglu_bwd(const moe_bf16* grad, const moe_bf16*
   }
   if (dwi != nullptr) {
     GemmCall c{GemmKind::kDrhsFc1, xs, dz, group_offsets, dwi, nullptr, nullptr, dev_status, d};
+    c.tile_ctr = static_cast<unsigned int*>(ws);
     moe_status st = from_cuda(moe::launch_grouped_gemm(c, stream));
     if (st != MOE_OK) return st;
   }

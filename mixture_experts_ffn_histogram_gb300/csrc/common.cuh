@@ -295,6 +295,10 @@ __device__ __forceinline__ void st_cluster_zero16(uint32_t cluster_addr) {
   asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(cluster_addr), "r"(0u)
                : "memory");
 }
+// 4-byte store into the shared memory of a CTA of the cluster.
+__device__ __forceinline__ void st_cluster_u32(uint32_t cluster_addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
+}
 // Arrive on a barrier of another CTA of the cluster (release, cluster scope).
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)

@@ -62,6 +62,7 @@ constexpr int kMaxStages = 8;
 constexpr int kEpiWarps = 4;
 constexpr int kBufBytes = 32 * 128;  // staging buffer: 32 rows x 64 bf16
 constexpr size_t kSmemLimit = 227 * 1024;
+constexpr int kSched = 8;  // tile-index slots of the dynamic (drhs) schedule
 
 struct SmemCtl {
   uint64_t full[kMaxStages];
@@ -69,10 +70,15 @@ struct SmemCtl {
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t zbar[kEpiWarps];  // z rows landed in an epilogue warp's buffers
+  uint64_t sfull[kSched];    // a tile index was written to the slot
+  uint64_t sempty[kSched];   // every role has read the slot
+  int sched[kSched];
   uint32_t tmem_base;
   int abort_flag;
   int off[kMaxExperts + 1];  // group offsets
-  int mt[kMaxExperts + 1];   // prefix of (128*CG)-row blocks per group
+  // forward/dlhs: prefix of (128*CG)-row blocks per group; drhs: sort keys
+  // whose low 10 bits are the experts by descending reduction length
+  int mt[kMaxExperts + 1];
 };
 
 // Tile shape: 128 x BN accumulator per CTA, CG CTAs per MMA, a `STAGES`-deep
@@ -115,6 +121,7 @@ struct Params {
   __nv_bfloat16* out1;
   const __nv_bfloat16* aux;
   int32_t* status;
+  unsigned int* tile_ctr;  // drhs: tiles claimed so far (zero at launch)
   uint64_t limit_ns;
   int E, Kdim, M, N, F;
   int m_tiles, n_tiles;
@@ -161,8 +168,9 @@ __device__ __forceinline__ Tile decode_tile(int t, int rank, const Params& p, co
     T.klen = p.Kdim;
   } else {
     const int per_e = p.m_tiles * p.n_tiles;
-    T.e = t / per_e;
-    const int r = t - T.e * per_e;
+    const int i = t / per_e;
+    T.e = s.mt[i] & (kMaxExperts - 1);
+    const int r = t - i * per_e;
     const int mt = r / p.n_tiles;
     T.m0 = mt * (BM * CG) + BM * rank;
     T.n0 = (r - mt * p.n_tiles) * BN;
@@ -178,6 +186,96 @@ template <int KIND, int BN, int CG>
 __device__ __forceinline__ int total_tiles(const Params& p, const SmemCtl& s) {
   if constexpr (!Traits<KIND, BN, CG>::kGroupedK) return s.mt[p.E] * p.n_tiles;
   else return p.E * p.m_tiles * p.n_tiles;
+}
+
+// Dynamic tile schedule of the drhs GEMMs.  Their tiles take as long as
+// their group has rows, so a fixed assignment leaves pairs idle while
+// others finish long groups.  Instead the even CTA's producer claims tile
+// indices from a global counter, in the order of descending group length
+// (longest first, so that the last tiles handed out are the short ones), and
+// writes each index into one of kSched shared-memory slots of both CTAs; the
+// MMA warp, the epilogue warps and the odd CTA's producer read it from there
+// and release the slot on the even CTA's `sempty` barrier.  An index >=
+// the tile count ends the sequence.
+
+// Readers of one slot: the MMA warp and the epilogue warps of the even CTA,
+// plus the producer and the epilogue warps of the odd CTA.
+template <int CG>
+__host__ __device__ constexpr uint32_t sched_readers() { return CG == 2 ? 2 * kEpiWarps + 2 : kEpiWarps + 1; }
+
+// Next tile index for a reader (every thread of `mask` calls it; `releaser`
+// releases the slot).  Returns -1 when the wait gave up.
+template <int CG>
+__device__ __forceinline__ int sched_take(SmemCtl& s, uint32_t& seq, bool leader, bool releaser,
+                                          unsigned mask, const WaitCtl& wc) {
+  const uint32_t slot = seq % kSched;
+  const uint32_t par = (seq / kSched) & 1u;
+  ++seq;
+  const bool got = (CG == 2) ? mbar_wait_cluster(&s.sfull[slot], par, wc)
+                             : mbar_wait(&s.sfull[slot], par, wc);
+  if (!__all_sync(mask, got)) return -1;
+  const int t = *reinterpret_cast<volatile int*>(&s.sched[slot]);
+  __syncwarp(mask);
+  if (releaser) {
+    if (CG == 2 && !leader)
+      mbar_arrive_remote(mapa_shared(smem_u32(&s.sempty[slot]), 0));
+    else
+      mbar_arrive(&s.sempty[slot]);
+  }
+  return t;
+}
+
+// The even CTA's producer publishes tile index t to every reader.  Returns
+// false when the wait for a free slot gave up.
+template <int CG>
+__device__ __forceinline__ bool sched_publish(SmemCtl& s, uint32_t& seq, int t, const WaitCtl& wc) {
+  const uint32_t slot = seq % kSched;
+  const uint32_t par = (seq / kSched) & 1u;
+  ++seq;
+  const bool free_slot = (CG == 2) ? mbar_wait_cluster(&s.sempty[slot], par ^ 1u, wc)
+                                   : mbar_wait(&s.sempty[slot], par ^ 1u, wc);
+  if (!free_slot) return false;
+  *reinterpret_cast<volatile int*>(&s.sched[slot]) = t;
+  if constexpr (CG == 2) {
+    st_cluster_u32(mapa_shared(smem_u32(&s.sched[slot]), 1), static_cast<uint32_t>(t));
+    mbar_arrive_remote(mapa_shared(smem_u32(&s.sfull[slot]), 1));
+  }
+  mbar_arrive(&s.sfull[slot]);
+  return true;
+}
+
+// Orders the experts by descending reduction length (64-row blocks; ties by
+// expert index) into s.mt, identically in every CTA: bitonic sort of
+// 32-bit keys (blocks, clamped to 22 bits, inverted | expert).  All threads
+// of the CTA call it after s.off is complete.
+__device__ __forceinline__ void sort_groups_desc(SmemCtl& s, int E) {
+  int n = 1;
+  while (n < E) n <<= 1;
+  uint32_t* key = reinterpret_cast<uint32_t*>(s.mt);
+  for (int i = threadIdx.x; i < n; i += kThreads) {
+    uint32_t k = 0xFFFFFFFFu;
+    if (i < E) {
+      const int kb = min((s.off[i + 1] - s.off[i] + BK - 1) / BK, 0x3FFFFF);
+      k = (static_cast<uint32_t>(0x3FFFFF - kb) << 10) | static_cast<uint32_t>(i);
+    }
+    key[i] = k;
+  }
+  __syncthreads();
+  for (int k = 2; k <= n; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int i = threadIdx.x; i < n; i += kThreads) {
+        const int l = i ^ j;
+        if (l > i) {
+          const uint32_t a = key[i], b = key[l];
+          if ((a > b) == ((i & k) == 0)) {
+            key[i] = b;
+            key[l] = a;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
 }
 
 // One TMA load of a stage: for a pair, the bytes complete on the even CTA's
@@ -654,6 +752,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&s.tempty[i], kEpiWarps * CG);
     }
     for (int i = 0; i < kEpiWarps; ++i) mbar_init(&s.zbar[i], 1);
+    for (int i = 0; i < kSched; ++i) {
+      mbar_init(&s.sfull[i], 1);
+      mbar_init(&s.sempty[i], sched_readers<CG>());
+    }
     s.abort_flag = 0;
     mbar_fence_init();
   }
@@ -693,9 +795,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   if constexpr (CG == 2) cluster_sync();  // the peer's barriers exist before any remote arrive
   tc_fence_after();
+  if constexpr (Tr::kGroupedK) sort_groups_desc(s, p.E);
   const uint32_t tmem_base = s.tmem_base;
   const WaitCtl wc{&s.abort_flag, p.status, p.limit_ns};
   const int ntiles = total_tiles<KIND, BNT, CG>(p, s);
+  // drhs tiles come from the dynamic schedule, the others in a fixed stride
+  constexpr bool kDyn = Tr::kGroupedK;
+  uint32_t sseq = 0;      // dynamic: slots read (or written) so far
+  int tstat = unit;       // fixed: this unit's next tile
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -708,9 +815,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; i < kStages; ++i) fills[i] = 0;
       const uint32_t full0 = (CG == 2) ? mapa_shared(smem_u32(&s.full[0]), 0) : smem_u32(&s.full[0]);
       bool aborted = false;
-      for (int t = unit; t < ntiles && !aborted; t += units) {
+      // dynamic schedule: the even CTA claims the next tile a little before
+      // the current one's loads end (the atomic's latency hides behind them)
+      int claimed = (kDyn && leader) ? static_cast<int>(atomicAdd(p.tile_ctr, 1u)) : 0;
+      while (!aborted) {
+        int t;
+        if constexpr (!kDyn) {
+          t = tstat;
+          tstat += units;
+        } else if (leader) {
+          t = claimed;
+          if (!sched_publish<CG>(s, sseq, t, wc)) { aborted = true; break; }
+        } else {
+          t = sched_take<CG>(s, sseq, leader, true, 1u, wc);
+          if (t < 0) { aborted = true; break; }
+        }
+        if (t >= ntiles) break;
         const Tile T = decode_tile<KIND, BNT, CG>(t, rank, p, s);
+        bool next_claimed = !(kDyn && leader);
         for (int kb = 0; kb < T.kb; ++kb) {
+          if (!next_claimed && kb + 2 >= T.kb) {
+            claimed = static_cast<int>(atomicAdd(p.tile_ctr, 1u));
+            next_claimed = true;
+          }
           if (!mbar_wait(&s.empty[stage], phase ^ 1u, wc)) { aborted = true; break; }
           uint8_t* sa = ring + stage * kStageBytes;
           if (leader) mbar_arrive_expect_tx(&s.full[stage], kStageBytes * CG);
@@ -720,6 +847,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++fills[stage];
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
+        if (!next_claimed) claimed = static_cast<int>(atomicAdd(p.tile_ctr, 1u));
       }
       if (aborted && leader) {  // let copies already in flight land before the CTA exits
         for (int i = 0; i < kStages; ++i)
@@ -735,14 +863,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; i < kStages; ++i) commits[i] = 0;
       int last_stage = -1;
       bool aborted = false;
-      for (int t = unit; t < ntiles && !aborted; t += units) {
+      while (!aborted) {
+        int t;
+        if constexpr (!kDyn) {
+          t = tstat;
+          tstat += units;
+        } else {
+          t = sched_take<CG>(s, sseq, leader, lane == 0, 0xffffffffu, wc);
+          if (t < 0) { aborted = true; break; }
+        }
+        if (t >= ntiles) break;
         const Tile T = decode_tile<KIND, BNT, CG>(t, rank, p, s);
         if (T.kb == 0) continue;
-        if (!mbar_wait(&s.tempty[acc], acc_phase ^ 1u, wc)) { aborted = true; break; }
+        if (!__all_sync(0xffffffffu, mbar_wait(&s.tempty[acc], acc_phase ^ 1u, wc))) {
+          aborted = true;
+          break;
+        }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * S::kAccStride;
         for (int kb = 0; kb < T.kb; ++kb) {
-          if (!mbar_wait(&s.full[stage], phase, wc)) { aborted = true; break; }
+          if (!__all_sync(0xffffffffu, mbar_wait(&s.full[stage], phase, wc))) {
+            aborted = true;
+            break;
+          }
           tc_fence_after();
           uint8_t* sa = ring + stage * kStageBytes;
           uint8_t* sb = sa + kAStageBytes;
@@ -799,7 +942,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t tempty_peer = 0;
     if constexpr (CG == 2) tempty_peer = mapa_shared(smem_u32(&s.tempty[0]), 0);
     uint32_t acc = 0, acc_phase = 0;
-    for (int t = unit; t < ntiles; t += units) {
+    for (;;) {
+      int t;
+      if constexpr (!kDyn) {
+        t = tstat;
+        tstat += units;
+      } else {
+        t = sched_take<CG>(s, sseq, leader, lane == 0, 0xffffffffu, wc);
+        if (t < 0) break;
+      }
+      if (t >= ntiles) break;
       const Tile T = decode_tile<KIND, BNT, CG>(t, rank, p, s);
       if (T.kb == 0) {
         if constexpr (Tr::kGroupedK) {
@@ -813,7 +965,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         continue;
       }
       if (z_by_tma<KIND, S::kZB, RING>(T, ec, p)) z_request(T, 0, ec, p);
-      if (!mbar_wait(&s.tfull[acc], acc_phase, wc)) break;
+      if (!__all_sync(0xffffffffu, mbar_wait(&s.tfull[acc], acc_phase, wc))) break;
       tc_fence_after();
 #pragma unroll
       for (int a = 0; a < NACC; ++a) {
@@ -956,6 +1108,7 @@ cudaError_t launch_shape(const GemmCall& c, cudaStream_t s) {
   p.out1 = static_cast<__nv_bfloat16*>(c.out1);
   p.aux = static_cast<const __nv_bfloat16*>(c.aux);
   p.status = c.dev_status;
+  p.tile_ctr = c.tile_ctr;
   p.limit_ns = kDefaultWaitLimitNs;
   p.E = d.E;
   p.F = d.F;
@@ -1022,7 +1175,9 @@ cudaError_t launch_shape(const GemmCall& c, cudaStream_t s) {
       p.n_tiles = static_cast<int>(cdiv(d.D, BN * S::kNacc));
       ok = map2d(&ma, c.a, d.F, R, 64, 64) && map2d(&mb, c.b, d.D, R, 64, 64) &&
            map3d(&mc, c.out0, d.D, d.F, d.E, 64, 32);
-      if (!ok) return cudaErrorInvalidValue;
+      if (!ok || c.tile_ctr == nullptr) return cudaErrorInvalidValue;
+      if (cudaError_t e = cudaMemsetAsync(c.tile_ctr, 0, sizeof(unsigned int), s); e != cudaSuccess)
+        return e;
       return launch_kind<4, S>(ma, mb, mc, mc, p, static_cast<long>(d.E) * p.m_tiles * p.n_tiles,
                                s);
     case GemmKind::kDrhsFc1:
@@ -1032,7 +1187,9 @@ cudaError_t launch_shape(const GemmCall& c, cudaStream_t s) {
       p.n_tiles = static_cast<int>(cdiv(F2, BN * S::kNacc));
       ok = map2d(&ma, c.a, d.D, R, 64, 64) && map2d(&mb, c.b, F2, R, 64, 64) &&
            map3d(&mc, c.out0, F2, d.D, d.E, 64, 32);
-      if (!ok) return cudaErrorInvalidValue;
+      if (!ok || c.tile_ctr == nullptr) return cudaErrorInvalidValue;
+      if (cudaError_t e = cudaMemsetAsync(c.tile_ctr, 0, sizeof(unsigned int), s); e != cudaSuccess)
+        return e;
       return launch_kind<5, S>(ma, mb, mc, mc, p, static_cast<long>(d.E) * p.m_tiles * p.n_tiles,
                                s);
   }

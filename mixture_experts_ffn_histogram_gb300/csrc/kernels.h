@@ -58,7 +58,12 @@ struct GemmCall {
   const void* aux;         // z for the fused SwiGLU backward, or nullptr
   int32_t* dev_status;
   moe_dims d;
+  unsigned int* tile_ctr = nullptr;  // drhs: a device counter for the dynamic tile schedule
 };
+
+// Bytes at the start of `ws` that hold the drhs tile counter; the SwiGLU
+// backward's dz scratch follows them.
+constexpr size_t kWsCounterBytes = 256;
 
 cudaError_t launch_grouped_gemm(const GemmCall& c, cudaStream_t s);
 
