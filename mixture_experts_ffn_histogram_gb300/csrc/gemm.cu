@@ -292,49 +292,114 @@ __device__ __forceinline__ void load3(void* dst, const CUtensorMap* map, uint32_
   if constexpr (CG == 1) tma_load_3d_addr(dst, map, bar, c0, c1, c2);
   else tma_load_3d_pair(dst, map, bar, c0, c1, c2);
 }
+template <int CG>
+__device__ __forceinline__ void load4(void* dst, const CUtensorMap* map, uint32_t bar, int c0,
+                                      int c1, int c2, int c3) {
+  if constexpr (CG == 1) tma_load_4d_addr(dst, map, bar, c0, c1, c2, c3);
+  else tma_load_4d_pair(dst, map, bar, c0, c1, c2, c3);
+}
 
-// TMA loads of one reduction block: this CTA's 128 A rows and its BN/CG B
-// columns (CTA `rank` of the pair takes the rank-th half).
+// MMA width of accumulator `a` of tile T: its valid output columns rounded
+// up to what the B layout allows (whole 64-column chunks per CTA for an
+// MN-major B, 8-row groups per CTA for a K-major B); 0 when the accumulator
+// lies wholly past the last column.  Narrow tail tiles thus cost only their
+// valid columns.  For FC1 the width is that of gate and up together:
+// columns [0, w/2) are gate columns n0.., [w/2, w) up columns F + n0...
+template <int KIND, int BN, int CG>
+__device__ __forceinline__ int acc_cols(const Tile& T, int a, const Params& p) {
+  if constexpr (KIND == static_cast<int>(GemmKind::kFc1)) {
+    return 2 * min(BN / 2, p.N - T.n0);  // p.N = F, a multiple of 64
+  } else {
+    const int nv = min(BN, p.N - (T.n0 + a * BN));
+    if (nv <= 0) return 0;
+    constexpr int g = Traits<KIND, BN, CG>::kBMn ? 64 * CG : 16 * CG;
+    return min(BN, (nv + g - 1) / g * g);
+  }
+}
+
+// Whether accumulator `a` of T is narrower than a full tile in a kind whose B
+// columns, when narrow, come in single 64-wide chunks (the multi-chunk box
+// would put them at the wrong offsets of a pair's halves).
+template <int KIND, int BN, int CG>
+__device__ __forceinline__ bool narrow_chunks(int w) {
+  return (KIND == static_cast<int>(GemmKind::kFc2) || Traits<KIND, BN, CG>::kGroupedK) && w < BN;
+}
+
+// Bytes that one reduction block of tile T brings into ONE CTA's stage.
+template <int KIND, int BN, int CG, int NACC>
+__device__ __forceinline__ uint32_t stage_bytes(const Tile& T, const Params& p) {
+  constexpr int kBChunks = BN / 64 / CG;
+  if constexpr (KIND == static_cast<int>(GemmKind::kDlhsFc2) ||
+                KIND == static_cast<int>(GemmKind::kDlhsFc1)) {
+    return kAStageBytes + (BN / CG) * BK * 2;  // K-major B: one box of BN/CG rows
+  } else if constexpr (KIND == static_cast<int>(GemmKind::kFc1)) {
+    return kAStageBytes + kBChunks * kChunkBytes;  // whole boxes, also for the tail
+  } else {
+    uint32_t chunks = 0;
+#pragma unroll
+    for (int a = 0; a < NACC; ++a) {
+      const int w = acc_cols<KIND, BN, CG>(T, a, p);
+      chunks += narrow_chunks<KIND, BN, CG>(w) ? w / (64 * CG) : kBChunks;
+    }
+    return kAStageBytes + chunks * kChunkBytes;
+  }
+}
+
+// TMA loads of one reduction block: this CTA's 128 A rows and its share of
+// the B columns: of an accumulator w columns wide, CTA `rank` of a pair
+// holds columns [rank*w/2, (rank+1)*w/2), which tcgen05.mma.cta_group::2
+// takes as accumulator columns in that order.  An MN-major operand's 64-wide
+// chunks come in ONE box per operand and accumulator (a map with a chunk
+// dimension of stride 128 bytes): the number of TMA instructions, more than
+// their bytes, limits how fast a stage fills.  Maps: A (map_a), B (map_b),
+// and for narrow fc2/drhs accumulators B in single chunks (map_d).
 template <int KIND, int BN, int CG, int NACC = 1>
 __device__ __forceinline__ void issue_loads(const Tile& T, int kb, int rank, uint8_t* sa,
                                             uint8_t* sb, uint32_t bar, const CUtensorMap* ma,
-                                            const CUtensorMap* mb, const Params& p) {
+                                            const CUtensorMap* mb, const CUtensorMap* md,
+                                            const Params& p) {
   const int k0 = kb * BK;
-  constexpr int kBChunks = BN / 64 / CG;  // 64-wide B chunks held by this CTA
+  constexpr int kBChunks = BN / 64 / CG;  // 64-wide B chunks a CTA holds per accumulator
   if constexpr (KIND == static_cast<int>(GemmKind::kFc1)) {
-    // accumulator columns [0, BN/2) = gate columns n0.., [BN/2, BN) = up columns F + n0..
+    // B = wi[e] as [chunk of 2F][D][64]: for a pair the even CTA takes the
+    // gate chunks n0.., the odd one the up chunks F + n0..; alone, a CTA
+    // takes both (gate in slots [0, kBChunks/2), up after).
     load2<CG>(sa, ma, bar, k0, T.row0);
     if constexpr (CG == 1) {
-#pragma unroll
-      for (int j = 0; j < kBChunks / 2; ++j) {
-        load3<CG>(sb + j * kChunkBytes, mb, bar, T.n0 + 64 * j, k0, T.e);
-        load3<CG>(sb + (kBChunks / 2 + j) * kChunkBytes, mb, bar, p.F + T.n0 + 64 * j, k0, T.e);
-      }
+      load4<CG>(sb, mb, bar, 0, k0, T.n0 / 64, T.e);
+      load4<CG>(sb + (kBChunks / 2) * kChunkBytes, mb, bar, 0, k0, (p.F + T.n0) / 64, T.e);
     } else {
-      const int base = rank == 0 ? T.n0 : p.F + T.n0;
-#pragma unroll
-      for (int j = 0; j < kBChunks; ++j)
-        load3<CG>(sb + j * kChunkBytes, mb, bar, base + 64 * j, k0, T.e);
+      load4<CG>(sb, mb, bar, 0, k0, (rank == 0 ? T.n0 : p.F + T.n0) / 64, T.e);
     }
   } else if constexpr (KIND == static_cast<int>(GemmKind::kFc2)) {
+    const int w = acc_cols<KIND, BN, CG>(T, 0, p);
     load2<CG>(sa, ma, bar, k0, T.row0);
-#pragma unroll
-    for (int j = 0; j < kBChunks; ++j)
-      load3<CG>(sb + j * kChunkBytes, mb, bar, T.n0 + (BN / CG) * rank + 64 * j, k0, T.e);
+    if (!narrow_chunks<KIND, BN, CG>(w)) {
+      load4<CG>(sb, mb, bar, 0, k0, (T.n0 + (BN / CG) * rank) / 64, T.e);
+    } else {
+      for (int j = 0; j < w / (64 * CG); ++j)
+        load3<CG>(sb + j * kChunkBytes, md, bar, T.n0 + (w / CG) * rank + 64 * j, k0, T.e);
+    }
   } else if constexpr (KIND == static_cast<int>(GemmKind::kDlhsFc2) ||
                        KIND == static_cast<int>(GemmKind::kDlhsFc1)) {
+    const int w = acc_cols<KIND, BN, CG>(T, 0, p);
     load2<CG>(sa, ma, bar, k0, T.row0);
-    load3<CG>(sb, mb, bar, k0, T.n0 + (BN / CG) * rank, T.e);  // K-major B rows
+    load3<CG>(sb, mb, bar, k0, T.n0 + (w / CG) * rank, T.e);  // K-major B rows
   } else {
+    // A = [chunk of M][R][64], B = [chunk of N][R][64]
     const int kr = T.row0 + k0;
-    load2<CG>(sa, ma, bar, T.m0, kr);
-    load2<CG>(sa + kChunkBytes, ma, bar, T.m0 + 64, kr);
+    load3<CG>(sa, ma, bar, 0, kr, T.m0 / 64);
 #pragma unroll
-    for (int a = 0; a < NACC; ++a)
-#pragma unroll
-      for (int j = 0; j < kBChunks; ++j)
-        load2<CG>(sb + (a * kBChunks + j) * kChunkBytes, mb, bar,
-                  T.n0 + a * BN + (BN / CG) * rank + 64 * j, kr);
+    for (int a = 0; a < NACC; ++a) {
+      const int w = acc_cols<KIND, BN, CG>(T, a, p);
+      uint8_t* sba = sb + a * kBChunks * kChunkBytes;
+      if (!narrow_chunks<KIND, BN, CG>(w)) {
+        load3<CG>(sba, mb, bar, 0, kr, (T.n0 + a * BN + (BN / CG) * rank) / 64);
+      } else {
+        for (int j = 0; j < w / (64 * CG); ++j)
+          load2<CG>(sba + j * kChunkBytes, md, bar, T.n0 + a * BN + (w / CG) * rank + 64 * j, kr);
+      }
+    }
   }
 }
 
@@ -505,6 +570,7 @@ __device__ __forceinline__ void epilogue_tile(const Tile& T, uint32_t tbase, Epi
     const long r = static_cast<long>(y) + lane;
     if constexpr (KIND == static_cast<int>(GemmKind::kFc1)) {
       const bool with_z = p.out1 != nullptr;
+      const int hw = acc_cols<KIND, BN, CG>(T, 0, p) / 2;  // first up column of the accumulator
       for (int ch = 0; ch < BN / 128; ++ch) {
         const int f0 = T.n0 + 64 * ch;
         if (f0 >= p.F) break;
@@ -514,7 +580,7 @@ __device__ __forceinline__ void epilogue_tile(const Tile& T, uint32_t tbase, Epi
         for (int h = 0; h < 2; ++h) {
           uint32_t u[32];
           tmem_ld_32x32b_x32(tbase + 64 * ch + 32 * h, v);
-          tmem_ld_32x32b_x32(tbase + BN / 2 + 64 * ch + 32 * h, u);
+          tmem_ld_32x32b_x32(tbase + hw + 64 * ch + 32 * h, u);
           tmem_ld_wait();
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
@@ -743,6 +809,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_map(&map_a);
     tma_prefetch_map(&map_b);
     tma_prefetch_map(&map_c);
+    tma_prefetch_map(&map_d);
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&s.full[i], 1);
       mbar_init(&s.empty[i], 1);
@@ -832,6 +899,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (t >= ntiles) break;
         const Tile T = decode_tile<KIND, BNT, CG>(t, rank, p, s);
+        const uint32_t tx_bytes = stage_bytes<KIND, BN, CG, NACC>(T, p) * CG;
         bool next_claimed = !(kDyn && leader);
         for (int kb = 0; kb < T.kb; ++kb) {
           if (!next_claimed && kb + 2 >= T.kb) {
@@ -840,10 +908,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (!mbar_wait(&s.empty[stage], phase ^ 1u, wc)) { aborted = true; break; }
           uint8_t* sa = ring + stage * kStageBytes;
-          if (leader) mbar_arrive_expect_tx(&s.full[stage], kStageBytes * CG);
+          if (leader) mbar_arrive_expect_tx(&s.full[stage], tx_bytes);
           issue_loads<KIND, BN, CG, NACC>(T, kb, rank, sa, sa + kAStageBytes,
-                                    full0 + stage * static_cast<uint32_t>(sizeof(uint64_t)),
-                                    &map_a, &map_b, p);
+                                          full0 + stage * static_cast<uint32_t>(sizeof(uint64_t)),
+                                          &map_a, &map_b, &map_d, p);
           ++fills[stage];
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
@@ -881,6 +949,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * S::kAccStride;
+        // a lone CTA's narrow FC1 tile reads the first gate and the first up
+        // chunk, which the boxes left two chunks apart
+        const uint32_t b_lbo = (KIND == static_cast<int>(GemmKind::kFc1) && CG == 1 &&
+                                acc_cols<KIND, BN, CG>(T, 0, p) < BN)
+                                   ? 2 * kChunkBytes
+                                   : kChunkBytes;
+        uint32_t idesc[NACC];  // instruction descriptors with each accumulator's MMA width
+#pragma unroll
+        for (int a = 0; a < NACC; ++a)
+          idesc[a] = (Tr::kIdesc & ~(0x3Fu << 17)) |
+                     (static_cast<uint32_t>(acc_cols<KIND, BN, CG>(T, a, p) >> 3) << 17);
         for (int kb = 0; kb < T.kb; ++kb) {
           if (!__all_sync(0xffffffffu, mbar_wait(&s.full[stage], phase, wc))) {
             aborted = true;
@@ -909,11 +988,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                                       : smem_desc_sw128(a_addr + kk * 32, 16, 1024);
 #pragma unroll
               for (int a = 0; a < NACC; ++a) {
+                if (a > 0 && (idesc[a] & (0x3Fu << 17)) == 0) break;  // nothing valid
                 const uint32_t b_acc = b_addr + a * (BN / CG) * BK * 2;
-                const uint64_t bd = Tr::kBMn
-                                        ? smem_desc_sw128(b_acc + kk * 2048, kChunkBytes, 1024)
-                                        : smem_desc_sw128(b_acc + kk * 32, 16, 1024);
-                umma_bf16<CG>(d_tmem + a * BN, ad, bd, Tr::kIdesc, (kb > 0 || kk > 0) ? 1u : 0u);
+                const uint64_t bd = Tr::kBMn ? smem_desc_sw128(b_acc + kk * 2048, b_lbo, 1024)
+                                             : smem_desc_sw128(b_acc + kk * 32, 16, 1024);
+                umma_bf16<CG>(d_tmem + a * BN, ad, bd, idesc[a], (kb > 0 || kk > 0) ? 1u : 0u);
               }
             }
             umma_commit<CG>(&s.empty[stage]);
@@ -1023,8 +1102,8 @@ bool make_map(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
               const uint64_t* strides, const uint32_t* box) {
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return false;
-  cuuint64_t gd[3], gs[2];
-  cuuint32_t bd[3], es[3] = {1, 1, 1};
+  cuuint64_t gd[4], gs[3];
+  cuuint32_t bd[4], es[4] = {1, 1, 1, 1};
   for (int i = 0; i < rank; ++i) {
     gd[i] = dims[i];
     bd[i] = box[i];
@@ -1049,6 +1128,20 @@ bool map3d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t mid, uint6
   const uint64_t strides[2] = {inner * 2, inner * mid * 2};
   const uint32_t box[3] = {box_inner, box_mid, 1};
   return make_map(m, base, 3, dims, strides, box);
+}
+
+// An MN-major operand [outer][rows][inner] (inner contiguous, a multiple of
+// 64) seen as [outer][inner/64][rows][64]: one box of `box_chunks` 64-wide
+// chunks x 64 rows lands as consecutive 8 KB chunks, the layout the MMA
+// descriptors expect.  Dims (innermost first): 64, rows, chunks[, outer].
+// The map's rank must match the load instruction: 4 for the per-expert
+// weights (loaded with 4-D coordinates even when E = 1), 3 for a 2-D operand.
+bool map_chunks(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint64_t outer,
+                uint32_t box_chunks, int rank) {
+  const uint64_t dims[4] = {64, rows, inner / 64, outer};
+  const uint64_t strides[3] = {inner * 2, 128, inner * rows * 2};
+  const uint32_t box[4] = {64, 64, box_chunks, 1};
+  return make_map(m, base, rank, dims, strides, box);
 }
 
 template <int KIND, class S>
@@ -1128,7 +1221,8 @@ cudaError_t launch_shape(const GemmCall& c, cudaStream_t s) {
               p.Kdim = d.D;
               p.N = d.F;
               p.n_tiles = static_cast<int>(cdiv(d.F, BN / 2));
-              ok = map2d(&ma, c.a, d.D, R, 64, BM) && map3d(&mb, c.b, F2, d.D, d.E, 64, 64) &&
+              ok = map2d(&ma, c.a, d.D, R, 64, BM) &&
+                   map_chunks(&mb, c.b, F2, d.D, d.E, BN / 64 / 2, 4) &&
                    map2d(&mc, c.out0, d.F, R, 64, 32);
               if (ok) ok = (c.out1 != nullptr) ? map2d(&md, c.out1, F2, R, 64, 32) : (md = mc, true);
               if (!ok) return cudaErrorInvalidValue;
@@ -1139,10 +1233,11 @@ cudaError_t launch_shape(const GemmCall& c, cudaStream_t s) {
             p.Kdim = d.F;
             p.N = d.D;
             p.n_tiles = static_cast<int>(cdiv(d.D, BN));
-            ok = map2d(&ma, c.a, d.F, R, 64, BM) && map3d(&mb, c.b, d.D, d.F, d.E, 64, 64) &&
-                 map2d(&mc, c.out0, d.D, R, 64, 32);
+            ok = map2d(&ma, c.a, d.F, R, 64, BM) &&
+                 map_chunks(&mb, c.b, d.D, d.F, d.E, BN / 64 / CG, 4) &&
+                 map2d(&mc, c.out0, d.D, R, 64, 32) && map3d(&md, c.b, d.D, d.F, d.E, 64, 64);
             if (!ok) return cudaErrorInvalidValue;
-            return launch_kind<1, S>(ma, mb, mc, mc, p, row_blocks_bound * p.n_tiles, s);
+            return launch_kind<1, S>(ma, mb, mc, md, p, row_blocks_bound * p.n_tiles, s);
           case GemmKind::kDlhsFc2:
             if constexpr (S::kRing >= 2) {  // dgate and dup are staged together
               p.Kdim = d.D;
@@ -1173,24 +1268,24 @@ cudaError_t launch_shape(const GemmCall& c, cudaStream_t s) {
       p.N = d.D;
       p.m_tiles = static_cast<int>(cdiv(d.F, BM * CG));
       p.n_tiles = static_cast<int>(cdiv(d.D, BN * S::kNacc));
-      ok = map2d(&ma, c.a, d.F, R, 64, 64) && map2d(&mb, c.b, d.D, R, 64, 64) &&
-           map3d(&mc, c.out0, d.D, d.F, d.E, 64, 32);
+      ok = map_chunks(&ma, c.a, d.F, R, 1, 2, 3) && map_chunks(&mb, c.b, d.D, R, 1, BN / 64 / CG, 3) &&
+           map3d(&mc, c.out0, d.D, d.F, d.E, 64, 32) && map2d(&md, c.b, d.D, R, 64, 64);
       if (!ok || c.tile_ctr == nullptr) return cudaErrorInvalidValue;
       if (cudaError_t e = cudaMemsetAsync(c.tile_ctr, 0, sizeof(unsigned int), s); e != cudaSuccess)
         return e;
-      return launch_kind<4, S>(ma, mb, mc, mc, p, static_cast<long>(d.E) * p.m_tiles * p.n_tiles,
+      return launch_kind<4, S>(ma, mb, mc, md, p, static_cast<long>(d.E) * p.m_tiles * p.n_tiles,
                                s);
     case GemmKind::kDrhsFc1:
       p.M = d.D;
       p.N = 2 * d.F;
       p.m_tiles = static_cast<int>(cdiv(d.D, BM * CG));
       p.n_tiles = static_cast<int>(cdiv(F2, BN * S::kNacc));
-      ok = map2d(&ma, c.a, d.D, R, 64, 64) && map2d(&mb, c.b, F2, R, 64, 64) &&
-           map3d(&mc, c.out0, F2, d.D, d.E, 64, 32);
+      ok = map_chunks(&ma, c.a, d.D, R, 1, 2, 3) && map_chunks(&mb, c.b, F2, R, 1, BN / 64 / CG, 3) &&
+           map3d(&mc, c.out0, F2, d.D, d.E, 64, 32) && map2d(&md, c.b, F2, R, 64, 64);
       if (!ok || c.tile_ctr == nullptr) return cudaErrorInvalidValue;
       if (cudaError_t e = cudaMemsetAsync(c.tile_ctr, 0, sizeof(unsigned int), s); e != cudaSuccess)
         return e;
-      return launch_kind<5, S>(ma, mb, mc, mc, p, static_cast<long>(d.E) * p.m_tiles * p.n_tiles,
+      return launch_kind<5, S>(ma, mb, mc, md, p, static_cast<long>(d.E) * p.m_tiles * p.n_tiles,
                                s);
   }
   return cudaErrorInvalidValue;
