@@ -169,6 +169,88 @@ def peaks():
 
 
 # ------------------------------------------------------------------ clocks
+class NvmlSampler:
+    """Samples the SM clock and the clock-event (throttle) reasons through
+    NVML every few milliseconds while the timed region runs; read-only (no
+    NVML call here changes a setting).  `ok` is False when NVML cannot be
+    loaded, and the nvidia-smi sampler below is used instead."""
+    REASONS = {0x8: "hw_slowdown", 0x40: "hw_thermal_slowdown", 0x20: "sw_thermal_slowdown",
+               0x4: "sw_power_cap", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, dev: torch.device, period_s: float = 0.004):
+        import ctypes
+        self.period = period_s
+        self.samples = []
+        self.ok = False
+        try:
+            L = ctypes.CDLL("libnvidia-ml.so.1")
+            if L.nvmlInit_v2() != 0:
+                return
+            h = ctypes.c_void_p()
+            found = False
+            props = torch.cuda.get_device_properties(dev)
+            bus = getattr(props, "pci_bus_id", None)
+            if bus is not None:
+                pci = "%08x:%02x:%02x.0" % (getattr(props, "pci_domain_id", 0), bus,
+                                             getattr(props, "pci_device_id", 0))
+                found = L.nvmlDeviceGetHandleByPciBusId_v2(pci.encode(), ctypes.byref(h)) == 0
+            if not found:
+                found = L.nvmlDeviceGetHandleByIndex_v2(dev.index or 0, ctypes.byref(h)) == 0
+            if not found:
+                return
+            self.L, self.h, self.ct = L, h, ctypes
+            mx = ctypes.c_uint()
+            self.max_mhz = float(mx.value) if L.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0 else None
+            self.reasons_fn = getattr(L, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                getattr(L, "nvmlDeviceGetCurrentClocksThrottleReasons")
+            self.ok = self._read() is not None
+        except (OSError, AttributeError):
+            self.ok = False
+
+    def _read(self):
+        c, r = self.ct.c_uint(), self.ct.c_ulonglong()
+        if self.L.nvmlDeviceGetClockInfo(self.h, 1, self.ct.byref(c)) != 0:
+            return None
+        if self.reasons_fn(self.h, self.ct.byref(r)) != 0:
+            return None
+        return float(c.value), int(r.value)
+
+    def _loop(self):
+        while not self._stop:
+            v = self._read()
+            if v is not None:
+                self.samples.append(v)
+            time.sleep(self.period)
+
+    def __enter__(self):
+        import threading
+        self._stop = False
+        self._thread = threading.Thread(target=self._loop, daemon=True)
+        self._thread.start()
+        return self
+
+    def __exit__(self, *a):
+        self._stop = True
+        self._thread.join(timeout=2)
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["unsampled"]}
+        reasons = set()
+        for _, bits in self.samples:
+            for bit, name in self.REASONS.items():
+                if bits & bit:
+                    reasons.add(name)
+        sm = [c for c, _ in self.samples]
+        return {"sm_mhz": statistics.median(sm), "sm_min_mhz": min(sm), "sm_max_mhz": self.max_mhz,
+                "reasons": sorted(reasons), "samples": len(sm), "source": "nvml"}
+
+
+def clock_sampler(dev: torch.device):
+    s = NvmlSampler(dev)
+    return s if s.ok else ClockSampler(dev.index)
+
+
 class ClockSampler:
     """Samples SM clock and throttle reasons with nvidia-smi while the timed
     region runs (started, and seen producing samples, before the region)."""
@@ -336,7 +418,7 @@ def run_ours(args, dist, rank, world):
     # ---- timed region: K steps, events around every launch
     barrier(dist)
     torch.cuda.synchronize()
-    with ClockSampler(dev.index) as clk:
+    with clock_sampler(dev) as clk:
         start = torch.cuda.Event(enable_timing=True)
         end = torch.cuda.Event(enable_timing=True)
         start.record()
