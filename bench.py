@@ -521,44 +521,48 @@ def run_ours(args, dist, rank, world):
 
 
 def measure_e2e(step, inp, args, dist, fwd_only):
-    """The same steps with the step's activations copied in from pinned host
-    memory and the block's outputs copied back, inside the timed region."""
+    """The same steps through the block's host-memory API (HostPipeline):
+    every step's activations are copied in from pinned host memory and its
+    outputs (out, and dx when training) copied back inside the timed region,
+    with the copies overlapped with the kernels of neighbouring steps."""
+    from mixture_experts_ffn_histogram_gb300.block import HostPipeline
     wl = step.wl
-    host_x = inp["x"].cpu().pin_memory()
-    host_logits = inp["logits"].cpu().pin_memory() if inp["logits"] is not None else None
-    host_dy = inp["dy"].cpu().pin_memory() if not fwd_only else None
-    dx_ = torch.empty_like(inp["x"])
-    dl_ = torch.empty_like(inp["logits"]) if host_logits is not None else None
-    ddy = torch.empty_like(inp["dy"]) if host_dy is not None else None
+    given = step.blk.mode == step.B.SCORE_GIVEN
+    pin = lambda t: t.cpu().pin_memory()  # noqa: E731
+    host = {"x_h": pin(inp["x"])}
+    if given:
+        host["ids_h"], host["w_h"] = pin(inp["ids"]), pin(inp["w"])
+    else:
+        host["logits_h"] = pin(inp["logits"])
+    if not fwd_only:
+        host["dy_h"] = pin(inp["dy"])
     out_h = torch.empty_like(step.blk.out, device="cpu").pin_memory()
-    dx_h = torch.empty_like(step.blk.out, device="cpu").pin_memory() if not fwd_only else None
-    h2d = host_x.numel() * 2 + (host_logits.numel() * 4 if host_logits is not None else 0) + \
-        (host_dy.numel() * 2 if host_dy is not None else 0)
+    dx_h = None if fwd_only else torch.empty_like(step.blk.out, device="cpu").pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = out_h.numel() * 2 + (dx_h.numel() * 2 if dx_h is not None else 0)
+    pipe = HostPipeline(step.blk, inp["wi"], inp["wo"], inp["bias"])
 
     def one():
-        dx_.copy_(host_x, non_blocking=True)
-        if dl_ is not None:
-            dl_.copy_(host_logits, non_blocking=True)
-        if ddy is not None:
-            ddy.copy_(host_dy, non_blocking=True)
-        step.run(x=dx_, logits=dl_, dy=ddy)
-        out_h.copy_(step.blk.out, non_blocking=True)
-        if dx_h is not None:
-            dx_h.copy_(step.blk.dx, non_blocking=True)
+        pipe.step(out_h=out_h, dx_h=dx_h, **host)
 
     for _ in range(2):
         one()
+    pipe.synchronize()
     torch.cuda.synchronize()
     barrier(dist)
     t0 = time.perf_counter()
     for _ in range(args.steps):
         one()
-    torch.cuda.synchronize()
+    pipe.synchronize()
     el = max_over_ranks(dist, time.perf_counter() - t0)
+    status = int(step.blk.status.item())
+    if status != 0:
+        raise RuntimeError(f"device status {status} after the end-to-end steps")
     world = int(os.environ.get("WORLD_SIZE", "1"))
     return {"value": world * wl.T * args.steps / el, "unit": "tokens/s",
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "copies": "overlapped with neighbouring steps' kernels (upload, compute and "
+                      "download streams)"}
 
 
 # ------------------------------------------------------ oracle (CPU) arm

@@ -76,3 +76,95 @@ class MoEBlock:
                                           self.dxs, self.dwi, self.status, self.ws, d, stream)
         B.moe_permute_bwd(self.dxs, self.pos, self.dx, d, stream)
         return self.dx
+
+
+class HostPipeline:
+    """Steps of a MoEBlock (fwd+bwd when the block trains, else forward only)
+    whose per-step activations live in pinned host memory, with the
+    host<->device copies overlapped with the kernels.
+
+    Step i's inputs (x, dy, and logits or ids/w) go up on an upload stream
+    into one of two device slots while step i-1 computes; step i's `out` goes
+    down on a download stream while its backward (or step i+1) runs, and its
+    `dx` while step i+1 runs.  Ordering comes from CUDA events only (no host
+    sync):
+    - an upload into a slot waits until the step that last used it is done;
+    - a step waits for its upload, and its forward (backward) waits until the
+      previous `out` (`dx`) download has read the block's buffer.
+    Every step still moves all of its bytes across the host link; only the
+    waiting is hidden.  `synchronize()` waits for the last download.
+    """
+
+    def __init__(self, blk: MoEBlock, wi, wo, bias=None):
+        self.blk, self.wi, self.wo, self.bias = blk, wi, wo, bias
+        self.train = blk.train
+        dev = blk.out.device
+        self.compute = torch.cuda.Stream(dev)
+        self.up = torch.cuda.Stream(dev)
+        self.down = torch.cuda.Stream(dev)
+        T, D, E, K = blk.T, blk.D, blk.E, blk.K
+        given = blk.mode == B.SCORE_GIVEN
+        self.slots = []
+        for _ in range(2):
+            self.slots.append({
+                "x": torch.empty((T, D), dtype=torch.bfloat16, device=dev),
+                "dy": torch.empty((T, D), dtype=torch.bfloat16, device=dev) if self.train else None,
+                "logits": None if given else torch.empty((T, E), dtype=torch.float32, device=dev),
+                "ids": torch.empty((T, K), dtype=torch.int32, device=dev) if given else None,
+                "w": torch.empty((T, K), dtype=torch.float32, device=dev) if given else None,
+            })
+        self.slot_free = [None, None]   # event: the last step using the slot is done
+        self.out_read = None            # event: the last `out` download has read blk.out
+        self.dx_read = None             # event: the last `dx` download has read blk.dx
+        self.i = 0
+
+    def step(self, x_h, out_h, dy_h=None, dx_h=None, logits_h=None, ids_h=None, w_h=None):
+        """Queues one step: inputs from the pinned host tensors, `out` (and,
+        training, `dx`) into the pinned host tensors `out_h` (`dx_h`), valid
+        after the next synchronize()."""
+        blk, k = self.blk, self.i % 2
+        s = self.slots[k]
+        with torch.cuda.stream(self.up):
+            if self.slot_free[k] is not None:
+                self.up.wait_event(self.slot_free[k])
+            s["x"].copy_(x_h, non_blocking=True)
+            if self.train:
+                s["dy"].copy_(dy_h, non_blocking=True)
+            if s["logits"] is not None:
+                s["logits"].copy_(logits_h, non_blocking=True)
+            else:
+                s["ids"].copy_(ids_h, non_blocking=True)
+                s["w"].copy_(w_h, non_blocking=True)
+            uploaded = torch.cuda.Event()
+            uploaded.record(self.up)
+        with torch.cuda.stream(self.compute):
+            self.compute.wait_event(uploaded)
+            if self.out_read is not None:
+                self.compute.wait_event(self.out_read)
+            blk.forward(s["x"], self.wi, self.wo, logits=s["logits"], bias=self.bias,
+                        ids=s["ids"], w=s["w"])
+            fwd_done = torch.cuda.Event()
+            fwd_done.record(self.compute)
+            done = fwd_done
+            if self.train:
+                if self.dx_read is not None:
+                    self.compute.wait_event(self.dx_read)
+                blk.backward(s["dy"], self.wi, self.wo)
+                done = torch.cuda.Event()
+                done.record(self.compute)
+        self.slot_free[k] = done
+        with torch.cuda.stream(self.down):
+            self.down.wait_event(fwd_done)
+            out_h.copy_(blk.out, non_blocking=True)
+            self.out_read = torch.cuda.Event()
+            self.out_read.record(self.down)
+            if self.train:
+                self.down.wait_event(done)
+                dx_h.copy_(blk.dx, non_blocking=True)
+                self.dx_read = torch.cuda.Event()
+                self.dx_read.record(self.down)
+        self.i += 1
+
+    def synchronize(self):
+        self.down.synchronize()
+        self.compute.synchronize()
