@@ -1305,15 +1305,29 @@ using Shape2Dz = Shape<256, 4, 2, 2, 1>;
 
 // Whether a grouped GEMM runs on CTA pairs.  The pair's 256-row block is the
 // unit of rows for the forward and dlhs GEMMs, so pairs pay off when groups
-// are long; drhs tiles are over output rows (F or D), where the pair loses
-// nothing.  MOE_GEMM_PAIR=0/1 forces the choice.
+// are long.  drhs tiles reduce over their group's rows: with short groups
+// (a few 64-row blocks per tile) a tile is mostly epilogue, and single CTAs
+// with double-buffered accumulators do best (E=256 experts of ~256 rows: FC1
+// drhs 4.9 ms alone, 5.1 ms as 256-wide pairs, 5.3 ms as 512-wide pairs);
+// with long groups, 512-wide pair tiles do (E=128 of ~2048 rows: the step
+// takes 7.73 ms with them, 8.07 ms with 256-wide pair tiles).
+// MOE_GEMM_PAIR=0/1 forces the choice.
 bool use_pairs(const GemmCall& c) {
   const char* env = std::getenv("MOE_GEMM_PAIR");
   if (env != nullptr && env[0] == '0') return false;
   if (env != nullptr && env[0] == '1') return true;
-  if (c.kind == GemmKind::kDrhsFc2 || c.kind == GemmKind::kDrhsFc1) return true;
   const long R = static_cast<long>(c.d.T) * c.d.K;
   return R / c.d.E >= 1024;
+}
+
+// Whether drhs tiles on pairs are 512 columns wide (two accumulators, one
+// TMEM slot) rather than 256 (double-buffered).  MOE_GEMM_WIDE=0/1 forces it.
+bool wide_drhs(const GemmCall& c) {
+  const char* env = std::getenv("MOE_GEMM_WIDE");
+  if (env != nullptr && env[0] == '0') return false;
+  if (env != nullptr && env[0] == '1') return true;
+  (void)c;
+  return true;
 }
 
 }  // namespace
@@ -1332,7 +1346,7 @@ cudaError_t launch_grouped_gemm(const GemmCall& c, cudaStream_t s) {
   const bool dz = (c.kind == GemmKind::kDlhsFc2 && c.aux != nullptr);
   if (!use_pairs(c)) return dz ? launch_shape<Shape1Dz>(c, s) : launch_shape<Shape1>(c, s);
   if (c.kind == GemmKind::kDrhsFc2 || c.kind == GemmKind::kDrhsFc1)
-    return launch_shape<Shape2Drhs>(c, s);
+    return wide_drhs(c) ? launch_shape<Shape2Drhs>(c, s) : launch_shape<Shape2>(c, s);
   if (c.kind == GemmKind::kFc1) return launch_shape<Shape2Fc1>(c, s);
   return dz ? launch_shape<Shape2Dz>(c, s) : launch_shape<Shape2>(c, s);
 }

@@ -37,14 +37,16 @@ def _gpu():
 
 
 # The grouped GEMMs run either one CTA per tile or on CTA pairs (a 2-CTA
-# cluster sharing one 256-row tile); MOE_GEMM_PAIR forces the path so that
-# both are checked on every shape.
-PAIR_MODES = pytest.mark.parametrize("pair", ["0", "1"], ids=["cta1", "cta2"])
+# cluster sharing one 256-row tile), and drhs pair tiles are 512 or 256
+# columns wide; MOE_GEMM_PAIR and MOE_GEMM_WIDE force the path so that every
+# one is checked on every shape.
+PAIR_MODES = pytest.mark.parametrize("pair", ["0", "1", "1n"], ids=["cta1", "cta2", "cta2narrow"])
 
 
 @pytest.fixture
 def pair_env(monkeypatch, pair):
-    monkeypatch.setenv("MOE_GEMM_PAIR", pair)
+    monkeypatch.setenv("MOE_GEMM_PAIR", pair[0])
+    monkeypatch.setenv("MOE_GEMM_WIDE", "0" if pair.endswith("n") else "1")
     return pair
 
 
