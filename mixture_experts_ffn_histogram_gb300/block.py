@@ -168,3 +168,41 @@ class HostPipeline:
     def synchronize(self):
         self.down.synchronize()
         self.compute.synchronize()
+
+
+class GraphStep:
+    """One step of a MoEBlock (forward, plus backward when `dy` is given)
+    captured once into a CUDA graph and replayed with `replay()`.
+
+    The graph holds the block's launches with the device addresses of the
+    tensors passed here, so a caller feeds new data by writing into those
+    same tensors (x, logits or ids/w, dy) before each replay; outputs land in
+    the block's buffers (blk.out, blk.dx, ...).  Replaying one graph costs
+    one launch on the host instead of one per kernel, which is what small
+    steps (a few thousand tokens) are bound by.  The constructor runs the
+    step once uncaptured first, so that the library's once-per-process setup
+    (SM count, driver entry point, occupancy queries) happens outside the
+    capture.
+    """
+
+    def __init__(self, blk: MoEBlock, x, wi, wo, logits=None, bias=None, ids=None, w=None,
+                 dy=None):
+        self.blk = blk
+        self.args = (x, wi, wo, logits, bias, ids, w, dy)
+        side = torch.cuda.Stream(blk.out.device)
+        side.wait_stream(torch.cuda.current_stream(blk.out.device))
+        with torch.cuda.stream(side):
+            self._run()
+        torch.cuda.current_stream(blk.out.device).wait_stream(side)
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            self._run()
+
+    def _run(self):
+        x, wi, wo, logits, bias, ids, w, dy = self.args
+        self.blk.forward(x, wi, wo, logits=logits, bias=bias, ids=ids, w=w)
+        if dy is not None:
+            self.blk.backward(dy, wi, wo)
+
+    def replay(self):
+        self.graph.replay()

@@ -42,6 +42,7 @@
 // block, N block) with the group's rows as the reduction.
 #include <cuda.h>
 
+#include <atomic>
 #include <cstdlib>
 #include <mutex>
 
@@ -1149,9 +1150,18 @@ cudaError_t launch_kind(const CUtensorMap& ma, const CUtensorMap& mb, const CUte
                         const CUtensorMap& md, const Params& p, long max_units, cudaStream_t s) {
   auto kern = grouped_gemm_kernel<KIND, S>;
   constexpr size_t bytes = S::kSmemBytes;
-  cudaError_t err =
-      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  // the shared-memory opt-in is set once per device (not on every launch, so
+  // that launches being captured into a CUDA graph make no such call)
+  static std::atomic<bool> attr_set[64];
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!attr_set[dev].load(std::memory_order_acquire)) {
+    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (err != cudaSuccess) return err;
+    attr_set[dev].store(true, std::memory_order_release);
+  }
   long units = sm_count() / S::CG;
   if (max_units < units) units = max_units;
   if (units <= 0) return cudaSuccess;
@@ -1304,20 +1314,23 @@ using Shape1Dz = Shape<256, 3, 1, 2, 1>;
 using Shape2Dz = Shape<256, 4, 2, 2, 1>;
 
 // Whether a grouped GEMM runs on CTA pairs.  The pair's 256-row block is the
-// unit of rows for the forward and dlhs GEMMs, so pairs pay off when groups
-// are long.  drhs tiles reduce over their group's rows: with short groups
-// (a few 64-row blocks per tile) a tile is mostly epilogue, and single CTAs
-// with double-buffered accumulators do best (E=256 experts of ~256 rows: FC1
+// unit of rows for the forward and dlhs GEMMs; pairs pay off from ~256 rows
+// per group (2048 tokens, E=128, top-8: 128 rows, FC1 167 us alone, 176 us
+// on pairs; 4096 tokens: 226 vs 223 us; 8192 tokens: 352 vs 333 us).  drhs
+// tiles reduce over their group's rows: with short groups (a few 64-row
+// blocks per tile) a tile is mostly epilogue, and single CTAs with
+// double-buffered accumulators do best (E=256 experts of ~256 rows: FC1
 // drhs 4.9 ms alone, 5.1 ms as 256-wide pairs, 5.3 ms as 512-wide pairs);
-// with long groups, 512-wide pair tiles do (E=128 of ~2048 rows: the step
-// takes 7.73 ms with them, 8.07 ms with 256-wide pair tiles).
+// from ~1024 rows per group 512-wide pair tiles do (E=128 of ~2048 rows:
+// the step takes 7.73 ms with them, 8.07 ms with 256-wide pair tiles).
 // MOE_GEMM_PAIR=0/1 forces the choice.
 bool use_pairs(const GemmCall& c) {
   const char* env = std::getenv("MOE_GEMM_PAIR");
   if (env != nullptr && env[0] == '0') return false;
   if (env != nullptr && env[0] == '1') return true;
-  const long R = static_cast<long>(c.d.T) * c.d.K;
-  return R / c.d.E >= 1024;
+  const long rows_per_group = static_cast<long>(c.d.T) * c.d.K / c.d.E;
+  const bool drhs = c.kind == GemmKind::kDrhsFc2 || c.kind == GemmKind::kDrhsFc1;
+  return rows_per_group >= (drhs ? 1024 : 256);
 }
 
 // Whether drhs tiles on pairs are 512 columns wide (two accumulators, one
