@@ -462,7 +462,8 @@ def run_ours(args, dist, rank, world):
     for n in step.names:
         ts = step.times[n]
         avg = sum(ts) / len(ts)
-        per_kernel[n] = {"avg_us": avg * 1e6, "share": sum(ts) / max(1e-12, sum(sum(v) for v in step.times.values()))}
+        per_kernel[n] = {"avg_us": avg * 1e6, "median_us": statistics.median(ts) * 1e6,
+                         "share": sum(ts) / max(1e-12, sum(sum(v) for v in step.times.values()))}
         if n in ("fc1", "fc2", "fc2_dlhs", "fc2_drhs", "fc1_dlhs", "fc1_drhs"):
             fl = gemm_flops(n, wl.R, wl.D, wl.F)
             per_kernel[n]["tflops"] = fl / avg / 1e12
