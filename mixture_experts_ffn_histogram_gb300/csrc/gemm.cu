@@ -533,8 +533,7 @@ __device__ __forceinline__ void z_request(const Tile& T, int ch, EpiCtx<RING>& c
     const int y = T.row0 + 32 * c.q;
     const uint32_t bar = smem_u32(c.zbar);
     mbar_arrive_expect_tx(c.zbar, 2 * kBufBytes);
-    tma_load_2d_addr(c.zbuf, c.map_d, bar, f0, y);
-    tma_load_2d_addr(c.zbuf + kBufBytes, c.map_d, bar, p.F + f0, y);
+    tma_load_3d_addr(c.zbuf, c.map_d, bar, f0, y, 0);  // gate chunk, then up chunk
   }
 }
 
@@ -611,10 +610,7 @@ __device__ __forceinline__ void epilogue_tile(const Tile& T, uint32_t tbase, Epi
         if (full) {
           publish();
           flush_2d(hb, c.map_c, f0, y, lane);
-          if (with_z) {
-            flush_2d(c.ring.after(hb, 1), c.map_d, f0, y, lane);
-            flush_2d(c.ring.after(hb, 2), c.map_d, p.F + f0, y, lane);
-          }
+          if (with_z) flush_3d(c.ring.after(hb, 1), c.map_d, f0, y, 0, lane);  // zg, zu
         }
       }
     } else if constexpr (KIND == static_cast<int>(GemmKind::kDlhsFc2)) {
@@ -667,8 +663,7 @@ __device__ __forceinline__ void epilogue_tile(const Tile& T, uint32_t tbase, Epi
             put_half(c.ring.after(gb, 1), lane, h, wu);
           }
           publish();
-          flush_2d(gb, c.map_c, f0, y, lane);
-          flush_2d(c.ring.after(gb, 1), c.map_c, p.F + f0, y, lane);
+          flush_3d(gb, c.map_c, f0, y, 0, lane);  // dgate, dup
         }
         return;
       }
@@ -731,8 +726,8 @@ __device__ __forceinline__ void epilogue_tile(const Tile& T, uint32_t tbase, Epi
         }
         if (full) {
           publish();
-          flush_2d(gb, c.map_c, f0, y, lane);
-          if (fused) flush_2d(c.ring.after(gb, 1), c.map_c, p.F + f0, y, lane);
+          if (fused) flush_3d(gb, c.map_c, f0, y, 0, lane);  // dgate, dup
+          else flush_2d(gb, c.map_c, f0, y, lane);
         }
       }
     } else {
@@ -1131,6 +1126,17 @@ bool map3d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t mid, uint6
   return make_map(m, base, 3, dims, strides, box);
 }
 
+// A [rows][2F] tensor of gate and up halves (z, dz) seen as [2][rows][F]:
+// one box of 32 rows x 64 columns per half moves a gate chunk and the up
+// chunk F columns to its right with one instruction, into two consecutive
+// 4 KB staging buffers.  Dims (innermost first): F, rows, 2.
+bool map_halves(CUtensorMap* m, const void* base, uint64_t F, uint64_t rows) {
+  const uint64_t dims[3] = {F, rows, 2};
+  const uint64_t strides[2] = {4 * F, 2 * F};
+  const uint32_t box[3] = {64, 32, 2};
+  return make_map(m, base, 3, dims, strides, box);
+}
+
 // An MN-major operand [outer][rows][inner] (inner contiguous, a multiple of
 // 64) seen as [outer][inner/64][rows][64]: one box of `box_chunks` 64-wide
 // chunks x 64 rows lands as consecutive 8 KB chunks, the layout the MMA
@@ -1227,14 +1233,16 @@ cudaError_t launch_shape(const GemmCall& c, cudaStream_t s) {
       if constexpr (S::kNacc == 1) {
         switch (c.kind) {
           case GemmKind::kFc1:
-            if constexpr (S::kRing >= 3) {  // h, z gate and z up are staged together
+            // h, z gate and z up are staged together, z gate and z up in
+            // adjacent buffers (one 3-D store): the ring holds whole triples
+            if constexpr (S::kRing % 3 == 0) {
               p.Kdim = d.D;
               p.N = d.F;
               p.n_tiles = static_cast<int>(cdiv(d.F, BN / 2));
               ok = map2d(&ma, c.a, d.D, R, 64, BM) &&
                    map_chunks(&mb, c.b, F2, d.D, d.E, BN / 64 / 2, 4) &&
                    map2d(&mc, c.out0, d.F, R, 64, 32);
-              if (ok) ok = (c.out1 != nullptr) ? map2d(&md, c.out1, F2, R, 64, 32) : (md = mc, true);
+              if (ok) ok = (c.out1 != nullptr) ? map_halves(&md, c.out1, d.F, R) : (md = mc, true);
               if (!ok) return cudaErrorInvalidValue;
               return launch_kind<0, S>(ma, mb, mc, md, p, row_blocks_bound * p.n_tiles, s);
             }
@@ -1249,13 +1257,17 @@ cudaError_t launch_shape(const GemmCall& c, cudaStream_t s) {
             if (!ok) return cudaErrorInvalidValue;
             return launch_kind<1, S>(ma, mb, mc, md, p, row_blocks_bound * p.n_tiles, s);
           case GemmKind::kDlhsFc2:
-            if constexpr (S::kRing >= 2) {  // dgate and dup are staged together
+            // fused, dgate and dup are staged together in adjacent buffers
+            // (one 3-D store): the ring must hold whole pairs
+            if (c.aux != nullptr && S::kRing % 2 != 0) return cudaErrorInvalidValue;
+            if constexpr (S::kRing >= 2) {
               p.Kdim = d.D;
               p.N = d.F;
               p.n_tiles = static_cast<int>(cdiv(d.F, BN));
               ok = map2d(&ma, c.a, d.D, R, 64, BM) && map3d(&mb, c.b, d.D, d.F, d.E, 64, kBRows) &&
-                   map2d(&mc, c.out0, c.aux != nullptr ? F2 : d.F, R, 64, 32);
-              if (ok) ok = (c.aux != nullptr) ? map2d(&md, c.aux, F2, R, 64, 32) : (md = mc, true);
+                   (c.aux != nullptr ? map_halves(&mc, c.out0, d.F, R)
+                                     : map2d(&mc, c.out0, d.F, R, 64, 32));
+              if (ok) ok = (c.aux != nullptr) ? map_halves(&md, c.aux, d.F, R) : (md = mc, true);
               if (!ok) return cudaErrorInvalidValue;
               return launch_kind<2, S>(ma, mb, mc, md, p, row_blocks_bound * p.n_tiles, s);
             }
@@ -1301,8 +1313,8 @@ cudaError_t launch_shape(const GemmCall& c, cudaStream_t s) {
   return cudaErrorInvalidValue;
 }
 
-// Single-CTA shape: 3 stages of 48 KB and 4 staging buffers per warp.
-using Shape1 = Shape<256, 3, 1, 4>;
+// Single-CTA shape: 3 stages of 48 KB and 3 staging buffers per warp.
+using Shape1 = Shape<256, 3, 1, 3>;
 // CTA-pair shapes: stages of 32 KB per CTA.  FC1 stages three buffers at once
 // (h, z gate, z up); the others need at most two.  FC1's fifth stage (paid
 // for with its fourth staging buffer) cuts the MMA's waits for operands from
