@@ -28,6 +28,11 @@ CASES = {
     "zipf_given": custom("zipf_given", T=640, D=256, E=24, K=4, F=256, score_mode=2, zipf_s=1.2,
                          train=True),
     "tiny_fwd": WORKLOADS["tiny_fwd"],
+    # the largest E the ABI takes: 32-lane top-k groups, a full 1024-key sort
+    # in the drhs schedule, hundreds of experts with no rows
+    "e_max": custom("e_max", T=300, D=128, E=1024, K=8, F=64, bias_std=0.5, train=True),
+    # the largest K: 32 slots per token, sigmoid-normalised weights
+    "k_max": custom("k_max", T=96, D=192, E=40, K=32, F=128, score_mode=1, train=True),
 }
 
 
