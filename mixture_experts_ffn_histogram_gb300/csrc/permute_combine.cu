@@ -39,21 +39,51 @@ int grid_for_tokens(int T) {
   return want < cap ? want : cap;
 }
 
-template <int VPL>  // 16-byte vectors per lane per pass
+// Warps per token row for the gathers.  With few tokens one warp per row
+// leaves the SMs with too few loads in flight (1024 tokens: ~7 warps per
+// SM), so a row is split into column slices of whole 32*VPL-vector passes,
+// one warp each, until about 64 warps per SM are busy.  Every output element
+// is still computed by one lane in the same order, so results do not change.
+int split_for_tokens(int T, int Dv, int vpl) {
+  const long want = static_cast<long>(sm_count()) * 64;
+  const int max_split = max(1, Dv / (32 * vpl));
+  long sp = T > 0 ? want / T : 1;
+  if (sp < 1) sp = 1;
+  if (sp > max_split) sp = max_split;
+  return static_cast<int>(sp);
+}
+int grid_for_rows(int T, int split) {
+  const long want = (static_cast<long>(T) * split + kWarps - 1) / kWarps;
+  const long cap = static_cast<long>(sm_count()) * 16;
+  return static_cast<int>(want < cap ? want : cap);
+}
+
+// VPL: 16-byte vectors per lane per pass; SPLIT: rows shared by `split`
+// warps (a separate instantiation, so that one warp per row keeps its
+// register count)
+template <int VPL, bool SPLIT>
 __global__ void __launch_bounds__(kThreads) permute_kernel(const uint4* __restrict__ x,
                                                            const int32_t* __restrict__ pos,
                                                            uint4* __restrict__ xs, int T, int K,
-                                                           int Dv) {
+                                                           int Dv, int split_arg) {
   const int lane = threadIdx.x & 31;
-  for (int t = blockIdx.x * kWarps + (threadIdx.x >> 5); t < T; t += gridDim.x * kWarps) {
+  const int split = SPLIT ? split_arg : 1;
+  const int passes = (Dv + 32 * VPL - 1) / (32 * VPL);  // 32*VPL-vector passes per row
+  const int slice = (passes + split - 1) / split * (32 * VPL);  // vectors per slice
+  const long items = static_cast<long>(T) * split;
+  for (long u = static_cast<long>(blockIdx.x) * kWarps + (threadIdx.x >> 5); u < items;
+       u += static_cast<long>(gridDim.x) * kWarps) {
+    const int t = static_cast<int>(u / split);
+    const int c0 = static_cast<int>(u - static_cast<long>(t) * split) * slice;
+    const int c1 = min(Dv, c0 + slice);
     const int p_lane = (lane < K) ? __ldg(pos + static_cast<long>(t) * K + lane) : -1;
     const uint4* src = x + static_cast<long>(t) * Dv;
-    for (int v0 = 0; v0 < Dv; v0 += 32 * VPL) {
+    for (int v0 = c0; v0 < c1; v0 += 32 * VPL) {
       uint4 buf[VPL];
 #pragma unroll
       for (int i = 0; i < VPL; ++i) {
         const int idx = v0 + i * 32 + lane;
-        if (idx < Dv) buf[i] = ld_stream(src + idx);
+        if (idx < c1) buf[i] = ld_stream(src + idx);
       }
       for (int k = 0; k < K; ++k) {
         const int p = __shfl_sync(0xffffffffu, p_lane, k);
@@ -62,7 +92,7 @@ __global__ void __launch_bounds__(kThreads) permute_kernel(const uint4* __restri
 #pragma unroll
         for (int i = 0; i < VPL; ++i) {
           const int idx = v0 + i * 32 + lane;
-          if (idx < Dv) dst[idx] = buf[i];
+          if (idx < c1) dst[idx] = buf[i];
         }
       }
     }
@@ -79,18 +109,26 @@ __device__ __forceinline__ void axpy8(float (&acc)[8], float wk, const uint4& v)
 }
 
 // out[t] = bf16(sum_k w[t,k] * ys[pos[t,k]]); w == nullptr means unit weights.
-template <int VPL>
+template <int VPL, bool SPLIT>
 __global__ void __launch_bounds__(kThreads) combine_kernel(const uint4* __restrict__ ys,
                                                            const float* __restrict__ w,
                                                            const int32_t* __restrict__ pos,
                                                            uint4* __restrict__ out, int T, int K,
-                                                           int Dv) {
+                                                           int Dv, int split_arg) {
   const int lane = threadIdx.x & 31;
-  for (int t = blockIdx.x * kWarps + (threadIdx.x >> 5); t < T; t += gridDim.x * kWarps) {
+  const int split = SPLIT ? split_arg : 1;
+  const int passes = (Dv + 32 * VPL - 1) / (32 * VPL);  // 32*VPL-vector passes per row
+  const int slice = (passes + split - 1) / split * (32 * VPL);  // vectors per slice
+  const long items = static_cast<long>(T) * split;
+  for (long u = static_cast<long>(blockIdx.x) * kWarps + (threadIdx.x >> 5); u < items;
+       u += static_cast<long>(gridDim.x) * kWarps) {
+    const int t = static_cast<int>(u / split);
+    const int c0 = static_cast<int>(u - static_cast<long>(t) * split) * slice;
+    const int c1 = min(Dv, c0 + slice);
     const long j = static_cast<long>(t) * K + lane;
     const int p_lane = (lane < K) ? __ldg(pos + j) : -1;
     const float w_lane = (lane < K) ? (w != nullptr ? __ldg(w + j) : 1.0f) : 0.f;
-    for (int v0 = 0; v0 < Dv; v0 += 32 * VPL) {
+    for (int v0 = c0; v0 < c1; v0 += 32 * VPL) {
       float acc[VPL][8];
 #pragma unroll
       for (int i = 0; i < VPL; ++i)
@@ -105,7 +143,7 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const uint4* __restri
 #pragma unroll
         for (int i = 0; i < VPL; ++i) {
           const int idx = v0 + i * 32 + lane;
-          if (idx < Dv) v[i] = ld_stream(src + idx);
+          if (idx < c1) v[i] = ld_stream(src + idx);
         }
 #pragma unroll
         for (int i = 0; i < VPL; ++i) axpy8(acc[i], wk, v[i]);
@@ -113,7 +151,7 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const uint4* __restri
 #pragma unroll
       for (int i = 0; i < VPL; ++i) {
         const int idx = v0 + i * 32 + lane;
-        if (idx < Dv) {
+        if (idx < c1) {
           uint4 o;
           o.x = pack_bf16x2(acc[i][0], acc[i][1]);
           o.y = pack_bf16x2(acc[i][2], acc[i][3]);
@@ -241,16 +279,22 @@ __global__ void bounded_wait_selftest_kernel(int32_t* status, uint64_t limit_ns)
 cudaError_t launch_permute(const uint16_t* x, const int32_t* pos, uint16_t* xs, const moe_dims& d,
                            cudaStream_t s) {
   if (d.T == 0) return cudaSuccess;
-  permute_kernel<4><<<grid_for_tokens(d.T), kThreads, 0, s>>>(
-      reinterpret_cast<const uint4*>(x), pos, reinterpret_cast<uint4*>(xs), d.T, d.K, d.D / 8);
+  const int split = split_for_tokens(d.T, d.D / 8, 4);
+  auto kern = split > 1 ? permute_kernel<4, true> : permute_kernel<4, false>;
+  kern<<<grid_for_rows(d.T, split), kThreads, 0, s>>>(
+      reinterpret_cast<const uint4*>(x), pos, reinterpret_cast<uint4*>(xs), d.T, d.K, d.D / 8,
+      split);
   return cudaGetLastError();
 }
 
 cudaError_t launch_combine(const uint16_t* ys, const float* w, const int32_t* pos, uint16_t* out,
                            const moe_dims& d, cudaStream_t s) {
   if (d.T == 0) return cudaSuccess;
-  combine_kernel<2><<<grid_for_tokens(d.T), kThreads, 0, s>>>(
-      reinterpret_cast<const uint4*>(ys), w, pos, reinterpret_cast<uint4*>(out), d.T, d.K, d.D / 8);
+  const int split = split_for_tokens(d.T, d.D / 8, 2);
+  auto kern = split > 1 ? combine_kernel<2, true> : combine_kernel<2, false>;
+  kern<<<grid_for_rows(d.T, split), kThreads, 0, s>>>(
+      reinterpret_cast<const uint4*>(ys), w, pos, reinterpret_cast<uint4*>(out), d.T, d.K, d.D / 8,
+      split);
   return cudaGetLastError();
 }
 
