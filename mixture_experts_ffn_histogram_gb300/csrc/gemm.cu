@@ -19,17 +19,20 @@
 //
 // Design: persistent warp-specialised kernel, one CTA per SM, 192 threads.
 //   warp 0     TMA producer: 128x64 A tiles and (BN/CG)x64 B tiles (bf16,
-//              128-byte swizzle) into a shared-memory ring; for the forward
-//              and dlhs GEMMs B comes from a 3-D tensor map whose outer
-//              coordinate is the expert.
-//   warp 1     TMEM allocation (two 128xBN fp32 accumulators) and MMA issue:
-//              one thread issues tcgen05.mma (K=16) and tcgen05.commit; for
-//              drhs the warp zero-fills the rows of the last reduction block
-//              that belong to the next group.
+//              128-byte swizzle) into a shared-memory ring, one box per
+//              operand (MN-major operands through a map with a chunk
+//              dimension); the per-expert weights come through maps whose
+//              outer coordinate is the expert.  For drhs the even CTA's
+//              producer also claims tiles for the dynamic schedule.
+//   warp 1     TMEM allocation (512 columns: two 128xBN fp32 accumulators,
+//              or one 512 wide for drhs pair tiles) and MMA issue: one
+//              thread issues tcgen05.mma (K=16) and tcgen05.commit; for drhs
+//              the warp zero-fills the rows of the last reduction block that
+//              belong to the next group.
 //   warps 2-5  epilogue: tcgen05.ld (one row per thread), SwiGLU / SwiGLU
 //              backward / bf16 conversion, staged in swizzled shared memory
-//              and written by TMA stores; the second accumulator lets the
-//              next tile's MMAs overlap it.
+//              and written by TMA stores; with two accumulators the next
+//              tile's MMAs overlap it.
 // CG = 2 runs the CTA pair of a 2-CTA cluster on one 256-row tile: each CTA
 // loads its own 128 A rows and half of the B columns, the even CTA issues
 // tcgen05.mma.cta_group::2 (M = 256) reading both CTAs' shared memory, and
