@@ -64,6 +64,11 @@ def load_library(path: str) -> ctypes.CDLL:
         "oracle_fc1_bwd": ([P, P, P, P, I, I, I, P, P], I),
         "oracle_permute_bwd": ([P, P, I, I, I, P], I),
         "oracle_num_threads": ([], I),
+        "oracle_e4m3_to_f64": ([ctypes.c_uint8], ctypes.c_double),
+        "oracle_f64_to_e4m3": ([ctypes.c_double], ctypes.c_uint8),
+        "oracle_mx_quantize": ([P, I, I, P, P], I),
+        "oracle_mx_fc1_swiglu": ([P, P, P, P, P, I, I, I, P], I),
+        "oracle_mx_fc2": ([P, P, P, P, P, I, I, I, P], I),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -254,6 +259,118 @@ def permute_bwd(dxs, pos, T, D):
 
 def num_threads() -> int:
     return int(lib().oracle_num_threads())
+
+
+# ------------------------------------------------------------------- MXFP8
+def e4m3_to_f64(codes) -> np.ndarray:
+    """Value of every E4M3 code in ``codes`` (elementwise)."""
+    L = lib()
+    c = np.asarray(codes, dtype=np.uint8)
+    return np.array([L.oracle_e4m3_to_f64(int(v)) for v in c.ravel()],
+                    dtype=np.float64).reshape(c.shape)
+
+
+def f64_to_e4m3(values) -> np.ndarray:
+    """E4M3 code of every value (nearest, ties to even, saturating)."""
+    L = lib()
+    v = np.asarray(values, dtype=np.float64)
+    return np.array([L.oracle_f64_to_e4m3(float(x)) for x in v.ravel()],
+                    dtype=np.uint8).reshape(v.shape)
+
+
+def mx_quantize(x):
+    """MXFP8 block quantization of fp32 rows ``x [rows, K]`` along K:
+    returns (codes uint8 [rows, K], scales uint8 [rows, K/32])."""
+    x = _c(x, np.float32)
+    rows, K = x.shape
+    q = np.zeros((rows, K), np.uint8)
+    sc = np.zeros((rows, K // 32), np.uint8)
+    _check(lib().oracle_mx_quantize(_p(x), rows, K, _p(q), _p(sc)), "mx_quantize")
+    return q, sc
+
+
+def mx_dequantize(q, sc) -> np.ndarray:
+    """float64 values of MX codes ``q [rows, K]`` with scales ``sc [rows, K/32]``."""
+    vals = e4m3_lut()[np.asarray(q, dtype=np.uint8)]
+    return vals * np.exp2(np.repeat(np.asarray(sc, np.int64) - 127, 32, axis=-1))
+
+
+_LUT = None
+
+
+def e4m3_lut() -> np.ndarray:
+    """The oracle's value of each of the 256 E4M3 codes."""
+    global _LUT
+    if _LUT is None:
+        _LUT = e4m3_to_f64(np.arange(256, dtype=np.uint8))
+    return _LUT
+
+
+def mx_fc1_swiglu(xq, xsc, wq, wsc, offs):
+    """FC1 + SwiGLU on MX operands (``wq [E, 2F, D]``, wi transposed);
+    returns h fp32 [R, F]."""
+    xq, xsc = _c(xq, np.uint8), _c(xsc, np.uint8)
+    wq, wsc = _c(wq, np.uint8), _c(wsc, np.uint8)
+    offs = _c(offs, np.int32)
+    E, N, D = wq.shape
+    F = N // 2
+    R = int(offs[E])
+    h = np.zeros((R, F), np.float32)
+    _check(lib().oracle_mx_fc1_swiglu(_p(xq), _p(xsc), _p(wq), _p(wsc), _p(offs), E, D, F, _p(h)),
+           "mx_fc1")
+    return h
+
+
+def mx_fc2(hq, hsc, wq, wsc, offs):
+    """FC2 on MX operands (``wq [E, D, F]``, wo transposed); returns ys bf16 bits."""
+    hq, hsc = _c(hq, np.uint8), _c(hsc, np.uint8)
+    wq, wsc = _c(wq, np.uint8), _c(wsc, np.uint8)
+    offs = _c(offs, np.int32)
+    E, D, F = wq.shape
+    R = int(offs[E])
+    ys = np.zeros((R, D), np.uint16)
+    _check(lib().oracle_mx_fc2(_p(hq), _p(hsc), _p(wq), _p(wsc), _p(offs), E, F, D, _p(ys)),
+           "mx_fc2")
+    return ys
+
+
+def mx_weights(wi, wo):
+    """MX operands of the expert weights, quantized along each GEMM's
+    contraction axis: wi [E, D, 2F] -> (wq [E, 2F, D], wsc [E, 2F, D/32]);
+    wo [E, F, D] -> (oq [E, D, F], osc [E, D, F/32])."""
+    wi = np.asarray(wi, np.uint16)
+    wo = np.asarray(wo, np.uint16)
+    E, D, N = wi.shape
+    F = wo.shape[1]
+    wit = np.ascontiguousarray(bf16_to_f32(wi).transpose(0, 2, 1)).reshape(E * N, D)
+    wot = np.ascontiguousarray(bf16_to_f32(wo).transpose(0, 2, 1)).reshape(E * D, F)
+    wq, wsc = mx_quantize(wit)
+    oq, osc = mx_quantize(wot)
+    return (wq.reshape(E, N, D), wsc.reshape(E, N, D // 32),
+            oq.reshape(E, D, F), osc.reshape(E, D, F // 32))
+
+
+def mx_block_forward(inp: dict) -> dict:
+    """The MXFP8 forward in order: route, histogram, permute + quantize of
+    the sorted rows, FC1 + SwiGLU on MX operands, quantize h, FC2 on MX
+    operands, combine.  ``inp`` as for :func:`block_forward`."""
+    wl = inp["workload"]
+    T, D, E, K = wl.T, wl.D, wl.E, wl.K
+    if wl.score_mode == GIVEN:
+        ids, w = inp["ids"], inp["w"]
+    else:
+        ids, w = route(inp["logits"], inp["bias"], wl.score_mode, T, E, K)
+    gs, off, pos, row_src, bad = histogram(ids, E)
+    xs = permute(inp["x"], pos)
+    xq, xsc = mx_quantize(bf16_to_f32(xs))
+    wq, wsc, oq, osc = mx_weights(inp["wi"], inp["wo"])
+    h = mx_fc1_swiglu(xq, xsc, wq, wsc, off)
+    hq, hsc = mx_quantize(h)
+    ys = mx_fc2(hq, hsc, oq, osc, off)
+    out = combine(ys, w, pos, T, D)
+    return dict(ids=ids, w=w, group_sizes=gs, group_offsets=off, pos=pos, row_src=row_src,
+                xq=xq, xsc=xsc, wq=wq, wsc=wsc, oq=oq, osc=osc, h=h, hq=hq, hsc=hsc, ys=ys,
+                out=out)
 
 
 # ------------------------------------------------------- whole-block drivers

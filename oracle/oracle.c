@@ -395,3 +395,143 @@ int oracle_permute_bwd(const uint16_t* dxs, const int32_t* pos, int T, int K, in
                        uint16_t* dx) {
   return oracle_combine(dxs, NULL, pos, T, K, D, dx);
 }
+
+/* ------------------------------------------------------------------ MXFP8
+ * [TE MoE, Changes item 1 and Flowchart], with the format read as OCP MX
+ * v1.0 MXFP8 (see oracle.h). */
+
+/* E4M3 code -> value: sign bit, 4 exponent bits (bias 7), 3 mantissa bits;
+ * exponent field 0 holds the subnormals m * 2^-9; S.1111.111 is NaN. */
+double oracle_e4m3_to_f64(uint8_t c) {
+  const int s = c >> 7, e = (c >> 3) & 15, m = c & 7;
+  if (e == 15 && m == 7) return NAN;
+  const double v = (e == 0) ? ldexp((double)m, -9) : ldexp((double)(8 + m), e - 10);
+  return s ? -v : v;
+}
+
+/* value -> E4M3 code, round to nearest with ties to even, magnitudes beyond
+ * the largest finite value 448 saturated to it. */
+uint8_t oracle_f64_to_e4m3(double v) {
+  if (isnan(v)) return 0x7F;
+  const uint8_t s = signbit(v) ? 0x80 : 0x00;
+  const double a = fabs(v);
+  if (a >= 448.0) return (uint8_t)(s | 0x7E);
+  if (a < ldexp(1.0, -6)) {
+    /* subnormal spacing 2^-9; rounding up to 8 * 2^-9 gives the smallest
+     * normal, whose code is 8 as well */
+    const double m = nearbyint(a * 512.0);
+    return (uint8_t)(s | (uint8_t)m);
+  }
+  int ex;
+  frexp(a, &ex);
+  int E = ex - 1;                                /* a in [2^E, 2^(E+1)), E in [-6, 8] */
+  double m = nearbyint(ldexp(a, 3 - E));         /* 8 .. 16: 1.mmm with 3 bits */
+  if (m == 16.0) {
+    m = 8.0;
+    E += 1;
+  }
+  if (E > 8 || (E == 8 && m > 14.0)) return (uint8_t)(s | 0x7E);
+  return (uint8_t)(s | (uint8_t)(((E + 7) << 3) | ((int)m - 8)));
+}
+
+/* Shared exponent of one block: floor(log2(amax)) - 8 (8 = the exponent of
+ * E4M3's largest power of two), clamped below to E8M0's -127. */
+static int mx_shared_exp(const float* v, int n) {
+  double amax = 0.0;
+  for (int i = 0; i < n; ++i) {
+    const double a = fabs((double)v[i]);
+    if (a > amax) amax = a;
+  }
+  if (amax == 0.0) return -127;
+  int ex;
+  frexp(amax, &ex);
+  const int s = (ex - 1) - 8;
+  return s < -127 ? -127 : s;
+}
+
+int oracle_mx_quantize(const float* x, int rows, int K, uint8_t* q, uint8_t* sc) {
+  if (rows < 0 || K <= 0 || K % 32 != 0) return -1;
+  const int nb = K / 32;
+#pragma omp parallel for schedule(static)
+  for (int r = 0; r < rows; ++r) {
+    for (int b = 0; b < nb; ++b) {
+      const float* v = x + (size_t)r * K + (size_t)b * 32;
+      const int s = mx_shared_exp(v, 32);
+      sc[(size_t)r * nb + b] = (uint8_t)(s + 127);
+      for (int i = 0; i < 32; ++i)
+        q[(size_t)r * K + (size_t)b * 32 + i] = oracle_f64_to_e4m3(ldexp((double)v[i], -s));
+    }
+  }
+  return 0;
+}
+
+/* Dequantized row of n elements (n % 32 == 0): code * 2^(scale - 127). */
+static void mx_row(const uint8_t* q, const uint8_t* sc, int n, double* out) {
+  for (int i = 0; i < n; ++i) out[i] = ldexp(oracle_e4m3_to_f64(q[i]), (int)sc[i / 32] - 127);
+}
+
+/* FC1 + SwiGLU on MX operands: per row r of group e and output column n,
+ * a[n] = sum_d x[r,d] * w[e,n,d] of the dequantized values (float64), then
+ * h[r,f] = fp32(silu(a[f]) * a[F+f]). */
+int oracle_mx_fc1_swiglu(const uint8_t* xq, const uint8_t* xsc, const uint8_t* wq,
+                         const uint8_t* wsc, const int32_t* offs, int E, int D, int F,
+                         float* h) {
+  if (E <= 0 || D <= 0 || F <= 0 || D % 32 != 0) return -1;
+  const int N = 2 * F, R = offs[E], nb = D / 32;
+#pragma omp parallel
+  {
+    double* xr = (double*)malloc(sizeof(double) * (size_t)D);
+    double* wr = (double*)malloc(sizeof(double) * (size_t)D);
+    double* a = (double*)malloc(sizeof(double) * (size_t)N);
+#pragma omp for schedule(dynamic, 4)
+    for (int r = 0; r < R; ++r) {
+      int e = 0;
+      while (offs[e + 1] <= r) ++e;
+      mx_row(xq + (size_t)r * D, xsc + (size_t)r * nb, D, xr);
+      for (int n = 0; n < N; ++n) {
+        const size_t wrow = (size_t)e * N + n;
+        mx_row(wq + wrow * D, wsc + wrow * nb, D, wr);
+        double acc = 0.0;
+        for (int d = 0; d < D; ++d) acc += xr[d] * wr[d];
+        a[n] = acc;
+      }
+      for (int f = 0; f < F; ++f) {
+        const double g = a[f], u = a[F + f];
+        h[(size_t)r * F + f] = (float)((g / (1.0 + exp(-g))) * u);
+      }
+    }
+    free(xr);
+    free(wr);
+    free(a);
+  }
+  return 0;
+}
+
+/* FC2 on MX operands: ys[r,d] = bf16(fp32(sum_f h[r,f] * w[e,d,f])) of the
+ * dequantized values (float64 sum). */
+int oracle_mx_fc2(const uint8_t* hq, const uint8_t* hsc, const uint8_t* wq, const uint8_t* wsc,
+                  const int32_t* offs, int E, int F, int D, uint16_t* ys) {
+  if (E <= 0 || D <= 0 || F <= 0 || F % 32 != 0) return -1;
+  const int R = offs[E], nb = F / 32;
+#pragma omp parallel
+  {
+    double* hr = (double*)malloc(sizeof(double) * (size_t)F);
+    double* wr = (double*)malloc(sizeof(double) * (size_t)F);
+#pragma omp for schedule(dynamic, 4)
+    for (int r = 0; r < R; ++r) {
+      int e = 0;
+      while (offs[e + 1] <= r) ++e;
+      mx_row(hq + (size_t)r * F, hsc + (size_t)r * nb, F, hr);
+      for (int d = 0; d < D; ++d) {
+        const size_t wrow = (size_t)e * D + d;
+        mx_row(wq + wrow * F, wsc + wrow * nb, F, wr);
+        double acc = 0.0;
+        for (int f = 0; f < F; ++f) acc += hr[f] * wr[f];
+        ys[(size_t)r * D + d] = RN((float)acc);
+      }
+    }
+    free(hr);
+    free(wr);
+  }
+  return 0;
+}

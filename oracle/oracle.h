@@ -60,6 +60,37 @@ int oracle_permute_bwd(const uint16_t* dxs, const int32_t* pos, int T, int K, in
                        uint16_t* dx);
 int oracle_num_threads(void);
 
+/*
+ * MXFP8 forward [TE MoE, Changes item 1 ("MXFP8 quantization in the MoE
+ * block") and Flowchart ("Grouped FC1 quantize and GEMM" -> "Activation and
+ * grouped FC2 GEMM")].  The pages name the format only; its definition is
+ * read as the OCP Microscaling (MX) v1.0 MXFP8 format: blocks of 32
+ * consecutive elements along the contraction axis share one E8M0 scale
+ * (the byte c means 2^(c-127)); each element is an E4M3 code (bias 7, no
+ * infinities, S.1111.111 = NaN, largest finite 448).
+ *   Block quantization: X = 2^s, s = max(floor(log2(amax)) - 8, -127)
+ *   (s = -127 when amax = 0), code_i = E4M3(v_i / X) rounded to nearest,
+ *   ties to even, magnitudes beyond 448 saturated to 448.
+ * The MX GEMMs sum the exact products of dequantized elements in float64 in
+ * ascending index order (nothing but the sum's rounding differs from the
+ * real-number result).
+ */
+double oracle_e4m3_to_f64(uint8_t c);
+uint8_t oracle_f64_to_e4m3(double v);
+/* x fp32 [rows, K], K % 32 == 0 -> q [rows, K] codes, sc [rows, K/32]. */
+int oracle_mx_quantize(const float* x, int rows, int K, uint8_t* q, uint8_t* sc);
+/* FC1 + SwiGLU on MX operands: xq/xsc [R, D] / [R, D/32]; wq/wsc are wi
+ * transposed, [E, 2F, D] / [E, 2F, D/32] (row n = output column n; gate =
+ * rows [0,F), up = [F,2F)).  h fp32 [R, F] = fp32(silu(g) * u) of the
+ * float64 sums. */
+int oracle_mx_fc1_swiglu(const uint8_t* xq, const uint8_t* xsc, const uint8_t* wq,
+                         const uint8_t* wsc, const int32_t* group_offsets, int E, int D, int F,
+                         float* h);
+/* FC2 on MX operands: hq/hsc [R, F] / [R, F/32]; wq/wsc are wo transposed,
+ * [E, D, F] / [E, D, F/32].  ys bf16 [R, D] = bf16(fp32(sum)). */
+int oracle_mx_fc2(const uint8_t* hq, const uint8_t* hsc, const uint8_t* wq, const uint8_t* wsc,
+                  const int32_t* group_offsets, int E, int F, int D, uint16_t* ys);
+
 #ifdef __cplusplus
 }
 #endif

@@ -367,7 +367,119 @@ def check_finite_differences(orc):
             f"finite differences disagree for d{name}: fd={fd} oracle={an}"
 
 
+# -------------------------------------------------------------------- MXFP8
+def _torch_e4m3(values):
+    """torch's float32 -> float8_e4m3fn conversion (nearest, ties to even) of
+    values already clamped to the finite range; codes as uint8."""
+    t = torch.tensor(np.asarray(values, np.float32))
+    return t.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+def check_e4m3_decode(orc):
+    """Every code's value equals torch's float8_e4m3fn reading of the same
+    byte, and the format's landmarks hold: 1.0 = 0x38, the largest finite
+    value 448 = 0x7E, the smallest normal 2^-6 = 0x08, the smallest
+    subnormal 2^-9 = 0x01, NaN = 0x7F / 0xFF and no infinities."""
+    codes = np.arange(256, dtype=np.uint8)
+    got = orc.e4m3_to_f64(codes)
+    want = torch.from_numpy(codes).view(torch.float8_e4m3fn).double().numpy()
+    nan = np.isnan(want)
+    assert np.array_equal(np.isnan(got), nan) and np.array_equal(got[~nan], want[~nan]), \
+        "E4M3 decoding differs from torch's float8_e4m3fn"
+    assert list(np.flatnonzero(nan)) == [0x7F, 0xFF]
+    assert got[0x38] == 1.0 and got[0x7E] == 448.0 and got[0x08] == 2.0 ** -6
+    assert got[0x01] == 2.0 ** -9 and got[0x07] == 0.875 * 2.0 ** -6 and np.isfinite(got[~nan]).all()
+
+
+def check_e4m3_encode(orc):
+    """Encoding: every finite code round-trips; random values, exact
+    midpoints between neighbours and subnormals round like torch's
+    conversion (nearest, ties to even); magnitudes beyond 448 saturate."""
+    codes = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], np.uint8)
+    vals = orc.e4m3_to_f64(codes)
+    assert np.array_equal(orc.f64_to_e4m3(vals), codes), "finite codes do not round-trip"
+    pos = np.sort(vals[(vals > 0)])
+    mids = (pos[:-1] + pos[1:]) / 2
+    rng = _rng(41)
+    rand = np.concatenate([rng.uniform(-448, 448, 3000), rng.uniform(-1, 1, 2000) * 2.0 ** -6,
+                           rng.standard_normal(2000)])
+    probe = np.concatenate([mids, -mids, rand, mids * (1 + 1e-7), mids * (1 - 1e-7)])
+    probe = probe[np.abs(probe) <= 448].astype(np.float32).astype(np.float64)
+    assert np.array_equal(orc.f64_to_e4m3(probe), _torch_e4m3(probe)), \
+        "E4M3 rounding differs from torch's nearest-even conversion"
+    sat = orc.f64_to_e4m3(np.array([448.0, 449.0, 463.9, 464.0, 500.0, 1e30, -1e30, -470.0]))
+    assert list(sat) == [0x7E] * 6 + [0xFE, 0xFE], "magnitudes beyond 448 must saturate"
+
+
+def _mx_quantize_ref(x):
+    """Block quantization from library routines: the block's floor(log2(amax))
+    from numpy's frexp, the elements by torch's E4M3 conversion."""
+    rows, K = x.shape
+    blocks = x.astype(np.float64).reshape(rows, K // 32, 32)
+    amax = np.abs(blocks).max(axis=2)
+    _, ex = np.frexp(amax)
+    s = np.where(amax == 0, -127, np.maximum(ex - 1 - 8, -127))
+    scaled = np.clip(blocks * np.exp2(-s)[:, :, None], -448, 448)
+    q = _torch_e4m3(scaled.reshape(rows, K))
+    return q, (s + 127).astype(np.uint8)
+
+
+def check_mx_quantize(orc):
+    """MXFP8 quantization against library routines on random rows (several
+    magnitudes, bf16 subnormals included), and its special cases: a zero
+    block takes the smallest scale (code 0) and zero codes; a block whose
+    amax is 2^k takes scale code k - 8 + 127 and stores amax as 256 (0x78);
+    a block of exactly representable values round-trips exactly."""
+    rng = _rng(42)
+    x = np.concatenate([rng.standard_normal((16, 128)) * m for m in (1e-3, 0.02, 1.0, 300.0)])
+    x = np.concatenate([x, rng.standard_normal((2, 128)) * 1e-39]).astype(np.float32)
+    q, sc = orc.mx_quantize(x)
+    rq, rsc = _mx_quantize_ref(x)
+    assert np.array_equal(sc, rsc), "MX scales differ from floor(log2(amax)) - 8"
+    assert np.array_equal(q, rq), "MX element codes differ from the library conversion"
+    z = np.zeros((1, 64), np.float32)
+    q, sc = orc.mx_quantize(z)
+    assert (sc == 0).all() and (q == 0).all()
+    for k in (-20, -3, 0, 5):
+        blk = (rng.uniform(-1, 1, (1, 32)) * 2.0 ** k).astype(np.float32)
+        blk[0, 7] = -(2.0 ** k)
+        q, sc = orc.mx_quantize(blk)
+        assert sc[0, 0] == k - 8 + 127 and q[0, 7] == 0xF8
+    exact = (rng.integers(-7, 8, (4, 64)) * 2.0 ** -2).astype(np.float32)
+    exact[:, 0] = 1.75      # amax * 2^-s = 448, the largest finite code
+    q, sc = orc.mx_quantize(exact)
+    assert np.array_equal(orc.mx_dequantize(q, sc), exact.astype(np.float64))
+
+
+def check_mx_gemms(orc):
+    """The MX GEMMs against numpy float64 matmuls of the dequantized operands
+    (per group, the expert's own weights), with SwiGLU written out from its
+    definition and the bf16 output rounding by torch."""
+    rng = _rng(43)
+    E, D, F = 3, 64, 32
+    offs, ids = _random_grouped_rows(rng, 40, E, empty=(1,))
+    R = int(offs[-1])
+    xq, xsc = orc.mx_quantize(rng.standard_normal((R, D)).astype(np.float32))
+    wq, wsc = orc.mx_quantize((rng.standard_normal((E * 2 * F, D)) * 0.1).astype(np.float32))
+    wq, wsc = wq.reshape(E, 2 * F, D), wsc.reshape(E, 2 * F, D // 32)
+    h = orc.mx_fc1_swiglu(xq, xsc, wq, wsc, offs)
+    xd = orc.mx_dequantize(xq, xsc)
+    wd = orc.mx_dequantize(wq, wsc)
+    a = np.einsum("rd,rnd->rn", xd, wd[ids])
+    g, u = a[:, :F], a[:, F:]
+    want = g / (1 + np.exp(-g)) * u
+    assert np.abs(h - want).max() <= 1e-6 * np.abs(want).max() + 1e-30, "MX FC1 differs"
+    hq, hsc = orc.mx_quantize(h)
+    oq, osc = orc.mx_quantize((rng.standard_normal((E * D, F)) * 0.1).astype(np.float32))
+    oq, osc = oq.reshape(E, D, F), osc.reshape(E, D, F // 32)
+    ys = orc.mx_fc2(hq, hsc, oq, osc, offs)
+    y = np.einsum("rf,rdf->rd", orc.mx_dequantize(hq, hsc), orc.mx_dequantize(oq, osc)[ids])
+    want_ys = f32_to_bf16_bits_torch(y.astype(np.float32))
+    assert np.array_equal(ys, want_ys), "MX FC2 differs from the float64 matmul rounded to bf16"
+
+
 ALL_CHECKS = [check_bf16_rounding, check_route, check_histogram, check_permute_combine,
               check_combine_bwd, check_fc1_fc2, check_swiglu_closed_forms,
               check_dense_special_case, check_gemm_backward, check_block_against_dense,
-              check_finite_differences]
+              check_finite_differences, check_e4m3_decode, check_e4m3_encode, check_mx_quantize,
+              check_mx_gemms]

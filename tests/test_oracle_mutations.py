@@ -54,6 +54,20 @@ MUTATIONS = {
     "dxs_gate_half_only": ("for (int n = 0; n < N; ++n) acc = acc + BF(dz[(size_t)r * N + n]) * BF(W[(size_t)d * N + n]);",
                            "for (int n = 0; n < F; ++n) acc = acc + BF(dz[(size_t)r * N + n]) * BF(W[(size_t)d * N + n]);"),
     "bf16_round_half_up": ("u += 0x7fffu + lsb;", "u += 0x8000u;"),
+    "mx_emax_7": ("const int s = (ex - 1) - 8;", "const int s = (ex - 1) - 7;"),
+    "e4m3_ties_away": ("double m = nearbyint(ldexp(a, 3 - E));",
+                       "double m = floor(ldexp(a, 3 - E) + 0.5);"),
+    "e4m3_subnormal_spacing": ("const double m = nearbyint(a * 512.0);",
+                               "const double m = nearbyint(a * 1024.0);"),
+    "e4m3_bias_8": ("ldexp((double)(8 + m), e - 10)", "ldexp((double)(8 + m), e - 11)"),
+    "mx_dequant_scale_dropped": ("out[i] = ldexp(oracle_e4m3_to_f64(q[i]), (int)sc[i / 32] - 127);",
+                                 "out[i] = oracle_e4m3_to_f64(q[i]);"),
+    "mx_scale_block_index": ("(int)sc[i / 32] - 127", "(int)sc[i / 64] - 127"),
+    "mx_fc1_gate_up_swapped": ("const double g = a[f], u = a[F + f];",
+                               "const double g = a[F + f], u = a[f];"),
+    "mx_fc2_first_expert_only": ("const size_t wrow = (size_t)e * D + d;",
+                                 "const size_t wrow = (size_t)0 * D + d;"),
+    "mx_zero_block_scale": ("if (amax == 0.0) return -127;", "if (amax == 0.0) return 0;"),
 }
 
 
