@@ -256,6 +256,107 @@ moe_status moe_combine_bwd(const moe_bf16* dout, const moe_bf16* ys, const float
                            cudaStream_t stream);
 
 /*
+ * ------------------------------------------------------------------ MXFP8
+ * The forward in MXFP8 [TE MoE, Changes item 1 ("MXFP8 quantization in the
+ * MoE block") and Flowchart ("Grouped FC1 quantize and GEMM" -> "Activation
+ * and grouped FC2 GEMM")].  MXFP8 is read as the OCP MX v1.0 format: each
+ * block of 32 consecutive elements along a GEMM's contraction axis shares
+ * one E8M0 scale byte c (value 2^(c-127)); each element is an E4M3 code
+ * (bias 7, no infinities, largest finite 448).  Quantizing a block:
+ *   s = max(floor(log2(amax)) - 8, -127)  (s = -127 when amax = 0),
+ *   c = s + 127,  code_i = E4M3(v_i * 2^-s), nearest-even, saturating.
+ * Inputs must be finite.
+ *
+ * Scale blocks.  Scales are stored in 512-byte blocks, each covering 128
+ * rows and one k-block of 128 contraction elements (4 scales per row): the
+ * scale of row m (0..127) for elements [32j, 32j+32) of the k-block is byte
+ * (m % 32) * 16 + (m / 32) * 4 + j, the order the tensor cores read.
+ * KB(k) = ceil(k / 128) k-blocks; bytes of a block past the contraction
+ * length, or for rows past the tensor's rows, are never used.
+ *
+ * Activation layout (xq/xsc, hq/hsc; rows in expert-sorted order): codes
+ * [R, k] row-major.  Scales are tile-blocked: the rows of each group e are
+ * cut into 128-row tiles starting at group_offsets[e]; the tiles of all
+ * groups are numbered in order (group e's first tile is
+ * tb[e] = sum_{e' < e} ceil(group_size[e'] / 128)), and tile g's scales
+ * for k-block kb are the block at byte (g * KB(k) + kb) * 512.
+ *
+ * Weight layout (wq/wsc): the weight transposed so that its contraction
+ * axis is contiguous, codes [E, N, k] (FC1: N = 2F rows, k = D; FC2: N = D,
+ * k = F), scales [E, KB(k), NBp, 512] with NBp = 2 * ceil(N / 256) blocks
+ * of 128 rows.  FC1's rows are interleaved in 64-row chunks, gate then up:
+ * column n of wi (gate f = n for n < F, up f = n - F) is row
+ * 128 * (f / 64) + 64 * (n >= F) + f % 64.
+ *
+ * moe_mx_bytes(d, which) gives each buffer's size in bytes.
+ */
+typedef enum {
+  MOE_MX_XQ = 0,   /* xq codes [R, D] */
+  MOE_MX_XSC = 1,  /* xq scales, tile-blocked, (ceil(R/128) + E) * KB(D) * 512 */
+  MOE_MX_WIQ = 2,  /* wi codes [E, 2F, D] */
+  MOE_MX_WISC = 3, /* wi scales [E, KB(D), 2*ceil(2F/256), 512] */
+  MOE_MX_WOQ = 4,  /* wo codes [E, D, F] */
+  MOE_MX_WOSC = 5, /* wo scales [E, KB(F), 2*ceil(D/256), 512] */
+  MOE_MX_HQ = 6,   /* hq codes [R, F] */
+  MOE_MX_HSC = 7   /* hq scales, tile-blocked, (ceil(R/128) + E) * KB(F) * 512 */
+} moe_mx_buffer;
+
+/* Bytes of MX buffer `which` for dims d (0 for invalid dims or `which`). */
+size_t moe_mx_bytes(moe_dims d, moe_mx_buffer which);
+
+/*
+ * Grouped quantize of the expert weights (once per weight update):
+ *   moe_mx_quantize_wi: wi bf16 [E, D, 2F] -> wq [E, 2F, D] (interleaved
+ *                       rows) + wsc, blocks along D;
+ *   moe_mx_quantize_wo: wo bf16 [E, F, D]  -> wq [E, D, F] + wsc, blocks
+ *                       along F.
+ * Scale bytes of padding blocks are left as they are.
+ */
+moe_status moe_mx_quantize_wi(const moe_bf16* wi, uint8_t* wq, uint8_t* wsc, moe_dims d,
+                              cudaStream_t stream);
+moe_status moe_mx_quantize_wo(const moe_bf16* wo, uint8_t* wq, uint8_t* wsc, moe_dims d,
+                              cudaStream_t stream);
+
+/*
+ * Grouped FC1 quantize [TE MoE, Flowchart]: the permute of moe_permute with
+ * each token row quantized once (blocks along D) and its codes written to
+ * xq[pos[t,k]] for every slot with pos >= 0; the scales go to the
+ * tile-blocked xsc of the destination row.  Needs the group_offsets of the
+ * histogram that produced pos.
+ *   x bf16 [T,D];  pos int32 [T,K];  group_offsets int32 [E+1];
+ *   xq [R,D] out;  xsc out.
+ */
+moe_status moe_mx_permute_quantize(const moe_bf16* x, const int32_t* pos,
+                                   const int32_t* group_offsets, uint8_t* xq, uint8_t* xsc,
+                                   moe_dims d, cudaStream_t stream);
+
+/*
+ * FC1 + SwiGLU on MX operands: for every row r of group e
+ *   a[n] = sum_d x[r,d] * wi[e,d,n] of the dequantized operands (fp32
+ *   accumulation of exact products), g = a[:F], u = a[F:],
+ *   h[r,f] = fp32(silu(g_f) * u_f), written as MX codes hq [R,F] with the
+ *   tile-blocked scales hsc (blocks along F: the A operand of the MX FC2)
+ *   and/or as bf16 h [R,F].  hq/hsc (both or neither) and h may each be
+ *   NULL, not all three.
+ */
+moe_status moe_mx_grouped_gemm_fc1_swiglu(const uint8_t* xq, const uint8_t* xsc,
+                                          const uint8_t* wq, const uint8_t* wsc,
+                                          const int32_t* group_offsets, uint8_t* hq,
+                                          uint8_t* hsc, moe_bf16* h, int32_t* dev_status,
+                                          moe_dims d, cudaStream_t stream);
+
+/*
+ * FC2 on MX operands: ys[r,:] = bf16(sum_f h[r,f] * wo[e,f,:]) of the
+ * dequantized operands (fp32 accumulation).
+ *   hq, hsc from moe_mx_grouped_gemm_fc1_swiglu;  wq, wsc from
+ *   moe_mx_quantize_wo;  ys bf16 [R,D] out.
+ */
+moe_status moe_mx_grouped_gemm_fc2(const uint8_t* hq, const uint8_t* hsc, const uint8_t* wq,
+                                   const uint8_t* wsc, const int32_t* group_offsets,
+                                   moe_bf16* ys, int32_t* dev_status, moe_dims d,
+                                   cudaStream_t stream);
+
+/*
  * Self-test of the kernels' bounded waits (no counterpart on the pages):
  * launches one block that waits on a barrier nothing ever arrives at, with a
  * limit of `limit_ns` nanoseconds (at most 10^9).  The wait gives up,

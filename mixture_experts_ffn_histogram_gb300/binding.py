@@ -31,7 +31,12 @@ ENTRY_POINTS = (
     "moe_permute", "moe_permute_bwd", "moe_grouped_gemm_fc1_swiglu",
     "moe_grouped_gemm_fc1_swiglu_bwd", "moe_grouped_gemm_fc2", "moe_grouped_gemm_fc2_bwd",
     "moe_combine", "moe_combine_bwd", "moe_selftest_bounded_wait", "moe_route_histogram_noalloc",
+    "moe_mx_bytes", "moe_mx_quantize_wi", "moe_mx_quantize_wo", "moe_mx_permute_quantize",
+    "moe_mx_grouped_gemm_fc1_swiglu", "moe_mx_grouped_gemm_fc2",
 )
+
+# moe_mx_buffer
+MX_XQ, MX_XSC, MX_WIQ, MX_WISC, MX_WOQ, MX_WOSC, MX_HQ, MX_HSC = range(8)
 
 # int32 capacity of the fixed scratch behind moe_route_histogram_noalloc
 NOALLOC_ROUTE_SCRATCH_INTS = 262144
@@ -91,6 +96,12 @@ def lib() -> ctypes.CDLL:
             "moe_combine_bwd": ([P, P, P, P, P, P, D_, P], I),
             "moe_selftest_bounded_wait": ([P, ctypes.c_uint64, P], I),
             "moe_route_histogram_noalloc": ([P, P, I, P, P, P, P, P, P, P, D_, P], I),
+            "moe_mx_bytes": ([D_, I], ctypes.c_size_t),
+            "moe_mx_quantize_wi": ([P, P, P, D_, P], I),
+            "moe_mx_quantize_wo": ([P, P, P, D_, P], I),
+            "moe_mx_permute_quantize": ([P, P, P, P, P, D_, P], I),
+            "moe_mx_grouped_gemm_fc1_swiglu": ([P, P, P, P, P, P, P, P, P, D_, P], I),
+            "moe_mx_grouped_gemm_fc2": ([P, P, P, P, P, P, P, D_, P], I),
         }
         for name, (args, res) in sig.items():
             fn = getattr(L, name)
@@ -204,3 +215,35 @@ def moe_combine_bwd(dout, ys, w, pos, dys, dw, d: MoeDims, stream=None):
 def moe_selftest_bounded_wait(dev_status, limit_ns: int, stream=None):
     _ok("moe_selftest_bounded_wait",
         lib().moe_selftest_bounded_wait(_p(dev_status), int(limit_ns), _s(stream)))
+
+
+# ------------------------------------------------------------------ MXFP8
+def moe_mx_bytes(d: MoeDims, which: int) -> int:
+    return int(lib().moe_mx_bytes(d, int(which)))
+
+
+def moe_mx_quantize_wi(wi, wq, wsc, d: MoeDims, stream=None):
+    _ok("moe_mx_quantize_wi", lib().moe_mx_quantize_wi(_p(wi), _p(wq), _p(wsc), d, _s(stream)))
+
+
+def moe_mx_quantize_wo(wo, wq, wsc, d: MoeDims, stream=None):
+    _ok("moe_mx_quantize_wo", lib().moe_mx_quantize_wo(_p(wo), _p(wq), _p(wsc), d, _s(stream)))
+
+
+def moe_mx_permute_quantize(x, pos, group_offsets, xq, xsc, d: MoeDims, stream=None):
+    _ok("moe_mx_permute_quantize", lib().moe_mx_permute_quantize(
+        _p(x), _p(pos), _p(group_offsets), _p(xq), _p(xsc), d, _s(stream)))
+
+
+def moe_mx_grouped_gemm_fc1_swiglu(xq, xsc, wq, wsc, group_offsets, hq, hsc, h, dev_status,
+                                   d: MoeDims, stream=None):
+    _ok("moe_mx_grouped_gemm_fc1_swiglu", lib().moe_mx_grouped_gemm_fc1_swiglu(
+        _p(xq), _p(xsc), _p(wq), _p(wsc), _p(group_offsets), _p(hq), _p(hsc), _p(h),
+        _p(dev_status), d, _s(stream)))
+
+
+def moe_mx_grouped_gemm_fc2(hq, hsc, wq, wsc, group_offsets, ys, dev_status, d: MoeDims,
+                            stream=None):
+    _ok("moe_mx_grouped_gemm_fc2", lib().moe_mx_grouped_gemm_fc2(
+        _p(hq), _p(hsc), _p(wq), _p(wsc), _p(group_offsets), _p(ys), _p(dev_status), d,
+        _s(stream)))

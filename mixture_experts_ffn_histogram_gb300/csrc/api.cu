@@ -5,6 +5,7 @@
 
 #include "kernels.h"
 #include "moe.h"
+#include "mx.h"
 
 namespace moe {
 
@@ -299,6 +300,95 @@ moe_status moe_grouped_gemm_fc1_swiglu_bwd(const moe_bf16* grad, const moe_bf16*
     if (st != MOE_OK) return st;
   }
   return MOE_OK;
+}
+
+size_t moe_mx_bytes(moe_dims d, moe_mx_buffer which) {
+  if (check_dims(d) != MOE_OK) return 0;
+  const size_t R = static_cast<size_t>(rows(d)), D = d.D, F = d.F, E = d.E;
+  const size_t tiles = static_cast<size_t>(moe::mx_tile_bound(d));
+  const size_t kbd = static_cast<size_t>(moe::mx_kblocks(d.D));
+  const size_t kbf = static_cast<size_t>(moe::mx_kblocks(d.F));
+  switch (which) {
+    case MOE_MX_XQ: return R * D;
+    case MOE_MX_XSC: return tiles * kbd * 512;
+    case MOE_MX_WIQ: return E * 2 * F * D;
+    case MOE_MX_WISC: return E * kbd * static_cast<size_t>(moe::mx_weight_row_blocks(2 * F)) * 512;
+    case MOE_MX_WOQ: return E * D * F;
+    case MOE_MX_WOSC: return E * kbf * static_cast<size_t>(moe::mx_weight_row_blocks(d.D)) * 512;
+    case MOE_MX_HQ: return R * F;
+    case MOE_MX_HSC: return tiles * kbf * 512;
+  }
+  return 0;
+}
+
+moe_status moe_mx_quantize_wi(const moe_bf16* wi, uint8_t* wq, uint8_t* wsc, moe_dims d,
+                              cudaStream_t stream) {
+  MOE_CHECK_DIMS(d);
+  MOE_REQUIRE(wi);
+  MOE_REQUIRE(wq);
+  MOE_REQUIRE(wsc);
+  return from_cuda(moe::launch_mx_quantize_weights(wi, wq, wsc, d.E, d.D, 2 * d.F, true, stream));
+}
+
+moe_status moe_mx_quantize_wo(const moe_bf16* wo, uint8_t* wq, uint8_t* wsc, moe_dims d,
+                              cudaStream_t stream) {
+  MOE_CHECK_DIMS(d);
+  MOE_REQUIRE(wo);
+  MOE_REQUIRE(wq);
+  MOE_REQUIRE(wsc);
+  return from_cuda(moe::launch_mx_quantize_weights(wo, wq, wsc, d.E, d.F, d.D, false, stream));
+}
+
+moe_status moe_mx_permute_quantize(const moe_bf16* x, const int32_t* pos,
+                                   const int32_t* group_offsets, uint8_t* xq, uint8_t* xsc,
+                                   moe_dims d, cudaStream_t stream) {
+  MOE_CHECK_DIMS(d);
+  if (d.T == 0) return MOE_OK;
+  MOE_REQUIRE(x);
+  MOE_REQUIRE(pos);
+  MOE_REQUIRE(group_offsets);
+  MOE_REQUIRE(xq);
+  MOE_REQUIRE(xsc);
+  return from_cuda(moe::launch_mx_permute_quantize(x, pos, group_offsets, xq, xsc, d, stream));
+}
+
+moe_status moe_mx_grouped_gemm_fc1_swiglu(const uint8_t* xq, const uint8_t* xsc,
+                                          const uint8_t* wq, const uint8_t* wsc,
+                                          const int32_t* group_offsets, uint8_t* hq,
+                                          uint8_t* hsc, moe_bf16* h, int32_t* dev_status,
+                                          moe_dims d, cudaStream_t stream) {
+  MOE_CHECK_DIMS(d);
+  MOE_OPTIONAL(dev_status);
+  MOE_OPTIONAL(hq);
+  MOE_OPTIONAL(hsc);
+  MOE_OPTIONAL(h);
+  if ((hq == nullptr) != (hsc == nullptr)) return MOE_ERR_INVALID_ARG;
+  if (hq == nullptr && h == nullptr) return MOE_ERR_INVALID_ARG;
+  if (d.T == 0) return MOE_OK;
+  MOE_REQUIRE(xq);
+  MOE_REQUIRE(xsc);
+  MOE_REQUIRE(wq);
+  MOE_REQUIRE(wsc);
+  MOE_REQUIRE(group_offsets);
+  moe::MxGemmCall c{true, xq, xsc, wq, wsc, group_offsets, hq, hsc, h, dev_status, d};
+  return from_cuda(moe::launch_mx_grouped_gemm(c, stream));
+}
+
+moe_status moe_mx_grouped_gemm_fc2(const uint8_t* hq, const uint8_t* hsc, const uint8_t* wq,
+                                   const uint8_t* wsc, const int32_t* group_offsets,
+                                   moe_bf16* ys, int32_t* dev_status, moe_dims d,
+                                   cudaStream_t stream) {
+  MOE_CHECK_DIMS(d);
+  MOE_OPTIONAL(dev_status);
+  if (d.T == 0) return MOE_OK;
+  MOE_REQUIRE(hq);
+  MOE_REQUIRE(hsc);
+  MOE_REQUIRE(wq);
+  MOE_REQUIRE(wsc);
+  MOE_REQUIRE(group_offsets);
+  MOE_REQUIRE(ys);
+  moe::MxGemmCall c{false, hq, hsc, wq, wsc, group_offsets, nullptr, nullptr, ys, dev_status, d};
+  return from_cuda(moe::launch_mx_grouped_gemm(c, stream));
 }
 
 moe_status moe_selftest_bounded_wait(int32_t* dev_status, uint64_t limit_ns, cudaStream_t stream) {

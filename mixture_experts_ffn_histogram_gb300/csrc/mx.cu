@@ -1,0 +1,785 @@
+// MXFP8 forward of the MoE block on the fifth-generation tensor cores.
+//
+// What is computed (TransformerEngine "[DRAFT][JAX] Optimize MoE block",
+// Changes item 1: MXFP8 quantization in the MoE block; Flowchart: "Grouped
+// FC1 quantize and GEMM" -> "Activation and grouped FC2 GEMM"), with MXFP8
+// read as the OCP MX v1.0 format: blocks of 32 elements along the
+// contraction axis share an E8M0 scale 2^s, s = max(floor(log2 amax) - 8,
+// -127); elements are E4M3 codes of v / 2^s, nearest-even, saturating.
+//   grouped quantize   the expert weights (once, transposed so that the
+//                      contraction axis is contiguous) and the tokens while
+//                      they are gathered into expert-sorted order
+//   FC1 + SwiGLU       h = silu(a[:F]) * a[F:], a = x . wi[e] on MX operands,
+//                      h quantized to MX in the epilogue for FC2
+//   FC2                ys = h . wo[e] on MX operands, bf16 output
+//
+// GEMM design: persistent warp-specialised kernel, one CTA per SM, 192
+// threads, 128-row x 256-column tiles, k-blocks of 128 fp8 elements.
+//   warp 0     producer: per k-block one TMA box of A (128 x 128 B), one of
+//              B (256 x 128 B, 128-byte swizzle) and two bulk copies of the
+//              tile's scale blocks (512 B for A, 1 KB for B) into a 4-deep
+//              shared-memory ring.
+//   warp 1     TMEM allocation and MMA issue: per k-block the scale blocks
+//              are copied into TMEM (tcgen05.cp) and each 32-element k-step
+//              issues two block-scaled MMAs (M = 128, N = 128), one per tile
+//              half, sharing the A operand.
+//   warps 2-5  epilogue: one row per thread (tcgen05.ld), SwiGLU and MX
+//              quantization of h (FC1) or bf16 conversion (FC2), TMA stores
+//              from per-warp staging.
+// TMEM: three 128-column accumulator regions used in rotation (a tile takes
+// two; the next tile needs only the region its predecessor's first half
+// frees first), and 16 columns of scale factors per ring stage.  Two full
+// 256-column accumulators would leave no columns for the scales.
+// The scale-factor layout in TMEM (checked on GB300 by an in-bounds probe
+// whose scale bytes encoded their own positions): for 128 rows and a
+// 128-element k-block, the 512-byte block holds row m's scale for k-step j
+// at byte (m % 32) * 16 + (m / 32) * 4 + j; tcgen05.cp.32x128b.warpx4 places
+// it in four TMEM columns and the instruction descriptor's scale ids pick j.
+#include <cuda.h>
+#include <cuda_fp8.h>
+
+#include <atomic>
+#include <cstdlib>
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "mx.h"
+
+namespace moe {
+
+namespace {
+
+constexpr int kMaxE = 1024;
+constexpr int kThreads = 192;
+constexpr int kStages = 4;
+constexpr int kAStage = 128 * 128;               // 16 KB
+constexpr int kBStage = 256 * 128;               // 32 KB
+constexpr int kSfaOff = kAStage + kBStage;       // 48 KB
+constexpr int kSfbOff = kSfaOff + 1024;
+constexpr int kStageBytes = kSfbOff + 1024;      // 50 KB (keeps every operand 1024-aligned)
+constexpr uint32_t kTxBytes = kAStage + kBStage + 512 + 1024;
+constexpr int kEpiBytes = 4096;                  // staging per epilogue warp
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kSfCol0 = 384;                // scale slots: 16 columns per stage
+
+struct MxCtl {
+  uint64_t full[kStages];
+  uint64_t empty[kStages];
+  uint64_t tfull[3];
+  uint64_t tempty[3];
+  uint32_t tmem_base;
+  int abort_flag;
+  int off[kMaxE + 1];  // group offsets
+  int tb[kMaxE + 1];   // first 128-row tile of each group (exclusive prefix)
+};
+constexpr size_t kSmemBytes =
+    1024 + static_cast<size_t>(kStages) * kStageBytes + 4 * kEpiBytes + sizeof(MxCtl);
+static_assert(kSmemBytes <= 227 * 1024, "shared memory");
+
+// ------------------------------------------------------------ MX helpers
+// Shared exponent of a block from its largest magnitude: floor(log2 amax) - 8
+// from the fp32 exponent field, -127 for zero and fp32 subnormals (whose
+// floor(log2) - 8 lies below -127 anyway).
+__device__ __forceinline__ int mx_shared_exp(float amax) {
+  const int be = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFFu);
+  if (be == 0) return -127;
+  return max(be - 127 - 8, -127);
+}
+// 2^-s as an fp32 (s in [-127, 119], so 127 - s is a normal exponent)
+__device__ __forceinline__ float mx_inv_scale(int s) {
+  return __uint_as_float(static_cast<uint32_t>(127 - s) << 23);
+}
+// Codes of 32 values (already multiplied by 2^-s), packed little-endian.
+__device__ __forceinline__ void mx_pack32(const float (&v)[32], float mul, uint32_t (&w)[8]) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(v[4 * i] * mul, v[4 * i + 1] * mul),
+                                                 __NV_SATFINITE, __NV_E4M3);
+    const uint32_t hi = __nv_cvt_float2_to_fp8x2(
+        make_float2(v[4 * i + 2] * mul, v[4 * i + 3] * mul), __NV_SATFINITE, __NV_E4M3);
+    w[i] = (lo & 0xFFFFu) | (hi << 16);
+  }
+}
+// Quantize 32 values: codes into w, returns the scale byte.
+__device__ __forceinline__ uint32_t mx_quant32(const float (&v)[32], uint32_t (&w)[8]) {
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+  const int s = mx_shared_exp(amax);
+  mx_pack32(v, mx_inv_scale(s), w);
+  return static_cast<uint32_t>(s + 127);
+}
+// Byte of row m (0..127) and 32-element step j (0..3) inside a 512-byte
+// scale block.
+__device__ __forceinline__ int sf_byte(int m, int j) { return (m & 31) * 16 + (m >> 5) * 4 + j; }
+
+// Group offsets into shared memory (all threads), then the exclusive prefix
+// of ceil(rows/128) over the groups (one warp).  Ends with __syncthreads().
+__device__ __forceinline__ void load_tile_bases(const int32_t* offs, int E, int* s_off, int* s_tb,
+                                                int scan_warp) {
+  for (int i = threadIdx.x; i <= E; i += blockDim.x) s_off[i] = __ldg(offs + i);
+  __syncthreads();
+  if (static_cast<int>(threadIdx.x >> 5) == scan_warp) {
+    const int lane = threadIdx.x & 31;
+    const int per = (E + 31) / 32;
+    const int e0 = min(E, lane * per), e1 = min(E, e0 + per);
+    int local = 0;
+    for (int e = e0; e < e1; ++e) local += (s_off[e + 1] - s_off[e] + 127) >> 7;
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    int run = incl - local;
+    for (int e = e0; e < e1; ++e) {
+      s_tb[e] = run;
+      run += (s_off[e + 1] - s_off[e] + 127) >> 7;
+    }
+    if (lane == 31) s_tb[E] = incl;
+  }
+  __syncthreads();
+}
+
+// Group of sorted row r: the largest e with s_off[e] <= r (r < s_off[E]).
+__device__ __forceinline__ int group_of_row(const int* s_off, int E, int r) {
+  int lo = 0, hi = E - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (s_off[mid] <= r) lo = mid;
+    else hi = mid - 1;
+  }
+  return lo;
+}
+
+// ------------------------------------------------------- weight quantize
+// w [E][Kd][N] bf16 (the contraction axis Kd is the middle one) -> q [E][N][Kd]
+// codes with blocked scales [E][KB][NBp][512].  FC1's output rows are
+// interleaved in 64-row chunks, gate chunk then up chunk: logical column n
+// of wi (gate f = n < F, up f = n - F) lands on row 128*(f/64) + 64*(n >= F)
+// + f%64, so that each 128-row half of a 256-row tile holds 64 gate and the
+// matching 64 up columns.  One block quantizes 128 contraction rows x 64
+// columns: coalesced 128-byte loads, a transpose through shared memory, one
+// 32-element block per thread.
+__global__ void __launch_bounds__(256) mx_quantize_weights_kernel(const uint16_t* __restrict__ w,
+                                                                  uint8_t* __restrict__ q,
+                                                                  uint8_t* __restrict__ sc, int Kd,
+                                                                  int N, int KB, int NBp,
+                                                                  int fc1) {
+  __shared__ float tile[128][65];
+  const int n0 = blockIdx.x * 64, k0 = blockIdx.y * 128, e = blockIdx.z;
+  const int tid = threadIdx.x;
+  const uint16_t* src = w + (static_cast<size_t>(e) * Kd + k0) * N + n0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int idx = tid + 256 * i;
+    const int row = idx >> 3, c8 = idx & 7;
+    if (k0 + row < Kd) {
+      const uint4 u = *reinterpret_cast<const uint4*>(src + static_cast<size_t>(row) * N + 8 * c8);
+      const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        tile[row][8 * c8 + 2 * j] = bf16lo(wv[j]);
+        tile[row][8 * c8 + 2 * j + 1] = bf16hi(wv[j]);
+      }
+    }
+  }
+  __syncthreads();
+  const int n = tid & 63, blk = tid >> 6;
+  const int k = k0 + 32 * blk;
+  if (k >= Kd) return;
+  float v[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = tile[32 * blk + i][n];
+  uint32_t codes[8];
+  const uint32_t sbyte = mx_quant32(v, codes);
+  const int ng = n0 + n;
+  int p = ng;
+  if (fc1) {
+    const int F = N / 2;
+    const int f = ng < F ? ng : ng - F;
+    p = 128 * (f >> 6) + (ng < F ? 0 : 64) + (f & 63);
+  }
+  uint4* dst = reinterpret_cast<uint4*>(q + (static_cast<size_t>(e) * N + p) * Kd + k);
+  dst[0] = make_uint4(codes[0], codes[1], codes[2], codes[3]);
+  dst[1] = make_uint4(codes[4], codes[5], codes[6], codes[7]);
+  const size_t blkoff = ((static_cast<size_t>(e) * KB + (k >> 7)) * NBp + (p >> 7)) * 512;
+  sc[blkoff + sf_byte(p & 127, (k & 127) >> 5)] = static_cast<uint8_t>(sbyte);
+}
+
+// ------------------------------------------------ permute + quantize
+// xq[pos[t,k]] = codes of x[t] (each token row quantized once, written K
+// times); the scales go to the tile-blocked layout of the destination row:
+// block (tb[e] + i/128) * KB + k-block, row i % 128, where i is the row's
+// index inside its group e.  One warp per token; lane l handles 32-element
+// blocks l, l+32, ...
+constexpr int kPqWarps = 8;
+__global__ void __launch_bounds__(256) mx_permute_quantize_kernel(
+    const uint16_t* __restrict__ x, const int32_t* __restrict__ pos,
+    const int32_t* __restrict__ offs, uint8_t* __restrict__ xq, uint8_t* __restrict__ xsc, int T,
+    int D, int K, int E, int KB) {
+  __shared__ int s_off[kMaxE + 1];
+  __shared__ int s_tb[kMaxE + 1];
+  __shared__ int s_row[kPqWarps][32];
+  __shared__ int s_blk[kPqWarps][32];  // scale block base (bytes) of the slot's row
+  __shared__ int s_m[kPqWarps][32];
+  load_tile_bases(offs, E, s_off, s_tb, 0);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nb = D / 32;
+  const int R = s_off[E];
+  for (int t = blockIdx.x * kPqWarps + warp; t < T; t += gridDim.x * kPqWarps) {
+    if (lane < K) {
+      int r = __ldg(pos + static_cast<size_t>(t) * K + lane);
+      if (r >= R) r = -1;
+      int blk = 0, m = 0;
+      if (r >= 0) {
+        const int e = group_of_row(s_off, E, r);
+        const int i = r - s_off[e];
+        blk = (s_tb[e] + (i >> 7)) * KB;
+        m = i & 127;
+      }
+      s_row[warp][lane] = r;
+      s_blk[warp][lane] = blk;
+      s_m[warp][lane] = m;
+    }
+    __syncwarp();
+    const uint16_t* xr = x + static_cast<size_t>(t) * D;
+    for (int b = lane; b < nb; b += 32) {
+      const uint4* src = reinterpret_cast<const uint4*>(xr + 32 * b);
+      float v[32];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint4 u = src[i];
+        const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          v[8 * i + 2 * j] = bf16lo(wv[j]);
+          v[8 * i + 2 * j + 1] = bf16hi(wv[j]);
+        }
+      }
+      uint32_t codes[8];
+      const uint8_t sbyte = static_cast<uint8_t>(mx_quant32(v, codes));
+      const uint4 c0 = make_uint4(codes[0], codes[1], codes[2], codes[3]);
+      const uint4 c1 = make_uint4(codes[4], codes[5], codes[6], codes[7]);
+      for (int k = 0; k < K; ++k) {
+        const int r = s_row[warp][k];
+        if (r < 0) continue;
+        uint4* dst = reinterpret_cast<uint4*>(xq + static_cast<size_t>(r) * D + 32 * b);
+        dst[0] = c0;
+        dst[1] = c1;
+        const size_t blk = static_cast<size_t>(s_blk[warp][k]) + (b >> 2);
+        xsc[blk * 512 + sf_byte(s_m[warp][k], b & 3)] = sbyte;
+      }
+    }
+    __syncwarp();
+  }
+}
+
+// ---------------------------------------------------------------- GEMM
+struct MxParams {
+  const uint8_t* sfa;   // A scales, tile-blocked [tiles][KB][512]
+  const uint8_t* sfb;   // B scales [E][KB][NBp][512]
+  const int32_t* offs;
+  uint8_t* hq;          // FC1: h codes [R][F] or nullptr
+  uint8_t* hsc;         // FC1: h scales, tile-blocked [tiles][KBF][512]
+  __nv_bfloat16* out;   // FC1: h bf16 [R][F] or nullptr; FC2: ys [R][D]
+  int32_t* status;
+  uint64_t limit_ns;
+  int E;
+  int Kd;       // contraction length (D for FC1, F for FC2)
+  int KB;       // k-blocks of Kd
+  int Nout;     // FC1: F (h columns); FC2: D
+  int NBp;      // 128-row blocks of B per (expert, k-block), even
+  int n_tiles;  // 256-row B tiles per expert
+  int KBF;      // FC1: k-blocks of F (h scale blocks per tile row)
+};
+
+struct MxTile {
+  int e, g, nt, row0, rows;
+};
+
+__device__ __forceinline__ MxTile mx_decode(int t, const MxParams& p, const MxCtl& s) {
+  MxTile T;
+  T.g = t / p.n_tiles;
+  T.nt = t - T.g * p.n_tiles;
+  int lo = 0, hi = p.E - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (s.tb[mid] <= T.g) lo = mid;
+    else hi = mid - 1;
+  }
+  T.e = lo;
+  T.row0 = s.off[lo] + (T.g - s.tb[lo]) * 128;
+  T.rows = min(128, s.off[lo + 1] - T.row0);
+  return T;
+}
+
+// Whether half h (128 B rows) of tile nt holds any output column.
+template <bool FC1>
+__device__ __forceinline__ bool half_valid(int nt, int h, const MxParams& p) {
+  return FC1 ? 64 * (2 * nt + h) < p.Nout : 256 * nt + 128 * h < p.Nout;
+}
+
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
+                                          uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+// Descriptor of a 512-byte scale block in shared memory (32 rows of 16 B,
+// no swizzle) for tcgen05.cp.
+__device__ __forceinline__ uint64_t sf_desc(uint32_t saddr) {
+  return static_cast<uint64_t>((saddr >> 4) & 0x3FFFu) | (static_cast<uint64_t>(128 >> 4) << 16) |
+         (static_cast<uint64_t>(128 >> 4) << 32) | (1ull << 46);
+}
+__device__ __forceinline__ void tmem_cp_sf(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
+               : "memory");
+}
+// Block-scaled MMA: e4m3 A (M = 128) and B (N = 128), both K-major, K = 32,
+// E8M0 scales at sfa/sfb in TMEM.
+__device__ __forceinline__ void umma_mxf8(uint32_t d, uint64_t ad, uint64_t bd, uint32_t idesc,
+                                          uint32_t sfa, uint32_t sfb, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], "
+      "[%5], p;\n\t}" ::"r"(d),
+      "l"(ad), "l"(bd), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+      : "memory");
+}
+// Instruction descriptor, kind::mxf8f6f4 with block scaling: B scale id in
+// bits 4-5, A and B formats e4m3 (0) in bits 7-9 and 10-12, K-major A and
+// B, N >> 3 in bits 17-22, E8M0 scales (bit 23), M >> 4 in bits 24-28, A
+// scale id in bits 29-30.
+__host__ __device__ constexpr uint32_t mx_idesc(int M, int N, int sf_id) {
+  return (static_cast<uint32_t>(sf_id) << 4) | ((static_cast<uint32_t>(N) >> 3) << 17) |
+         (1u << 23) | ((static_cast<uint32_t>(M) >> 4) << 24) |
+         (static_cast<uint32_t>(sf_id) << 29);
+}
+
+__device__ __forceinline__ float silu(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
+
+// 16 packed bf16 pairs = 32 columns (half `hh` of a 64-column row) of row
+// `lane` in a 128-byte-swizzled staging buffer.
+__device__ __forceinline__ void put_half_sw(uint8_t* buf, int lane, int hh, const uint32_t (&w)[16]) {
+  uint8_t* row = buf + lane * 128;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int unit = hh * 4 + j;
+    *reinterpret_cast<uint4*>(row + ((unit ^ (lane & 7)) << 4)) =
+        make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+  }
+}
+
+template <bool FC1>
+__global__ void __launch_bounds__(kThreads, 1)
+    mx_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
+                   const __grid_constant__ CUtensorMap map_b,
+                   const __grid_constant__ CUtensorMap map_o, const MxParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* ring = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+  uint8_t* epi = ring + kStages * kStageBytes;
+  MxCtl& s = *reinterpret_cast<MxCtl*>(epi + 4 * kEpiBytes);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_map(&map_a);
+    tma_prefetch_map(&map_b);
+    tma_prefetch_map(&map_o);
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&s.full[i], 1);
+      mbar_init(&s.empty[i], 1);
+    }
+    for (int i = 0; i < 3; ++i) {
+      mbar_init(&s.tfull[i], 1);
+      mbar_init(&s.tempty[i], 4);
+    }
+    s.abort_flag = 0;
+    mbar_fence_init();
+  }
+  if (warp == 1) {
+    tmem_alloc<1>(&s.tmem_base, kTmemCols);
+    tmem_relinquish<1>();
+  }
+  load_tile_bases(p.offs, p.E, s.off, s.tb, 2);  // ends with __syncthreads
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = s.tmem_base;
+  const WaitCtl wc{&s.abort_flag, p.status, p.limit_ns};
+  const int ntiles = s.tb[p.E] * p.n_tiles;
+
+  if (warp == 0) {
+    // -------------------------------------------------------- producer
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0;
+      uint32_t fills[kStages] = {0, 0, 0, 0};
+      bool aborted = false;
+      for (int t = blockIdx.x; t < ntiles && !aborted; t += gridDim.x) {
+        const MxTile T = mx_decode(t, p, s);
+        const uint8_t* sfa = p.sfa + static_cast<size_t>(T.g) * p.KB * 512;
+        const uint8_t* sfb =
+            p.sfb + (static_cast<size_t>(T.e) * p.KB * p.NBp + 2 * T.nt) * 512;
+        for (int kb = 0; kb < p.KB; ++kb) {
+          if (!mbar_wait(&s.empty[stage], phase ^ 1u, wc)) { aborted = true; break; }
+          uint8_t* st = ring + stage * kStageBytes;
+          mbar_arrive_expect_tx(&s.full[stage], kTxBytes);
+          tma_load_2d(st, &map_a, &s.full[stage], kb * 128, T.row0);
+          tma_load_3d(st + kAStage, &map_b, &s.full[stage], kb * 128, 256 * T.nt, T.e);
+          bulk_load(st + kSfaOff, sfa + static_cast<size_t>(kb) * 512, 512, &s.full[stage]);
+          bulk_load(st + kSfbOff, sfb + static_cast<size_t>(kb) * p.NBp * 512, 1024,
+                    &s.full[stage]);
+          ++fills[stage];
+          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        }
+      }
+      if (aborted) {  // copies in flight land before the CTA exits
+        for (int i = 0; i < kStages; ++i)
+          if (fills[i] > 0) (void)mbar_wait_drain(&s.full[i], (fills[i] - 1u) & 1u, 100000000ull);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------- MMA
+    uint32_t stage = 0, phase = 0, it = 0;
+    uint32_t commits[kStages] = {0, 0, 0, 0};
+    int last_stage = -1;
+    bool aborted = false;
+    for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
+      const MxTile T = mx_decode(t, p, s);
+      const bool h1 = half_valid<FC1>(T.nt, 1, p);
+      const uint32_t q0 = 2 * it, q1 = 2 * it + 1;  // uses of the region rotation
+      const uint32_t r0 = q0 % 3, r1 = q1 % 3;
+      bool ok = mbar_wait(&s.tempty[r0], ((q0 / 3) & 1u) ^ 1u, wc);
+      ok = ok && mbar_wait(&s.tempty[r1], ((q1 / 3) & 1u) ^ 1u, wc);
+      if (!__all_sync(0xffffffffu, ok)) { aborted = true; break; }
+      tc_fence_after();
+      const uint32_t d0 = tmem_base + 128 * r0, d1 = tmem_base + 128 * r1;
+      for (int kb = 0; kb < p.KB; ++kb) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&s.full[stage], phase, wc))) {
+          aborted = true;
+          break;
+        }
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t a_addr = smem_u32(ring + stage * kStageBytes);
+          const uint32_t b_addr = a_addr + kAStage;
+          const uint32_t sf = tmem_base + kSfCol0 + 16 * stage;
+          tmem_cp_sf(sf, sf_desc(a_addr + kSfaOff));
+          tmem_cp_sf(sf + 4, sf_desc(a_addr + kSfbOff));
+          if (h1) tmem_cp_sf(sf + 8, sf_desc(a_addr + kSfbOff + 512));
+          const int nk = min(4, (p.Kd - kb * 128) / 32);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            if (kk >= nk) break;
+            const uint32_t idesc = mx_idesc(128, 128, kk);
+            const uint64_t ad = smem_desc_sw128(a_addr + 32 * kk, 16, 1024);
+            const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
+            umma_mxf8(d0, ad, smem_desc_sw128(b_addr + 32 * kk, 16, 1024), idesc, sf, sf + 4, acc);
+            if (h1)
+              umma_mxf8(d1, ad, smem_desc_sw128(b_addr + 16384 + 32 * kk, 16, 1024), idesc, sf,
+                        sf + 8, acc);
+          }
+          umma_commit<1>(&s.empty[stage]);
+        }
+        __syncwarp();
+        ++commits[stage];
+        last_stage = static_cast<int>(stage);
+        if (++stage == kStages) { stage = 0; phase ^= 1u; }
+      }
+      if (aborted) break;
+      if (lane == 0) {
+        umma_commit<1>(&s.tfull[r0]);
+        umma_commit<1>(&s.tfull[r1]);
+      }
+      __syncwarp();
+    }
+    if (aborted && last_stage >= 0)  // issued MMAs finish before TMEM is freed
+      (void)mbar_wait_drain(&s.empty[last_stage], (commits[last_stage] - 1u) & 1u, 100000000ull);
+  } else {
+    // -------------------------------------------------------- epilogue
+    const int q = warp & 3;  // TMEM lane quarter: rows 32q..32q+31 of the tile
+    uint8_t* buf = epi + (warp - 2) * kEpiBytes;
+    uint32_t it = 0;
+    bool aborted = false;
+    for (int t = blockIdx.x; t < ntiles && !aborted; t += gridDim.x, ++it) {
+      const MxTile T = mx_decode(t, p, s);
+      const int vw = min(32, max(0, T.rows - 32 * q));  // valid rows of this warp
+      const int y = T.row0 + 32 * q;
+      const bool row_ok = lane < vw;
+      const long r = static_cast<long>(y) + lane;
+      for (int hh = 0; hh < 2; ++hh) {
+        const uint32_t qn = 2 * it + hh, reg = qn % 3;
+        if (!__all_sync(0xffffffffu, mbar_wait(&s.tfull[reg], (qn / 3) & 1u, wc))) {
+          aborted = true;
+          break;
+        }
+        tc_fence_after();
+        const bool live = half_valid<FC1>(T.nt, hh, p) && vw > 0;
+        uint32_t v[128];
+        if (live) {
+          const uint32_t ta = tmem_base + 128 * reg + (static_cast<uint32_t>(32 * q) << 16);
+          tmem_ld_32x32b_x32(ta, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+          tmem_ld_32x32b_x32(ta + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+          tmem_ld_32x32b_x32(ta + 64, *reinterpret_cast<uint32_t(*)[32]>(&v[64]));
+          tmem_ld_32x32b_x32(ta + 96, *reinterpret_cast<uint32_t(*)[32]>(&v[96]));
+          tmem_ld_wait();
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s.tempty[reg]);
+        if (!live) continue;
+        if constexpr (FC1) {
+          // gate = columns 0..63, up = 64..127 of the region: h for f0..f0+63
+          const int f0 = 64 * (2 * T.nt + hh);
+          float hv[64];
+#pragma unroll
+          for (int j = 0; j < 64; ++j)
+            hv[j] = silu(__uint_as_float(v[j])) * __uint_as_float(v[64 + j]);
+          if (p.out != nullptr && row_ok) {
+            uint4* dst = reinterpret_cast<uint4*>(p.out + r * p.Nout + f0);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              dst[i] = make_uint4(pack_bf16x2(hv[8 * i], hv[8 * i + 1]),
+                                  pack_bf16x2(hv[8 * i + 2], hv[8 * i + 3]),
+                                  pack_bf16x2(hv[8 * i + 4], hv[8 * i + 5]),
+                                  pack_bf16x2(hv[8 * i + 6], hv[8 * i + 7]));
+          }
+          if (p.hq != nullptr) {
+            uint32_t c[2][8];
+            uint32_t sb[2];
+#pragma unroll
+            for (int b = 0; b < 2; ++b) {
+              float blk[32];
+#pragma unroll
+              for (int i = 0; i < 32; ++i) blk[i] = hv[32 * b + i];
+              sb[b] = mx_quant32(blk, c[b]);
+            }
+            if (row_ok) {
+              const int m = 32 * q + lane;
+              uint8_t* sc = p.hsc + (static_cast<size_t>(T.g) * p.KBF + (f0 >> 7)) * 512 +
+                            sf_byte(m, (f0 & 127) >> 5);
+              *reinterpret_cast<uint16_t*>(sc) = static_cast<uint16_t>(sb[0] | (sb[1] << 8));
+            }
+            if (vw == 32) {
+              if (lane == 0) bulk_wait_read<0>();
+              __syncwarp();
+              uint4* row = reinterpret_cast<uint4*>(buf + lane * 64);
+#pragma unroll
+              for (int b = 0; b < 2; ++b) {
+                row[2 * b] = make_uint4(c[b][0], c[b][1], c[b][2], c[b][3]);
+                row[2 * b + 1] = make_uint4(c[b][4], c[b][5], c[b][6], c[b][7]);
+              }
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) {
+                tma_store_2d(&map_o, buf, f0, y);
+                bulk_commit();
+              }
+            } else if (row_ok) {
+              uint4* dst = reinterpret_cast<uint4*>(p.hq + r * p.Nout + f0);
+#pragma unroll
+              for (int b = 0; b < 2; ++b) {
+                dst[2 * b] = make_uint4(c[b][0], c[b][1], c[b][2], c[b][3]);
+                dst[2 * b + 1] = make_uint4(c[b][4], c[b][5], c[b][6], c[b][7]);
+              }
+            }
+          }
+        } else {
+          const int d0 = 256 * T.nt + 128 * hh;
+#pragma unroll
+          for (int ch = 0; ch < 2; ++ch) {
+            const int col = d0 + 64 * ch;
+            if (col >= p.Nout) break;
+            uint32_t w0[16], w1[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              w0[i] = pack_bf16x2(__uint_as_float(v[64 * ch + 2 * i]),
+                                  __uint_as_float(v[64 * ch + 2 * i + 1]));
+              w1[i] = pack_bf16x2(__uint_as_float(v[64 * ch + 32 + 2 * i]),
+                                  __uint_as_float(v[64 * ch + 32 + 2 * i + 1]));
+            }
+            if (vw == 32) {
+              if (lane == 0) bulk_wait_read<0>();
+              __syncwarp();
+              put_half_sw(buf, lane, 0, w0);
+              put_half_sw(buf, lane, 1, w1);
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) {
+                tma_store_2d(&map_o, buf, col, y);
+                bulk_commit();
+              }
+            } else if (row_ok) {
+              uint4* dst = reinterpret_cast<uint4*>(p.out + r * p.Nout + col);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w0[4 * i], w0[4 * i + 1], w0[4 * i + 2], w0[4 * i + 3]);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) dst[4 + i] = make_uint4(w1[4 * i], w1[4 * i + 1], w1[4 * i + 2], w1[4 * i + 3]);
+            }
+          }
+        }
+      }
+    }
+    if (lane == 0) bulk_wait_all();  // every store has finished before the CTA exits
+    __syncwarp();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc<1>(tmem_base, kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------ host side
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
+
+// Tensor map, dims innermost first, strides in bytes for dims 1..rank-1.
+bool make_map(CUtensorMap* m, CUtensorMapDataType type, const void* base, int rank,
+              const uint64_t* dims, const uint64_t* strides, const uint32_t* box,
+              CUtensorMapSwizzle swz) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t gd[3], gs[2];
+  cuuint32_t bd[3], es[3] = {1, 1, 1};
+  for (int i = 0; i < rank; ++i) {
+    gd[i] = dims[i];
+    bd[i] = box[i];
+  }
+  for (int i = 0; i + 1 < rank; ++i) gs[i] = strides[i];
+  return fn(m, type, rank, const_cast<void*>(base), gd, gs, bd, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <bool FC1>
+cudaError_t launch_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mo,
+                        const MxParams& p, long max_tiles, cudaStream_t s) {
+  auto kern = mx_gemm_kernel<FC1>;
+  static std::atomic<bool> attr_set[64];
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!attr_set[dev].load(std::memory_order_acquire)) {
+    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(kSmemBytes));
+    if (err != cudaSuccess) return err;
+    attr_set[dev].store(true, std::memory_order_release);
+  }
+  long grid = sm_count();
+  if (max_tiles < grid) grid = max_tiles;
+  if (grid <= 0) return cudaSuccess;
+  kern<<<static_cast<int>(grid), kThreads, kSmemBytes, s>>>(ma, mb, mo, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_mx_quantize_weights(const uint16_t* w, uint8_t* q, uint8_t* sc, int E, int Kd,
+                                       int N, bool fc1_interleave, cudaStream_t s) {
+  const int KB = static_cast<int>(mx_kblocks(Kd));
+  const int NBp = static_cast<int>(mx_weight_row_blocks(N));
+  dim3 grid(static_cast<unsigned>(N / 64), static_cast<unsigned>(KB), static_cast<unsigned>(E));
+  mx_quantize_weights_kernel<<<grid, 256, 0, s>>>(w, q, sc, Kd, N, KB, NBp, fc1_interleave ? 1 : 0);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_mx_permute_quantize(const uint16_t* x, const int32_t* pos, const int32_t* offs,
+                                       uint8_t* xq, uint8_t* xsc, const moe_dims& d,
+                                       cudaStream_t s) {
+  if (d.T == 0) return cudaSuccess;
+  long blocks = mx_cdiv(d.T, kPqWarps);
+  const long cap = 8L * sm_count();
+  if (blocks > cap) blocks = cap;
+  mx_permute_quantize_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(
+      x, pos, offs, xq, xsc, d.T, d.D, d.K, d.E, static_cast<int>(mx_kblocks(d.D)));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_mx_grouped_gemm(const MxGemmCall& c, cudaStream_t s) {
+  const moe_dims& d = c.d;
+  const long R = static_cast<long>(d.T) * d.K;
+  if (R == 0) return cudaSuccess;
+  MxParams p{};
+  p.sfa = c.a_sc;
+  p.sfb = c.b_sc;
+  p.offs = c.offs;
+  p.hq = c.hq;
+  p.hsc = c.hsc;
+  p.out = reinterpret_cast<__nv_bfloat16*>(c.out);
+  p.status = c.dev_status;
+  p.limit_ns = kDefaultWaitLimitNs;
+  p.E = d.E;
+  const long Nb = c.fc1 ? 2L * d.F : d.D;  // B rows per expert
+  p.Kd = c.fc1 ? d.D : d.F;
+  p.KB = static_cast<int>(mx_kblocks(p.Kd));
+  p.Nout = c.fc1 ? d.F : d.D;
+  p.NBp = static_cast<int>(mx_weight_row_blocks(Nb));
+  p.n_tiles = static_cast<int>(mx_cdiv(Nb, 256));
+  p.KBF = static_cast<int>(mx_kblocks(d.F));
+  CUtensorMap ma, mb, mo;
+  const uint64_t adims[2] = {static_cast<uint64_t>(p.Kd), static_cast<uint64_t>(R)};
+  const uint64_t astr[1] = {static_cast<uint64_t>(p.Kd)};
+  const uint32_t abox[2] = {128, 128};
+  const uint64_t bdims[3] = {static_cast<uint64_t>(p.Kd), static_cast<uint64_t>(Nb),
+                             static_cast<uint64_t>(d.E)};
+  const uint64_t bstr[2] = {static_cast<uint64_t>(p.Kd), static_cast<uint64_t>(p.Kd) * Nb};
+  const uint32_t bbox[3] = {128, 256, 1};
+  bool ok = make_map(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT8, c.a, 2, adims, astr, abox,
+                     CU_TENSOR_MAP_SWIZZLE_128B) &&
+            make_map(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, c.b, 3, bdims, bstr, bbox,
+                     CU_TENSOR_MAP_SWIZZLE_128B);
+  if (!ok) return cudaErrorInvalidValue;
+  const long max_tiles = mx_tile_bound(d) * p.n_tiles;
+  if (c.fc1) {
+    // h codes: 32 rows x 64 bytes per store, unswizzled staging (or a dummy
+    // map over the bf16 h when only that is written)
+    const uint64_t odims[2] = {static_cast<uint64_t>(d.F), static_cast<uint64_t>(R)};
+    const uint32_t obox[2] = {64, 32};
+    if (c.hq != nullptr) {
+      const uint64_t ostr[1] = {static_cast<uint64_t>(d.F)};
+      ok = make_map(&mo, CU_TENSOR_MAP_DATA_TYPE_UINT8, c.hq, 2, odims, ostr, obox,
+                    CU_TENSOR_MAP_SWIZZLE_NONE);
+    } else {
+      const uint64_t ostr[1] = {static_cast<uint64_t>(d.F) * 2};
+      ok = make_map(&mo, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, c.out, 2, odims, ostr, obox,
+                    CU_TENSOR_MAP_SWIZZLE_128B);
+    }
+    if (!ok) return cudaErrorInvalidValue;
+    return launch_gemm<true>(ma, mb, mo, p, max_tiles, s);
+  }
+  const uint64_t odims[2] = {static_cast<uint64_t>(d.D), static_cast<uint64_t>(R)};
+  const uint64_t ostr[1] = {static_cast<uint64_t>(d.D) * 2};
+  const uint32_t obox[2] = {64, 32};
+  ok = make_map(&mo, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, c.out, 2, odims, ostr, obox,
+                CU_TENSOR_MAP_SWIZZLE_128B);
+  if (!ok) return cudaErrorInvalidValue;
+  return launch_gemm<false>(ma, mb, mo, p, max_tiles, s);
+}
+
+}  // namespace moe

@@ -1,0 +1,98 @@
+"""The byte layouts of libmoe.so's MXFP8 buffers, written out from their
+statement in include/moe.h, for the tests: pack the oracle's logical codes
+and scales into the library's layouts, and read the library's buffers back
+into logical form.  Shares no code with the oracle or the CUDA path.
+
+Logical forms (the oracle's): activation codes [R, k] with scales [R, k/32];
+weight codes [E, N, k] (row n = output column n) with scales [E, N, k/32].
+"""
+from __future__ import annotations
+
+import numpy as np
+
+
+def cdiv(a, b):
+    return -(-a // b)
+
+
+def sf_byte(m, j):
+    """Byte of row m (0..127) and 32-element step j (0..3) in a 512-byte block."""
+    return (m % 32) * 16 + (m // 32) * 4 + j
+
+
+def tile_bases(offs):
+    """First 128-row tile of each group and the total: prefix of ceil(size/128)."""
+    gs = np.diff(np.asarray(offs, np.int64))
+    tiles = cdiv(gs, 128)
+    return np.concatenate([[0], np.cumsum(tiles)])
+
+
+def act_scale_index(offs, k):
+    """Flat byte index [R_used, k/32] of each row's scales in the tile-blocked
+    layout (rows 0 .. offs[E]-1 in expert-sorted order)."""
+    offs = np.asarray(offs, np.int64)
+    E = len(offs) - 1
+    R = int(offs[E])
+    tb = tile_bases(offs)
+    kb = cdiv(k, 128)
+    r = np.arange(R)
+    e = np.searchsorted(offs, r, side="right") - 1
+    i = r - offs[e]
+    g = tb[e] + i // 128
+    m = i % 128
+    b = np.arange(k // 32)
+    return ((g[:, None] * kb + b[None, :] // 4) * 512 + sf_byte(m[:, None], b[None, :] % 4))
+
+
+def pack_act_scales(sc, offs, nbytes):
+    buf = np.full(nbytes, 127, np.uint8)
+    idx = act_scale_index(offs, sc.shape[1] * 32)
+    buf[idx] = sc[: idx.shape[0]]
+    return buf
+
+
+def unpack_act_scales(buf, offs, k):
+    return np.asarray(buf)[act_scale_index(offs, k)]
+
+
+def weight_rows(N, interleave):
+    """Physical row of each logical output column n (FC1: 64-row chunks,
+    gate then up)."""
+    n = np.arange(N)
+    if not interleave:
+        return n
+    F = N // 2
+    f = np.where(n < F, n, n - F)
+    return 128 * (f // 64) + 64 * (n >= F) + f % 64
+
+
+def weight_scale_index(E, N, k, interleave):
+    """Flat byte index [E, N, k/32] of each (expert, logical row, block)."""
+    kb = cdiv(k, 128)
+    nbp = 2 * cdiv(N, 256)
+    p = weight_rows(N, interleave)
+    e = np.arange(E)[:, None, None]
+    b = np.arange(k // 32)[None, None, :]
+    pp = p[None, :, None]
+    return ((e * kb + b // 4) * nbp + pp // 128) * 512 + sf_byte(pp % 128, b % 4)
+
+
+def weight_scale_bytes(E, N, k):
+    return E * cdiv(k, 128) * 2 * cdiv(N, 256) * 512
+
+
+def pack_weight(q, sc, interleave):
+    """Logical (codes [E,N,k], scales [E,N,k/32]) -> library (codes, scale bytes)."""
+    E, N, k = q.shape
+    codes = np.empty_like(q)
+    codes[:, weight_rows(N, interleave), :] = q
+    buf = np.full(weight_scale_bytes(E, N, k), 127, np.uint8)
+    buf[weight_scale_index(E, N, k, interleave)] = sc
+    return codes, buf
+
+
+def unpack_weight(codes, buf, interleave):
+    E, N, k = codes.shape
+    q = codes[:, weight_rows(N, interleave), :]
+    sc = np.asarray(buf)[weight_scale_index(E, N, k, interleave)]
+    return q, sc
