@@ -52,6 +52,7 @@ def parse():
     ap.add_argument("--fwd-only", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-mx", action="store_true", help="skip the MXFP8 forward measurement")
     ap.add_argument("--tokens", type=int, default=None,
                     help="override T (small cases for profiling; not a bench line)")
     ap.add_argument("--experts", type=int, default=None,
@@ -404,6 +405,103 @@ class Step:
 
 
 GEMMS = ("fc1", "fc2", "fc2_dlhs", "fc2_drhs", "fc1_dlhs", "fc1_drhs")
+
+MX_STEPS = ("route", "permute_quantize", "fc1", "fc2", "combine")
+
+
+def mx_bytes(kind, T, D, E, K, F):
+    """Algorithmic bytes of the MXFP8 forward's steps: e4m3 codes (1 B) plus
+    one scale byte per 32 elements."""
+    R = T * K
+    return {
+        "permute_quantize": 2 * T * D + R * D + R * D // 32 + 4 * T * K,
+        "fc1": R * D + R * D // 32 + 2 * E * F * D + 2 * E * F * D // 32 + R * F + R * F // 32,
+        "fc2": R * F + R * F // 32 + E * D * F + E * D * F // 32 + 2 * R * D,
+    }[kind]
+
+
+def measure_mx(wl, inp, steps, pk, flush):
+    """The MXFP8 forward (route, permute + quantize, FC1 + SwiGLU + quantize
+    h, FC2, combine) through the C ABI, weights quantized once before the
+    timed loop; an event pair around every launch."""
+    from mixture_experts_ffn_histogram_gb300 import binding as B
+    from mixture_experts_ffn_histogram_gb300.block import MoEBlockMX
+    blk = MoEBlockMX(wl.T, wl.D, wl.E, wl.K, wl.F, wl.score_mode)
+    d = blk.d
+    q0, q1, q2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+    q0.record()
+    B.moe_mx_quantize_wi(inp["wi"], blk.wiq, blk.wisc, d)
+    q1.record()
+    B.moe_mx_quantize_wo(inp["wo"], blk.woq, blk.wosc, d)
+    q2.record()
+    if wl.score_mode == B.SCORE_GIVEN:
+        blk.ids.copy_(inp["ids"])
+        blk.w.copy_(inp["w"])
+
+    def run(ev):
+        def mark():
+            if ev is not None:
+                e = torch.cuda.Event(enable_timing=True)
+                e.record()
+                ev.append(e)
+        mark()
+        B.moe_route_histogram(inp.get("logits"), inp.get("bias"), blk.mode, blk.ids, blk.w,
+                              blk.group_sizes, blk.group_offsets, blk.pos, blk.row_src,
+                              blk.status, blk.ws, d)
+        mark()
+        B.moe_mx_permute_quantize(inp["x"], blk.pos, blk.group_offsets, blk.xq, blk.xsc, d)
+        mark()
+        B.moe_mx_grouped_gemm_fc1_swiglu(blk.xq, blk.xsc, blk.wiq, blk.wisc, blk.group_offsets,
+                                         blk.hq, blk.hsc, None, blk.status, d)
+        mark()
+        B.moe_mx_grouped_gemm_fc2(blk.hq, blk.hsc, blk.woq, blk.wosc, blk.group_offsets, blk.ys,
+                                  blk.status, d)
+        mark()
+        B.moe_combine(blk.ys, blk.w, blk.pos, blk.out, d)
+        mark()
+
+    for _ in range(3):
+        run(None)
+    torch.cuda.synchronize()
+    evs = []
+    for _ in range(steps):
+        if flush is not None:
+            flush.zero_()
+        ev = []
+        run(ev)
+        evs.append(ev)
+    torch.cuda.synchronize()
+    if int(blk.status.item()) != 0:
+        raise RuntimeError(f"device status {int(blk.status.item())} after the MX steps")
+    times = {n: [ev[i].elapsed_time(ev[i + 1]) * 1e-3 for ev in evs] for i, n in enumerate(MX_STEPS)}
+    step_s = sum(ev[0].elapsed_time(ev[-1]) * 1e-3 for ev in evs) / steps
+    fp8_peak = 2.0 * pk["bf16_sustained"]
+    kern = {}
+    for n in MX_STEPS:
+        avg = sum(times[n]) / len(times[n])
+        kern[n] = {"avg_us": avg * 1e6, "median_us": statistics.median(times[n]) * 1e6}
+        if n in ("fc1", "fc2"):
+            fl = gemm_flops(n, wl.R, wl.D, wl.F)
+            kern[n]["tflops"] = fl / avg / 1e12
+            kern[n]["frac_tensor"] = fl / avg / 1e12 / fp8_peak
+            kern[n]["frac_hbm"] = mx_bytes(n, wl.T, wl.D, wl.E, wl.K, wl.F) / avg / 1e9 / pk["hbm"]
+        elif n == "permute_quantize":
+            kern[n]["frac_hbm"] = mx_bytes(n, wl.T, wl.D, wl.E, wl.K, wl.F) / avg / 1e9 / pk["hbm"]
+        else:
+            kern[n]["frac_hbm"] = hbm_bytes(n, wl.T, wl.D, wl.E, wl.K, wl.F) / avg / 1e9 / pk["hbm"]
+    return {
+        "metric": "MoE block tokens/s (fwd, MXFP8)",
+        "value": wl.T / step_s,
+        "unit": "tokens/s",
+        "ms_per_step": step_s * 1e3,
+        "steps": steps,
+        "dtype": "e4m3 x e4m3 (E8M0 scales per 32), fp32 accumulation, bf16 out",
+        "fp8_peak_tflops": fp8_peak,
+        "fp8_peak_source": f"{pk['source']} bf16_tflops_sustained x 2 (nominal fp8/bf16 ratio)",
+        "weights_quantize_us": {"wi": q0.elapsed_time(q1) * 1e3, "wo": q1.elapsed_time(q2) * 1e3},
+        "gpu_launches_per_step": len(MX_STEPS),
+        "kernels": kern,
+    }
 L2_BYTES = 129 << 20
 
 
@@ -478,6 +576,11 @@ def run_ours(args, dist, rank, world):
         torch.cuda.synchronize()
         fwd_tps = wl.T * args.steps / (s0.elapsed_time(s1) * 1e-3)
         del fstep
+
+    # ---- the MXFP8 forward on the same inputs (a separate timed loop)
+    mx = None
+    if not args.no_mx:
+        mx = measure_mx(wl_rank, inp, args.steps, peaks(), flush)
 
     # ---- end to end through the C ABI from pinned host buffers
     e2e = None
@@ -560,6 +663,9 @@ def run_ours(args, dist, rank, world):
     }
     if fwd_tps is not None:
         line["fwd_tokens_per_s"] = world * fwd_tps
+    if mx is not None:
+        mx["value"] *= world
+        line["mxfp8_forward"] = mx
     if rank == 0:
         print(json.dumps(line), flush=True)
 

@@ -78,6 +78,61 @@ class MoEBlock:
         return self.dx
 
 
+class MoEBlockMX:
+    """The block's forward in MXFP8 (inference): the expert weights are
+    quantized once by ``set_weights``; each ``forward`` routes, quantizes the
+    tokens while permuting them, runs FC1 + SwiGLU and FC2 on the tensor
+    cores' block-scaled MMA (h quantized in FC1's epilogue) and combines.
+    Every buffer is allocated once, in the library's MX layouts."""
+
+    def __init__(self, T, D, E, K, F, score_mode=B.SCORE_SOFTMAX_TOPK, device="cuda"):
+        self.d = d = B.dims(T, D, E, K, F)
+        self.T, self.D, self.E, self.K, self.F = T, D, E, K, F
+        self.R = R = T * K
+        self.mode = score_mode
+        dev = torch.device(device)
+        i32 = torch.int32
+
+        def u8(which):
+            return torch.empty(max(B.moe_mx_bytes(d, which), 16), dtype=torch.uint8, device=dev)
+
+        self.ids = torch.empty((T, K), dtype=i32, device=dev)
+        self.w = torch.empty((T, K), dtype=torch.float32, device=dev)
+        self.group_sizes = torch.empty(E, dtype=i32, device=dev)
+        self.group_offsets = torch.empty(E + 1, dtype=i32, device=dev)
+        self.pos = torch.empty((T, K), dtype=i32, device=dev)
+        self.row_src = torch.empty(R, dtype=i32, device=dev)
+        self.status = torch.zeros(1, dtype=i32, device=dev)
+        self.ws = torch.empty(max(B.moe_workspace_bytes(d), 256), dtype=torch.uint8, device=dev)
+        self.wiq, self.wisc = u8(B.MX_WIQ), u8(B.MX_WISC)
+        self.woq, self.wosc = u8(B.MX_WOQ), u8(B.MX_WOSC)
+        self.xq, self.xsc = u8(B.MX_XQ), u8(B.MX_XSC)
+        self.hq, self.hsc = u8(B.MX_HQ), u8(B.MX_HSC)
+        self.ys = torch.empty((R, D), dtype=torch.bfloat16, device=dev)
+        self.out = torch.empty((T, D), dtype=torch.bfloat16, device=dev)
+
+    def set_weights(self, wi, wo, stream=None):
+        B.moe_mx_quantize_wi(wi, self.wiq, self.wisc, self.d, stream)
+        B.moe_mx_quantize_wo(wo, self.woq, self.wosc, self.d, stream)
+
+    def forward(self, x, logits=None, bias=None, ids=None, w=None, stream=None):
+        d = self.d
+        if self.mode == B.SCORE_GIVEN:
+            self.ids.copy_(ids)
+            self.w.copy_(w)
+        B.moe_route_histogram(logits, bias, self.mode, self.ids, self.w, self.group_sizes,
+                              self.group_offsets, self.pos, self.row_src, self.status, self.ws,
+                              d, stream)
+        B.moe_mx_permute_quantize(x, self.pos, self.group_offsets, self.xq, self.xsc, d, stream)
+        B.moe_mx_grouped_gemm_fc1_swiglu(self.xq, self.xsc, self.wiq, self.wisc,
+                                         self.group_offsets, self.hq, self.hsc, None,
+                                         self.status, d, stream)
+        B.moe_mx_grouped_gemm_fc2(self.hq, self.hsc, self.woq, self.wosc, self.group_offsets,
+                                  self.ys, self.status, d, stream)
+        B.moe_combine(self.ys, self.w, self.pos, self.out, d, stream)
+        return self.out
+
+
 class HostPipeline:
     """Steps of a MoEBlock (fwd+bwd when the block trains, else forward only)
     whose per-step activations live in pinned host memory, with the
