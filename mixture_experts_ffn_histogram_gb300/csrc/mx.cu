@@ -19,22 +19,28 @@
 //              B (256 x 128 B, 128-byte swizzle) and two bulk copies of the
 //              tile's scale blocks (512 B for A, 1 KB for B) into a 4-deep
 //              shared-memory ring.
-//   warp 1     TMEM allocation and MMA issue: per k-block the scale blocks
-//              are copied into TMEM (tcgen05.cp) and each 32-element k-step
-//              issues two block-scaled MMAs (M = 128, N = 128), one per tile
-//              half, sharing the A operand.
+//   warp 1     TMEM allocation and MMA issue by one thread: per k-block the
+//              scale blocks are copied into TMEM (tcgen05.cp) and each
+//              32-element k-step issues one block-scaled MMA (M = 128,
+//              N = 256).  The thread's issue rate bounds the kernel: two
+//              N = 128 MMAs per k-step took 25% longer, and per-k-step
+//              descriptor arithmetic and warp votes cost 15% more, so the
+//              descriptors are stage bases plus constant offsets and no other
+//              lane takes part.
 //   warps 2-5  epilogue: one row per thread (tcgen05.ld), SwiGLU and MX
 //              quantization of h (FC1) or bf16 conversion (FC2), TMA stores
 //              from per-warp staging.
-// TMEM: three 128-column accumulator regions used in rotation (a tile takes
-// two; the next tile needs only the region its predecessor's first half
-// frees first), and 16 columns of scale factors per ring stage.  Two full
-// 256-column accumulators would leave no columns for the scales.
+// TMEM: two 256-column accumulators; the tile in one keeps its scale slots
+// (16 columns per ring stage, 64 in all) in the first columns of the other,
+// which the epilogue reads first and releases early (sffree), so the next
+// tile waits only for that half of the previous tile's accumulator.  (Two
+// whole accumulators would leave no columns for scales otherwise.)
 // The scale-factor layout in TMEM (checked on GB300 by an in-bounds probe
 // whose scale bytes encoded their own positions): for 128 rows and a
 // 128-element k-block, the 512-byte block holds row m's scale for k-step j
 // at byte (m % 32) * 16 + (m / 32) * 4 + j; tcgen05.cp.32x128b.warpx4 places
 // it in four TMEM columns and the instruction descriptor's scale ids pick j.
+// For N = 256 the B scales of rows 128-255 are the next block, four columns on.
 #include <cuda.h>
 #include <cuda_fp8.h>
 
@@ -61,13 +67,15 @@ constexpr int kStageBytes = kSfbOff + 1024;      // 50 KB (keeps every operand 1
 constexpr uint32_t kTxBytes = kAStage + kBStage + 512 + 1024;
 constexpr int kEpiBytes = 4096;                  // staging per epilogue warp
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kSfCol0 = 384;                // scale slots: 16 columns per stage
+constexpr uint32_t kSfStride = 16;               // scale slot per stage: A 4 + B 8 columns (16-aligned)
+constexpr uint32_t kSfCols = kStages * kSfStride;  // 64, inside half 0 of a buffer
 
 struct MxCtl {
   uint64_t full[kStages];
   uint64_t empty[kStages];
-  uint64_t tfull[3];
-  uint64_t tempty[3];
+  uint64_t tfull[2];   // accumulator buffer b holds a finished tile
+  uint64_t tempty[2];  // the epilogue has read all of buffer b
+  uint64_t sffree[2];  // the epilogue has read buffer b's first kSfCols columns
   uint32_t tmem_base;
   int abort_flag;
   int off[kMaxE + 1];  // group offsets
@@ -396,9 +404,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&s.full[i], 1);
       mbar_init(&s.empty[i], 1);
     }
-    for (int i = 0; i < 3; ++i) {
+    for (int i = 0; i < 2; ++i) {
       mbar_init(&s.tfull[i], 1);
       mbar_init(&s.tempty[i], 4);
+      mbar_init(&s.sffree[i], 4);
     }
     s.abort_flag = 0;
     mbar_fence_init();
@@ -446,61 +455,66 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------- MMA
-    uint32_t stage = 0, phase = 0, it = 0;
-    uint32_t commits[kStages] = {0, 0, 0, 0};
-    int last_stage = -1;
-    bool aborted = false;
-    for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
-      const MxTile T = mx_decode(t, p, s);
-      const bool h1 = half_valid<FC1>(T.nt, 1, p);
-      const uint32_t q0 = 2 * it, q1 = 2 * it + 1;  // uses of the region rotation
-      const uint32_t r0 = q0 % 3, r1 = q1 % 3;
-      bool ok = mbar_wait(&s.tempty[r0], ((q0 / 3) & 1u) ^ 1u, wc);
-      ok = ok && mbar_wait(&s.tempty[r1], ((q1 / 3) & 1u) ^ 1u, wc);
-      if (!__all_sync(0xffffffffu, ok)) { aborted = true; break; }
-      tc_fence_after();
-      const uint32_t d0 = tmem_base + 128 * r0, d1 = tmem_base + 128 * r1;
-      for (int kb = 0; kb < p.KB; ++kb) {
-        if (!__all_sync(0xffffffffu, mbar_wait(&s.full[stage], phase, wc))) {
+    // one thread: waits, scale copies, MMAs and commits
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0, it = 0;
+      uint32_t commits[kStages] = {0, 0, 0, 0};
+      int last_stage = -1;
+      bool aborted = false;
+      // descriptors of stage 0's A and scale blocks; stage i adds i * kStageBytes >> 4,
+      // a k-step 2 (32 B >> 4)
+      const uint64_t da0 = smem_desc_sw128(smem_u32(ring), 16, 1024);
+      const uint64_t ds0 = sf_desc(smem_u32(ring) + kSfaOff);
+      for (int t = blockIdx.x; t < ntiles && !aborted; t += gridDim.x, ++it) {
+        const MxTile T = mx_decode(t, p, s);
+        const bool h1 = half_valid<FC1>(T.nt, 1, p);
+        // tile it accumulates in buffer it % 2 (256 columns) while its scale
+        // slots sit in the first kSfCols columns of the other buffer, which
+        // the epilogue empties first
+        const uint32_t buf = it & 1u, use = it >> 1;
+        if (!mbar_wait(&s.tempty[buf], (use & 1u) ^ 1u, wc) ||
+            (it > 0 && !mbar_wait(&s.sffree[buf ^ 1u], ((it - 1) >> 1) & 1u, wc))) {
           aborted = true;
           break;
         }
         tc_fence_after();
-        if (lane == 0) {
-          const uint32_t a_addr = smem_u32(ring + stage * kStageBytes);
-          const uint32_t b_addr = a_addr + kAStage;
-          const uint32_t sf = tmem_base + kSfCol0 + 16 * stage;
-          tmem_cp_sf(sf, sf_desc(a_addr + kSfaOff));
-          tmem_cp_sf(sf + 4, sf_desc(a_addr + kSfbOff));
-          if (h1) tmem_cp_sf(sf + 8, sf_desc(a_addr + kSfbOff + 512));
-          const int nk = min(4, (p.Kd - kb * 128) / 32);
+        const uint32_t d0 = tmem_base + 256 * buf;
+        const uint32_t sf_base = tmem_base + 256 * (buf ^ 1u);
+        const uint32_t idn = h1 ? 256u : 128u;
+        for (int kb = 0; kb < p.KB; ++kb) {
+          if (!mbar_wait(&s.full[stage], phase, wc)) { aborted = true; break; }
+          tc_fence_after();
+          const uint32_t sf = sf_base + kSfStride * stage;
+          const uint64_t a0 = da0 + stage * (kStageBytes >> 4);
+          const uint64_t b0 = a0 + (kAStage >> 4), b1 = b0 + (16384 >> 4);
+          const uint64_t s0 = ds0 + stage * (kStageBytes >> 4);
+          tmem_cp_sf(sf, s0);
+          tmem_cp_sf(sf + 4, s0 + (1024 >> 4));
+          if (h1) tmem_cp_sf(sf + 8, s0 + (1536 >> 4));
+          if (kb * 128 + 128 <= p.Kd) {
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            if (kk >= nk) break;
-            const uint32_t idesc = mx_idesc(128, 128, kk);
-            const uint64_t ad = smem_desc_sw128(a_addr + 32 * kk, 16, 1024);
-            const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
-            umma_mxf8(d0, ad, smem_desc_sw128(b_addr + 32 * kk, 16, 1024), idesc, sf, sf + 4, acc);
-            if (h1)
-              umma_mxf8(d1, ad, smem_desc_sw128(b_addr + 16384 + 32 * kk, 16, 1024), idesc, sf,
-                        sf + 8, acc);
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
+              umma_mxf8(d0, a0 + 2 * kk, b0 + 2 * kk, mx_idesc(128, idn, kk), sf, sf + 4, acc);
+            }
+          } else {
+            const int nk = (p.Kd - kb * 128) / 32;
+            for (int kk = 0; kk < nk; ++kk) {
+              const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
+              umma_mxf8(d0, a0 + 2 * kk, b0 + 2 * kk, mx_idesc(128, idn, kk), sf, sf + 4, acc);
+            }
           }
           umma_commit<1>(&s.empty[stage]);
+          ++commits[stage];
+          last_stage = static_cast<int>(stage);
+          if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
-        __syncwarp();
-        ++commits[stage];
-        last_stage = static_cast<int>(stage);
-        if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        if (aborted) break;
+        umma_commit<1>(&s.tfull[buf]);
       }
-      if (aborted) break;
-      if (lane == 0) {
-        umma_commit<1>(&s.tfull[r0]);
-        umma_commit<1>(&s.tfull[r1]);
-      }
-      __syncwarp();
+      if (aborted && last_stage >= 0)  // issued MMAs finish before TMEM is freed
+        (void)mbar_wait_drain(&s.empty[last_stage], (commits[last_stage] - 1u) & 1u, 100000000ull);
     }
-    if (aborted && last_stage >= 0)  // issued MMAs finish before TMEM is freed
-      (void)mbar_wait_drain(&s.empty[last_stage], (commits[last_stage] - 1u) & 1u, 100000000ull);
   } else {
     // -------------------------------------------------------- epilogue
     const int q = warp & 3;  // TMEM lane quarter: rows 32q..32q+31 of the tile
@@ -513,26 +527,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int y = T.row0 + 32 * q;
       const bool row_ok = lane < vw;
       const long r = static_cast<long>(y) + lane;
+      const uint32_t bsel = it & 1u;
+      if (!__all_sync(0xffffffffu, mbar_wait(&s.tfull[bsel], (it >> 1) & 1u, wc))) {
+        aborted = true;
+        break;
+      }
+      tc_fence_after();
       for (int hh = 0; hh < 2; ++hh) {
-        const uint32_t qn = 2 * it + hh, reg = qn % 3;
-        if (!__all_sync(0xffffffffu, mbar_wait(&s.tfull[reg], (qn / 3) & 1u, wc))) {
-          aborted = true;
-          break;
-        }
-        tc_fence_after();
         const bool live = half_valid<FC1>(T.nt, hh, p) && vw > 0;
         uint32_t v[128];
         if (live) {
-          const uint32_t ta = tmem_base + 128 * reg + (static_cast<uint32_t>(32 * q) << 16);
+          const uint32_t ta = tmem_base + 256 * bsel + 128 * hh + (static_cast<uint32_t>(32 * q) << 16);
           tmem_ld_32x32b_x32(ta, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
           tmem_ld_32x32b_x32(ta + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
           tmem_ld_32x32b_x32(ta + 64, *reinterpret_cast<uint32_t(*)[32]>(&v[64]));
           tmem_ld_32x32b_x32(ta + 96, *reinterpret_cast<uint32_t(*)[32]>(&v[96]));
           tmem_ld_wait();
         }
+        // half 0 holds the next tile's scale slots (its first kSfCols
+        // columns); half 1 ends this warp's reads of the buffer
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&s.tempty[reg]);
+        if (lane == 0) mbar_arrive(hh == 0 ? &s.sffree[bsel] : &s.tempty[bsel]);
         if (!live) continue;
         if constexpr (FC1) {
           // gate = columns 0..63, up = 64..127 of the region: h for f0..f0+63
