@@ -137,10 +137,15 @@ NCU_NAME = {
 }
 
 
+# the files holding the device code of the bf16 block's kernels (the traffic
+# figures under profiles/ are valid while these are unchanged)
+KERNEL_SOURCES = ("common.cuh", "gemm.cu", "kernels.h", "permute_combine.cu", "route.cu")
+
+
 def source_hash() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "mixture_experts_ffn_histogram_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    for f in KERNEL_SOURCES:
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
