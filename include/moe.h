@@ -207,6 +207,38 @@ moe_status moe_grouped_gemm_fc1_swiglu_bwd(const moe_bf16* grad, const moe_bf16*
                                            moe_dims d, cudaStream_t stream);
 
 /*
+ * FC1 for one range of experts whose weights are a separate buffer: the
+ * split-expert wi layout [Fused p/c, Context item 2 and Commits table row 3]
+ * stores wi as expert halves that are gathered separately and consumed by
+ * two chained grouped GEMM calls writing into one shared output buffer.
+ * Here any split works: a call covers experts [e_begin, e_end) with
+ * wi_part = their [e_end - e_begin, D, 2F] weights, and computes exactly
+ * the rows moe_grouped_gemm_fc1_swiglu computes for those groups (rows
+ * group_offsets[e_begin] .. group_offsets[e_end]-1 of h, and of z when
+ * given); other rows are untouched.  Calls over ranges that tile [0, E)
+ * give the whole FC1.  0 <= e_begin < e_end <= E, else MOE_ERR_INVALID_ARG.
+ */
+moe_status moe_grouped_gemm_fc1_swiglu_experts(const moe_bf16* xs, const moe_bf16* wi_part,
+                                               const int32_t* group_offsets, int32_t e_begin,
+                                               int32_t e_end, moe_bf16* h, moe_bf16* z,
+                                               int32_t* dev_status, void* ws, moe_dims d,
+                                               cudaStream_t stream);
+
+/*
+ * The FC1 backward for one range of experts (see above): from dz bf16
+ * [R,2F], dlhs writes the rows of groups [e_begin, e_end) of dxs against
+ * wi_part, and drhs writes dwi_part [e_end - e_begin, D, 2F] (zero for an
+ * empty group).  Either output may be NULL, not both; ws is required with
+ * dwi_part (the counter of the drhs's dynamic tile schedule).
+ */
+moe_status moe_grouped_gemm_fc1_bwd_experts(const moe_bf16* dz, const moe_bf16* xs,
+                                            const moe_bf16* wi_part,
+                                            const int32_t* group_offsets, int32_t e_begin,
+                                            int32_t e_end, moe_bf16* dxs, moe_bf16* dwi_part,
+                                            int32_t* dev_status, void* ws, moe_dims d,
+                                            cudaStream_t stream);
+
+/*
  * FC2 [TE MoE, Flowchart "grouped FC2 GEMM"]:
  *   ys[r,:] = bf16(h[r] . wo[e])  (fp32 accumulation).
  *   h bf16 [R,F];  wo bf16 [E,F,D];  ys bf16 [R,D] out.

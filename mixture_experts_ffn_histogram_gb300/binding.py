@@ -33,6 +33,7 @@ ENTRY_POINTS = (
     "moe_combine", "moe_combine_bwd", "moe_selftest_bounded_wait", "moe_route_histogram_noalloc",
     "moe_mx_bytes", "moe_mx_quantize_wi", "moe_mx_quantize_wo", "moe_mx_permute_quantize",
     "moe_mx_grouped_gemm_fc1_swiglu", "moe_mx_grouped_gemm_fc2",
+    "moe_grouped_gemm_fc1_swiglu_experts", "moe_grouped_gemm_fc1_bwd_experts",
 )
 
 # moe_mx_buffer
@@ -97,6 +98,8 @@ def lib() -> ctypes.CDLL:
             "moe_selftest_bounded_wait": ([P, ctypes.c_uint64, P], I),
             "moe_route_histogram_noalloc": ([P, P, I, P, P, P, P, P, P, P, D_, P], I),
             "moe_mx_bytes": ([D_, I], ctypes.c_size_t),
+            "moe_grouped_gemm_fc1_swiglu_experts": ([P, P, P, I, I, P, P, P, P, D_, P], I),
+            "moe_grouped_gemm_fc1_bwd_experts": ([P, P, P, P, I, I, P, P, P, P, D_, P], I),
             "moe_mx_quantize_wi": ([P, P, P, D_, P], I),
             "moe_mx_quantize_wo": ([P, P, P, D_, P], I),
             "moe_mx_permute_quantize": ([P, P, P, P, P, D_, P], I),
@@ -215,6 +218,20 @@ def moe_combine_bwd(dout, ys, w, pos, dys, dw, d: MoeDims, stream=None):
 def moe_selftest_bounded_wait(dev_status, limit_ns: int, stream=None):
     _ok("moe_selftest_bounded_wait",
         lib().moe_selftest_bounded_wait(_p(dev_status), int(limit_ns), _s(stream)))
+
+
+def moe_grouped_gemm_fc1_swiglu_experts(xs, wi_part, group_offsets, e_begin, e_end, h, z,
+                                        dev_status, ws, d: MoeDims, stream=None):
+    _ok("moe_grouped_gemm_fc1_swiglu_experts", lib().moe_grouped_gemm_fc1_swiglu_experts(
+        _p(xs), _p(wi_part), _p(group_offsets), int(e_begin), int(e_end), _p(h), _p(z),
+        _p(dev_status), _p(ws), d, _s(stream)))
+
+
+def moe_grouped_gemm_fc1_bwd_experts(dz, xs, wi_part, group_offsets, e_begin, e_end, dxs,
+                                     dwi_part, dev_status, ws, d: MoeDims, stream=None):
+    _ok("moe_grouped_gemm_fc1_bwd_experts", lib().moe_grouped_gemm_fc1_bwd_experts(
+        _p(dz), _p(xs), _p(wi_part), _p(group_offsets), int(e_begin), int(e_end), _p(dxs),
+        _p(dwi_part), _p(dev_status), _p(ws), d, _s(stream)))
 
 
 # ------------------------------------------------------------------ MXFP8

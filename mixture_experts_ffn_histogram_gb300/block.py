@@ -60,8 +60,16 @@ class MoEBlock:
                               self.group_offsets, self.pos, self.row_src, self.status, self.ws,
                               d, stream)
         B.moe_permute(x, self.pos, self.xs, d, stream)
-        B.moe_grouped_gemm_fc1_swiglu(self.xs, wi, self.group_offsets, self.h, self.z,
-                                      self.status, self.ws, d, stream)
+        if isinstance(wi, (list, tuple)):
+            # split-expert layout: wi as expert-range buffers, FC1 as chained
+            # grouped GEMM calls into the one h (and z)
+            for e0, e1, part in self._ranges(wi):
+                B.moe_grouped_gemm_fc1_swiglu_experts(self.xs, part, self.group_offsets, e0, e1,
+                                                      self.h, self.z, self.status, self.ws, d,
+                                                      stream)
+        else:
+            B.moe_grouped_gemm_fc1_swiglu(self.xs, wi, self.group_offsets, self.h, self.z,
+                                          self.status, self.ws, d, stream)
         B.moe_grouped_gemm_fc2(self.h, wo, self.group_offsets, self.ys, self.status, self.ws, d,
                                stream)
         B.moe_combine(self.ys, self.w, self.pos, self.out, d, stream)
@@ -72,10 +80,32 @@ class MoEBlock:
         B.moe_combine_bwd(dy, self.ys, self.w, self.pos, self.dys, self.dw, d, stream)
         B.moe_grouped_gemm_fc2_bwd(self.dys, self.h, wo, self.z, self.group_offsets, self.dz,
                                    self.dwo, self.status, self.ws, d, stream)
-        B.moe_grouped_gemm_fc1_swiglu_bwd(self.dz, None, self.xs, wi, self.group_offsets,
-                                          self.dxs, self.dwi, self.status, self.ws, d, stream)
+        if isinstance(wi, (list, tuple)):
+            # split-expert layout: dxs chained over the ranges; dwi_parts[i]
+            # is the gradient of wi[i]
+            if getattr(self, "dwi_parts", None) is None or \
+                    [p.shape for p in self.dwi_parts] != [p.shape for p in wi]:
+                self.dwi_parts = [torch.empty_like(p) for p in wi]
+            for (e0, e1, part), dpart in zip(self._ranges(wi), self.dwi_parts):
+                B.moe_grouped_gemm_fc1_bwd_experts(self.dz, self.xs, part, self.group_offsets, e0,
+                                                   e1, self.dxs, dpart, self.status, self.ws, d,
+                                                   stream)
+        else:
+            B.moe_grouped_gemm_fc1_swiglu_bwd(self.dz, None, self.xs, wi, self.group_offsets,
+                                              self.dxs, self.dwi, self.status, self.ws, d, stream)
         B.moe_permute_bwd(self.dxs, self.pos, self.dx, d, stream)
         return self.dx
+
+    def _ranges(self, parts):
+        """(e_begin, e_end, tensor) of each expert-range buffer of a split wi."""
+        out, e0 = [], 0
+        for part in parts:
+            e1 = e0 + int(part.shape[0])
+            out.append((e0, e1, part))
+            e0 = e1
+        if e0 != self.E:
+            raise ValueError(f"the wi parts cover {e0} experts, the block has {self.E}")
+        return out
 
 
 class MoEBlockMX:

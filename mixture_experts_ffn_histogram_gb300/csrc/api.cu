@@ -210,6 +210,73 @@ moe_status moe_grouped_gemm_fc1_swiglu(const moe_bf16* xs, const moe_bf16* wi,
   return from_cuda(moe::launch_grouped_gemm(c, stream));
 }
 
+// Dims of a GEMM over experts [e_begin, e_end): the R = T*K rows are passed
+// as T = R, K = 1 (the grouped GEMMs use only R), E = the range's experts.
+static moe_dims range_dims(const moe_dims& d, int32_t e_begin, int32_t e_end) {
+  moe_dims r = d;
+  r.T = d.T * d.K;
+  r.K = 1;
+  r.E = e_end - e_begin;
+  return r;
+}
+
+moe_status moe_grouped_gemm_fc1_swiglu_experts(const moe_bf16* xs, const moe_bf16* wi_part,
+                                               const int32_t* group_offsets, int32_t e_begin,
+                                               int32_t e_end, moe_bf16* h, moe_bf16* z,
+                                               int32_t* dev_status, void* ws, moe_dims d,
+                                               cudaStream_t stream) {
+  (void)ws;
+  MOE_CHECK_DIMS(d);
+  if (e_begin < 0 || e_end <= e_begin || e_end > d.E) return MOE_ERR_INVALID_ARG;
+  MOE_OPTIONAL(dev_status);
+  MOE_OPTIONAL(z);
+  if (d.T == 0) return MOE_OK;
+  MOE_REQUIRE(xs);
+  MOE_REQUIRE(wi_part);
+  MOE_REQUIRE(group_offsets);  // the caller's whole array; the range reads a 4-byte-aligned slice
+  MOE_REQUIRE(h);
+  GemmCall c{GemmKind::kFc1, xs, wi_part, group_offsets + e_begin, h, z, nullptr, dev_status,
+             range_dims(d, e_begin, e_end)};
+  return from_cuda(moe::launch_grouped_gemm(c, stream));
+}
+
+moe_status moe_grouped_gemm_fc1_bwd_experts(const moe_bf16* dz, const moe_bf16* xs,
+                                            const moe_bf16* wi_part,
+                                            const int32_t* group_offsets, int32_t e_begin,
+                                            int32_t e_end, moe_bf16* dxs, moe_bf16* dwi_part,
+                                            int32_t* dev_status, void* ws, moe_dims d,
+                                            cudaStream_t stream) {
+  MOE_CHECK_DIMS(d);
+  if (e_begin < 0 || e_end <= e_begin || e_end > d.E) return MOE_ERR_INVALID_ARG;
+  MOE_OPTIONAL(dev_status);
+  MOE_OPTIONAL(dxs);
+  MOE_OPTIONAL(dwi_part);
+  if (dxs == nullptr && dwi_part == nullptr) return MOE_ERR_INVALID_ARG;
+  MOE_REQUIRE(group_offsets);
+  const moe_dims rd = range_dims(d, e_begin, e_end);
+  const int32_t* offs = group_offsets + e_begin;
+  if (d.T > 0) {
+    MOE_REQUIRE(dz);
+    if (dxs != nullptr) MOE_REQUIRE(wi_part);
+    if (dwi_part != nullptr) {
+      MOE_REQUIRE(xs);
+      MOE_REQUIRE(ws);
+    }
+  }
+  if (dxs != nullptr && d.T > 0) {
+    GemmCall c{GemmKind::kDlhsFc1, dz, wi_part, offs, dxs, nullptr, nullptr, dev_status, rd};
+    moe_status st = from_cuda(moe::launch_grouped_gemm(c, stream));
+    if (st != MOE_OK) return st;
+  }
+  if (dwi_part != nullptr) {
+    GemmCall c{GemmKind::kDrhsFc1, xs, dz, offs, dwi_part, nullptr, nullptr, dev_status, rd};
+    c.tile_ctr = static_cast<unsigned int*>(ws);
+    moe_status st = from_cuda(moe::launch_grouped_gemm(c, stream));
+    if (st != MOE_OK) return st;
+  }
+  return MOE_OK;
+}
+
 moe_status moe_grouped_gemm_fc2(const moe_bf16* h, const moe_bf16* wo,
                                 const int32_t* group_offsets, moe_bf16* ys, int32_t* dev_status,
                                 void* ws, moe_dims d, cudaStream_t stream) {
