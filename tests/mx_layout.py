@@ -96,3 +96,25 @@ def unpack_weight(codes, buf, interleave):
     q = codes[:, weight_rows(N, interleave), :]
     sc = np.asarray(buf)[weight_scale_index(E, N, k, interleave)]
     return q, sc
+
+
+def act_scale_index_rows(offs, rows, k):
+    """act_scale_index for the given sorted-order rows only."""
+    offs = np.asarray(offs, np.int64)
+    tb = tile_bases(offs)
+    kb = cdiv(k, 128)
+    r = np.asarray(rows, np.int64)
+    e = np.searchsorted(offs, r, side="right") - 1
+    i = r - offs[e]
+    g = tb[e] + i // 128
+    m = i % 128
+    b = np.arange(k // 32)
+    return ((g[:, None] * kb + b[None, :] // 4) * 512 + sf_byte(m[:, None], b[None, :] % 4))
+
+
+def unpack_weight_expert(codes_e, buf, e, N, k, interleave):
+    """Logical (codes [N,k], scales [N,k/32]) of expert e from the library's
+    weight buffers (codes_e = that expert's [N, k] codes)."""
+    per = cdiv(k, 128) * 2 * cdiv(N, 256) * 512
+    q, sc = unpack_weight(codes_e[None], np.asarray(buf)[e * per:(e + 1) * per], interleave)
+    return q[0], sc[0]

@@ -9,11 +9,14 @@ Bars:
   so the error is the bf16 rounding of the output (<= 2^-8 relative) plus fp32
   summation error (~1e-6 relative);
 - FC1's MX codes of h are decided from the kernel's fp32 h.  The oracle
-  decides from its float64 h, so the two may differ where h lies within
-  rounding distance of a decision boundary.  The test therefore checks
-  validity: a block's scale may differ only where its amax is within 1e-5 of
-  a power of two, and every code is the correct rounding of h at the scale
-  taken, within 1e-5 relative;
+  decides from its float64 h, so the two may differ where h lies within the
+  fp32 accumulation bound of a decision boundary (a near-tie of a small
+  element in a block of larger ones is the usual case).  The test therefore
+  checks validity against that bound (mx_h_bound: D * 2^-24 * sum |x w| for
+  gate and up, carried through SwiGLU).  A block's scale may differ only
+  where its amax lies within the bound of a power of two, and every code
+  must be the nearest E4M3 value, at the scale taken, of a value within the
+  bound of the oracle's h;
 - the block end to end (route -> quantize -> FC1 -> FC2 -> combine) is within
   2e-2 |ref| + 2e-2 rms(ref) of the oracle's MX forward.
 Sizes span several 128-row tiles per group, ragged k-blocks (contraction
@@ -108,11 +111,42 @@ def test_permute_quantize_exact(case):
     assert_exact("xq scales", sc, ref["xsc"][:used])
 
 
-def _check_mx_codes(name, q, sc, h, offs):
+def mx_h_bound(xq, xsc, wq, wsc, offs):
+    """Bound on |h_kernel - h_oracle| per element: the kernel sums the exact
+    products of FC1 in fp32, so its gate and up sums g, u each lie within
+    D * 2^-24 * sum_d |x_d w_d| of the exact ones (the worst-case bound of a
+    length-D fp32 sum); that moves h = silu(g) u by at most
+    |silu'(g) u| dg + |silu(g)| du, plus the fp32 rounding of SwiGLU's own
+    operations (4 * 2^-24 |h|)."""
+    offs = np.asarray(offs, np.int64)
+    E, N, D = wq.shape
+    F = N // 2
+    x = oracle.mx_dequantize(xq, xsc)
+    w = oracle.mx_dequantize(wq.reshape(E * N, D), wsc.reshape(E * N, D // 32)).reshape(E, N, D)
+    R = int(offs[-1])
+    a = np.zeros((R, N))
+    s = np.zeros((R, N))
+    for e in range(E):   # one matmul per group
+        r0, r1 = int(offs[e]), int(offs[e + 1])
+        if r1 > r0:
+            a[r0:r1] = x[r0:r1] @ w[e].T
+            s[r0:r1] = np.abs(x[r0:r1]) @ np.abs(w[e]).T
+    g, u = a[:, :F], a[:, F:]
+    gamma = D * 2.0 ** -24
+    sig = 1.0 / (1.0 + np.exp(-g))
+    dsilu = sig * (1.0 + g * (1.0 - sig))
+    h = g * sig * u
+    return np.abs(dsilu * u) * gamma * s[:, :F] + np.abs(g * sig) * gamma * s[:, F:] + \
+        4 * 2.0 ** -24 * np.abs(h)
+
+
+def _check_mx_codes(name, q, sc, h, offs, hb):
     """The codes of h written by the kernel are a valid quantization of h
-    (see the module docstring)."""
+    (see the module docstring): each is the nearest E4M3 value, at the
+    block's scale, of some value within hb (mx_h_bound) of the oracle's h."""
     used = int(offs[-1])
     q, sc, h = q[:used], sc[:used].astype(np.int64), h[:used].astype(np.float64)
+    hb = hb[:used]
     R, F = h.shape
     blocks = h.reshape(R, F // 32, 32)
     amax = np.abs(blocks).max(axis=2)
@@ -120,21 +154,30 @@ def _check_mx_codes(name, q, sc, h, offs):
     s_ref = np.where(amax == 0, -127, np.maximum(ex - 1 - 8, -127))
     s = sc - 127
     diff = s != s_ref
-    near_pow2 = np.abs(np.log2(np.where(amax > 0, amax, 1.0)) -
-                       np.round(np.log2(np.where(amax > 0, amax, 1.0)))) < 1e-5
+    # the block's amax may sit on either side of a power of two within hb
+    p2 = np.exp2(np.round(np.log2(np.where(amax > 0, amax, 1.0))))
+    near_pow2 = np.abs(amax - p2) <= hb.reshape(R, F // 32, 32).max(axis=2) + 1e-7 * amax
     assert not (diff & ~near_pow2).any(), \
         f"{name}: {int((diff & ~near_pow2).sum())} block scales are not floor(log2 amax) - 8"
     scale = np.exp2(np.repeat(s, 32, axis=1).astype(np.float64))
     v = np.abs(h) / scale
     deq = oracle.mx_dequantize(q, sc.astype(np.uint8))
-    sat = v > 448 * (1 + 1e-5)
+    slack = hb / scale  # the bound in units of the scaled value
+    sat = v - slack > 448
     assert np.all(deq[sat] == np.sign(h[sat]) * 448 * scale[sat]), f"{name}: saturation"
     e = np.floor(np.log2(np.maximum(v, 2.0 ** -6)))
     half_step = 0.5 * np.exp2(e - 3) * scale
     err = np.abs(deq - h)
-    ok = sat | (err <= half_step * (1 + 1e-6) + 1e-5 * np.abs(h))
-    assert ok.all(), (f"{name}: {int((~ok).sum())} codes are not the nearest E4M3 value; "
-                      f"worst excess {np.max(err - half_step):.3g}")
+    near_sat = (v + slack > 448) & ~sat   # within the bound of the saturation edge
+    ok = sat | (err <= half_step * (1 + 1e-6) + hb) | (near_sat & (np.abs(deq) == 448 * scale))
+    if not ok.all():
+        r, c = np.argwhere(~ok)[0]
+        b = c // 32
+        raise AssertionError(
+            f"{name}: {int((~ok).sum())} codes are not the nearest E4M3 value; first at row {r} "
+            f"col {c}: h {h[r, c]!r} deq {deq[r, c]!r} code {int(q[r, c]):#04x} scale 2^{int(s[r, b])} "
+            f"(oracle 2^{int(s_ref[r, b])}, block amax {amax[r, b]!r}) v {v[r, c]!r}; block h "
+            f"{h[r, 32 * b:32 * b + 32].tolist()} codes {q[r, 32 * b:32 * b + 32].tolist()}")
     same = np.mean(q == oracle.mx_quantize(h.astype(np.float32))[0])
     assert same > 0.999, f"{name}: only {same:.4f} of the codes match the oracle's"
 
@@ -161,7 +204,8 @@ def test_fc1_swiglu(case):
     _close("h", to_host(h)[:used], want, 8e-3, 1e-3)
     q = to_host(hq).reshape(R, F)
     sc = L.unpack_act_scales(to_host(hsc), offs, F)
-    _check_mx_codes("hq", q, sc, ref["h"], offs)
+    hb = mx_h_bound(ref["xq"], ref["xsc"], ref["wq"], ref["wsc"], offs)
+    _check_mx_codes("hq", q, sc, ref["h"], offs, hb)
 
 
 def test_fc2(case):
