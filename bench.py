@@ -640,6 +640,8 @@ def run_ours(args, dist, rank, world):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(wl, fwd_only, budget_s=20.0)
+        if mx is not None:
+            mx["cpu_baseline"] = mx_cpu_baseline(wl, budget_s=10.0)
 
     line = {
         "metric": METRIC_FWD if fwd_only else METRIC,
@@ -761,6 +763,46 @@ def cpu_baseline(wl, fwd_only, budget_s=20.0, T_sample=None):
             "kind": "oracle",
             "sample": f"{T_sample} of {wl.T} tokens of {wl.name} (same D,E,K,F), "
                       f"{'fwd' if fwd_only else 'fwd+bwd'}, one pass, {dt:.1f} s"}
+
+
+def _oracle_mx_step(wl_s, inp, wq):
+    """The oracle's MX forward of one step, the weights already quantized
+    (as the GPU leg runs it): route, histogram, permute + quantize, FC1 +
+    SwiGLU, quantize h, FC2, combine."""
+    import oracle
+    if wl_s.score_mode == oracle.GIVEN:
+        ids, w = inp["ids"], inp["w"]
+    else:
+        ids, w = oracle.route(inp["logits"], inp["bias"], wl_s.score_mode, wl_s.T, wl_s.E, wl_s.K)
+    _, off, pos, _, _ = oracle.histogram(ids, wl_s.E)
+    xq, xsc = oracle.mx_quantize(oracle.bf16_to_f32(oracle.permute(inp["x"], pos)))
+    h = oracle.mx_fc1_swiglu(xq, xsc, wq[0], wq[1], off)
+    hq, hsc = oracle.mx_quantize(h)
+    ys = oracle.mx_fc2(hq, hsc, wq[2], wq[3], off)
+    oracle.combine(ys, w, pos, wl_s.T, wl_s.D)
+
+
+def mx_cpu_baseline(wl, budget_s=10.0):
+    """The oracle's MX forward on the host cores, on a bounded token sample of
+    the workload; the weights are quantized once, outside the timing."""
+    import oracle
+    oracle.build()
+    wl8 = _sample_workload(wl, 8)
+    inp = _oracle_inputs(wl8, True)
+    wq = oracle.mx_weights(inp["wi"], inp["wo"])
+    t0 = time.perf_counter()
+    _oracle_mx_step(wl8, inp, wq)
+    dt = time.perf_counter() - t0
+    T_sample = int(max(8, min(wl.T, 8 * budget_s / max(dt, 1e-3))))
+    wl_s = _sample_workload(wl, T_sample)
+    inp = _oracle_inputs(wl_s, True)
+    t0 = time.perf_counter()
+    _oracle_mx_step(wl_s, inp, wq)
+    dt = time.perf_counter() - t0
+    return {"value": T_sample / dt, "unit": "tokens/s", "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": f"{T_sample} of {wl.T} tokens of {wl.name} (same D,E,K,F), MXFP8 fwd, "
+                      f"weights quantized beforehand, one pass, {dt:.1f} s"}
 
 
 def run_reference(args, dist, rank, world):
