@@ -267,6 +267,30 @@ def test_forward_end_to_end(case):
     _close("out", out, ref["out"], 2e-2, 2e-2)
 
 
+def _edge(kind):
+    """Small MX edge cases: one token with one slot; a single expert; every
+    token routed to one expert of four (given routing)."""
+    if kind == "one_row":
+        wl = custom("mx_one_row", T=1, D=128, E=4, K=1, F=64)
+        return wl, oracle.to_numpy(make_inputs(wl, "cpu"))
+    if kind == "e1":
+        wl = custom("mx_e1", T=200, D=192, E=1, K=1, F=128)
+        return wl, oracle.to_numpy(make_inputs(wl, "cpu"))
+    wl = custom("mx_all_to_one", T=300, D=128, E=4, K=1, F=64, score_mode=2)
+    inp = oracle.to_numpy(make_inputs(wl, "cpu"))
+    inp["ids"] = np.full((300, 1), 2, np.int32)
+    inp["w"] = np.ones((300, 1), np.float32)
+    return wl, inp
+
+
+@pytest.mark.parametrize("kind", ["one_row", "e1", "all_to_one"])
+def test_edge_cases(kind):
+    wl, inp = _edge(kind)
+    ref = oracle.mx_block_forward(inp)
+    out = mx_forward_gpu(wl, inp)
+    _close("out", out, ref["out"], 2e-2, 2e-2)
+
+
 def test_t0_and_argument_errors():
     d0 = B.dims(0, 128, 4, 2, 64)
     z = _u8(16)
