@@ -58,24 +58,20 @@ namespace {
 
 constexpr int kMaxE = 1024;
 constexpr int kThreads = 192;
+constexpr int kStages = 4;
 constexpr int kAStage = 128 * 128;               // 16 KB
-// One CTA holds all 256 B rows of a tile; a CTA pair (CG = 2) holds 128 each.
-template <int CG> constexpr int kBStage = 256 * 128 / CG;
-template <int CG> constexpr int kSfaOff = kAStage + kBStage<CG>;
-template <int CG> constexpr int kSfbOff = kSfaOff<CG> + 1024;
-// 50 KB (CG = 1) or 34 KB (CG = 2) per stage, every operand 1024-aligned
-template <int CG> constexpr int kStageBytes = kSfbOff<CG> + 1024;
-template <int CG> constexpr int kStages = CG == 1 ? 4 : 5;
-// bytes landing in one CTA per stage (a pair's even CTA expects twice this)
-template <int CG> constexpr uint32_t kTxBytes = kAStage + kBStage<CG> + 512 + 1024;
+constexpr int kBStage = 256 * 128;               // 32 KB
+constexpr int kSfaOff = kAStage + kBStage;       // 48 KB
+constexpr int kSfbOff = kSfaOff + 1024;
+constexpr int kStageBytes = kSfbOff + 1024;      // 50 KB (keeps every operand 1024-aligned)
+constexpr uint32_t kTxBytes = kAStage + kBStage + 512 + 1024;
 constexpr int kEpiBytes = 4096;                  // staging per epilogue warp
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSfStride = 16;               // scale slot per stage: A 4 + B 8 columns (16-aligned)
 
-template <int CG>
 struct MxCtl {
-  uint64_t full[kStages<CG>];
-  uint64_t empty[kStages<CG>];
+  uint64_t full[kStages];
+  uint64_t empty[kStages];
   uint64_t tfull[2];   // accumulator buffer b holds a finished tile
   uint64_t tempty[2];  // the epilogue has read all of buffer b
   uint64_t sffree[2];  // the epilogue has read half 0 of buffer b (the scale slots)
@@ -83,12 +79,10 @@ struct MxCtl {
   int abort_flag;
   int off[kMaxE + 1];  // group offsets
   int tb[kMaxE + 1];   // first 128-row tile of each group (exclusive prefix)
-  int tbp[CG == 2 ? kMaxE + 1 : 1];  // pairs: first tile pair of each group
 };
-template <int CG>
-constexpr size_t kSmemBytes = 1024 + static_cast<size_t>(kStages<CG>) * kStageBytes<CG> +
-                              4 * kEpiBytes + sizeof(MxCtl<CG>);
-static_assert(kSmemBytes<1> <= 227 * 1024 && kSmemBytes<2> <= 227 * 1024, "shared memory");
+constexpr size_t kSmemBytes =
+    1024 + static_cast<size_t>(kStages) * kStageBytes + 4 * kEpiBytes + sizeof(MxCtl);
+static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 
 // ------------------------------------------------------------ MX helpers
 // Shared exponent of a block from its largest magnitude: floor(log2 amax) - 8
@@ -127,49 +121,30 @@ __device__ __forceinline__ uint32_t mx_quant32(const float (&v)[32], uint32_t (&
 // scale block.
 __device__ __forceinline__ int sf_byte(int m, int j) { return (m & 31) * 16 + (m >> 5) * 4 + j; }
 
-// Warp-wide exclusive prefix of `local` (lane order); the total in `total`.
-__device__ __forceinline__ int warp_excl_scan(int local, int lane, int& total) {
-  int incl = local;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int v = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += v;
-  }
-  total = __shfl_sync(0xffffffffu, incl, 31);
-  return incl - local;
-}
-
-// Group offsets into shared memory (all threads), then (one warp) the
-// exclusive prefixes over the groups of ceil(rows/128) tiles and, when s_tbp
-// is given, of ceil(tiles/2) tile pairs.  Ends with __syncthreads().
+// Group offsets into shared memory (all threads), then the exclusive prefix
+// of ceil(rows/128) over the groups (one warp).  Ends with __syncthreads().
 __device__ __forceinline__ void load_tile_bases(const int32_t* offs, int E, int* s_off, int* s_tb,
-                                                int* s_tbp, int scan_warp) {
+                                                int scan_warp) {
   for (int i = threadIdx.x; i <= E; i += blockDim.x) s_off[i] = __ldg(offs + i);
   __syncthreads();
   if (static_cast<int>(threadIdx.x >> 5) == scan_warp) {
     const int lane = threadIdx.x & 31;
     const int per = (E + 31) / 32;
     const int e0 = min(E, lane * per), e1 = min(E, e0 + per);
-    int l1 = 0, l2 = 0;
+    int local = 0;
+    for (int e = e0; e < e1; ++e) local += (s_off[e + 1] - s_off[e] + 127) >> 7;
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    int run = incl - local;
     for (int e = e0; e < e1; ++e) {
-      const int mt = (s_off[e + 1] - s_off[e] + 127) >> 7;
-      l1 += mt;
-      l2 += (mt + 1) >> 1;
+      s_tb[e] = run;
+      run += (s_off[e + 1] - s_off[e] + 127) >> 7;
     }
-    int t1, t2;
-    int r1 = warp_excl_scan(l1, lane, t1);
-    int r2 = warp_excl_scan(l2, lane, t2);
-    for (int e = e0; e < e1; ++e) {
-      const int mt = (s_off[e + 1] - s_off[e] + 127) >> 7;
-      s_tb[e] = r1;
-      r1 += mt;
-      if (s_tbp != nullptr) s_tbp[e] = r2;
-      r2 += (mt + 1) >> 1;
-    }
-    if (lane == 0) {
-      s_tb[E] = t1;
-      if (s_tbp != nullptr) s_tbp[E] = t2;
-    }
+    if (lane == 31) s_tb[E] = incl;
   }
   __syncthreads();
 }
@@ -260,7 +235,7 @@ __global__ void __launch_bounds__(256) mx_permute_quantize_kernel(
   __shared__ int s_row[kPqWarps][32];
   __shared__ int s_blk[kPqWarps][32];  // scale block base (bytes) of the slot's row
   __shared__ int s_m[kPqWarps][32];
-  load_tile_bases(offs, E, s_off, s_tb, nullptr, 0);
+  load_tile_bases(offs, E, s_off, s_tb, 0);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nb = D / 32;
   const int R = s_off[E];
@@ -368,33 +343,23 @@ struct MxParams {
   int KBF;      // FC1: k-blocks of F (h scale blocks per tile row)
 };
 
-// A unit of the schedule is one 128-row tile and a 256-wide B tile (CG = 1)
-// or, for a CTA pair (CG = 2), two consecutive 128-row tiles of one group
-// (the pair's 256-row MMA): CTA rank r takes tile 2*pair + r.  A CTA whose
-// tile lies past its group's last (odd tile count) has no rows; it still
-// loads its half of the operands, which the pair's MMA reads.
 struct MxTile {
   int e, g, nt, row0, rows;
 };
 
-template <int CG>
-__device__ __forceinline__ MxTile mx_decode(int u, int rank, const MxParams& p, const MxCtl<CG>& s) {
+__device__ __forceinline__ MxTile mx_decode(int t, const MxParams& p, const MxCtl& s) {
   MxTile T;
-  const int gu = u / p.n_tiles;
-  T.nt = u - gu * p.n_tiles;
-  const int* base = (CG == 1) ? s.tb : s.tbp;
+  T.g = t / p.n_tiles;
+  T.nt = t - T.g * p.n_tiles;
   int lo = 0, hi = p.E - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (base[mid] <= gu) lo = mid;
+    if (s.tb[mid] <= T.g) lo = mid;
     else hi = mid - 1;
   }
   T.e = lo;
-  const int mt = (CG == 1) ? gu - s.tb[lo] : 2 * (gu - base[lo]) + rank;
-  const int tiles = s.tb[lo + 1] - s.tb[lo];
-  T.g = s.tb[lo] + min(mt, tiles - 1);
-  T.row0 = s.off[lo] + 128 * mt;
-  T.rows = mt < tiles ? min(128, s.off[lo + 1] - T.row0) : 0;
+  T.row0 = s.off[lo] + (T.g - s.tb[lo]) * 128;
+  T.rows = min(128, s.off[lo + 1] - T.row0);
   return T;
 }
 
@@ -418,38 +383,21 @@ __device__ __forceinline__ uint64_t sf_desc(uint32_t saddr) {
   return static_cast<uint64_t>((saddr >> 4) & 0x3FFFu) | (static_cast<uint64_t>(128 >> 4) << 16) |
          (static_cast<uint64_t>(128 >> 4) << 32) | (1ull << 46);
 }
-// CG = 2: issued by the pair's even CTA, each CTA's block goes to its own TMEM.
-template <int CG>
 __device__ __forceinline__ void tmem_cp_sf(uint32_t taddr, uint64_t sdesc) {
-  if constexpr (CG == 1)
-    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
-                 : "memory");
-  else
-    asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
-                 : "memory");
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
+               : "memory");
 }
-// Block-scaled MMA: e4m3 A and B, both K-major, K = 32, E8M0 scales at
-// sfa/sfb in TMEM.  CG = 2: the pair's 256-row MMA, issued by the even CTA;
-// each CTA holds its 128 A rows, half of the B rows and its own scales.
-template <int CG>
+// Block-scaled MMA: e4m3 A (M = 128) and B (N = 128), both K-major, K = 32,
+// E8M0 scales at sfa/sfb in TMEM.
 __device__ __forceinline__ void umma_mxf8(uint32_t d, uint64_t ad, uint64_t bd, uint32_t idesc,
                                           uint32_t sfa, uint32_t sfb, uint32_t accumulate) {
-  if constexpr (CG == 1)
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %6, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], "
-        "[%5], p;\n\t}" ::"r"(d),
-        "l"(ad), "l"(bd), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
-        : "memory");
-  else
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %6, 0;\n\t"
-        "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], "
-        "[%5], p;\n\t}" ::"r"(d),
-        "l"(ad), "l"(bd), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
-        : "memory");
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], "
+      "[%5], p;\n\t}" ::"r"(d),
+      "l"(ad), "l"(bd), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+      : "memory");
 }
 // Instruction descriptor, kind::mxf8f6f4 with block scaling: B scale id in
 // bits 4-5, A and B formats e4m3 (0) in bits 7-9 and 10-12, K-major A and
@@ -475,127 +423,94 @@ __device__ __forceinline__ void put_half_sw(uint8_t* buf, int lane, int hh, cons
   }
 }
 
-template <bool FC1, int CG>
+template <bool FC1>
 __global__ void __launch_bounds__(kThreads, 1)
     mx_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                    const __grid_constant__ CUtensorMap map_b,
-                   const __grid_constant__ CUtensorMap map_o,
-                   const __grid_constant__ CUtensorMap map_sfa,
-                   const __grid_constant__ CUtensorMap map_sfb, const MxParams p) {
-  constexpr int kSt = kStages<CG>;
-  constexpr int kStB = kStageBytes<CG>;
+                   const __grid_constant__ CUtensorMap map_o, const MxParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* ring = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
-  uint8_t* epi = ring + kSt * kStB;
-  MxCtl<CG>& s = *reinterpret_cast<MxCtl<CG>*>(epi + 4 * kEpiBytes);
+  uint8_t* epi = ring + kStages * kStageBytes;
+  MxCtl& s = *reinterpret_cast<MxCtl*>(epi + 4 * kEpiBytes);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int rank = (CG == 2) ? static_cast<int>(cluster_ctarank()) : 0;
-  const bool leader = (rank == 0);
-  const int unit0 = blockIdx.x / CG, units_step = gridDim.x / CG;
 
   if (warp == 0 && lane == 0) {
     tma_prefetch_map(&map_a);
     tma_prefetch_map(&map_b);
     tma_prefetch_map(&map_o);
-    if constexpr (CG == 2) {
-      tma_prefetch_map(&map_sfa);
-      tma_prefetch_map(&map_sfb);
-    }
-    for (int i = 0; i < kSt; ++i) {
+    for (int i = 0; i < kStages; ++i) {
       mbar_init(&s.full[i], 1);
       mbar_init(&s.empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s.tfull[i], 1);
-      mbar_init(&s.tempty[i], 4 * CG);   // every epilogue warp of the pair (even CTA's copy)
-      mbar_init(&s.sffree[i], 4 * CG);
+      mbar_init(&s.tempty[i], 4);
+      mbar_init(&s.sffree[i], 4);
     }
     s.abort_flag = 0;
     mbar_fence_init();
   }
   if (warp == 1) {
-    tmem_alloc<CG>(&s.tmem_base, kTmemCols);
-    tmem_relinquish<CG>();
+    tmem_alloc<1>(&s.tmem_base, kTmemCols);
+    tmem_relinquish<1>();
   }
-  load_tile_bases(p.offs, p.E, s.off, s.tb, CG == 2 ? s.tbp : nullptr, 2);  // ends with __syncthreads
+  load_tile_bases(p.offs, p.E, s.off, s.tb, 2);  // ends with __syncthreads
   tc_fence_before();
   __syncthreads();
-  if constexpr (CG == 2) cluster_sync();  // the peer's barriers exist before any remote arrive
   tc_fence_after();
   const uint32_t tmem_base = s.tmem_base;
   const WaitCtl wc{&s.abort_flag, p.status, p.limit_ns};
-  const int nunits = ((CG == 1) ? s.tb[p.E] : s.tbp[p.E]) * p.n_tiles;
+  const int ntiles = s.tb[p.E] * p.n_tiles;
 
   if (warp == 0) {
     // -------------------------------------------------------- producer
     if (lane == 0) {
       uint32_t stage = 0, phase = 0;
-      uint32_t fills[kSt] = {};
+      uint32_t fills[kStages] = {0, 0, 0, 0};
       bool aborted = false;
-      // a pair's loads complete on the even CTA's full barrier, which the
-      // even CTA arms with both CTAs' bytes
-      const uint32_t full0 = (CG == 2) ? mapa_shared(smem_u32(&s.full[0]), 0) : smem_u32(&s.full[0]);
-      for (int u = unit0; u < nunits && !aborted; u += units_step) {
-        const MxTile T = mx_decode<CG>(u, rank, p, s);
+      for (int t = blockIdx.x; t < ntiles && !aborted; t += gridDim.x) {
+        const MxTile T = mx_decode(t, p, s);
         const uint8_t* sfa = p.sfa + static_cast<size_t>(T.g) * p.KB * 512;
         const uint8_t* sfb =
             p.sfb + (static_cast<size_t>(T.e) * p.KB * p.NBp + 2 * T.nt) * 512;
         for (int kb = 0; kb < p.KB; ++kb) {
           if (!mbar_wait(&s.empty[stage], phase ^ 1u, wc)) { aborted = true; break; }
-          uint8_t* st = ring + stage * kStB;
-          if constexpr (CG == 1) {
-            mbar_arrive_expect_tx(&s.full[stage], kTxBytes<1>);
-            tma_load_2d(st, &map_a, &s.full[stage], kb * 128, T.row0);
-            tma_load_3d(st + kAStage, &map_b, &s.full[stage], kb * 128, 256 * T.nt, T.e);
-            bulk_load(st + kSfaOff<1>, sfa + static_cast<size_t>(kb) * 512, 512, &s.full[stage]);
-            bulk_load(st + kSfbOff<1>, sfb + static_cast<size_t>(kb) * p.NBp * 512, 1024,
-                      &s.full[stage]);
-          } else {
-            const uint32_t bar = full0 + stage * static_cast<uint32_t>(sizeof(uint64_t));
-            if (leader) mbar_arrive_expect_tx(&s.full[stage], 2 * kTxBytes<2>);
-            tma_load_2d_pair(st, &map_a, bar, kb * 128, T.row0);
-            tma_load_3d_pair(st + kAStage, &map_b, bar, kb * 128, 256 * T.nt + 128 * rank, T.e);
-            // the scale blocks as rows of 256 bytes: this CTA's A block, the tile's two B blocks
-            tma_load_2d_pair(st + kSfaOff<2>, &map_sfa, bar, 0, 2 * (T.g * p.KB + kb));
-            tma_load_2d_pair(st + kSfbOff<2>, &map_sfb, bar, 0,
-                             2 * ((T.e * p.KB + kb) * p.NBp + 2 * T.nt));
-          }
+          uint8_t* st = ring + stage * kStageBytes;
+          mbar_arrive_expect_tx(&s.full[stage], kTxBytes);
+          tma_load_2d(st, &map_a, &s.full[stage], kb * 128, T.row0);
+          tma_load_3d(st + kAStage, &map_b, &s.full[stage], kb * 128, 256 * T.nt, T.e);
+          bulk_load(st + kSfaOff, sfa + static_cast<size_t>(kb) * 512, 512, &s.full[stage]);
+          bulk_load(st + kSfbOff, sfb + static_cast<size_t>(kb) * p.NBp * 512, 1024,
+                    &s.full[stage]);
           ++fills[stage];
-          if (++stage == kSt) { stage = 0; phase ^= 1u; }
+          if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
       }
-      for (int i = 0; i < kSt; ++i) {
-        if (fills[i] == 0) continue;
-        // copies in flight land before the CTA exits (abort)
-        if (aborted && (CG == 1 || leader))
-          (void)mbar_wait_drain(&s.full[i], (fills[i] - 1u) & 1u, 100000000ull);
-        // a pair's last stage releases (multicast by the even CTA) have arrived
-        if (CG == 2) (void)mbar_wait_drain(&s.empty[i], (fills[i] - 1u) & 1u, 100000000ull);
+      if (aborted) {  // copies in flight land before the CTA exits
+        for (int i = 0; i < kStages; ++i)
+          if (fills[i] > 0) (void)mbar_wait_drain(&s.full[i], (fills[i] - 1u) & 1u, 100000000ull);
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------- MMA
-    // one thread (of the even CTA for a pair): waits, scale copies, MMAs and
-    // commits; the odd CTA's MMA warp only takes part in TMEM allocation
-    if (lane == 0 && leader) {
+    // one thread: waits, scale copies, MMAs and commits
+    if (lane == 0) {
       uint32_t stage = 0, phase = 0, it = 0;
-      uint32_t commits[kSt] = {};
+      uint32_t commits[kStages] = {0, 0, 0, 0};
       int last_stage = -1;
       bool aborted = false;
-      // descriptors of stage 0's A and scale blocks; stage i adds i * kStB >> 4,
+      // descriptors of stage 0's A and scale blocks; stage i adds i * kStageBytes >> 4,
       // a k-step 2 (32 B >> 4)
       const uint64_t da0 = smem_desc_sw128(smem_u32(ring), 16, 1024);
-      const uint64_t ds0 = sf_desc(smem_u32(ring) + kSfaOff<CG>);
-      for (int u = unit0; u < nunits && !aborted; u += units_step, ++it) {
-        const MxTile T = mx_decode<CG>(u, rank, p, s);
-        // a pair always runs N = 256 (its B rows are split 128/128 between
-        // the CTAs); B rows past the columns are zero-filled and not stored
-        const bool h1 = CG == 2 || half_valid<FC1>(T.nt, 1, p);
+      const uint64_t ds0 = sf_desc(smem_u32(ring) + kSfaOff);
+      for (int t = blockIdx.x; t < ntiles && !aborted; t += gridDim.x, ++it) {
+        const MxTile T = mx_decode(t, p, s);
+        const bool h1 = half_valid<FC1>(T.nt, 1, p);
         // tile it accumulates in buffer it % 2 (256 columns) while its scale
-        // slots sit in the first kSt * kSfStride columns of the other buffer,
-        // which the epilogue empties first
+        // slots sit in the first kStages * kSfStride columns of the other buffer, which
+        // the epilogue empties first
         const uint32_t buf = it & 1u, use = it >> 1;
         if (!mbar_wait(&s.tempty[buf], (use & 1u) ^ 1u, wc) ||
             (it > 0 && !mbar_wait(&s.sffree[buf ^ 1u], ((it - 1) >> 1) & 1u, wc))) {
@@ -610,34 +525,32 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!mbar_wait(&s.full[stage], phase, wc)) { aborted = true; break; }
           tc_fence_after();
           const uint32_t sf = sf_base + kSfStride * stage;
-          const uint64_t a0 = da0 + stage * (kStB >> 4);
+          const uint64_t a0 = da0 + stage * (kStageBytes >> 4);
           const uint64_t b0 = a0 + (kAStage >> 4);
-          const uint64_t s0 = ds0 + stage * (kStB >> 4);
-          tmem_cp_sf<CG>(sf, s0);
-          tmem_cp_sf<CG>(sf + 4, s0 + (1024 >> 4));
-          if (h1) tmem_cp_sf<CG>(sf + 8, s0 + (1536 >> 4));
+          const uint64_t s0 = ds0 + stage * (kStageBytes >> 4);
+          tmem_cp_sf(sf, s0);
+          tmem_cp_sf(sf + 4, s0 + (1024 >> 4));
+          if (h1) tmem_cp_sf(sf + 8, s0 + (1536 >> 4));
           if (kb * 128 + 128 <= p.Kd) {
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
               const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
-              umma_mxf8<CG>(d0, a0 + 2 * kk, b0 + 2 * kk, mx_idesc(128 * CG, idn, kk), sf, sf + 4,
-                            acc);
+              umma_mxf8(d0, a0 + 2 * kk, b0 + 2 * kk, mx_idesc(128, idn, kk), sf, sf + 4, acc);
             }
           } else {
             const int nk = (p.Kd - kb * 128) / 32;
             for (int kk = 0; kk < nk; ++kk) {
               const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
-              umma_mxf8<CG>(d0, a0 + 2 * kk, b0 + 2 * kk, mx_idesc(128 * CG, idn, kk), sf, sf + 4,
-                            acc);
+              umma_mxf8(d0, a0 + 2 * kk, b0 + 2 * kk, mx_idesc(128, idn, kk), sf, sf + 4, acc);
             }
           }
-          umma_commit<CG>(&s.empty[stage]);
+          umma_commit<1>(&s.empty[stage]);
           ++commits[stage];
           last_stage = static_cast<int>(stage);
-          if (++stage == kSt) { stage = 0; phase ^= 1u; }
+          if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
         if (aborted) break;
-        umma_commit<CG>(&s.tfull[buf]);
+        umma_commit<1>(&s.tfull[buf]);
       }
       if (aborted && last_stage >= 0)  // issued MMAs finish before TMEM is freed
         (void)mbar_wait_drain(&s.empty[last_stage], (commits[last_stage] - 1u) & 1u, 100000000ull);
@@ -648,14 +561,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* buf = epi + (warp - 2) * kEpiBytes;
     uint32_t it = 0;
     bool aborted = false;
-    // a pair's releases go to the even CTA, whose MMA thread waits on them
-    uint32_t sffree_at = smem_u32(&s.sffree[0]), tempty_at = smem_u32(&s.tempty[0]);
-    if constexpr (CG == 2) {
-      sffree_at = mapa_shared(sffree_at, 0);
-      tempty_at = mapa_shared(tempty_at, 0);
-    }
-    for (int u = unit0; u < nunits && !aborted; u += units_step, ++it) {
-      const MxTile T = mx_decode<CG>(u, rank, p, s);
+    for (int t = blockIdx.x; t < ntiles && !aborted; t += gridDim.x, ++it) {
+      const MxTile T = mx_decode(t, p, s);
       const int vw = min(32, max(0, T.rows - 32 * q));  // valid rows of this warp
       const int y = T.row0 + 32 * q;
       const bool row_ok = lane < vw;
@@ -681,12 +588,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // columns); half 1 ends this warp's reads of the buffer
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) {
-          const uint32_t at = (hh == 0 ? sffree_at : tempty_at) +
-                              bsel * static_cast<uint32_t>(sizeof(uint64_t));
-          if (CG == 2 && !leader) mbar_arrive_remote(at);
-          else mbar_arrive(hh == 0 ? &s.sffree[bsel] : &s.tempty[bsel]);
-        }
+        if (lane == 0) mbar_arrive(hh == 0 ? &s.sffree[bsel] : &s.tempty[bsel]);
         if (!live) continue;
         if constexpr (FC1) {
           // gate = columns 0..63, up = 64..127 of the region: h for f0..f0+63
@@ -786,10 +688,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if constexpr (CG == 2) cluster_sync();  // both CTAs are done with each other's memory
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc<CG>(tmem_base, kTmemCols);
+    tmem_dealloc<1>(tmem_base, kTmemCols);
   }
 }
 
@@ -831,12 +732,10 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType type, const void* base, int ra
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <bool FC1, int CG>
+template <bool FC1>
 cudaError_t launch_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mo,
-                        const CUtensorMap& msa, const CUtensorMap& msb, const MxParams& p,
-                        long max_units, cudaStream_t s) {
-  auto kern = mx_gemm_kernel<FC1, CG>;
-  constexpr size_t kSmem = kSmemBytes<CG>;
+                        const MxParams& p, long max_tiles, cudaStream_t s) {
+  auto kern = mx_gemm_kernel<FC1>;
   static std::atomic<bool> attr_set[64];
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
@@ -844,51 +743,15 @@ cudaError_t launch_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const CUte
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!attr_set[dev].load(std::memory_order_acquire)) {
     err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(kSmem));
+                               static_cast<int>(kSmemBytes));
     if (err != cudaSuccess) return err;
     attr_set[dev].store(true, std::memory_order_release);
   }
-  long units = sm_count() / CG;
-  if (max_units < units) units = max_units;
-  if (units <= 0) return cudaSuccess;
-  if constexpr (CG == 1) {
-    kern<<<static_cast<int>(units), kThreads, kSmem, s>>>(ma, mb, mo, msa, msb, p);
-    return cudaGetLastError();
-  } else {
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = kSmem;
-    cfg.stream = s;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    // clusters resident at once (one CTA per SM), cached per kernel
-    static int max_clusters = 0;
-    static std::once_flag once;
-    std::call_once(once, [&] {
-      cfg.gridDim = dim3(static_cast<unsigned>(2 * (sm_count() / 2)), 1, 1);
-      int n = 0;
-      if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) == cudaSuccess && n > 0) max_clusters = n;
-      else max_clusters = sm_count() / 2;
-    });
-    if (units > max_clusters) units = max_clusters;
-    cfg.gridDim = dim3(static_cast<unsigned>(2 * units), 1, 1);
-    return cudaLaunchKernelEx(&cfg, kern, ma, mb, mo, msa, msb, p);
-  }
-}
-
-// Whether a grouped MX GEMM runs on CTA pairs (256-row MMAs): from ~256 rows
-// per group, where few pairs idle on a group's odd last tile.
-// MOE_MX_PAIR=0/1 forces the choice.
-bool mx_pairs(const moe_dims& d) {
-  const char* env = std::getenv("MOE_MX_PAIR");
-  if (env != nullptr && env[0] == '0') return false;
-  if (env != nullptr && env[0] == '1') return true;
-  return static_cast<long>(d.T) * d.K / d.E >= 256;
+  long grid = sm_count();
+  if (max_tiles < grid) grid = max_tiles;
+  if (grid <= 0) return cudaSuccess;
+  kern<<<static_cast<int>(grid), kThreads, kSmemBytes, s>>>(ma, mb, mo, p);
+  return cudaGetLastError();
 }
 
 }  // namespace
@@ -918,8 +781,6 @@ cudaError_t launch_mx_grouped_gemm(const MxGemmCall& c, cudaStream_t s) {
   const moe_dims& d = c.d;
   const long R = static_cast<long>(d.T) * d.K;
   if (R == 0) return cudaSuccess;
-  const bool pairs = mx_pairs(d);
-  const int CG = pairs ? 2 : 1;
   MxParams p{};
   p.sfa = c.a_sc;
   p.sfb = c.b_sc;
@@ -937,47 +798,36 @@ cudaError_t launch_mx_grouped_gemm(const MxGemmCall& c, cudaStream_t s) {
   p.NBp = static_cast<int>(mx_weight_row_blocks(Nb));
   p.n_tiles = static_cast<int>(mx_cdiv(Nb, 256));
   p.KBF = static_cast<int>(mx_kblocks(d.F));
-  CUtensorMap ma, mb, mo, msa, msb;
+  CUtensorMap ma, mb, mo;
   const uint64_t adims[2] = {static_cast<uint64_t>(p.Kd), static_cast<uint64_t>(R)};
   const uint64_t astr[1] = {static_cast<uint64_t>(p.Kd)};
   const uint32_t abox[2] = {128, 128};
   const uint64_t bdims[3] = {static_cast<uint64_t>(p.Kd), static_cast<uint64_t>(Nb),
                              static_cast<uint64_t>(d.E)};
   const uint64_t bstr[2] = {static_cast<uint64_t>(p.Kd), static_cast<uint64_t>(p.Kd) * Nb};
-  const uint32_t bbox[3] = {128, static_cast<uint32_t>(256 / CG), 1};
+  const uint32_t bbox[3] = {128, 256, 1};
   bool ok = make_map(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT8, c.a, 2, adims, astr, abox,
                      CU_TENSOR_MAP_SWIZZLE_128B) &&
             make_map(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, c.b, 3, bdims, bstr, bbox,
                      CU_TENSOR_MAP_SWIZZLE_128B);
   if (!ok) return cudaErrorInvalidValue;
-  // pairs load the 512-byte scale blocks by TMA as rows of 256 bytes (so
-  // that both CTAs' bytes complete on the even CTA's barrier)
-  msa = ma;
-  msb = ma;
-  if (pairs) {
-    const uint64_t sadims[2] = {256, static_cast<uint64_t>(mx_tile_bound(d) * p.KB * 2)};
-    const uint64_t sbdims[2] = {256, static_cast<uint64_t>(d.E) * p.KB * p.NBp * 2};
-    const uint64_t sstr[1] = {256};
-    const uint32_t sabox[2] = {256, 2}, sbbox[2] = {256, 4};
-    ok = make_map(&msa, CU_TENSOR_MAP_DATA_TYPE_UINT8, c.a_sc, 2, sadims, sstr, sabox,
-                  CU_TENSOR_MAP_SWIZZLE_NONE) &&
-         make_map(&msb, CU_TENSOR_MAP_DATA_TYPE_UINT8, c.b_sc, 2, sbdims, sstr, sbbox,
-                  CU_TENSOR_MAP_SWIZZLE_NONE);
-    if (!ok) return cudaErrorInvalidValue;
-  }
-  const long max_units = (mx_tile_bound(d) / CG + d.E) * p.n_tiles;
+  const long max_tiles = mx_tile_bound(d) * p.n_tiles;
   if (c.fc1) {
-    // h codes: 32 rows x 64 bytes per store, unswizzled staging (a map over
-    // the bf16 h when only that is written; it is then never used)
+    // h codes: 32 rows x 64 bytes per store, unswizzled staging (or a dummy
+    // map over the bf16 h when only that is written)
     const uint64_t odims[2] = {static_cast<uint64_t>(d.F), static_cast<uint64_t>(R)};
-    const uint64_t ostr[1] = {static_cast<uint64_t>(d.F)};
     const uint32_t obox[2] = {64, 32};
-    ok = make_map(&mo, CU_TENSOR_MAP_DATA_TYPE_UINT8,
-                  c.hq != nullptr ? static_cast<const void*>(c.hq) : static_cast<const void*>(c.out),
-                  2, odims, ostr, obox, CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (c.hq != nullptr) {
+      const uint64_t ostr[1] = {static_cast<uint64_t>(d.F)};
+      ok = make_map(&mo, CU_TENSOR_MAP_DATA_TYPE_UINT8, c.hq, 2, odims, ostr, obox,
+                    CU_TENSOR_MAP_SWIZZLE_NONE);
+    } else {
+      const uint64_t ostr[1] = {static_cast<uint64_t>(d.F) * 2};
+      ok = make_map(&mo, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, c.out, 2, odims, ostr, obox,
+                    CU_TENSOR_MAP_SWIZZLE_128B);
+    }
     if (!ok) return cudaErrorInvalidValue;
-    return pairs ? launch_gemm<true, 2>(ma, mb, mo, msa, msb, p, max_units, s)
-                 : launch_gemm<true, 1>(ma, mb, mo, msa, msb, p, max_units, s);
+    return launch_gemm<true>(ma, mb, mo, p, max_tiles, s);
   }
   const uint64_t odims[2] = {static_cast<uint64_t>(d.D), static_cast<uint64_t>(R)};
   const uint64_t ostr[1] = {static_cast<uint64_t>(d.D) * 2};
@@ -985,8 +835,7 @@ cudaError_t launch_mx_grouped_gemm(const MxGemmCall& c, cudaStream_t s) {
   ok = make_map(&mo, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, c.out, 2, odims, ostr, obox,
                 CU_TENSOR_MAP_SWIZZLE_128B);
   if (!ok) return cudaErrorInvalidValue;
-  return pairs ? launch_gemm<false, 2>(ma, mb, mo, msa, msb, p, max_units, s)
-               : launch_gemm<false, 1>(ma, mb, mo, msa, msb, p, max_units, s);
+  return launch_gemm<false>(ma, mb, mo, p, max_tiles, s);
 }
 
 }  // namespace moe

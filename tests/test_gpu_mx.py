@@ -19,7 +19,6 @@ Bars:
   bound of the oracle's h;
 - the block end to end (route -> quantize -> FC1 -> FC2 -> combine) is within
   2e-2 |ref| + 2e-2 rms(ref) of the oracle's MX forward.
-Both GEMM paths (one CTA per tile, CTA pairs) run every case.
 Sizes span several 128-row tiles per group, ragged k-blocks (contraction
 lengths that are odd multiples of 64), weight tiles whose second half lies
 past the output columns, empty groups and the largest E.
@@ -51,17 +50,6 @@ CASES = {
 @pytest.fixture(scope="module", autouse=True)
 def _gpu():
     need_gpu()
-
-
-# The MX GEMMs run one CTA per 128-row tile or CTA pairs (256-row MMAs);
-# MOE_MX_PAIR forces the path so that both are checked on every case.
-PAIR = pytest.mark.parametrize("pair", ["0", "1"], ids=["cta1", "cta2"])
-
-
-@pytest.fixture
-def pair_env(monkeypatch, pair):
-    monkeypatch.setenv("MOE_MX_PAIR", pair)
-    return pair
 
 
 @pytest.fixture(params=sorted(CASES), scope="module")
@@ -194,8 +182,7 @@ def _check_mx_codes(name, q, sc, h, offs, hb):
     assert same > 0.999, f"{name}: only {same:.4f} of the codes match the oracle's"
 
 
-@PAIR
-def test_fc1_swiglu(case, pair_env):
+def test_fc1_swiglu(case):
     wl, inp, ref = case
     d = _dims(wl)
     R, D, F, E = wl.T * wl.K, wl.D, wl.F, wl.E
@@ -221,8 +208,7 @@ def test_fc1_swiglu(case, pair_env):
     _check_mx_codes("hq", q, sc, ref["h"], offs, hb)
 
 
-@PAIR
-def test_fc2(case, pair_env):
+def test_fc2(case):
     wl, inp, ref = case
     d = _dims(wl)
     R, D, F = wl.T * wl.K, wl.D, wl.F
@@ -275,8 +261,7 @@ def mx_forward_gpu(wl, inp, stream=None):
     return to_host(out)
 
 
-@PAIR
-def test_forward_end_to_end(case, pair_env):
+def test_forward_end_to_end(case):
     wl, inp, ref = case
     out = mx_forward_gpu(wl, inp)
     _close("out", out, ref["out"], 2e-2, 2e-2)
@@ -298,9 +283,8 @@ def _edge(kind):
     return wl, inp
 
 
-@PAIR
 @pytest.mark.parametrize("kind", ["one_row", "e1", "all_to_one"])
-def test_edge_cases(kind, pair_env):
+def test_edge_cases(kind):
     wl, inp = _edge(kind)
     ref = oracle.mx_block_forward(inp)
     out = mx_forward_gpu(wl, inp)
