@@ -104,8 +104,9 @@ size_t moe_workspace_bytes(moe_dims d);
 /* A static English description of a status code. */
 const char* moe_status_string(moe_status s);
 
-/* Version of this ABI (1); lets a loader check the library it opened
- * without touching a GPU. */
+/* Version of this ABI; lets a loader check the library it opened without
+ * touching a GPU.  2: adds the MXFP8 entry points (moe_mx_*) and the FC1
+ * calls over expert ranges (moe_grouped_gemm_fc1_*_experts) to version 1's. */
 int moe_abi_version(void);
 
 /*

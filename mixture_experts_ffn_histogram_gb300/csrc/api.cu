@@ -86,7 +86,7 @@ const char* moe_status_string(moe_status s) {
   return "unknown status";
 }
 
-int moe_abi_version(void) { return 1; }
+int moe_abi_version(void) { return 2; }
 
 moe_status moe_route_histogram(const float* logits, const float* bias, moe_score_mode mode,
                                int32_t* ids, float* w, int32_t* group_sizes,
