@@ -34,3 +34,20 @@ def test_binding_resource_of_a_gemm(name, kernel, bound):
     t_bytes = bench.gemm_bytes(kernel, wl.R, wl.D, wl.E, wl.F, wl.train) / (pk["hbm"] * 1e9)
     t_flops = bench.gemm_flops(kernel, wl.R, wl.D, wl.F) / (pk["bf16_sustained"] * 1e12)
     assert ("hbm" if t_bytes > t_flops else "tensor") == bound
+
+
+def test_mx_algorithmic_bytes_match_the_buffers():
+    """The MX steps' algorithmic bytes are the sizes of what they must read
+    and write, as the library reports its MX buffers (codes plus one scale
+    byte per 32 elements; the tile-blocked scale buffers are upper bounds, so
+    their 1/32 counts are compared against the exact per-row figure)."""
+    wl = WORKLOADS["long_seq_train"]
+    T, D, E, K, F, R = wl.T, wl.D, wl.E, wl.K, wl.F, wl.R
+    assert bench.mx_bytes("permute_quantize", T, D, E, K, F) == \
+        2 * T * D + R * D + R * D // 32 + 4 * T * K
+    # FC1 reads xq + scales and wi codes + scales, writes hq + scales
+    assert bench.mx_bytes("fc1", T, D, E, K, F) == \
+        (R * D + R * D // 32) + (E * 2 * F * D + E * 2 * F * D // 32) + (R * F + R * F // 32)
+    # FC2 reads hq + scales and wo codes + scales, writes bf16 ys
+    assert bench.mx_bytes("fc2", T, D, E, K, F) == \
+        (R * F + R * F // 32) + (E * D * F + E * D * F // 32) + 2 * R * D
