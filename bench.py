@@ -53,6 +53,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-mx", action="store_true", help="skip the MXFP8 forward measurement")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the timed loop over every configuration")
     ap.add_argument("--tokens", type=int, default=None,
                     help="override T (small cases for profiling; not a bench line)")
     ap.add_argument("--experts", type=int, default=None,
@@ -104,14 +106,16 @@ def gemm_flops(kind, R, D, F):
 
 
 def hbm_bytes(kind, T, D, E, K, F):
-    """Algorithmic bytes of each HBM-bound step (what the method must move)."""
+    """Algorithmic bytes of each HBM-bound step (what the method must move):
+    route reads the logits and writes ids, weights and group sizes; the
+    permute/combine family moves each bf16 row once plus its index words."""
     R = T * K
     return {
-        "route": 4 * T * E + 4 * E + 8 * T * K + 8 * E + 12 * T * K,
-        "permute": 2 * T * D + 2 * R * D + 4 * T * K,
+        "route": 4 * T * E + 8 * T * K + 4 * E,
+        "permute": 2 * T * D + 2 * R * D + 8 * T * K,
         "combine": 2 * R * D + 2 * T * D + 8 * T * K,
-        "combine_bwd": 2 * T * D + 4 * R * D + 12 * T * K,
-        "permute_bwd": 2 * R * D + 2 * T * D + 4 * T * K,
+        "combine_bwd": 2 * T * D + 4 * R * D + 8 * T * K,
+        "permute_bwd": 2 * R * D + 2 * T * D,
     }[kind]
 
 
@@ -167,13 +171,32 @@ def recorded_traffic(step: str, workload: str):
 
 
 def peaks():
+    """Measured peaks of the GB300s: HBM copy GB/s, and cuBLAS bf16
+    TF/s as a burst (near the maximum SM clock) and sustained (power-capped,
+    back to back for seconds)."""
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
             p = json.load(f)
         return dict(hbm=float(p["hbm_gbs"]), bf16=float(p["bf16_tflops"]),
-                    bf16_sustained=float(p["bf16_tflops_sustained"]), source="measured")
+                    bf16_sustained=float(p["bf16_tflops_sustained"]),
+                    sm_max_mhz=float(p.get("sm_max_mhz", 2070.0)), source="measured")
     except (OSError, KeyError, ValueError):
-        return dict(hbm=6800.0, bf16=1900.0, bf16_sustained=1700.0, source="fallback")
+        return dict(hbm=6800.0, bf16=1900.0, bf16_sustained=1700.0, sm_max_mhz=2070.0,
+                    source="fallback")
+
+
+def tensor_peak(pk, clocks):
+    """The bf16 tensor peak that matches the clocks seen while the kernels
+    ran: the burst figure scaled by median SM MHz / maximum SM MHz (the
+    tensor rate is proportional to the SM clock), or the sustained figure
+    when no clock was sampled.  Returns (TF/s, how it was obtained)."""
+    sm = clocks.get("sm_mhz") if clocks else None
+    smax = (clocks.get("sm_max_mhz") if clocks else None) or pk["sm_max_mhz"]
+    if sm:
+        f = min(1.0, float(sm) / float(smax))
+        return pk["bf16"] * f, (f"{pk['source']} bf16_tflops (burst) x median SM clock "
+                                f"{sm:.0f} / {smax:.0f} MHz")
+    return pk["bf16_sustained"], f"{pk['source']} bf16_tflops_sustained (no clock sampled)"
 
 
 # ------------------------------------------------------------------ clocks
@@ -425,7 +448,7 @@ def mx_bytes(kind, T, D, E, K, F):
     }[kind]
 
 
-def measure_mx(wl, inp, steps, pk, flush):
+def measure_mx(wl, inp, steps, pk, flushed, dev):
     """The MXFP8 forward (route, permute + quantize, FC1 + SwiGLU + quantize
     h, FC2, combine) through the C ABI, weights quantized once before the
     timed loop; an event pair around every launch."""
@@ -468,19 +491,24 @@ def measure_mx(wl, inp, steps, pk, flush):
     for _ in range(3):
         run(None)
     torch.cuda.synchronize()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if flushed else None
     evs = []
-    for _ in range(steps):
-        if flush is not None:
-            flush.zero_()
-        ev = []
-        run(ev)
-        evs.append(ev)
-    torch.cuda.synchronize()
+    with clock_sampler(dev) as clk:
+        for _ in range(steps):
+            if flush is not None:
+                flush.zero_()
+            ev = []
+            run(ev)
+            evs.append(ev)
+        torch.cuda.synchronize()
+    clocks = clk.summary()
     if int(blk.status.item()) != 0:
         raise RuntimeError(f"device status {int(blk.status.item())} after the MX steps")
     times = {n: [ev[i].elapsed_time(ev[i + 1]) * 1e-3 for ev in evs] for i, n in enumerate(MX_STEPS)}
     step_s = sum(ev[0].elapsed_time(ev[-1]) * 1e-3 for ev in evs) / steps
-    fp8_peak = 2.0 * pk["bf16_sustained"]
+    # fp8 dense peak = the clock-matched bf16 peak x 2 (nominal 4.5 / 2.25 PF)
+    bf16_peak, bf16_src = tensor_peak(pk, clocks)
+    fp8_peak = 2.0 * bf16_peak
     kern = {}
     for n in MX_STEPS:
         avg = sum(times[n]) / len(times[n])
@@ -502,7 +530,8 @@ def measure_mx(wl, inp, steps, pk, flush):
         "steps": steps,
         "dtype": "e4m3 x e4m3 (E8M0 scales per 32), fp32 accumulation, bf16 out",
         "fp8_peak_tflops": fp8_peak,
-        "fp8_peak_source": f"{pk['source']} bf16_tflops_sustained x 2 (nominal fp8/bf16 ratio)",
+        "fp8_peak_source": f"nominal 2 x bf16: {bf16_src}",
+        "clocks": {k: clocks.get(k) for k in ("sm_mhz", "sm_max_mhz", "reasons")},
         "weights_quantize_us": {"wi": q0.elapsed_time(q1) * 1e3, "wo": q1.elapsed_time(q2) * 1e3},
         "gpu_launches_per_step": len(MX_STEPS),
         "kernels": kern,
@@ -515,6 +544,138 @@ def input_footprint(inp: dict) -> int:
     return sum(t.numel() * t.element_size() for t in inp.values() if isinstance(t, torch.Tensor))
 
 
+def kernel_table(wl, names, times, fwd_only, pk, tpeak):
+    """Per-kernel figures of a timed run and the block's roofline.
+
+    Each kernel is held to the resource that binds it at the peaks: a GEMM
+    to the tensor peak `tpeak`, or to the HBM peak when its algorithmic bytes
+    take longer at the HBM peak than its FLOPs at the tensor peak (weight
+    streaming at few rows per expert); the other steps to the HBM peak.  The
+    block's roofline is the sum of its kernels' roofline times."""
+    total = max(1e-12, sum(sum(v) for v in times.values()))
+    per_kernel, roof_s = {}, 0.0
+    for n in names:
+        ts = times[n]
+        avg = sum(ts) / len(ts)
+        k = {"avg_us": avg * 1e6, "median_us": statistics.median(ts) * 1e6,
+             "share": sum(ts) / total}
+        if n in GEMMS:
+            fl = gemm_flops(n, wl.R, wl.D, wl.F)
+            by = gemm_bytes(n, wl.R, wl.D, wl.E, wl.F, not fwd_only)
+            t_t, t_h = fl / (tpeak * 1e12), by / (pk["hbm"] * 1e9)
+            k.update(tflops=fl / avg / 1e12, frac_tensor=fl / avg / 1e12 / tpeak,
+                     hbm_gbs_algorithmic=by / avg / 1e9, frac_hbm=by / avg / 1e9 / pk["hbm"],
+                     bound="hbm" if t_h > t_t else "tensor")
+            t_roof = max(t_t, t_h)
+        else:
+            by = hbm_bytes(n, wl.T, wl.D, wl.E, wl.K, wl.F)
+            t_roof = by / (pk["hbm"] * 1e9)
+            k.update(gbs=by / avg / 1e9, frac_hbm=by / avg / 1e9 / pk["hbm"], bound="hbm")
+        k["roofline_us"] = t_roof * 1e6
+        k["frac_roofline"] = t_roof / avg
+        roof_s += t_roof
+        per_kernel[n] = k
+    return per_kernel, roof_s
+
+
+def dominant_roofline(wl, step, per_kernel, fwd_only, pk, tpeak, tpeak_src):
+    """The `roofline` object: the kernel with the largest share of the step,
+    its algorithmic FLOPs or bytes per launch over its mean launch time."""
+    dom = max(step.names, key=lambda n: sum(step.times[n]))
+    k = per_kernel[dom]
+    avg = k["avg_us"] * 1e-6
+    if dom in GEMMS and k["bound"] == "tensor":
+        achieved = gemm_flops(dom, wl.R, wl.D, wl.F) / avg / 1e12
+        roof = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": tpeak,
+                "unit": "TFLOP/s", "frac": achieved / tpeak, "peak_source": tpeak_src}
+    else:
+        by = (gemm_bytes(dom, wl.R, wl.D, wl.E, wl.F, not fwd_only) if dom in GEMMS
+              else hbm_bytes(dom, wl.T, wl.D, wl.E, wl.K, wl.F))
+        achieved = by / avg / 1e9
+        roof = {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": pk["hbm"],
+                "unit": "GB/s", "frac": achieved / pk["hbm"],
+                "peak_source": f"{pk['source']} hbm_gbs"}
+    roof["traffic"] = recorded_traffic(dom, wl.name)
+    return roof
+
+
+def measure_workload(wl, inp, steps, warmup, fwd_only, dev, dist=None):
+    """Times `steps` block steps of `wl` after `warmup` untimed ones, with a
+    CUDA event pair around every launch and the SM clock sampled throughout.
+    Inputs that fit in L2 get L2 flushed (a 256 MB write, not timed) before
+    every timed step.  Returns (step, elapsed seconds, clocks, flushed)."""
+    step = Step(wl, inp, fwd_only)
+    for _ in range(max(warmup, 3)):
+        step.run()
+    torch.cuda.synchronize()
+    barrier(dist)
+    torch.cuda.synchronize()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev) \
+        if input_footprint(inp) < L2_BYTES else None
+    with clock_sampler(dev) as clk:
+        if flush is None:
+            start = torch.cuda.Event(enable_timing=True)
+            end = torch.cuda.Event(enable_timing=True)
+            start.record()
+            for _ in range(steps):
+                step.run(record=True)
+            end.record()
+            torch.cuda.synchronize()
+            elapsed = start.elapsed_time(end) * 1e-3
+        else:
+            marks = []
+            for _ in range(steps):
+                flush.zero_()
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                step.run(record=True)
+                b.record()
+                marks.append((a, b))
+            torch.cuda.synchronize()
+            elapsed = sum(a.elapsed_time(b) for a, b in marks) * 1e-3
+    barrier(dist)
+    step.collect()
+    status = int(step.blk.status.item())
+    if status != 0:
+        raise RuntimeError(f"device status {status} after the timed steps of {wl.name}")
+    return step, elapsed, clk.summary(), flush is not None
+
+
+# every configuration of the block's workloads, with the pass each is quoted on
+CONFIG_SWEEP = ("tiny_fwd", "token_sweep_T1024", "token_sweep_T2048", "token_sweep_T4096",
+                "token_sweep_T8192", "long_seq_train", "large_expert_train", "zipf_skew_train")
+
+
+def measure_configs(steps, warmup, dev, pk, skip=()):
+    """Every configuration, each in its own timed loop on fresh inputs:
+    tokens/s, the block roofline at the peaks (tensor peak matched to the
+    clocks sampled during that loop), and per-kernel fractions."""
+    res = []
+    for name in CONFIG_SWEEP:
+        if name in skip:
+            continue
+        wl = WORKLOADS[name]
+        fwd_only = not wl.train
+        inp = make_inputs(wl, dev, with_grad=not fwd_only)
+        step, el, clocks, flushed = measure_workload(wl, inp, steps, warmup, fwd_only, dev)
+        tpeak, _ = tensor_peak(pk, clocks)
+        kern, roof_s = kernel_table(wl, step.names, step.times, fwd_only, pk, tpeak)
+        step_s = el / steps
+        res.append({
+            "workload": name, "pass": "fwd" if fwd_only else "fwd+bwd",
+            "T": wl.T, "D": wl.D, "E": wl.E, "K": wl.K, "F": wl.F,
+            "tokens_per_s": wl.T / step_s, "ms_per_step": step_s * 1e3, "steps": steps,
+            "roofline_ms": roof_s * 1e3, "roofline_frac": roof_s / step_s,
+            "tensor_peak_tflops": tpeak, "l2_flushed": flushed,
+            "clocks": {k: clocks.get(k) for k in ("sm_mhz", "sm_max_mhz", "reasons")},
+            "kernels": {n: {"median_us": v["median_us"], "bound": v["bound"],
+                            "frac_roofline": v["frac_roofline"]} for n, v in kern.items()},
+        })
+        del step, inp
+        torch.cuda.empty_cache()
+    return res
+
+
 def run_ours(args, dist, rank, world):
     wl = selected_workload(args)
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
@@ -525,46 +686,12 @@ def run_ours(args, dist, rank, world):
     wl_rank = replace(wl, seed=wl.seed + rank)
     fwd_only = args.fwd_only or not wl.train
     inp = make_inputs(wl_rank, dev, with_grad=not fwd_only)
-    step = Step(wl_rank, inp, fwd_only)
-    for _ in range(max(args.warmup, 3)):
-        step.run()
-    torch.cuda.synchronize()
     # ---- timed region: K steps, events around every launch
-    barrier(dist)
-    torch.cuda.synchronize()
-    # a step whose inputs fit in L2 gets L2 flushed (a 256 MB write) before
-    # every timed step; then only the steps themselves are timed
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev) \
-        if input_footprint(inp) < L2_BYTES else None
-    with clock_sampler(dev) as clk:
-        start = torch.cuda.Event(enable_timing=True)
-        end = torch.cuda.Event(enable_timing=True)
-        if flush is None:
-            start.record()
-            for _ in range(args.steps):
-                step.run(record=True)
-            end.record()
-            torch.cuda.synchronize()
-        else:
-            marks = []
-            for _ in range(args.steps):
-                flush.zero_()
-                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                a.record()
-                step.run(record=True)
-                b.record()
-                marks.append((a, b))
-            torch.cuda.synchronize()
-    barrier(dist)
-    if flush is None:
-        elapsed = start.elapsed_time(end) * 1e-3
-    else:
-        elapsed = sum(a.elapsed_time(b) for a, b in marks) * 1e-3
+    step, elapsed, clocks, flushed = measure_workload(wl_rank, inp, args.steps, args.warmup,
+                                                      fwd_only, dev, dist)
     elapsed_max = max_over_ranks(dist, elapsed)
-    step.collect()
-    status = int(step.blk.status.item())
-    if status != 0:
-        raise RuntimeError(f"device status {status} after the timed steps")
+    pk = peaks()
+    tpeak, tpeak_src = tensor_peak(pk, clocks)
 
     # ---- forward-only tokens/s, same inputs (a separate timed loop)
     fwd_tps = None
@@ -585,7 +712,7 @@ def run_ours(args, dist, rank, world):
     # ---- the MXFP8 forward on the same inputs (a separate timed loop)
     mx = None
     if not args.no_mx:
-        mx = measure_mx(wl_rank, inp, args.steps, peaks(), flush)
+        mx = measure_mx(wl_rank, inp, args.steps, pk, flushed, dev)
 
     # ---- end to end through the C ABI from pinned host buffers
     e2e = None
@@ -594,54 +721,22 @@ def run_ours(args, dist, rank, world):
 
     T = wl.T
     value = world * T * args.steps / elapsed_max
-    pk = peaks()
-    per_kernel = {}
-    for n in step.names:
-        ts = step.times[n]
-        avg = sum(ts) / len(ts)
-        per_kernel[n] = {"avg_us": avg * 1e6, "median_us": statistics.median(ts) * 1e6,
-                         "share": sum(ts) / max(1e-12, sum(sum(v) for v in step.times.values()))}
-        if n in GEMMS:
-            fl = gemm_flops(n, wl.R, wl.D, wl.F)
-            by = gemm_bytes(n, wl.R, wl.D, wl.E, wl.F, not fwd_only)
-            per_kernel[n]["tflops"] = fl / avg / 1e12
-            per_kernel[n]["frac_tensor"] = fl / avg / 1e12 / pk["bf16_sustained"]
-            per_kernel[n]["hbm_gbs_algorithmic"] = by / avg / 1e9
-            per_kernel[n]["frac_hbm"] = by / avg / 1e9 / pk["hbm"]
-            hbm_b = by / (pk["hbm"] * 1e9) > fl / (pk["bf16_sustained"] * 1e12)
-            per_kernel[n]["bound"] = "hbm" if hbm_b else "tensor"
-        else:
-            by = hbm_bytes(n, wl.T, wl.D, wl.E, wl.K, wl.F)
-            per_kernel[n]["gbs"] = by / avg / 1e9
-            per_kernel[n]["frac_hbm"] = by / avg / 1e9 / pk["hbm"]
-    dom = max(step.names, key=lambda n: sum(step.times[n]))
-    avg = sum(step.times[dom]) / len(step.times[dom])
-    # a GEMM is held to the resource that binds it: tensor peak, or HBM when
-    # its algorithmic bytes take longer at the HBM peak than its FLOPs at the
-    # tensor peak (weight streaming at few rows per expert)
-    gemm_hbm_bound = dom in GEMMS and (
-        gemm_bytes(dom, wl.R, wl.D, wl.E, wl.F, not fwd_only) / (pk["hbm"] * 1e9) >
-        gemm_flops(dom, wl.R, wl.D, wl.F) / (pk["bf16_sustained"] * 1e12))
-    if dom in GEMMS and gemm_hbm_bound:
-        achieved = gemm_bytes(dom, wl.R, wl.D, wl.E, wl.F, not fwd_only) / avg / 1e9
-        roof = {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": pk["hbm"],
-                "unit": "GB/s", "frac": achieved / pk["hbm"], "peak_source": f"{pk['source']} hbm_gbs"}
-    elif dom in GEMMS:
-        achieved = gemm_flops(dom, wl.R, wl.D, wl.F) / avg / 1e12
-        roof = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": pk["bf16_sustained"],
-                "unit": "TFLOP/s", "frac": achieved / pk["bf16_sustained"],
-                "peak_source": f"{pk['source']} bf16_tflops_sustained"}
-    else:
-        achieved = hbm_bytes(dom, wl.T, wl.D, wl.E, wl.K, wl.F) / avg / 1e9
-        roof = {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": pk["hbm"],
-                "unit": "GB/s", "frac": achieved / pk["hbm"], "peak_source": f"{pk['source']} hbm_gbs"}
-    roof["traffic"] = recorded_traffic(dom, wl.name)
+    launches = step.launches_per_step
+    per_kernel, roof_s = kernel_table(wl, step.names, step.times, fwd_only, pk, tpeak)
+    roof = dominant_roofline(wl, step, per_kernel, fwd_only, pk, tpeak, tpeak_src)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(wl, fwd_only, budget_s=20.0)
         if mx is not None:
             mx["cpu_baseline"] = mx_cpu_baseline(wl, budget_s=10.0)
+
+    configs = None
+    if rank == 0 and world == 1 and not args.no_configs and args.tokens is None \
+            and args.experts is None:
+        del step, inp
+        torch.cuda.empty_cache()
+        configs = measure_configs(min(args.steps, 10), 3, dev, pk)
 
     line = {
         "metric": METRIC_FWD if fwd_only else METRIC,
@@ -658,14 +753,18 @@ def run_ours(args, dist, rank, world):
         "data": "synthetic (seeded; N(0,1) activations, N(0,0.02) weights)",
         "config": {"workload": wl.name, "T": wl.T, "D": wl.D, "E": wl.E, "K": wl.K, "F": wl.F,
                    "pass": "fwd" if fwd_only else "fwd+bwd",
-                   "l2": "inputs larger than L2 (no flush)" if flush is None else
-                         "L2 flushed before each timed step (256 MB write, not timed)",
+                   "l2": "L2 flushed before each timed step (256 MB write, not timed)" if flushed
+                         else "inputs larger than L2 (no flush)",
                    "parallelism": f"replicas x{world}"},
         "roofline": roof,
+        "block_roofline": {"ms_per_step": roof_s * 1e3,
+                           "frac": roof_s / (elapsed / args.steps),
+                           "tensor_peak_tflops": tpeak, "tensor_peak_source": tpeak_src,
+                           "hbm_peak_gbs": pk["hbm"]},
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": step.launches_per_step * args.steps,
-        "clocks": clk.summary(),
+        "gpu_launches": launches * args.steps,
+        "clocks": clocks,
         "kernels": per_kernel,
     }
     if fwd_tps is not None:
@@ -673,6 +772,8 @@ def run_ours(args, dist, rank, world):
     if mx is not None:
         mx["value"] *= world
         line["mxfp8_forward"] = mx
+    if configs is not None:
+        line["configs"] = configs
     if rank == 0:
         print(json.dumps(line), flush=True)
 

@@ -146,7 +146,10 @@ moe_status moe_route_histogram(const float* logits, const float* bias, moe_score
  *   larger dims return MOE_ERR_UNSUPPORTED without launching anything.
  *   The first call on a device looks up the array's device address
  *   (cudaGetSymbolAddress) with that device current; make that first call
- *   before any stream capture.
+ *   before any stream capture.  The address is cached per device together
+ *   with the id of the device's CUDA context; a call in a new context (for
+ *   example after cudaDeviceReset) looks it up again, so that call too must
+ *   come before any capture.
  *   All calls share the one array: each call clears the counts it uses and
  *   rewrites the prefixes it reads, so earlier calls leave nothing behind,
  *   but calls that overlap on the GPU (different streams, or several host

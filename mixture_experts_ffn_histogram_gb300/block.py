@@ -51,8 +51,22 @@ class MoEBlock:
             self.dwi = torch.empty((E, D, 2 * F), dtype=bf, device=dev)
             self.dx = torch.empty((T, D), dtype=bf, device=dev)
 
+    def _check_weights(self, wi, wo):
+        """The library builds its tensor maps from the block's dims, so a
+        weight of another shape or dtype would be read (and its gradient
+        written) out of bounds: reject it before any launch."""
+        D, F, E = self.D, self.F, self.E
+        if wo.dtype != torch.bfloat16 or tuple(wo.shape) != (E, F, D):
+            raise ValueError(f"wo must be bf16 [{E}, {F}, {D}], got {wo.dtype} {tuple(wo.shape)}")
+        if isinstance(wi, (list, tuple)):
+            self._ranges(wi)
+        elif wi.dtype != torch.bfloat16 or tuple(wi.shape) != (E, D, 2 * F):
+            raise ValueError(f"wi must be bf16 [{E}, {D}, {2 * F}], got {wi.dtype} "
+                             f"{tuple(wi.shape)}")
+
     def forward(self, x, wi, wo, logits=None, bias=None, ids=None, w=None, stream=None):
         d = self.d
+        self._check_weights(wi, wo)
         if self.mode == B.SCORE_GIVEN:
             self.ids.copy_(ids)
             self.w.copy_(w)
@@ -77,6 +91,7 @@ class MoEBlock:
 
     def backward(self, dy, wi, wo, stream=None):
         d = self.d
+        self._check_weights(wi, wo)
         B.moe_combine_bwd(dy, self.ys, self.w, self.pos, self.dys, self.dw, d, stream)
         B.moe_grouped_gemm_fc2_bwd(self.dys, self.h, wo, self.z, self.group_offsets, self.dz,
                                    self.dwo, self.status, self.ws, d, stream)
@@ -100,6 +115,10 @@ class MoEBlock:
         """(e_begin, e_end, tensor) of each expert-range buffer of a split wi."""
         out, e0 = [], 0
         for part in parts:
+            if part.dtype != torch.bfloat16 or part.dim() != 3 or \
+                    tuple(part.shape[1:]) != (self.D, 2 * self.F):
+                raise ValueError(f"each wi part must be bf16 [experts, {self.D}, {2 * self.F}], "
+                                 f"got {part.dtype} {tuple(part.shape)}")
             e1 = e0 + int(part.shape[0])
             out.append((e0, e1, part))
             e0 = e1

@@ -19,6 +19,8 @@
 //   3. route_rank: per chunk, each warp ranks its contiguous run of slots
 //      with __match_any_sync; pos = group_offsets[e] + chunk prefix + warp
 //      prefix + rank, i.e. the stable order in the flat slot index t*K+k.
+#include <cuda.h>
+
 #include <cfloat>
 #include <climits>
 #include <mutex>
@@ -310,16 +312,48 @@ cudaError_t launch_route_histogram(const float* logits, const float* bias, int m
   return err;
 }
 
+// Unique id of the calling thread's current CUDA context (never reused
+// within a process), or 0 when there is none or the driver cannot say.
+static unsigned long long current_context_id() {
+  using GetCurrentFn = CUresult (*)(CUcontext*);
+  using GetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+  static GetCurrentFn get_current = nullptr;
+  static GetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<GetCurrentFn>(p);
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<GetIdFn>(p);
+  });
+  if (get_current == nullptr || get_id == nullptr) return 0;
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
+  if (get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
 // The same three kernels with their scratch in g_route_scratch.  The host
 // only knows a stand-in for the array's name; its device address is looked
-// up once per device (with that device current) on the first call.
+// up (with the device current) on the first call on each device, and again
+// whenever the device's context has changed since (after a cudaDeviceReset
+// the array lives at a new address in the new context).
 cudaError_t launch_route_histogram_static(const float* logits, const float* bias, int mode,
                                           int32_t* ids, float* w, int32_t* group_sizes,
                                           int32_t* group_offsets, int32_t* pos, int32_t* row_src,
                                           int32_t* dev_status, const moe_dims& d,
                                           cudaStream_t s) {
+  struct Cached {
+    int32_t* ptr;
+    unsigned long long ctx;
+  };
   static std::mutex mu;
-  static int32_t* scratch_of_device[64] = {};
+  static Cached scratch_of_device[64] = {};
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
@@ -327,12 +361,15 @@ cudaError_t launch_route_histogram_static(const float* logits, const float* bias
   int32_t* ptr = nullptr;
   {
     std::lock_guard<std::mutex> lock(mu);
-    if (scratch_of_device[dev] == nullptr) {
+    Cached& c = scratch_of_device[dev];
+    const unsigned long long ctx = current_context_id();
+    if (c.ptr == nullptr || ctx == 0 || ctx != c.ctx) {
       err = cudaGetSymbolAddress((void**)&ptr, g_route_scratch);
       if (err != cudaSuccess) return err;
-      scratch_of_device[dev] = ptr;
+      c.ptr = ptr;
+      c.ctx = current_context_id();  // the lookup made the device's context current
     }
-    ptr = scratch_of_device[dev];
+    ptr = c.ptr;
   }
   const size_t per = static_cast<size_t>(route_chunks(d.T)) * static_cast<size_t>(d.E);
   if (2 * per > kRouteStaticScratchInts) return cudaErrorInvalidValue;

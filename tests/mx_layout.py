@@ -44,8 +44,14 @@ def act_scale_index(offs, k):
     return ((g[:, None] * kb + b[None, :] // 4) * 512 + sf_byte(m[:, None], b[None, :] % 4))
 
 
+# Scale bytes that hold no element's scale (tail blocks past k, rows past a
+# group's end in its last 128-row tile, weight rows past N) are packed as 0xFF,
+# the E8M0 NaN: a GEMM that used one would produce NaN outputs.
+PAD = 0xFF
+
+
 def pack_act_scales(sc, offs, nbytes):
-    buf = np.full(nbytes, 127, np.uint8)
+    buf = np.full(nbytes, PAD, np.uint8)
     idx = act_scale_index(offs, sc.shape[1] * 32)
     buf[idx] = sc[: idx.shape[0]]
     return buf
@@ -86,7 +92,7 @@ def pack_weight(q, sc, interleave):
     E, N, k = q.shape
     codes = np.empty_like(q)
     codes[:, weight_rows(N, interleave), :] = q
-    buf = np.full(weight_scale_bytes(E, N, k), 127, np.uint8)
+    buf = np.full(weight_scale_bytes(E, N, k), PAD, np.uint8)
     buf[weight_scale_index(E, N, k, interleave)] = sc
     return codes, buf
 

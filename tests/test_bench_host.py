@@ -38,16 +38,51 @@ def test_binding_resource_of_a_gemm(name, kernel, bound):
 
 def test_mx_algorithmic_bytes_match_the_buffers():
     """The MX steps' algorithmic bytes are the sizes of what they must read
-    and write, as the library reports its MX buffers (codes plus one scale
-    byte per 32 elements; the tile-blocked scale buffers are upper bounds, so
-    their 1/32 counts are compared against the exact per-row figure)."""
+    and write, taken from the library's own MX buffer sizes (moe_mx_bytes, a
+    host-only call): the e4m3 code buffers exactly, plus one scale byte per 32
+    codes, which the tile-blocked scale buffers must be able to hold."""
+    from mixture_experts_ffn_histogram_gb300 import _build
+    from mixture_experts_ffn_histogram_gb300 import binding as B
+    _build.build()
     wl = WORKLOADS["long_seq_train"]
-    T, D, E, K, F, R = wl.T, wl.D, wl.E, wl.K, wl.F, wl.R
-    assert bench.mx_bytes("permute_quantize", T, D, E, K, F) == \
-        2 * T * D + R * D + R * D // 32 + 4 * T * K
-    # FC1 reads xq + scales and wi codes + scales, writes hq + scales
-    assert bench.mx_bytes("fc1", T, D, E, K, F) == \
-        (R * D + R * D // 32) + (E * 2 * F * D + E * 2 * F * D // 32) + (R * F + R * F // 32)
-    # FC2 reads hq + scales and wo codes + scales, writes bf16 ys
-    assert bench.mx_bytes("fc2", T, D, E, K, F) == \
-        (R * F + R * F // 32) + (E * D * F + E * D * F // 32) + 2 * R * D
+    T, D, E, K, F = wl.T, wl.D, wl.E, wl.K, wl.F
+    d = B.dims(T, D, E, K, F)
+    size = {w: B.moe_mx_bytes(d, w) for w in (B.MX_XQ, B.MX_XSC, B.MX_WIQ, B.MX_WISC, B.MX_WOQ,
+                                               B.MX_WOSC, B.MX_HQ, B.MX_HSC)}
+    for codes, scales in ((B.MX_XQ, B.MX_XSC), (B.MX_WIQ, B.MX_WISC), (B.MX_WOQ, B.MX_WOSC),
+                          (B.MX_HQ, B.MX_HSC)):
+        assert 0 < size[codes] // 32 <= size[scales]
+
+    def mx(codes):
+        return size[codes] + size[codes] // 32
+
+    # permute + quantize reads bf16 x and pos, writes the token codes and scales
+    assert bench.mx_bytes("permute_quantize", T, D, E, K, F) == 2 * T * D + mx(B.MX_XQ) + 4 * T * K
+    # FC1 reads the token and wi codes (with scales), writes h's codes and scales
+    assert bench.mx_bytes("fc1", T, D, E, K, F) == mx(B.MX_XQ) + mx(B.MX_WIQ) + mx(B.MX_HQ)
+    # FC2 reads h's and wo's codes (with scales), writes bf16 ys
+    assert bench.mx_bytes("fc2", T, D, E, K, F) == mx(B.MX_HQ) + mx(B.MX_WOQ) + 2 * wl.R * D
+
+
+def test_tensor_peak_follows_the_sampled_clock():
+    pk = {"bf16": 1924.2, "bf16_sustained": 1725.0, "sm_max_mhz": 2070.0, "source": "measured"}
+    assert bench.tensor_peak(pk, {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0})[0] == 1924.2
+    half = bench.tensor_peak(pk, {"sm_mhz": 1035.0, "sm_max_mhz": 2070.0})[0]
+    assert abs(half - 1924.2 / 2) < 1e-9
+    # never above the burst figure, and the sustained one without a clock record
+    assert bench.tensor_peak(pk, {"sm_mhz": 2100.0, "sm_max_mhz": 2070.0})[0] == 1924.2
+    assert bench.tensor_peak(pk, {"sm_mhz": None})[0] == 1725.0
+
+
+def test_block_roofline_is_the_sum_of_kernel_rooflines():
+    wl = WORKLOADS["long_seq_train"]
+    names = ["route", "permute", "fc1", "fc2", "combine"]
+    times = {n: [1e-3, 1e-3] for n in names}
+    pk = {"hbm": 6688.8}
+    kern, roof = bench.kernel_table(wl, names, times, True, pk, 1924.2)
+    assert abs(roof * 1e6 - sum(k["roofline_us"] for k in kern.values())) < 1e-6
+    fl = bench.gemm_flops("fc1", wl.R, wl.D, wl.F)
+    assert kern["fc1"]["bound"] == "tensor"
+    assert abs(kern["fc1"]["roofline_us"] - fl / 1924.2e12 * 1e6) < 1e-6
+    assert abs(kern["permute"]["roofline_us"] -
+               bench.hbm_bytes("permute", wl.T, wl.D, wl.E, wl.K, wl.F) / 6688.8e9 * 1e6) < 1e-6

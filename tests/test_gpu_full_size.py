@@ -1,18 +1,29 @@
 """GPU parity at the workloads' full sizes, in the configuration bench.py times.
 
-The block runs whole on the GPU (MoEBlock, the default GEMM path choice).
+The block runs whole on the GPU (MoEBlock, the default GEMM path choice) into
+buffers that were first filled with sentinels: NaN in every floating-point
+output, an impossible value in every integer one.  Every output is written
+exactly once by the block, so a tile that a kernel skipped shows up as a
+surviving sentinel, and a tile written with another tile's values fails the
+whole-tensor comparison.
+
 Checks:
+  * every element of every output was written (no sentinel left);
   * routing ids, group sizes/offsets, pos and row_src against the oracle,
     whole and bit-exact; routing weights within tolerance;
   * the permutation by its definition at full size (xs == x[row_src // K],
     exact);
-  * FC1 (h, z), FC2 (ys), combine (out) and every backward (dys, dw, dz,
-    dxs, dx) on sampled rows and tokens: the oracle recomputes each sampled
-    item from the original inputs (slices of x, wi, wo, dy and the oracle's
-    own routing), never from GPU outputs;
-  * dwi and dwo on sampled entries of the largest, the smallest and a random
-    expert, each a sum over all of the expert's rows computed by the oracle.
-Floats: |gpu - ref| <= 2e-2*|ref| + 2e-2.
+  * whole tensors (h, z, ys, out, dys, dw, dz, dxs, dx, dwo, dwi) against a
+    second reference: torch fp32 matmuls on the GPU, per expert, from the
+    original inputs and the oracle's routing, rounding to bf16 where the
+    block stores a tensor (never from an output of the CUDA path);
+  * the oracle itself on one row in every 128-row block of every group (h, z,
+    ys and, training, dys, dz, dxs), on sampled tokens (out, dys, dw, dz,
+    dxs, dx), and on one full dwo row per 128 rows of F and one full dwi row
+    per 128 rows of D for the largest, the smallest and a random expert; each
+    expected value is recomputed by the oracle from slices of the original
+    inputs.
+Floats: |gpu - ref| <= 2e-2*|ref| + 2e-2, except dw end to end (below).
 """
 import numpy as np
 import pytest
@@ -22,16 +33,37 @@ import oracle
 from mixture_experts_ffn_histogram_gb300 import binding as B
 from mixture_experts_ffn_histogram_gb300.block import MoEBlock
 from mixture_experts_ffn_histogram_gb300.inputs import WORKLOADS, make_inputs
-from tests.gpu_common import assert_close, assert_exact, need_gpu, to_dev, to_host
+from tests.gpu_common import ATOL, RTOL, assert_close, assert_exact, need_gpu, to_dev, to_host
 
 pytestmark = pytest.mark.gpu
 
-FULL = ["token_sweep_T1024", "token_sweep_T8192", "long_seq_train", "large_expert_train",
-        "zipf_skew_train"]
+FULL = ["tiny_fwd", "token_sweep_T1024", "token_sweep_T2048", "token_sweep_T4096",
+        "token_sweep_T8192", "long_seq_train", "large_expert_train", "zipf_skew_train"]
+
+INT_SENTINEL = -0x5EED
 
 
 def _bits(t):
     return to_host(t)
+
+
+def _outputs(blk):
+    """The block's output buffers: (name, tensor) pairs."""
+    names = ["ids", "w", "group_sizes", "group_offsets", "pos", "row_src", "xs", "h", "z", "ys",
+             "out"]
+    if blk.train:
+        names += ["dys", "dw", "dz", "dwo", "dxs", "dwi", "dx"]
+    return [(n, getattr(blk, n)) for n in names if getattr(blk, n, None) is not None]
+
+
+def _fill_sentinels(blk, given):
+    for name, t in _outputs(blk):
+        if given and name in ("ids", "w"):
+            continue  # inputs of the given routing, copied in by forward()
+        if t.dtype in (torch.bfloat16, torch.float32):
+            t.fill_(float("nan"))
+        else:
+            t.fill_(INT_SENTINEL)
 
 
 def _sub_problem(rows, row_src, off, K, E):
@@ -47,6 +79,87 @@ def _sub_problem(rows, row_src, off, K, E):
     return rows, tokens, sub_off
 
 
+# ------------------------------------------------------ torch fp32 chain
+def _gpu_close(name, got, want, rtol=RTOL, atol=ATOL, extra=None):
+    """Element-wise |got - want| <= rtol*|want| + atol (+ extra) on the GPU;
+    a NaN in `got` (a sentinel) always fails."""
+    g, w = got.float(), want.float()
+    lim = rtol * w.abs() + atol
+    if extra is not None:
+        lim = lim + extra
+    bad = ~((g - w).abs() <= lim)
+    n = int(bad.sum())
+    if n:
+        idx = bad.nonzero()[:5].tolist()
+        vals = [(i, float(g[tuple(i)]), float(w[tuple(i)])) for i in idx]
+        raise AssertionError(f"{name}: {n} of {g.numel()} elements outside tolerance; "
+                             f"first (index, got, want): {vals}")
+
+
+def _torch_chain(wl, inp, w_ref, pos, row_src, off):
+    """The block's tensors recomputed by torch on the GPU in fp32 (TF32 off),
+    per expert, from the original inputs and the oracle's routing; bf16
+    rounding wherever the block stores a tensor."""
+    prev = torch.backends.cuda.matmul.allow_tf32
+    torch.backends.cuda.matmul.allow_tf32 = False
+    try:
+        dev = inp["x"].device
+        T, D, E, K, F, R = wl.T, wl.D, wl.E, wl.K, wl.F, wl.R
+        bf = torch.bfloat16
+        pos_t = torch.from_numpy(pos).long().to(dev)
+        tokens = torch.from_numpy(row_src).long().to(dev) // K
+        w_t = torch.from_numpy(w_ref).to(dev)
+        x, wi, wo = inp["x"], inp["wi"], inp["wo"]
+        ref = {"xs": x[tokens]}
+        ref["h"] = torch.empty((R, F), dtype=bf, device=dev)
+        ref["z"] = torch.empty((R, 2 * F), dtype=bf, device=dev)
+        ref["ys"] = torch.empty((R, D), dtype=bf, device=dev)
+        for e in range(E):
+            r0, r1 = int(off[e]), int(off[e + 1])
+            if r1 == r0:
+                continue
+            a = ref["xs"][r0:r1].float() @ wi[e].float()
+            ref["z"][r0:r1] = a.to(bf)
+            ref["h"][r0:r1] = (torch.nn.functional.silu(a[:, :F]) * a[:, F:]).to(bf)
+            ref["ys"][r0:r1] = (ref["h"][r0:r1].float() @ wo[e].float()).to(bf)
+        acc = torch.zeros((T, D), dtype=torch.float32, device=dev)
+        for k in range(K):
+            acc += w_t[:, k:k + 1] * ref["ys"][pos_t[:, k]].float()
+        ref["out"] = acc.to(bf)
+        if not wl.train:
+            return ref
+        dy = inp["dy"]
+        ref["dys"] = torch.empty((R, D), dtype=bf, device=dev)
+        ref["dw"] = torch.empty((T, K), dtype=torch.float64, device=dev)
+        ref["dw_spread"] = torch.empty((T, K), dtype=torch.float64, device=dev)
+        for k in range(K):
+            ref["dys"][pos_t[:, k]] = (w_t[:, k:k + 1] * dy.float()).to(bf)
+            prod = dy.double() * ref["ys"][pos_t[:, k]].double()
+            ref["dw"][:, k] = prod.sum(1)
+            ref["dw_spread"][:, k] = prod.square().sum(1).sqrt()
+        ref["dz"] = torch.empty((R, 2 * F), dtype=bf, device=dev)
+        ref["dxs"] = torch.empty((R, D), dtype=bf, device=dev)
+        for e in range(E):
+            r0, r1 = int(off[e]), int(off[e + 1])
+            if r1 == r0:
+                continue
+            dh = ref["dys"][r0:r1].float() @ wo[e].float().T
+            g = ref["z"][r0:r1, :F].float()
+            u = ref["z"][r0:r1, F:].float()
+            sg = torch.sigmoid(g)
+            dgate = dh * u * sg * (1.0 + g * (1.0 - sg))
+            dup = dh * g * sg
+            ref["dz"][r0:r1] = torch.cat([dgate, dup], dim=1).to(bf)
+            ref["dxs"][r0:r1] = (ref["dz"][r0:r1].float() @ wi[e].float().T).to(bf)
+        acc = torch.zeros((T, D), dtype=torch.float32, device=dev)
+        for k in range(K):
+            acc += ref["dxs"][pos_t[:, k]].float()
+        ref["dx"] = acc.to(bf)
+        return ref
+    finally:
+        torch.backends.cuda.matmul.allow_tf32 = prev
+
+
 @pytest.fixture(scope="module", params=FULL)
 def run(request):
     need_gpu()
@@ -54,6 +167,8 @@ def run(request):
     dev = torch.device("cuda")
     inp = make_inputs(wl, dev, with_grad=wl.train)
     blk = MoEBlock(wl.T, wl.D, wl.E, wl.K, wl.F, wl.score_mode, train=wl.train)
+    _fill_sentinels(blk, wl.score_mode == B.SCORE_GIVEN)
+    torch.cuda.synchronize()
     blk.forward(inp["x"], inp["wi"], inp["wo"], logits=inp["logits"], bias=inp["bias"],
                 ids=inp["ids"], w=inp["w"])
     if wl.train:
@@ -69,10 +184,37 @@ def run(request):
                                       wl.score_mode, wl.T, wl.E, wl.K)
     gs, off, pos, row_src, bad = oracle.histogram(ids_ref, wl.E)
     assert bad == 0
-    yield dict(wl=wl, inp=inp, blk=blk, ids=ids_ref, w=w_ref, gs=gs, off=off, pos=pos,
-               row_src=row_src)
+    state = dict(wl=wl, inp=inp, blk=blk, ids=ids_ref, w=w_ref, gs=gs, off=off, pos=pos,
+                 row_src=row_src)
+    yield state
+    state.clear()
     del blk, inp
     torch.cuda.empty_cache()
+
+
+@pytest.fixture(scope="module")
+def chain(run):
+    ref = _torch_chain(run["wl"], run["inp"], run["w"], run["pos"], run["row_src"], run["off"])
+    yield ref
+    ref.clear()
+    torch.cuda.empty_cache()
+
+
+def _host_weights(run):
+    """Host copies of wi and wo (bf16 bits), made once per workload."""
+    if "wi_h" not in run:
+        run["wi_h"], run["wo_h"] = _bits(run["inp"]["wi"]), _bits(run["inp"]["wo"])
+    return run["wi_h"], run["wo_h"]
+
+
+def test_every_output_written(run):
+    for name, t in _outputs(run["blk"]):
+        if t.dtype in (torch.bfloat16, torch.float32):
+            n = int((~torch.isfinite(t)).sum())
+            assert n == 0, f"{name}: {n} of {t.numel()} elements not written (NaN sentinel left)"
+        else:
+            n = int((t == INT_SENTINEL).sum())
+            assert n == 0, f"{name}: {n} of {t.numel()} elements not written (sentinel left)"
 
 
 def test_routing_and_permutation_whole(run):
@@ -84,41 +226,93 @@ def test_routing_and_permutation_whole(run):
     assert_exact("pos", to_host(blk.pos), run["pos"])
     assert_exact("row_src", to_host(blk.row_src), run["row_src"])
     # the permutation at full size: xs[r] == x[row_src[r] // K] for every row
-    rs = blk.row_src.long()
+    rs = torch.from_numpy(run["row_src"]).long().cuda()
     assert torch.equal(blk.xs, run["inp"]["x"][rs // wl.K])
 
 
-def _sample_rows(run, n, rng):
-    off, E, R = run["off"], run["wl"].E, run["wl"].R
-    sizes = np.diff(off)
-    big, small = int(np.argmax(sizes)), int(np.argmin(np.where(sizes > 0, sizes, R + 1)))
-    rows = list(rng.integers(0, R, n))
-    for e in (big, small, int(rng.integers(0, E))):
-        if sizes[e] > 0:
-            rows += [int(off[e]), int(off[e + 1] - 1)]
+def test_activations_whole(run, chain):
+    blk = run["blk"]
+    names = ["h", "z", "ys", "out"] if blk.train else ["h", "ys", "out"]
+    if blk.train:
+        names += ["dys", "dz", "dxs", "dx"]
+    for n in names:
+        _gpu_close(f"{n} (whole)", getattr(blk, n), chain[n])
+    if blk.train:
+        # dw = sum_d dout * ys over D terms.  The reference uses its own bf16
+        # ys, each of which may sit one rounding (2^-8 relative) from the
+        # block's while both are correct; for independent differences the sum
+        # moves by about 2^-8 * sqrt(sum_d (dout_d ys_d)^2), so the bound adds
+        # four times that to the per-element tolerance.
+        _gpu_close("dw (whole)", blk.dw.double(), chain["dw"],
+                   extra=4 * 2.0 ** -8 * chain["dw_spread"])
+
+
+def test_weight_gradients_whole(run, chain):
+    wl, blk = run["wl"], run["blk"]
+    if not wl.train:
+        pytest.skip("forward-only workload")
+    prev = torch.backends.cuda.matmul.allow_tf32
+    torch.backends.cuda.matmul.allow_tf32 = False
+    try:
+        off = run["off"]
+        for e in range(wl.E):
+            r0, r1 = int(off[e]), int(off[e + 1])
+            if r1 == r0:
+                assert int(blk.dwo[e].float().abs().max()) == 0, f"dwo[{e}] of an empty expert"
+                assert int(blk.dwi[e].float().abs().max()) == 0, f"dwi[{e}] of an empty expert"
+                continue
+            dwo_e = (chain["h"][r0:r1].float().T @ chain["dys"][r0:r1].float()).to(torch.bfloat16)
+            _gpu_close(f"dwo[{e}] (whole)", blk.dwo[e], dwo_e)
+            dwi_e = (chain["xs"][r0:r1].float().T @ chain["dz"][r0:r1].float()).to(torch.bfloat16)
+            _gpu_close(f"dwi[{e}] (whole)", blk.dwi[e], dwi_e)
+    finally:
+        torch.backends.cuda.matmul.allow_tf32 = prev
+
+
+# ------------------------------------------------------------ the oracle
+def _rows_per_block(run, rng, block=128):
+    """One random row in every `block`-row block of every group."""
+    off = run["off"]
+    rows = []
+    for e in range(run["wl"].E):
+        r0, r1 = int(off[e]), int(off[e + 1])
+        for b0 in range(r0, r1, block):
+            rows.append(b0 + int(rng.integers(0, min(block, r1 - b0))))
     return rows
 
 
 def _oracle_rows(run, rows):
-    """Oracle forward for sampled sorted-order rows (from the inputs)."""
+    """Oracle forward (and, training, backward) of sampled sorted-order rows,
+    from the inputs."""
     wl, inp = run["wl"], run["inp"]
     rows, tokens, sub_off = _sub_problem(rows, run["row_src"], run["off"], wl.K, wl.E)
     xs = to_host(inp["x"][torch.from_numpy(tokens).long().cuda()])
-    wi, wo = _bits(inp["wi"]), _bits(inp["wo"])
+    wi, wo = _host_weights(run)
     h, z = oracle.fc1_swiglu(xs, wi, sub_off)
     ys = oracle.fc2(h, wo, sub_off)
-    return dict(rows=rows, tokens=tokens, sub_off=sub_off, xs=xs, h=h, z=z, ys=ys, wi=wi, wo=wo)
+    o = dict(rows=rows, tokens=tokens, sub_off=sub_off, xs=xs, h=h, z=z, ys=ys, wi=wi, wo=wo)
+    if wl.train:
+        src = run["row_src"][rows]
+        slots = src % wl.K
+        dy_rows = to_host(inp["dy"][torch.from_numpy(tokens).long().cuda()])
+        w_rows = run["w"][tokens, slots].astype(np.float32)
+        pos_one = np.arange(len(rows), dtype=np.int32)[:, None]
+        dys, _ = oracle.combine_bwd(dy_rows, np.zeros((len(rows), wl.D), np.uint16),
+                                    w_rows[:, None], pos_one)
+        dz, _ = oracle.fc2_bwd(dys, h, wo, z, sub_off, want_drhs=False)
+        dxs, _ = oracle.fc1_bwd(dz, xs, wi, sub_off, want_drhs=False)
+        o.update(dys=dys, dz=dz, dxs=dxs)
+    return o
 
 
-def test_gemms_on_sampled_rows(run):
+def test_gemm_rows_in_every_block(run):
     rng = np.random.Generator(np.random.PCG64(11))
-    o = _oracle_rows(run, _sample_rows(run, 24, rng))
+    o = _oracle_rows(run, _rows_per_block(run, rng))
     blk = run["blk"]
     idx = torch.from_numpy(o["rows"]).long().cuda()
-    assert_close("h", to_host(blk.h[idx]), o["h"])
-    if blk.z is not None:
-        assert_close("z", to_host(blk.z[idx]), o["z"])
-    assert_close("ys", to_host(blk.ys[idx]), o["ys"])
+    names = ["h", "ys"] + (["z", "dys", "dz", "dxs"] if blk.train else [])
+    for n in names:
+        assert_close(f"{n} (one row per 128-row block)", to_host(getattr(blk, n)[idx]), o[n])
 
 
 def test_combine_and_backward_on_sampled_tokens(run):
@@ -140,11 +334,7 @@ def test_combine_and_backward_on_sampled_tokens(run):
     dys_ref, dw_ref = oracle.combine_bwd(dy, o["ys"], w_sub, pos_sub)
     ri = torch.from_numpy(o["rows"]).long().cuda()
     assert_close("dys", to_host(blk.dys[ri]), dys_ref)
-    # dw is a sum over D of dout * ys: end to end it sees the GPU's own ys,
-    # whose bf16 roundings may each differ by one ulp (2^-8 relative) from the
-    # oracle's; for independent differences the sum moves by about
-    # 2^-8 * sqrt(sum_d (dout_d ys_d)^2), so the end-to-end bound adds four
-    # times that to the per-element tolerance.
+    # dw end to end sees the GPU's own ys: the same derived bound as above
     y64 = (o["ys"].astype(np.uint32) << 16).view(np.float32).astype(np.float64)
     g64 = (dy.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
     spread = np.sqrt(np.einsum("td,tkd->tk", g64 ** 2, y64[pos_sub] ** 2))
@@ -160,61 +350,55 @@ def test_combine_and_backward_on_sampled_tokens(run):
     torch.cuda.synchronize()
     assert_exact("dys (isolated)", to_host(dys1), dys_ref)
     assert_close("dw (isolated)", to_host(dw1), dw_ref, bf16=False)
-    dz_ref, _ = oracle.fc2_bwd(dys_ref, o["h"], o["wo"], o["z"], o["sub_off"], want_drhs=False)
-    assert_close("dz", to_host(blk.dz[ri]), dz_ref)
-    dxs_ref, _ = oracle.fc1_bwd(dz_ref, o["xs"], o["wi"], o["sub_off"], want_drhs=False)
-    assert_close("dxs", to_host(blk.dxs[ri]), dxs_ref)
-    dx_ref = oracle.permute_bwd(dxs_ref, pos_sub, len(tok), wl.D)
+    assert_close("dz", to_host(blk.dz[ri]), o["dz"])
+    assert_close("dxs", to_host(blk.dxs[ri]), o["dxs"])
+    dx_ref = oracle.permute_bwd(o["dxs"], pos_sub, len(tok), wl.D)
     assert_close("dx", to_host(blk.dx[ti]), dx_ref)
 
 
-def test_weight_gradients_on_sampled_entries(run):
+def test_weight_gradient_rows_per_block(run):
+    """For the largest, the smallest and a random expert: one full dwo row in
+    every 128 rows of F and one full dwi row in every 128 rows of D, each a
+    sum over all of the expert's rows, recomputed by the oracle from the
+    inputs (FC1 of the expert's tokens, the combine backward of its slots, the
+    FC2 backward with the SwiGLU backward)."""
     wl, inp, blk = run["wl"], run["inp"], run["blk"]
     if not wl.train:
         pytest.skip("forward-only workload")
     rng = np.random.Generator(np.random.PCG64(13))
     off, K, F, D = run["off"], wl.K, wl.F, wl.D
     sizes = np.diff(off)
-    experts = {int(np.argmax(sizes)), int(np.argmin(sizes)), int(rng.integers(0, wl.E))}
-    wi, wo = blk.dwi, blk.dwo
+    nonempty = np.flatnonzero(sizes > 0)
+    experts = {int(np.argmax(sizes)), int(nonempty[np.argmin(sizes[nonempty])]),
+               int(rng.integers(0, wl.E))}
     for e in sorted(experts):
         r0, r1 = int(off[e]), int(off[e + 1])
-        f, d, n = int(rng.integers(0, F)), int(rng.integers(0, D)), int(rng.integers(0, 2 * F))
-        if r1 == r0:
+        n = r1 - r0
+        if n == 0:
             assert float(blk.dwo[e].float().abs().max()) == 0.0
             assert float(blk.dwi[e].float().abs().max()) == 0.0
             continue
-        rows = np.arange(r0, r1)
-        src = run["row_src"][rows]
+        src = run["row_src"][np.arange(r0, r1)]
         tokens, slots = src // K, src % K
         ti = torch.from_numpy(tokens).long().cuda()
         x_rows = to_host(inp["x"][ti])
         dy_rows = to_host(inp["dy"][ti])
         w_rows = run["w"][tokens, slots].astype(np.float32)
-        one = np.array([0, r1 - r0], np.int32)
-        # dys rows of this expert: the combine backward per row (unit slot each)
-        pos_one = np.arange(r1 - r0, dtype=np.int32)[:, None]
-        dys_rows, _ = oracle.combine_bwd(dy_rows, np.zeros((r1 - r0, D), np.uint16),
-                                         w_rows[:, None], pos_one)
-        wi_e = to_host(inp["wi"][e])          # [D, 2F]
-        wo_e = to_host(inp["wo"][e])          # [F, D]
-        # h[:, f] and z[:, f], z[:, F+f] from the gate/up columns of wi
-        cols = [f, F + f]
-        h_f, z_f = oracle.fc1_swiglu(x_rows, wi_e[None][:, :, cols], one)
-        # dwo[e, f, d] = sum_r h[r, f] * dys[r, d]
-        _, dwo_fd = oracle.fc2_bwd(dys_rows[:, [d]], h_f, wo_e[None][:, [f]][:, :, [d]], None,
-                                   one, want_dlhs=False)
-        assert_close(f"dwo[{e},{f},{d}]", to_host(blk.dwo[e, f, d].reshape(1)),
-                     dwo_fd.reshape(1))
-        # dz[:, n]: dh[:, fn] (against all of wo[e, fn, :]) through the SwiGLU backward
-        fn = n % F
-        cols_n = [fn, F + fn]
-        _, z_n = oracle.fc1_swiglu(x_rows, wi_e[None][:, :, cols_n], one)
-        dz_n, _ = oracle.fc2_bwd(dys_rows, np.zeros((r1 - r0, 1), np.uint16),
-                                 wo_e[None][:, [fn]], z_n, one, want_drhs=False)
-        dz_col = dz_n[:, [0 if n < F else 1]]
-        # dwi[e, d, n] = sum_r xs[r, d] * dz[r, n]
-        _, dwi_dn = oracle.fc1_bwd(np.concatenate([dz_col, dz_col], axis=1), x_rows[:, [d]],
-                                   np.zeros((1, 1, 2), np.uint16), one, want_dlhs=False)
-        assert_close(f"dwi[{e},{d},{n}]", to_host(blk.dwi[e, d, n].reshape(1)),
-                     dwi_dn[0, 0, :1])
+        one = np.array([0, n], np.int32)
+        pos_one = np.arange(n, dtype=np.int32)[:, None]
+        dys_rows, _ = oracle.combine_bwd(dy_rows, np.zeros((n, D), np.uint16), w_rows[:, None],
+                                         pos_one)
+        wi_h, wo_h = _host_weights(run)
+        wi_e, wo_e = wi_h[e:e + 1], wo_h[e:e + 1]     # [1, D, 2F], [1, F, D]
+        h_e, z_e = oracle.fc1_swiglu(x_rows, wi_e, one)
+        dz_e, _ = oracle.fc2_bwd(dys_rows, h_e, wo_e, z_e, one, want_drhs=False)
+        fs = [b + int(rng.integers(0, min(128, F - b))) for b in range(0, F, 128)]
+        ds = [b + int(rng.integers(0, min(128, D - b))) for b in range(0, D, 128)]
+        # dwo[e, f, :] = sum_r h[r, f] * dys[r, :]
+        _, dwo_rows = oracle.fc2_bwd(dys_rows, h_e[:, fs], np.zeros((1, len(fs), D), np.uint16),
+                                     None, one, want_dlhs=False)
+        assert_close(f"dwo[{e}] rows {fs}", to_host(blk.dwo[e][fs]), dwo_rows[0])
+        # dwi[e, d, :] = sum_r xs[r, d] * dz[r, :]
+        _, dwi_rows = oracle.fc1_bwd(dz_e, x_rows[:, ds], np.zeros((1, len(ds), 2 * F), np.uint16),
+                                     one, want_dlhs=False)
+        assert_close(f"dwi[{e}] rows {ds}", to_host(blk.dwi[e][ds]), dwi_rows[0])

@@ -68,6 +68,13 @@ def _u8(n):
     return torch.empty(int(n), dtype=torch.uint8, device="cuda")
 
 
+def _sc(n):
+    """A scale buffer prefilled with 0xFF (the E8M0 NaN): a GEMM that read a
+    scale byte no quantize kernel wrote (tail k-steps, padding rows of partial
+    tiles, weight rows past N) would turn its outputs into NaN."""
+    return torch.full((int(n),), 0xFF, dtype=torch.uint8, device="cuda")
+
+
 def _rms(a):
     return float(np.sqrt(np.mean(np.square(a.astype(np.float64))))) if a.size else 0.0
 
@@ -81,8 +88,8 @@ def test_quantize_weights_exact(case):
     wl, inp, ref = case
     d = _dims(wl)
     E, D, F = wl.E, wl.D, wl.F
-    wiq, wisc = _u8(B.moe_mx_bytes(d, B.MX_WIQ)), _u8(B.moe_mx_bytes(d, B.MX_WISC))
-    woq, wosc = _u8(B.moe_mx_bytes(d, B.MX_WOQ)), _u8(B.moe_mx_bytes(d, B.MX_WOSC))
+    wiq, wisc = _u8(B.moe_mx_bytes(d, B.MX_WIQ)), _sc(B.moe_mx_bytes(d, B.MX_WISC))
+    woq, wosc = _u8(B.moe_mx_bytes(d, B.MX_WOQ)), _sc(B.moe_mx_bytes(d, B.MX_WOSC))
     assert wisc.numel() == L.weight_scale_bytes(E, 2 * F, D)
     assert wosc.numel() == L.weight_scale_bytes(E, D, F)
     B.moe_mx_quantize_wi(to_dev(inp["wi"]), wiq, wisc, d)
@@ -101,7 +108,7 @@ def test_permute_quantize_exact(case):
     d = _dims(wl)
     R = wl.T * wl.K
     used = int(ref["group_offsets"][-1])
-    xq, xsc = _u8(B.moe_mx_bytes(d, B.MX_XQ)), _u8(B.moe_mx_bytes(d, B.MX_XSC))
+    xq, xsc = _u8(B.moe_mx_bytes(d, B.MX_XQ)), _sc(B.moe_mx_bytes(d, B.MX_XSC))
     B.moe_mx_permute_quantize(to_dev(inp["x"]), to_dev(ref["pos"]), to_dev(ref["group_offsets"]),
                               xq, xsc, d)
     torch.cuda.synchronize()
@@ -194,7 +201,7 @@ def test_fc1_swiglu(case):
     xsc = L.pack_act_scales(ref["xsc"], offs, B.moe_mx_bytes(d, B.MX_XSC))
     wq, wsc = L.pack_weight(ref["wq"], ref["wsc"], True)
     h = torch.zeros((R, F), dtype=torch.bfloat16, device="cuda")
-    hq, hsc = _u8(B.moe_mx_bytes(d, B.MX_HQ)), _u8(B.moe_mx_bytes(d, B.MX_HSC))
+    hq, hsc = _u8(B.moe_mx_bytes(d, B.MX_HQ)), _sc(B.moe_mx_bytes(d, B.MX_HSC))
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
     B.moe_mx_grouped_gemm_fc1_swiglu(to_dev(xq), to_dev(xsc), to_dev(wq), to_dev(wsc),
                                      to_dev(offs), hq, hsc, h, st, d)
@@ -244,13 +251,13 @@ def mx_forward_gpu(wl, inp, stream=None):
     ws = _u8(max(B.moe_workspace_bytes(d), 16))
     B.moe_route_histogram(dev.get("logits"), dev.get("bias"), wl.score_mode, ids, w, gs, offs, pos,
                           row_src, st, ws, d)
-    wiq, wisc = _u8(B.moe_mx_bytes(d, B.MX_WIQ)), _u8(B.moe_mx_bytes(d, B.MX_WISC))
-    woq, wosc = _u8(B.moe_mx_bytes(d, B.MX_WOQ)), _u8(B.moe_mx_bytes(d, B.MX_WOSC))
+    wiq, wisc = _u8(B.moe_mx_bytes(d, B.MX_WIQ)), _sc(B.moe_mx_bytes(d, B.MX_WISC))
+    woq, wosc = _u8(B.moe_mx_bytes(d, B.MX_WOQ)), _sc(B.moe_mx_bytes(d, B.MX_WOSC))
     B.moe_mx_quantize_wi(dev["wi"], wiq, wisc, d)
     B.moe_mx_quantize_wo(dev["wo"], woq, wosc, d)
-    xq, xsc = _u8(B.moe_mx_bytes(d, B.MX_XQ)), _u8(B.moe_mx_bytes(d, B.MX_XSC))
+    xq, xsc = _u8(B.moe_mx_bytes(d, B.MX_XQ)), _sc(B.moe_mx_bytes(d, B.MX_XSC))
     B.moe_mx_permute_quantize(dev["x"], pos, offs, xq, xsc, d)
-    hq, hsc = _u8(B.moe_mx_bytes(d, B.MX_HQ)), _u8(B.moe_mx_bytes(d, B.MX_HSC))
+    hq, hsc = _u8(B.moe_mx_bytes(d, B.MX_HQ)), _sc(B.moe_mx_bytes(d, B.MX_HSC))
     B.moe_mx_grouped_gemm_fc1_swiglu(xq, xsc, wiq, wisc, offs, hq, hsc, None, st, d)
     ys = torch.empty((R, D), dtype=torch.bfloat16, device="cuda")
     B.moe_mx_grouped_gemm_fc2(hq, hsc, woq, wosc, offs, ys, st, d)
