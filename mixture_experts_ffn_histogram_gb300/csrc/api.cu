@@ -111,12 +111,10 @@ moe_status moe_route_histogram(const float* logits, const float* bias, moe_score
       MOE_OPTIONAL(w);
     }
   }
-  int32_t* counts = static_cast<int32_t*>(ws);
-  int32_t* chunk_excl =
-      counts + static_cast<size_t>(moe::route_chunks(d.T)) * static_cast<size_t>(d.E);
   return from_cuda(moe::launch_route_histogram(logits, bias, static_cast<int>(mode), ids, w,
                                                group_sizes, group_offsets, pos, row_src,
-                                               dev_status, counts, chunk_excl, d, stream));
+                                               dev_status, ws, moe::route_max_blocks(d.T), d,
+                                               stream));
 }
 
 moe_status moe_route_histogram_noalloc(const float* logits, const float* bias, moe_score_mode mode,

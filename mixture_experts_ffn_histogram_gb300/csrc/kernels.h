@@ -10,25 +10,33 @@
 
 namespace moe {
 
-// Routing: tokens handled by one block of the routing kernels.
-constexpr int kRouteTokensPerChunk = 256;
-
-inline int route_chunks(int T) { return (T + kRouteTokensPerChunk - 1) / kRouteTokensPerChunk; }
-// Scratch of the routing/histogram step: per-chunk expert counts and their
-// exclusive prefix over chunks, both int32 [chunks, E].
+// Routing scratch (a caller workspace, or the no-allocation call's fixed
+// array): the grid barrier's word inside the first kRouteBarrierBytes, then
+// one int32 per (block, expert) for the blocks' per-expert totals, for up to
+// `max_blocks` blocks.  A block of the routing kernel covers at least one
+// token and there is at most one block per SM, so min(T, kRouteBlocksBound)
+// blocks bound the grid on any device.
+constexpr size_t kRouteBarrierBytes = 256;
+constexpr long kRouteBlocksBound = 1024;
+inline long route_max_blocks(int T) { return T < kRouteBlocksBound ? T : kRouteBlocksBound; }
 inline size_t route_ws_bytes(const moe_dims& d) {
-  return 2ull * static_cast<size_t>(route_chunks(d.T)) * static_cast<size_t>(d.E) * sizeof(int32_t);
+  return kRouteBarrierBytes + static_cast<size_t>(route_max_blocks(d.T)) *
+                                  static_cast<size_t>(d.E) * sizeof(int32_t);
 }
 
+// Routing over `max_blocks` blocks at most (the per-block totals that fit in
+// `scratch` after the barrier word).
 cudaError_t launch_route_histogram(const float* logits, const float* bias, int mode, int32_t* ids,
                                    float* w, int32_t* group_sizes, int32_t* group_offsets,
                                    int32_t* pos, int32_t* row_src, int32_t* dev_status,
-                                   int32_t* counts, int32_t* chunk_excl, const moe_dims& d,
+                                   void* scratch, long max_blocks, const moe_dims& d,
                                    cudaStream_t s);
 
 // Capacity, in int32, of the fixed scratch of the no-allocation routing
-// call: 2 * ceil(T/256) * E must not exceed it.
+// call.  Its documented limit, 2 * ceil(T/256) * E <= this, is what the C
+// entry point checks; the kernel needs less.
 constexpr size_t kRouteStaticScratchInts = 262144;  // 1 MiB
+inline int route_chunks(int T) { return (T + 255) / 256; }
 cudaError_t launch_route_histogram_static(const float* logits, const float* bias, int mode,
                                           int32_t* ids, float* w, int32_t* group_sizes,
                                           int32_t* group_offsets, int32_t* pos, int32_t* row_src,

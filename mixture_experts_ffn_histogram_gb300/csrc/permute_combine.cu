@@ -40,14 +40,13 @@ int grid_for_tokens(int T) {
 }
 
 // Warps per token row for the gathers.  With few tokens one warp per row
-// leaves the SMs with too few loads in flight (1024 tokens: ~7 warps per
-// SM), so a row is split into column slices of whole 32*VPL-vector passes,
-// one warp each, until about 64 warps per SM are busy.  Every output element
-// is still computed by one lane in the same order, so results do not change.
-int split_for_tokens(int T, int Dv, int vpl) {
-  const long want = static_cast<long>(sm_count()) * 64;
+// leaves the SMs with too few loads in flight, so a row is split into
+// column slices of whole 32*VPL-vector passes, one warp each, until about
+// `want_warps` warps are busy.  Every output element is still computed by
+// one lane in the same order, so results do not change.
+int split_for_tokens(int T, int Dv, int vpl, long want_warps) {
   const int max_split = max(1, Dv / (32 * vpl));
-  long sp = T > 0 ? want / T : 1;
+  long sp = T > 0 ? (want_warps + T - 1) / T : 1;
   if (sp < 1) sp = 1;
   if (sp > max_split) sp = max_split;
   return static_cast<int>(sp);
@@ -108,6 +107,15 @@ __device__ __forceinline__ void axpy8(float (&acc)[8], float wk, const uint4& v)
   }
 }
 
+// Slots of the combine backward whose ys rows one lane has in flight at once:
+// their loads are issued before any of them is used, so a warp waits for one
+// DRAM round trip per batch instead of one per slot (measured at the
+// long-sequence shape: 522 -> 474 us).  The forward gather is the opposite
+// case: there one slot at a time beat batches of 2, 4 and 8 slots at every
+// measured shape (long sequence, 8192 and 1024 tokens), and more warps per
+// row are what helps when tokens are few.
+constexpr int kSlotBatch = 8;
+
 // out[t] = bf16(sum_k w[t,k] * ys[pos[t,k]]); w == nullptr means unit weights.
 template <int VPL, bool SPLIT>
 __global__ void __launch_bounds__(kThreads) combine_kernel(const uint4* __restrict__ ys,
@@ -165,6 +173,10 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const uint4* __restri
 }
 
 // dys[pos[t,k]] = bf16(w * dout[t]);  dw[t,k] = <dout[t], ys[pos[t,k]]>.
+// Slots go in batches of kSlotBatch: per column chunk, the dout vectors and
+// the ys vectors of every slot of the batch are loaded before any is used.
+// Each lane accumulates its part of a dot product over the chunks in
+// ascending column order; the warp then sums the lanes' parts.
 template <int VPL>
 __global__ void __launch_bounds__(kThreads) combine_bwd_kernel(
     const uint4* __restrict__ dout, const uint4* __restrict__ ys, const float* __restrict__ w,
@@ -176,36 +188,50 @@ __global__ void __launch_bounds__(kThreads) combine_bwd_kernel(
     const int p_lane = (lane < K) ? __ldg(pos + j) : -1;
     const float w_lane = (lane < K) ? __ldg(w + j) : 0.f;
     const uint4* g = dout + static_cast<long>(t) * Dv;
-    for (int k = 0; k < K; ++k) {
-      const int p = __shfl_sync(0xffffffffu, p_lane, k);
-      const float wk = __shfl_sync(0xffffffffu, w_lane, k);
-      float dot = 0.f;
-      if (p >= 0) {
-        const uint4* y = ys + static_cast<long>(p) * Dv;
-        uint4* dst = dys + static_cast<long>(p) * Dv;
-        for (int v0 = 0; v0 < Dv; v0 += 32 * VPL) {
-          uint4 gv[VPL], yv[VPL];
+    for (int k0 = 0; k0 < K; k0 += kSlotBatch) {
+      int pk[kSlotBatch];
+      float wk[kSlotBatch], dot[kSlotBatch];
+#pragma unroll
+      for (int b = 0; b < kSlotBatch; ++b) {
+        const int k = k0 + b;
+        pk[b] = (k < K) ? __shfl_sync(0xffffffffu, p_lane, k) : -1;
+        wk[b] = (k < K) ? __shfl_sync(0xffffffffu, w_lane, k) : 0.f;
+        dot[b] = 0.f;
+      }
+      for (int v0 = 0; v0 < Dv; v0 += 32 * VPL) {
+        uint4 gv[VPL], yv[kSlotBatch][VPL];
+#pragma unroll
+        for (int i = 0; i < VPL; ++i) {
+          const int idx = v0 + i * 32 + lane;
+          if (idx < Dv) gv[i] = __ldg(g + idx);
+        }
+#pragma unroll
+        for (int b = 0; b < kSlotBatch; ++b) {
+          if (pk[b] < 0) continue;
+          const uint4* y = ys + static_cast<long>(pk[b]) * Dv;
 #pragma unroll
           for (int i = 0; i < VPL; ++i) {
             const int idx = v0 + i * 32 + lane;
-            if (idx < Dv) {
-              gv[i] = __ldg(g + idx);
-              yv[i] = ld_stream(y + idx);
-            }
+            if (idx < Dv) yv[b][i] = ld_stream(y + idx);
           }
+        }
+#pragma unroll
+        for (int b = 0; b < kSlotBatch; ++b) {
+          if (pk[b] < 0) continue;
+          uint4* dst = dys + static_cast<long>(pk[b]) * Dv;
 #pragma unroll
           for (int i = 0; i < VPL; ++i) {
             const int idx = v0 + i * 32 + lane;
             if (idx < Dv) {
               const uint32_t gu[4] = {gv[i].x, gv[i].y, gv[i].z, gv[i].w};
-              const uint32_t yu[4] = {yv[i].x, yv[i].y, yv[i].z, yv[i].w};
+              const uint32_t yu[4] = {yv[b][i].x, yv[b][i].y, yv[b][i].z, yv[b][i].w};
               uint32_t o[4];
 #pragma unroll
               for (int q = 0; q < 4; ++q) {
                 const float g0 = bf16lo(gu[q]), g1 = bf16hi(gu[q]);
-                o[q] = pack_bf16x2(__fmul_rn(wk, g0), __fmul_rn(wk, g1));
-                dot = fmaf(g0, bf16lo(yu[q]), dot);
-                dot = fmaf(g1, bf16hi(yu[q]), dot);
+                o[q] = pack_bf16x2(__fmul_rn(wk[b], g0), __fmul_rn(wk[b], g1));
+                dot[b] = fmaf(g0, bf16lo(yu[q]), dot[b]);
+                dot[b] = fmaf(g1, bf16hi(yu[q]), dot[b]);
               }
               dst[idx] = make_uint4(o[0], o[1], o[2], o[3]);
             }
@@ -213,8 +239,12 @@ __global__ void __launch_bounds__(kThreads) combine_bwd_kernel(
         }
       }
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
-      if (lane == 0) dw[static_cast<long>(t) * K + k] = dot;
+      for (int b = 0; b < kSlotBatch; ++b) {
+        float d = dot[b];
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
+        if (lane == 0 && k0 + b < K) dw[static_cast<long>(t) * K + k0 + b] = d;
+      }
     }
   }
 }
@@ -279,7 +309,7 @@ __global__ void bounded_wait_selftest_kernel(int32_t* status, uint64_t limit_ns)
 cudaError_t launch_permute(const uint16_t* x, const int32_t* pos, uint16_t* xs, const moe_dims& d,
                            cudaStream_t s) {
   if (d.T == 0) return cudaSuccess;
-  const int split = split_for_tokens(d.T, d.D / 8, 4);
+  const int split = split_for_tokens(d.T, d.D / 8, 4, static_cast<long>(sm_count()) * 64);
   auto kern = split > 1 ? permute_kernel<4, true> : permute_kernel<4, false>;
   kern<<<grid_for_rows(d.T, split), kThreads, 0, s>>>(
       reinterpret_cast<const uint4*>(x), pos, reinterpret_cast<uint4*>(xs), d.T, d.K, d.D / 8,
@@ -290,11 +320,21 @@ cudaError_t launch_permute(const uint16_t* x, const int32_t* pos, uint16_t* xs, 
 cudaError_t launch_combine(const uint16_t* ys, const float* w, const int32_t* pos, uint16_t* out,
                            const moe_dims& d, cudaStream_t s) {
   if (d.T == 0) return cudaSuccess;
-  const int split = split_for_tokens(d.T, d.D / 8, 2);
+  // measured on GB300: from 16384 tokens one warp per row with 4 vectors per
+  // lane (long sequence, 32768 tokens: 271 vs 284 us with 2); below, rows
+  // split until ~16384 warps run (8192 tokens: 57 vs 65 us unsplit; 1024
+  // tokens: 14 vs 28 us)
+  const auto* src = reinterpret_cast<const uint4*>(ys);
+  auto* dst = reinterpret_cast<uint4*>(out);
+  const int Dv = d.D / 8;
+  if (d.T >= 16384) {
+    combine_kernel<4, false><<<grid_for_rows(d.T, 1), kThreads, 0, s>>>(src, w, pos, dst, d.T,
+                                                                             d.K, Dv, 1);
+    return cudaGetLastError();
+  }
+  const int split = split_for_tokens(d.T, Dv, 2, 16384);
   auto kern = split > 1 ? combine_kernel<2, true> : combine_kernel<2, false>;
-  kern<<<grid_for_rows(d.T, split), kThreads, 0, s>>>(
-      reinterpret_cast<const uint4*>(ys), w, pos, reinterpret_cast<uint4*>(out), d.T, d.K, d.D / 8,
-      split);
+  kern<<<grid_for_rows(d.T, split), kThreads, 0, s>>>(src, w, pos, dst, d.T, d.K, Dv, split);
   return cudaGetLastError();
 }
 

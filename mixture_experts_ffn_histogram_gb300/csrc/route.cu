@@ -6,21 +6,26 @@
 // kernels and split-expert wi layout for TPU v6e", Commits table row 2: the
 // group_size histogram is computed before the token gather.
 //
-// Three kernels, all deterministic (no atomic decides an order; atomics only
-// add up counts):
-//   1. route_topk: one group of G lanes per token (32/G tokens per warp,
-//      grid-stride over all tokens) selects the top-K scores by K rounds of
-//      a group-wide (score desc, id asc) arg-max, computes the routing
-//      weights, and adds each slot to the count of its (chunk of 256
-//      tokens, expert) pair in global memory.
-//   2. route_scan: per expert, the exclusive prefix of the counts over
-//      chunks, group_sizes, and the exclusive prefix over experts
-//      (group_offsets); threads are indexed by expert so reads coalesce.
-//   3. route_rank: per chunk, each warp ranks its contiguous run of slots
-//      with __match_any_sync; pos = group_offsets[e] + chunk prefix + warp
-//      prefix + rank, i.e. the stable order in the flat slot index t*K+k.
+// One cooperative kernel (every block resident at once), three phases
+// separated by one grid-wide barrier; deterministic (no atomic decides an
+// order):
+//   1. Each warp owns a contiguous run of tokens.  For each of them a group
+//      of G lanes selects the top-K scores by K rounds of a group-wide
+//      (score desc, id asc) arg-max and computes the routing weights (or, for
+//      given routing, reads the ids).  Each slot's rank among the warp's
+//      earlier slots of the same expert (__match_any_sync over 32 slots at a
+//      time, plus the warp's running count per expert in shared memory) is
+//      stored in pos for now.  The block then turns the per-warp counts into
+//      prefixes over its warps and publishes its per-expert totals.
+//   2. After the barrier every block sums the published totals of the
+//      blocks before it (its prefix per expert) and of all blocks
+//      (group_sizes), and scans group_sizes over experts (group_offsets).
+//   3. pos = group_offsets[e] + block prefix + warp prefix + rank in warp,
+//      i.e. the stable order in the flat slot index t*K+k; row_src[pos] = j.
+// The kernel is the only launch: the grid barrier's word needs no clearing.
 #include <cuda.h>
 
+#include <atomic>
 #include <cfloat>
 #include <climits>
 #include <mutex>
@@ -31,251 +36,406 @@
 namespace moe {
 namespace {
 
-constexpr int kRouteThreads = 256;  // 8 warps
-constexpr int kRouteWarps = kRouteThreads / 32;
+constexpr int kRouteMaxWarps = 16;
 
-__device__ __forceinline__ bool better(float v1, int e1, float v2, int e2) {
-  return v1 > v2 || (v1 == v2 && e1 < e2);
+// A score and its expert id as one 64-bit key whose unsigned order is the
+// selection order (score descending, then id ascending): the score's bits
+// made monotone (sign flipped for positives, all bits for negatives; -0 is
+// first turned into +0 so that equal scores tie), and the id inverted in the
+// low half.  Key 0 lies below every real key and stands for "no expert".
+__device__ __forceinline__ uint64_t score_key(float v, int e) {
+  uint32_t u = __float_as_uint(v + 0.0f);
+  u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  return (static_cast<uint64_t>(u) << 32) | static_cast<uint32_t>(~static_cast<uint32_t>(e));
+}
+__device__ __forceinline__ float key_score(uint64_t k) {
+  const uint32_t u = static_cast<uint32_t>(k >> 32);
+  return __uint_as_float((u & 0x80000000u) ? (u & 0x7FFFFFFFu) : ~u);
+}
+__device__ __forceinline__ int key_expert(uint64_t k) {
+  return static_cast<int>(~static_cast<uint32_t>(k));
 }
 
-// One group of G lanes per token (G a power of two, G >= K, G * VPL >= E):
-// a warp selects the top-K of 32/G tokens at once.  Lane i of a group holds
-// the scores of experts i, i+G, i+2G, ...; each of the K rounds takes the
-// group-wide (score desc, id asc) arg-max over the experts not yet taken, so
-// slot k is the k-th largest score.
-template <int VPL>
-__global__ void __launch_bounds__(kRouteThreads) route_topk(
-    const float* __restrict__ logits, const float* __restrict__ bias, int mode,
-    int32_t* __restrict__ ids, float* __restrict__ w, int32_t* __restrict__ counts, int T, int E,
-    int K, int G, int32_t* status) {
-  const int lane = threadIdx.x & 31;
-  if (mode == MOE_SCORE_GIVEN) {
-    const long R = static_cast<long>(T) * K;
-    for (long j = static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x; j < R;
-         j += static_cast<long>(gridDim.x) * blockDim.x) {
-      const int e = ids[j];
-      const int chunk = static_cast<int>(j / K) / kRouteTokensPerChunk;
-      if (e >= 0 && e < E) atomicAdd(&counts[static_cast<long>(chunk) * E + e], 1);
-      else report(status, MOE_ERR_DEVICE);
-    }
-    return;
-  }
-  const int gl = lane & (G - 1);   // lane within the group
-  const int gbase = lane - gl;     // first lane of the group
-  const int groups_per_warp = 32 / G;
-  const long groups_total = static_cast<long>(gridDim.x) * kRouteWarps * groups_per_warp;
-  const long first = (static_cast<long>(blockIdx.x) * kRouteWarps + (threadIdx.x >> 5)) *
-                         groups_per_warp + (lane / G);
-  // every lane of a warp runs the same number of iterations (shuffles stay converged)
-  const long warp_first = first - lane / G;
-  for (long base = warp_first; base < T; base += groups_total) {
-    const long t = base + lane / G;
-    const bool live = t < T;
-    float s[VPL];
-    const float* row = logits + t * E;
-#pragma unroll
-    for (int i = 0; i < VPL; ++i) {
-      const int e = gl + G * i;
-      if (live && e < E) {
-        float v = __ldg(row + e);
-        if (bias != nullptr) v = __fadd_rn(v, __ldg(bias + e));
-        s[i] = v;
-      } else {
-        s[i] = -FLT_MAX;
+__device__ __forceinline__ unsigned int ld_acquire_gpu(const unsigned int* p) {
+  unsigned int v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ unsigned long long ld_acquire_gpu_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Grid-wide barrier of a cooperative launch on one 64-bit word: a tag
+// (high half) and an arrival count (low half).  Every launch leaves the word
+// at (tag, 0) for the next: the last block through clears the count.  A word
+// that does not carry the tag (memory never used for this, or other data) is
+// claimed by compare-and-swap, so it needs no clearing before the first use.
+// Every block then waits (bounded) until the count reaches the number of
+// blocks.  Returns false, after recording MOE_ERR_TIMEOUT, when a wait gave
+// up; the word is then left in an unknown state.
+constexpr uint32_t kBarrierTag = 0x5EC0DEu;
+
+__device__ __forceinline__ bool grid_barrier(unsigned long long* word, uint32_t nblocks,
+                                             int32_t* status, uint64_t limit_ns) {
+  __shared__ int ok_flag;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const unsigned long long tagged = static_cast<unsigned long long>(kBarrierTag) << 32;
+    bool ok = true;
+    unsigned long long cur = atomicAdd(word, 1ull);
+    if (static_cast<uint32_t>(cur >> 32) != kBarrierTag) {
+      // the add landed on an untagged word: count this block into a tagged one
+      ok = false;
+      cur += 1ull;
+      for (uint32_t it = 0; it < kMaxWaitIters; ++it) {
+        const unsigned long long want =
+            (static_cast<uint32_t>(cur >> 32) == kBarrierTag) ? cur + 1ull : tagged + 1ull;
+        const unsigned long long got = atomicCAS(word, cur, want);
+        if (got == cur) { ok = true; break; }
+        cur = got;
       }
     }
-    uint32_t taken = 0;
-    float my_v = 0.f;
-    int my_e = 0;
-    for (int k = 0; k < K; ++k) {
-      float bv = -FLT_MAX;
-      int be = INT_MAX;  // "no candidate" loses to every real expert
+    if (ok) {
+      ok = false;
+      const uint64_t start = global_timer_ns();
+      for (uint32_t it = 0; it < kMaxWaitIters; ++it) {
+        const unsigned long long v = ld_acquire_gpu_u64(word);
+        if (static_cast<uint32_t>(v >> 32) == kBarrierTag && static_cast<uint32_t>(v) >= nblocks) {
+          ok = true;
+          break;
+        }
+        if ((it & 63u) == 63u && global_timer_ns() - start > limit_ns) break;
+        __nanosleep(32);
+      }
+    }
+    if (ok) {
+      // leave: the last of the blocks to leave resets the count for the next
+      // launch (a replay of this one in a CUDA graph included)
+      const unsigned long long old = atomicAdd(word, 1ull);
+      if (static_cast<uint32_t>(old) + 1u == 2u * nblocks) atomicExch(word, tagged);
+    } else {
+      report(status, MOE_ERR_TIMEOUT);
+    }
+    __threadfence();
+    ok_flag = ok ? 1 : 0;
+  }
+  __syncthreads();
+  return ok_flag != 0;
+}
+
+// Rank of each lane's slot (expert e, or -1 for none) among the warp's slots
+// so far of the same expert: the lanes hold 32 consecutive slots in order,
+// `wc` the warp's running count per expert.
+__device__ __forceinline__ int warp_rank(int e, int32_t* wc, int lane) {
+  const uint32_t peers = __match_any_sync(0xffffffffu, e);
+  int before = 0;
+  if (e >= 0) before = wc[e];
+  __syncwarp();
+  if (e >= 0 && lane == __ffs(peers) - 1) wc[e] = before + __popc(peers);
+  __syncwarp();
+  return before + __popc(peers & ((1u << lane) - 1u));
+}
+
+// The routing kernel.  VPL: scores per lane (G lanes per token, G a power of
+// two with G >= K and G * VPL >= E); WARPS = blockDim.x / 32 warps per
+// block (at most kRouteMaxWarps).  Each warp owns `tpw` consecutive tokens.
+// Shared memory: per-warp counts [WARPS][E], then totals, block prefixes and
+// bases [E] each, then the per-run partial sums [max(32 * WARPS, E)] twice.
+// Global scratch: the barrier word and the blocks' totals [blocks][E].
+template <int VPL>
+__global__ void __launch_bounds__(kRouteMaxWarps * 32, 1) route_kernel(
+    const float* __restrict__ logits, const float* __restrict__ bias, int mode,
+    int32_t* __restrict__ ids, float* __restrict__ w, int32_t* __restrict__ group_sizes,
+    int32_t* __restrict__ group_offsets, int32_t* __restrict__ pos,
+    int32_t* __restrict__ row_src, unsigned long long* bar, int32_t* counts, int T, int E, int K,
+    int G, int tpw, int32_t* status, uint64_t limit_ns) {
+  const int NT = static_cast<int>(blockDim.x);
+  const int WARPS = NT >> 5;
+  extern __shared__ int32_t sm[];
+  int32_t* wcnt = sm;               // [WARPS][E]
+  int32_t* tot = sm + WARPS * E;    // [E]
+  int32_t* pre = tot + E;           // [E]
+  int32_t* basev = pre + E;         // [E]
+  int32_t* part_tot = basev + E;    // [max(NT, E)]
+  int32_t* part_pre = part_tot + (NT > E ? NT : E);
+  __shared__ int32_t wsum[32];
+  __shared__ int s_filled;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  for (int i = tid; i < WARPS * E; i += NT) wcnt[i] = 0;
+  __syncthreads();
+  int32_t* wc = wcnt + warp * E;
+  const long t0 = min(static_cast<long>(T), (static_cast<long>(blockIdx.x) * WARPS + warp) * tpw);
+  const long t1 = min(static_cast<long>(T), t0 + tpw);
+
+  // ---------------------------------------------------------------- phase 1
+  if (mode == MOE_SCORE_GIVEN) {
+    for (long jb = t0 * K; jb < t1 * K; jb += 32) {
+      const long j = jb + lane;
+      int e = -1;
+      if (j < t1 * K) {
+        e = ids[j];
+        if (e < 0 || e >= E) {
+          report(status, MOE_ERR_DEVICE);
+          pos[j] = -1;
+          e = -1;
+        }
+      }
+      const int r = warp_rank(e, wc, lane);
+      if (e >= 0) pos[j] = r;
+    }
+  } else {
+    const int gl = lane & (G - 1);  // lane within the token's group
+    const int gbase = lane - gl;    // first lane of the group
+    const int tpp = 32 / G;         // tokens per pass of the warp
+    for (long tb = t0; tb < t1; tb += tpp) {  // the same trip count in every lane
+      const long t = tb + lane / G;
+      const bool live = t < t1;
+      // all of the lane's scores are loaded before any is used: the compiler
+      // would otherwise sink each load into the selection chain below and
+      // pay one memory round trip per score (measured: ~10 us per pass at
+      // E = 128)
+      float sv[VPL], bv[VPL];
+      const float* row = logits + t * E;
 #pragma unroll
       for (int i = 0; i < VPL; ++i) {
         const int e = gl + G * i;
-        if (e < E && !((taken >> i) & 1u) && better(s[i], e, bv, be)) { bv = s[i]; be = e; }
+        const bool ok = live && e < E;
+        sv[i] = ok ? __ldg(row + e) : 0.f;
+        bv[i] = (ok && bias != nullptr) ? __ldg(bias + e) : 0.f;
       }
-      for (int off = G >> 1; off > 0; off >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-        const int oe = __shfl_xor_sync(0xffffffffu, be, off);
-        if (better(ov, oe, bv, be)) { bv = ov; be = oe; }
+      asm volatile("" ::: "memory");
+      uint64_t key[VPL];
+#pragma unroll
+      for (int i = 0; i < VPL; ++i) {
+        const int e = gl + G * i;
+        key[i] = (live && e < E)
+                     ? score_key(bias != nullptr ? __fadd_rn(sv[i], bv[i]) : sv[i], e)
+                     : 0ull;
       }
-      if (be != INT_MAX && (be & (G - 1)) == gl) taken |= 1u << (be / G);
-      if (gl == k) { my_v = bv; my_e = be; }
+      // round k takes the group's largest key below round k-1's: the k-th
+      // largest score (ties: lower id first); within a lane as a max tree
+      // (a short dependency chain), then across the group's lanes
+      uint64_t last = ~0ull, mine = 0;
+      for (int k = 0; k < K; ++k) {
+        uint64_t c[VPL];
+#pragma unroll
+        for (int i = 0; i < VPL; ++i) c[i] = key[i] < last ? key[i] : 0ull;
+#pragma unroll
+        for (int w = VPL / 2; w > 0; w >>= 1)
+#pragma unroll
+          for (int i = 0; i < w; ++i) c[i] = c[i + w] > c[i] ? c[i + w] : c[i];
+        uint64_t best = c[0];
+        for (int off = G >> 1; off > 0; off >>= 1) {
+          const uint64_t o = __shfl_xor_sync(0xffffffffu, best, off);
+          best = o > best ? o : best;
+        }
+        last = best;
+        if (gl == k) mine = best;
+      }
+      const float my_v = key_score(mine);
+      const int my_e = key_expert(mine);
+      // routing weights of the K selected scores (group lane k holds slot k)
+      float ex = 0.f;
+      if (mode == MOE_SCORE_SOFTMAX_TOPK) {
+        const float m = __shfl_sync(0xffffffffu, my_v, gbase);
+        if (gl < K) ex = expf(my_v - m);
+      } else {
+        if (gl < K) ex = 1.0f / (1.0f + expf(-my_v));
+      }
+      float sum = 0.f;  // ascending slot order
+      for (int k = 0; k < K; ++k) sum = __fadd_rn(sum, __shfl_sync(0xffffffffu, ex, gbase + k));
+      int e = -1;
+      if (live && gl < K) {
+        const long j = t * K + gl;
+        ids[j] = my_e;
+        w[j] = __fdiv_rn(ex, sum);
+        e = my_e;
+      }
+      // the lanes hold the pass's slots in flat order (token, then slot)
+      const int r = warp_rank(e, wc, lane);
+      if (e >= 0) pos[t * K + gl] = r;
     }
-    // routing weights of the K selected scores (group lane k holds slot k)
-    float ex = 0.f;
-    if (mode == MOE_SCORE_SOFTMAX_TOPK) {
-      const float m = __shfl_sync(0xffffffffu, my_v, gbase);
-      if (gl < K) ex = expf(my_v - m);
-    } else {
-      if (gl < K) ex = 1.0f / (1.0f + expf(-my_v));
-    }
-    float sum = 0.f;  // ascending slot order
-    for (int k = 0; k < K; ++k) sum = __fadd_rn(sum, __shfl_sync(0xffffffffu, ex, gbase + k));
-    if (live && gl < K) {
-      const long j = t * K + gl;
-      ids[j] = my_e;
-      w[j] = __fdiv_rn(ex, sum);
-      atomicAdd(&counts[(t / kRouteTokensPerChunk) * E + my_e], 1);
-    }
-  }
-}
-
-// One block of 1024 threads.  Thread (g, e) = (tid / E, tid % E) covers
-// expert e over chunk group g (a contiguous run of chunks), so that each
-// load of counts[c, 0..E) is coalesced across the threads of a group.
-__global__ void __launch_bounds__(1024) route_scan(const int32_t* __restrict__ counts,
-                                                   int32_t* __restrict__ chunk_excl, int nchunks,
-                                                   int E, int32_t* __restrict__ group_sizes,
-                                                   int32_t* __restrict__ group_offsets) {
-  __shared__ int32_t part[1024];
-  __shared__ int32_t tot[1024];
-  __shared__ int32_t warp_sum[32];
-  const int tid = threadIdx.x;
-  const int lane = tid & 31;
-  const int warp = tid >> 5;
-  const int G = max(1, 1024 / E);
-  const int e = tid % E, g = tid / E;
-  const bool active = g < G;
-  const int cpg = (nchunks + G - 1) / G;
-  const int c0 = min(nchunks, g * cpg), c1 = min(nchunks, c0 + cpg);
-  if (active) {
-    int local = 0;
-#pragma unroll 4
-    for (int c = c0; c < c1; ++c) local += counts[static_cast<long>(c) * E + e];
-    part[g * E + e] = local;
   }
   __syncthreads();
-  if (tid < E) {
+  // per-warp counts -> exclusive prefixes over the block's warps; totals out
+  for (int e = tid; e < E; e += NT) {
     int run = 0;
-    for (int q = 0; q < G; ++q) {
-      const int v = part[q * E + tid];
-      part[q * E + tid] = run;
+    for (int q = 0; q < WARPS; ++q) {
+      const int v = wcnt[q * E + e];
+      wcnt[q * E + e] = run;
       run += v;
     }
-    tot[tid] = run;
-    group_sizes[tid] = run;
+    counts[static_cast<long>(blockIdx.x) * E + e] = run;
+  }
+  const int nb = static_cast<int>(gridDim.x);
+  if (!grid_barrier(bar, static_cast<uint32_t>(nb), status, limit_ns)) return;
+
+  // ---------------------------------------------------------------- phase 2
+  // The blocks' totals per expert summed before this block (its prefix) and
+  // over all blocks (group_sizes).  Thread (g, e) sums expert e over the g-th
+  // of S runs of blocks, threads indexed by expert so that loads coalesce and
+  // with several independent loads in flight; the runs' sums then meet in
+  // shared memory.
+  {
+    const int S = max(1, NT / E);
+    const int self = static_cast<int>(blockIdx.x);
+    const int per_run = (nb + S - 1) / S;
+    for (int i = tid; i < S * E; i += NT) {
+      const int g = i / E, e = i - g * E;
+      const int q0 = min(nb, g * per_run), q1 = min(nb, q0 + per_run);
+      int p = 0, sum = 0;
+#pragma unroll 8
+      for (int q = q0; q < q1; ++q) {
+        const int v = __ldcg(counts + static_cast<long>(q) * E + e);
+        sum += v;
+        p += (q < self) ? v : 0;
+      }
+      part_tot[i] = sum;
+      part_pre[i] = p;
+    }
+    __syncthreads();
+    for (int e = tid; e < E; e += NT) {
+      int p = 0, sum = 0;
+      for (int g = 0; g < S; ++g) {
+        sum += part_tot[g * E + e];
+        p += part_pre[g * E + e];
+      }
+      tot[e] = sum;
+      pre[e] = p;
+    }
   }
   __syncthreads();
-  // exclusive scan of tot[0..E) over the block
-  const int v = (tid < E) ? tot[tid] : 0;
-  int incl = v;
+  // exclusive scan of tot over the experts: thread i holds `per` consecutive ones
+  const int per = (E + NT - 1) / NT;
+  const int e0 = min(E, tid * per), e1 = min(E, e0 + per);
+  int local = 0;
+  for (int e = e0; e < e1; ++e) local += tot[e];
+  int incl = local;
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
     const int u = __shfl_up_sync(0xffffffffu, incl, off);
     if (lane >= off) incl += u;
   }
-  if (lane == 31) warp_sum[warp] = incl;
+  if (lane == 31) wsum[warp] = incl;
   __syncthreads();
   if (warp == 0) {
-    const int ws = warp_sum[lane];
-    int wi = ws;
+    const int v = lane < WARPS ? wsum[lane] : 0;
+    int x = v;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
-      const int u = __shfl_up_sync(0xffffffffu, wi, off);
-      if (lane >= off) wi += u;
+      const int u = __shfl_up_sync(0xffffffffu, x, off);
+      if (lane >= off) x += u;
     }
-    warp_sum[lane] = wi - ws;
+    if (lane < WARPS) wsum[lane] = x - v;
   }
   __syncthreads();
-  const int excl = warp_sum[warp] + incl - v;
-  if (tid < E) group_offsets[tid] = excl;
-  if (tid == E - 1) group_offsets[E] = excl + v;
-  if (active) {
-    int run = part[g * E + e];
-#pragma unroll 4
-    for (int c = c0; c < c1; ++c) {
-      const long idx = static_cast<long>(c) * E + e;
-      const int cv = counts[idx];
-      chunk_excl[idx] = run;
-      run += cv;
+  int run = wsum[warp] + incl - local;
+  for (int e = e0; e < e1; ++e) {
+    basev[e] = run + pre[e];
+    if (blockIdx.x == 0) {
+      group_sizes[e] = tot[e];
+      group_offsets[e] = run;
     }
+    run += tot[e];
   }
-}
-
-// One block per chunk; warp w ranks slots [j0 + w*32K, j0 + (w+1)*32K).
-__global__ void __launch_bounds__(kRouteThreads) route_rank(
-    const int32_t* __restrict__ ids, const int32_t* __restrict__ chunk_excl,
-    const int32_t* __restrict__ group_offsets, int32_t* __restrict__ pos,
-    int32_t* __restrict__ row_src, int T, int K, int E) {
-  extern __shared__ int32_t sm[];
-  int32_t* wrun = sm;                      // [kRouteWarps][E]
-  int32_t* base = sm + kRouteWarps * E;    // [E]
-  const int lane = threadIdx.x & 31;
-  const int warp = threadIdx.x >> 5;
-  const long R = static_cast<long>(T) * K;
-  // rows that no valid slot fills (only when some id was out of range)
-  const long filled = group_offsets[E];
-  for (long r = filled + static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x; r < R;
-       r += static_cast<long>(gridDim.x) * blockDim.x)
-    row_src[r] = -1;
-
-  for (int i = threadIdx.x; i < kRouteWarps * E; i += blockDim.x) wrun[i] = 0;
+  if (e0 < e1 && e1 == E) {
+    s_filled = run;
+    if (blockIdx.x == 0) group_offsets[E] = run;
+  }
   __syncthreads();
-  const long chunk_j0 = static_cast<long>(blockIdx.x) * kRouteTokensPerChunk * K;
-  const long per_warp = 32L * K;
-  const long j0 = chunk_j0 + warp * per_warp;
-  const long j1 = min(R, j0 + per_warp);
-  for (long j = j0 + lane; j < j1; j += 32) {
+
+  // ---------------------------------------------------------------- phase 3
+  for (long j = t0 * K + lane; j < t1 * K; j += 32) {
     const int e = ids[j];
-    if (e >= 0 && e < E) atomicAdd(&wrun[warp * E + e], 1);
+    if (e < 0 || e >= E) continue;  // dropped slot: pos is already -1
+    const int p = basev[e] + wc[e] + pos[j];
+    pos[j] = p;
+    row_src[p] = static_cast<int32_t>(j);
   }
-  __syncthreads();
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    int run = 0;
-    for (int w = 0; w < kRouteWarps; ++w) {
-      const int v = wrun[w * E + e];
-      wrun[w * E + e] = run;
-      run += v;
-    }
-    base[e] = group_offsets[e] + chunk_excl[static_cast<long>(blockIdx.x) * E + e];
-  }
-  __syncthreads();
-  const uint32_t lt_mask = (1u << lane) - 1u;
-  for (long jb = j0; jb < j1; jb += 32) {
-    const long j = jb + lane;
-    int e = (j < j1) ? ids[j] : -1;
-    const bool valid = (e >= 0 && e < E);
-    if (!valid) e = -1;
-    const uint32_t peers = __match_any_sync(0xffffffffu, e);
-    int before = 0;
-    if (valid) before = wrun[warp * E + e];
-    __syncwarp();
-    if (valid) {
-      const int rank = __popc(peers & lt_mask);
-      const int p = base[e] + before + rank;
-      if (lane == __ffs(peers) - 1) wrun[warp * E + e] = before + __popc(peers);
-      pos[j] = p;
-      row_src[p] = static_cast<int32_t>(j);
-    } else if (j < j1) {
-      pos[j] = -1;
-    }
-    __syncwarp();
-  }
+  // rows that no valid slot fills (only when some id was out of range)
+  const long R = static_cast<long>(T) * K;
+  for (long r = s_filled + static_cast<long>(blockIdx.x) * NT + tid; r < R;
+       r += static_cast<long>(gridDim.x) * NT)
+    row_src[r] = -1;
 }
 
+size_t route_smem_bytes(int warps, int E) {
+  const size_t part = static_cast<size_t>(32 * warps > E ? 32 * warps : E);
+  return (static_cast<size_t>(warps + 3) * static_cast<size_t>(E) + 2 * part) * sizeof(int32_t);
+}
+
+// A block's warps each own a run of tokens; with few tokens it is the
+// latency of one pass of the top-K that counts, so blocks start at 8 warps
+// (2 per scheduler) to spread the passes over the SMs, and grow to
+// kRouteMaxWarps warps when there are more passes than that covers.  Blocks
+// stay at 8 warps or more because after the barrier each block reads every
+// block's totals, (blocks * E) / (threads per block) loads per thread.
 template <int VPL>
-cudaError_t launch_topk(const float* logits, const float* bias, int mode, int32_t* ids, float* w,
-                        int32_t* counts, const moe_dims& d, int G, int32_t* status,
-                        cudaStream_t s) {
-  long blocks;
-  if (mode == MOE_SCORE_GIVEN) {
-    blocks = (static_cast<long>(d.T) * d.K + kRouteThreads - 1) / kRouteThreads;
-  } else {
-    const long tokens_per_block = static_cast<long>(kRouteWarps) * (32 / G);
-    blocks = (d.T + tokens_per_block - 1) / tokens_per_block;
+cudaError_t launch_route(const float* logits, const float* bias, int mode, int32_t* ids, float* w,
+                         int32_t* group_sizes, int32_t* group_offsets, int32_t* pos,
+                         int32_t* row_src, int32_t* dev_status, unsigned long long* bar,
+                         int32_t* counts, long max_blocks, const moe_dims& d, int G,
+                         cudaStream_t s) {
+  auto kern = route_kernel<VPL>;
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  // the shared-memory opt-in (for the largest block and E) once per device,
+  // and the blocks of that size one SM holds (a bound for smaller ones)
+  static std::atomic<int> per_sm[64];
+  int bps = per_sm[dev].load(std::memory_order_acquire);
+  if (bps == 0) {
+    const size_t smax = route_smem_bytes(kRouteMaxWarps, 1024);
+    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(smax));
+    if (err != cudaSuccess) return err;
+    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bps, kern, kRouteMaxWarps * 32, smax);
+    if (err != cudaSuccess) return err;
+    if (bps < 1) return cudaErrorInvalidConfiguration;
+    per_sm[dev].store(bps, std::memory_order_release);
   }
-  const long cap = static_cast<long>(sm_count()) * 8;
-  if (blocks > cap) blocks = cap;
-  route_topk<VPL><<<static_cast<int>(blocks), kRouteThreads, 0, s>>>(
-      logits, bias, mode, ids, w, counts, d.T, d.E, d.K, G, status);
-  return cudaGetLastError();
+  const int sms = sm_count();
+  const int tpp = 32 / G;  // tokens per warp pass
+  const long passes = (d.T + tpp - 1) / tpp;
+  int warps = 8;
+  while (warps < kRouteMaxWarps && (passes + warps - 1) / warps > sms) warps <<= 1;
+  // at most one block per SM: every block reads every block's totals after
+  // the barrier, so the grid is kept about as wide as the machine, not wider
+  long blocks = (passes + warps - 1) / warps;
+  long resident = static_cast<long>(bps) * sms;
+  if (resident > sms) resident = sms;
+  if (blocks > resident) blocks = resident;
+  if (blocks > max_blocks) blocks = max_blocks;
+  if (blocks < 1) blocks = 1;
+  // tokens per warp: a whole number of passes, the fewest that cover T
+  long tpw = (d.T + blocks * warps - 1) / (blocks * warps);
+  tpw = (tpw + tpp - 1) / tpp * tpp;
+  blocks = (d.T + static_cast<long>(warps) * tpw - 1) / (static_cast<long>(warps) * tpw);
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.gridDim = dim3(static_cast<unsigned>(blocks), 1, 1);
+  cfg.blockDim = dim3(static_cast<unsigned>(warps * 32), 1, 1);
+  cfg.dynamicSmemBytes = route_smem_bytes(warps, d.E);
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, logits, bias, mode, ids, w, group_sizes, group_offsets,
+                            pos, row_src, bar, counts, d.T, d.E, d.K, G,
+                            static_cast<int>(tpw),
+                            dev_status, kDefaultWaitLimitNs);
 }
 
-// Scratch of moe_route_histogram_noalloc: the per-chunk expert counts and
-// their prefixes live in this fixed array instead of a caller workspace.
-// Every GPU that loads the library holds it (1 MiB) until the process exits.
+// Scratch of moe_route_histogram_noalloc: the barrier counter (first 256
+// bytes) and the per-block expert totals live in this fixed array instead
+// of a caller workspace.  Every GPU that loads the library holds it (1 MiB)
+// until the process exits.
 static __device__ __align__(256) int32_t g_route_scratch[kRouteStaticScratchInts];
 
 }  // namespace
@@ -283,33 +443,30 @@ static __device__ __align__(256) int32_t g_route_scratch[kRouteStaticScratchInts
 cudaError_t launch_route_histogram(const float* logits, const float* bias, int mode, int32_t* ids,
                                    float* w, int32_t* group_sizes, int32_t* group_offsets,
                                    int32_t* pos, int32_t* row_src, int32_t* dev_status,
-                                   int32_t* counts, int32_t* chunk_excl, const moe_dims& d,
+                                   void* scratch, long max_blocks, const moe_dims& d,
                                    cudaStream_t s) {
-  const int nchunks = route_chunks(d.T);
-  cudaError_t err = cudaSuccess;
-  if (nchunks > 0) {
-    err = cudaMemsetAsync(counts, 0, static_cast<size_t>(nchunks) * d.E * sizeof(int32_t), s);
+  if (d.T == 0) {
+    cudaError_t err = cudaMemsetAsync(group_sizes, 0, static_cast<size_t>(d.E) * 4, s);
     if (err != cudaSuccess) return err;
-    // G lanes per token: a power of two with G >= K and G * VPL >= E, VPL <= 32
-    int G = 1;
-    while (G < d.K) G <<= 1;
-    while (G * 32 < d.E) G <<= 1;
-    int vpl = (d.E + G - 1) / G;
-    if (vpl <= 4) err = launch_topk<4>(logits, bias, mode, ids, w, counts, d, G, dev_status, s);
-    else if (vpl <= 8) err = launch_topk<8>(logits, bias, mode, ids, w, counts, d, G, dev_status, s);
-    else if (vpl <= 16) err = launch_topk<16>(logits, bias, mode, ids, w, counts, d, G, dev_status, s);
-    else err = launch_topk<32>(logits, bias, mode, ids, w, counts, d, G, dev_status, s);
-    if (err != cudaSuccess) return err;
+    return cudaMemsetAsync(group_offsets, 0, static_cast<size_t>(d.E + 1) * 4, s);
   }
-  route_scan<<<1, 1024, 0, s>>>(counts, chunk_excl, nchunks, d.E, group_sizes, group_offsets);
-  if ((err = cudaGetLastError()) != cudaSuccess) return err;
-  if (nchunks > 0) {
-    const size_t smem = static_cast<size_t>(kRouteWarps + 1) * d.E * sizeof(int32_t);
-    route_rank<<<nchunks, kRouteThreads, smem, s>>>(ids, chunk_excl, group_offsets, pos, row_src,
-                                                    d.T, d.K, d.E);
-    err = cudaGetLastError();
-  }
-  return err;
+  // the barrier word at byte 64: the GEMMs keep their tile counter at byte 0
+  // of the same workspace
+  auto* bar = reinterpret_cast<unsigned long long*>(static_cast<uint8_t*>(scratch) + 64);
+  int32_t* counts = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(scratch) + kRouteBarrierBytes);
+  // G lanes per token: a power of two with G >= K and G * VPL >= E, VPL <= 32
+  int G = 1;
+  while (G < d.K) G <<= 1;
+  while (G * 32 < d.E) G <<= 1;
+  const int vpl = (d.E + G - 1) / G;
+#define MOE_ROUTE(V)                                                                     \
+  launch_route<V>(logits, bias, mode, ids, w, group_sizes, group_offsets, pos, row_src, \
+                  dev_status, bar, counts, max_blocks, d, G, s)
+  if (vpl <= 4) return MOE_ROUTE(4);
+  if (vpl <= 8) return MOE_ROUTE(8);
+  if (vpl <= 16) return MOE_ROUTE(16);
+  return MOE_ROUTE(32);
+#undef MOE_ROUTE
 }
 
 // Unique id of the calling thread's current CUDA context (never reused
@@ -371,12 +528,14 @@ cudaError_t launch_route_histogram_static(const float* logits, const float* bias
     }
     ptr = c.ptr;
   }
-  const size_t per = static_cast<size_t>(route_chunks(d.T)) * static_cast<size_t>(d.E);
-  if (2 * per > kRouteStaticScratchInts) return cudaErrorInvalidValue;
-  // launch_route_histogram clears the counts it uses before counting, and
-  // rewrites every prefix it reads, so nothing left by an earlier call leaks.
+  // the barrier word, then the totals of at most max_blocks blocks
+  const long max_blocks =
+      static_cast<long>((kRouteStaticScratchInts - kRouteBarrierBytes / sizeof(int32_t)) /
+                        static_cast<size_t>(d.E));
+  // the kernel writes every total it reads, and every launch leaves the
+  // barrier word ready for the next, so nothing left by an earlier call leaks
   return launch_route_histogram(logits, bias, mode, ids, w, group_sizes, group_offsets, pos,
-                                row_src, dev_status, ptr, ptr + per, d, s);
+                                row_src, dev_status, ptr, max_blocks, d, s);
 }
 
 }  // namespace moe
