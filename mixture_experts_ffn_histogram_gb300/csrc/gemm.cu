@@ -73,7 +73,7 @@ struct SmemCtl {
   uint64_t empty[kMaxStages];
   uint64_t tfull[2];
   uint64_t tempty[2];
-  uint64_t zbar[kEpiWarps];  // z rows landed in an epilogue warp's buffers
+  uint64_t zbar[kEpiWarps][2];  // z rows landed in a slot of an epilogue warp
   uint64_t sfull[kSched];    // a tile index was written to the slot
   uint64_t sempty[kSched];   // every role has read the slot
   int sched[kSched];
@@ -86,9 +86,9 @@ struct SmemCtl {
 };
 
 // Tile shape: 128 x BN accumulator per CTA, CG CTAs per MMA, a `STAGES`-deep
-// operand ring, RING staging buffers per epilogue warp, and (ZB) two more
-// buffers per epilogue warp into which TMA loads the z rows that the fused
-// SwiGLU backward reads.
+// operand ring, RING staging buffers per epilogue warp, and (ZB > 0) ZB slots
+// per epilogue warp into which TMA loads the z rows that the fused SwiGLU
+// backward reads and from which it stores dz (no staging ring needed then).
 //
 // NACC = 2 makes a tile two accumulators wide (2*BN columns per CTA, all 512
 // TMEM columns): each A stage feeds two MMAs, so each SM loads 25% fewer bytes
@@ -100,8 +100,9 @@ struct Shape {
   static constexpr int CG = CG_;
   static constexpr int kRing = RING_;
   static constexpr bool kZB = ZB_ != 0;
+  static constexpr int kZSlots = ZB_;
   static constexpr int kNacc = NACC_;
-  static constexpr int kZBytes = kZB ? kEpiWarps * 2 * kBufBytes : 0;
+  static constexpr int kZBytes = kEpiWarps * ZB_ * 2 * kBufBytes;
   static constexpr int kBRows = BN / CG;  // B columns held by one CTA, per accumulator
   static constexpr int kBStageBytes = NACC_ * kBRows * BK * 2;
   static constexpr int kStageBytes = kAStageBytes + kBStageBytes;
@@ -115,7 +116,8 @@ struct Shape {
   static_assert(BN == 256, "tile width");
   static_assert(CG == 1 || CG == 2, "CTA group");
   static_assert(STAGES_ >= 2 && STAGES_ <= kMaxStages, "stages");
-  static_assert(RING_ >= 1 && RING_ <= 4, "staging ring");
+  static_assert(RING_ >= (ZB_ ? 0 : 1) && RING_ <= 4, "staging ring");
+  static_assert(ZB_ == 0 || ZB_ == 2, "z slots");
   static_assert(kSmemBytes <= kSmemLimit, "shared memory");
 };
 
@@ -508,6 +510,22 @@ __device__ __forceinline__ void flush_3d(uint8_t* buf, const CUtensorMap* map, i
   }
 }
 
+// z rows of the fused SwiGLU backward, by TMA: two slots per epilogue warp,
+// each the gate and up rows (32 x 64 bf16 each) of one 64-column chunk.  The
+// backward of a chunk is written over the z it read, and stored from there.
+// Requests run up to two chunks ahead, into the next tile of the warp's
+// (static) schedule: that tile's first chunks then arrive while its
+// accumulator is still being computed, instead of one DRAM round trip per
+// chunk in the epilogue.
+struct ZPipe {
+  uint8_t* buf;    // this warp's two slots
+  uint64_t* bar;   // their barriers
+  uint32_t ph;     // phase bit of each slot
+  int send, recv;  // slot of the next request, of the next chunk to consume
+  int out;         // requests not yet consumed
+  int qt, qch;     // next chunk to request: tile index and chunk
+};
+
 template <int RING>
 struct EpiCtx {
   const CUtensorMap* map_c;  // out0
@@ -515,34 +533,111 @@ struct EpiCtx {
   Ring<RING> ring;
   int q;                     // lane quarter: rows [32q, 32q+32) of this CTA's tile
   int lane;
-  uint8_t* zbuf;             // gate and up z rows of one 64-column chunk (TMA-loaded)
-  uint64_t* zbar;
-  uint32_t zphase;
+  ZPipe zp;
   const WaitCtl* wc;
 };
 
 // Whether this warp's z rows come by TMA: the fused SwiGLU backward, a shape
-// with z buffers, and all 32 of the warp's rows inside the group.
+// with z slots, and all 32 of the warp's rows inside the group.
 template <int KIND, bool ZB, int RING>
 __device__ __forceinline__ bool z_by_tma(const Tile& T, const EpiCtx<RING>& c, const Params& p) {
   return KIND == static_cast<int>(GemmKind::kDlhsFc2) && ZB && p.aux != nullptr &&
          T.rows - 32 * c.q >= 32;
 }
-// Request the gate and up z rows of 64-column chunk `ch` of tile T.
+// 64-column chunks of tile T that hold output columns (FC2 dlhs: N = F).
+__device__ __forceinline__ int z_chunks(const Tile& T, int BN, const Params& p) {
+  return max(0, min(BN, p.F - T.n0) + 63) / 64;
+}
+// Request the gate and up z rows of chunk `ch` of tile T into the next slot,
+// once the store that last read that slot has read it.
 template <int RING>
-__device__ __forceinline__ void z_request(const Tile& T, int ch, EpiCtx<RING>& c, const Params& p) {
+__device__ __forceinline__ void z_issue(const Tile& T, int ch, EpiCtx<RING>& c) {
+  ZPipe& z = c.zp;
   if (c.lane == 0) {
-    const int f0 = T.n0 + 64 * ch;
-    const int y = T.row0 + 32 * c.q;
-    const uint32_t bar = smem_u32(c.zbar);
-    mbar_arrive_expect_tx(c.zbar, 2 * kBufBytes);
-    tma_load_3d_addr(c.zbuf, c.map_d, bar, f0, y, 0);  // gate chunk, then up chunk
+    bulk_wait_read<0>();
+    uint64_t* b = z.bar + z.send;
+    mbar_arrive_expect_tx(b, 2 * kBufBytes);
+    tma_load_3d_addr(z.buf + z.send * 2 * kBufBytes, c.map_d, smem_u32(b), T.n0 + 64 * ch,
+                     T.row0 + 32 * c.q, 0);  // gate chunk, then up chunk
+  }
+  __syncwarp();
+  z.send ^= 1;
+  ++z.out;
+}
+// Keep two requests in flight: the rest of tile t's chunks, then (when it
+// also takes its z by TMA) the first chunks of the warp's next tile tn.
+template <int KIND, int BN, bool ZB, int RING>
+__device__ __forceinline__ void z_fill(int t, const Tile& T, int tn, const Tile& Tn,
+                                       EpiCtx<RING>& c, const Params& p) {
+  ZPipe& z = c.zp;
+  while (z.out < 2) {
+    if (z.qt == t && z.qch < z_chunks(T, BN, p)) {
+      z_issue(T, z.qch++, c);
+    } else if (z.qt == t && tn >= 0 && z_by_tma<KIND, ZB, RING>(Tn, c, p)) {
+      z.qt = tn;
+      z.qch = 0;
+    } else if (z.qt == tn && tn >= 0 && z.qch < z_chunks(Tn, BN, p)) {
+      z_issue(Tn, z.qch++, c);
+    } else {
+      break;
+    }
+  }
+}
+// Wait for the oldest request; returns its slot, or -1 when the wait gave up.
+template <int RING>
+__device__ __forceinline__ int z_take(EpiCtx<RING>& c) {
+  ZPipe& z = c.zp;
+  const int slot = z.recv;
+  if (!mbar_wait(z.bar + slot, (z.ph >> slot) & 1u, *c.wc)) return -1;
+  z.ph ^= 1u << slot;
+  z.recv ^= 1;
+  --z.out;
+  return slot;
+}
+// Requests still in flight land before the CTA exits (bounded).
+template <int RING>
+__device__ __forceinline__ void z_drain(EpiCtx<RING>& c) {
+  ZPipe& z = c.zp;
+  while (z.out > 0) {
+    (void)mbar_wait_drain(z.bar + z.recv, (z.ph >> z.recv) & 1u, 100000000ull);
+    z.ph ^= 1u << z.recv;
+    z.recv ^= 1;
+    --z.out;
   }
 }
 
+// dgate, dup of 32 columns of one row (packed bf16 pairs), from the fp32 dh
+// in v and the bf16 gate and up z of the same columns (4 x uint4 each).
+__device__ __forceinline__ void swiglu_bwd32(const uint32_t (&v)[32], const uint4* zg,
+                                             const uint4* zu, uint32_t (&wg)[16],
+                                             uint32_t (&wu)[16]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t gq[4] = {zg[i].x, zg[i].y, zg[i].z, zg[i].w};
+    const uint32_t uq[4] = {zu[i].x, zu[i].y, zu[i].z, zu[i].w};
+#pragma unroll
+    for (int qq = 0; qq < 4; ++qq) {
+      float rg[2], ru[2];
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const float dh = __uint_as_float(v[8 * i + 2 * qq + hh]);
+        const float g = hh ? bf16hi(gq[qq]) : bf16lo(gq[qq]);
+        const float u = hh ? bf16hi(uq[qq]) : bf16lo(uq[qq]);
+        const float sg = sigmoid_fast(g);
+        rg[hh] = dh * u * sg * (1.0f + g * (1.0f - sg));
+        ru[hh] = dh * g * sg;
+      }
+      wg[4 * i + qq] = pack_bf16x2(rg[0], rg[1]);
+      wu[4 * i + qq] = pack_bf16x2(ru[0], ru[1]);
+    }
+  }
+}
+
+// t, tn, Tn: the tile's index and the warp's next tile (index, or -1), for
+// the z requests of the fused SwiGLU backward.
 template <int KIND, int BN, int CG, int RING, bool ZB>
 __device__ __forceinline__ void epilogue_tile(const Tile& T, uint32_t tbase, EpiCtx<RING>& c,
-                                              const Params& p) {
+                                              const Params& p, int t, int tn, const Tile& Tn) {
   const int lane = c.lane;
   uint32_t v[32];
   uint32_t w[16];
@@ -616,60 +711,68 @@ __device__ __forceinline__ void epilogue_tile(const Tile& T, uint32_t tbase, Epi
           if (with_z) flush_3d(c.ring.after(hb, 1), c.map_d, f0, y, 0, lane);  // zg, zu
         }
       }
-    } else if constexpr (KIND == static_cast<int>(GemmKind::kDlhsFc2)) {
-      const bool fused = p.aux != nullptr;
-      if (z_by_tma<KIND, ZB, RING>(T, c, p)) {
-        // z rows arrive by TMA; chunk 0 was requested before the accumulator wait
+    } else if constexpr (KIND == static_cast<int>(GemmKind::kDlhsFc2) && ZB) {
+      // fused SwiGLU backward on a shape with z slots (these run nothing else)
+      if (full) {
         for (int ch = 0; ch < BN / 64; ++ch) {
           const int f0 = T.n0 + 64 * ch;
           if (f0 >= p.F) break;
-          if (!mbar_wait(c.zbar, c.zphase, *c.wc)) return;
-          c.zphase ^= 1u;
+          const int slot = z_take(c);
+          if (slot < 0) return;
+          uint8_t* gbuf = c.zp.buf + slot * 2 * kBufBytes;
+          uint8_t* ubuf = gbuf + kBufBytes;
           uint4 zg[8], zu[8];
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
             const int off = lane * 128 + ((j ^ (lane & 7)) << 4);
-            zg[j] = *reinterpret_cast<const uint4*>(c.zbuf + off);
-            zu[j] = *reinterpret_cast<const uint4*>(c.zbuf + kBufBytes + off);
+            zg[j] = *reinterpret_cast<const uint4*>(gbuf + off);
+            zu[j] = *reinterpret_cast<const uint4*>(ubuf + off);
           }
-          fence_proxy_async_smem();  // the reads are done before TMA refills the buffers
-          __syncwarp();
-          if (ch + 1 < BN / 64 && f0 + 64 < p.F) z_request(T, ch + 1, c, p);
-          uint8_t* gb = c.ring.template take<2>(lane);
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             tmem_ld_32x32b_x32(tbase + 64 * ch + 32 * h, v);
             tmem_ld_wait();
             uint32_t wg[16], wu[16];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const uint4 gv = zg[4 * h + i], uv = zu[4 * h + i];
-              const uint32_t gq[4] = {gv.x, gv.y, gv.z, gv.w};
-              const uint32_t uq[4] = {uv.x, uv.y, uv.z, uv.w};
-#pragma unroll
-              for (int qq = 0; qq < 4; ++qq) {
-                float rg[2], ru[2];
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                  const float dh = __uint_as_float(v[8 * i + 2 * qq + hh]);
-                  const float g = hh ? bf16hi(gq[qq]) : bf16lo(gq[qq]);
-                  const float u = hh ? bf16hi(uq[qq]) : bf16lo(uq[qq]);
-                  const float sg = sigmoid_fast(g);
-                  rg[hh] = dh * u * sg * (1.0f + g * (1.0f - sg));
-                  ru[hh] = dh * g * sg;
-                }
-                wg[4 * i + qq] = pack_bf16x2(rg[0], rg[1]);
-                wu[4 * i + qq] = pack_bf16x2(ru[0], ru[1]);
-              }
-            }
-            put_half(gb, lane, h, wg);
-            put_half(c.ring.after(gb, 1), lane, h, wu);
+            swiglu_bwd32(v, zg + 4 * h, zu + 4 * h, wg, wu);
+            // each lane overwrites its own row of the z it has read
+            put_half(gbuf, lane, h, wg);
+            put_half(ubuf, lane, h, wu);
           }
           publish();
-          flush_3d(gb, c.map_c, f0, y, 0, lane);  // dgate, dup
+          flush_3d(gbuf, c.map_c, f0, y, 0, lane);  // dgate, dup
+          z_fill<KIND, BN, ZB, RING>(t, T, tn, Tn, c, p);
         }
         return;
       }
+      // a warp with rows past the group's end: z and dz per thread
+      for (int ch = 0; ch < BN / 64; ++ch) {
+        const int f0 = T.n0 + 64 * ch;
+        if (f0 >= p.F) break;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int fc = f0 + 32 * h;
+          uint4 zg[4], zu[4];
+          if (row_ok) {
+            const uint4* pg = reinterpret_cast<const uint4*>(p.aux + r * 2 * p.F + fc);
+            const uint4* pu = reinterpret_cast<const uint4*>(p.aux + r * 2 * p.F + p.F + fc);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              zg[i] = __ldg(pg + i);
+              zu[i] = __ldg(pu + i);
+            }
+          }
+          tmem_ld_32x32b_x32(tbase + 64 * ch + 32 * h, v);
+          tmem_ld_wait();
+          if (row_ok) {
+            uint32_t wg[16], wu[16];
+            swiglu_bwd32(v, zg, zu, wg, wu);
+            store_row32(p.out0 + r * 2 * p.F + fc, wg);
+            store_row32(p.out0 + r * 2 * p.F + p.F + fc, wu);
+          }
+        }
+      }
+    } else if constexpr (KIND == static_cast<int>(GemmKind::kDlhsFc2)) {
+      const bool fused = p.aux != nullptr;
       for (int ch = 0; ch < BN / 64; ++ch) {
         const int f0 = T.n0 + 64 * ch;
         if (f0 >= p.F) break;
@@ -817,7 +920,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&s.tfull[i], 1);
       mbar_init(&s.tempty[i], kEpiWarps * CG);
     }
-    for (int i = 0; i < kEpiWarps; ++i) mbar_init(&s.zbar[i], 1);
+    for (int i = 0; i < kEpiWarps; ++i) {
+      mbar_init(&s.zbar[i][0], 1);
+      mbar_init(&s.zbar[i][1], 1);
+    }
     for (int i = 0; i < kSched; ++i) {
       mbar_init(&s.sfull[i], 1);
       mbar_init(&s.sempty[i], sched_readers<CG>());
@@ -1016,7 +1122,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // -------------------------------------------------------- epilogue
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     EpiCtx<RING> ec{&map_c, &map_d, Ring<RING>{epi + (warp - 2) * RING * kBufBytes, 0u}, q, lane,
-                    zarea + (warp - 2) * 2 * kBufBytes, &s.zbar[warp - 2], 0u, &wc};
+                    ZPipe{zarea + (warp - 2) * S::kZSlots * 2 * kBufBytes, &s.zbar[warp - 2][0],
+                          0u, 0, 0, 0, -1, 0},
+                    &wc};
     uint32_t tempty_peer = 0;
     if constexpr (CG == 2) tempty_peer = mapa_shared(smem_u32(&s.tempty[0]), 0);
     uint32_t acc = 0, acc_phase = 0;
@@ -1042,7 +1150,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         continue;
       }
-      if (z_by_tma<KIND, S::kZB, RING>(T, ec, p)) z_request(T, 0, ec, p);
+      // the fused SwiGLU backward's z: the tile's first chunks are requested
+      // before its accumulator is waited for (if the previous tile has not
+      // requested them already), with the warp's next tile known
+      int tn = -1;
+      Tile Tn{};
+      if constexpr (S::kZB) {
+        if (z_by_tma<KIND, true, RING>(T, ec, p)) {
+          if (tstat < ntiles) {
+            tn = tstat;
+            Tn = decode_tile<KIND, BNT, CG>(tn, rank, p, s);
+          }
+          if (ec.zp.qt != t) {
+            ec.zp.qt = t;
+            ec.zp.qch = 0;
+          }
+          z_fill<KIND, BN, true, RING>(t, T, tn, Tn, ec, p);
+        }
+      }
       if (!__all_sync(0xffffffffu, mbar_wait(&s.tfull[acc], acc_phase, wc))) break;
       tc_fence_after();
 #pragma unroll
@@ -1051,7 +1176,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         Ta.n0 = T.n0 + a * BN;
         epilogue_tile<KIND, BN, CG, RING, S::kZB>(
             Ta, tmem_base + acc * S::kAccStride + a * BN + (static_cast<uint32_t>(q * 32) << 16),
-            ec, p);
+            ec, p, t, tn, Tn);
       }
       tc_fence_before();
       __syncwarp();
@@ -1063,6 +1188,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (++acc == S::kAccSlots) { acc = 0; acc_phase ^= 1u; }
     }
+    z_drain(ec);                     // z requests still in flight land (abort)
     if (lane == 0) bulk_wait_all();  // every store has finished before the CTA exits
     __syncwarp();
   }
@@ -1228,90 +1354,102 @@ cudaError_t launch_shape(const GemmCall& c, cudaStream_t s) {
   bool ok = false;
   const long row_blocks_bound = R / (BM * CG) + d.E;
   const long F2 = 2L * d.F;
-  switch (c.kind) {
-    case GemmKind::kFc1:
-    case GemmKind::kFc2:
-    case GemmKind::kDlhsFc2:
-    case GemmKind::kDlhsFc1:
-      if constexpr (S::kNacc == 1) {
-        switch (c.kind) {
-          case GemmKind::kFc1:
-            // h, z gate and z up are staged together, z gate and z up in
-            // adjacent buffers (one 3-D store): the ring holds whole triples
-            if constexpr (S::kRing % 3 == 0) {
-              p.Kdim = d.D;
-              p.N = d.F;
-              p.n_tiles = static_cast<int>(cdiv(d.F, BN / 2));
-              ok = map2d(&ma, c.a, d.D, R, 64, BM) &&
-                   map_chunks(&mb, c.b, F2, d.D, d.E, BN / 64 / 2, 4) &&
-                   map2d(&mc, c.out0, d.F, R, 64, 32);
-              if (ok) ok = (c.out1 != nullptr) ? map_halves(&md, c.out1, d.F, R) : (md = mc, true);
+  if constexpr (S::kZB) {
+    // shapes with z slots run only the FC2 dlhs with the fused SwiGLU backward
+    if (c.kind != GemmKind::kDlhsFc2 || c.aux == nullptr) return cudaErrorInvalidValue;
+    p.Kdim = d.D;
+    p.N = d.F;
+    p.n_tiles = static_cast<int>(cdiv(d.F, BN));
+    ok = map2d(&ma, c.a, d.D, R, 64, BM) && map3d(&mb, c.b, d.D, d.F, d.E, 64, kBRows) &&
+         map_halves(&mc, c.out0, d.F, R) && map_halves(&md, c.aux, d.F, R);
+    if (!ok) return cudaErrorInvalidValue;
+    return launch_kind<2, S>(ma, mb, mc, md, p, row_blocks_bound * p.n_tiles, s);
+  } else {
+    switch (c.kind) {
+      case GemmKind::kFc1:
+      case GemmKind::kFc2:
+      case GemmKind::kDlhsFc2:
+      case GemmKind::kDlhsFc1:
+        if constexpr (S::kNacc == 1) {
+          switch (c.kind) {
+            case GemmKind::kFc1:
+              // h, z gate and z up are staged together, z gate and z up in
+              // adjacent buffers (one 3-D store): the ring holds whole triples
+              if constexpr (S::kRing % 3 == 0) {
+                p.Kdim = d.D;
+                p.N = d.F;
+                p.n_tiles = static_cast<int>(cdiv(d.F, BN / 2));
+                ok = map2d(&ma, c.a, d.D, R, 64, BM) &&
+                     map_chunks(&mb, c.b, F2, d.D, d.E, BN / 64 / 2, 4) &&
+                     map2d(&mc, c.out0, d.F, R, 64, 32);
+                if (ok) ok = (c.out1 != nullptr) ? map_halves(&md, c.out1, d.F, R) : (md = mc, true);
+                if (!ok) return cudaErrorInvalidValue;
+                return launch_kind<0, S>(ma, mb, mc, md, p, row_blocks_bound * p.n_tiles, s);
+              }
+              return cudaErrorInvalidValue;
+            case GemmKind::kFc2:
+              p.Kdim = d.F;
+              p.N = d.D;
+              p.n_tiles = static_cast<int>(cdiv(d.D, BN));
+              ok = map2d(&ma, c.a, d.F, R, 64, BM) &&
+                   map_chunks(&mb, c.b, d.D, d.F, d.E, BN / 64 / CG, 4) &&
+                   map2d(&mc, c.out0, d.D, R, 64, 32) && map3d(&md, c.b, d.D, d.F, d.E, 64, 64);
               if (!ok) return cudaErrorInvalidValue;
-              return launch_kind<0, S>(ma, mb, mc, md, p, row_blocks_bound * p.n_tiles, s);
-            }
-            return cudaErrorInvalidValue;
-          case GemmKind::kFc2:
-            p.Kdim = d.F;
-            p.N = d.D;
-            p.n_tiles = static_cast<int>(cdiv(d.D, BN));
-            ok = map2d(&ma, c.a, d.F, R, 64, BM) &&
-                 map_chunks(&mb, c.b, d.D, d.F, d.E, BN / 64 / CG, 4) &&
-                 map2d(&mc, c.out0, d.D, R, 64, 32) && map3d(&md, c.b, d.D, d.F, d.E, 64, 64);
-            if (!ok) return cudaErrorInvalidValue;
-            return launch_kind<1, S>(ma, mb, mc, md, p, row_blocks_bound * p.n_tiles, s);
-          case GemmKind::kDlhsFc2:
-            // fused, dgate and dup are staged together in adjacent buffers
-            // (one 3-D store): the ring must hold whole pairs
-            if (c.aux != nullptr && S::kRing % 2 != 0) return cudaErrorInvalidValue;
-            if constexpr (S::kRing >= 2) {
-              p.Kdim = d.D;
-              p.N = d.F;
-              p.n_tiles = static_cast<int>(cdiv(d.F, BN));
-              ok = map2d(&ma, c.a, d.D, R, 64, BM) && map3d(&mb, c.b, d.D, d.F, d.E, 64, kBRows) &&
-                   (c.aux != nullptr ? map_halves(&mc, c.out0, d.F, R)
-                                     : map2d(&mc, c.out0, d.F, R, 64, 32));
-              if (ok) ok = (c.aux != nullptr) ? map_halves(&md, c.aux, d.F, R) : (md = mc, true);
+              return launch_kind<1, S>(ma, mb, mc, md, p, row_blocks_bound * p.n_tiles, s);
+            case GemmKind::kDlhsFc2:
+              // fused, dgate and dup are staged together in adjacent buffers
+              // (one 3-D store): the ring must hold whole pairs
+              if (c.aux != nullptr && S::kRing % 2 != 0) return cudaErrorInvalidValue;
+              if constexpr (S::kRing >= 2) {
+                p.Kdim = d.D;
+                p.N = d.F;
+                p.n_tiles = static_cast<int>(cdiv(d.F, BN));
+                ok = map2d(&ma, c.a, d.D, R, 64, BM) && map3d(&mb, c.b, d.D, d.F, d.E, 64, kBRows) &&
+                     (c.aux != nullptr ? map_halves(&mc, c.out0, d.F, R)
+                                       : map2d(&mc, c.out0, d.F, R, 64, 32));
+                if (ok) ok = (c.aux != nullptr) ? map_halves(&md, c.aux, d.F, R) : (md = mc, true);
+                if (!ok) return cudaErrorInvalidValue;
+                return launch_kind<2, S>(ma, mb, mc, md, p, row_blocks_bound * p.n_tiles, s);
+              }
+              return cudaErrorInvalidValue;
+            case GemmKind::kDlhsFc1:
+              p.Kdim = 2 * d.F;
+              p.N = d.D;
+              p.n_tiles = static_cast<int>(cdiv(d.D, BN));
+              ok = map2d(&ma, c.a, F2, R, 64, BM) && map3d(&mb, c.b, F2, d.D, d.E, 64, kBRows) &&
+                   map2d(&mc, c.out0, d.D, R, 64, 32);
               if (!ok) return cudaErrorInvalidValue;
-              return launch_kind<2, S>(ma, mb, mc, md, p, row_blocks_bound * p.n_tiles, s);
-            }
-            return cudaErrorInvalidValue;
-          case GemmKind::kDlhsFc1:
-            p.Kdim = 2 * d.F;
-            p.N = d.D;
-            p.n_tiles = static_cast<int>(cdiv(d.D, BN));
-            ok = map2d(&ma, c.a, F2, R, 64, BM) && map3d(&mb, c.b, F2, d.D, d.E, 64, kBRows) &&
-                 map2d(&mc, c.out0, d.D, R, 64, 32);
-            if (!ok) return cudaErrorInvalidValue;
-            return launch_kind<3, S>(ma, mb, mc, mc, p, row_blocks_bound * p.n_tiles, s);
-          default:
-            break;
+              return launch_kind<3, S>(ma, mb, mc, mc, p, row_blocks_bound * p.n_tiles, s);
+            default:
+              break;
+          }
         }
-      }
-      return cudaErrorInvalidValue;
-    case GemmKind::kDrhsFc2:
-      p.M = d.F;
-      p.N = d.D;
-      p.m_tiles = static_cast<int>(cdiv(d.F, BM * CG));
-      p.n_tiles = static_cast<int>(cdiv(d.D, BN * S::kNacc));
-      ok = map_chunks(&ma, c.a, d.F, R, 1, 2, 3) && map_chunks(&mb, c.b, d.D, R, 1, BN / 64 / CG, 3) &&
-           map3d(&mc, c.out0, d.D, d.F, d.E, 64, 32) && map2d(&md, c.b, d.D, R, 64, 64);
-      if (!ok || c.tile_ctr == nullptr) return cudaErrorInvalidValue;
-      if (cudaError_t e = cudaMemsetAsync(c.tile_ctr, 0, sizeof(unsigned int), s); e != cudaSuccess)
-        return e;
-      return launch_kind<4, S>(ma, mb, mc, md, p, static_cast<long>(d.E) * p.m_tiles * p.n_tiles,
-                               s);
-    case GemmKind::kDrhsFc1:
-      p.M = d.D;
-      p.N = 2 * d.F;
-      p.m_tiles = static_cast<int>(cdiv(d.D, BM * CG));
-      p.n_tiles = static_cast<int>(cdiv(F2, BN * S::kNacc));
-      ok = map_chunks(&ma, c.a, d.D, R, 1, 2, 3) && map_chunks(&mb, c.b, F2, R, 1, BN / 64 / CG, 3) &&
-           map3d(&mc, c.out0, F2, d.D, d.E, 64, 32) && map2d(&md, c.b, F2, R, 64, 64);
-      if (!ok || c.tile_ctr == nullptr) return cudaErrorInvalidValue;
-      if (cudaError_t e = cudaMemsetAsync(c.tile_ctr, 0, sizeof(unsigned int), s); e != cudaSuccess)
-        return e;
-      return launch_kind<5, S>(ma, mb, mc, md, p, static_cast<long>(d.E) * p.m_tiles * p.n_tiles,
-                               s);
+        return cudaErrorInvalidValue;
+      case GemmKind::kDrhsFc2:
+        p.M = d.F;
+        p.N = d.D;
+        p.m_tiles = static_cast<int>(cdiv(d.F, BM * CG));
+        p.n_tiles = static_cast<int>(cdiv(d.D, BN * S::kNacc));
+        ok = map_chunks(&ma, c.a, d.F, R, 1, 2, 3) && map_chunks(&mb, c.b, d.D, R, 1, BN / 64 / CG, 3) &&
+             map3d(&mc, c.out0, d.D, d.F, d.E, 64, 32) && map2d(&md, c.b, d.D, R, 64, 64);
+        if (!ok || c.tile_ctr == nullptr) return cudaErrorInvalidValue;
+        if (cudaError_t e = cudaMemsetAsync(c.tile_ctr, 0, sizeof(unsigned int), s); e != cudaSuccess)
+          return e;
+        return launch_kind<4, S>(ma, mb, mc, md, p, static_cast<long>(d.E) * p.m_tiles * p.n_tiles,
+                                 s);
+      case GemmKind::kDrhsFc1:
+        p.M = d.D;
+        p.N = 2 * d.F;
+        p.m_tiles = static_cast<int>(cdiv(d.D, BM * CG));
+        p.n_tiles = static_cast<int>(cdiv(F2, BN * S::kNacc));
+        ok = map_chunks(&ma, c.a, d.D, R, 1, 2, 3) && map_chunks(&mb, c.b, F2, R, 1, BN / 64 / CG, 3) &&
+             map3d(&mc, c.out0, F2, d.D, d.E, 64, 32) && map2d(&md, c.b, F2, R, 64, 64);
+        if (!ok || c.tile_ctr == nullptr) return cudaErrorInvalidValue;
+        if (cudaError_t e = cudaMemsetAsync(c.tile_ctr, 0, sizeof(unsigned int), s); e != cudaSuccess)
+          return e;
+        return launch_kind<5, S>(ma, mb, mc, md, p, static_cast<long>(d.E) * p.m_tiles * p.n_tiles,
+                                 s);
+    }
   }
   return cudaErrorInvalidValue;
 }
@@ -1326,9 +1464,10 @@ using Shape2Fc1 = Shape<256, 5, 2, 3>;
 using Shape2 = Shape<256, 5, 2, 2>;
 // drhs: tiles two accumulators wide (fewer bytes loaded per MMA).
 using Shape2Drhs = Shape<256, 3, 2, 2, 0, 2>;
-// The FC2 dlhs with the fused SwiGLU backward also stages z rows.
-using Shape1Dz = Shape<256, 3, 1, 2, 1>;
-using Shape2Dz = Shape<256, 4, 2, 2, 1>;
+// The FC2 dlhs with the fused SwiGLU backward: two z slots per epilogue
+// warp, in which dz is also staged (no staging ring).
+using Shape1Dz = Shape<256, 3, 1, 0, 2>;
+using Shape2Dz = Shape<256, 4, 2, 0, 2>;
 
 // Whether a grouped GEMM runs on CTA pairs.  The pair's 256-row block is the
 // unit of rows for the forward and dlhs GEMMs; pairs pay off from ~256 rows
