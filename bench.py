@@ -641,6 +641,38 @@ def measure_workload(wl, inp, steps, warmup, fwd_only, dev, dist=None):
     return step, elapsed, clk.summary(), flush is not None
 
 
+def measure_fused(wl, inp, steps, dev, flushed):
+    """The inference forward through moe_fused_forward (routing, FC1 on rows
+    gathered from x, FC2 with the weighted combine in its epilogue, the fp32
+    accumulator converted to bf16), one event pair around each step."""
+    from mixture_experts_ffn_histogram_gb300.block import MoEBlock
+    blk = MoEBlock(wl.T, wl.D, wl.E, wl.K, wl.F, wl.score_mode, train=False, device=dev)
+
+    def one():
+        blk.forward_fused(inp["x"], inp["wi"], inp["wo"], logits=inp.get("logits"),
+                          bias=inp.get("bias"), ids=inp.get("ids"), w=inp.get("w"))
+
+    for _ in range(3):
+        one()
+    torch.cuda.synchronize()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if flushed else None
+    marks = []
+    for _ in range(steps):
+        if flush is not None:
+            flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        one()
+        b.record()
+        marks.append((a, b))
+    torch.cuda.synchronize()
+    if int(blk.status.item()) != 0:
+        raise RuntimeError(f"device status {int(blk.status.item())} after the fused steps")
+    step_s = sum(a.elapsed_time(b) for a, b in marks) * 1e-3 / steps
+    return {"tokens_per_s": wl.T / step_s, "ms_per_step": step_s * 1e3,
+            "launches_per_step": 5, "l2_flushed": flushed}
+
+
 # every configuration of the block's workloads, with the pass each is quoted on
 CONFIG_SWEEP = ("tiny_fwd", "token_sweep_T1024", "token_sweep_T2048", "token_sweep_T4096",
                 "token_sweep_T8192", "long_seq_train", "large_expert_train", "zipf_skew_train")
@@ -671,6 +703,9 @@ def measure_configs(steps, warmup, dev, pk, skip=()):
             "kernels": {n: {"median_us": v["median_us"], "bound": v["bound"],
                             "frac_roofline": v["frac_roofline"]} for n, v in kern.items()},
         })
+        if fwd_only:
+            # the same forward through the fused entry point (no xs, no ys)
+            res[-1]["fused_forward"] = measure_fused(wl, inp, steps, dev, flushed)
         del step, inp
         torch.cuda.empty_cache()
     return res

@@ -106,7 +106,8 @@ const char* moe_status_string(moe_status s);
 
 /* Version of this ABI; lets a loader check the library it opened without
  * touching a GPU.  2: adds the MXFP8 entry points (moe_mx_*) and the FC1
- * calls over expert ranges (moe_grouped_gemm_fc1_*_experts) to version 1's. */
+ * calls over expert ranges (moe_grouped_gemm_fc1_*_experts) to version 1's.
+ * 3: adds moe_fused_forward. */
 int moe_abi_version(void);
 
 /*
@@ -391,6 +392,31 @@ moe_status moe_mx_grouped_gemm_fc2(const uint8_t* hq, const uint8_t* hsc, const 
                                    const uint8_t* wsc, const int32_t* group_offsets,
                                    moe_bf16* ys, int32_t* dev_status, moe_dims d,
                                    cudaStream_t stream);
+
+/*
+ * Fused forward for inference [Fused MoE Summary: gather, GMM1, activation
+ * and GMM2 in one pass; Fused p/c Commits table row 1: the combine as the
+ * unpermute plus the top-K weighted sum].  After moe_route_histogram, the
+ * block's forward without the permuted copy xs and without ys:
+ *   h = silu(a[:F]) * a[F:], a = x[row_src[r] / K] . wi[e]   (FC1 on rows
+ *       gathered from the token-major x; the sorted order is row_src's)
+ *   out[t] = bf16(sum_k w[t,k] * (h[pos[t,k]] . wo[e]))       (FC2 with the
+ *       weighted combine in its epilogue, summed in fp32 in acc)
+ *   x bf16 [T,D], w fp32 [T,K], row_src int32 [R] and group_offsets [E+1]
+ *   from moe_route_histogram, wi, wo as for the unfused calls;
+ *   h    bf16 [R,F]  scratch (FC1's output, FC2's input), caller-owned;
+ *   acc  fp32 [T,D]  scratch, caller-owned (zeroed by the call);
+ *   out  bf16 [T,D]  out.
+ * Rows of row_src that are -1 (dropped slots) contribute nothing.  The fp32
+ * sums of the combine are added in an unspecified order, so out is not
+ * bitwise reproducible between runs; each element is within the block's
+ * tolerance of the unfused moe_combine result (which rounds each ys to bf16
+ * first).  No z is produced: this is the inference forward.
+ */
+moe_status moe_fused_forward(const moe_bf16* x, const float* w, const int32_t* row_src,
+                             const int32_t* group_offsets, const moe_bf16* wi, const moe_bf16* wo,
+                             moe_bf16* h, float* acc, moe_bf16* out, int32_t* dev_status,
+                             void* ws, moe_dims d, cudaStream_t stream);
 
 /*
  * Self-test of the kernels' bounded waits (no counterpart on the pages):

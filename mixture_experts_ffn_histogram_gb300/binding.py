@@ -34,6 +34,7 @@ ENTRY_POINTS = (
     "moe_mx_bytes", "moe_mx_quantize_wi", "moe_mx_quantize_wo", "moe_mx_permute_quantize",
     "moe_mx_grouped_gemm_fc1_swiglu", "moe_mx_grouped_gemm_fc2",
     "moe_grouped_gemm_fc1_swiglu_experts", "moe_grouped_gemm_fc1_bwd_experts",
+    "moe_fused_forward",
 )
 
 # moe_mx_buffer
@@ -94,6 +95,7 @@ def lib() -> ctypes.CDLL:
             "moe_grouped_gemm_fc2": ([P, P, P, P, P, P, D_, P], I),
             "moe_grouped_gemm_fc2_bwd": ([P, P, P, P, P, P, P, P, P, D_, P], I),
             "moe_combine": ([P, P, P, P, D_, P], I),
+            "moe_fused_forward": ([P, P, P, P, P, P, P, P, P, P, P, D_, P], I),
             "moe_combine_bwd": ([P, P, P, P, P, P, D_, P], I),
             "moe_selftest_bounded_wait": ([P, ctypes.c_uint64, P], I),
             "moe_route_histogram_noalloc": ([P, P, I, P, P, P, P, P, P, P, D_, P], I),
@@ -208,6 +210,13 @@ def moe_grouped_gemm_fc2_bwd(dys, h, wo, z, group_offsets, dh_or_dz, dwo, dev_st
 
 def moe_combine(ys, w, pos, out, d: MoeDims, stream=None):
     _ok("moe_combine", lib().moe_combine(_p(ys), _p(w), _p(pos), _p(out), d, _s(stream)))
+
+
+def moe_fused_forward(x, w, row_src, group_offsets, wi, wo, h, acc, out, dev_status, ws,
+                      d: MoeDims, stream=None):
+    _ok("moe_fused_forward", lib().moe_fused_forward(
+        _p(x), _p(w), _p(row_src), _p(group_offsets), _p(wi), _p(wo), _p(h), _p(acc), _p(out),
+        _p(dev_status), _p(ws), d, _s(stream)))
 
 
 def moe_combine_bwd(dout, ys, w, pos, dys, dw, d: MoeDims, stream=None):

@@ -51,6 +51,27 @@ class MoEBlock:
             self.dwi = torch.empty((E, D, 2 * F), dtype=bf, device=dev)
             self.dx = torch.empty((T, D), dtype=bf, device=dev)
 
+    def forward_fused(self, x, wi, wo, logits=None, bias=None, ids=None, w=None, stream=None):
+        """The inference forward through moe_fused_forward: routing, then FC1
+        on rows gathered straight from x and FC2 with the weighted combine in
+        its epilogue (no xs, no ys).  Needs a whole wi; h and an fp32 [T, D]
+        accumulator are the block's scratch."""
+        d = self.d
+        self._check_weights(wi, wo)
+        if isinstance(wi, (list, tuple)):
+            raise ValueError("the fused forward takes a whole wi")
+        if self.mode == B.SCORE_GIVEN:
+            self.ids.copy_(ids)
+            self.w.copy_(w)
+        if getattr(self, "acc", None) is None:
+            self.acc = torch.empty((self.T, self.D), dtype=torch.float32, device=self.out.device)
+        B.moe_route_histogram(logits, bias, self.mode, self.ids, self.w, self.group_sizes,
+                              self.group_offsets, self.pos, self.row_src, self.status, self.ws,
+                              d, stream)
+        B.moe_fused_forward(x, self.w, self.row_src, self.group_offsets, wi, wo, self.h, self.acc,
+                            self.out, self.status, self.ws, d, stream)
+        return self.out
+
     def _check_weights(self, wi, wo):
         """The library builds its tensor maps from the block's dims, so a
         weight of another shape or dtype would be read (and its gradient

@@ -86,7 +86,7 @@ const char* moe_status_string(moe_status s) {
   return "unknown status";
 }
 
-int moe_abi_version(void) { return 2; }
+int moe_abi_version(void) { return 3; }
 
 moe_status moe_route_histogram(const float* logits, const float* bias, moe_score_mode mode,
                                int32_t* ids, float* w, int32_t* group_sizes,
@@ -175,6 +175,39 @@ moe_status moe_combine(const moe_bf16* ys, const float* w, const int32_t* pos, m
   MOE_REQUIRE(pos);
   MOE_REQUIRE(out);
   return from_cuda(moe::launch_combine(ys, w, pos, out, d, stream));
+}
+
+moe_status moe_fused_forward(const moe_bf16* x, const float* w, const int32_t* row_src,
+                             const int32_t* group_offsets, const moe_bf16* wi, const moe_bf16* wo,
+                             moe_bf16* h, float* acc, moe_bf16* out, int32_t* dev_status,
+                             void* ws, moe_dims d, cudaStream_t stream) {
+  (void)ws;
+  MOE_CHECK_DIMS(d);
+  MOE_OPTIONAL(dev_status);
+  if (d.T == 0) return MOE_OK;
+  MOE_REQUIRE(x);
+  MOE_REQUIRE(w);
+  MOE_REQUIRE(row_src);
+  MOE_REQUIRE(group_offsets);
+  MOE_REQUIRE(wi);
+  MOE_REQUIRE(wo);
+  MOE_REQUIRE(h);
+  MOE_REQUIRE(acc);
+  MOE_REQUIRE(out);
+  GemmCall c1{GemmKind::kFc1Gather, x, wi, group_offsets, h, nullptr, nullptr, dev_status, d};
+  c1.row_src = row_src;
+  cudaError_t err = moe::launch_grouped_gemm(c1, stream);
+  if (err != cudaSuccess) return from_cuda(err);
+  const size_t n = static_cast<size_t>(d.T) * static_cast<size_t>(d.D);
+  err = cudaMemsetAsync(acc, 0, n * sizeof(float), stream);
+  if (err != cudaSuccess) return from_cuda(err);
+  GemmCall c2{GemmKind::kFc2Combine, h, wo, group_offsets, nullptr, nullptr, nullptr, dev_status, d};
+  c2.row_src = row_src;
+  c2.w = w;
+  c2.acc = acc;
+  err = moe::launch_grouped_gemm(c2, stream);
+  if (err != cudaSuccess) return from_cuda(err);
+  return from_cuda(moe::launch_acc_to_bf16(acc, out, static_cast<long>(n), stream));
 }
 
 moe_status moe_combine_bwd(const moe_bf16* dout, const moe_bf16* ys, const float* w,

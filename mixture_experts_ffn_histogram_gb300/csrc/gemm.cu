@@ -83,6 +83,7 @@ struct SmemCtl {
   // forward/dlhs: prefix of (128*CG)-row blocks per group; drhs: sort keys
   // whose low 10 bits are the experts by descending reduction length
   int mt[kMaxExperts + 1];
+  int gtok[BM];              // gathered FC1: token of each row of the current tile
 };
 
 // Tile shape: 128 x BN accumulator per CTA, CG CTAs per MMA, a `STAGES`-deep
@@ -128,18 +129,35 @@ struct Params {
   const __nv_bfloat16* aux;
   int32_t* status;
   unsigned int* tile_ctr;  // drhs: tiles claimed so far (zero at launch)
+  const uint16_t* xin;     // gathered FC1: token-major x [T, D]
+  const int32_t* row_src;  // gathered FC1, combined FC2: slot j = t*K + k of each row
+  const float* wts;        // combined FC2: routing weights [T, K]
+  float* acc;              // combined FC2: fp32 [T, D] accumulator
+  int Ktop;                // top_k
+  long R;                  // rows (T * K)
   uint64_t limit_ns;
   int E, Kdim, M, N, F;
   int m_tiles, n_tiles;
 };
+
+// The kinds that share FC1's (FC2's) operands, tiles and epilogue: the
+// gathered FC1 differs only in where its A rows come from, the combined FC2
+// only in where its output goes.
+template <int KIND>
+__host__ __device__ constexpr bool fc1_like() {
+  return KIND == static_cast<int>(GemmKind::kFc1) || KIND == static_cast<int>(GemmKind::kFc1Gather);
+}
+template <int KIND>
+__host__ __device__ constexpr bool fc2_like() {
+  return KIND == static_cast<int>(GemmKind::kFc2) || KIND == static_cast<int>(GemmKind::kFc2Combine);
+}
 
 template <int KIND, int BN, int CG>
 struct Traits {
   static constexpr bool kGroupedK = (KIND == static_cast<int>(GemmKind::kDrhsFc2) ||
                                      KIND == static_cast<int>(GemmKind::kDrhsFc1));
   static constexpr bool kAMn = kGroupedK;
-  static constexpr bool kBMn = (KIND == static_cast<int>(GemmKind::kFc1) ||
-                                KIND == static_cast<int>(GemmKind::kFc2) || kGroupedK);
+  static constexpr bool kBMn = (fc1_like<KIND>() || fc2_like<KIND>() || kGroupedK);
   static constexpr uint32_t kIdesc = instr_desc_bf16(BM * CG, BN, kAMn, kBMn);
 };
 
@@ -169,7 +187,7 @@ __device__ __forceinline__ Tile decode_tile(int t, int rank, const Params& p, co
     T.row0 = s.off[lo] + (mt - s.mt[lo]) * (BM * CG) + BM * rank;
     T.rows = max(0, min(BM, s.off[lo + 1] - T.row0));
     T.m0 = 0;
-    T.n0 = nt * (KIND == static_cast<int>(GemmKind::kFc1) ? BN / 2 : BN);
+    T.n0 = nt * (fc1_like<KIND>() ? BN / 2 : BN);
     T.kb = p.Kdim / BK;
     T.klen = p.Kdim;
   } else {
@@ -313,7 +331,7 @@ __device__ __forceinline__ void load4(void* dst, const CUtensorMap* map, uint32_
 // columns [0, w/2) are gate columns n0.., [w/2, w) up columns F + n0...
 template <int KIND, int BN, int CG>
 __device__ __forceinline__ int acc_cols(const Tile& T, int a, const Params& p) {
-  if constexpr (KIND == static_cast<int>(GemmKind::kFc1)) {
+  if constexpr (fc1_like<KIND>()) {
     return 2 * min(BN / 2, p.N - T.n0);  // p.N = F, a multiple of 64
   } else {
     const int nv = min(BN, p.N - (T.n0 + a * BN));
@@ -328,7 +346,7 @@ __device__ __forceinline__ int acc_cols(const Tile& T, int a, const Params& p) {
 // would put them at the wrong offsets of a pair's halves).
 template <int KIND, int BN, int CG>
 __device__ __forceinline__ bool narrow_chunks(int w) {
-  return (KIND == static_cast<int>(GemmKind::kFc2) || Traits<KIND, BN, CG>::kGroupedK) && w < BN;
+  return (fc2_like<KIND>() || Traits<KIND, BN, CG>::kGroupedK) && w < BN;
 }
 
 // Bytes that one reduction block of tile T brings into ONE CTA's stage.
@@ -338,7 +356,7 @@ __device__ __forceinline__ uint32_t stage_bytes(const Tile& T, const Params& p) 
   if constexpr (KIND == static_cast<int>(GemmKind::kDlhsFc2) ||
                 KIND == static_cast<int>(GemmKind::kDlhsFc1)) {
     return kAStageBytes + (BN / CG) * BK * 2;  // K-major B: one box of BN/CG rows
-  } else if constexpr (KIND == static_cast<int>(GemmKind::kFc1)) {
+  } else if constexpr (fc1_like<KIND>()) {
     return kAStageBytes + kBChunks * kChunkBytes;  // whole boxes, also for the tail
   } else {
     uint32_t chunks = 0;
@@ -366,18 +384,19 @@ __device__ __forceinline__ void issue_loads(const Tile& T, int kb, int rank, uin
                                             const Params& p) {
   const int k0 = kb * BK;
   constexpr int kBChunks = BN / 64 / CG;  // 64-wide B chunks a CTA holds per accumulator
-  if constexpr (KIND == static_cast<int>(GemmKind::kFc1)) {
+  if constexpr (fc1_like<KIND>()) {
     // B = wi[e] as [chunk of 2F][D][64]: for a pair the even CTA takes the
     // gate chunks n0.., the odd one the up chunks F + n0..; alone, a CTA
-    // takes both (gate in slots [0, kBChunks/2), up after).
-    load2<CG>(sa, ma, bar, k0, T.row0);
+    // takes both (gate in slots [0, kBChunks/2), up after).  The gathered
+    // FC1's A rows are copied by the producer warp instead.
+    if constexpr (KIND != static_cast<int>(GemmKind::kFc1Gather)) load2<CG>(sa, ma, bar, k0, T.row0);
     if constexpr (CG == 1) {
       load4<CG>(sb, mb, bar, 0, k0, T.n0 / 64, T.e);
       load4<CG>(sb + (kBChunks / 2) * kChunkBytes, mb, bar, 0, k0, (p.F + T.n0) / 64, T.e);
     } else {
       load4<CG>(sb, mb, bar, 0, k0, (rank == 0 ? T.n0 : p.F + T.n0) / 64, T.e);
     }
-  } else if constexpr (KIND == static_cast<int>(GemmKind::kFc2)) {
+  } else if constexpr (fc2_like<KIND>()) {
     const int w = acc_cols<KIND, BN, CG>(T, 0, p);
     load2<CG>(sa, ma, bar, k0, T.row0);
     if (!narrow_chunks<KIND, BN, CG>(w)) {
@@ -666,7 +685,7 @@ __device__ __forceinline__ void epilogue_tile(const Tile& T, uint32_t tbase, Epi
     const bool row_ok = lane < vw;
     const int y = T.row0 + 32 * c.q;
     const long r = static_cast<long>(y) + lane;
-    if constexpr (KIND == static_cast<int>(GemmKind::kFc1)) {
+    if constexpr (fc1_like<KIND>()) {
       const bool with_z = p.out1 != nullptr;
       const int hw = acc_cols<KIND, BN, CG>(T, 0, p) / 2;  // first up column of the accumulator
       for (int ch = 0; ch < BN / 128; ++ch) {
@@ -836,6 +855,31 @@ __device__ __forceinline__ void epilogue_tile(const Tile& T, uint32_t tbase, Epi
           else flush_2d(gb, c.map_c, f0, y, lane);
         }
       }
+    } else if constexpr (KIND == static_cast<int>(GemmKind::kFc2Combine)) {
+      // the combine, in place of a stored ys: each row's fp32 output times
+      // its routing weight goes into its token's fp32 accumulator,
+      // acc[t] += w[t,k] * ys[r] (16-byte vector reductions)
+      const int j = row_ok ? __ldg(p.row_src + r) : -1;
+      const float wk = j >= 0 ? __ldg(p.wts + j) : 0.0f;
+      float* dst = j >= 0 ? p.acc + static_cast<long>(j / p.Ktop) * p.N : nullptr;
+      for (int ch = 0; ch < BN / 64; ++ch) {
+        const int col = T.n0 + 64 * ch;
+        if (col >= p.N) break;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          tmem_ld_32x32b_x32(tbase + 64 * ch + 32 * h, v);
+          tmem_ld_wait();
+          if (j >= 0) {
+            float4* o = reinterpret_cast<float4*>(dst + col + 32 * h);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              atomicAdd(o + i, make_float4(wk * __uint_as_float(v[4 * i]),
+                                           wk * __uint_as_float(v[4 * i + 1]),
+                                           wk * __uint_as_float(v[4 * i + 2]),
+                                           wk * __uint_as_float(v[4 * i + 3])));
+          }
+        }
+      }
     } else {
       // plain bf16 store: FC2 and the dlhs of FC1 (N = D columns)
       for (int ch = 0; ch < BN / 64; ++ch) {
@@ -912,8 +956,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_map(&map_b);
     tma_prefetch_map(&map_c);
     tma_prefetch_map(&map_d);
+    // the gathered FC1's stages complete on the producer lane's arrival
+    // (with the B bytes) and on the 32 lanes' cp.async arrivals
+    constexpr uint32_t kFullArrivals = (KIND == static_cast<int>(GemmKind::kFc1Gather)) ? 33 : 1;
     for (int i = 0; i < kStages; ++i) {
-      mbar_init(&s.full[i], 1);
+      mbar_init(&s.full[i], kFullArrivals);
       mbar_init(&s.empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -976,7 +1023,66 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t sseq = 0;      // dynamic: slots read (or written) so far
   int tstat = unit;       // fixed: this unit's next tile
 
-  if (warp == 0) {
+  if (warp == 0 && KIND == static_cast<int>(GemmKind::kFc1Gather)) {
+    // ----------------------------------------- producer (gathered FC1 rows)
+    // The whole warp: lane 0 waits for a free stage, arms it and loads the B
+    // operand by TMA; then every lane copies its share of the tile's 128 A
+    // rows straight from the token-major x (row r of the tile is token
+    // row_src[r] / K) with 16-byte cp.async into the 128-byte-swizzled
+    // layout, and arrives on the stage's barrier when its copies have landed.
+    if constexpr (KIND == static_cast<int>(GemmKind::kFc1Gather) && CG == 1) {
+      uint32_t stage = 0, phase = 0;
+      uint32_t fills[kStages];
+#pragma unroll
+      for (int i = 0; i < kStages; ++i) fills[i] = 0;
+      bool aborted = false;
+      while (!aborted) {
+        const int t = tstat;
+        tstat += units;
+        if (t >= ntiles) break;
+        const Tile T = decode_tile<KIND, BNT, CG>(t, rank, p, s);
+        __syncwarp();  // the previous tile's tokens have been read
+        for (int i = lane; i < BM; i += 32) {
+          const long r = static_cast<long>(T.row0) + i;
+          int tok = 0;  // rows past the last are computed from token 0 and never stored
+          if (r < p.R) {
+            const int j = __ldg(p.row_src + r);
+            tok = j >= 0 ? j / p.Ktop : 0;
+          }
+          s.gtok[i] = tok;
+        }
+        __syncwarp();
+        const uint32_t tx_bytes = stage_bytes<KIND, BN, CG, NACC>(T, p) - kAStageBytes;
+        const int c = lane & 7;  // 16-byte chunk of a 128-byte row
+        for (int kb = 0; kb < T.kb; ++kb) {
+          bool ok = true;
+          if (lane == 0) ok = mbar_wait(&s.empty[stage], phase ^ 1u, wc);
+          if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) { aborted = true; break; }
+          uint8_t* sa = ring + stage * kStageBytes;
+          if (lane == 0) {
+            mbar_arrive_expect_tx(&s.full[stage], tx_bytes);
+            issue_loads<KIND, BN, CG, NACC>(T, kb, rank, sa, sa + kAStageBytes,
+                                            smem_u32(&s.full[stage]), &map_a, &map_b, &map_d, p);
+            ++fills[stage];
+          }
+          const uint16_t* xk = p.xin + static_cast<long>(kb) * BK + 8 * c;
+#pragma unroll 8
+          for (int i = 0; i < BM / 4; ++i) {
+            const int row = (lane >> 3) + 4 * i;
+            cp_async16(sa + row * 128 + ((c ^ (row & 7)) << 4),
+                       xk + static_cast<long>(s.gtok[row]) * p.Kdim);
+          }
+          cp_async_arrive_noinc(&s.full[stage]);
+          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        }
+      }
+      cp_async_wait_all();  // this lane's copies have landed
+      if (aborted && lane == 0) {  // and the TMA bytes of stages in flight
+        for (int i = 0; i < kStages; ++i)
+          if (fills[i] > 0) (void)mbar_wait_drain(&s.full[i], (fills[i] - 1u) & 1u, 100000000ull);
+      }
+    }
+  } else if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       // For a pair, both CTAs' bytes complete on the even CTA's full barrier,
@@ -1056,7 +1162,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t d_tmem = tmem_base + acc * S::kAccStride;
         // a lone CTA's narrow FC1 tile reads the first gate and the first up
         // chunk, which the boxes left two chunks apart
-        const uint32_t b_lbo = (KIND == static_cast<int>(GemmKind::kFc1) && CG == 1 &&
+        const uint32_t b_lbo = (fc1_like<KIND>() && CG == 1 &&
                                 acc_cols<KIND, BN, CG>(T, 0, p) < BN)
                                    ? 2 * kChunkBytes
                                    : kChunkBytes;
@@ -1071,6 +1177,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
+          // the gathered A rows were written by cp.async (the generic proxy);
+          // the MMA reads them through the async proxy
+          if constexpr (KIND == static_cast<int>(GemmKind::kFc1Gather)) fence_proxy_async_smem();
           uint8_t* sa = ring + stage * kStageBytes;
           uint8_t* sb = sa + kAStageBytes;
           int ksteps = BK / kUmmaK;
@@ -1370,6 +1479,8 @@ cudaError_t launch_shape(const GemmCall& c, cudaStream_t s) {
       case GemmKind::kFc2:
       case GemmKind::kDlhsFc2:
       case GemmKind::kDlhsFc1:
+      case GemmKind::kFc1Gather:
+      case GemmKind::kFc2Combine:
         if constexpr (S::kNacc == 1) {
           switch (c.kind) {
             case GemmKind::kFc1:
@@ -1420,6 +1531,44 @@ cudaError_t launch_shape(const GemmCall& c, cudaStream_t s) {
                    map2d(&mc, c.out0, d.D, R, 64, 32);
               if (!ok) return cudaErrorInvalidValue;
               return launch_kind<3, S>(ma, mb, mc, mc, p, row_blocks_bound * p.n_tiles, s);
+            case GemmKind::kFc1Gather:
+              // FC1 on rows gathered from x by row_src (single CTAs); the A
+              // map is unused (the producer warp copies the rows)
+              if constexpr (S::CG == 1 && S::kRing % 3 == 0) {
+                p.Kdim = d.D;
+                p.N = d.F;
+                p.n_tiles = static_cast<int>(cdiv(d.F, BN / 2));
+                p.xin = static_cast<const uint16_t*>(c.a);
+                p.row_src = c.row_src;
+                p.Ktop = d.K;
+                p.R = R;
+                ok = map_chunks(&mb, c.b, F2, d.D, d.E, BN / 64 / 2, 4) &&
+                     map2d(&mc, c.out0, d.F, R, 64, 32);
+                if (ok) ok = (c.out1 != nullptr) ? map_halves(&md, c.out1, d.F, R) : (md = mc, true);
+                if (!ok || c.row_src == nullptr) return cudaErrorInvalidValue;
+                return launch_kind<6, S>(mb, mb, mc, md, p, row_blocks_bound * p.n_tiles, s);
+              }
+              return cudaErrorInvalidValue;
+            case GemmKind::kFc2Combine:
+              // FC2 whose rows go, weighted, into the fp32 accumulator
+              // (single CTAs); no output map
+              if constexpr (S::CG == 1) {
+                p.Kdim = d.F;
+                p.N = d.D;
+                p.n_tiles = static_cast<int>(cdiv(d.D, BN));
+                p.row_src = c.row_src;
+                p.wts = c.w;
+                p.acc = c.acc;
+                p.Ktop = d.K;
+                p.R = R;
+                ok = map2d(&ma, c.a, d.F, R, 64, BM) &&
+                     map_chunks(&mb, c.b, d.D, d.F, d.E, BN / 64 / CG, 4) &&
+                     map3d(&md, c.b, d.D, d.F, d.E, 64, 64);
+                if (!ok || c.row_src == nullptr || c.w == nullptr || c.acc == nullptr)
+                  return cudaErrorInvalidValue;
+                return launch_kind<7, S>(ma, mb, ma, md, p, row_blocks_bound * p.n_tiles, s);
+              }
+              return cudaErrorInvalidValue;
             default:
               break;
           }
@@ -1512,6 +1661,10 @@ cudaError_t launch_grouped_gemm(const GemmCall& c, cudaStream_t s) {
       return cudaMemsetAsync(c.out0, 0, static_cast<size_t>(d.E) * d.D * 2 * d.F * 2, s);
     return cudaSuccess;
   }
+  // the gathered FC1 and the combined FC2 run on single CTAs (their A rows
+  // and output rows are per token, not per pair of CTAs)
+  if (c.kind == GemmKind::kFc1Gather || c.kind == GemmKind::kFc2Combine)
+    return launch_shape<Shape1>(c, s);
   const bool dz = (c.kind == GemmKind::kDlhsFc2 && c.aux != nullptr);
   if (!use_pairs(c)) return dz ? launch_shape<Shape1Dz>(c, s) : launch_shape<Shape1>(c, s);
   if (c.kind == GemmKind::kDrhsFc2 || c.kind == GemmKind::kDrhsFc1)

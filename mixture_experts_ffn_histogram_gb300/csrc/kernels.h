@@ -52,9 +52,17 @@ cudaError_t launch_combine_bwd(const uint16_t* dout, const uint16_t* ys, const f
 cudaError_t launch_swiglu_bwd(const uint16_t* dh, const uint16_t* z, uint16_t* dz, long R, int F,
                               cudaStream_t s);
 cudaError_t launch_bounded_wait_selftest(int32_t* dev_status, uint64_t limit_ns, cudaStream_t s);
+// out = bf16(acc) elementwise, n elements (a multiple of 8)
+cudaError_t launch_acc_to_bf16(const float* acc, uint16_t* out, long n, cudaStream_t s);
 
 // Grouped GEMMs (tcgen05).  `rows` = T*K.
-enum class GemmKind : int { kFc1 = 0, kFc2 = 1, kDlhsFc2 = 2, kDlhsFc1 = 3, kDrhsFc2 = 4, kDrhsFc1 = 5 };
+// kFc1Gather: FC1 whose rows are gathered from the token-major x by row_src
+// (no permuted copy); kFc2Combine: FC2 whose rows are weighted by w and added
+// into an fp32 [T, D] accumulator (no ys, no separate combine).
+enum class GemmKind : int {
+  kFc1 = 0, kFc2 = 1, kDlhsFc2 = 2, kDlhsFc1 = 3, kDrhsFc2 = 4, kDrhsFc1 = 5,
+  kFc1Gather = 6, kFc2Combine = 7
+};
 
 struct GemmCall {
   GemmKind kind;
@@ -67,6 +75,9 @@ struct GemmCall {
   int32_t* dev_status;
   moe_dims d;
   unsigned int* tile_ctr = nullptr;  // drhs: a device counter for the dynamic tile schedule
+  const int32_t* row_src = nullptr;  // gather / combine: slot j = t*K + k of each sorted row
+  const float* w = nullptr;          // combine: routing weights [T, K]
+  float* acc = nullptr;              // combine: fp32 [T, D] accumulator
 };
 
 // Bytes at the start of `ws` that hold the drhs tile counter; the SwiGLU

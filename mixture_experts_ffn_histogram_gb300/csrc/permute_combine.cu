@@ -288,6 +288,17 @@ __global__ void __launch_bounds__(kThreads) swiglu_bwd_kernel(const uint4* __res
   }
 }
 
+// out = bf16(acc), 8 elements per thread (the fused forward's last step).
+__global__ void __launch_bounds__(kThreads) acc_to_bf16_kernel(const float4* __restrict__ acc,
+                                                               uint4* __restrict__ out, long n8) {
+  for (long i = static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8;
+       i += static_cast<long>(gridDim.x) * blockDim.x) {
+    const float4 a = __ldg(acc + 2 * i), b = __ldg(acc + 2 * i + 1);
+    out[i] = make_uint4(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w), pack_bf16x2(b.x, b.y),
+                        pack_bf16x2(b.z, b.w));
+  }
+}
+
 // A block that waits on a barrier nothing arrives at, to exercise the
 // bounded wait: it must give up, record MOE_ERR_TIMEOUT and return.
 __global__ void bounded_wait_selftest_kernel(int32_t* status, uint64_t limit_ns) {
@@ -358,6 +369,17 @@ cudaError_t launch_swiglu_bwd(const uint16_t* dh, const uint16_t* z, uint16_t* d
   swiglu_bwd_kernel<<<static_cast<int>(blocks), kThreads, 0, s>>>(
       reinterpret_cast<const uint4*>(dh), reinterpret_cast<const uint4*>(z),
       reinterpret_cast<uint4*>(dz), R, F / 8);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_acc_to_bf16(const float* acc, uint16_t* out, long n, cudaStream_t s) {
+  const long n8 = n / 8;
+  if (n8 == 0) return cudaSuccess;
+  long blocks = (n8 + kThreads - 1) / kThreads;
+  const long cap = static_cast<long>(sm_count()) * 16;
+  if (blocks > cap) blocks = cap;
+  acc_to_bf16_kernel<<<static_cast<int>(blocks), kThreads, 0, s>>>(
+      reinterpret_cast<const float4*>(acc), reinterpret_cast<uint4*>(out), n8);
   return cudaGetLastError();
 }
 
