@@ -67,8 +67,12 @@ def load_library(path: str) -> ctypes.CDLL:
         "oracle_e4m3_to_f64": ([ctypes.c_uint8], ctypes.c_double),
         "oracle_f64_to_e4m3": ([ctypes.c_double], ctypes.c_uint8),
         "oracle_mx_quantize": ([P, I, I, P, P], I),
-        "oracle_mx_fc1_swiglu": ([P, P, P, P, P, I, I, I, P], I),
+        "oracle_mx_fc1_swiglu": ([P, P, P, P, P, I, I, I, P, P], I),
         "oracle_mx_fc2": ([P, P, P, P, P, I, I, I, P], I),
+        "oracle_f32_to_bf16_array": ([P, ctypes.c_long, P], I),
+        "oracle_mx_quantize_tokens": ([P, P, I, I, P, P, P], I),
+        "oracle_mx_wgrad": ([P, P, P, P, P, P, I, I, I, P], I),
+        "oracle_mx_fc2_dgrad_swiglu": ([P, P, P, P, P, P, I, I, I, P], I),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -118,10 +122,10 @@ def _check(rc, name):
 # ----------------------------------------------------------------- wrappers
 def f32_to_bf16(a) -> np.ndarray:
     """RNE rounding of an fp32 array to bf16 bit patterns (elementwise)."""
-    L = lib()
-    a = np.asarray(a, dtype=np.float32)
-    return np.array([L.oracle_f32_to_bf16(float(v)) for v in a.ravel()],
-                    dtype=np.uint16).reshape(a.shape)
+    a = np.ascontiguousarray(a, dtype=np.float32)
+    out = np.empty(a.shape, np.uint16)
+    _check(lib().oracle_f32_to_bf16_array(_p(a), a.size, _p(out)), "f32_to_bf16")
+    return out
 
 
 def bf16_to_f32(b) -> np.ndarray:
@@ -306,9 +310,10 @@ def e4m3_lut() -> np.ndarray:
     return _LUT
 
 
-def mx_fc1_swiglu(xq, xsc, wq, wsc, offs):
+def mx_fc1_swiglu(xq, xsc, wq, wsc, offs, want_z=False):
     """FC1 + SwiGLU on MX operands (``wq [E, 2F, D]``, wi transposed);
-    returns h fp32 [R, F]."""
+    returns h fp32 [R, F], or (h, z) with z bf16 bits [R, 2F] when
+    ``want_z``."""
     xq, xsc = _c(xq, np.uint8), _c(xsc, np.uint8)
     wq, wsc = _c(wq, np.uint8), _c(wsc, np.uint8)
     offs = _c(offs, np.int32)
@@ -316,9 +321,10 @@ def mx_fc1_swiglu(xq, xsc, wq, wsc, offs):
     F = N // 2
     R = int(offs[E])
     h = np.zeros((R, F), np.float32)
-    _check(lib().oracle_mx_fc1_swiglu(_p(xq), _p(xsc), _p(wq), _p(wsc), _p(offs), E, D, F, _p(h)),
-           "mx_fc1")
-    return h
+    z = np.zeros((R, N), np.uint16) if want_z else None
+    _check(lib().oracle_mx_fc1_swiglu(_p(xq), _p(xsc), _p(wq), _p(wsc), _p(offs), E, D, F, _p(h),
+                                      _p(z)), "mx_fc1")
+    return (h, z) if want_z else h
 
 
 def mx_fc2(hq, hsc, wq, wsc, offs):
@@ -350,6 +356,80 @@ def mx_weights(wi, wo):
             oq.reshape(E, D, F), osc.reshape(E, D, F // 32))
 
 
+def mx_weights_bwd(wi, wo):
+    """MX operands of the expert weights for the dgrads, quantized along
+    their last axis (the dgrads' contraction axis), in their own layout:
+    wi [E, D, 2F] -> (q [E, D, 2F], sc [E, D, 2F/32]); wo [E, F, D] ->
+    (q [E, F, D], sc [E, F, D/32])."""
+    wi = np.asarray(wi, np.uint16)
+    wo = np.asarray(wo, np.uint16)
+    E, D, N = wi.shape
+    F = wo.shape[1]
+    iq, isc = mx_quantize(bf16_to_f32(wi).reshape(E * D, N))
+    oq, osc = mx_quantize(bf16_to_f32(wo).reshape(E * F, D))
+    return (iq.reshape(E, D, N), isc.reshape(E, D, N // 32),
+            oq.reshape(E, F, D), osc.reshape(E, F, D // 32))
+
+
+def mx_quantize_tokens(x, offs):
+    """MX quantization of ``x`` fp32 [R, C] along the tokens of each group
+    (blocks of 32 rows from the group's first row): returns (q [R, C],
+    sc [NB, C], boff [E+1])."""
+    x = _c(x, np.float32)
+    offs = _c(offs, np.int32)
+    R, C = x.shape
+    E = len(offs) - 1
+    sizes = np.diff(offs.astype(np.int64))
+    NB = int(((sizes + 31) // 32).sum())
+    q = np.zeros((R, C), np.uint8)
+    sc = np.zeros((NB, C), np.uint8)
+    boff = np.zeros(E + 1, np.int32)
+    _check(lib().oracle_mx_quantize_tokens(_p(x), _p(offs), E, C, _p(q), _p(sc), _p(boff)),
+           "mx_quantize_tokens")
+    return q, sc, boff
+
+
+def mx_dequantize_tokens(q, sc, offs, boff) -> np.ndarray:
+    """float64 values of token-quantized codes ``q [R, C]``."""
+    offs = np.asarray(offs, np.int64)
+    R = int(offs[-1])
+    blk = np.zeros(R, np.int64)
+    for e in range(len(offs) - 1):
+        r = np.arange(offs[e], offs[e + 1])
+        blk[r] = boff[e] + (r - offs[e]) // 32
+    return e4m3_lut()[np.asarray(q, np.uint8)] * np.exp2(np.asarray(sc, np.int64)[blk] - 127)
+
+
+def mx_wgrad(a, b, offs):
+    """Weight gradient out[e] = A_e^T B_e on token-quantized operands
+    ``a = (aq, asc, boff)`` [R, Ca] and ``b`` [R, Cb] (from
+    :func:`mx_quantize_tokens` with the same offsets); returns bf16 bits
+    [E, Ca, Cb]."""
+    aq, asc, boff = _c(a[0], np.uint8), _c(a[1], np.uint8), _c(a[2], np.int32)
+    bq, bsc = _c(b[0], np.uint8), _c(b[1], np.uint8)
+    offs = _c(offs, np.int32)
+    E = len(offs) - 1
+    Ca, Cb = aq.shape[1], bq.shape[1]
+    out = np.zeros((E, Ca, Cb), np.uint16)
+    _check(lib().oracle_mx_wgrad(_p(aq), _p(asc), _p(bq), _p(bsc), _p(offs), _p(boff), E, Ca, Cb,
+                                 _p(out)), "mx_wgrad")
+    return out
+
+
+def mx_fc2_dgrad_swiglu(dq, dsc, wq, wsc, z, offs):
+    """FC2 dgrad (``wq [E, F, D]``: wo quantized along D) followed by the
+    SwiGLU backward at ``z`` bf16 [R, 2F]; returns dz bf16 bits [R, 2F]."""
+    dq, dsc = _c(dq, np.uint8), _c(dsc, np.uint8)
+    wq, wsc = _c(wq, np.uint8), _c(wsc, np.uint8)
+    z, offs = _c(z, np.uint16), _c(offs, np.int32)
+    E, F, D = wq.shape
+    R = int(offs[E])
+    dz = np.zeros((R, 2 * F), np.uint16)
+    _check(lib().oracle_mx_fc2_dgrad_swiglu(_p(dq), _p(dsc), _p(wq), _p(wsc), _p(z), _p(offs), E,
+                                            D, F, _p(dz)), "mx_fc2_dgrad_swiglu")
+    return dz
+
+
 def mx_block_forward(inp: dict) -> dict:
     """The MXFP8 forward in order: route, histogram, permute + quantize of
     the sorted rows, FC1 + SwiGLU on MX operands, quantize h, FC2 on MX
@@ -364,13 +444,42 @@ def mx_block_forward(inp: dict) -> dict:
     xs = permute(inp["x"], pos)
     xq, xsc = mx_quantize(bf16_to_f32(xs))
     wq, wsc, oq, osc = mx_weights(inp["wi"], inp["wo"])
-    h = mx_fc1_swiglu(xq, xsc, wq, wsc, off)
+    h, z = mx_fc1_swiglu(xq, xsc, wq, wsc, off, want_z=True)
     hq, hsc = mx_quantize(h)
     ys = mx_fc2(hq, hsc, oq, osc, off)
     out = combine(ys, w, pos, T, D)
     return dict(ids=ids, w=w, group_sizes=gs, group_offsets=off, pos=pos, row_src=row_src,
-                xq=xq, xsc=xsc, wq=wq, wsc=wsc, oq=oq, osc=osc, h=h, hq=hq, hsc=hsc, ys=ys,
-                out=out)
+                xs=xs, xq=xq, xsc=xsc, wq=wq, wsc=wsc, oq=oq, osc=osc, h=h, z=z, hq=hq,
+                hsc=hsc, ys=ys, out=out)
+
+
+def mx_block_backward(inp: dict, fwd: dict) -> dict:
+    """The MXFP8 backward in order, after :func:`mx_block_forward`: combine
+    backward (bf16, as in the bf16 block); dys quantized along D and wo along
+    D for the FC2 dgrad, whose output passes through the SwiGLU backward;
+    dz quantized along 2F and wi along 2F for the FC1 dgrad; permute
+    backward; then xs, h (both as the bf16 copies the block keeps), dys and
+    dz quantized along the tokens of each group for the two wgrads."""
+    wl = inp["workload"]
+    T, D = wl.T, wl.D
+    off = fwd["group_offsets"]
+    dys, dw = combine_bwd(inp["dy"], fwd["ys"], fwd["w"], fwd["pos"])
+    dq, dsc = mx_quantize(bf16_to_f32(dys))
+    iq, isc, oq, osc = mx_weights_bwd(inp["wi"], inp["wo"])
+    dz = mx_fc2_dgrad_swiglu(dq, dsc, oq, osc, fwd["z"], off)
+    dzq, dzsc = mx_quantize(bf16_to_f32(dz))
+    dxs = mx_fc2(dzq, dzsc, iq, isc, off)
+    dx = permute_bwd(dxs, fwd["pos"], T, D)
+    hb = f32_to_bf16(fwd["h"])
+    xt = mx_quantize_tokens(bf16_to_f32(fwd["xs"]), off)
+    ht = mx_quantize_tokens(bf16_to_f32(hb), off)
+    dyt = mx_quantize_tokens(bf16_to_f32(dys), off)
+    dzt = mx_quantize_tokens(bf16_to_f32(dz), off)
+    dwo = mx_wgrad(ht, dyt, off)
+    dwi = mx_wgrad(xt, dzt, off)
+    return dict(dys=dys, dw=dw, dq=dq, dsc=dsc, wiq_b=iq, wisc_b=isc, woq_b=oq, wosc_b=osc,
+                dz=dz, dzq=dzq, dzsc=dzsc, dxs=dxs, dx=dx, hb=hb, xt=xt, ht=ht, dyt=dyt,
+                dzt=dzt, dwo=dwo, dwi=dwi)
 
 
 # ------------------------------------------------------- whole-block drivers

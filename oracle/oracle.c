@@ -475,7 +475,7 @@ static void mx_row(const uint8_t* q, const uint8_t* sc, int n, double* out) {
  * h[r,f] = fp32(silu(a[f]) * a[F+f]). */
 int oracle_mx_fc1_swiglu(const uint8_t* xq, const uint8_t* xsc, const uint8_t* wq,
                          const uint8_t* wsc, const int32_t* offs, int E, int D, int F,
-                         float* h) {
+                         float* h, uint16_t* z) {
   if (E <= 0 || D <= 0 || F <= 0 || D % 32 != 0) return -1;
   const int N = 2 * F, R = offs[E], nb = D / 32;
 #pragma omp parallel
@@ -499,6 +499,8 @@ int oracle_mx_fc1_swiglu(const uint8_t* xq, const uint8_t* xsc, const uint8_t* w
         const double g = a[f], u = a[F + f];
         h[(size_t)r * F + f] = (float)((g / (1.0 + exp(-g))) * u);
       }
+      if (z)
+        for (int n = 0; n < N; ++n) z[(size_t)r * N + n] = RN((float)a[n]);
     }
     free(xr);
     free(wr);
@@ -531,6 +533,128 @@ int oracle_mx_fc2(const uint8_t* hq, const uint8_t* hsc, const uint8_t* wq, cons
       }
     }
     free(hr);
+    free(wr);
+  }
+  return 0;
+}
+
+/* Elementwise RN of n fp32 values to bf16 bit patterns. */
+int oracle_f32_to_bf16_array(const float* x, long n, uint16_t* out) {
+  if (n < 0) return -1;
+  for (long i = 0; i < n; ++i) out[i] = RN(x[i]);
+  return 0;
+}
+
+/* ---------------------------------------------------------- MXFP8 backward
+ * [TE MoE, Changes item 1: the block takes MXFP8 quantization in training;
+ * Flowchart: the grouped GEMMs of the forward and of the backward].  Read
+ * as: every GEMM of the backward takes both operands as MXFP8 with blocks
+ * along its own contraction axis:
+ *   FC2 dgrad  dh[r,f]    = sum_d dys[r,d] * wo[e,f,d]   dys along D, wo along its last axis;
+ *   FC1 dgrad  dxs[r,d]   = sum_n dz[r,n] * wi[e,d,n]    dz along 2F, wi along its last axis
+ *              (the form of oracle_mx_fc2 with wq = wi [E, D, 2F]);
+ *   wgrads     dwo[e,f,d] = sum_{r in e} h[r,f] * dys[r,d],
+ *              dwi[e,d,n] = sum_{r in e} xs[r,d] * dz[r,n]   both along the tokens of group e.
+ * What is quantized is what the bf16 block keeps for its backward (xs, and
+ * h and z rounded to bf16) and the bf16 gradients dys and dz. */
+
+/* Token-axis quantization within groups: the rows of group e are cut into
+ * blocks of 32 from its first row (its last block shorter); for each column
+ * c the rows of one block share a scale, computed from those rows only (a
+ * short block is as if padded with zeros).  x fp32 [R, C] -> q [R, C]
+ * codes and sc [NB, C] scales, where block b of group e is scale row
+ * boff[e] + b and boff[e] = sum_{e' < e} ceil(size_e' / 32) (boff [E+1] is
+ * written; NB = boff[E]). */
+int oracle_mx_quantize_tokens(const float* x, const int32_t* offs, int E, int C, uint8_t* q,
+                              uint8_t* sc, int32_t* boff) {
+  if (E <= 0 || C <= 0) return -1;
+  boff[0] = 0;
+  for (int e = 0; e < E; ++e) boff[e + 1] = boff[e] + (offs[e + 1] - offs[e] + 31) / 32;
+  const int NB = boff[E];
+#pragma omp parallel for schedule(dynamic, 4)
+  for (int gb = 0; gb < NB; ++gb) {
+    int e = 0;
+    while (boff[e + 1] <= gb) ++e;
+    const int r0 = offs[e] + 32 * (gb - boff[e]);
+    const int n = offs[e + 1] - r0 < 32 ? offs[e + 1] - r0 : 32;
+    float v[32];
+    for (int c = 0; c < C; ++c) {
+      for (int i = 0; i < n; ++i) v[i] = x[(size_t)(r0 + i) * C + c];
+      const int s = mx_shared_exp(v, n);
+      sc[(size_t)gb * C + c] = (uint8_t)(s + 127);
+      for (int i = 0; i < n; ++i)
+        q[(size_t)(r0 + i) * C + c] = oracle_f64_to_e4m3(ldexp((double)v[i], -s));
+    }
+  }
+  return 0;
+}
+
+/* Weight gradient on operands quantized along tokens:
+ *   out[e,i,j] = bf16(fp32(sum_{r in group e, ascending} A[r,i] * B[r,j]))
+ * of the dequantized values (float64 sum), zero for an empty group.
+ * A = (aq [R, Ca], asc [NB, Ca]) and B = (bq [R, Cb], bsc [NB, Cb]), both
+ * from oracle_mx_quantize_tokens with these offsets (boff its output). */
+int oracle_mx_wgrad(const uint8_t* aq, const uint8_t* asc, const uint8_t* bq, const uint8_t* bsc,
+                    const int32_t* offs, const int32_t* boff, int E, int Ca, int Cb,
+                    uint16_t* out) {
+  if (E <= 0 || Ca <= 0 || Cb <= 0) return -1;
+  double val[256], p2[256];
+  for (int c = 0; c < 256; ++c) {
+    val[c] = oracle_e4m3_to_f64((uint8_t)c);
+    p2[c] = ldexp(1.0, c - 127);
+  }
+#pragma omp parallel
+  {
+    double* acc = (double*)malloc(sizeof(double) * (size_t)Cb);
+#pragma omp for collapse(2) schedule(dynamic, 4)
+    for (int e = 0; e < E; ++e)
+      for (int i = 0; i < Ca; ++i) {
+        for (int j = 0; j < Cb; ++j) acc[j] = 0.0;
+        for (int r = offs[e]; r < offs[e + 1]; ++r) {
+          const size_t blk = (size_t)boff[e] + (size_t)((r - offs[e]) / 32);
+          const double a = val[aq[(size_t)r * Ca + i]] * p2[asc[blk * Ca + i]];
+          for (int j = 0; j < Cb; ++j)
+            acc[j] += a * (val[bq[(size_t)r * Cb + j]] * p2[bsc[blk * Cb + j]]);
+        }
+        for (int j = 0; j < Cb; ++j) out[((size_t)e * Ca + i) * Cb + j] = RN((float)acc[j]);
+      }
+    free(acc);
+  }
+  return 0;
+}
+
+/* FC2 dgrad with the SwiGLU backward on MX operands: per row r of group e,
+ *   dh[r,f] = fp32(sum_d dys[r,d] * wo[e,f,d]) of the dequantized values
+ * (float64 sum; dq/dsc = dys [R, D] with blocks along D, wq/wsc = wo
+ * [E, F, D] with blocks along D), then dz[r,f], dz[r,F+f] =
+ * bf16(swiglu_bwd(dh, z[r,f], z[r,F+f])) as in oracle_fc2_bwd. */
+int oracle_mx_fc2_dgrad_swiglu(const uint8_t* dq, const uint8_t* dsc, const uint8_t* wq,
+                               const uint8_t* wsc, const uint16_t* z, const int32_t* offs, int E,
+                               int D, int F, uint16_t* dz) {
+  if (E <= 0 || D <= 0 || F <= 0 || D % 32 != 0) return -1;
+  const int R = offs[E], nb = D / 32;
+#pragma omp parallel
+  {
+    double* dr = (double*)malloc(sizeof(double) * (size_t)D);
+    double* wr = (double*)malloc(sizeof(double) * (size_t)D);
+#pragma omp for schedule(dynamic, 4)
+    for (int r = 0; r < R; ++r) {
+      int e = 0;
+      while (offs[e + 1] <= r) ++e;
+      mx_row(dq + (size_t)r * D, dsc + (size_t)r * nb, D, dr);
+      for (int f = 0; f < F; ++f) {
+        const size_t wrow = (size_t)e * F + f;
+        mx_row(wq + wrow * D, wsc + wrow * nb, D, wr);
+        double acc = 0.0;
+        for (int d = 0; d < D; ++d) acc += dr[d] * wr[d];
+        float dg, du;
+        swiglu_bwd_one((float)acc, BF(z[(size_t)r * 2 * F + f]), BF(z[(size_t)r * 2 * F + F + f]),
+                       &dg, &du);
+        dz[(size_t)r * 2 * F + f] = RN(dg);
+        dz[(size_t)r * 2 * F + F + f] = RN(du);
+      }
+    }
+    free(dr);
     free(wr);
   }
   return 0;

@@ -82,14 +82,41 @@ int oracle_mx_quantize(const float* x, int rows, int K, uint8_t* q, uint8_t* sc)
 /* FC1 + SwiGLU on MX operands: xq/xsc [R, D] / [R, D/32]; wq/wsc are wi
  * transposed, [E, 2F, D] / [E, 2F, D/32] (row n = output column n; gate =
  * rows [0,F), up = [F,2F)).  h fp32 [R, F] = fp32(silu(g) * u) of the
- * float64 sums. */
+ * float64 sums; z (may be NULL) bf16 [R, 2F] = bf16(fp32(sum)) of every
+ * output column, kept for the backward. */
 int oracle_mx_fc1_swiglu(const uint8_t* xq, const uint8_t* xsc, const uint8_t* wq,
                          const uint8_t* wsc, const int32_t* group_offsets, int E, int D, int F,
-                         float* h);
+                         float* h, uint16_t* z);
 /* FC2 on MX operands: hq/hsc [R, F] / [R, F/32]; wq/wsc are wo transposed,
  * [E, D, F] / [E, D, F/32].  ys bf16 [R, D] = bf16(fp32(sum)). */
 int oracle_mx_fc2(const uint8_t* hq, const uint8_t* hsc, const uint8_t* wq, const uint8_t* wsc,
                   const int32_t* group_offsets, int E, int F, int D, uint16_t* ys);
+int oracle_f32_to_bf16_array(const float* x, long n, uint16_t* out);
+
+/*
+ * MXFP8 backward [TE MoE, Changes item 1; Flowchart].  Every GEMM of the
+ * backward on MX operands with blocks along its own contraction axis: the
+ * dgrads take the gradient rows (blocks along the row) and the weight
+ * quantized along its last axis; the wgrads take both operands quantized
+ * along the tokens of each group, in blocks of 32 rows from the group's
+ * first row (a group's last block may be short).  The quantized tensors are
+ * the bf16 ones the block keeps (xs, h, z) and the bf16 gradients.
+ */
+/* x fp32 [R, C] -> q [R, C], sc [NB, C], boff [E+1]: block b of group e
+ * covers rows offs[e] + 32b .. min(offs[e] + 32b + 32, offs[e+1]) and its
+ * scales are row boff[e] + b of sc, boff[e] = sum_{e'<e} ceil(size_e'/32). */
+int oracle_mx_quantize_tokens(const float* x, const int32_t* group_offsets, int E, int C,
+                              uint8_t* q, uint8_t* sc, int32_t* boff);
+/* out bf16 [E, Ca, Cb] = bf16(fp32(sum_{r in group e} A[r,i] * B[r,j])) on
+ * token-quantized A [R, Ca] and B [R, Cb]; zero for an empty group. */
+int oracle_mx_wgrad(const uint8_t* aq, const uint8_t* asc, const uint8_t* bq, const uint8_t* bsc,
+                    const int32_t* group_offsets, const int32_t* boff, int E, int Ca, int Cb,
+                    uint16_t* out);
+/* dz bf16 [R, 2F] = SwiGLU backward of dh = fp32(sum_d dys[r,d] * wo[e,f,d])
+ * (dys [R, D] and wo [E, F, D] both with blocks along D) at z bf16 [R, 2F]. */
+int oracle_mx_fc2_dgrad_swiglu(const uint8_t* dq, const uint8_t* dsc, const uint8_t* wq,
+                               const uint8_t* wsc, const uint16_t* z,
+                               const int32_t* group_offsets, int E, int D, int F, uint16_t* dz);
 
 #ifdef __cplusplus
 }

@@ -478,8 +478,151 @@ def check_mx_gemms(orc):
     assert np.array_equal(ys, want_ys), "MX FC2 differs from the float64 matmul rounded to bf16"
 
 
+def _e4m3_decode_torch(q):
+    """Values of E4M3 codes as torch's float8_e4m3fn reads them."""
+    t = torch.from_numpy(np.ascontiguousarray(q, np.uint8))
+    return t.view(torch.float8_e4m3fn).double().numpy()
+
+
+def _dequant_rows(q, sc):
+    """float64 values of row-quantized codes (blocks of 32 along the last axis)."""
+    return _e4m3_decode_torch(q) * np.exp2(np.repeat(sc.astype(np.float64) - 127, 32, axis=-1))
+
+
+def _token_blocks(sizes):
+    """Scale row of every row of the groups: group e's rows in blocks of 32
+    from its first row, the groups' blocks numbered in order."""
+    blk, nb = [], 0
+    for s in sizes:
+        blk += [nb + i // 32 for i in range(s)]
+        nb += -(-s // 32)
+    return np.array(blk, np.int64), nb
+
+
+def check_mx_quantize_tokens(orc):
+    """Token-axis MX quantization against the row quantization by library
+    routines (frexp, torch's E4M3) of each group's 32-row blocks, transposed
+    and padded with zero rows when short; the block index restarts at every
+    group (short last blocks, an empty group and an exact multiple of 32)."""
+    rng = _rng(44)
+    sizes = [33, 0, 64, 1, 70]
+    offs = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+    R, C = int(offs[-1]), 64
+    # row magnitudes spread over 2^-6 .. 2^5, so that a block's scale depends
+    # on which rows it holds
+    x = (rng.standard_normal((R, C)) * np.exp2(rng.integers(-6, 6, (R, 1)))).astype(np.float32)
+    q, sc, boff = orc.mx_quantize_tokens(x, offs)
+    blk, nb = _token_blocks(sizes)
+    assert np.array_equal(boff, np.concatenate([[0], np.cumsum([-(-s // 32) for s in sizes])])), \
+        "token block offsets differ from the prefix of ceil(size / 32)"
+    assert sc.shape == (nb, C)
+    for b in range(nb):
+        rows = np.nonzero(blk == b)[0]
+        pad = np.zeros((C, 32), np.float32)
+        pad[:, :len(rows)] = x[rows].T
+        rq, rsc = _mx_quantize_ref(pad)
+        assert np.array_equal(sc[b], rsc[:, 0]), f"token block {b}: scales differ"
+        assert np.array_equal(q[rows].T, rq[:, :len(rows)]), f"token block {b}: codes differ"
+
+
+def check_mx_wgrad(orc):
+    """The MX weight gradient against float64 matmuls, per group, of the
+    operands dequantized by torch's E4M3 reading and the per-row block
+    scales, rounded to bf16 by torch; an empty group gives zeros."""
+    rng = _rng(45)
+    sizes = [33, 0, 40, 1, 64]
+    offs = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+    R, Ca, Cb = int(offs[-1]), 64, 96
+    a = (rng.standard_normal((R, Ca)) * np.exp2(rng.integers(-4, 4, (R, 1)))).astype(np.float32)
+    b = rng.standard_normal((R, Cb)).astype(np.float32)
+    at, bt = orc.mx_quantize_tokens(a, offs), orc.mx_quantize_tokens(b, offs)
+    out = orc.mx_wgrad(at, bt, offs)
+    blk, _ = _token_blocks(sizes)
+    A = _e4m3_decode_torch(at[0]) * np.exp2(at[1][blk].astype(np.float64) - 127)
+    Bm = _e4m3_decode_torch(bt[0]) * np.exp2(bt[1][blk].astype(np.float64) - 127)
+    want = np.stack([A[offs[e]:offs[e + 1]].T @ Bm[offs[e]:offs[e + 1]]
+                     for e in range(len(sizes))])
+    want = f32_to_bf16_bits_torch(want.astype(np.float32))
+    assert np.array_equal(out, want), "MX wgrad differs from the per-group float64 matmul"
+    assert not out[1].any(), "an empty group's weight gradient must be zero"
+
+
+def check_mx_dgrads(orc):
+    """The MX dgrads: weights quantized along their last axis (against the
+    library-routine row quantization), the FC2 dgrad + SwiGLU backward
+    against a float64 matmul and torch autograd of silu(g) * u, and the FC1
+    dgrad (the same contraction form as FC2) against a float64 matmul
+    rounded to bf16 by torch."""
+    rng = _rng(46)
+    E, D, F = 3, 64, 32
+    offs, ids = _random_grouped_rows(rng, 40, E, empty=(1,))
+    R = int(offs[-1])
+    wi = _bf16(rng, (E, D, 2 * F), 0.1)
+    wo = _bf16(rng, (E, F, D), 0.1)
+    iq, isc, oq, osc = orc.mx_weights_bwd(wi, wo)
+    rq, rsc = _mx_quantize_ref(bits_to_f64(wo).reshape(E * F, D).astype(np.float32))
+    assert np.array_equal(oq.reshape(E * F, D), rq) and np.array_equal(osc.reshape(E * F, -1), rsc)
+    rq, rsc = _mx_quantize_ref(bits_to_f64(wi).reshape(E * D, 2 * F).astype(np.float32))
+    assert np.array_equal(iq.reshape(E * D, 2 * F), rq) and np.array_equal(isc.reshape(E * D, -1), rsc)
+    dq, dsc = orc.mx_quantize(rng.standard_normal((R, D)).astype(np.float32))
+    z = _bf16(rng, (R, 2 * F), 2.0)
+    dz = orc.mx_fc2_dgrad_swiglu(dq, dsc, oq, osc, z, offs)
+    dh = np.einsum("rd,rfd->rf", _dequant_rows(dq, dsc), _dequant_rows(oq, osc)[ids])
+    dh = dh.astype(np.float32).astype(np.float64)
+    zv = bits_to_f64(z)
+    G = torch.tensor(zv[:, :F], requires_grad=True)
+    Uu = torch.tensor(zv[:, F:], requires_grad=True)
+    (torch.nn.functional.silu(G) * Uu).backward(torch.tensor(dh))
+    want = np.concatenate([G.grad.numpy(), Uu.grad.numpy()], axis=1)
+    assert max_excess(bits_to_f64(dz), want, U, 1e-6 * np.abs(want).max()) <= 0, \
+        "MX FC2 dgrad + SwiGLU backward differs"
+    dzq, dzsc = orc.mx_quantize(bits_to_f64(dz).astype(np.float32))
+    dxs = orc.mx_fc2(dzq, dzsc, iq, isc, offs)
+    want = np.einsum("rn,rdn->rd", _dequant_rows(dzq, dzsc), _dequant_rows(iq, isc)[ids])
+    assert np.array_equal(dxs, f32_to_bf16_bits_torch(want.astype(np.float32))), \
+        "MX FC1 dgrad differs from the float64 matmul rounded to bf16"
+
+
+def check_mx_block_backward(orc):
+    """The MX forward + backward drivers end to end against torch autograd
+    of the float64 dense block (per token, its top-k experts): the MX
+    results stay within the format's error in relative norm (E4M3 keeps 3
+    significand bits), the routing-weight gradient too; and z is the FC1
+    pre-activation whose SwiGLU is h."""
+    from types import SimpleNamespace
+    logits, b, x, wi, wo, dy = _tiny_block(47, T=100, D=64, E=4, K=2, F=32)
+    wl = SimpleNamespace(T=100, D=64, E=4, K=2, F=32, score_mode=0)
+    inp = dict(workload=wl, logits=logits, bias=b, x=x, wi=wi, wo=wo, dy=dy)
+    f = orc.mx_block_forward(inp)
+    g = orc.mx_block_backward(inp, f)
+    zv = bits_to_f64(f["z"])
+    with np.errstate(over="ignore"):
+        hz = zv[:, :32] / (1 + np.exp(-zv[:, :32])) * zv[:, 32:]
+    # z is rounded to bf16: silu(g) * u from it is within a few bf16 ulps of h
+    assert np.linalg.norm(f["h"] - hz) <= 4 * U * np.linalg.norm(hz), \
+        "z is not FC1's pre-activation"
+    X = torch.tensor(bits_to_f64(x), requires_grad=True)
+    WI = torch.tensor(bits_to_f64(wi), requires_grad=True)
+    WO = torch.tensor(bits_to_f64(wo), requires_grad=True)
+    W = torch.tensor(f["w"].astype(np.float64), requires_grad=True)
+    ref = dense_block(X, WI, WO, torch.from_numpy(f["ids"]), W)
+    (ref * torch.tensor(bits_to_f64(dy))).sum().backward()
+
+    def rel(got, want):
+        return np.linalg.norm(got - want) / np.linalg.norm(want)
+
+    # measured: 0.07-0.08 for each (several E4M3 roundings compound); a
+    # transposed operand, a swapped half or a misplaced block gives ~1
+    assert rel(bits_to_f64(f["out"]), ref.detach().numpy()) < 0.12, "MX out vs dense"
+    for name, gr in (("dx", X.grad), ("dwi", WI.grad), ("dwo", WO.grad), ("dw", W.grad)):
+        got = g[name] if name == "dw" else bits_to_f64(g[name])
+        r = rel(got, gr.numpy())
+        assert r < 0.12, f"MX {name} vs dense autograd: relative error {r:.3f}"
+
+
 ALL_CHECKS = [check_bf16_rounding, check_route, check_histogram, check_permute_combine,
               check_combine_bwd, check_fc1_fc2, check_swiglu_closed_forms,
               check_dense_special_case, check_gemm_backward, check_block_against_dense,
               check_finite_differences, check_e4m3_decode, check_e4m3_encode, check_mx_quantize,
-              check_mx_gemms]
+              check_mx_gemms, check_mx_quantize_tokens, check_mx_wgrad, check_mx_dgrads,
+              check_mx_block_backward]

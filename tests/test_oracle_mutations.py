@@ -68,6 +68,22 @@ MUTATIONS = {
     "mx_fc2_first_expert_only": ("const size_t wrow = (size_t)e * D + d;",
                                  "const size_t wrow = (size_t)0 * D + d;"),
     "mx_zero_block_scale": ("if (amax == 0.0) return -127;", "if (amax == 0.0) return 0;"),
+    "mx_z_gate_up_swapped": ("z[(size_t)r * N + n] = RN((float)a[n]);",
+                             "z[(size_t)r * N + n] = RN((float)a[(n + F) % N]);"),
+    "mx_tok_short_block_dropped": ("boff[e + 1] = boff[e] + (offs[e + 1] - offs[e] + 31) / 32;",
+                                   "boff[e + 1] = boff[e] + (offs[e + 1] - offs[e]) / 32;"),
+    "mx_tok_block_origin_global": ("const int r0 = offs[e] + 32 * (gb - boff[e]);",
+                                   "const int r0 = 32 * (offs[e] / 32) + 32 * (gb - boff[e]);"),
+    "mx_tok_scale_axis": ("sc[(size_t)gb * C + c] = (uint8_t)(s + 127);",
+                          "sc[((size_t)c * NB + gb) % ((size_t)NB * C)] = (uint8_t)(s + 127);"),
+    "mx_wgrad_block_index": ("(size_t)((r - offs[e]) / 32)", "(size_t)((r - offs[e]) / 64)"),
+    "mx_wgrad_first_row_dropped": ("for (int r = offs[e]; r < offs[e + 1]; ++r) {\n          const size_t blk",
+                                   "for (int r = offs[e] + 1; r < offs[e + 1]; ++r) {\n          const size_t blk"),
+    "mx_wgrad_b_scale_one_column": ("p2[bsc[blk * Cb + j]]", "p2[bsc[blk * Cb]]"),
+    "mx_dgrad_gate_up_swapped": ("swiglu_bwd_one((float)acc, BF(z[(size_t)r * 2 * F + f]), BF(z[(size_t)r * 2 * F + F + f]),",
+                                 "swiglu_bwd_one((float)acc, BF(z[(size_t)r * 2 * F + F + f]), BF(z[(size_t)r * 2 * F + f]),"),
+    "mx_dgrad_wrong_expert": ("const size_t wrow = (size_t)e * F + f;",
+                              "const size_t wrow = (size_t)((e + 1) % E) * F + f;"),
 }
 
 
