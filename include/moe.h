@@ -107,7 +107,9 @@ const char* moe_status_string(moe_status s);
 /* Version of this ABI; lets a loader check the library it opened without
  * touching a GPU.  2: adds the MXFP8 entry points (moe_mx_*) and the FC1
  * calls over expert ranges (moe_grouped_gemm_fc1_*_experts) to version 1's.
- * 3: adds moe_fused_forward. */
+ * 3: adds moe_fused_forward.  4: adds the MXFP8 backward (moe_mx_*_bwd,
+ * moe_mx_quantize_rows, moe_mx_quantize_tokens, the backward's MX buffers)
+ * and z to moe_mx_grouped_gemm_fc1_swiglu. */
 int moe_abi_version(void);
 
 /*
@@ -335,7 +337,24 @@ typedef enum {
   MOE_MX_WOQ = 4,  /* wo codes [E, D, F] */
   MOE_MX_WOSC = 5, /* wo scales [E, KB(F), 2*ceil(D/256), 512] */
   MOE_MX_HQ = 6,   /* hq codes [R, F] */
-  MOE_MX_HSC = 7   /* hq scales, tile-blocked, (ceil(R/128) + E) * KB(F) * 512 */
+  MOE_MX_HSC = 7,  /* hq scales, tile-blocked, (ceil(R/128) + E) * KB(F) * 512 */
+  /* backward (see the MXFP8 backward below) */
+  MOE_MX_DYQ = 8,        /* dys codes [R, D], blocks along D */
+  MOE_MX_DYSC = 9,       /* their scales, tile-blocked, TB * KB(D) * 512 */
+  MOE_MX_DZQ = 10,       /* dz codes [R, 2F], blocks along 2F */
+  MOE_MX_DZSC = 11,      /* tile-blocked, TB * KB(2F) * 512 */
+  MOE_MX_WIQ_BWD = 12,   /* wi codes [E, D, 2F], blocks along 2F */
+  MOE_MX_WISC_BWD = 13,  /* [E, KB(2F), 2*ceil(D/256), 512] */
+  MOE_MX_WOQ_BWD = 14,   /* wo codes [E, F, D], blocks along D */
+  MOE_MX_WOSC_BWD = 15,  /* [E, KB(D), 2*ceil(F/256), 512] */
+  MOE_MX_XT = 16,        /* xs along tokens: codes [D, Rp] */
+  MOE_MX_XTSC = 17,      /* [TB, 2*ceil(D/256), 512] */
+  MOE_MX_HT = 18,        /* h along tokens: codes [F, Rp] */
+  MOE_MX_HTSC = 19,      /* [TB, 2*ceil(F/256), 512] */
+  MOE_MX_DYT = 20,       /* dys along tokens: codes [D, Rp] */
+  MOE_MX_DYTSC = 21,     /* [TB, 2*ceil(D/256), 512] */
+  MOE_MX_DZT = 22,       /* dz along tokens: codes [2F, Rp] */
+  MOE_MX_DZTSC = 23      /* [TB, 2*ceil(2F/256), 512] */
 } moe_mx_buffer;
 
 /* Bytes of MX buffer `which` for dims d (0 for invalid dims or `which`). */
@@ -374,13 +393,14 @@ moe_status moe_mx_permute_quantize(const moe_bf16* x, const int32_t* pos,
  *   h[r,f] = fp32(silu(g_f) * u_f), written as MX codes hq [R,F] with the
  *   tile-blocked scales hsc (blocks along F: the A operand of the MX FC2)
  *   and/or as bf16 h [R,F].  hq/hsc (both or neither) and h may each be
- *   NULL, not all three.
+ *   NULL, not all three.  z (may be NULL) bf16 [R, 2F] = bf16(a) in wi's
+ *   column order [gate | up], kept for the backward.
  */
 moe_status moe_mx_grouped_gemm_fc1_swiglu(const uint8_t* xq, const uint8_t* xsc,
                                           const uint8_t* wq, const uint8_t* wsc,
                                           const int32_t* group_offsets, uint8_t* hq,
-                                          uint8_t* hsc, moe_bf16* h, int32_t* dev_status,
-                                          moe_dims d, cudaStream_t stream);
+                                          uint8_t* hsc, moe_bf16* h, moe_bf16* z,
+                                          int32_t* dev_status, moe_dims d, cudaStream_t stream);
 
 /*
  * FC2 on MX operands: ys[r,:] = bf16(sum_f h[r,f] * wo[e,f,:]) of the
@@ -392,6 +412,74 @@ moe_status moe_mx_grouped_gemm_fc2(const uint8_t* hq, const uint8_t* hsc, const 
                                    const uint8_t* wsc, const int32_t* group_offsets,
                                    moe_bf16* ys, int32_t* dev_status, moe_dims d,
                                    cudaStream_t stream);
+
+/*
+ * MXFP8 backward [TE MoE, Changes item 1: MXFP8 quantization in the MoE
+ * block, which trains; Flowchart].  Every backward GEMM takes both operands
+ * as MXFP8 with blocks along its own contraction axis (format and scale
+ * blocks as above):
+ *   FC2 dgrad  dh[r,f] = sum_d dys[r,d] * wo[e,f,d]: dys quantized along D
+ *              (moe_mx_quantize_rows), wo along its last axis
+ *              (moe_mx_quantize_wo_bwd); dh (fp32) goes straight into the
+ *              SwiGLU backward at z, giving dz bf16 [R, 2F] = [dgate | dup];
+ *   FC1 dgrad  dxs[r,d] = bf16(sum_n dz[r,n] * wi[e,d,n]): dz along 2F, wi
+ *              along its last axis (moe_mx_quantize_wi_bwd);
+ *   wgrads     dwo[e,f,d] = bf16(sum_{r in e} h[r,f] * dys[r,d]) and
+ *              dwi[e,d,n] = bf16(sum_{r in e} xs[r,d] * dz[r,n]): both
+ *              operands quantized along the tokens of each group
+ *              (moe_mx_quantize_tokens), in 32-row blocks from the group's
+ *              first row (a group's last block may be short; it is padded
+ *              with zeros); an expert without rows gets zeros.
+ * The quantized tensors are the bf16 ones the block keeps (xs, h, z) and
+ * the bf16 gradients (dys from moe_combine_bwd, dz).
+ *
+ * Layouts.  Weights quantized along their last axis keep their own layout,
+ * codes [E, N, k] (wi: N = D, k = 2F; wo: N = F, k = D), with scales
+ * [E, KB(k), NBp(N), 512] (the weight layout above without a transpose).
+ * Row-quantized gradients use the activation layout above (codes [R, C],
+ * tile-blocked scales).  Token-axis operands are stored transposed: with
+ * TB = ceil(R/128) + E tiles and Rp = 128 * TB, codes [C, Rp] where the
+ * rows of group e fill token columns 128 * tb[e] + i (i < size_e; tb as
+ * for tile-blocked scales; the rest of each tile is zero codes, and a
+ * 32-token step of padding only has the scale of a zero block, byte 0), and scales
+ * [TB, NBp(C), 512]: tile g's scales for rows c of block c / 128 are the
+ * block at ((g * NBp(C)) + c / 128) * 512, byte (c % 128 % 32) * 16 +
+ * (c % 128 / 32) * 4 + j for tokens [32j, 32j+32) of the tile.
+ */
+moe_status moe_mx_quantize_wi_bwd(const moe_bf16* wi, uint8_t* wq, uint8_t* wsc, moe_dims d,
+                                  cudaStream_t stream);
+moe_status moe_mx_quantize_wo_bwd(const moe_bf16* wo, uint8_t* wq, uint8_t* wsc, moe_dims d,
+                                  cudaStream_t stream);
+/* src bf16 [R, C] in expert-sorted order (C = D for dys, 2F for dz) -> q
+ * [R, C] codes and tile-blocked scales sc (blocks along C). */
+moe_status moe_mx_quantize_rows(const moe_bf16* src, int C, const int32_t* group_offsets,
+                                uint8_t* q, uint8_t* sc, moe_dims d, cudaStream_t stream);
+/* Token-axis quantization of src bf16 [R, C] in expert-sorted order, or,
+ * when row_src is given, of the token-major x [T, C] read at token
+ * row_src[r] / K for sorted row r (xs without its permuted copy).  C is D,
+ * F or 2F.  qt [C, Rp] and sct as described above. */
+moe_status moe_mx_quantize_tokens(const moe_bf16* src, const int32_t* row_src, int C,
+                                  const int32_t* group_offsets, uint8_t* qt, uint8_t* sct,
+                                  moe_dims d, cudaStream_t stream);
+/* FC2 backward: dz from (dyq, dysc) and (woq, wosc) of moe_mx_quantize_wo_bwd
+ * and z; dwo bf16 [E, F, D] from ht/htsc (h along tokens) and dyt/dytsc
+ * (dys along tokens).  dz and dwo may each be NULL (their inputs then too),
+ * not both. */
+moe_status moe_mx_grouped_gemm_fc2_bwd(const uint8_t* dyq, const uint8_t* dysc,
+                                       const uint8_t* woq, const uint8_t* wosc, const moe_bf16* z,
+                                       const uint8_t* ht, const uint8_t* htsc,
+                                       const uint8_t* dyt, const uint8_t* dytsc,
+                                       const int32_t* group_offsets, moe_bf16* dz, moe_bf16* dwo,
+                                       int32_t* dev_status, moe_dims d, cudaStream_t stream);
+/* FC1 backward: dxs bf16 [R, D] from (dzq, dzsc) and (wiq, wisc) of
+ * moe_mx_quantize_wi_bwd; dwi bf16 [E, D, 2F] from xt/xtsc (xs along
+ * tokens) and dzt/dztsc (dz along tokens).  Either output may be NULL. */
+moe_status moe_mx_grouped_gemm_fc1_bwd(const uint8_t* dzq, const uint8_t* dzsc,
+                                       const uint8_t* wiq, const uint8_t* wisc,
+                                       const uint8_t* xt, const uint8_t* xtsc,
+                                       const uint8_t* dzt, const uint8_t* dztsc,
+                                       const int32_t* group_offsets, moe_bf16* dxs, moe_bf16* dwi,
+                                       int32_t* dev_status, moe_dims d, cudaStream_t stream);
 
 /*
  * Fused forward for inference [Fused MoE Summary: gather, GMM1, activation

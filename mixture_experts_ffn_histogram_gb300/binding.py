@@ -34,11 +34,15 @@ ENTRY_POINTS = (
     "moe_mx_bytes", "moe_mx_quantize_wi", "moe_mx_quantize_wo", "moe_mx_permute_quantize",
     "moe_mx_grouped_gemm_fc1_swiglu", "moe_mx_grouped_gemm_fc2",
     "moe_grouped_gemm_fc1_swiglu_experts", "moe_grouped_gemm_fc1_bwd_experts",
-    "moe_fused_forward",
+    "moe_fused_forward", "moe_mx_quantize_wi_bwd", "moe_mx_quantize_wo_bwd",
+    "moe_mx_quantize_rows", "moe_mx_quantize_tokens", "moe_mx_grouped_gemm_fc2_bwd",
+    "moe_mx_grouped_gemm_fc1_bwd",
 )
 
 # moe_mx_buffer
-MX_XQ, MX_XSC, MX_WIQ, MX_WISC, MX_WOQ, MX_WOSC, MX_HQ, MX_HSC = range(8)
+(MX_XQ, MX_XSC, MX_WIQ, MX_WISC, MX_WOQ, MX_WOSC, MX_HQ, MX_HSC, MX_DYQ, MX_DYSC, MX_DZQ,
+ MX_DZSC, MX_WIQ_BWD, MX_WISC_BWD, MX_WOQ_BWD, MX_WOSC_BWD, MX_XT, MX_XTSC, MX_HT, MX_HTSC,
+ MX_DYT, MX_DYTSC, MX_DZT, MX_DZTSC) = range(24)
 
 # int32 capacity of the fixed scratch behind moe_route_histogram_noalloc
 NOALLOC_ROUTE_SCRATCH_INTS = 262144
@@ -105,8 +109,14 @@ def lib() -> ctypes.CDLL:
             "moe_mx_quantize_wi": ([P, P, P, D_, P], I),
             "moe_mx_quantize_wo": ([P, P, P, D_, P], I),
             "moe_mx_permute_quantize": ([P, P, P, P, P, D_, P], I),
-            "moe_mx_grouped_gemm_fc1_swiglu": ([P, P, P, P, P, P, P, P, P, D_, P], I),
+            "moe_mx_grouped_gemm_fc1_swiglu": ([P, P, P, P, P, P, P, P, P, P, D_, P], I),
             "moe_mx_grouped_gemm_fc2": ([P, P, P, P, P, P, P, D_, P], I),
+            "moe_mx_quantize_wi_bwd": ([P, P, P, D_, P], I),
+            "moe_mx_quantize_wo_bwd": ([P, P, P, D_, P], I),
+            "moe_mx_quantize_rows": ([P, I, P, P, P, D_, P], I),
+            "moe_mx_quantize_tokens": ([P, P, I, P, P, P, D_, P], I),
+            "moe_mx_grouped_gemm_fc2_bwd": ([P] * 13 + [D_, P], I),
+            "moe_mx_grouped_gemm_fc1_bwd": ([P] * 12 + [D_, P], I),
         }
         for name, (args, res) in sig.items():
             fn = getattr(L, name)
@@ -262,9 +272,9 @@ def moe_mx_permute_quantize(x, pos, group_offsets, xq, xsc, d: MoeDims, stream=N
 
 
 def moe_mx_grouped_gemm_fc1_swiglu(xq, xsc, wq, wsc, group_offsets, hq, hsc, h, dev_status,
-                                   d: MoeDims, stream=None):
+                                   d: MoeDims, stream=None, z=None):
     _ok("moe_mx_grouped_gemm_fc1_swiglu", lib().moe_mx_grouped_gemm_fc1_swiglu(
-        _p(xq), _p(xsc), _p(wq), _p(wsc), _p(group_offsets), _p(hq), _p(hsc), _p(h),
+        _p(xq), _p(xsc), _p(wq), _p(wsc), _p(group_offsets), _p(hq), _p(hsc), _p(h), _p(z),
         _p(dev_status), d, _s(stream)))
 
 
@@ -273,3 +283,37 @@ def moe_mx_grouped_gemm_fc2(hq, hsc, wq, wsc, group_offsets, ys, dev_status, d: 
     _ok("moe_mx_grouped_gemm_fc2", lib().moe_mx_grouped_gemm_fc2(
         _p(hq), _p(hsc), _p(wq), _p(wsc), _p(group_offsets), _p(ys), _p(dev_status), d,
         _s(stream)))
+
+
+def moe_mx_quantize_wi_bwd(wi, wq, wsc, d: MoeDims, stream=None):
+    _ok("moe_mx_quantize_wi_bwd", lib().moe_mx_quantize_wi_bwd(_p(wi), _p(wq), _p(wsc), d,
+                                                               _s(stream)))
+
+
+def moe_mx_quantize_wo_bwd(wo, wq, wsc, d: MoeDims, stream=None):
+    _ok("moe_mx_quantize_wo_bwd", lib().moe_mx_quantize_wo_bwd(_p(wo), _p(wq), _p(wsc), d,
+                                                               _s(stream)))
+
+
+def moe_mx_quantize_rows(src, C, group_offsets, q, sc, d: MoeDims, stream=None):
+    _ok("moe_mx_quantize_rows", lib().moe_mx_quantize_rows(
+        _p(src), int(C), _p(group_offsets), _p(q), _p(sc), d, _s(stream)))
+
+
+def moe_mx_quantize_tokens(src, row_src, C, group_offsets, qt, sct, d: MoeDims, stream=None):
+    _ok("moe_mx_quantize_tokens", lib().moe_mx_quantize_tokens(
+        _p(src), _p(row_src), int(C), _p(group_offsets), _p(qt), _p(sct), d, _s(stream)))
+
+
+def moe_mx_grouped_gemm_fc2_bwd(dyq, dysc, woq, wosc, z, ht, htsc, dyt, dytsc, group_offsets,
+                                dz, dwo, dev_status, d: MoeDims, stream=None):
+    _ok("moe_mx_grouped_gemm_fc2_bwd", lib().moe_mx_grouped_gemm_fc2_bwd(
+        _p(dyq), _p(dysc), _p(woq), _p(wosc), _p(z), _p(ht), _p(htsc), _p(dyt), _p(dytsc),
+        _p(group_offsets), _p(dz), _p(dwo), _p(dev_status), d, _s(stream)))
+
+
+def moe_mx_grouped_gemm_fc1_bwd(dzq, dzsc, wiq, wisc, xt, xtsc, dzt, dztsc, group_offsets, dxs,
+                                dwi, dev_status, d: MoeDims, stream=None):
+    _ok("moe_mx_grouped_gemm_fc1_bwd", lib().moe_mx_grouped_gemm_fc1_bwd(
+        _p(dzq), _p(dzsc), _p(wiq), _p(wisc), _p(xt), _p(xtsc), _p(dzt), _p(dztsc),
+        _p(group_offsets), _p(dxs), _p(dwi), _p(dev_status), d, _s(stream)))

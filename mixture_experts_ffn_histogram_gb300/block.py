@@ -149,19 +149,27 @@ class MoEBlock:
 
 
 class MoEBlockMX:
-    """The block's forward in MXFP8 (inference): the expert weights are
-    quantized once by ``set_weights``; each ``forward`` routes, quantizes the
-    tokens while permuting them, runs FC1 + SwiGLU and FC2 on the tensor
-    cores' block-scaled MMA (h quantized in FC1's epilogue) and combines.
-    Every buffer is allocated once, in the library's MX layouts."""
+    """The block in MXFP8.  ``set_weights`` quantizes the expert weights (for
+    the forward, and with ``train`` also along their other axis for the
+    dgrads); each ``forward`` routes, quantizes the tokens while permuting
+    them, runs FC1 + SwiGLU and FC2 on the tensor cores' block-scaled MMA (h
+    quantized in FC1's epilogue; with ``train`` also h and z in bf16) and
+    combines.  ``backward`` (train only): combine backward, the gradient
+    quantized along D and along tokens, the FC2 dgrad with the SwiGLU
+    backward and the dwo wgrad, dz quantized along 2F and along tokens, x
+    quantized along tokens straight from its token-major rows, the FC1
+    dgrad and the dwi wgrad, and the permute backward.  Every buffer is
+    allocated once, in the library's MX layouts."""
 
-    def __init__(self, T, D, E, K, F, score_mode=B.SCORE_SOFTMAX_TOPK, device="cuda"):
+    def __init__(self, T, D, E, K, F, score_mode=B.SCORE_SOFTMAX_TOPK, device="cuda",
+                 train=False):
         self.d = d = B.dims(T, D, E, K, F)
         self.T, self.D, self.E, self.K, self.F = T, D, E, K, F
         self.R = R = T * K
         self.mode = score_mode
+        self.train = train
         dev = torch.device(device)
-        i32 = torch.int32
+        i32, bf = torch.int32, torch.bfloat16
 
         def u8(which):
             return torch.empty(max(B.moe_mx_bytes(d, which), 16), dtype=torch.uint8, device=dev)
@@ -178,12 +186,34 @@ class MoEBlockMX:
         self.woq, self.wosc = u8(B.MX_WOQ), u8(B.MX_WOSC)
         self.xq, self.xsc = u8(B.MX_XQ), u8(B.MX_XSC)
         self.hq, self.hsc = u8(B.MX_HQ), u8(B.MX_HSC)
-        self.ys = torch.empty((R, D), dtype=torch.bfloat16, device=dev)
-        self.out = torch.empty((T, D), dtype=torch.bfloat16, device=dev)
+        self.ys = torch.empty((R, D), dtype=bf, device=dev)
+        self.out = torch.empty((T, D), dtype=bf, device=dev)
+        if train:
+            self.h = torch.empty((R, F), dtype=bf, device=dev)
+            self.z = torch.empty((R, 2 * F), dtype=bf, device=dev)
+            self.dys = torch.empty((R, D), dtype=bf, device=dev)
+            self.dw = torch.empty((T, K), dtype=torch.float32, device=dev)
+            self.dz = torch.empty((R, 2 * F), dtype=bf, device=dev)
+            self.dxs = torch.empty((R, D), dtype=bf, device=dev)
+            self.dx = torch.empty((T, D), dtype=bf, device=dev)
+            self.dwi = torch.empty((E, D, 2 * F), dtype=bf, device=dev)
+            self.dwo = torch.empty((E, F, D), dtype=bf, device=dev)
+            self.wiq_b, self.wisc_b = u8(B.MX_WIQ_BWD), u8(B.MX_WISC_BWD)
+            self.woq_b, self.wosc_b = u8(B.MX_WOQ_BWD), u8(B.MX_WOSC_BWD)
+            self.dyq, self.dysc = u8(B.MX_DYQ), u8(B.MX_DYSC)
+            self.dzq, self.dzsc = u8(B.MX_DZQ), u8(B.MX_DZSC)
+            self.xt, self.xtsc = u8(B.MX_XT), u8(B.MX_XTSC)
+            self.ht, self.htsc = u8(B.MX_HT), u8(B.MX_HTSC)
+            self.dyt, self.dytsc = u8(B.MX_DYT), u8(B.MX_DYTSC)
+            self.dzt, self.dztsc = u8(B.MX_DZT), u8(B.MX_DZTSC)
+        self.x = None
 
     def set_weights(self, wi, wo, stream=None):
         B.moe_mx_quantize_wi(wi, self.wiq, self.wisc, self.d, stream)
         B.moe_mx_quantize_wo(wo, self.woq, self.wosc, self.d, stream)
+        if self.train:
+            B.moe_mx_quantize_wi_bwd(wi, self.wiq_b, self.wisc_b, self.d, stream)
+            B.moe_mx_quantize_wo_bwd(wo, self.woq_b, self.wosc_b, self.d, stream)
 
     def forward(self, x, logits=None, bias=None, ids=None, w=None, stream=None):
         d = self.d
@@ -195,12 +225,37 @@ class MoEBlockMX:
                               d, stream)
         B.moe_mx_permute_quantize(x, self.pos, self.group_offsets, self.xq, self.xsc, d, stream)
         B.moe_mx_grouped_gemm_fc1_swiglu(self.xq, self.xsc, self.wiq, self.wisc,
-                                         self.group_offsets, self.hq, self.hsc, None,
-                                         self.status, d, stream)
+                                         self.group_offsets, self.hq, self.hsc,
+                                         self.h if self.train else None, self.status, d, stream,
+                                         z=self.z if self.train else None)
         B.moe_mx_grouped_gemm_fc2(self.hq, self.hsc, self.woq, self.wosc, self.group_offsets,
                                   self.ys, self.status, d, stream)
         B.moe_combine(self.ys, self.w, self.pos, self.out, d, stream)
+        self.x = x
         return self.out
+
+    def backward(self, dy, stream=None):
+        if not self.train:
+            raise RuntimeError("the block was built without train=True")
+        if self.x is None:
+            raise RuntimeError("backward needs a forward first")
+        d, D, F = self.d, self.D, self.F
+        offs = self.group_offsets
+        B.moe_combine_bwd(dy, self.ys, self.w, self.pos, self.dys, self.dw, d, stream)
+        B.moe_mx_quantize_rows(self.dys, D, offs, self.dyq, self.dysc, d, stream)
+        B.moe_mx_quantize_tokens(self.dys, None, D, offs, self.dyt, self.dytsc, d, stream)
+        B.moe_mx_quantize_tokens(self.h, None, F, offs, self.ht, self.htsc, d, stream)
+        B.moe_mx_grouped_gemm_fc2_bwd(self.dyq, self.dysc, self.woq_b, self.wosc_b, self.z,
+                                      self.ht, self.htsc, self.dyt, self.dytsc, offs, self.dz,
+                                      self.dwo, self.status, d, stream)
+        B.moe_mx_quantize_rows(self.dz, 2 * F, offs, self.dzq, self.dzsc, d, stream)
+        B.moe_mx_quantize_tokens(self.dz, None, 2 * F, offs, self.dzt, self.dztsc, d, stream)
+        B.moe_mx_quantize_tokens(self.x, self.row_src, D, offs, self.xt, self.xtsc, d, stream)
+        B.moe_mx_grouped_gemm_fc1_bwd(self.dzq, self.dzsc, self.wiq_b, self.wisc_b, self.xt,
+                                      self.xtsc, self.dzt, self.dztsc, offs, self.dxs, self.dwi,
+                                      self.status, d, stream)
+        B.moe_permute_bwd(self.dxs, self.pos, self.dx, d, stream)
+        return self.dx
 
 
 class HostPipeline:

@@ -86,7 +86,7 @@ const char* moe_status_string(moe_status s) {
   return "unknown status";
 }
 
-int moe_abi_version(void) { return 3; }
+int moe_abi_version(void) { return 4; }
 
 moe_status moe_route_histogram(const float* logits, const float* bias, moe_score_mode mode,
                                int32_t* ids, float* w, int32_t* group_sizes,
@@ -415,6 +415,26 @@ size_t moe_mx_bytes(moe_dims d, moe_mx_buffer which) {
     case MOE_MX_WOSC: return E * kbf * static_cast<size_t>(moe::mx_weight_row_blocks(d.D)) * 512;
     case MOE_MX_HQ: return R * F;
     case MOE_MX_HSC: return tiles * kbf * 512;
+    case MOE_MX_DYQ: return R * D;
+    case MOE_MX_DYSC: return tiles * kbd * 512;
+    case MOE_MX_DZQ: return R * 2 * F;
+    case MOE_MX_DZSC: return tiles * static_cast<size_t>(moe::mx_kblocks(2L * d.F)) * 512;
+    case MOE_MX_WIQ_BWD: return E * D * 2 * F;
+    case MOE_MX_WISC_BWD:
+      return E * static_cast<size_t>(moe::mx_kblocks(2L * d.F)) *
+             static_cast<size_t>(moe::mx_weight_row_blocks(d.D)) * 512;
+    case MOE_MX_WOQ_BWD: return E * F * D;
+    case MOE_MX_WOSC_BWD:
+      return E * kbd * static_cast<size_t>(moe::mx_weight_row_blocks(d.F)) * 512;
+    case MOE_MX_XT:
+    case MOE_MX_DYT: return D * static_cast<size_t>(moe::mx_token_cols(d));
+    case MOE_MX_HT: return F * static_cast<size_t>(moe::mx_token_cols(d));
+    case MOE_MX_DZT: return 2 * F * static_cast<size_t>(moe::mx_token_cols(d));
+    case MOE_MX_XTSC:
+    case MOE_MX_DYTSC: return tiles * static_cast<size_t>(moe::mx_weight_row_blocks(d.D)) * 512;
+    case MOE_MX_HTSC: return tiles * static_cast<size_t>(moe::mx_weight_row_blocks(d.F)) * 512;
+    case MOE_MX_DZTSC:
+      return tiles * static_cast<size_t>(moe::mx_weight_row_blocks(2L * d.F)) * 512;
   }
   return 0;
 }
@@ -453,13 +473,14 @@ moe_status moe_mx_permute_quantize(const moe_bf16* x, const int32_t* pos,
 moe_status moe_mx_grouped_gemm_fc1_swiglu(const uint8_t* xq, const uint8_t* xsc,
                                           const uint8_t* wq, const uint8_t* wsc,
                                           const int32_t* group_offsets, uint8_t* hq,
-                                          uint8_t* hsc, moe_bf16* h, int32_t* dev_status,
-                                          moe_dims d, cudaStream_t stream) {
+                                          uint8_t* hsc, moe_bf16* h, moe_bf16* z,
+                                          int32_t* dev_status, moe_dims d, cudaStream_t stream) {
   MOE_CHECK_DIMS(d);
   MOE_OPTIONAL(dev_status);
   MOE_OPTIONAL(hq);
   MOE_OPTIONAL(hsc);
   MOE_OPTIONAL(h);
+  MOE_OPTIONAL(z);
   if ((hq == nullptr) != (hsc == nullptr)) return MOE_ERR_INVALID_ARG;
   if (hq == nullptr && h == nullptr) return MOE_ERR_INVALID_ARG;
   if (d.T == 0) return MOE_OK;
@@ -468,7 +489,8 @@ moe_status moe_mx_grouped_gemm_fc1_swiglu(const uint8_t* xq, const uint8_t* xsc,
   MOE_REQUIRE(wq);
   MOE_REQUIRE(wsc);
   MOE_REQUIRE(group_offsets);
-  moe::MxGemmCall c{true, xq, xsc, wq, wsc, group_offsets, hq, hsc, h, dev_status, d};
+  moe::MxGemmCall c{moe::MxKind::kFc1, xq, xsc, wq, wsc, group_offsets, hq, hsc, h, nullptr, z,
+                    dev_status, d, 0, 0, 0};
   return from_cuda(moe::launch_mx_grouped_gemm(c, stream));
 }
 
@@ -485,8 +507,128 @@ moe_status moe_mx_grouped_gemm_fc2(const uint8_t* hq, const uint8_t* hsc, const 
   MOE_REQUIRE(wsc);
   MOE_REQUIRE(group_offsets);
   MOE_REQUIRE(ys);
-  moe::MxGemmCall c{false, hq, hsc, wq, wsc, group_offsets, nullptr, nullptr, ys, dev_status, d};
+  moe::MxGemmCall c{moe::MxKind::kRows, hq, hsc, wq, wsc, group_offsets, nullptr, nullptr, ys,
+                    nullptr, nullptr, dev_status, d, d.F, d.D, 0};
   return from_cuda(moe::launch_mx_grouped_gemm(c, stream));
+}
+
+moe_status moe_mx_quantize_wi_bwd(const moe_bf16* wi, uint8_t* wq, uint8_t* wsc, moe_dims d,
+                                  cudaStream_t stream) {
+  MOE_CHECK_DIMS(d);
+  MOE_REQUIRE(wi);
+  MOE_REQUIRE(wq);
+  MOE_REQUIRE(wsc);
+  return from_cuda(moe::launch_mx_quantize_lastaxis(wi, wq, wsc, d.E, d.D, 2 * d.F, stream));
+}
+
+moe_status moe_mx_quantize_wo_bwd(const moe_bf16* wo, uint8_t* wq, uint8_t* wsc, moe_dims d,
+                                  cudaStream_t stream) {
+  MOE_CHECK_DIMS(d);
+  MOE_REQUIRE(wo);
+  MOE_REQUIRE(wq);
+  MOE_REQUIRE(wsc);
+  return from_cuda(moe::launch_mx_quantize_lastaxis(wo, wq, wsc, d.E, d.F, d.D, stream));
+}
+
+moe_status moe_mx_quantize_rows(const moe_bf16* src, int C, const int32_t* group_offsets,
+                                uint8_t* q, uint8_t* sc, moe_dims d, cudaStream_t stream) {
+  MOE_CHECK_DIMS(d);
+  if (C != d.D && C != 2 * d.F) return MOE_ERR_INVALID_ARG;
+  if (d.T == 0) return MOE_OK;
+  MOE_REQUIRE(src);
+  MOE_REQUIRE(group_offsets);
+  MOE_REQUIRE(q);
+  MOE_REQUIRE(sc);
+  return from_cuda(moe::launch_mx_quantize_rows(src, group_offsets, q, sc, C, d, stream));
+}
+
+moe_status moe_mx_quantize_tokens(const moe_bf16* src, const int32_t* row_src, int C,
+                                  const int32_t* group_offsets, uint8_t* qt, uint8_t* sct,
+                                  moe_dims d, cudaStream_t stream) {
+  MOE_CHECK_DIMS(d);
+  if (C != d.D && C != d.F && C != 2 * d.F) return MOE_ERR_INVALID_ARG;
+  MOE_OPTIONAL(row_src);
+  if (d.T == 0) return MOE_OK;
+  MOE_REQUIRE(src);
+  MOE_REQUIRE(group_offsets);
+  MOE_REQUIRE(qt);
+  MOE_REQUIRE(sct);
+  return from_cuda(
+      moe::launch_mx_quantize_tokens(src, row_src, group_offsets, qt, sct, C, d, stream));
+}
+
+namespace {
+// out bf16 [E, m, n] of an MX wgrad (zeros where no token reaches an expert)
+moe_status mx_wgrad(const uint8_t* at, const uint8_t* atsc, const uint8_t* bt,
+                    const uint8_t* btsc, const int32_t* group_offsets, moe_bf16* out, int m,
+                    int n, int32_t* dev_status, const moe_dims& d, cudaStream_t stream) {
+  if (d.T == 0)
+    return from_cuda(cudaMemsetAsync(out, 0, static_cast<size_t>(d.E) * m * n * 2, stream));
+  MOE_REQUIRE(at);
+  MOE_REQUIRE(atsc);
+  MOE_REQUIRE(bt);
+  MOE_REQUIRE(btsc);
+  moe::MxGemmCall c{moe::MxKind::kWgrad, at, atsc, bt, btsc, group_offsets, nullptr, nullptr, out,
+                    nullptr, nullptr, dev_status, d, 0, n, m};
+  return from_cuda(moe::launch_mx_grouped_gemm(c, stream));
+}
+}  // namespace
+
+moe_status moe_mx_grouped_gemm_fc2_bwd(const uint8_t* dyq, const uint8_t* dysc,
+                                       const uint8_t* woq, const uint8_t* wosc, const moe_bf16* z,
+                                       const uint8_t* ht, const uint8_t* htsc,
+                                       const uint8_t* dyt, const uint8_t* dytsc,
+                                       const int32_t* group_offsets, moe_bf16* dz, moe_bf16* dwo,
+                                       int32_t* dev_status, moe_dims d, cudaStream_t stream) {
+  MOE_CHECK_DIMS(d);
+  MOE_OPTIONAL(dev_status);
+  MOE_OPTIONAL(dz);
+  MOE_OPTIONAL(dwo);
+  if (dz == nullptr && dwo == nullptr) return MOE_ERR_INVALID_ARG;
+  if (dwo != nullptr && d.T > 0) MOE_REQUIRE(group_offsets);
+  if (dz != nullptr && d.T > 0) {
+    MOE_REQUIRE(dyq);
+    MOE_REQUIRE(dysc);
+    MOE_REQUIRE(woq);
+    MOE_REQUIRE(wosc);
+    MOE_REQUIRE(z);
+    MOE_REQUIRE(group_offsets);
+    moe::MxGemmCall c{moe::MxKind::kRowsSwigluBwd, dyq, dysc, woq, wosc, group_offsets, nullptr,
+                      nullptr, dz, z, nullptr, dev_status, d, 0, 0, 0};
+    moe_status st = from_cuda(moe::launch_mx_grouped_gemm(c, stream));
+    if (st != MOE_OK) return st;
+  }
+  if (dwo != nullptr)
+    return mx_wgrad(ht, htsc, dyt, dytsc, group_offsets, dwo, d.F, d.D, dev_status, d, stream);
+  return MOE_OK;
+}
+
+moe_status moe_mx_grouped_gemm_fc1_bwd(const uint8_t* dzq, const uint8_t* dzsc,
+                                       const uint8_t* wiq, const uint8_t* wisc,
+                                       const uint8_t* xt, const uint8_t* xtsc,
+                                       const uint8_t* dzt, const uint8_t* dztsc,
+                                       const int32_t* group_offsets, moe_bf16* dxs, moe_bf16* dwi,
+                                       int32_t* dev_status, moe_dims d, cudaStream_t stream) {
+  MOE_CHECK_DIMS(d);
+  MOE_OPTIONAL(dev_status);
+  MOE_OPTIONAL(dxs);
+  MOE_OPTIONAL(dwi);
+  if (dxs == nullptr && dwi == nullptr) return MOE_ERR_INVALID_ARG;
+  if (dwi != nullptr && d.T > 0) MOE_REQUIRE(group_offsets);
+  if (dxs != nullptr && d.T > 0) {
+    MOE_REQUIRE(dzq);
+    MOE_REQUIRE(dzsc);
+    MOE_REQUIRE(wiq);
+    MOE_REQUIRE(wisc);
+    MOE_REQUIRE(group_offsets);
+    moe::MxGemmCall c{moe::MxKind::kRows, dzq, dzsc, wiq, wisc, group_offsets, nullptr, nullptr,
+                      dxs, nullptr, nullptr, dev_status, d, 2 * d.F, d.D, 0};
+    moe_status st = from_cuda(moe::launch_mx_grouped_gemm(c, stream));
+    if (st != MOE_OK) return st;
+  }
+  if (dwi != nullptr)
+    return mx_wgrad(xt, xtsc, dzt, dztsc, group_offsets, dwi, d.D, 2 * d.F, dev_status, d, stream);
+  return MOE_OK;
 }
 
 moe_status moe_selftest_bounded_wait(int32_t* dev_status, uint64_t limit_ns, cudaStream_t stream) {

@@ -454,7 +454,6 @@ __device__ __forceinline__ void zero_tail(uint8_t* sa, uint8_t* sb, int valid, i
   else fence_proxy_async_smem();
 }
 
-__device__ __forceinline__ float sigmoid_fast(float g) { return __fdividef(1.0f, 1.0f + __expf(-g)); }
 __device__ __forceinline__ float silu_f(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
 
 // ---------------------------------------------------------------- epilogue
@@ -622,33 +621,6 @@ __device__ __forceinline__ void z_drain(EpiCtx<RING>& c) {
     z.ph ^= 1u << z.recv;
     z.recv ^= 1;
     --z.out;
-  }
-}
-
-// dgate, dup of 32 columns of one row (packed bf16 pairs), from the fp32 dh
-// in v and the bf16 gate and up z of the same columns (4 x uint4 each).
-__device__ __forceinline__ void swiglu_bwd32(const uint32_t (&v)[32], const uint4* zg,
-                                             const uint4* zu, uint32_t (&wg)[16],
-                                             uint32_t (&wu)[16]) {
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const uint32_t gq[4] = {zg[i].x, zg[i].y, zg[i].z, zg[i].w};
-    const uint32_t uq[4] = {zu[i].x, zu[i].y, zu[i].z, zu[i].w};
-#pragma unroll
-    for (int qq = 0; qq < 4; ++qq) {
-      float rg[2], ru[2];
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        const float dh = __uint_as_float(v[8 * i + 2 * qq + hh]);
-        const float g = hh ? bf16hi(gq[qq]) : bf16lo(gq[qq]);
-        const float u = hh ? bf16hi(uq[qq]) : bf16lo(uq[qq]);
-        const float sg = sigmoid_fast(g);
-        rg[hh] = dh * u * sg * (1.0f + g * (1.0f - sg));
-        ru[hh] = dh * g * sg;
-      }
-      wg[4 * i + qq] = pack_bf16x2(rg[0], rg[1]);
-      wu[4 * i + qq] = pack_bf16x2(ru[0], ru[1]);
-    }
   }
 }
 

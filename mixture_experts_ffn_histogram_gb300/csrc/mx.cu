@@ -241,7 +241,8 @@ __global__ void __launch_bounds__(256) mx_permute_quantize_kernel(
   const int R = s_off[E];
   for (int t = blockIdx.x * kPqWarps + warp; t < T; t += gridDim.x * kPqWarps) {
     if (lane < K) {
-      int r = __ldg(pos + static_cast<size_t>(t) * K + lane);
+      // pos == nullptr: the rows are already in sorted order (K == 1)
+      int r = pos != nullptr ? __ldg(pos + static_cast<size_t>(t) * K + lane) : t;
       if (r >= R) r = -1;
       int blk = 0, m = 0;
       if (r >= 0) {
@@ -324,31 +325,164 @@ __global__ void __launch_bounds__(256) mx_permute_quantize_kernel(
   }
 }
 
+// ------------------------------------------------ last-axis quantize
+// w [E][N][Kd] -> codes in the same layout (blocks along the contiguous
+// last axis) and scales [E][KB][NBp][512]: one 32-element block per thread,
+// consecutive threads on consecutive blocks of a row.
+__global__ void __launch_bounds__(256) mx_quantize_lastaxis_kernel(const uint16_t* __restrict__ w,
+                                                                   uint8_t* __restrict__ q,
+                                                                   uint8_t* __restrict__ sc,
+                                                                   long nblocks, int N, int Kd,
+                                                                   int KB, int NBp) {
+  const long i = static_cast<long>(blockIdx.x) * 256 + threadIdx.x;
+  if (i >= nblocks) return;
+  const int nb = Kd / 32;
+  const long row = i / nb;
+  const int b = static_cast<int>(i - row * nb);
+  const int e = static_cast<int>(row / N), n = static_cast<int>(row - static_cast<long>(e) * N);
+  const uint4* src = reinterpret_cast<const uint4*>(w + row * Kd + 32 * b);
+  float v[32];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const uint4 u = src[k];
+    const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      v[8 * k + 2 * j] = bf16lo(wv[j]);
+      v[8 * k + 2 * j + 1] = bf16hi(wv[j]);
+    }
+  }
+  uint32_t codes[8];
+  const uint32_t sbyte = mx_quant32(v, codes);
+  uint4* dst = reinterpret_cast<uint4*>(q + row * Kd + 32 * b);
+  dst[0] = make_uint4(codes[0], codes[1], codes[2], codes[3]);
+  dst[1] = make_uint4(codes[4], codes[5], codes[6], codes[7]);
+  sc[((static_cast<size_t>(e) * KB + (b >> 2)) * NBp + (n >> 7)) * 512 + sf_byte(n & 127, b & 3)] =
+      static_cast<uint8_t>(sbyte);
+}
+
+// ------------------------------------------------- token-axis quantize
+// The weight gradients contract over the tokens of each group, so their
+// operands are quantized along the token axis and stored transposed:
+// codes qt [C][Rp], the rows of group e in 128-row tiles from its first
+// row (tile g = tb[e] + i covers token columns 128g .. 128g + 127, rows
+// past the group's end as zeros) and scales [TB][NBp][512], tile g's
+// 128-column block of rows c = 128j .. at ((g * NBp) + j) * 512, byte
+// sf_byte(c % 128, 32-row step).  One block per (tile, 64 columns): coalesced
+// 128-byte row loads (gathered through row_src / K when given), a transpose
+// through shared memory, one 32-row block per thread.
+__global__ void __launch_bounds__(256) mx_quantize_tokens_kernel(
+    const uint16_t* __restrict__ src, const int32_t* __restrict__ row_src, int gather_k,
+    const int32_t* __restrict__ offs, uint8_t* __restrict__ qt, uint8_t* __restrict__ sct, int C,
+    int E, long Rp, int NBp) {
+  __shared__ int s_off[kMaxE + 1];
+  __shared__ int s_tb[kMaxE + 1];
+  __shared__ float tile[128][65];
+  load_tile_bases(offs, E, s_off, s_tb, 0);
+  const int g = blockIdx.y;
+  if (g >= s_tb[E]) return;  // block-uniform
+  int lo = 0, hi = E - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (s_tb[mid] <= g) lo = mid;
+    else hi = mid - 1;
+  }
+  const int row0 = s_off[lo] + 128 * (g - s_tb[lo]);
+  const int rows = min(128, s_off[lo + 1] - row0);
+  const int c0 = blockIdx.x * 64;
+  const int tid = threadIdx.x;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int idx = tid + 256 * i;
+    const int row = idx >> 3, c8 = idx & 7;
+    long sr = -1;
+    if (row < rows) {
+      sr = row0 + row;
+      if (row_src != nullptr) {
+        const int j = __ldg(row_src + sr);
+        sr = j >= 0 ? j / gather_k : -1;
+      }
+    }
+    uint4 u = make_uint4(0u, 0u, 0u, 0u);
+    if (sr >= 0) u = *reinterpret_cast<const uint4*>(src + sr * C + c0 + 8 * c8);
+    const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      tile[row][8 * c8 + 2 * j] = bf16lo(wv[j]);
+      tile[row][8 * c8 + 2 * j + 1] = bf16hi(wv[j]);
+    }
+  }
+  __syncthreads();
+  const int n = tid & 63, blk = tid >> 6;
+  float v[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = tile[32 * blk + i][n];
+  uint32_t codes[8];
+  const uint32_t sbyte = mx_quant32(v, codes);
+  const int c = c0 + n;
+  uint4* dst = reinterpret_cast<uint4*>(qt + static_cast<size_t>(c) * Rp + 128 * static_cast<size_t>(g) +
+                                        32 * blk);
+  dst[0] = make_uint4(codes[0], codes[1], codes[2], codes[3]);
+  dst[1] = make_uint4(codes[4], codes[5], codes[6], codes[7]);
+  sct[(static_cast<size_t>(g) * NBp + (c >> 7)) * 512 + sf_byte(c & 127, blk)] =
+      static_cast<uint8_t>(sbyte);
+}
+
 // ---------------------------------------------------------------- GEMM
+constexpr int kKFc1 = static_cast<int>(MxKind::kFc1);
+constexpr int kKRows = static_cast<int>(MxKind::kRows);
+constexpr int kKSwigluBwd = static_cast<int>(MxKind::kRowsSwigluBwd);
+constexpr int kKWgrad = static_cast<int>(MxKind::kWgrad);
+
 struct MxParams {
   const uint8_t* sfa;   // A scales, tile-blocked [tiles][KB][512]
   const uint8_t* sfb;   // B scales [E][KB][NBp][512]
   const int32_t* offs;
   uint8_t* hq;          // FC1: h codes [R][F] or nullptr
   uint8_t* hsc;         // FC1: h scales, tile-blocked [tiles][KBF][512]
-  __nv_bfloat16* out;   // FC1: h bf16 [R][F] or nullptr; FC2: ys [R][D]
+  __nv_bfloat16* out;   // FC1: h bf16 [R][F] or nullptr; rows: [R][Nout]; SwiGLU
+                        // backward: dz [R][2 Nout]; wgrad: [E][Ma][Nout]
+  const __nv_bfloat16* zin;  // SwiGLU backward: z [R][2 Nout]
+  __nv_bfloat16* zout;  // FC1: z [R][2F] or nullptr
   int32_t* status;
   uint64_t limit_ns;
   int E;
-  int Kd;       // contraction length (D for FC1, F for FC2)
+  int Kd;       // contraction length (rows kinds; a bound on it for the wgrad)
   int KB;       // k-blocks of Kd
-  int Nout;     // FC1: F (h columns); FC2: D
-  int NBp;      // 128-row blocks of B per (expert, k-block), even
+  int Nout;     // output columns: FC1 F (h columns); others the B rows per expert
+  int NBp;      // 128-row blocks of B per (expert or token tile, k-block), even
   int n_tiles;  // 256-row B tiles per expert
   int KBF;      // FC1: k-blocks of F (h scale blocks per tile row)
+  int Ma;       // wgrad: output rows per expert (A rows)
+  int m_tiles;  // wgrad: 128-row A tiles
+  int NBpA;     // wgrad: 128-row blocks of A per token tile
 };
 
+// One output tile: expert e, B tile nt; rows kinds: sorted-row tile g whose
+// rows row0 .. row0 + rows - 1 are A's and the output's; wgrad: A tile mt,
+// output rows row0 = e * Ma + 128 mt ..; the k-blocks kb0 .. kb0 + nkb - 1.
 struct MxTile {
-  int e, g, nt, row0, rows;
+  int e, g, nt, mt, row0, rows, kb0, nkb;
 };
 
+template <int KIND>
 __device__ __forceinline__ MxTile mx_decode(int t, const MxParams& p, const MxCtl& s) {
   MxTile T;
+  if constexpr (KIND == kKWgrad) {
+    T.nt = t % p.n_tiles;
+    const int em = t / p.n_tiles;
+    T.mt = em % p.m_tiles;
+    T.e = em / p.m_tiles;
+    T.g = 0;
+    T.row0 = T.e * p.Ma + 128 * T.mt;
+    T.rows = min(128, p.Ma - 128 * T.mt);
+    T.kb0 = s.tb[T.e];
+    T.nkb = s.tb[T.e + 1] - T.kb0;
+    return T;
+  }
+  T.mt = 0;
+  T.kb0 = 0;
+  T.nkb = p.KB;
   T.g = t / p.n_tiles;
   T.nt = t - T.g * p.n_tiles;
   int lo = 0, hi = p.E - 1;
@@ -364,9 +498,9 @@ __device__ __forceinline__ MxTile mx_decode(int t, const MxParams& p, const MxCt
 }
 
 // Whether half h (128 B rows) of tile nt holds any output column.
-template <bool FC1>
+template <int KIND>
 __device__ __forceinline__ bool half_valid(int nt, int h, const MxParams& p) {
-  return FC1 ? 64 * (2 * nt + h) < p.Nout : 256 * nt + 128 * h < p.Nout;
+  return KIND == kKFc1 ? 64 * (2 * nt + h) < p.Nout : 256 * nt + 128 * h < p.Nout;
 }
 
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
@@ -423,7 +557,7 @@ __device__ __forceinline__ void put_half_sw(uint8_t* buf, int lane, int hh, cons
   }
 }
 
-template <bool FC1>
+template <int KIND>
 __global__ void __launch_bounds__(kThreads, 1)
     mx_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                    const __grid_constant__ CUtensorMap map_b,
@@ -462,7 +596,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = s.tmem_base;
   const WaitCtl wc{&s.abort_flag, p.status, p.limit_ns};
-  const int ntiles = s.tb[p.E] * p.n_tiles;
+  const int ntiles =
+      KIND == kKWgrad ? p.E * p.m_tiles * p.n_tiles : s.tb[p.E] * p.n_tiles;
 
   if (warp == 0) {
     // -------------------------------------------------------- producer
@@ -471,17 +606,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t fills[kStages] = {0, 0, 0, 0};
       bool aborted = false;
       for (int t = blockIdx.x; t < ntiles && !aborted; t += gridDim.x) {
-        const MxTile T = mx_decode(t, p, s);
-        const uint8_t* sfa = p.sfa + static_cast<size_t>(T.g) * p.KB * 512;
-        const uint8_t* sfb =
-            p.sfb + (static_cast<size_t>(T.e) * p.KB * p.NBp + 2 * T.nt) * 512;
-        for (int kb = 0; kb < p.KB; ++kb) {
+        const MxTile T = mx_decode<KIND>(t, p, s);
+        const uint8_t* sfa;
+        const uint8_t* sfb;
+        size_t sfa_step;
+        if constexpr (KIND == kKWgrad) {
+          sfa = p.sfa + (static_cast<size_t>(T.kb0) * p.NBpA + T.mt) * 512;
+          sfb = p.sfb + (static_cast<size_t>(T.kb0) * p.NBp + 2 * T.nt) * 512;
+          sfa_step = static_cast<size_t>(p.NBpA) * 512;
+        } else {
+          sfa = p.sfa + static_cast<size_t>(T.g) * p.KB * 512;
+          sfb = p.sfb + (static_cast<size_t>(T.e) * p.KB * p.NBp + 2 * T.nt) * 512;
+          sfa_step = 512;
+        }
+        for (int kb = 0; kb < T.nkb; ++kb) {
           if (!mbar_wait(&s.empty[stage], phase ^ 1u, wc)) { aborted = true; break; }
           uint8_t* st = ring + stage * kStageBytes;
           mbar_arrive_expect_tx(&s.full[stage], kTxBytes);
-          tma_load_2d(st, &map_a, &s.full[stage], kb * 128, T.row0);
-          tma_load_3d(st + kAStage, &map_b, &s.full[stage], kb * 128, 256 * T.nt, T.e);
-          bulk_load(st + kSfaOff, sfa + static_cast<size_t>(kb) * 512, 512, &s.full[stage]);
+          const int kx = (T.kb0 + kb) * 128;
+          if constexpr (KIND == kKWgrad) {
+            tma_load_2d(st, &map_a, &s.full[stage], kx, 128 * T.mt);
+            tma_load_3d(st + kAStage, &map_b, &s.full[stage], kx, 256 * T.nt, 0);
+          } else {
+            tma_load_2d(st, &map_a, &s.full[stage], kx, T.row0);
+            tma_load_3d(st + kAStage, &map_b, &s.full[stage], kx, 256 * T.nt, T.e);
+          }
+          bulk_load(st + kSfaOff, sfa + kb * sfa_step, 512, &s.full[stage]);
           bulk_load(st + kSfbOff, sfb + static_cast<size_t>(kb) * p.NBp * 512, 1024,
                     &s.full[stage]);
           ++fills[stage];
@@ -506,8 +656,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t da0 = smem_desc_sw128(smem_u32(ring), 16, 1024);
       const uint64_t ds0 = sf_desc(smem_u32(ring) + kSfaOff);
       for (int t = blockIdx.x; t < ntiles && !aborted; t += gridDim.x, ++it) {
-        const MxTile T = mx_decode(t, p, s);
-        const bool h1 = half_valid<FC1>(T.nt, 1, p);
+        const MxTile T = mx_decode<KIND>(t, p, s);
+        const bool h1 = half_valid<KIND>(T.nt, 1, p);
         // tile it accumulates in buffer it % 2 (256 columns) while its scale
         // slots sit in the first kStages * kSfStride columns of the other buffer, which
         // the epilogue empties first
@@ -521,7 +671,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t d0 = tmem_base + 256 * buf;
         const uint32_t sf_base = tmem_base + 256 * (buf ^ 1u);
         const uint32_t idn = h1 ? 256u : 128u;
-        for (int kb = 0; kb < p.KB; ++kb) {
+        for (int kb = 0; kb < T.nkb; ++kb) {
           if (!mbar_wait(&s.full[stage], phase, wc)) { aborted = true; break; }
           tc_fence_after();
           const uint32_t sf = sf_base + kSfStride * stage;
@@ -562,7 +712,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t it = 0;
     bool aborted = false;
     for (int t = blockIdx.x; t < ntiles && !aborted; t += gridDim.x, ++it) {
-      const MxTile T = mx_decode(t, p, s);
+      const MxTile T = mx_decode<KIND>(t, p, s);
       const int vw = min(32, max(0, T.rows - 32 * q));  // valid rows of this warp
       const int y = T.row0 + 32 * q;
       const bool row_ok = lane < vw;
@@ -574,9 +724,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_after();
       for (int hh = 0; hh < 2; ++hh) {
-        const bool live = half_valid<FC1>(T.nt, hh, p) && vw > 0;
+        const bool live = half_valid<KIND>(T.nt, hh, p) && vw > 0;
+        // a wgrad tile of an empty group has no accumulator: its rows are zeros
+        const bool empty = KIND == kKWgrad && T.nkb == 0;
         uint32_t v[128];
-        if (live) {
+        if (live && !empty) {
           const uint32_t ta = tmem_base + 256 * bsel + 128 * hh + (static_cast<uint32_t>(32 * q) << 16);
           tmem_ld_32x32b_x32(ta, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
           tmem_ld_32x32b_x32(ta + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
@@ -590,9 +742,36 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(hh == 0 ? &s.sffree[bsel] : &s.tempty[bsel]);
         if (!live) continue;
-        if constexpr (FC1) {
+        if constexpr (KIND == kKWgrad) {
+          if (empty) {
+            if (row_ok) {
+              const int d0 = 256 * T.nt + 128 * hh;
+              for (int col = d0; col < min(d0 + 128, p.Nout); col += 8)
+                *reinterpret_cast<uint4*>(p.out + r * p.Nout + col) = make_uint4(0u, 0u, 0u, 0u);
+            }
+            continue;
+          }
+        }
+        if constexpr (KIND == kKFc1) {
           // gate = columns 0..63, up = 64..127 of the region: h for f0..f0+63
           const int f0 = 64 * (2 * T.nt + hh);
+          if (p.zout != nullptr && row_ok) {  // z = [gate | up] for the backward
+            uint4* zg = reinterpret_cast<uint4*>(p.zout + r * 2 * p.Nout + f0);
+            uint4* zu = reinterpret_cast<uint4*>(p.zout + r * 2 * p.Nout + p.Nout + f0);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const uint32_t* a = v + 8 * i;
+              zg[i] = make_uint4(pack_bf16x2(__uint_as_float(a[0]), __uint_as_float(a[1])),
+                                 pack_bf16x2(__uint_as_float(a[2]), __uint_as_float(a[3])),
+                                 pack_bf16x2(__uint_as_float(a[4]), __uint_as_float(a[5])),
+                                 pack_bf16x2(__uint_as_float(a[6]), __uint_as_float(a[7])));
+              const uint32_t* b = v + 64 + 8 * i;
+              zu[i] = make_uint4(pack_bf16x2(__uint_as_float(b[0]), __uint_as_float(b[1])),
+                                 pack_bf16x2(__uint_as_float(b[2]), __uint_as_float(b[3])),
+                                 pack_bf16x2(__uint_as_float(b[4]), __uint_as_float(b[5])),
+                                 pack_bf16x2(__uint_as_float(b[6]), __uint_as_float(b[7])));
+            }
+          }
           float hv[64];
 #pragma unroll
           for (int j = 0; j < 64; ++j)
@@ -643,6 +822,33 @@ __global__ void __launch_bounds__(kThreads, 1)
               for (int b = 0; b < 2; ++b) {
                 dst[2 * b] = make_uint4(c[b][0], c[b][1], c[b][2], c[b][3]);
                 dst[2 * b + 1] = make_uint4(c[b][4], c[b][5], c[b][6], c[b][7]);
+              }
+            }
+          }
+        } else if constexpr (KIND == kKSwigluBwd) {
+          // dh for f = fb .. fb + 127 of this row; z and dz are [gate | up] rows
+          if (row_ok) {
+            const int fb = 256 * T.nt + 128 * hh;
+            const __nv_bfloat16* zr = p.zin + r * 2 * p.Nout;
+            __nv_bfloat16* dzr = p.out + r * 2 * p.Nout;
+#pragma unroll
+            for (int ch = 0; ch < 4; ++ch) {
+              const int f = fb + 32 * ch;
+              if (f >= p.Nout) break;
+              uint4 zg[4], zu[4];
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                zg[i] = reinterpret_cast<const uint4*>(zr + f)[i];
+                zu[i] = reinterpret_cast<const uint4*>(zr + p.Nout + f)[i];
+              }
+              uint32_t wg[16], wu[16];
+              swiglu_bwd32(*reinterpret_cast<const uint32_t(*)[32]>(&v[32 * ch]), zg, zu, wg, wu);
+              uint4* og = reinterpret_cast<uint4*>(dzr + f);
+              uint4* ou = reinterpret_cast<uint4*>(dzr + p.Nout + f);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                og[i] = make_uint4(wg[4 * i], wg[4 * i + 1], wg[4 * i + 2], wg[4 * i + 3]);
+                ou[i] = make_uint4(wu[4 * i], wu[4 * i + 1], wu[4 * i + 2], wu[4 * i + 3]);
               }
             }
           }
@@ -732,10 +938,10 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType type, const void* base, int ra
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <bool FC1>
+template <int KIND>
 cudaError_t launch_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mo,
                         const MxParams& p, long max_tiles, cudaStream_t s) {
-  auto kern = mx_gemm_kernel<FC1>;
+  auto kern = mx_gemm_kernel<KIND>;
   static std::atomic<bool> attr_set[64];
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
@@ -777,6 +983,42 @@ cudaError_t launch_mx_permute_quantize(const uint16_t* x, const int32_t* pos, co
   return cudaGetLastError();
 }
 
+cudaError_t launch_mx_quantize_lastaxis(const uint16_t* w, uint8_t* q, uint8_t* sc, int E, int N,
+                                        int Kd, cudaStream_t s) {
+  const long nblocks = static_cast<long>(E) * N * (Kd / 32);
+  if (nblocks == 0) return cudaSuccess;
+  mx_quantize_lastaxis_kernel<<<static_cast<unsigned>(mx_cdiv(nblocks, 256)), 256, 0, s>>>(
+      w, q, sc, nblocks, N, Kd, static_cast<int>(mx_kblocks(Kd)),
+      static_cast<int>(mx_weight_row_blocks(N)));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_mx_quantize_rows(const uint16_t* src, const int32_t* offs, uint8_t* q,
+                                    uint8_t* sc, int C, const moe_dims& d, cudaStream_t s) {
+  const long R = static_cast<long>(d.T) * d.K;
+  if (R == 0) return cudaSuccess;
+  long blocks = mx_cdiv(R, kPqWarps);
+  const long cap = 8L * sm_count();
+  if (blocks > cap) blocks = cap;
+  mx_permute_quantize_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(
+      src, nullptr, offs, q, sc, static_cast<int>(R), C, 1, d.E,
+      static_cast<int>(mx_kblocks(C)));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_mx_quantize_tokens(const uint16_t* src, const int32_t* row_src,
+                                      const int32_t* offs, uint8_t* qt, uint8_t* sct, int C,
+                                      const moe_dims& d, cudaStream_t s) {
+  if (static_cast<long>(d.T) * d.K == 0) return cudaSuccess;
+  const long tiles = mx_tile_bound(d);
+  if (tiles > 65535) return cudaErrorInvalidValue;
+  dim3 grid(static_cast<unsigned>(C / 64), static_cast<unsigned>(tiles));
+  mx_quantize_tokens_kernel<<<grid, 256, 0, s>>>(src, row_src, d.K, offs, qt, sct, C, d.E,
+                                                 mx_token_cols(d),
+                                                 static_cast<int>(mx_weight_row_blocks(C)));
+  return cudaGetLastError();
+}
+
 cudaError_t launch_mx_grouped_gemm(const MxGemmCall& c, cudaStream_t s) {
   const moe_dims& d = c.d;
   const long R = static_cast<long>(d.T) * d.K;
@@ -788,54 +1030,101 @@ cudaError_t launch_mx_grouped_gemm(const MxGemmCall& c, cudaStream_t s) {
   p.hq = c.hq;
   p.hsc = c.hsc;
   p.out = reinterpret_cast<__nv_bfloat16*>(c.out);
+  p.zin = reinterpret_cast<const __nv_bfloat16*>(c.z_in);
+  p.zout = reinterpret_cast<__nv_bfloat16*>(c.z_out);
   p.status = c.dev_status;
   p.limit_ns = kDefaultWaitLimitNs;
   p.E = d.E;
-  const long Nb = c.fc1 ? 2L * d.F : d.D;  // B rows per expert
-  p.Kd = c.fc1 ? d.D : d.F;
+  const long Rp = mx_token_cols(d);
+  long Nb = 0;  // B rows per expert
+  switch (c.kind) {
+    case MxKind::kFc1: p.Kd = d.D; Nb = 2L * d.F; p.Nout = d.F; break;
+    case MxKind::kRows: p.Kd = c.kd; Nb = c.n; p.Nout = c.n; break;
+    case MxKind::kRowsSwigluBwd: p.Kd = d.D; Nb = d.F; p.Nout = d.F; break;
+    case MxKind::kWgrad:
+      if (Rp > (1L << 30)) return cudaErrorInvalidValue;
+      p.Kd = static_cast<int>(Rp);
+      Nb = c.n;
+      p.Nout = c.n;
+      p.Ma = c.m;
+      p.m_tiles = static_cast<int>(mx_cdiv(c.m, 128));
+      p.NBpA = static_cast<int>(mx_weight_row_blocks(c.m));
+      break;
+  }
   p.KB = static_cast<int>(mx_kblocks(p.Kd));
-  p.Nout = c.fc1 ? d.F : d.D;
   p.NBp = static_cast<int>(mx_weight_row_blocks(Nb));
   p.n_tiles = static_cast<int>(mx_cdiv(Nb, 256));
   p.KBF = static_cast<int>(mx_kblocks(d.F));
   CUtensorMap ma, mb, mo;
-  const uint64_t adims[2] = {static_cast<uint64_t>(p.Kd), static_cast<uint64_t>(R)};
-  const uint64_t astr[1] = {static_cast<uint64_t>(p.Kd)};
   const uint32_t abox[2] = {128, 128};
-  const uint64_t bdims[3] = {static_cast<uint64_t>(p.Kd), static_cast<uint64_t>(Nb),
-                             static_cast<uint64_t>(d.E)};
-  const uint64_t bstr[2] = {static_cast<uint64_t>(p.Kd), static_cast<uint64_t>(p.Kd) * Nb};
   const uint32_t bbox[3] = {128, 256, 1};
-  bool ok = make_map(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT8, c.a, 2, adims, astr, abox,
-                     CU_TENSOR_MAP_SWIZZLE_128B) &&
-            make_map(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, c.b, 3, bdims, bstr, bbox,
-                     CU_TENSOR_MAP_SWIZZLE_128B);
-  if (!ok) return cudaErrorInvalidValue;
-  const long max_tiles = mx_tile_bound(d) * p.n_tiles;
-  if (c.fc1) {
-    // h codes: 32 rows x 64 bytes per store, unswizzled staging (or a dummy
-    // map over the bf16 h when only that is written)
-    const uint64_t odims[2] = {static_cast<uint64_t>(d.F), static_cast<uint64_t>(R)};
-    const uint32_t obox[2] = {64, 32};
-    if (c.hq != nullptr) {
-      const uint64_t ostr[1] = {static_cast<uint64_t>(d.F)};
-      ok = make_map(&mo, CU_TENSOR_MAP_DATA_TYPE_UINT8, c.hq, 2, odims, ostr, obox,
-                    CU_TENSOR_MAP_SWIZZLE_NONE);
-    } else {
-      const uint64_t ostr[1] = {static_cast<uint64_t>(d.F) * 2};
-      ok = make_map(&mo, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, c.out, 2, odims, ostr, obox,
-                    CU_TENSOR_MAP_SWIZZLE_128B);
-    }
-    if (!ok) return cudaErrorInvalidValue;
-    return launch_gemm<true>(ma, mb, mo, p, max_tiles, s);
-  }
-  const uint64_t odims[2] = {static_cast<uint64_t>(d.D), static_cast<uint64_t>(R)};
-  const uint64_t ostr[1] = {static_cast<uint64_t>(d.D) * 2};
   const uint32_t obox[2] = {64, 32};
-  ok = make_map(&mo, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, c.out, 2, odims, ostr, obox,
-                CU_TENSOR_MAP_SWIZZLE_128B);
+  bool ok;
+  if (c.kind == MxKind::kWgrad) {
+    // A [m][Rp], B [n][Rp]: token-axis codes; the k coordinate is the token column
+    const uint64_t adims[2] = {static_cast<uint64_t>(Rp), static_cast<uint64_t>(c.m)};
+    const uint64_t astr[1] = {static_cast<uint64_t>(Rp)};
+    const uint64_t bdims[3] = {static_cast<uint64_t>(Rp), static_cast<uint64_t>(Nb), 1};
+    const uint64_t bstr[2] = {static_cast<uint64_t>(Rp), static_cast<uint64_t>(Rp) * Nb};
+    ok = make_map(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT8, c.a, 2, adims, astr, abox,
+                  CU_TENSOR_MAP_SWIZZLE_128B) &&
+         make_map(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, c.b, 3, bdims, bstr, bbox,
+                  CU_TENSOR_MAP_SWIZZLE_128B);
+  } else {
+    const uint64_t adims[2] = {static_cast<uint64_t>(p.Kd), static_cast<uint64_t>(R)};
+    const uint64_t astr[1] = {static_cast<uint64_t>(p.Kd)};
+    const uint64_t bdims[3] = {static_cast<uint64_t>(p.Kd), static_cast<uint64_t>(Nb),
+                               static_cast<uint64_t>(d.E)};
+    const uint64_t bstr[2] = {static_cast<uint64_t>(p.Kd), static_cast<uint64_t>(p.Kd) * Nb};
+    ok = make_map(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT8, c.a, 2, adims, astr, abox,
+                  CU_TENSOR_MAP_SWIZZLE_128B) &&
+         make_map(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, c.b, 3, bdims, bstr, bbox,
+                  CU_TENSOR_MAP_SWIZZLE_128B);
+  }
   if (!ok) return cudaErrorInvalidValue;
-  return launch_gemm<false>(ma, mb, mo, p, max_tiles, s);
+  const long max_tiles = c.kind == MxKind::kWgrad
+                             ? static_cast<long>(d.E) * p.m_tiles * p.n_tiles
+                             : mx_tile_bound(d) * p.n_tiles;
+  switch (c.kind) {
+    case MxKind::kFc1: {
+      // h codes: 32 rows x 64 bytes per store, unswizzled staging (or a dummy
+      // map over the bf16 h when only that is written)
+      const uint64_t odims[2] = {static_cast<uint64_t>(d.F), static_cast<uint64_t>(R)};
+      if (c.hq != nullptr) {
+        const uint64_t ostr[1] = {static_cast<uint64_t>(d.F)};
+        ok = make_map(&mo, CU_TENSOR_MAP_DATA_TYPE_UINT8, c.hq, 2, odims, ostr, obox,
+                      CU_TENSOR_MAP_SWIZZLE_NONE);
+      } else {
+        const uint64_t ostr[1] = {static_cast<uint64_t>(d.F) * 2};
+        ok = make_map(&mo, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, c.out, 2, odims, ostr, obox,
+                      CU_TENSOR_MAP_SWIZZLE_128B);
+      }
+      if (!ok) return cudaErrorInvalidValue;
+      return launch_gemm<kKFc1>(ma, mb, mo, p, max_tiles, s);
+    }
+    case MxKind::kRowsSwigluBwd: {
+      // dz is written by plain stores; the map (over dz) is not used
+      const uint64_t odims[2] = {2 * static_cast<uint64_t>(d.F), static_cast<uint64_t>(R)};
+      const uint64_t ostr[1] = {static_cast<uint64_t>(d.F) * 4};
+      if (!make_map(&mo, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, c.out, 2, odims, ostr, obox,
+                    CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+      return launch_gemm<kKSwigluBwd>(ma, mb, mo, p, max_tiles, s);
+    }
+    case MxKind::kRows:
+    case MxKind::kWgrad: {
+      const uint64_t rows = c.kind == MxKind::kWgrad ? static_cast<uint64_t>(d.E) * c.m
+                                                      : static_cast<uint64_t>(R);
+      const uint64_t odims[2] = {static_cast<uint64_t>(p.Nout), rows};
+      const uint64_t ostr[1] = {static_cast<uint64_t>(p.Nout) * 2};
+      if (!make_map(&mo, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, c.out, 2, odims, ostr, obox,
+                    CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+      if (c.kind == MxKind::kWgrad) return launch_gemm<kKWgrad>(ma, mb, mo, p, max_tiles, s);
+      return launch_gemm<kKRows>(ma, mb, mo, p, max_tiles, s);
+    }
+  }
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace moe

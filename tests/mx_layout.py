@@ -4,7 +4,11 @@ and scales into the library's layouts, and read the library's buffers back
 into logical form.  Shares no code with the oracle or the CUDA path.
 
 Logical forms (the oracle's): activation codes [R, k] with scales [R, k/32];
-weight codes [E, N, k] (row n = output column n) with scales [E, N, k/32].
+weight codes [E, N, k] (row n = output column n) with scales [E, N, k/32];
+token-axis codes [R, C] with scales [NB, C], block b of group e (rows
+offs[e] + 32b ..) at scale row boff[e] + b.  A weight quantized along its
+last axis has the weight layout without the transpose (unpack_weight with
+interleave False).
 """
 from __future__ import annotations
 
@@ -124,3 +128,96 @@ def unpack_weight_expert(codes_e, buf, e, N, k, interleave):
     per = cdiv(k, 128) * 2 * cdiv(N, 256) * 512
     q, sc = unpack_weight(codes_e[None], np.asarray(buf)[e * per:(e + 1) * per], interleave)
     return q[0], sc[0]
+
+
+def token_cols(R, E):
+    """Rp: token columns of the transposed token-axis codes (128 per tile of
+    the tile bound ceil(R/128) + E)."""
+    return 128 * (cdiv(R, 128) + E)
+
+
+def token_index(offs):
+    """For each sorted row r < offs[E]: its token column (128 tb[e] + i), its
+    tile g and its 32-row step j inside the tile; and each group's first
+    token block (boff, the prefix of ceil(size/32))."""
+    offs = np.asarray(offs, np.int64)
+    tb = tile_bases(offs)
+    R = int(offs[-1])
+    r = np.arange(R)
+    e = np.searchsorted(offs, r, side="right") - 1
+    i = r - offs[e]
+    col = 128 * tb[e] + i
+    gs = np.diff(offs)
+    boff = np.concatenate([[0], np.cumsum(cdiv(gs, 32))])
+    return col, e, i, boff
+
+
+def token_scale_index(offs, C):
+    """Flat byte index [NB, C] of each token block's scales: block b of group
+    e lies in tile tb[e] + b // 4 at step b % 4."""
+    offs = np.asarray(offs, np.int64)
+    tb = tile_bases(offs)
+    gs = np.diff(offs)
+    nbp = 2 * cdiv(C, 256)
+    g, j = [], []
+    for e in range(len(gs)):
+        b = np.arange(cdiv(int(gs[e]), 32))
+        g.append(tb[e] + b // 4)
+        j.append(b % 4)
+    g = np.concatenate(g).astype(np.int64) if g else np.zeros(0, np.int64)
+    j = np.concatenate(j).astype(np.int64) if j else np.zeros(0, np.int64)
+    c = np.arange(C)
+    return (g[:, None] * nbp + c[None, :] // 128) * 512 + sf_byte(c[None, :] % 128, j[:, None])
+
+
+def token_scale_bytes(R, E, C):
+    return (cdiv(R, 128) + E) * 2 * cdiv(C, 256) * 512
+
+
+def token_pad_scale_index(offs, C):
+    """Flat byte index [n, C] of the scales of the 32-token steps of used
+    tiles that hold none of the group's rows (a group's last tile past its
+    last block): the quantization of zero rows, scale byte 0."""
+    offs = np.asarray(offs, np.int64)
+    tb = tile_bases(offs)
+    gs = np.diff(offs)
+    nbp = 2 * cdiv(C, 256)
+    g, j = [], []
+    for e in range(len(gs)):
+        nb = cdiv(int(gs[e]), 32)
+        for b in range(nb, 4 * cdiv(nb, 4)):
+            g.append(tb[e] + b // 4)
+            j.append(b % 4)
+    g = np.array(g, np.int64)
+    j = np.array(j, np.int64)
+    c = np.arange(C)
+    return (g[:, None] * nbp + c[None, :] // 128) * 512 + sf_byte(c[None, :] % 128, j[:, None])
+
+
+def pack_tokens(q, sc, offs, R, E):
+    """Logical (codes [R_used, C], scales [NB, C]) -> library (codes [C, Rp]
+    with zero codes in the padding columns and zero-block scales for the
+    steps they fill, scale bytes)."""
+    C = q.shape[1]
+    col, _, _, _ = token_index(offs)
+    codes = np.zeros((C, token_cols(R, E)), np.uint8)
+    codes[:, col] = q[: len(col)].T
+    buf = np.full(token_scale_bytes(R, E, C), PAD, np.uint8)
+    buf[token_scale_index(offs, C)] = sc
+    buf[token_pad_scale_index(offs, C)] = 0
+    return codes, buf
+
+
+def unpack_tokens(codes, buf, offs):
+    """Library (codes [C, Rp], scale bytes) -> logical (codes [R_used, C],
+    scales [NB, C]), the codes of the padding columns of used tiles and the
+    scales of the steps that hold only padding."""
+    C = codes.shape[0]
+    col, _, _, _ = token_index(offs)
+    q = np.ascontiguousarray(codes[:, col].T)
+    sc = np.asarray(buf)[token_scale_index(offs, C)]
+    tb = tile_bases(offs)
+    used = np.zeros(codes.shape[1], bool)
+    used[: 128 * int(tb[-1])] = True
+    used[col] = False
+    return q, sc, codes[:, used], np.asarray(buf)[token_pad_scale_index(offs, C)]

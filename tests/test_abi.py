@@ -52,7 +52,7 @@ def test_binding_names_match_the_header(libpath):
 
 def test_host_only_queries(libpath):
     from mixture_experts_ffn_histogram_gb300 import binding as B
-    assert B.moe_abi_version() == 3
+    assert B.moe_abi_version() == 4
     d = B.dims(32768, 2816, 128, 8, 704)
     ws = B.moe_workspace_bytes(d)
     assert ws >= 32768 * 8 * 2 * 704 * 2 and ws % 256 == 0
