@@ -52,7 +52,8 @@ def parse():
     ap.add_argument("--fwd-only", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--no-mx", action="store_true", help="skip the MXFP8 forward measurement")
+    ap.add_argument("--no-mx", action="store_true",
+                    help="skip the MXFP8 forward (and training step) measurements")
     ap.add_argument("--no-configs", action="store_true",
                     help="skip the timed loop over every configuration")
     ap.add_argument("--tokens", type=int, default=None,
@@ -536,6 +537,156 @@ def measure_mx(wl, inp, steps, pk, flushed, dev):
         "gpu_launches_per_step": len(MX_STEPS),
         "kernels": kern,
     }
+def mx_train_work(wl):
+    """Per launch of the MXFP8 training step: (name, kind, amount) with kind
+    "tensor" (FLOPs of a block-scaled GEMM) or "hbm" (algorithmic bytes: bf16
+    read once, e4m3 codes and one scale byte per 32 elements written once)."""
+    T, D, E, K, F = wl.T, wl.D, wl.E, wl.K, wl.F
+    R = T * K
+
+    def quant(n_in, n_out):   # bf16 in, e4m3 + scales out
+        return 2 * n_in + n_out + n_out // 32
+
+    return [   # each weight read once for its two MX copies
+        ("quantize_wi", "hbm", quant(E * D * 2 * F, 2 * E * D * 2 * F)),
+        ("quantize_wo", "hbm", quant(E * F * D, 2 * E * F * D)),
+        ("route", "hbm", hbm_bytes("route", T, D, E, K, F)),
+        ("permute_quantize", "hbm", mx_bytes("permute_quantize", T, D, E, K, F)),
+        ("fc1", "tensor", gemm_flops("fc1", R, D, F)),
+        ("fc2", "tensor", gemm_flops("fc2", R, D, F)),
+        ("combine", "hbm", hbm_bytes("combine", T, D, E, K, F)),
+        ("combine_bwd", "hbm", hbm_bytes("combine_bwd", T, D, E, K, F)),
+        ("quantize_dys_rows", "hbm", quant(R * D, R * D)),
+        ("quantize_dys_tokens", "hbm", quant(R * D, R * D)),
+        ("quantize_h_tokens", "hbm", quant(R * F, R * F)),
+        ("fc2_dgrad", "tensor", gemm_flops("fc2_dlhs", R, D, F)),
+        ("fc2_wgrad", "tensor", gemm_flops("fc2_drhs", R, D, F)),
+        ("quantize_dz_rows", "hbm", quant(R * 2 * F, R * 2 * F)),
+        ("quantize_dz_tokens", "hbm", quant(R * 2 * F, R * 2 * F)),
+        ("quantize_x_tokens", "hbm", quant(R * D, R * D) + 4 * R),
+        ("fc1_dgrad", "tensor", gemm_flops("fc1_dlhs", R, D, F)),
+        ("fc1_wgrad", "tensor", gemm_flops("fc1_drhs", R, D, F)),
+        ("permute_bwd", "hbm", hbm_bytes("permute_bwd", T, D, E, K, F)),
+    ]
+
+
+def measure_mx_train(wl, inp, steps, pk, flushed, dev):
+    """One MXFP8 training step per iteration through the C ABI: the weight
+    quantizations (the weights change every step; one launch per weight
+    writes its forward and dgrad copies), the MX forward
+    with h and z kept in bf16, and the MX backward (see MoEBlockMX); an event
+    pair around every launch."""
+    from mixture_experts_ffn_histogram_gb300 import binding as B
+    from mixture_experts_ffn_histogram_gb300.block import MoEBlockMX
+    blk = MoEBlockMX(wl.T, wl.D, wl.E, wl.K, wl.F, wl.score_mode, train=True)
+    d, D, F = blk.d, wl.D, wl.F
+    offs = blk.group_offsets
+    if wl.score_mode == B.SCORE_GIVEN:
+        blk.ids.copy_(inp["ids"])
+        blk.w.copy_(inp["w"])
+    wi, wo, x, dy = inp["wi"], inp["wo"], inp["x"], inp["dy"]
+    calls = [
+        lambda: B.moe_mx_quantize_wi(wi, blk.wiq, blk.wisc, d, wq_bwd=blk.wiq_b,
+                                     wsc_bwd=blk.wisc_b),
+        lambda: B.moe_mx_quantize_wo(wo, blk.woq, blk.wosc, d, wq_bwd=blk.woq_b,
+                                     wsc_bwd=blk.wosc_b),
+        lambda: B.moe_route_histogram(inp.get("logits"), inp.get("bias"), blk.mode, blk.ids,
+                                      blk.w, blk.group_sizes, offs, blk.pos, blk.row_src,
+                                      blk.status, blk.ws, d),
+        lambda: B.moe_mx_permute_quantize(x, blk.pos, offs, blk.xq, blk.xsc, d),
+        lambda: B.moe_mx_grouped_gemm_fc1_swiglu(blk.xq, blk.xsc, blk.wiq, blk.wisc, offs,
+                                                 blk.hq, blk.hsc, blk.h, blk.status, d, z=blk.z),
+        lambda: B.moe_mx_grouped_gemm_fc2(blk.hq, blk.hsc, blk.woq, blk.wosc, offs, blk.ys,
+                                          blk.status, d),
+        lambda: B.moe_combine(blk.ys, blk.w, blk.pos, blk.out, d),
+        lambda: B.moe_combine_bwd(dy, blk.ys, blk.w, blk.pos, blk.dys, blk.dw, d),
+        lambda: B.moe_mx_quantize_rows(blk.dys, D, offs, blk.dyq, blk.dysc, d),
+        lambda: B.moe_mx_quantize_tokens(blk.dys, None, D, offs, blk.dyt, blk.dytsc, d),
+        lambda: B.moe_mx_quantize_tokens(blk.h, None, F, offs, blk.ht, blk.htsc, d),
+        lambda: B.moe_mx_grouped_gemm_fc2_bwd(blk.dyq, blk.dysc, blk.woq_b, blk.wosc_b, blk.z,
+                                              None, None, None, None, offs, blk.dz, None,
+                                              blk.status, d),
+        lambda: B.moe_mx_grouped_gemm_fc2_bwd(None, None, None, None, None, blk.ht, blk.htsc,
+                                              blk.dyt, blk.dytsc, offs, None, blk.dwo,
+                                              blk.status, d),
+        lambda: B.moe_mx_quantize_rows(blk.dz, 2 * F, offs, blk.dzq, blk.dzsc, d),
+        lambda: B.moe_mx_quantize_tokens(blk.dz, None, 2 * F, offs, blk.dzt, blk.dztsc, d),
+        lambda: B.moe_mx_quantize_tokens(x, blk.row_src, D, offs, blk.xt, blk.xtsc, d),
+        lambda: B.moe_mx_grouped_gemm_fc1_bwd(blk.dzq, blk.dzsc, blk.wiq_b, blk.wisc_b, None,
+                                              None, None, None, offs, blk.dxs, None, blk.status,
+                                              d),
+        lambda: B.moe_mx_grouped_gemm_fc1_bwd(None, None, None, None, blk.xt, blk.xtsc, blk.dzt,
+                                              blk.dztsc, offs, None, blk.dwi, blk.status, d),
+        lambda: B.moe_permute_bwd(blk.dxs, blk.pos, blk.dx, d),
+    ]
+    work = mx_train_work(wl)
+    assert len(work) == len(calls)
+
+    def run(ev):
+        for c in calls:
+            if ev is not None:
+                e = torch.cuda.Event(enable_timing=True)
+                e.record()
+                ev.append(e)
+            c()
+        if ev is not None:
+            e = torch.cuda.Event(enable_timing=True)
+            e.record()
+            ev.append(e)
+
+    for _ in range(3):
+        run(None)
+    torch.cuda.synchronize()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if flushed else None
+    evs = []
+    with clock_sampler(dev) as clk:
+        for _ in range(steps):
+            if flush is not None:
+                flush.zero_()
+            ev = []
+            run(ev)
+            evs.append(ev)
+        torch.cuda.synchronize()
+    clocks = clk.summary()
+    if int(blk.status.item()) != 0:
+        raise RuntimeError(f"device status {int(blk.status.item())} after the MX training steps")
+    step_s = sum(ev[0].elapsed_time(ev[-1]) * 1e-3 for ev in evs) / steps
+    bf16_peak, bf16_src = tensor_peak(pk, clocks)
+    fp8_peak = 2.0 * bf16_peak
+    kern = {}
+    gemm_s = 0.0
+    for i, (n, kind, amount) in enumerate(work):
+        ts = [ev[i].elapsed_time(ev[i + 1]) * 1e-3 for ev in evs]
+        avg = sum(ts) / len(ts)
+        k = {"avg_us": avg * 1e6, "median_us": statistics.median(ts) * 1e6}
+        if kind == "tensor":
+            k["tflops"] = amount / avg / 1e12
+            k["frac_tensor"] = amount / avg / 1e12 / fp8_peak
+            gemm_s += avg
+        else:
+            k["gbs"] = amount / avg / 1e9
+            k["frac_hbm"] = amount / avg / 1e9 / pk["hbm"]
+        kern[n] = k
+    flops = sum(a for _, kind, a in work if kind == "tensor")
+    return {
+        "metric": "MoE block tokens/s (fwd+bwd, MXFP8)",
+        "value": wl.T / step_s,
+        "unit": "tokens/s",
+        "ms_per_step": step_s * 1e3,
+        "steps": steps,
+        "dtype": "e4m3 x e4m3 (E8M0 scales per 32) in all six GEMMs, fp32 accumulation, "
+                 "bf16 activations and gradients between them",
+        "step": "weights quantized (2 launches, both copies) + MX forward + MX backward",
+        "fp8_peak_tflops": fp8_peak,
+        "fp8_peak_source": f"nominal 2 x bf16: {bf16_src}",
+        "gemm_ms": gemm_s * 1e3,
+        "gemm_frac_tensor": flops / gemm_s / 1e12 / fp8_peak if gemm_s > 0 else None,
+        "clocks": {k: clocks.get(k) for k in ("sm_mhz", "sm_max_mhz", "reasons")},
+        "gpu_launches_per_step": len(calls) + 2,   # route_histogram is three launches
+        "kernels": kern,
+    }
+
+
 L2_BYTES = 129 << 20
 
 
@@ -745,9 +896,11 @@ def run_ours(args, dist, rank, world):
         del fstep
 
     # ---- the MXFP8 forward on the same inputs (a separate timed loop)
-    mx = None
+    mx = mx_train = None
     if not args.no_mx:
         mx = measure_mx(wl_rank, inp, args.steps, pk, flushed, dev)
+        if not fwd_only:
+            mx_train = measure_mx_train(wl_rank, inp, args.steps, pk, flushed, dev)
 
     # ---- end to end through the C ABI from pinned host buffers
     e2e = None
@@ -807,6 +960,9 @@ def run_ours(args, dist, rank, world):
     if mx is not None:
         mx["value"] *= world
         line["mxfp8_forward"] = mx
+    if mx_train is not None:
+        mx_train["value"] *= world
+        line["mxfp8_train"] = mx_train
     if configs is not None:
         line["configs"] = configs
     if rank == 0:

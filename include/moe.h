@@ -107,9 +107,10 @@ const char* moe_status_string(moe_status s);
 /* Version of this ABI; lets a loader check the library it opened without
  * touching a GPU.  2: adds the MXFP8 entry points (moe_mx_*) and the FC1
  * calls over expert ranges (moe_grouped_gemm_fc1_*_experts) to version 1's.
- * 3: adds moe_fused_forward.  4: adds the MXFP8 backward (moe_mx_*_bwd,
- * moe_mx_quantize_rows, moe_mx_quantize_tokens, the backward's MX buffers)
- * and z to moe_mx_grouped_gemm_fc1_swiglu. */
+ * 3: adds moe_fused_forward.  4: adds the MXFP8 backward
+ * (moe_mx_grouped_gemm_fc2_bwd and _fc1_bwd, moe_mx_quantize_rows, moe_mx_quantize_tokens, the backward's MX buffers),
+ * z to moe_mx_grouped_gemm_fc1_swiglu and the dgrad copies to
+ * moe_mx_quantize_wi/wo. */
 int moe_abi_version(void);
 
 /*
@@ -361,17 +362,22 @@ typedef enum {
 size_t moe_mx_bytes(moe_dims d, moe_mx_buffer which);
 
 /*
- * Grouped quantize of the expert weights (once per weight update):
+ * Grouped quantize of the expert weights (once per weight update), one read
+ * of the weight for both of its MX copies:
  *   moe_mx_quantize_wi: wi bf16 [E, D, 2F] -> wq [E, 2F, D] (interleaved
- *                       rows) + wsc, blocks along D;
+ *                       rows) + wsc, blocks along D (the forward's FC1), and
+ *                       wq_bwd [E, D, 2F] + wsc_bwd, blocks along 2F (the
+ *                       FC1 dgrad; see the MXFP8 backward below);
  *   moe_mx_quantize_wo: wo bf16 [E, F, D]  -> wq [E, D, F] + wsc, blocks
- *                       along F.
+ *                       along F (FC2), and wq_bwd [E, F, D] + wsc_bwd,
+ *                       blocks along D (the FC2 dgrad).
+ * Each (codes, scales) pair may be NULL (both of it), not both pairs.
  * Scale bytes of padding blocks are left as they are.
  */
-moe_status moe_mx_quantize_wi(const moe_bf16* wi, uint8_t* wq, uint8_t* wsc, moe_dims d,
-                              cudaStream_t stream);
-moe_status moe_mx_quantize_wo(const moe_bf16* wo, uint8_t* wq, uint8_t* wsc, moe_dims d,
-                              cudaStream_t stream);
+moe_status moe_mx_quantize_wi(const moe_bf16* wi, uint8_t* wq, uint8_t* wsc, uint8_t* wq_bwd,
+                              uint8_t* wsc_bwd, moe_dims d, cudaStream_t stream);
+moe_status moe_mx_quantize_wo(const moe_bf16* wo, uint8_t* wq, uint8_t* wsc, uint8_t* wq_bwd,
+                              uint8_t* wsc_bwd, moe_dims d, cudaStream_t stream);
 
 /*
  * Grouped FC1 quantize [TE MoE, Flowchart]: the permute of moe_permute with
@@ -420,10 +426,10 @@ moe_status moe_mx_grouped_gemm_fc2(const uint8_t* hq, const uint8_t* hsc, const 
  * blocks as above):
  *   FC2 dgrad  dh[r,f] = sum_d dys[r,d] * wo[e,f,d]: dys quantized along D
  *              (moe_mx_quantize_rows), wo along its last axis
- *              (moe_mx_quantize_wo_bwd); dh (fp32) goes straight into the
+ *              (wq_bwd of moe_mx_quantize_wo); dh (fp32) goes straight into the
  *              SwiGLU backward at z, giving dz bf16 [R, 2F] = [dgate | dup];
  *   FC1 dgrad  dxs[r,d] = bf16(sum_n dz[r,n] * wi[e,d,n]): dz along 2F, wi
- *              along its last axis (moe_mx_quantize_wi_bwd);
+ *              along its last axis (wq_bwd of moe_mx_quantize_wi);
  *   wgrads     dwo[e,f,d] = bf16(sum_{r in e} h[r,f] * dys[r,d]) and
  *              dwi[e,d,n] = bf16(sum_{r in e} xs[r,d] * dz[r,n]): both
  *              operands quantized along the tokens of each group
@@ -446,10 +452,6 @@ moe_status moe_mx_grouped_gemm_fc2(const uint8_t* hq, const uint8_t* hsc, const 
  * block at ((g * NBp(C)) + c / 128) * 512, byte (c % 128 % 32) * 16 +
  * (c % 128 / 32) * 4 + j for tokens [32j, 32j+32) of the tile.
  */
-moe_status moe_mx_quantize_wi_bwd(const moe_bf16* wi, uint8_t* wq, uint8_t* wsc, moe_dims d,
-                                  cudaStream_t stream);
-moe_status moe_mx_quantize_wo_bwd(const moe_bf16* wo, uint8_t* wq, uint8_t* wsc, moe_dims d,
-                                  cudaStream_t stream);
 /* src bf16 [R, C] in expert-sorted order (C = D for dys, 2F for dz) -> q
  * [R, C] codes and tile-blocked scales sc (blocks along C). */
 moe_status moe_mx_quantize_rows(const moe_bf16* src, int C, const int32_t* group_offsets,
@@ -461,7 +463,7 @@ moe_status moe_mx_quantize_rows(const moe_bf16* src, int C, const int32_t* group
 moe_status moe_mx_quantize_tokens(const moe_bf16* src, const int32_t* row_src, int C,
                                   const int32_t* group_offsets, uint8_t* qt, uint8_t* sct,
                                   moe_dims d, cudaStream_t stream);
-/* FC2 backward: dz from (dyq, dysc) and (woq, wosc) of moe_mx_quantize_wo_bwd
+/* FC2 backward: dz from (dyq, dysc) and (woq, wosc) = wq_bwd of moe_mx_quantize_wo
  * and z; dwo bf16 [E, F, D] from ht/htsc (h along tokens) and dyt/dytsc
  * (dys along tokens).  dz and dwo may each be NULL (their inputs then too),
  * not both. */
@@ -472,7 +474,7 @@ moe_status moe_mx_grouped_gemm_fc2_bwd(const uint8_t* dyq, const uint8_t* dysc,
                                        const int32_t* group_offsets, moe_bf16* dz, moe_bf16* dwo,
                                        int32_t* dev_status, moe_dims d, cudaStream_t stream);
 /* FC1 backward: dxs bf16 [R, D] from (dzq, dzsc) and (wiq, wisc) of
- * moe_mx_quantize_wi_bwd; dwi bf16 [E, D, 2F] from xt/xtsc (xs along
+ * moe_mx_quantize_wi (wq_bwd); dwi bf16 [E, D, 2F] from xt/xtsc (xs along
  * tokens) and dzt/dztsc (dz along tokens).  Either output may be NULL. */
 moe_status moe_mx_grouped_gemm_fc1_bwd(const uint8_t* dzq, const uint8_t* dzsc,
                                        const uint8_t* wiq, const uint8_t* wisc,

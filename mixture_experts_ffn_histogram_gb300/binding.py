@@ -34,8 +34,7 @@ ENTRY_POINTS = (
     "moe_mx_bytes", "moe_mx_quantize_wi", "moe_mx_quantize_wo", "moe_mx_permute_quantize",
     "moe_mx_grouped_gemm_fc1_swiglu", "moe_mx_grouped_gemm_fc2",
     "moe_grouped_gemm_fc1_swiglu_experts", "moe_grouped_gemm_fc1_bwd_experts",
-    "moe_fused_forward", "moe_mx_quantize_wi_bwd", "moe_mx_quantize_wo_bwd",
-    "moe_mx_quantize_rows", "moe_mx_quantize_tokens", "moe_mx_grouped_gemm_fc2_bwd",
+    "moe_fused_forward", "moe_mx_quantize_rows", "moe_mx_quantize_tokens", "moe_mx_grouped_gemm_fc2_bwd",
     "moe_mx_grouped_gemm_fc1_bwd",
 )
 
@@ -106,13 +105,11 @@ def lib() -> ctypes.CDLL:
             "moe_mx_bytes": ([D_, I], ctypes.c_size_t),
             "moe_grouped_gemm_fc1_swiglu_experts": ([P, P, P, I, I, P, P, P, P, D_, P], I),
             "moe_grouped_gemm_fc1_bwd_experts": ([P, P, P, P, I, I, P, P, P, P, D_, P], I),
-            "moe_mx_quantize_wi": ([P, P, P, D_, P], I),
-            "moe_mx_quantize_wo": ([P, P, P, D_, P], I),
+            "moe_mx_quantize_wi": ([P, P, P, P, P, D_, P], I),
+            "moe_mx_quantize_wo": ([P, P, P, P, P, D_, P], I),
             "moe_mx_permute_quantize": ([P, P, P, P, P, D_, P], I),
             "moe_mx_grouped_gemm_fc1_swiglu": ([P, P, P, P, P, P, P, P, P, P, D_, P], I),
             "moe_mx_grouped_gemm_fc2": ([P, P, P, P, P, P, P, D_, P], I),
-            "moe_mx_quantize_wi_bwd": ([P, P, P, D_, P], I),
-            "moe_mx_quantize_wo_bwd": ([P, P, P, D_, P], I),
             "moe_mx_quantize_rows": ([P, I, P, P, P, D_, P], I),
             "moe_mx_quantize_tokens": ([P, P, I, P, P, P, D_, P], I),
             "moe_mx_grouped_gemm_fc2_bwd": ([P] * 13 + [D_, P], I),
@@ -258,12 +255,14 @@ def moe_mx_bytes(d: MoeDims, which: int) -> int:
     return int(lib().moe_mx_bytes(d, int(which)))
 
 
-def moe_mx_quantize_wi(wi, wq, wsc, d: MoeDims, stream=None):
-    _ok("moe_mx_quantize_wi", lib().moe_mx_quantize_wi(_p(wi), _p(wq), _p(wsc), d, _s(stream)))
+def moe_mx_quantize_wi(wi, wq, wsc, d: MoeDims, stream=None, wq_bwd=None, wsc_bwd=None):
+    _ok("moe_mx_quantize_wi", lib().moe_mx_quantize_wi(_p(wi), _p(wq), _p(wsc), _p(wq_bwd),
+                                                       _p(wsc_bwd), d, _s(stream)))
 
 
-def moe_mx_quantize_wo(wo, wq, wsc, d: MoeDims, stream=None):
-    _ok("moe_mx_quantize_wo", lib().moe_mx_quantize_wo(_p(wo), _p(wq), _p(wsc), d, _s(stream)))
+def moe_mx_quantize_wo(wo, wq, wsc, d: MoeDims, stream=None, wq_bwd=None, wsc_bwd=None):
+    _ok("moe_mx_quantize_wo", lib().moe_mx_quantize_wo(_p(wo), _p(wq), _p(wsc), _p(wq_bwd),
+                                                       _p(wsc_bwd), d, _s(stream)))
 
 
 def moe_mx_permute_quantize(x, pos, group_offsets, xq, xsc, d: MoeDims, stream=None):
@@ -283,16 +282,6 @@ def moe_mx_grouped_gemm_fc2(hq, hsc, wq, wsc, group_offsets, ys, dev_status, d: 
     _ok("moe_mx_grouped_gemm_fc2", lib().moe_mx_grouped_gemm_fc2(
         _p(hq), _p(hsc), _p(wq), _p(wsc), _p(group_offsets), _p(ys), _p(dev_status), d,
         _s(stream)))
-
-
-def moe_mx_quantize_wi_bwd(wi, wq, wsc, d: MoeDims, stream=None):
-    _ok("moe_mx_quantize_wi_bwd", lib().moe_mx_quantize_wi_bwd(_p(wi), _p(wq), _p(wsc), d,
-                                                               _s(stream)))
-
-
-def moe_mx_quantize_wo_bwd(wo, wq, wsc, d: MoeDims, stream=None):
-    _ok("moe_mx_quantize_wo_bwd", lib().moe_mx_quantize_wo_bwd(_p(wo), _p(wq), _p(wsc), d,
-                                                               _s(stream)))
 
 
 def moe_mx_quantize_rows(src, C, group_offsets, q, sc, d: MoeDims, stream=None):

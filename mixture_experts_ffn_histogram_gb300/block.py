@@ -209,11 +209,11 @@ class MoEBlockMX:
         self.x = None
 
     def set_weights(self, wi, wo, stream=None):
-        B.moe_mx_quantize_wi(wi, self.wiq, self.wisc, self.d, stream)
-        B.moe_mx_quantize_wo(wo, self.woq, self.wosc, self.d, stream)
-        if self.train:
-            B.moe_mx_quantize_wi_bwd(wi, self.wiq_b, self.wisc_b, self.d, stream)
-            B.moe_mx_quantize_wo_bwd(wo, self.woq_b, self.wosc_b, self.d, stream)
+        tr = self.train
+        B.moe_mx_quantize_wi(wi, self.wiq, self.wisc, self.d, stream,
+                             wq_bwd=self.wiq_b if tr else None, wsc_bwd=self.wisc_b if tr else None)
+        B.moe_mx_quantize_wo(wo, self.woq, self.wosc, self.d, stream,
+                             wq_bwd=self.woq_b if tr else None, wsc_bwd=self.wosc_b if tr else None)
 
     def forward(self, x, logits=None, bias=None, ids=None, w=None, stream=None):
         d = self.d

@@ -439,22 +439,33 @@ size_t moe_mx_bytes(moe_dims d, moe_mx_buffer which) {
   return 0;
 }
 
-moe_status moe_mx_quantize_wi(const moe_bf16* wi, uint8_t* wq, uint8_t* wsc, moe_dims d,
+namespace {
+moe_status mx_quantize_weight(const moe_bf16* w, uint8_t* wq, uint8_t* wsc, uint8_t* wq_bwd,
+                              uint8_t* wsc_bwd, int E, int Kd, int N, bool fc1,
                               cudaStream_t stream) {
+  MOE_REQUIRE(w);
+  MOE_OPTIONAL(wq);
+  MOE_OPTIONAL(wsc);
+  MOE_OPTIONAL(wq_bwd);
+  MOE_OPTIONAL(wsc_bwd);
+  if ((wq == nullptr) != (wsc == nullptr) || (wq_bwd == nullptr) != (wsc_bwd == nullptr))
+    return MOE_ERR_INVALID_ARG;
+  if (wq == nullptr && wq_bwd == nullptr) return MOE_ERR_INVALID_ARG;
+  return from_cuda(moe::launch_mx_quantize_weights(w, wq, wsc, wq_bwd, wsc_bwd, E, Kd, N, fc1,
+                                                   stream));
+}
+}  // namespace
+
+moe_status moe_mx_quantize_wi(const moe_bf16* wi, uint8_t* wq, uint8_t* wsc, uint8_t* wq_bwd,
+                              uint8_t* wsc_bwd, moe_dims d, cudaStream_t stream) {
   MOE_CHECK_DIMS(d);
-  MOE_REQUIRE(wi);
-  MOE_REQUIRE(wq);
-  MOE_REQUIRE(wsc);
-  return from_cuda(moe::launch_mx_quantize_weights(wi, wq, wsc, d.E, d.D, 2 * d.F, true, stream));
+  return mx_quantize_weight(wi, wq, wsc, wq_bwd, wsc_bwd, d.E, d.D, 2 * d.F, true, stream);
 }
 
-moe_status moe_mx_quantize_wo(const moe_bf16* wo, uint8_t* wq, uint8_t* wsc, moe_dims d,
-                              cudaStream_t stream) {
+moe_status moe_mx_quantize_wo(const moe_bf16* wo, uint8_t* wq, uint8_t* wsc, uint8_t* wq_bwd,
+                              uint8_t* wsc_bwd, moe_dims d, cudaStream_t stream) {
   MOE_CHECK_DIMS(d);
-  MOE_REQUIRE(wo);
-  MOE_REQUIRE(wq);
-  MOE_REQUIRE(wsc);
-  return from_cuda(moe::launch_mx_quantize_weights(wo, wq, wsc, d.E, d.F, d.D, false, stream));
+  return mx_quantize_weight(wo, wq, wsc, wq_bwd, wsc_bwd, d.E, d.F, d.D, false, stream);
 }
 
 moe_status moe_mx_permute_quantize(const moe_bf16* x, const int32_t* pos,
@@ -510,24 +521,6 @@ moe_status moe_mx_grouped_gemm_fc2(const uint8_t* hq, const uint8_t* hsc, const 
   moe::MxGemmCall c{moe::MxKind::kRows, hq, hsc, wq, wsc, group_offsets, nullptr, nullptr, ys,
                     nullptr, nullptr, dev_status, d, d.F, d.D, 0};
   return from_cuda(moe::launch_mx_grouped_gemm(c, stream));
-}
-
-moe_status moe_mx_quantize_wi_bwd(const moe_bf16* wi, uint8_t* wq, uint8_t* wsc, moe_dims d,
-                                  cudaStream_t stream) {
-  MOE_CHECK_DIMS(d);
-  MOE_REQUIRE(wi);
-  MOE_REQUIRE(wq);
-  MOE_REQUIRE(wsc);
-  return from_cuda(moe::launch_mx_quantize_lastaxis(wi, wq, wsc, d.E, d.D, 2 * d.F, stream));
-}
-
-moe_status moe_mx_quantize_wo_bwd(const moe_bf16* wo, uint8_t* wq, uint8_t* wsc, moe_dims d,
-                                  cudaStream_t stream) {
-  MOE_CHECK_DIMS(d);
-  MOE_REQUIRE(wo);
-  MOE_REQUIRE(wq);
-  MOE_REQUIRE(wsc);
-  return from_cuda(moe::launch_mx_quantize_lastaxis(wo, wq, wsc, d.E, d.F, d.D, stream));
 }
 
 moe_status moe_mx_quantize_rows(const moe_bf16* src, int C, const int32_t* group_offsets,

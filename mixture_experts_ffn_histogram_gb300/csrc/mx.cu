@@ -121,6 +121,62 @@ __device__ __forceinline__ uint32_t mx_quant32(const float (&v)[32], uint32_t (&
 // scale block.
 __device__ __forceinline__ int sf_byte(int m, int j) { return (m & 31) * 16 + (m >> 5) * 4 + j; }
 
+// Shared exponent from the 8-bit exponent field of a block's largest
+// magnitude (bf16 and fp32 share it): floor(log2 amax) - 8, -127 for zero
+// and subnormals.
+__device__ __forceinline__ int mx_exp_field(uint32_t ef) {
+  return ef == 0 ? -127 : max(static_cast<int>(ef) - 127 - 8, -127);
+}
+// Two codes (low byte first) of two fp32 values already scaled.
+__device__ __forceinline__ uint32_t e4m3x2(float a, float b) {
+  return __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3) & 0xFFFFu;
+}
+// MX blocks of two columns at once: w[i] holds row i of column A (low bf16)
+// and of column B (high bf16), i = 0..31.  The largest magnitudes come from
+// a per-halfword unsigned max of the sign-cleared bf16 bits (magnitude order
+// is the unsigned order of those bits).  Returns the two scale bytes (A in
+// bits 0-7, B in 8-15); ca/cb get the 32 codes of each column in row order.
+__device__ __forceinline__ uint32_t mx_quant_col2(const uint32_t (&w)[32], uint32_t (&ca)[8],
+                                                  uint32_t (&cb)[8]) {
+  uint32_t m = 0;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) m = __vmaxu2(m, w[i] & 0x7FFF7FFFu);
+  const int sa = mx_exp_field((m >> 7) & 0xFFu), sb = mx_exp_field((m >> 23) & 0xFFu);
+  const float ma = mx_inv_scale(sa), mb = mx_inv_scale(sb);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint32_t* r = w + 4 * i;
+    const uint32_t a01 = e4m3x2(__uint_as_float(r[0] << 16) * ma, __uint_as_float(r[1] << 16) * ma);
+    const uint32_t a23 = e4m3x2(__uint_as_float(r[2] << 16) * ma, __uint_as_float(r[3] << 16) * ma);
+    const uint32_t b01 = e4m3x2(__uint_as_float(r[0] & 0xFFFF0000u) * mb,
+                                __uint_as_float(r[1] & 0xFFFF0000u) * mb);
+    const uint32_t b23 = e4m3x2(__uint_as_float(r[2] & 0xFFFF0000u) * mb,
+                                __uint_as_float(r[3] & 0xFFFF0000u) * mb);
+    ca[i] = __byte_perm(a01, a23, 0x5410);
+    cb[i] = __byte_perm(b01, b23, 0x5410);
+  }
+  return static_cast<uint32_t>(sa + 127) | (static_cast<uint32_t>(sb + 127) << 8);
+}
+// One MX block of 32 consecutive bf16 (w[i] = elements 2i, 2i+1): codes and
+// the scale byte.
+__device__ __forceinline__ uint32_t mx_quant_row32(const uint32_t (&w)[16], uint32_t (&c)[8]) {
+  uint32_t m = 0;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) m = __vmaxu2(m, w[i] & 0x7FFF7FFFu);
+  m = max(m & 0xFFFFu, m >> 16);
+  const int s = mx_exp_field((m >> 7) & 0xFFu);
+  const float mul = mx_inv_scale(s);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint32_t lo = e4m3x2(__uint_as_float(w[2 * i] << 16) * mul,
+                               __uint_as_float(w[2 * i] & 0xFFFF0000u) * mul);
+    const uint32_t hi = e4m3x2(__uint_as_float(w[2 * i + 1] << 16) * mul,
+                               __uint_as_float(w[2 * i + 1] & 0xFFFF0000u) * mul);
+    c[i] = __byte_perm(lo, hi, 0x5410);
+  }
+  return static_cast<uint32_t>(s + 127);
+}
+
 // Group offsets into shared memory (all threads), then the exclusive prefix
 // of ceil(rows/128) over the groups (one warp).  Ends with __syncthreads().
 __device__ __forceinline__ void load_tile_bases(const int32_t* offs, int E, int* s_off, int* s_tb,
@@ -160,59 +216,266 @@ __device__ __forceinline__ int group_of_row(const int* s_off, int E, int r) {
   return lo;
 }
 
-// ------------------------------------------------------- weight quantize
-// w [E][Kd][N] bf16 (the contraction axis Kd is the middle one) -> q [E][N][Kd]
-// codes with blocked scales [E][KB][NBp][512].  FC1's output rows are
-// interleaved in 64-row chunks, gate chunk then up chunk: logical column n
-// of wi (gate f = n < F, up f = n - F) lands on row 128*(f/64) + 64*(n >= F)
-// + f%64, so that each 128-row half of a 256-row tile holds 64 gate and the
-// matching 64 up columns.  One block quantizes 128 contraction rows x 64
-// columns: coalesced 128-byte loads, a transpose through shared memory, one
-// 32-element block per thread.
-__global__ void __launch_bounds__(256) mx_quantize_weights_kernel(const uint16_t* __restrict__ w,
-                                                                  uint8_t* __restrict__ q,
-                                                                  uint8_t* __restrict__ sc, int Kd,
-                                                                  int N, int KB, int NBp,
-                                                                  int fc1) {
-  __shared__ float tile[128][65];
-  const int n0 = blockIdx.x * 64, k0 = blockIdx.y * 128, e = blockIdx.z;
+// ------------------------------------------------- transpose-quantize
+// MX quantization along the ROWS of a bf16 matrix tile of 128 rows x 128
+// columns, stored transposed: each column's 128 values form four 32-element
+// blocks; a thread takes two adjacent columns of one block (one 32-bit
+// shared-memory read per row gives both, and their largest magnitudes come
+// from packed integer maxima of the bf16 bits).  The input tile is staged
+// in shared memory as bf16 (32 KB), copied with 16-byte cp.async row
+// segments (a warp reads two 256-byte row pieces); the codes are gathered
+// into a 128-byte-swizzled output tile (a row per column) that two TMA
+// stores write out, 64 output rows each (writing each column's 32 codes
+// from its own thread touched 32 lines per warp store and ran at half the
+// HBM rate).
+// Two uses:
+//   tokens   rows = 128 expert-sorted rows of tile g of group e (rows past
+//            the group's end as zeros), read in place or gathered from x at
+//            token row_src[r] / K: codes qt[c][128 g .. 128 g + 127], scales
+//            [TB][NBp(C)][512] block (g, c / 128);
+//   weights  rows = k-block kb of expert e of w [E][Kd][N] (rows past Kd as
+//            zeros): codes q[e][p(n)][Kd] with 128 (or, at a ragged last
+//            k-block, 64) bytes per column, scales [E][KB][NBp][512]; FC1's
+//            output rows are interleaved in 64-row chunks, gate chunk then up
+//            chunk: column n of wi (gate f = n < F, up f = n - F) lands on
+//            row p = 128 (f / 64) + 64 (n >= F) + f % 64, so that each
+//            128-row half of a 256-row tile holds 64 gate and the matching
+//            64 up columns.  Optionally the same tile also gives the weight
+//            quantized along its LAST axis N (the dgrads' contraction axis),
+//            codes in w's own layout and scales [E][KB(N)][NBp(Kd)][512].
+constexpr int kTqRows = 128;
+constexpr int kTqCols = 128;
+constexpr int kTqThreads = 256;
+constexpr int kTqBuf = kTqRows * kTqCols * 2;  // bytes of one staged input tile (32 KB)
+constexpr int kTqOut = kTqCols * 128;          // the codes of one item: 128 columns x 128 B
+// input double buffer, the output tile (two 64-row halves, 128-byte swizzled
+// for the TMA store), one 512-byte scale block, and slack for 1024-alignment
+constexpr int kTqSmem = 2 * kTqBuf + kTqOut + 512 + 1024;
+constexpr int kTqCtasPerSm = 2;
+
+struct TqArgs {
+  const uint16_t* src;     // tokens: [R or T][C]; weights: w [E][Kd][N]
+  const int32_t* row_src;  // tokens: gather through row_src[r] / K, or nullptr
+  const int32_t* offs;     // tokens: group offsets
+  uint8_t* q;              // transposed codes (see above), or nullptr (weights)
+  uint8_t* sc;
+  uint8_t* q2;             // weights: last-axis codes [E][Kd][N], or nullptr
+  uint8_t* sc2;
+  long Rp;                 // tokens: token columns of qt
+  int C;                   // columns (tokens: C; weights: N)
+  int K;                   // tokens: slots per token (row_src / K)
+  int E;
+  int Kd;                  // weights: rows per expert
+  int KB;                  // weights: k-blocks of Kd
+  int NBp;                 // 128-row scale blocks of the transposed output, even
+  int KB2;                 // weights: k-blocks of N (last-axis scales)
+  int NBp2;                // weights: 128-row blocks of Kd (last-axis scales)
+  int interleave;          // weights: FC1 row interleave
+};
+
+// One work item: 128 source rows from row0 (rows of them valid) x 128
+// columns from c0; tokens: tile g of group e; weights: k-block kb of expert e.
+struct TqItem {
+  long row0;
+  int rows, c0, e, g, kb;
+};
+
+// Persistent: each CTA takes work items it = blockIdx.x, + gridDim.x, ...
+// and copies the next item's tile into the other buffer (cp.async, rows past
+// the valid ones zero-filled) while it quantizes the current one.
+template <bool TOKENS>
+__global__ void __launch_bounds__(kTqThreads, kTqCtasPerSm)
+    mx_transpose_quantize_kernel(const __grid_constant__ CUtensorMap map_q, const TqArgs a) {
+  extern __shared__ __align__(128) uint8_t tq_raw[];
+  uint8_t* tq_smem = tq_raw + ((1024u - (smem_u32(tq_raw) & 1023u)) & 1023u);
+  uint8_t* stage = tq_smem + 2 * kTqBuf;  // codes: [2 halves][64 rows][128 B], swizzled
+  uint8_t* s_sc = stage + kTqOut;         // tokens: the item's scale block
+  __shared__ int s_off[TOKENS ? kMaxE + 1 : 1];
+  __shared__ int s_tb[TOKENS ? kMaxE + 1 : 1];
   const int tid = threadIdx.x;
-  const uint16_t* src = w + (static_cast<size_t>(e) * Kd + k0) * N + n0;
+  const int nchunks = (a.C + kTqCols - 1) / kTqCols;
+  long n_items;
+  if constexpr (TOKENS) {
+    load_tile_bases(a.offs, a.E, s_off, s_tb, 0);
+    n_items = static_cast<long>(s_tb[a.E]) * nchunks;
+  } else {
+    n_items = static_cast<long>(nchunks) * a.KB * a.E;
+  }
+  auto decode = [&](long it) {
+    TqItem I;
+    const int chunk = static_cast<int>(it % nchunks);
+    const long rest = it / nchunks;
+    I.c0 = chunk * kTqCols;
+    if constexpr (TOKENS) {
+      I.g = static_cast<int>(rest);
+      int lo = 0, hi = a.E - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (s_tb[mid] <= I.g) lo = mid;
+        else hi = mid - 1;
+      }
+      I.e = lo;
+      I.kb = 0;
+      I.row0 = s_off[lo] + 128L * (I.g - s_tb[lo]);
+      I.rows = min(128, static_cast<int>(s_off[lo + 1] - I.row0));
+    } else {
+      I.kb = static_cast<int>(rest % a.KB);
+      I.e = static_cast<int>(rest / a.KB);
+      I.g = 0;
+      I.row0 = static_cast<long>(I.e) * a.Kd + 128L * I.kb;
+      I.rows = min(128, a.Kd - 128 * I.kb);
+    }
+    return I;
+  };
+  // 128 rows x 16 16-byte segments: 8 per thread, a warp per two 256-byte
+  // rows; the gathered rows' indices are all loaded before any copy
+  auto issue = [&](const TqItem& I, uint8_t* buf) {
+    const int seg = tid & 15;
+    const bool col_ok = I.c0 + 8 * seg < a.C;
+    long sr[8];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int idx = tid + 256 * i;
-    const int row = idx >> 3, c8 = idx & 7;
-    if (k0 + row < Kd) {
-      const uint4 u = *reinterpret_cast<const uint4*>(src + static_cast<size_t>(row) * N + 8 * c8);
-      const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
+    for (int i = 0; i < 8; ++i) {
+      const int r = 16 * i + (tid >> 4);
+      sr[i] = (r < I.rows && col_ok) ? I.row0 + r : -1;
+      if (TOKENS && a.row_src != nullptr && sr[i] >= 0) sr[i] = __ldg(a.row_src + sr[i]);
+    }
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        tile[row][8 * c8 + 2 * j] = bf16lo(wv[j]);
-        tile[row][8 * c8 + 2 * j + 1] = bf16hi(wv[j]);
+    for (int i = 0; i < 8; ++i) {
+      const int r = 16 * i + (tid >> 4);
+      long row = sr[i];
+      if (TOKENS && a.row_src != nullptr && row >= 0) row /= a.K;
+      const uint16_t* src = row >= 0 ? a.src + row * a.C + I.c0 + 8 * seg : a.src;
+      cp_async16_zfill(buf + r * (kTqCols * 2) + 16 * seg, src, row >= 0 ? 16 : 0);
+    }
+    cp_async_commit();
+  };
+
+  long it = blockIdx.x;
+  if (it >= n_items) return;  // block-uniform
+  if (tid == 0 && a.q != nullptr) tma_prefetch_map(&map_q);
+  TqItem cur = decode(it);
+  issue(cur, tq_smem);
+  for (int k = 0; it < n_items; it += gridDim.x, ++k) {
+    const long nx = it + gridDim.x;
+    TqItem nxt = cur;
+    if (nx < n_items) {
+      nxt = decode(nx);
+      issue(nxt, tq_smem + ((k + 1) & 1) * kTqBuf);
+      cp_async_wait_group<1>();
+    } else {
+      cp_async_wait_group<0>();
+    }
+    if (tid == 0) bulk_wait_read<0>();  // the previous item's stores have read the stage
+    __syncthreads();
+    const uint8_t* tile = tq_smem + (k & 1) * kTqBuf;
+    // ---- two adjacent columns and one 32-row block per thread; the codes go
+    // to the swizzled output tile (row = column), written by two TMA stores
+    if (a.q != nullptr) {
+      const int cp = tid & 63, b = tid >> 6;
+      const int cl = 2 * cp;
+      const int c = cur.c0 + cl;
+      uint32_t ca[8], cb[8], sab = 0;
+      const bool ok = c < a.C && (TOKENS || 32 * b < cur.rows);
+      // (tokens: rows past the group's end are quantized too, giving zero
+      // codes and the zero block's scale; weights: rows past Kd are clipped
+      // by the store)
+      if (ok) {
+        uint32_t w[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          w[i] = *reinterpret_cast<const uint32_t*>(tile + (32 * b + i) * (kTqCols * 2) + 4 * cp);
+        sab = mx_quant_col2(w, ca, cb);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) ca[i] = cb[i] = 0u;
+      }
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int row = cl + h;  // output tile row (0..127)
+        const uint32_t* cw = h ? cb : ca;
+        uint8_t* rbase = stage + (row >> 6) * (kTqOut / 2) + (row & 63) * 128;
+        *reinterpret_cast<uint4*>(rbase + (((2 * b) ^ (row & 7)) << 4)) =
+            make_uint4(cw[0], cw[1], cw[2], cw[3]);
+        *reinterpret_cast<uint4*>(rbase + (((2 * b + 1) ^ (row & 7)) << 4)) =
+            make_uint4(cw[4], cw[5], cw[6], cw[7]);
+        const uint8_t sbyte = static_cast<uint8_t>(sab >> (8 * h));
+        if constexpr (TOKENS) {
+          s_sc[sf_byte(row, b)] = sbyte;
+        } else if (ok) {
+          const int cc = c + h;
+          int p = cc;
+          if (a.interleave) {
+            const int F = a.C / 2;
+            const int f = cc < F ? cc : cc - F;
+            p = 128 * (f >> 6) + (cc < F ? 0 : 64) + (f & 63);
+          }
+          const size_t sblk = (static_cast<size_t>(cur.e) * a.KB + cur.kb) * a.NBp + (p >> 7);
+          a.sc[sblk * 512 + sf_byte(p & 127, b)] = sbyte;
+        }
+      }
+      fence_proxy_async_smem();
+      __syncthreads();
+      if (tid == 0) {
+        for (int hh = 0; hh < 2; ++hh) {
+          const int cf = cur.c0 + 64 * hh;  // first column of the half
+          if (cf >= a.C) break;
+          if constexpr (TOKENS) {
+            tma_store_2d(&map_q, stage + hh * (kTqOut / 2), 128 * cur.g, cf);
+          } else {
+            int p0 = cf;
+            if (a.interleave) {
+              const int F = a.C / 2;
+              const bool up = cf >= F;
+              p0 = 128 * ((cf - (up ? F : 0)) >> 6) + (up ? 64 : 0);
+            }
+            tma_store_2d(&map_q, stage + hh * (kTqOut / 2), 128 * cur.kb, cur.e * a.C + p0);
+          }
+        }
+        bulk_commit();
+      }
+      if constexpr (TOKENS) {
+        if (tid < 32) {
+          const size_t sblk = static_cast<size_t>(cur.g) * a.NBp + (cur.c0 >> 7);
+          reinterpret_cast<uint4*>(a.sc + sblk * 512)[tid] =
+              reinterpret_cast<const uint4*>(s_sc)[tid];
+        }
       }
     }
-  }
-  __syncthreads();
-  const int n = tid & 63, blk = tid >> 6;
-  const int k = k0 + 32 * blk;
-  if (k >= Kd) return;
-  float v[32];
+    if constexpr (!TOKENS) {
+      // ---- the same tile along its last axis: 4 blocks of 32 columns per row
+      if (a.q2 != nullptr) {
+        for (int id = tid; id < kTqRows * 4; id += kTqThreads) {
+          const int r = id >> 2, nb = id & 3;
+          const int n0 = cur.c0 + 32 * nb;
+          if (r >= cur.rows || n0 >= a.C) continue;
+          uint32_t w[16];
+          const uint4* src4 = reinterpret_cast<const uint4*>(tile + r * (kTqCols * 2) + 64 * nb);
 #pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = tile[32 * blk + i][n];
-  uint32_t codes[8];
-  const uint32_t sbyte = mx_quant32(v, codes);
-  const int ng = n0 + n;
-  int p = ng;
-  if (fc1) {
-    const int F = N / 2;
-    const int f = ng < F ? ng : ng - F;
-    p = 128 * (f >> 6) + (ng < F ? 0 : 64) + (f & 63);
+          for (int i = 0; i < 4; ++i) {
+            const uint4 u = src4[i];
+            w[4 * i] = u.x;
+            w[4 * i + 1] = u.y;
+            w[4 * i + 2] = u.z;
+            w[4 * i + 3] = u.w;
+          }
+          uint32_t codes[8];
+          const uint32_t sbyte = mx_quant_row32(w, codes);
+          const long kr = 128L * cur.kb + r;  // row of the expert
+          uint4* d4 =
+              reinterpret_cast<uint4*>(a.q2 + (static_cast<size_t>(cur.e) * a.Kd + kr) * a.C + n0);
+          d4[0] = make_uint4(codes[0], codes[1], codes[2], codes[3]);
+          d4[1] = make_uint4(codes[4], codes[5], codes[6], codes[7]);
+          const size_t blk =
+              (static_cast<size_t>(cur.e) * a.KB2 + (n0 >> 7)) * a.NBp2 + (kr >> 7);
+          a.sc2[blk * 512 + sf_byte(static_cast<int>(kr & 127), (n0 & 127) >> 5)] =
+              static_cast<uint8_t>(sbyte);
+        }
+      }
+    }
+    __syncthreads();  // the input buffer is refilled two items on
+    cur = nxt;
   }
-  uint4* dst = reinterpret_cast<uint4*>(q + (static_cast<size_t>(e) * N + p) * Kd + k);
-  dst[0] = make_uint4(codes[0], codes[1], codes[2], codes[3]);
-  dst[1] = make_uint4(codes[4], codes[5], codes[6], codes[7]);
-  const size_t blkoff = ((static_cast<size_t>(e) * KB + (k >> 7)) * NBp + (p >> 7)) * 512;
-  sc[blkoff + sf_byte(p & 127, (k & 127) >> 5)] = static_cast<uint8_t>(sbyte);
+  if (tid == 0) bulk_wait_all();
 }
 
 // ------------------------------------------------ permute + quantize
@@ -323,109 +586,6 @@ __global__ void __launch_bounds__(256) mx_permute_quantize_kernel(
     }
     __syncwarp();
   }
-}
-
-// ------------------------------------------------ last-axis quantize
-// w [E][N][Kd] -> codes in the same layout (blocks along the contiguous
-// last axis) and scales [E][KB][NBp][512]: one 32-element block per thread,
-// consecutive threads on consecutive blocks of a row.
-__global__ void __launch_bounds__(256) mx_quantize_lastaxis_kernel(const uint16_t* __restrict__ w,
-                                                                   uint8_t* __restrict__ q,
-                                                                   uint8_t* __restrict__ sc,
-                                                                   long nblocks, int N, int Kd,
-                                                                   int KB, int NBp) {
-  const long i = static_cast<long>(blockIdx.x) * 256 + threadIdx.x;
-  if (i >= nblocks) return;
-  const int nb = Kd / 32;
-  const long row = i / nb;
-  const int b = static_cast<int>(i - row * nb);
-  const int e = static_cast<int>(row / N), n = static_cast<int>(row - static_cast<long>(e) * N);
-  const uint4* src = reinterpret_cast<const uint4*>(w + row * Kd + 32 * b);
-  float v[32];
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const uint4 u = src[k];
-    const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      v[8 * k + 2 * j] = bf16lo(wv[j]);
-      v[8 * k + 2 * j + 1] = bf16hi(wv[j]);
-    }
-  }
-  uint32_t codes[8];
-  const uint32_t sbyte = mx_quant32(v, codes);
-  uint4* dst = reinterpret_cast<uint4*>(q + row * Kd + 32 * b);
-  dst[0] = make_uint4(codes[0], codes[1], codes[2], codes[3]);
-  dst[1] = make_uint4(codes[4], codes[5], codes[6], codes[7]);
-  sc[((static_cast<size_t>(e) * KB + (b >> 2)) * NBp + (n >> 7)) * 512 + sf_byte(n & 127, b & 3)] =
-      static_cast<uint8_t>(sbyte);
-}
-
-// ------------------------------------------------- token-axis quantize
-// The weight gradients contract over the tokens of each group, so their
-// operands are quantized along the token axis and stored transposed:
-// codes qt [C][Rp], the rows of group e in 128-row tiles from its first
-// row (tile g = tb[e] + i covers token columns 128g .. 128g + 127, rows
-// past the group's end as zeros) and scales [TB][NBp][512], tile g's
-// 128-column block of rows c = 128j .. at ((g * NBp) + j) * 512, byte
-// sf_byte(c % 128, 32-row step).  One block per (tile, 64 columns): coalesced
-// 128-byte row loads (gathered through row_src / K when given), a transpose
-// through shared memory, one 32-row block per thread.
-__global__ void __launch_bounds__(256) mx_quantize_tokens_kernel(
-    const uint16_t* __restrict__ src, const int32_t* __restrict__ row_src, int gather_k,
-    const int32_t* __restrict__ offs, uint8_t* __restrict__ qt, uint8_t* __restrict__ sct, int C,
-    int E, long Rp, int NBp) {
-  __shared__ int s_off[kMaxE + 1];
-  __shared__ int s_tb[kMaxE + 1];
-  __shared__ float tile[128][65];
-  load_tile_bases(offs, E, s_off, s_tb, 0);
-  const int g = blockIdx.y;
-  if (g >= s_tb[E]) return;  // block-uniform
-  int lo = 0, hi = E - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (s_tb[mid] <= g) lo = mid;
-    else hi = mid - 1;
-  }
-  const int row0 = s_off[lo] + 128 * (g - s_tb[lo]);
-  const int rows = min(128, s_off[lo + 1] - row0);
-  const int c0 = blockIdx.x * 64;
-  const int tid = threadIdx.x;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int idx = tid + 256 * i;
-    const int row = idx >> 3, c8 = idx & 7;
-    long sr = -1;
-    if (row < rows) {
-      sr = row0 + row;
-      if (row_src != nullptr) {
-        const int j = __ldg(row_src + sr);
-        sr = j >= 0 ? j / gather_k : -1;
-      }
-    }
-    uint4 u = make_uint4(0u, 0u, 0u, 0u);
-    if (sr >= 0) u = *reinterpret_cast<const uint4*>(src + sr * C + c0 + 8 * c8);
-    const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      tile[row][8 * c8 + 2 * j] = bf16lo(wv[j]);
-      tile[row][8 * c8 + 2 * j + 1] = bf16hi(wv[j]);
-    }
-  }
-  __syncthreads();
-  const int n = tid & 63, blk = tid >> 6;
-  float v[32];
-#pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = tile[32 * blk + i][n];
-  uint32_t codes[8];
-  const uint32_t sbyte = mx_quant32(v, codes);
-  const int c = c0 + n;
-  uint4* dst = reinterpret_cast<uint4*>(qt + static_cast<size_t>(c) * Rp + 128 * static_cast<size_t>(g) +
-                                        32 * blk);
-  dst[0] = make_uint4(codes[0], codes[1], codes[2], codes[3]);
-  dst[1] = make_uint4(codes[4], codes[5], codes[6], codes[7]);
-  sct[(static_cast<size_t>(g) * NBp + (c >> 7)) * 512 + sf_byte(c & 127, blk)] =
-      static_cast<uint8_t>(sbyte);
 }
 
 // ---------------------------------------------------------------- GEMM
@@ -960,15 +1120,57 @@ cudaError_t launch_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const CUte
   return cudaGetLastError();
 }
 
+template <bool TOKENS>
+cudaError_t launch_tq(const TqArgs& a, const CUtensorMap& map_q, long max_items,
+                      cudaStream_t s) {
+  auto kern = mx_transpose_quantize_kernel<TOKENS>;
+  static std::atomic<bool> attr_set[64];
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!attr_set[dev].load(std::memory_order_acquire)) {
+    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kTqSmem);
+    if (err != cudaSuccess) return err;
+    attr_set[dev].store(true, std::memory_order_release);
+  }
+  long grid = static_cast<long>(kTqCtasPerSm) * sm_count();
+  if (max_items < grid) grid = max_items;
+  if (grid <= 0) return cudaSuccess;
+  kern<<<static_cast<unsigned>(grid), kTqThreads, kTqSmem, s>>>(map_q, a);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
-cudaError_t launch_mx_quantize_weights(const uint16_t* w, uint8_t* q, uint8_t* sc, int E, int Kd,
-                                       int N, bool fc1_interleave, cudaStream_t s) {
-  const int KB = static_cast<int>(mx_kblocks(Kd));
-  const int NBp = static_cast<int>(mx_weight_row_blocks(N));
-  dim3 grid(static_cast<unsigned>(N / 64), static_cast<unsigned>(KB), static_cast<unsigned>(E));
-  mx_quantize_weights_kernel<<<grid, 256, 0, s>>>(w, q, sc, Kd, N, KB, NBp, fc1_interleave ? 1 : 0);
-  return cudaGetLastError();
+cudaError_t launch_mx_quantize_weights(const uint16_t* w, uint8_t* q, uint8_t* sc, uint8_t* q2,
+                                       uint8_t* sc2, int E, int Kd, int N, bool fc1_interleave,
+                                       cudaStream_t s) {
+  TqArgs a{};
+  a.src = w;
+  a.q = q;
+  a.sc = sc;
+  a.q2 = q2;
+  a.sc2 = sc2;
+  a.C = N;
+  a.E = E;
+  a.Kd = Kd;
+  a.KB = static_cast<int>(mx_kblocks(Kd));
+  a.NBp = static_cast<int>(mx_weight_row_blocks(N));
+  a.KB2 = static_cast<int>(mx_kblocks(N));
+  a.NBp2 = static_cast<int>(mx_weight_row_blocks(Kd));
+  a.interleave = fc1_interleave ? 1 : 0;
+  CUtensorMap mq{};
+  if (q != nullptr) {  // the transposed codes as [E * N rows][Kd], 64-row stores
+    const uint64_t dims[2] = {static_cast<uint64_t>(Kd), static_cast<uint64_t>(E) * N};
+    const uint64_t str[1] = {static_cast<uint64_t>(Kd)};
+    const uint32_t box[2] = {128, 64};
+    if (!make_map(&mq, CU_TENSOR_MAP_DATA_TYPE_UINT8, q, 2, dims, str, box,
+                  CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+  }
+  const long items = mx_cdiv(N, kTqCols) * a.KB * E;
+  return launch_tq<false>(a, mq, items, s);
 }
 
 cudaError_t launch_mx_permute_quantize(const uint16_t* x, const int32_t* pos, const int32_t* offs,
@@ -980,16 +1182,6 @@ cudaError_t launch_mx_permute_quantize(const uint16_t* x, const int32_t* pos, co
   if (blocks > cap) blocks = cap;
   mx_permute_quantize_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(
       x, pos, offs, xq, xsc, d.T, d.D, d.K, d.E, static_cast<int>(mx_kblocks(d.D)));
-  return cudaGetLastError();
-}
-
-cudaError_t launch_mx_quantize_lastaxis(const uint16_t* w, uint8_t* q, uint8_t* sc, int E, int N,
-                                        int Kd, cudaStream_t s) {
-  const long nblocks = static_cast<long>(E) * N * (Kd / 32);
-  if (nblocks == 0) return cudaSuccess;
-  mx_quantize_lastaxis_kernel<<<static_cast<unsigned>(mx_cdiv(nblocks, 256)), 256, 0, s>>>(
-      w, q, sc, nblocks, N, Kd, static_cast<int>(mx_kblocks(Kd)),
-      static_cast<int>(mx_weight_row_blocks(N)));
   return cudaGetLastError();
 }
 
@@ -1010,13 +1202,25 @@ cudaError_t launch_mx_quantize_tokens(const uint16_t* src, const int32_t* row_sr
                                       const int32_t* offs, uint8_t* qt, uint8_t* sct, int C,
                                       const moe_dims& d, cudaStream_t s) {
   if (static_cast<long>(d.T) * d.K == 0) return cudaSuccess;
-  const long tiles = mx_tile_bound(d);
-  if (tiles > 65535) return cudaErrorInvalidValue;
-  dim3 grid(static_cast<unsigned>(C / 64), static_cast<unsigned>(tiles));
-  mx_quantize_tokens_kernel<<<grid, 256, 0, s>>>(src, row_src, d.K, offs, qt, sct, C, d.E,
-                                                 mx_token_cols(d),
-                                                 static_cast<int>(mx_weight_row_blocks(C)));
-  return cudaGetLastError();
+  TqArgs a{};
+  a.src = src;
+  a.row_src = row_src;
+  a.offs = offs;
+  a.q = qt;
+  a.sc = sct;
+  a.Rp = mx_token_cols(d);
+  a.C = C;
+  a.K = d.K;
+  a.E = d.E;
+  a.NBp = static_cast<int>(mx_weight_row_blocks(C));
+  CUtensorMap mq{};
+  const uint64_t dims[2] = {static_cast<uint64_t>(a.Rp), static_cast<uint64_t>(C)};
+  const uint64_t str[1] = {static_cast<uint64_t>(a.Rp)};
+  const uint32_t box[2] = {128, 64};
+  if (!make_map(&mq, CU_TENSOR_MAP_DATA_TYPE_UINT8, qt, 2, dims, str, box,
+                CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  return launch_tq<true>(a, mq, mx_cdiv(C, kTqCols) * mx_tile_bound(d), s);
 }
 
 cudaError_t launch_mx_grouped_gemm(const MxGemmCall& c, cudaStream_t s) {

@@ -29,8 +29,13 @@ inline long mx_weight_row_blocks(long n) { return 2 * mx_cdiv(n, 256); }
 // the tiles numbered as in the tile-blocked scales
 inline long mx_token_cols(const moe_dims& d) { return kMxRowsPerTile * mx_tile_bound(d); }
 
-cudaError_t launch_mx_quantize_weights(const uint16_t* w, uint8_t* q, uint8_t* sc, int E, int Kd,
-                                       int N, bool fc1_interleave, cudaStream_t s);
+// w [E][Kd][N] quantized along Kd into the transposed weight layout (codes
+// [E][N][Kd], FC1 rows interleaved when fc1_interleave) and/or along N in
+// its own layout (q2, sc2: codes [E][Kd][N], scales [E][KB(N)][NBp(Kd)][512]);
+// either pair may be null, one read of w serves both.
+cudaError_t launch_mx_quantize_weights(const uint16_t* w, uint8_t* q, uint8_t* sc, uint8_t* q2,
+                                       uint8_t* sc2, int E, int Kd, int N, bool fc1_interleave,
+                                       cudaStream_t s);
 cudaError_t launch_mx_permute_quantize(const uint16_t* x, const int32_t* pos, const int32_t* offs,
                                        uint8_t* xq, uint8_t* xsc, const moe_dims& d,
                                        cudaStream_t s);
@@ -45,11 +50,6 @@ cudaError_t launch_mx_quantize_tokens(const uint16_t* src, const int32_t* row_sr
 // Row quantization of an expert-sorted [R, C] (blocks along C, tile-blocked scales).
 cudaError_t launch_mx_quantize_rows(const uint16_t* src, const int32_t* offs, uint8_t* q,
                                     uint8_t* sc, int C, const moe_dims& d, cudaStream_t s);
-// w [E, N, Kd] quantized along its last axis: codes in the same layout,
-// scales [E, KB(Kd), NBp(N), 512].
-cudaError_t launch_mx_quantize_lastaxis(const uint16_t* w, uint8_t* q, uint8_t* sc, int E, int N,
-                                        int Kd, cudaStream_t s);
-
 enum class MxKind : int {
   kFc1 = 0,            // FC1 + SwiGLU: h (MX and/or bf16), optionally z
   kRows = 1,           // out[r, n] = sum_k A[r, k] * B_e[n, k], bf16

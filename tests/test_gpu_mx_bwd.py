@@ -107,9 +107,18 @@ def test_quantize_weights_bwd_exact(case):
     oq, osc = _u8(B.moe_mx_bytes(d, B.MX_WOQ_BWD)), _sc(B.moe_mx_bytes(d, B.MX_WOSC_BWD))
     assert isc.numel() == L.weight_scale_bytes(E, D, 2 * F)
     assert osc.numel() == L.weight_scale_bytes(E, F, D)
-    B.moe_mx_quantize_wi_bwd(to_dev(inp["wi"]), iq, isc, d)
-    B.moe_mx_quantize_wo_bwd(to_dev(inp["wo"]), oq, osc, d)
+    # the dgrad copies alone, then both copies from one read: the same bytes
+    B.moe_mx_quantize_wi(to_dev(inp["wi"]), None, None, d, wq_bwd=iq, wsc_bwd=isc)
+    B.moe_mx_quantize_wo(to_dev(inp["wo"]), None, None, d, wq_bwd=oq, wsc_bwd=osc)
     torch.cuda.synchronize()
+    fq, fsc = _u8(B.moe_mx_bytes(d, B.MX_WIQ)), _sc(B.moe_mx_bytes(d, B.MX_WISC))
+    iq2, isc2 = _u8(iq.numel()), _sc(isc.numel())
+    B.moe_mx_quantize_wi(to_dev(inp["wi"]), fq, fsc, d, wq_bwd=iq2, wsc_bwd=isc2)
+    torch.cuda.synchronize()
+    assert torch.equal(iq, iq2) and torch.equal(isc, isc2)
+    q, sc = L.unpack_weight(to_host(fq).reshape(E, 2 * F, D), to_host(fsc), True)
+    assert_exact("wi codes (along D, with the dgrad copy)", q, ref["wq"])
+    assert_exact("wi scales (along D, with the dgrad copy)", sc, ref["wsc"])
     q, sc = L.unpack_weight(to_host(iq).reshape(E, D, 2 * F), to_host(isc), False)
     assert_exact("wi codes (along 2F)", q, refb["wiq_b"])
     assert_exact("wi scales (along 2F)", sc, refb["wisc_b"])
@@ -302,6 +311,12 @@ def test_t0_and_argument_errors():
     assert ei.value.status == B.MOE_ERR_INVALID_ARG
     with pytest.raises(B.MoeError) as ei:   # rows: C must be D or 2F
         B.moe_mx_quantize_rows(z, 64, z, z, z, d)
+    assert ei.value.status == B.MOE_ERR_INVALID_ARG
+    with pytest.raises(B.MoeError) as ei:   # neither copy of the weight
+        B.moe_mx_quantize_wi(z, None, None, d)
+    assert ei.value.status == B.MOE_ERR_INVALID_ARG
+    with pytest.raises(B.MoeError) as ei:   # codes without scales
+        B.moe_mx_quantize_wo(z, z, None, d)
     assert ei.value.status == B.MOE_ERR_INVALID_ARG
     with pytest.raises(RuntimeError):
         MoEBlockMX(8, 128, 4, 2, 64).backward(None)
