@@ -717,11 +717,15 @@ __device__ __forceinline__ void put_half_sw(uint8_t* buf, int lane, int hh, cons
   }
 }
 
+// map_z, map_h: FC1 in training, z [R][2F] and the bf16 h [R][F] (64 x 32
+// boxes, 128-byte swizzle); other kinds get copies of map_o, unused.
 template <int KIND>
 __global__ void __launch_bounds__(kThreads, 1)
     mx_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                    const __grid_constant__ CUtensorMap map_b,
-                   const __grid_constant__ CUtensorMap map_o, const MxParams p) {
+                   const __grid_constant__ CUtensorMap map_o,
+                   const __grid_constant__ CUtensorMap map_z,
+                   const __grid_constant__ CUtensorMap map_h, const MxParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* ring = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
@@ -915,7 +919,47 @@ __global__ void __launch_bounds__(kThreads, 1)
         if constexpr (KIND == kKFc1) {
           // gate = columns 0..63, up = 64..127 of the region: h for f0..f0+63
           const int f0 = 64 * (2 * T.nt + hh);
-          if (p.zout != nullptr && row_ok) {  // z = [gate | up] for the backward
+          // a full warp stages z's gate and up chunks and h's bf16 chunk
+          // through its swizzled buffer, one TMA store each (per-thread
+          // stores of the same bytes cost the MMA: 1253 vs 794 us without
+          // these outputs)
+          if (vw == 32 && (p.zout != nullptr || (p.out != nullptr && p.hq != nullptr))) {
+            for (int part = 0; part < 3; ++part) {
+              if (part < 2 && p.zout == nullptr) continue;
+              if (part == 2 && !(p.out != nullptr && p.hq != nullptr)) continue;
+              uint32_t w0[16], w1[16];
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                float a0, a1, b0, b1;
+                if (part < 2) {
+                  const uint32_t* src = v + 64 * part;
+                  a0 = __uint_as_float(src[2 * i]);
+                  a1 = __uint_as_float(src[2 * i + 1]);
+                  b0 = __uint_as_float(src[32 + 2 * i]);
+                  b1 = __uint_as_float(src[32 + 2 * i + 1]);
+                } else {
+                  a0 = silu(__uint_as_float(v[2 * i])) * __uint_as_float(v[64 + 2 * i]);
+                  a1 = silu(__uint_as_float(v[2 * i + 1])) * __uint_as_float(v[64 + 2 * i + 1]);
+                  b0 = silu(__uint_as_float(v[32 + 2 * i])) * __uint_as_float(v[96 + 2 * i]);
+                  b1 = silu(__uint_as_float(v[33 + 2 * i])) * __uint_as_float(v[97 + 2 * i]);
+                }
+                w0[i] = pack_bf16x2(a0, a1);
+                w1[i] = pack_bf16x2(b0, b1);
+              }
+              if (lane == 0) bulk_wait_read<0>();
+              __syncwarp();
+              put_half_sw(buf, lane, 0, w0);
+              put_half_sw(buf, lane, 1, w1);
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) {
+                if (part == 0) tma_store_2d(&map_z, buf, f0, y);
+                else if (part == 1) tma_store_2d(&map_z, buf, p.Nout + f0, y);
+                else tma_store_2d(&map_h, buf, f0, y);
+                bulk_commit();
+              }
+            }
+          } else if (p.zout != nullptr && row_ok) {  // z = [gate | up] for the backward
             uint4* zg = reinterpret_cast<uint4*>(p.zout + r * 2 * p.Nout + f0);
             uint4* zu = reinterpret_cast<uint4*>(p.zout + r * 2 * p.Nout + p.Nout + f0);
 #pragma unroll
@@ -936,7 +980,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int j = 0; j < 64; ++j)
             hv[j] = silu(__uint_as_float(v[j])) * __uint_as_float(v[64 + j]);
-          if (p.out != nullptr && row_ok) {
+          if (p.out != nullptr && row_ok && !(vw == 32 && p.hq != nullptr)) {
             uint4* dst = reinterpret_cast<uint4*>(p.out + r * p.Nout + f0);
 #pragma unroll
             for (int i = 0; i < 8; ++i)
@@ -1100,7 +1144,8 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType type, const void* base, int ra
 
 template <int KIND>
 cudaError_t launch_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mo,
-                        const MxParams& p, long max_tiles, cudaStream_t s) {
+                        const CUtensorMap& mz, const CUtensorMap& mh, const MxParams& p,
+                        long max_tiles, cudaStream_t s) {
   auto kern = mx_gemm_kernel<KIND>;
   static std::atomic<bool> attr_set[64];
   int dev = 0;
@@ -1116,7 +1161,7 @@ cudaError_t launch_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const CUte
   long grid = sm_count();
   if (max_tiles < grid) grid = max_tiles;
   if (grid <= 0) return cudaSuccess;
-  kern<<<static_cast<int>(grid), kThreads, kSmemBytes, s>>>(ma, mb, mo, p);
+  kern<<<static_cast<int>(grid), kThreads, kSmemBytes, s>>>(ma, mb, mo, mz, mh, p);
   return cudaGetLastError();
 }
 
@@ -1304,7 +1349,22 @@ cudaError_t launch_mx_grouped_gemm(const MxGemmCall& c, cudaStream_t s) {
                       CU_TENSOR_MAP_SWIZZLE_128B);
       }
       if (!ok) return cudaErrorInvalidValue;
-      return launch_gemm<kKFc1>(ma, mb, mo, p, max_tiles, s);
+      // training: z and the bf16 h through TMA stores
+      CUtensorMap mz = mo, mh = mo;
+      if (c.z_out != nullptr) {
+        const uint64_t zdims[2] = {2 * static_cast<uint64_t>(d.F), static_cast<uint64_t>(R)};
+        const uint64_t zstr[1] = {static_cast<uint64_t>(d.F) * 4};
+        if (!make_map(&mz, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, c.z_out, 2, zdims, zstr, obox,
+                      CU_TENSOR_MAP_SWIZZLE_128B))
+          return cudaErrorInvalidValue;
+      }
+      if (c.hq != nullptr && c.out != nullptr) {
+        const uint64_t hstr[1] = {static_cast<uint64_t>(d.F) * 2};
+        if (!make_map(&mh, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, c.out, 2, odims, hstr, obox,
+                      CU_TENSOR_MAP_SWIZZLE_128B))
+          return cudaErrorInvalidValue;
+      }
+      return launch_gemm<kKFc1>(ma, mb, mo, mz, mh, p, max_tiles, s);
     }
     case MxKind::kRowsSwigluBwd: {
       // dz is written by plain stores; the map (over dz) is not used
@@ -1313,7 +1373,7 @@ cudaError_t launch_mx_grouped_gemm(const MxGemmCall& c, cudaStream_t s) {
       if (!make_map(&mo, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, c.out, 2, odims, ostr, obox,
                     CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
-      return launch_gemm<kKSwigluBwd>(ma, mb, mo, p, max_tiles, s);
+      return launch_gemm<kKSwigluBwd>(ma, mb, mo, mo, mo, p, max_tiles, s);
     }
     case MxKind::kRows:
     case MxKind::kWgrad: {
@@ -1324,8 +1384,9 @@ cudaError_t launch_mx_grouped_gemm(const MxGemmCall& c, cudaStream_t s) {
       if (!make_map(&mo, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, c.out, 2, odims, ostr, obox,
                     CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
-      if (c.kind == MxKind::kWgrad) return launch_gemm<kKWgrad>(ma, mb, mo, p, max_tiles, s);
-      return launch_gemm<kKRows>(ma, mb, mo, p, max_tiles, s);
+      if (c.kind == MxKind::kWgrad)
+        return launch_gemm<kKWgrad>(ma, mb, mo, mo, mo, p, max_tiles, s);
+      return launch_gemm<kKRows>(ma, mb, mo, mo, mo, p, max_tiles, s);
     }
   }
   return cudaErrorInvalidValue;
