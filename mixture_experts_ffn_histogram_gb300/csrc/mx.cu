@@ -58,31 +58,40 @@ namespace {
 
 constexpr int kMaxE = 1024;
 constexpr int kThreads = 192;
-constexpr int kStages = 4;
+constexpr int kMaxStages = 4;
 constexpr int kAStage = 128 * 128;               // 16 KB
 constexpr int kBStage = 256 * 128;               // 32 KB
 constexpr int kSfaOff = kAStage + kBStage;       // 48 KB
 constexpr int kSfbOff = kSfaOff + 1024;
 constexpr int kStageBytes = kSfbOff + 1024;      // 50 KB (keeps every operand 1024-aligned)
 constexpr uint32_t kTxBytes = kAStage + kBStage + 512 + 1024;
-constexpr int kEpiBytes = 4096;                  // staging per epilogue warp
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSfStride = 16;               // scale slot per stage: A 4 + B 8 columns (16-aligned)
 
 struct MxCtl {
-  uint64_t full[kStages];
-  uint64_t empty[kStages];
+  uint64_t full[kMaxStages];
+  uint64_t empty[kMaxStages];
   uint64_t tfull[2];   // accumulator buffer b holds a finished tile
   uint64_t tempty[2];  // the epilogue has read all of buffer b
   uint64_t sffree[2];  // the epilogue has read half 0 of buffer b (the scale slots)
+  uint64_t zbar[4][2]; // FC2 dgrad: z chunk slot s of epilogue warp w has landed
   uint32_t tmem_base;
   int abort_flag;
   int off[kMaxE + 1];  // group offsets
   int tb[kMaxE + 1];   // first 128-row tile of each group (exclusive prefix)
 };
-constexpr size_t kSmemBytes =
-    1024 + static_cast<size_t>(kStages) * kStageBytes + 4 * kEpiBytes + sizeof(MxCtl);
-static_assert(kSmemBytes <= 227 * 1024, "shared memory");
+// Per tile kind: ring stages and staging bytes per epilogue warp.  The FC2
+// dgrad gives up a ring stage for two 8 KB slots per epilogue warp, each
+// holding a 64-column chunk of z's gate and up halves (TMA loads) that the
+// SwiGLU backward turns into dz in place (TMA stores).
+template <int KIND>
+struct MxCfg {
+  static constexpr int kStages = KIND == 2 ? 3 : 4;
+  static constexpr int kEpiBytes = KIND == 2 ? 16384 : 4096;
+  static constexpr size_t kSmemBytes =
+      1024 + static_cast<size_t>(kStages) * kStageBytes + 4 * kEpiBytes + sizeof(MxCtl);
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory");
+};
 
 // ------------------------------------------------------------ MX helpers
 // Shared exponent of a block from its largest magnitude: floor(log2 amax) - 8
@@ -726,11 +735,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const __grid_constant__ CUtensorMap map_o,
                    const __grid_constant__ CUtensorMap map_z,
                    const __grid_constant__ CUtensorMap map_h, const MxParams p) {
+  using C = MxCfg<KIND>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* ring = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
-  uint8_t* epi = ring + kStages * kStageBytes;
-  MxCtl& s = *reinterpret_cast<MxCtl*>(epi + 4 * kEpiBytes);
+  uint8_t* epi = ring + C::kStages * kStageBytes;
+  MxCtl& s = *reinterpret_cast<MxCtl*>(epi + 4 * C::kEpiBytes);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
@@ -738,7 +748,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_map(&map_a);
     tma_prefetch_map(&map_b);
     tma_prefetch_map(&map_o);
-    for (int i = 0; i < kStages; ++i) {
+    for (int i = 0; i < C::kStages; ++i) {
       mbar_init(&s.full[i], 1);
       mbar_init(&s.empty[i], 1);
     }
@@ -747,6 +757,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&s.tempty[i], 4);
       mbar_init(&s.sffree[i], 4);
     }
+    for (int w = 0; w < 4; ++w)
+      for (int i = 0; i < 2; ++i) mbar_init(&s.zbar[w][i], 1);
     s.abort_flag = 0;
     mbar_fence_init();
   }
@@ -767,7 +779,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // -------------------------------------------------------- producer
     if (lane == 0) {
       uint32_t stage = 0, phase = 0;
-      uint32_t fills[kStages] = {0, 0, 0, 0};
+      uint32_t fills[C::kStages] = {};
       bool aborted = false;
       for (int t = blockIdx.x; t < ntiles && !aborted; t += gridDim.x) {
         const MxTile T = mx_decode<KIND>(t, p, s);
@@ -799,11 +811,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           bulk_load(st + kSfbOff, sfb + static_cast<size_t>(kb) * p.NBp * 512, 1024,
                     &s.full[stage]);
           ++fills[stage];
-          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+          if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
         }
       }
       if (aborted) {  // copies in flight land before the CTA exits
-        for (int i = 0; i < kStages; ++i)
+        for (int i = 0; i < C::kStages; ++i)
           if (fills[i] > 0) (void)mbar_wait_drain(&s.full[i], (fills[i] - 1u) & 1u, 100000000ull);
       }
     }
@@ -812,7 +824,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // one thread: waits, scale copies, MMAs and commits
     if (lane == 0) {
       uint32_t stage = 0, phase = 0, it = 0;
-      uint32_t commits[kStages] = {0, 0, 0, 0};
+      uint32_t commits[C::kStages] = {};
       int last_stage = -1;
       bool aborted = false;
       // descriptors of stage 0's A and scale blocks; stage i adds i * kStageBytes >> 4,
@@ -861,7 +873,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           umma_commit<1>(&s.empty[stage]);
           ++commits[stage];
           last_stage = static_cast<int>(stage);
-          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+          if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
         }
         if (aborted) break;
         umma_commit<1>(&s.tfull[buf]);
@@ -872,9 +884,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // -------------------------------------------------------- epilogue
     const int q = warp & 3;  // TMEM lane quarter: rows 32q..32q+31 of the tile
-    uint8_t* buf = epi + (warp - 2) * kEpiBytes;
+    const int ew = warp - 2;  // epilogue warp index
+    uint8_t* buf = epi + ew * C::kEpiBytes;
     uint32_t it = 0;
     bool aborted = false;
+    // FC2 dgrad, full warps: z chunk c (64 columns f = 256 nt + 64 c, gate
+    // and up) lands in slot c & 1 by TMA; zpar / zout track each slot's
+    // mbarrier phase and whether a load is outstanding
+    uint32_t zpar[2] = {0u, 0u};
+    bool zout[2] = {false, false};
+    auto zload = [&](int slot, int f, int yrow) {
+      uint8_t* dst = buf + slot * 8192;
+      mbar_arrive_expect_tx(&s.zbar[ew][slot], 8192);
+      tma_load_2d(dst, &map_z, &s.zbar[ew][slot], f, yrow);
+      tma_load_2d(dst + 4096, &map_z, &s.zbar[ew][slot], p.Nout + f, yrow);
+    };
     for (int t = blockIdx.x; t < ntiles && !aborted; t += gridDim.x, ++it) {
       const MxTile T = mx_decode<KIND>(t, p, s);
       const int vw = min(32, max(0, T.rows - 32 * q));  // valid rows of this warp
@@ -882,6 +906,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool row_ok = lane < vw;
       const long r = static_cast<long>(y) + lane;
       const uint32_t bsel = it & 1u;
+      const bool tma_z = KIND == kKSwigluBwd && vw == 32;
+      if (tma_z) {  // z's first two chunks, requested before the accumulator is ready
+        if (lane == 0) {
+          bulk_wait_read<0>();  // the previous tile's dz stores have read the slots
+          for (int c = 0; c < 2; ++c)
+            if (256 * T.nt + 64 * c < p.Nout) zload(c, 256 * T.nt + 64 * c, y);
+        }
+        for (int c = 0; c < 2; ++c) zout[c] = 256 * T.nt + 64 * c < p.Nout;
+        __syncwarp();
+      }
       if (!__all_sync(0xffffffffu, mbar_wait(&s.tfull[bsel], (it >> 1) & 1u, wc))) {
         aborted = true;
         break;
@@ -1030,7 +1064,64 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         } else if constexpr (KIND == kKSwigluBwd) {
-          // dh for f = fb .. fb + 127 of this row; z and dz are [gate | up] rows
+          if (tma_z) {
+            // chunks 2 hh + cc: wait for the slot, dz over z in place, two
+            // TMA stores, then (half 0) refill the slot with the chunk two on
+            bool ok = true;
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc) {  // unrolled: v is indexed by constants
+              const int f = 256 * T.nt + 128 * hh + 64 * cc;
+              if (!ok || f >= p.Nout) continue;
+              ok = __all_sync(0xffffffffu, mbar_wait(&s.zbar[ew][cc], zpar[cc], wc));
+              if (!ok) continue;
+              zpar[cc] ^= 1u;
+              zout[cc] = false;
+              uint8_t* sl = buf + cc * 8192 + lane * 128;
+#pragma unroll
+              for (int h32 = 0; h32 < 2; ++h32) {
+                uint4 zg[4], zu[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                  const int off = ((4 * h32 + i) ^ (lane & 7)) << 4;
+                  zg[i] = *reinterpret_cast<const uint4*>(sl + off);
+                  zu[i] = *reinterpret_cast<const uint4*>(sl + 4096 + off);
+                }
+                uint32_t wg[16], wu[16];
+                swiglu_bwd32(*reinterpret_cast<const uint32_t(*)[32]>(&v[64 * cc + 32 * h32]), zg, zu,
+                             wg, wu);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                  const int off = ((4 * h32 + i) ^ (lane & 7)) << 4;
+                  *reinterpret_cast<uint4*>(sl + off) =
+                      make_uint4(wg[4 * i], wg[4 * i + 1], wg[4 * i + 2], wg[4 * i + 3]);
+                  *reinterpret_cast<uint4*>(sl + 4096 + off) =
+                      make_uint4(wu[4 * i], wu[4 * i + 1], wu[4 * i + 2], wu[4 * i + 3]);
+                }
+              }
+              fence_proxy_async_smem();
+              __syncwarp();
+              const int f2 = f + 128;  // the chunk that reuses this slot
+              const bool refill = hh == 0 && f2 < p.Nout;
+              if (lane == 0) {
+                tma_store_2d(&map_h, buf + cc * 8192, f, y);
+                tma_store_2d(&map_h, buf + cc * 8192 + 4096, p.Nout + f, y);
+                bulk_commit();
+                if (refill) {
+                  bulk_wait_read<0>();
+                  zload(cc, f2, y);
+                }
+              }
+              zout[cc] = refill;
+              __syncwarp();
+            }
+            if (!ok) {
+              aborted = true;
+              break;
+            }
+            continue;
+          }
+          // a partial warp: dh for f = fb .. fb + 127 of each valid row, z read
+          // and dz written by the row's own thread (z and dz are [gate | up] rows)
           if (row_ok) {
             const int fb = 256 * T.nt + 128 * hh;
             const __nv_bfloat16* zr = p.zin + r * 2 * p.Nout;
@@ -1092,7 +1183,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-    if (lane == 0) bulk_wait_all();  // every store has finished before the CTA exits
+    if (lane == 0) {
+      for (int c = 0; c < 2; ++c)  // z loads still in flight (after an abort) land first
+        if (zout[c]) (void)mbar_wait_drain(&s.zbar[ew][c], zpar[c], 100000000ull);
+      bulk_wait_all();  // every store has finished before the CTA exits
+    }
     __syncwarp();
   }
 
@@ -1154,14 +1249,14 @@ cudaError_t launch_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const CUte
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!attr_set[dev].load(std::memory_order_acquire)) {
     err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(kSmemBytes));
+                               static_cast<int>(MxCfg<KIND>::kSmemBytes));
     if (err != cudaSuccess) return err;
     attr_set[dev].store(true, std::memory_order_release);
   }
   long grid = sm_count();
   if (max_tiles < grid) grid = max_tiles;
   if (grid <= 0) return cudaSuccess;
-  kern<<<static_cast<int>(grid), kThreads, kSmemBytes, s>>>(ma, mb, mo, mz, mh, p);
+  kern<<<static_cast<int>(grid), kThreads, MxCfg<KIND>::kSmemBytes, s>>>(ma, mb, mo, mz, mh, p);
   return cudaGetLastError();
 }
 
@@ -1367,13 +1462,16 @@ cudaError_t launch_mx_grouped_gemm(const MxGemmCall& c, cudaStream_t s) {
       return launch_gemm<kKFc1>(ma, mb, mo, mz, mh, p, max_tiles, s);
     }
     case MxKind::kRowsSwigluBwd: {
-      // dz is written by plain stores; the map (over dz) is not used
+      // z in and dz out, both [R][2F] bf16, 64-column chunks of 32 rows
       const uint64_t odims[2] = {2 * static_cast<uint64_t>(d.F), static_cast<uint64_t>(R)};
       const uint64_t ostr[1] = {static_cast<uint64_t>(d.F) * 4};
+      CUtensorMap mz;
       if (!make_map(&mo, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, c.out, 2, odims, ostr, obox,
+                    CU_TENSOR_MAP_SWIZZLE_128B) ||
+          !make_map(&mz, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, c.z_in, 2, odims, ostr, obox,
                     CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
-      return launch_gemm<kKSwigluBwd>(ma, mb, mo, mo, mo, p, max_tiles, s);
+      return launch_gemm<kKSwigluBwd>(ma, mb, mo, mz, mo, p, max_tiles, s);
     }
     case MxKind::kRows:
     case MxKind::kWgrad: {
