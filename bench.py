@@ -144,7 +144,8 @@ NCU_NAME = {
 
 # the files holding the device code of the bf16 block's kernels (the traffic
 # figures under profiles/ are valid while these are unchanged)
-KERNEL_SOURCES = ("common.cuh", "gemm.cu", "kernels.h", "permute_combine.cu", "route.cu")
+KERNEL_SOURCES = ("common.cuh", "gemm.cu", "kernels.h", "mx_common.cuh", "permute_combine.cu",
+                  "route.cu")
 
 
 def source_hash() -> str:
@@ -373,7 +374,8 @@ class Step:
         self.names = ["route", "permute", "fc1", "fc2", "combine"]
         if not fwd_only:
             self.names += ["combine_bwd", "fc2_dlhs", "fc2_drhs", "fc1_dlhs", "fc1_drhs", "permute_bwd"]
-        self.launches_per_step = 7 + (0 if fwd_only else 6)
+        # our kernels per step (the drhs schedule's counter memsets are not ours)
+        self.launches_per_step = 5 + (0 if fwd_only else 6)
         self.times = {n: [] for n in self.names}
         self._ev = []
 
@@ -555,8 +557,8 @@ def mx_train_work(wl):
         ("fc1", "tensor", gemm_flops("fc1", R, D, F)),
         ("fc2", "tensor", gemm_flops("fc2", R, D, F)),
         ("combine", "hbm", hbm_bytes("combine", T, D, E, K, F)),
-        ("combine_bwd", "hbm", hbm_bytes("combine_bwd", T, D, E, K, F)),
-        ("quantize_dys_rows", "hbm", quant(R * D, R * D)),
+        # the combine backward, writing dys also as MX codes along D
+        ("combine_bwd_quantize", "hbm", hbm_bytes("combine_bwd", T, D, E, K, F) + R * D + R * D // 32),
         ("quantize_dys_tokens", "hbm", quant(R * D, R * D)),
         ("quantize_h_tokens", "hbm", quant(R * F, R * F)),
         ("fc2_dgrad", "tensor", gemm_flops("fc2_dlhs", R, D, F)),
@@ -599,8 +601,8 @@ def measure_mx_train(wl, inp, steps, pk, flushed, dev):
         lambda: B.moe_mx_grouped_gemm_fc2(blk.hq, blk.hsc, blk.woq, blk.wosc, offs, blk.ys,
                                           blk.status, d),
         lambda: B.moe_combine(blk.ys, blk.w, blk.pos, blk.out, d),
-        lambda: B.moe_combine_bwd(dy, blk.ys, blk.w, blk.pos, blk.dys, blk.dw, d),
-        lambda: B.moe_mx_quantize_rows(blk.dys, D, offs, blk.dyq, blk.dysc, d),
+        lambda: B.moe_mx_combine_bwd(dy, blk.ys, blk.w, blk.pos, offs, blk.dys, blk.dyq,
+                                     blk.dysc, blk.dw, d),
         lambda: B.moe_mx_quantize_tokens(blk.dys, None, D, offs, blk.dyt, blk.dytsc, d),
         lambda: B.moe_mx_quantize_tokens(blk.h, None, F, offs, blk.ht, blk.htsc, d),
         lambda: B.moe_mx_grouped_gemm_fc2_bwd(blk.dyq, blk.dysc, blk.woq_b, blk.wosc_b, blk.z,
@@ -682,7 +684,7 @@ def measure_mx_train(wl, inp, steps, pk, flushed, dev):
         "gemm_ms": gemm_s * 1e3,
         "gemm_frac_tensor": flops / gemm_s / 1e12 / fp8_peak if gemm_s > 0 else None,
         "clocks": {k: clocks.get(k) for k in ("sm_mhz", "sm_max_mhz", "reasons")},
-        "gpu_launches_per_step": len(calls) + 2,   # route_histogram is three launches
+        "gpu_launches_per_step": len(calls),
         "kernels": kern,
     }
 

@@ -452,6 +452,15 @@ moe_status moe_mx_grouped_gemm_fc2(const uint8_t* hq, const uint8_t* hsc, const 
  * block at ((g * NBp(C)) + c / 128) * 512, byte (c % 128 % 32) * 16 +
  * (c % 128 / 32) * 4 + j for tokens [32j, 32j+32) of the tile.
  */
+/* The combine backward (moe_combine_bwd: dys bf16 [R, D] and dw) that also
+ * writes dys quantized along D for the FC2 dgrad, dyq [R, D] with the
+ * tile-blocked scales dysc, the bytes moe_mx_quantize_rows would make of
+ * the same dys, without reading it back.  group_offsets: those of the
+ * histogram that produced pos. */
+moe_status moe_mx_combine_bwd(const moe_bf16* dout, const moe_bf16* ys, const float* w,
+                              const int32_t* pos, const int32_t* group_offsets, moe_bf16* dys,
+                              uint8_t* dyq, uint8_t* dysc, float* dw, moe_dims d,
+                              cudaStream_t stream);
 /* src bf16 [R, C] in expert-sorted order (C = D for dys, 2F for dz) -> q
  * [R, C] codes and tile-blocked scales sc (blocks along C). */
 moe_status moe_mx_quantize_rows(const moe_bf16* src, int C, const int32_t* group_offsets,

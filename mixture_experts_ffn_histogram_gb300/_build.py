@@ -20,7 +20,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libmoe.so")
 SOURCES = ["api.cu", "route.cu", "permute_combine.cu", "gemm.cu", "mx.cu"]
 HEADERS = [os.path.join(CSRC, "common.cuh"), os.path.join(CSRC, "kernels.h"),
-           os.path.join(CSRC, "mx.h"),
+           os.path.join(CSRC, "mx.h"), os.path.join(CSRC, "mx_common.cuh"),
            os.path.join(INCLUDE, "moe.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]

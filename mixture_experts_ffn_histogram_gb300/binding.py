@@ -34,7 +34,7 @@ ENTRY_POINTS = (
     "moe_mx_bytes", "moe_mx_quantize_wi", "moe_mx_quantize_wo", "moe_mx_permute_quantize",
     "moe_mx_grouped_gemm_fc1_swiglu", "moe_mx_grouped_gemm_fc2",
     "moe_grouped_gemm_fc1_swiglu_experts", "moe_grouped_gemm_fc1_bwd_experts",
-    "moe_fused_forward", "moe_mx_quantize_rows", "moe_mx_quantize_tokens", "moe_mx_grouped_gemm_fc2_bwd",
+    "moe_fused_forward", "moe_mx_combine_bwd", "moe_mx_quantize_rows", "moe_mx_quantize_tokens", "moe_mx_grouped_gemm_fc2_bwd",
     "moe_mx_grouped_gemm_fc1_bwd",
 )
 
@@ -110,6 +110,7 @@ def lib() -> ctypes.CDLL:
             "moe_mx_permute_quantize": ([P, P, P, P, P, D_, P], I),
             "moe_mx_grouped_gemm_fc1_swiglu": ([P, P, P, P, P, P, P, P, P, P, D_, P], I),
             "moe_mx_grouped_gemm_fc2": ([P, P, P, P, P, P, P, D_, P], I),
+            "moe_mx_combine_bwd": ([P] * 9 + [D_, P], I),
             "moe_mx_quantize_rows": ([P, I, P, P, P, D_, P], I),
             "moe_mx_quantize_tokens": ([P, P, I, P, P, P, D_, P], I),
             "moe_mx_grouped_gemm_fc2_bwd": ([P] * 13 + [D_, P], I),
@@ -282,6 +283,13 @@ def moe_mx_grouped_gemm_fc2(hq, hsc, wq, wsc, group_offsets, ys, dev_status, d: 
     _ok("moe_mx_grouped_gemm_fc2", lib().moe_mx_grouped_gemm_fc2(
         _p(hq), _p(hsc), _p(wq), _p(wsc), _p(group_offsets), _p(ys), _p(dev_status), d,
         _s(stream)))
+
+
+def moe_mx_combine_bwd(dout, ys, w, pos, group_offsets, dys, dyq, dysc, dw, d: MoeDims,
+                       stream=None):
+    _ok("moe_mx_combine_bwd", lib().moe_mx_combine_bwd(
+        _p(dout), _p(ys), _p(w), _p(pos), _p(group_offsets), _p(dys), _p(dyq), _p(dysc), _p(dw),
+        d, _s(stream)))
 
 
 def moe_mx_quantize_rows(src, C, group_offsets, q, sc, d: MoeDims, stream=None):

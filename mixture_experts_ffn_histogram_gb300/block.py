@@ -13,7 +13,7 @@ import torch
 from . import binding as B
 
 # kernels launched per call sequence (used for the launch count of a step)
-FWD_LAUNCHES = 3 + 1 + 1 + 1 + 1     # route(topk+hist, scan, rank), permute, fc1, fc2, combine
+FWD_LAUNCHES = 1 + 1 + 1 + 1 + 1     # route (one cooperative kernel), permute, fc1, fc2, combine
 BWD_LAUNCHES = 1 + 2 + 2 + 1         # combine_bwd, fc2 dlhs+drhs, fc1 dlhs+drhs, permute_bwd
 
 
@@ -241,8 +241,8 @@ class MoEBlockMX:
             raise RuntimeError("backward needs a forward first")
         d, D, F = self.d, self.D, self.F
         offs = self.group_offsets
-        B.moe_combine_bwd(dy, self.ys, self.w, self.pos, self.dys, self.dw, d, stream)
-        B.moe_mx_quantize_rows(self.dys, D, offs, self.dyq, self.dysc, d, stream)
+        B.moe_mx_combine_bwd(dy, self.ys, self.w, self.pos, offs, self.dys, self.dyq, self.dysc,
+                             self.dw, d, stream)
         B.moe_mx_quantize_tokens(self.dys, None, D, offs, self.dyt, self.dytsc, d, stream)
         B.moe_mx_quantize_tokens(self.h, None, F, offs, self.ht, self.htsc, d, stream)
         B.moe_mx_grouped_gemm_fc2_bwd(self.dyq, self.dysc, self.woq_b, self.wosc_b, self.z,

@@ -523,6 +523,25 @@ moe_status moe_mx_grouped_gemm_fc2(const uint8_t* hq, const uint8_t* hsc, const 
   return from_cuda(moe::launch_mx_grouped_gemm(c, stream));
 }
 
+moe_status moe_mx_combine_bwd(const moe_bf16* dout, const moe_bf16* ys, const float* w,
+                              const int32_t* pos, const int32_t* group_offsets, moe_bf16* dys,
+                              uint8_t* dyq, uint8_t* dysc, float* dw, moe_dims d,
+                              cudaStream_t stream) {
+  MOE_CHECK_DIMS(d);
+  if (d.T == 0) return MOE_OK;
+  MOE_REQUIRE(dout);
+  MOE_REQUIRE(ys);
+  MOE_REQUIRE(w);
+  MOE_REQUIRE(pos);
+  MOE_REQUIRE(group_offsets);
+  MOE_REQUIRE(dys);
+  MOE_REQUIRE(dyq);
+  MOE_REQUIRE(dysc);
+  MOE_REQUIRE(dw);
+  return from_cuda(
+      moe::launch_mx_combine_bwd(dout, ys, w, pos, group_offsets, dys, dyq, dysc, dw, d, stream));
+}
+
 moe_status moe_mx_quantize_rows(const moe_bf16* src, int C, const int32_t* group_offsets,
                                 uint8_t* q, uint8_t* sc, moe_dims d, cudaStream_t stream) {
   MOE_CHECK_DIMS(d);

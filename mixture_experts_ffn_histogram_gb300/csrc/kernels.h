@@ -49,6 +49,12 @@ cudaError_t launch_combine(const uint16_t* ys, const float* w, const int32_t* po
 cudaError_t launch_combine_bwd(const uint16_t* dout, const uint16_t* ys, const float* w,
                                const int32_t* pos, uint16_t* dys, float* dw, const moe_dims& d,
                                cudaStream_t s);
+// the combine backward that also writes dys quantized along D (MXFP8 codes
+// [R][D] and tile-blocked scales of the rows' groups)
+cudaError_t launch_mx_combine_bwd(const uint16_t* dout, const uint16_t* ys, const float* w,
+                                  const int32_t* pos, const int32_t* offs, uint16_t* dys,
+                                  uint8_t* dyq, uint8_t* dysc, float* dw, const moe_dims& d,
+                                  cudaStream_t s);
 cudaError_t launch_swiglu_bwd(const uint16_t* dh, const uint16_t* z, uint16_t* dz, long R, int F,
                               cudaStream_t s);
 cudaError_t launch_bounded_wait_selftest(int32_t* dev_status, uint64_t limit_ns, cudaStream_t s);

@@ -18,6 +18,7 @@
 // product accumulated per lane and reduced across the warp.
 #include "common.cuh"
 #include "kernels.h"
+#include "mx_common.cuh"
 
 namespace moe {
 namespace {
@@ -177,36 +178,69 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const uint4* __restri
 // the ys vectors of every slot of the batch are loaded before any is used.
 // Each lane accumulates its part of a dot product over the chunks in
 // ascending column order; the warp then sums the lanes' parts.
-template <int VPL>
-__global__ void __launch_bounds__(kThreads) combine_bwd_kernel(
+// With QUANT, each dys row is also quantized along D as MXFP8 for the FC2
+// dgrad (moe_mx_combine_bwd): four consecutive lanes hold one 32-element
+// block (their 16-byte vectors), whose largest magnitude two shuffles
+// gather; each lane writes its 8 codes (a warp, 256 contiguous bytes) and
+// the block's first lane its scale byte, in the tile-blocked layout of the
+// row's group (the offsets and tile bases staged in shared memory).
+struct MxRowsOut {
+  const int32_t* offs;  // group offsets [E+1]
+  uint8_t* q;           // codes [R][D]
+  uint8_t* sc;          // tile-blocked scales
+  int E;
+  int KB;               // k-blocks of D
+};
+
+template <int VPL, bool QUANT>
+__global__ void __launch_bounds__(kThreads, 2) combine_bwd_kernel(
     const uint4* __restrict__ dout, const uint4* __restrict__ ys, const float* __restrict__ w,
     const int32_t* __restrict__ pos, uint4* __restrict__ dys, float* __restrict__ dw, int T, int K,
-    int Dv) {
+    int Dv, MxRowsOut mq) {
   const int lane = threadIdx.x & 31;
+  extern __shared__ int cb_bases[];  // QUANT: group offsets and tile bases
+  if constexpr (QUANT) load_tile_bases(mq.offs, mq.E, cb_bases, cb_bases + mq.E + 1, 0);
   for (int t = blockIdx.x * kWarps + (threadIdx.x >> 5); t < T; t += gridDim.x * kWarps) {
     const long j = static_cast<long>(t) * K + lane;
     const int p_lane = (lane < K) ? __ldg(pos + j) : -1;
     const float w_lane = (lane < K) ? __ldg(w + j) : 0.f;
     const uint4* g = dout + static_cast<long>(t) * Dv;
-    for (int k0 = 0; k0 < K; k0 += kSlotBatch) {
-      int pk[kSlotBatch];
-      float wk[kSlotBatch], dot[kSlotBatch];
+    // (the quantizing variant takes half the batch: two blocks per SM need
+    // its registers)
+    constexpr int kBatch = QUANT ? kSlotBatch / 2 : kSlotBatch;
+    for (int k0 = 0; k0 < K; k0 += kBatch) {
+      int pk[kBatch];
+      float wk[kBatch], dot[kBatch];
+      size_t sbase[kBatch];  // QUANT: the row's first scale block (bytes)
+      int sm[kBatch];        // QUANT: the row's place in its 128-row tile
 #pragma unroll
-      for (int b = 0; b < kSlotBatch; ++b) {
+      for (int b = 0; b < kBatch; ++b) {
         const int k = k0 + b;
         pk[b] = (k < K) ? __shfl_sync(0xffffffffu, p_lane, k) : -1;
         wk[b] = (k < K) ? __shfl_sync(0xffffffffu, w_lane, k) : 0.f;
         dot[b] = 0.f;
+        if constexpr (QUANT) {
+          sbase[b] = 0;
+          sm[b] = 0;
+          if (pk[b] >= 0) {
+            const int* s_off = cb_bases;
+            const int* s_tb = cb_bases + mq.E + 1;
+            const int e = group_of_row(s_off, mq.E, pk[b]);
+            const int i = pk[b] - s_off[e];
+            sbase[b] = static_cast<size_t>(s_tb[e] + (i >> 7)) * mq.KB * 512;
+            sm[b] = i & 127;
+          }
+        }
       }
       for (int v0 = 0; v0 < Dv; v0 += 32 * VPL) {
-        uint4 gv[VPL], yv[kSlotBatch][VPL];
+        uint4 gv[VPL], yv[kBatch][VPL];
 #pragma unroll
         for (int i = 0; i < VPL; ++i) {
           const int idx = v0 + i * 32 + lane;
           if (idx < Dv) gv[i] = __ldg(g + idx);
         }
 #pragma unroll
-        for (int b = 0; b < kSlotBatch; ++b) {
+        for (int b = 0; b < kBatch; ++b) {
           if (pk[b] < 0) continue;
           const uint4* y = ys + static_cast<long>(pk[b]) * Dv;
 #pragma unroll
@@ -216,7 +250,7 @@ __global__ void __launch_bounds__(kThreads) combine_bwd_kernel(
           }
         }
 #pragma unroll
-        for (int b = 0; b < kSlotBatch; ++b) {
+        for (int b = 0; b < kBatch; ++b) {
           if (pk[b] < 0) continue;
           uint4* dst = dys + static_cast<long>(pk[b]) * Dv;
 #pragma unroll
@@ -234,12 +268,35 @@ __global__ void __launch_bounds__(kThreads) combine_bwd_kernel(
                 dot[b] = fmaf(g1, bf16hi(yu[q]), dot[b]);
               }
               dst[idx] = make_uint4(o[0], o[1], o[2], o[3]);
+              if constexpr (QUANT) {
+                // the bf16 values just stored, quantized in blocks of 4 lanes
+                // (Dv % 4 == 0: a block's lanes are all in range together)
+                float amax = 0.f;
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                  amax = fmaxf(amax, fmaxf(fabsf(bf16lo(o[q])), fabsf(bf16hi(o[q]))));
+                amax = fmaxf(amax, __shfl_xor_sync(0x0000000Fu << (lane & 28), amax, 1));
+                amax = fmaxf(amax, __shfl_xor_sync(0x0000000Fu << (lane & 28), amax, 2));
+                const int sx = mx_shared_exp(amax);
+                const float mul = mx_inv_scale(sx);
+                const uint32_t c0 = e4m3x2(bf16lo(o[0]) * mul, bf16hi(o[0]) * mul);
+                const uint32_t c1 = e4m3x2(bf16lo(o[1]) * mul, bf16hi(o[1]) * mul);
+                const uint32_t c2 = e4m3x2(bf16lo(o[2]) * mul, bf16hi(o[2]) * mul);
+                const uint32_t c3 = e4m3x2(bf16lo(o[3]) * mul, bf16hi(o[3]) * mul);
+                *reinterpret_cast<uint2*>(mq.q + static_cast<size_t>(pk[b]) * Dv * 8 + idx * 8) =
+                    make_uint2(__byte_perm(c0, c1, 0x5410), __byte_perm(c2, c3, 0x5410));
+                if ((lane & 3) == 0) {
+                  const int blk = idx >> 2;  // 32-element block along D
+                  mq.sc[sbase[b] + static_cast<size_t>(blk >> 2) * 512 + sf_byte(sm[b], blk & 3)] =
+                      static_cast<uint8_t>(sx + 127);
+                }
+              }
             }
           }
         }
       }
 #pragma unroll
-      for (int b = 0; b < kSlotBatch; ++b) {
+      for (int b = 0; b < kBatch; ++b) {
         float d = dot[b];
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
@@ -353,9 +410,21 @@ cudaError_t launch_combine_bwd(const uint16_t* dout, const uint16_t* ys, const f
                                const int32_t* pos, uint16_t* dys, float* dw, const moe_dims& d,
                                cudaStream_t s) {
   if (d.T == 0) return cudaSuccess;
-  combine_bwd_kernel<2><<<grid_for_tokens(d.T), kThreads, 0, s>>>(
+  combine_bwd_kernel<2, false><<<grid_for_tokens(d.T), kThreads, 0, s>>>(
       reinterpret_cast<const uint4*>(dout), reinterpret_cast<const uint4*>(ys), w, pos,
-      reinterpret_cast<uint4*>(dys), dw, d.T, d.K, d.D / 8);
+      reinterpret_cast<uint4*>(dys), dw, d.T, d.K, d.D / 8, MxRowsOut{});
+  return cudaGetLastError();
+}
+
+cudaError_t launch_mx_combine_bwd(const uint16_t* dout, const uint16_t* ys, const float* w,
+                                  const int32_t* pos, const int32_t* offs, uint16_t* dys,
+                                  uint8_t* dyq, uint8_t* dysc, float* dw, const moe_dims& d,
+                                  cudaStream_t s) {
+  if (d.T == 0) return cudaSuccess;
+  const MxRowsOut mq{offs, dyq, dysc, d.E, (d.D + 127) / 128};
+  combine_bwd_kernel<2, true><<<grid_for_tokens(d.T), kThreads, 8 * (d.E + 1), s>>>(
+      reinterpret_cast<const uint4*>(dout), reinterpret_cast<const uint4*>(ys), w, pos,
+      reinterpret_cast<uint4*>(dys), dw, d.T, d.K, d.D / 8, mq);
   return cudaGetLastError();
 }
 

@@ -143,6 +143,29 @@ def test_quantize_rows_exact(case):
         assert_exact(f"{name} row scales", L.unpack_act_scales(to_host(sc), offs, C), wsc[:used])
 
 
+def test_combine_bwd_quantize_exact(case):
+    """moe_mx_combine_bwd on the oracle's ys: dys bit-exact (as
+    moe_combine_bwd), its MX codes and scales along D bit-exact, dw within
+    the tolerance."""
+    wl, inp, ref, refb = case
+    d = _dims(wl)
+    R, D = wl.T * wl.K, wl.D
+    offs = ref["group_offsets"]
+    used = int(offs[-1])
+    ys = np.zeros((R, D), np.uint16)
+    ys[:used] = ref["ys"]
+    dys = _nan_bf16((R, D))
+    dw = torch.full((wl.T, wl.K), float("nan"), dtype=torch.float32, device="cuda")
+    q, sc = _u8(B.moe_mx_bytes(d, B.MX_DYQ)), _sc(B.moe_mx_bytes(d, B.MX_DYSC))
+    B.moe_mx_combine_bwd(to_dev(inp["dy"]), to_dev(ys), to_dev(ref["w"]), to_dev(ref["pos"]),
+                         to_dev(offs), dys, q, sc, dw, d)
+    torch.cuda.synchronize()
+    assert_exact("dys", to_host(dys)[:used], refb["dys"])
+    assert_exact("dys codes along D", to_host(q).reshape(R, D)[:used], refb["dq"][:used])
+    assert_exact("dys scales along D", L.unpack_act_scales(to_host(sc), offs, D), refb["dsc"][:used])
+    assert_close("dw", to_host(dw), refb["dw"], bf16=False, atol=2e-2 * _rms(refb["dw"]))
+
+
 def test_quantize_tokens_exact(case):
     wl, inp, ref, refb = case
     d = _dims(wl)
