@@ -269,8 +269,11 @@ class HostPipeline:
     `dx` while step i+1 runs.  Ordering comes from CUDA events only (no host
     sync):
     - an upload into a slot waits until the step that last used it is done;
-    - a step waits for its upload, and its forward (backward) waits until the
-      previous `out` (`dx`) download has read the block's buffer.
+    - a step waits for its upload; `out` and `dx` alternate between two
+      device buffers, and a step's forward (backward) waits only until the
+      download of the `out` (`dx`) two steps back has read the buffer it
+      reuses (with one buffer each, a backward waited for the previous
+      step's whole `dx` download, which starts only when that step ends).
     Every step still moves all of its bytes across the host link; only the
     waiting is hidden.  `synchronize()` waits for the last download.
     """
@@ -293,9 +296,11 @@ class HostPipeline:
                 "ids": torch.empty((T, K), dtype=torch.int32, device=dev) if given else None,
                 "w": torch.empty((T, K), dtype=torch.float32, device=dev) if given else None,
             })
+        self.outs = [blk.out, torch.empty_like(blk.out)]
+        self.dxs = [blk.dx, torch.empty_like(blk.dx)] if self.train else [None, None]
         self.slot_free = [None, None]   # event: the last step using the slot is done
-        self.out_read = None            # event: the last `out` download has read blk.out
-        self.dx_read = None             # event: the last `dx` download has read blk.dx
+        self.out_read = [None, None]    # event: the download of outs[k] has read it
+        self.dx_read = [None, None]     # event: the download of dxs[k] has read it
         self.i = 0
 
     def step(self, x_h, out_h, dy_h=None, dx_h=None, logits_h=None, ids_h=None, w_h=None):
@@ -317,32 +322,36 @@ class HostPipeline:
                 s["w"].copy_(w_h, non_blocking=True)
             uploaded = torch.cuda.Event()
             uploaded.record(self.up)
+        out, dx = self.outs[k], self.dxs[k]
+        blk.out = out
+        if self.train:
+            blk.dx = dx
         with torch.cuda.stream(self.compute):
             self.compute.wait_event(uploaded)
-            if self.out_read is not None:
-                self.compute.wait_event(self.out_read)
+            if self.out_read[k] is not None:
+                self.compute.wait_event(self.out_read[k])
             blk.forward(s["x"], self.wi, self.wo, logits=s["logits"], bias=self.bias,
                         ids=s["ids"], w=s["w"])
             fwd_done = torch.cuda.Event()
             fwd_done.record(self.compute)
             done = fwd_done
             if self.train:
-                if self.dx_read is not None:
-                    self.compute.wait_event(self.dx_read)
+                if self.dx_read[k] is not None:
+                    self.compute.wait_event(self.dx_read[k])
                 blk.backward(s["dy"], self.wi, self.wo)
                 done = torch.cuda.Event()
                 done.record(self.compute)
         self.slot_free[k] = done
         with torch.cuda.stream(self.down):
             self.down.wait_event(fwd_done)
-            out_h.copy_(blk.out, non_blocking=True)
-            self.out_read = torch.cuda.Event()
-            self.out_read.record(self.down)
+            out_h.copy_(out, non_blocking=True)
+            self.out_read[k] = torch.cuda.Event()
+            self.out_read[k].record(self.down)
             if self.train:
                 self.down.wait_event(done)
-                dx_h.copy_(blk.dx, non_blocking=True)
-                self.dx_read = torch.cuda.Event()
-                self.dx_read.record(self.down)
+                dx_h.copy_(dx, non_blocking=True)
+                self.dx_read[k] = torch.cuda.Event()
+                self.dx_read[k].record(self.down)
         self.i += 1
 
     def synchronize(self):
