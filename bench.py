@@ -142,16 +142,23 @@ NCU_NAME = {
 }
 
 
-# the files holding the device code of the bf16 block's kernels (the traffic
-# figures under profiles/ are valid while these are unchanged)
-KERNEL_SOURCES = ("common.cuh", "gemm.cu", "kernels.h", "mx_common.cuh", "permute_combine.cu",
-                  "route.cu")
+# the files holding the device code behind each timed step of the bf16 block
+# (a step's traffic figure under profiles/ is valid while they are unchanged)
+_BASE_SOURCES = ("common.cuh", "kernels.h")
+_GATHER_SOURCES = _BASE_SOURCES + ("mx_common.cuh", "permute_combine.cu")
+_GEMM_SOURCES = _BASE_SOURCES + ("gemm.cu",)
+STEP_SOURCES = {
+    "route": _BASE_SOURCES + ("route.cu",),
+    **{n: _GATHER_SOURCES for n in ("permute", "combine", "combine_bwd", "permute_bwd")},
+    **{n: _GEMM_SOURCES for n in ("fc1", "fc2", "fc2_dlhs", "fc2_drhs", "fc1_dlhs", "fc1_drhs")},
+}
+KERNEL_SOURCES = tuple(sorted({f for v in STEP_SOURCES.values() for f in v}))
 
 
-def source_hash() -> str:
+def source_hash(files=KERNEL_SOURCES) -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "mixture_experts_ffn_histogram_gb300", "csrc")
-    for f in KERNEL_SOURCES:
+    for f in files:
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
@@ -159,17 +166,17 @@ def source_hash() -> str:
 
 def recorded_traffic(step: str, workload: str):
     """DRAM bytes per launch from a committed ncu summary, if it was taken on
-    the current kernel sources; else None."""
+    the current sources of that step's kernel; else None."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             rec = json.load(f)
     except (OSError, ValueError):
         return None
-    if rec.get("source_hash") != source_hash():
-        return None
     ent = rec.get("kernels", {}).get(workload, {}).get(step)
-    return None if ent is None else ent.get("dram_bytes_per_launch")
+    if ent is None or ent.get("source_hash") != source_hash(STEP_SOURCES[step]):
+        return None
+    return ent.get("dram_bytes_per_launch")
 
 
 def peaks():
