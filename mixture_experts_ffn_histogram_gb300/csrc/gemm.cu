@@ -441,14 +441,15 @@ __device__ __forceinline__ void zero_tail(uint8_t* sa, uint8_t* sb, int valid, i
   const int nrows = end - valid;
   if (nrows == 0) return;
   constexpr int kChunksAB = 2 + NACC * BN / 64 / CG;
-  const int nvec = kChunksAB * nrows * 8;
-  for (int i = lane; i < nvec; i += 32) {
-    const int line = i >> 3, part = i & 7;
-    const int chunk = line / nrows, j = valid + (line - chunk * nrows);
-    uint8_t* base = chunk < 2 ? sa + chunk * kChunkBytes : sb + (chunk - 2) * kChunkBytes;
-    uint8_t* addr = base + j * 128 + part * 16;
-    *reinterpret_cast<uint4*>(addr) = make_uint4(0u, 0u, 0u, 0u);
-    if constexpr (CG == 2) st_cluster_zero16(mapa_shared(smem_u32(addr), 1));
+  // lane i: 16-byte piece i % 8 of row valid + i / 8, in every 64-wide chunk
+  for (int i = lane; i < nrows * 8; i += 32) {
+    const int off = (valid + (i >> 3)) * 128 + (i & 7) * 16;
+#pragma unroll
+    for (int c = 0; c < kChunksAB; ++c) {
+      uint8_t* addr = (c < 2 ? sa + c * kChunkBytes : sb + (c - 2) * kChunkBytes) + off;
+      *reinterpret_cast<uint4*>(addr) = make_uint4(0u, 0u, 0u, 0u);
+      if constexpr (CG == 2) st_cluster_zero16(mapa_shared(smem_u32(addr), 1));
+    }
   }
   if constexpr (CG == 2) fence_proxy_async_cluster();
   else fence_proxy_async_smem();
@@ -1577,6 +1578,14 @@ cudaError_t launch_shape(const GemmCall& c, cudaStream_t s) {
 
 // Single-CTA shape: 3 stages of 48 KB and 3 staging buffers per warp.
 using Shape1 = Shape<256, 3, 1, 3>;
+// Lone-CTA drhs: a fourth operand stage in place of two of each epilogue
+// warp's staging buffers.  Short groups make these tiles a few k-blocks
+// long, each loading 48 KB of operands for 512 MMA cycles, and the feed is
+// bound by the bytes in flight: at E=256 experts of ~256 rows, FC1 drhs
+// 4.72 -> 4.07-4.25 ms, FC2 drhs 2.30 -> 1.94-2.13 ms.  (Two CTAs of a
+// cluster sharing B by TMA multicast were slower, 5.12 ms, as were CTA
+// pairs, 5.07 ms: both tie each stage to the slower of two CTAs.)
+using Shape1Drhs = Shape<256, 4, 1, 1>;
 // CTA-pair shapes: stages of 32 KB per CTA.  FC1 stages three buffers at once
 // (h, z gate, z up); the others need at most two.  FC1's fifth stage (paid
 // for with its fourth staging buffer) cuts the MMA's waits for operands from
@@ -1597,7 +1606,7 @@ using Shape2Dz = Shape<256, 4, 2, 0, 2>;
 // tiles reduce over their group's rows: with short groups (a few 64-row
 // blocks per tile) a tile is mostly epilogue, and single CTAs with
 // double-buffered accumulators do best (E=256 experts of ~256 rows: FC1
-// drhs 4.9 ms alone, 5.1 ms as 256-wide pairs, 5.3 ms as 512-wide pairs);
+// drhs 4.1-4.3 ms alone, 5.1 ms as 256-wide pairs, 5.6 ms as 512-wide pairs);
 // from ~1024 rows per group 512-wide pair tiles do (E=128 of ~2048 rows:
 // the step takes 7.73 ms with them, 8.07 ms with 256-wide pair tiles).
 // MOE_GEMM_PAIR=0/1 forces the choice.
@@ -1638,9 +1647,12 @@ cudaError_t launch_grouped_gemm(const GemmCall& c, cudaStream_t s) {
   if (c.kind == GemmKind::kFc1Gather || c.kind == GemmKind::kFc2Combine)
     return launch_shape<Shape1>(c, s);
   const bool dz = (c.kind == GemmKind::kDlhsFc2 && c.aux != nullptr);
-  if (!use_pairs(c)) return dz ? launch_shape<Shape1Dz>(c, s) : launch_shape<Shape1>(c, s);
-  if (c.kind == GemmKind::kDrhsFc2 || c.kind == GemmKind::kDrhsFc1)
-    return wide_drhs(c) ? launch_shape<Shape2Drhs>(c, s) : launch_shape<Shape2>(c, s);
+  const bool drhs = c.kind == GemmKind::kDrhsFc2 || c.kind == GemmKind::kDrhsFc1;
+  if (!use_pairs(c)) {
+    if (drhs) return launch_shape<Shape1Drhs>(c, s);
+    return dz ? launch_shape<Shape1Dz>(c, s) : launch_shape<Shape1>(c, s);
+  }
+  if (drhs) return wide_drhs(c) ? launch_shape<Shape2Drhs>(c, s) : launch_shape<Shape2>(c, s);
   if (c.kind == GemmKind::kFc1) return launch_shape<Shape2Fc1>(c, s);
   return dz ? launch_shape<Shape2Dz>(c, s) : launch_shape<Shape2>(c, s);
 }
