@@ -785,29 +785,39 @@ cudaError_t launch_route_histogram(const float* logits, const float* bias, int m
   // of the same workspace
   auto* bar = reinterpret_cast<unsigned long long*>(static_cast<uint8_t*>(scratch) + 64);
   int32_t* counts = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(scratch) + kRouteBarrierBytes);
-  // L: K rounded up to a power of two (at least 2); VPL keys per lane, 16
-  // or 32 with VPL >= L; G lanes per token, a power of two with G >= K and
-  // G * VPL >= E
+  // L: K rounded up to a power of two (at least 2).  G lanes per token, a
+  // power of two >= K, with VPL keys each (VPL >= L, at least 4, G * VPL >=
+  // E): the fewest keys per lane that cover E, the lanes doubled while a
+  // lane would hold more than 16 keys
   int L = 2;
   while (L < d.K) L <<= 1;
-  int vpl = 16;
-  while (vpl < L || vpl * 32 < d.E) vpl <<= 1;
   int G = 1;
-  while (G < d.K || G * vpl < d.E) G <<= 1;
+  while (G < d.K) G <<= 1;
+  int vpl = 4;
+  while (vpl < L || G * vpl < d.E) vpl <<= 1;
+  while (vpl > 16 && G < 32 && vpl / 2 >= L) {
+    G <<= 1;
+    vpl >>= 1;
+  }
 #define MOE_ROUTE(V, LL)                                                                   \
   launch_route_any<V, LL>(logits, bias, mode, ids, w, group_sizes, group_offsets, pos,   \
                           row_src, dev_status, bar, counts, max_blocks, d, G, s)
-  if (vpl == 16) {
-    if (L == 2) return MOE_ROUTE(16, 2);
-    if (L == 4) return MOE_ROUTE(16, 4);
-    if (L == 8) return MOE_ROUTE(16, 8);
-    return MOE_ROUTE(16, 16);
+  switch (vpl * 64 + L) {
+    case 4 * 64 + 2: return MOE_ROUTE(4, 2);
+    case 4 * 64 + 4: return MOE_ROUTE(4, 4);
+    case 8 * 64 + 2: return MOE_ROUTE(8, 2);
+    case 8 * 64 + 4: return MOE_ROUTE(8, 4);
+    case 8 * 64 + 8: return MOE_ROUTE(8, 8);
+    case 16 * 64 + 2: return MOE_ROUTE(16, 2);
+    case 16 * 64 + 4: return MOE_ROUTE(16, 4);
+    case 16 * 64 + 8: return MOE_ROUTE(16, 8);
+    case 16 * 64 + 16: return MOE_ROUTE(16, 16);
+    case 32 * 64 + 2: return MOE_ROUTE(32, 2);
+    case 32 * 64 + 4: return MOE_ROUTE(32, 4);
+    case 32 * 64 + 8: return MOE_ROUTE(32, 8);
+    case 32 * 64 + 16: return MOE_ROUTE(32, 16);
+    default: return MOE_ROUTE(32, 32);
   }
-  if (L == 2) return MOE_ROUTE(32, 2);
-  if (L == 4) return MOE_ROUTE(32, 4);
-  if (L == 8) return MOE_ROUTE(32, 8);
-  if (L == 16) return MOE_ROUTE(32, 16);
-  return MOE_ROUTE(32, 32);
 #undef MOE_ROUTE
 }
 
