@@ -206,17 +206,21 @@ __global__ void __launch_bounds__(kTqThreads, kTqCtasPerSm)
     return I;
   };
   // 128 rows x 16 16-byte segments: 8 per thread, a warp per two 256-byte
-  // rows; the gathered rows' indices are all loaded before any copy
-  auto issue = [&](const TqItem& I, uint8_t* buf) {
+  // rows.  The source rows of an item (gathered: loaded from row_src) are
+  // found one item before its copies are issued, so that no copy waits for
+  // an index load.
+  auto rows_of = [&](const TqItem& I, long (&sr)[8]) {
     const int seg = tid & 15;
     const bool col_ok = I.c0 + 8 * seg < a.C;
-    long sr[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const int r = 16 * i + (tid >> 4);
       sr[i] = (r < I.rows && col_ok) ? I.row0 + r : -1;
       if (TOKENS && a.row_src != nullptr && sr[i] >= 0) sr[i] = __ldg(a.row_src + sr[i]);
     }
+  };
+  auto issue = [&](const long (&sr)[8], const TqItem& I, uint8_t* buf) {
+    const int seg = tid & 15;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const int r = 16 * i + (tid >> 4);
@@ -232,13 +236,26 @@ __global__ void __launch_bounds__(kTqThreads, kTqCtasPerSm)
   if (it >= n_items) return;  // block-uniform
   if (tid == 0 && a.q != nullptr) tma_prefetch_map(&map_q);
   TqItem cur = decode(it);
-  issue(cur, tq_smem);
+  long sr_cur[8], sr_nxt[8];
+  rows_of(cur, sr_cur);
+  issue(sr_cur, cur, tq_smem);
+  TqItem nxt = cur;
+  if (it + gridDim.x < n_items) {
+    nxt = decode(it + gridDim.x);
+    rows_of(nxt, sr_nxt);
+  }
   for (int k = 0; it < n_items; it += gridDim.x, ++k) {
     const long nx = it + gridDim.x;
-    TqItem nxt = cur;
+    TqItem after = nxt;  // the item after the next one, and its rows
+    long sr_after[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) sr_after[i] = -1;
     if (nx < n_items) {
-      nxt = decode(nx);
-      issue(nxt, tq_smem + ((k + 1) & 1) * kTqBuf);
+      issue(sr_nxt, nxt, tq_smem + ((k + 1) & 1) * kTqBuf);
+      if (nx + gridDim.x < n_items) {
+        after = decode(nx + gridDim.x);
+        rows_of(after, sr_after);
+      }
       cp_async_wait_group<1>();
     } else {
       cp_async_wait_group<0>();
@@ -352,6 +369,9 @@ __global__ void __launch_bounds__(kTqThreads, kTqCtasPerSm)
     }
     __syncthreads();  // the input buffer is refilled two items on
     cur = nxt;
+    nxt = after;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) sr_nxt[i] = sr_after[i];
   }
   if (tid == 0) bulk_wait_all();
 }
