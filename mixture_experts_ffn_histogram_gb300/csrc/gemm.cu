@@ -68,7 +68,10 @@ constexpr int kBufBytes = 32 * 128;  // staging buffer: 32 rows x 64 bf16
 constexpr size_t kSmemLimit = 227 * 1024;
 constexpr int kSched = 8;  // tile-index slots of the dynamic (drhs) schedule
 
-struct SmemCtl {
+// CAP: experts the offset and block-prefix arrays hold (the launch's E must
+// not exceed it).
+template <int CAP>
+struct SmemCtlT {
   uint64_t full[kMaxStages];
   uint64_t empty[kMaxStages];
   uint64_t tfull[2];
@@ -79,12 +82,13 @@ struct SmemCtl {
   int sched[kSched];
   uint32_t tmem_base;
   int abort_flag;
-  int off[kMaxExperts + 1];  // group offsets
+  int off[CAP + 1];  // group offsets
   // forward/dlhs: prefix of (128*CG)-row blocks per group; drhs: sort keys
   // whose low 10 bits are the experts by descending reduction length
-  int mt[kMaxExperts + 1];
+  int mt[CAP + 1];
   int gtok[BM];              // gathered FC1: token of each row of the current tile
 };
+using SmemCtl = SmemCtlT<kMaxExperts>;
 
 // Tile shape: 128 x BN accumulator per CTA, CG CTAs per MMA, a `STAGES`-deep
 // operand ring, RING staging buffers per epilogue warp, and (ZB > 0) ZB slots
@@ -94,8 +98,11 @@ struct SmemCtl {
 // NACC = 2 makes a tile two accumulators wide (2*BN columns per CTA, all 512
 // TMEM columns): each A stage feeds two MMAs, so each SM loads 25% fewer bytes
 // per MMA, at the price of single-buffered accumulators.
-template <int BN_, int STAGES_, int CG_, int RING_, int ZB_ = 0, int NACC_ = 1>
+template <int BN_, int STAGES_, int CG_, int RING_, int ZB_ = 0, int NACC_ = 1,
+          int MAXE_ = kMaxExperts>
 struct Shape {
+  using Ctl = SmemCtlT<MAXE_>;
+  static constexpr int kMaxE = MAXE_;
   static constexpr int BN = BN_;
   static constexpr int kStages = STAGES_;
   static constexpr int CG = CG_;
@@ -113,7 +120,7 @@ struct Shape {
   static_assert(kTmemCols == 512, "TMEM columns");
   static constexpr int kEpiBytes = kEpiWarps * RING_ * kBufBytes;
   static constexpr size_t kSmemBytes =
-      1024 + static_cast<size_t>(STAGES_) * kStageBytes + kEpiBytes + kZBytes + sizeof(SmemCtl);
+      1024 + static_cast<size_t>(STAGES_) * kStageBytes + kEpiBytes + kZBytes + sizeof(Ctl);
   static_assert(BN == 256, "tile width");
   static_assert(CG == 1 || CG == 2, "CTA group");
   static_assert(STAGES_ >= 2 && STAGES_ <= kMaxStages, "stages");
@@ -171,8 +178,8 @@ struct Tile {
   int klen;   // drhs: group rows
 };
 
-template <int KIND, int BN, int CG>
-__device__ __forceinline__ Tile decode_tile(int t, int rank, const Params& p, const SmemCtl& s) {
+template <int KIND, int BN, int CG, class Ctl>
+__device__ __forceinline__ Tile decode_tile(int t, int rank, const Params& p, const Ctl& s) {
   Tile T;
   if constexpr (!Traits<KIND, BN, CG>::kGroupedK) {
     const int mt = t / p.n_tiles;
@@ -206,8 +213,8 @@ __device__ __forceinline__ Tile decode_tile(int t, int rank, const Params& p, co
   return T;
 }
 
-template <int KIND, int BN, int CG>
-__device__ __forceinline__ int total_tiles(const Params& p, const SmemCtl& s) {
+template <int KIND, int BN, int CG, class Ctl>
+__device__ __forceinline__ int total_tiles(const Params& p, const Ctl& s) {
   if constexpr (!Traits<KIND, BN, CG>::kGroupedK) return s.mt[p.E] * p.n_tiles;
   else return p.E * p.m_tiles * p.n_tiles;
 }
@@ -229,8 +236,8 @@ __host__ __device__ constexpr uint32_t sched_readers() { return CG == 2 ? 2 * kE
 
 // Next tile index for a reader (every thread of `mask` calls it; `releaser`
 // releases the slot).  Returns -1 when the wait gave up.
-template <int CG>
-__device__ __forceinline__ int sched_take(SmemCtl& s, uint32_t& seq, bool leader, bool releaser,
+template <int CG, class Ctl>
+__device__ __forceinline__ int sched_take(Ctl& s, uint32_t& seq, bool leader, bool releaser,
                                           unsigned mask, const WaitCtl& wc) {
   const uint32_t slot = seq % kSched;
   const uint32_t par = (seq / kSched) & 1u;
@@ -251,8 +258,8 @@ __device__ __forceinline__ int sched_take(SmemCtl& s, uint32_t& seq, bool leader
 
 // The even CTA's producer publishes tile index t to every reader.  Returns
 // false when the wait for a free slot gave up.
-template <int CG>
-__device__ __forceinline__ bool sched_publish(SmemCtl& s, uint32_t& seq, int t, const WaitCtl& wc) {
+template <int CG, class Ctl>
+__device__ __forceinline__ bool sched_publish(Ctl& s, uint32_t& seq, int t, const WaitCtl& wc) {
   const uint32_t slot = seq % kSched;
   const uint32_t par = (seq / kSched) & 1u;
   ++seq;
@@ -272,7 +279,8 @@ __device__ __forceinline__ bool sched_publish(SmemCtl& s, uint32_t& seq, int t, 
 // expert index) into s.mt, identically in every CTA: bitonic sort of
 // 32-bit keys (blocks, clamped to 22 bits, inverted | expert).  All threads
 // of the CTA call it after s.off is complete.
-__device__ __forceinline__ void sort_groups_desc(SmemCtl& s, int E) {
+template <class Ctl>
+__device__ __forceinline__ void sort_groups_desc(Ctl& s, int E) {
   int n = 1;
   while (n < E) n <<= 1;
   uint32_t* key = reinterpret_cast<uint32_t*>(s.mt);
@@ -915,7 +923,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* ring = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
   uint8_t* epi = ring + kStages * kStageBytes;  // staging of the epilogue warps
   uint8_t* zarea = epi + S::kEpiBytes;           // z rows of the fused SwiGLU backward
-  SmemCtl& s = *reinterpret_cast<SmemCtl*>(zarea + S::kZBytes);
+  typename S::Ctl& s = *reinterpret_cast<typename S::Ctl*>(zarea + S::kZBytes);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int rank = (CG == 2) ? static_cast<int>(cluster_ctarank()) : 0;
@@ -1421,6 +1429,7 @@ cudaError_t launch_shape(const GemmCall& c, cudaStream_t s) {
   constexpr int CG = S::CG;
   constexpr uint32_t kBRows = BN / CG;
   const moe_dims& d = c.d;
+  if (d.E > S::kMaxE) return cudaErrorInvalidValue;  // the control block's expert arrays
   const long R = static_cast<long>(d.T) * d.K;
   Params p{};
   p.offs = c.offs;
@@ -1598,6 +1607,11 @@ using Shape2Drhs = Shape<256, 3, 2, 2, 0, 2>;
 // warp, in which dz is also staged (no staging ring).
 using Shape1Dz = Shape<256, 3, 1, 0, 2>;
 using Shape2Dz = Shape<256, 4, 2, 0, 2>;
+// The same with a fifth operand stage, which fits beside the z slots when the
+// control block's expert arrays hold at most 128 experts.  Its operand feed
+// is bound by the bytes in flight (E=128, ~2048 rows per expert: 966 us with
+// three stages, 845 with four).
+using Shape2Dz5 = Shape<256, 5, 2, 0, 2, 1, 128>;
 
 // Whether a grouped GEMM runs on CTA pairs.  The pair's 256-row block is the
 // unit of rows for the forward and dlhs GEMMs; pairs pay off from ~256 rows
@@ -1654,7 +1668,8 @@ cudaError_t launch_grouped_gemm(const GemmCall& c, cudaStream_t s) {
   }
   if (drhs) return wide_drhs(c) ? launch_shape<Shape2Drhs>(c, s) : launch_shape<Shape2>(c, s);
   if (c.kind == GemmKind::kFc1) return launch_shape<Shape2Fc1>(c, s);
-  return dz ? launch_shape<Shape2Dz>(c, s) : launch_shape<Shape2>(c, s);
+  if (dz) return d.E <= Shape2Dz5::kMaxE ? launch_shape<Shape2Dz5>(c, s) : launch_shape<Shape2Dz>(c, s);
+  return launch_shape<Shape2>(c, s);
 }
 
 }  // namespace moe
