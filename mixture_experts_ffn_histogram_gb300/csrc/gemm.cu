@@ -1601,8 +1601,14 @@ using Shape1Drhs = Shape<256, 4, 1, 1>;
 // 20% to 16% of the kernel and its cycles by 5%.
 using Shape2Fc1 = Shape<256, 5, 2, 3>;
 using Shape2 = Shape<256, 5, 2, 2>;
+// With the control block's expert arrays for at most 128 experts a sixth
+// stage fits (E=128, ~2048 rows per expert: FC2 688 -> 674 us, FC2 drhs as
+// 256-wide pairs 687 -> 664 us, FC1 dlhs unchanged).
+using Shape2E128 = Shape<256, 6, 2, 2, 0, 1, 128>;
 // drhs: tiles two accumulators wide (fewer bytes loaded per MMA).
 using Shape2Drhs = Shape<256, 3, 2, 2, 0, 2>;
+// ... and a fourth stage for at most 128 experts (FC1 drhs 1243 -> 1219 us).
+using Shape2DrhsE128 = Shape<256, 4, 2, 2, 0, 2, 128>;
 // The FC2 dlhs with the fused SwiGLU backward: two z slots per epilogue
 // warp, in which dz is also staged (no staging ring).
 using Shape1Dz = Shape<256, 3, 1, 0, 2>;
@@ -1666,10 +1672,14 @@ cudaError_t launch_grouped_gemm(const GemmCall& c, cudaStream_t s) {
     if (drhs) return launch_shape<Shape1Drhs>(c, s);
     return dz ? launch_shape<Shape1Dz>(c, s) : launch_shape<Shape1>(c, s);
   }
-  if (drhs) return wide_drhs(c) ? launch_shape<Shape2Drhs>(c, s) : launch_shape<Shape2>(c, s);
+  const bool e128 = d.E <= 128;  // the shapes whose control block holds 128 experts
+  if (drhs) {
+    if (wide_drhs(c)) return e128 ? launch_shape<Shape2DrhsE128>(c, s) : launch_shape<Shape2Drhs>(c, s);
+    return e128 ? launch_shape<Shape2E128>(c, s) : launch_shape<Shape2>(c, s);
+  }
   if (c.kind == GemmKind::kFc1) return launch_shape<Shape2Fc1>(c, s);
-  if (dz) return d.E <= Shape2Dz5::kMaxE ? launch_shape<Shape2Dz5>(c, s) : launch_shape<Shape2Dz>(c, s);
-  return launch_shape<Shape2>(c, s);
+  if (dz) return e128 ? launch_shape<Shape2Dz5>(c, s) : launch_shape<Shape2Dz>(c, s);
+  return e128 ? launch_shape<Shape2E128>(c, s) : launch_shape<Shape2>(c, s);
 }
 
 }  // namespace moe
