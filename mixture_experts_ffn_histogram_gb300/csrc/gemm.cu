@@ -1616,7 +1616,7 @@ using Shape2Dz = Shape<256, 4, 2, 0, 2>;
 // The same with a fifth operand stage, which fits beside the z slots when the
 // control block's expert arrays hold at most 128 experts.  Its operand feed
 // is bound by the bytes in flight (E=128, ~2048 rows per expert: 966 us with
-// three stages, 845 with four).
+// three stages, 845 with four, 791 with five).
 using Shape2Dz5 = Shape<256, 5, 2, 0, 2, 1, 128>;
 
 // Whether a grouped GEMM runs on CTA pairs.  The pair's 256-row block is the
