@@ -86,7 +86,6 @@ struct SmemCtlT {
   // forward/dlhs: prefix of (128*CG)-row blocks per group; drhs: sort keys
   // whose low 10 bits are the experts by descending reduction length
   int mt[CAP + 1];
-  int gtok[BM];              // gathered FC1: token of each row of the current tile
 };
 using SmemCtl = SmemCtlT<kMaxExperts>;
 
@@ -136,7 +135,6 @@ struct Params {
   const __nv_bfloat16* aux;
   int32_t* status;
   unsigned int* tile_ctr;  // drhs: tiles claimed so far (zero at launch)
-  const uint16_t* xin;     // gathered FC1: token-major x [T, D]
   const int32_t* row_src;  // gathered FC1, combined FC2: slot j = t*K + k of each row
   const float* wts;        // combined FC2: routing weights [T, K]
   float* acc;              // combined FC2: fp32 [T, D] accumulator
@@ -329,6 +327,18 @@ __device__ __forceinline__ void load4(void* dst, const CUtensorMap* map, uint32_
                                       int c1, int c2, int c3) {
   if constexpr (CG == 1) tma_load_4d_addr(dst, map, bar, c0, c1, c2, c3);
   else tma_load_4d_pair(dst, map, bar, c0, c1, c2, c3);
+}
+
+// Four rows of a 2-D map whose box is 64 columns x 1 row, gathered into 512
+// consecutive bytes of shared memory (four 128-byte rows, swizzled by their
+// shared-memory address like any tile).
+__device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* map, uint32_t bar, int c0,
+                                            int r0, int r1, int r2, int r3) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3)
+      : "memory");
 }
 
 // MMA width of accumulator `a` of tile T: its valid output columns rounded
@@ -937,11 +947,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_map(&map_b);
     tma_prefetch_map(&map_c);
     tma_prefetch_map(&map_d);
-    // the gathered FC1's stages complete on the producer lane's arrival
-    // (with the B bytes) and on the 32 lanes' cp.async arrivals
-    constexpr uint32_t kFullArrivals = (KIND == static_cast<int>(GemmKind::kFc1Gather)) ? 33 : 1;
     for (int i = 0; i < kStages; ++i) {
-      mbar_init(&s.full[i], kFullArrivals);
+      mbar_init(&s.full[i], 1);
       mbar_init(&s.empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -1006,11 +1013,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0 && KIND == static_cast<int>(GemmKind::kFc1Gather)) {
     // ----------------------------------------- producer (gathered FC1 rows)
-    // The whole warp: lane 0 waits for a free stage, arms it and loads the B
-    // operand by TMA; then every lane copies its share of the tile's 128 A
-    // rows straight from the token-major x (row r of the tile is token
-    // row_src[r] / K) with 16-byte cp.async into the 128-byte-swizzled
-    // layout, and arrives on the stage's barrier when its copies have landed.
+    // The whole warp: lane 0 waits for a free stage, arms it with the whole
+    // stage's bytes and loads the B operand; then lane i gathers A rows
+    // 4i..4i+3 of the tile straight from the token-major x (row r of the
+    // tile is token row_src[r] / K) with one TMA gather of four 128-byte
+    // rows, which lands in the 128-byte-swizzled layout the MMA reads.
     if constexpr (KIND == static_cast<int>(GemmKind::kFc1Gather) && CG == 1) {
       uint32_t stage = 0, phase = 0;
       uint32_t fills[kStages];
@@ -1022,19 +1029,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         tstat += units;
         if (t >= ntiles) break;
         const Tile T = decode_tile<KIND, BNT, CG>(t, rank, p, s);
-        __syncwarp();  // the previous tile's tokens have been read
-        for (int i = lane; i < BM; i += 32) {
-          const long r = static_cast<long>(T.row0) + i;
-          int tok = 0;  // rows past the last are computed from token 0 and never stored
+        // this lane's four rows (rows past the last are gathered from token
+        // 0 and never stored)
+        int tok[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const long r = static_cast<long>(T.row0) + 4 * lane + q;
+          tok[q] = 0;
           if (r < p.R) {
             const int j = __ldg(p.row_src + r);
-            tok = j >= 0 ? j / p.Ktop : 0;
+            tok[q] = j >= 0 ? j / p.Ktop : 0;
           }
-          s.gtok[i] = tok;
         }
-        __syncwarp();
-        const uint32_t tx_bytes = stage_bytes<KIND, BN, CG, NACC>(T, p) - kAStageBytes;
-        const int c = lane & 7;  // 16-byte chunk of a 128-byte row
+        const uint32_t tx_bytes = stage_bytes<KIND, BN, CG, NACC>(T, p);
         for (int kb = 0; kb < T.kb; ++kb) {
           bool ok = true;
           if (lane == 0) ok = mbar_wait(&s.empty[stage], phase ^ 1u, wc);
@@ -1044,21 +1051,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive_expect_tx(&s.full[stage], tx_bytes);
             issue_loads<KIND, BN, CG, NACC>(T, kb, rank, sa, sa + kAStageBytes,
                                             smem_u32(&s.full[stage]), &map_a, &map_b, &map_d, p);
-            ++fills[stage];
           }
-          const uint16_t* xk = p.xin + static_cast<long>(kb) * BK + 8 * c;
-#pragma unroll 8
-          for (int i = 0; i < BM / 4; ++i) {
-            const int row = (lane >> 3) + 4 * i;
-            cp_async16(sa + row * 128 + ((c ^ (row & 7)) << 4),
-                       xk + static_cast<long>(s.gtok[row]) * p.Kdim);
-          }
-          cp_async_arrive_noinc(&s.full[stage]);
+          ++fills[stage];
+          __syncwarp();  // the stage is armed before any gather lands
+          tma_gather4(sa + 512 * lane, &map_a, smem_u32(&s.full[stage]), kb * BK, tok[0], tok[1],
+                      tok[2], tok[3]);
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
       }
-      cp_async_wait_all();  // this lane's copies have landed
-      if (aborted && lane == 0) {  // and the TMA bytes of stages in flight
+      if (aborted && lane == 0) {  // the copies of stages in flight land before the CTA exits
         for (int i = 0; i < kStages; ++i)
           if (fills[i] > 0) (void)mbar_wait_drain(&s.full[i], (fills[i] - 1u) & 1u, 100000000ull);
       }
@@ -1158,9 +1159,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          // the gathered A rows were written by cp.async (the generic proxy);
-          // the MMA reads them through the async proxy
-          if constexpr (KIND == static_cast<int>(GemmKind::kFc1Gather)) fence_proxy_async_smem();
           uint8_t* sa = ring + stage * kStageBytes;
           uint8_t* sb = sa + kAStageBytes;
           int ksteps = BK / kUmmaK;
@@ -1515,20 +1513,20 @@ cudaError_t launch_shape(const GemmCall& c, cudaStream_t s) {
               return launch_kind<3, S>(ma, mb, mc, mc, p, row_blocks_bound * p.n_tiles, s);
             case GemmKind::kFc1Gather:
               // FC1 on rows gathered from x by row_src (single CTAs); the A
-              // map is unused (the producer warp copies the rows)
+              // map is x [T][D] with a box of one row, for four-row gathers
               if constexpr (S::CG == 1 && S::kRing % 3 == 0) {
                 p.Kdim = d.D;
                 p.N = d.F;
                 p.n_tiles = static_cast<int>(cdiv(d.F, BN / 2));
-                p.xin = static_cast<const uint16_t*>(c.a);
                 p.row_src = c.row_src;
                 p.Ktop = d.K;
                 p.R = R;
-                ok = map_chunks(&mb, c.b, F2, d.D, d.E, BN / 64 / 2, 4) &&
+                ok = map2d(&ma, c.a, d.D, d.T, 64, 1) &&
+                     map_chunks(&mb, c.b, F2, d.D, d.E, BN / 64 / 2, 4) &&
                      map2d(&mc, c.out0, d.F, R, 64, 32);
                 if (ok) ok = (c.out1 != nullptr) ? map_halves(&md, c.out1, d.F, R) : (md = mc, true);
                 if (!ok || c.row_src == nullptr) return cudaErrorInvalidValue;
-                return launch_kind<6, S>(mb, mb, mc, md, p, row_blocks_bound * p.n_tiles, s);
+                return launch_kind<6, S>(ma, mb, mc, md, p, row_blocks_bound * p.n_tiles, s);
               }
               return cudaErrorInvalidValue;
             case GemmKind::kFc2Combine:
