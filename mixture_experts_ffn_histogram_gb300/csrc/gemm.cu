@@ -350,12 +350,13 @@ __device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* map, u
 // With larger groups row blocks of one expert re-read its weights, and the
 // hint costs more than it saves (8192 tokens: FC2 175 -> 183 us), so the
 // loads keep the normal policy.
+// (Not volatile: a kind that loads no weights drops it.)
 __device__ __forceinline__ uint64_t weight_policy(int evict_first) {
   uint64_t pol;
   if (evict_first)
-    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
   else
-    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
+    asm("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
   return pol;
 }
 template <int CG>
