@@ -100,3 +100,35 @@ def test_route_tied_scores(T):
     assert np.mean(np.any(srt[:, 1:] == srt[:, :-1], axis=1)) > 0.5
     g = _run(wl, logits, None)
     _check(wl, g, logits, None)
+
+
+@pytest.mark.parametrize("T", [64, 1024, 8192])
+def test_bad_ids_on_both_kernels(T):
+    """Given routing with ids out of range: MOE_ERR_DEVICE, the bad slots
+    dropped (pos -1), the rest placed as the oracle places them, and the
+    rows that no valid slot fills set to -1 (64 and 1024 tokens on the
+    cluster kernel, 8192 on the cooperative one)."""
+    E, K = 16, 4
+    d = B.dims(T, 64, E, K, 64)
+    rng = np.random.Generator(np.random.PCG64(T))
+    ids = rng.integers(0, E, (T, K)).astype(np.int32)
+    bad_t = rng.choice(T, size=min(T, 5), replace=False)
+    for i, t in enumerate(bad_t):
+        ids[t, i % K] = E + i if i % 2 == 0 else -1 - i
+    w = np.full((T, K), 0.25, np.float32)
+    gs = torch.full((E,), -7, dtype=torch.int32, device="cuda")
+    off = torch.full((E + 1,), -7, dtype=torch.int32, device="cuda")
+    pos = torch.full((T, K), -7, dtype=torch.int32, device="cuda")
+    row_src = torch.full((T * K,), -7, dtype=torch.int32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ws = torch.empty(max(B.moe_workspace_bytes(d), 256), dtype=torch.uint8, device="cuda")
+    B.moe_route_histogram(None, None, B.SCORE_GIVEN, to_dev(ids), to_dev(w), gs, off, pos,
+                          row_src, st, ws, d)
+    torch.cuda.synchronize()
+    assert int(st.item()) == B.MOE_ERR_DEVICE
+    gref, oref, pref, rref, bad = oracle.histogram(ids, E)
+    assert bad == len(bad_t)
+    assert_exact("group_sizes", to_host(gs), gref)
+    assert_exact("group_offsets", to_host(off), oref)
+    assert_exact("pos", to_host(pos), pref)
+    assert_exact("row_src", to_host(row_src), rref)
