@@ -93,12 +93,14 @@ using SmemCtl = SmemCtlT<kMaxExperts>;
 // operand ring, RING staging buffers per epilogue warp, and (ZB > 0) ZB slots
 // per epilogue warp into which TMA loads the z rows that the fused SwiGLU
 // backward reads and from which it stores dz (no staging ring needed then).
+// A z slot holds the gate and up halves of 32 rows x ZW columns: 8 KB at 64
+// columns (128-byte rows), 4 KB at 32 (64-byte rows, 64-byte swizzle).
 //
 // NACC = 2 makes a tile two accumulators wide (2*BN columns per CTA, all 512
 // TMEM columns): each A stage feeds two MMAs, so each SM loads 25% fewer bytes
 // per MMA, at the price of single-buffered accumulators.
 template <int BN_, int STAGES_, int CG_, int RING_, int ZB_ = 0, int NACC_ = 1,
-          int MAXE_ = kMaxExperts>
+          int MAXE_ = kMaxExperts, int ZW_ = 64>
 struct Shape {
   using Ctl = SmemCtlT<MAXE_>;
   static constexpr int kMaxE = MAXE_;
@@ -109,7 +111,9 @@ struct Shape {
   static constexpr bool kZB = ZB_ != 0;
   static constexpr int kZSlots = ZB_;
   static constexpr int kNacc = NACC_;
-  static constexpr int kZBytes = kEpiWarps * ZB_ * 2 * kBufBytes;
+  static constexpr int kZW = ZW_;                  // z chunk width (columns)
+  static constexpr int kZBuf = 32 * ZW_ * 2;       // one half (gate or up) of a slot
+  static constexpr int kZBytes = kEpiWarps * ZB_ * 2 * kZBuf;
   static constexpr int kBRows = BN / CG;  // B columns held by one CTA, per accumulator
   static constexpr int kBStageBytes = NACC_ * kBRows * BK * 2;
   static constexpr int kStageBytes = kAStageBytes + kBStageBytes;
@@ -125,6 +129,7 @@ struct Shape {
   static_assert(STAGES_ >= 2 && STAGES_ <= kMaxStages, "stages");
   static_assert(RING_ >= (ZB_ ? 0 : 1) && RING_ <= 4, "staging ring");
   static_assert(ZB_ == 0 || ZB_ == 2, "z slots");
+  static_assert(ZW_ == 64 || ZW_ == 32, "z chunk width");
   static_assert(kSmemBytes <= kSmemLimit, "shared memory");
 };
 
@@ -570,6 +575,17 @@ __device__ __forceinline__ void put_half(uint8_t* buf, int lane, int h, const ui
   }
 }
 
+// A buffer of 64-byte rows under the 64-byte swizzle: 16-byte unit j of row
+// r sits at unit j ^ ((r >> 1) & 3) of the row (address bits 4-5 XOR bits 7-8).
+__device__ __forceinline__ int row64_unit(int r, int j) { return r * 64 + ((j ^ ((r >> 1) & 3)) << 4); }
+// 16 packed bf16 pairs = the 32 columns of row `lane` of such a buffer.
+__device__ __forceinline__ void put_row64(uint8_t* buf, int lane, const uint32_t (&w)[16]) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    *reinterpret_cast<uint4*>(buf + row64_unit(lane, j)) =
+        make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+}
+
 __device__ __forceinline__ void pack16(const uint32_t (&v)[32], uint32_t (&w)[16]) {
 #pragma unroll
   for (int i = 0; i < 16; ++i)
@@ -603,7 +619,7 @@ __device__ __forceinline__ void flush_3d(uint8_t* buf, const CUtensorMap* map, i
 }
 
 // z rows of the fused SwiGLU backward, by TMA: two slots per epilogue warp,
-// each the gate and up rows (32 x 64 bf16 each) of one 64-column chunk.  The
+// each the gate and up rows (32 x ZW bf16 each) of one ZW-column chunk.  The
 // backward of a chunk is written over the z it read, and stored from there.
 // Requests run up to two chunks ahead, into the next tile of the warp's
 // (static) schedule: that tile's first chunks then arrive while its
@@ -636,20 +652,22 @@ __device__ __forceinline__ bool z_by_tma(const Tile& T, const EpiCtx<RING>& c, c
   return KIND == static_cast<int>(GemmKind::kDlhsFc2) && ZB && p.aux != nullptr &&
          T.rows - 32 * c.q >= 32;
 }
-// 64-column chunks of tile T that hold output columns (FC2 dlhs: N = F).
+// ZW-column chunks of tile T that hold output columns (FC2 dlhs: N = F).
+template <int ZW>
 __device__ __forceinline__ int z_chunks(const Tile& T, int BN, const Params& p) {
-  return max(0, min(BN, p.F - T.n0) + 63) / 64;
+  return max(0, min(BN, p.F - T.n0) + ZW - 1) / ZW;
 }
 // Request the gate and up z rows of chunk `ch` of tile T into the next slot,
 // once the store that last read that slot has read it.
-template <int RING>
+template <int ZW, int RING>
 __device__ __forceinline__ void z_issue(const Tile& T, int ch, EpiCtx<RING>& c) {
+  constexpr int kZBuf = 32 * ZW * 2;
   ZPipe& z = c.zp;
   if (c.lane == 0) {
     bulk_wait_read<0>();
     uint64_t* b = z.bar + z.send;
-    mbar_arrive_expect_tx(b, 2 * kBufBytes);
-    tma_load_3d_addr(z.buf + z.send * 2 * kBufBytes, c.map_d, smem_u32(b), T.n0 + 64 * ch,
+    mbar_arrive_expect_tx(b, 2 * kZBuf);
+    tma_load_3d_addr(z.buf + z.send * 2 * kZBuf, c.map_d, smem_u32(b), T.n0 + ZW * ch,
                      T.row0 + 32 * c.q, 0);  // gate chunk, then up chunk
   }
   __syncwarp();
@@ -658,18 +676,18 @@ __device__ __forceinline__ void z_issue(const Tile& T, int ch, EpiCtx<RING>& c) 
 }
 // Keep two requests in flight: the rest of tile t's chunks, then (when it
 // also takes its z by TMA) the first chunks of the warp's next tile tn.
-template <int KIND, int BN, bool ZB, int RING>
+template <int KIND, int BN, bool ZB, int RING, int ZW>
 __device__ __forceinline__ void z_fill(int t, const Tile& T, int tn, const Tile& Tn,
                                        EpiCtx<RING>& c, const Params& p) {
   ZPipe& z = c.zp;
   while (z.out < 2) {
-    if (z.qt == t && z.qch < z_chunks(T, BN, p)) {
-      z_issue(T, z.qch++, c);
+    if (z.qt == t && z.qch < z_chunks<ZW>(T, BN, p)) {
+      z_issue<ZW>(T, z.qch++, c);
     } else if (z.qt == t && tn >= 0 && z_by_tma<KIND, ZB, RING>(Tn, c, p)) {
       z.qt = tn;
       z.qch = 0;
-    } else if (z.qt == tn && tn >= 0 && z.qch < z_chunks(Tn, BN, p)) {
-      z_issue(Tn, z.qch++, c);
+    } else if (z.qt == tn && tn >= 0 && z.qch < z_chunks<ZW>(Tn, BN, p)) {
+      z_issue<ZW>(Tn, z.qch++, c);
     } else {
       break;
     }
@@ -700,7 +718,7 @@ __device__ __forceinline__ void z_drain(EpiCtx<RING>& c) {
 
 // t, tn, Tn: the tile's index and the warp's next tile (index, or -1), for
 // the z requests of the fused SwiGLU backward.
-template <int KIND, int BN, int CG, int RING, bool ZB>
+template <int KIND, int BN, int CG, int RING, bool ZB, int ZW>
 __device__ __forceinline__ void epilogue_tile(const Tile& T, uint32_t tbase, EpiCtx<RING>& c,
                                               const Params& p, int t, int tn, const Tile& Tn) {
   const int lane = c.lane;
@@ -779,33 +797,50 @@ __device__ __forceinline__ void epilogue_tile(const Tile& T, uint32_t tbase, Epi
     } else if constexpr (KIND == static_cast<int>(GemmKind::kDlhsFc2) && ZB) {
       // fused SwiGLU backward on a shape with z slots (these run nothing else)
       if (full) {
-        for (int ch = 0; ch < BN / 64; ++ch) {
-          const int f0 = T.n0 + 64 * ch;
+        constexpr int kZBuf = 32 * ZW * 2;
+        for (int ch = 0; ch < BN / ZW; ++ch) {
+          const int f0 = T.n0 + ZW * ch;
           if (f0 >= p.F) break;
           const int slot = z_take(c);
           if (slot < 0) return;
-          uint8_t* gbuf = c.zp.buf + slot * 2 * kBufBytes;
-          uint8_t* ubuf = gbuf + kBufBytes;
-          uint4 zg[8], zu[8];
+          uint8_t* gbuf = c.zp.buf + slot * 2 * kZBuf;
+          uint8_t* ubuf = gbuf + kZBuf;
+          if constexpr (ZW == 64) {
+            uint4 zg[8], zu[8];
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const int off = lane * 128 + ((j ^ (lane & 7)) << 4);
-            zg[j] = *reinterpret_cast<const uint4*>(gbuf + off);
-            zu[j] = *reinterpret_cast<const uint4*>(ubuf + off);
-          }
+            for (int j = 0; j < 8; ++j) {
+              const int off = lane * 128 + ((j ^ (lane & 7)) << 4);
+              zg[j] = *reinterpret_cast<const uint4*>(gbuf + off);
+              zu[j] = *reinterpret_cast<const uint4*>(ubuf + off);
+            }
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            tmem_ld_32x32b_x32(tbase + 64 * ch + 32 * h, v);
+            for (int h = 0; h < 2; ++h) {
+              tmem_ld_32x32b_x32(tbase + 64 * ch + 32 * h, v);
+              tmem_ld_wait();
+              uint32_t wg[16], wu[16];
+              swiglu_bwd32(v, zg + 4 * h, zu + 4 * h, wg, wu);
+              // each lane overwrites its own row of the z it has read
+              put_half(gbuf, lane, h, wg);
+              put_half(ubuf, lane, h, wu);
+            }
+          } else {
+            uint4 zg[4], zu[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const int off = row64_unit(lane, j);
+              zg[j] = *reinterpret_cast<const uint4*>(gbuf + off);
+              zu[j] = *reinterpret_cast<const uint4*>(ubuf + off);
+            }
+            tmem_ld_32x32b_x32(tbase + 32 * ch, v);
             tmem_ld_wait();
             uint32_t wg[16], wu[16];
-            swiglu_bwd32(v, zg + 4 * h, zu + 4 * h, wg, wu);
-            // each lane overwrites its own row of the z it has read
-            put_half(gbuf, lane, h, wg);
-            put_half(ubuf, lane, h, wu);
+            swiglu_bwd32(v, zg, zu, wg, wu);
+            put_row64(gbuf, lane, wg);
+            put_row64(ubuf, lane, wu);
           }
           publish();
           flush_3d(gbuf, c.map_c, f0, y, 0, lane);  // dgate, dup
-          z_fill<KIND, BN, ZB, RING>(t, T, tn, Tn, c, p);
+          z_fill<KIND, BN, ZB, RING, ZW>(t, T, tn, Tn, c, p);
         }
         return;
       }
@@ -1265,7 +1300,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // -------------------------------------------------------- epilogue
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     EpiCtx<RING> ec{&map_c, &map_d, Ring<RING>{epi + (warp - 2) * RING * kBufBytes, 0u}, q, lane,
-                    ZPipe{zarea + (warp - 2) * S::kZSlots * 2 * kBufBytes, &s.zbar[warp - 2][0],
+                    ZPipe{zarea + (warp - 2) * S::kZSlots * 2 * S::kZBuf, &s.zbar[warp - 2][0],
                           0u, 0, 0, 0, -1, 0},
                     &wc};
     uint32_t tempty_peer = 0;
@@ -1308,7 +1343,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ec.zp.qt = t;
             ec.zp.qch = 0;
           }
-          z_fill<KIND, BN, true, RING>(t, T, tn, Tn, ec, p);
+          z_fill<KIND, BN, true, RING, S::kZW>(t, T, tn, Tn, ec, p);
         }
       }
       if (!__all_sync(0xffffffffu, mbar_wait(&s.tfull[acc], acc_phase, wc))) break;
@@ -1317,7 +1352,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int a = 0; a < NACC; ++a) {
         Tile Ta = T;
         Ta.n0 = T.n0 + a * BN;
-        epilogue_tile<KIND, BN, CG, RING, S::kZB>(
+        epilogue_tile<KIND, BN, CG, RING, S::kZB, S::kZW>(
             Ta, tmem_base + acc * S::kAccStride + a * BN + (static_cast<uint32_t>(q * 32) << 16),
             ec, p, t, tn, Tn);
       }
@@ -1366,8 +1401,10 @@ EncodeTiledFn encode_fn() {
 }
 
 // bf16 tensor map, dims innermost first; strides in bytes for dims 1..rank-1.
+// The swizzle span must equal the box's inner extent in bytes (128 or 64).
 bool make_map(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
-              const uint64_t* strides, const uint32_t* box) {
+              const uint64_t* strides, const uint32_t* box,
+              CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return false;
   cuuint64_t gd[4], gs[3];
@@ -1378,8 +1415,7 @@ bool make_map(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
   }
   for (int i = 0; i + 1 < rank; ++i) gs[i] = strides[i];
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), gd, gs, bd, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+            CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 bool map2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner,
@@ -1399,14 +1435,16 @@ bool map3d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t mid, uint6
 }
 
 // A [rows][2F] tensor of gate and up halves (z, dz) seen as [2][rows][F]:
-// one box of 32 rows x 64 columns per half moves a gate chunk and the up
+// one box of 32 rows x `cols` columns per half moves a gate chunk and the up
 // chunk F columns to its right with one instruction, into two consecutive
-// 4 KB staging buffers.  Dims (innermost first): F, rows, 2.
-bool map_halves(CUtensorMap* m, const void* base, uint64_t F, uint64_t rows) {
+// staging buffers (4 KB with 128-byte rows at 64 columns, 2 KB with 64-byte
+// rows at 32).  Dims (innermost first): F, rows, 2.
+bool map_halves(CUtensorMap* m, const void* base, uint64_t F, uint64_t rows, uint32_t cols = 64) {
   const uint64_t dims[3] = {F, rows, 2};
   const uint64_t strides[2] = {4 * F, 2 * F};
-  const uint32_t box[3] = {64, 32, 2};
-  return make_map(m, base, 3, dims, strides, box);
+  const uint32_t box[3] = {cols, 32, 2};
+  return make_map(m, base, 3, dims, strides, box,
+                  cols == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
 // An MN-major operand [outer][rows][inner] (inner contiguous, a multiple of
@@ -1508,7 +1546,7 @@ cudaError_t launch_shape(const GemmCall& c, cudaStream_t s) {
     p.N = d.F;
     p.n_tiles = static_cast<int>(cdiv(d.F, BN));
     ok = map2d(&ma, c.a, d.D, R, 64, BM) && map3d(&mb, c.b, d.D, d.F, d.E, 64, kBRows) &&
-         map_halves(&mc, c.out0, d.F, R) && map_halves(&md, c.aux, d.F, R);
+         map_halves(&mc, c.out0, d.F, R, S::kZW) && map_halves(&md, c.aux, d.F, R, S::kZW);
     if (!ok) return cudaErrorInvalidValue;
     return launch_kind<2, S>(ma, mb, mc, md, p, row_blocks_bound * p.n_tiles, s);
   } else {
@@ -1666,14 +1704,19 @@ using Shape2Drhs = Shape<256, 3, 2, 2, 0, 2>;
 // ... and a fourth stage for at most 128 experts (FC1 drhs 1243 -> 1219 us).
 using Shape2DrhsE128 = Shape<256, 4, 2, 2, 0, 2, 128>;
 // The FC2 dlhs with the fused SwiGLU backward: two z slots per epilogue
-// warp, in which dz is also staged (no staging ring).
+// warp, in which dz is also staged (no staging ring).  Its operand feed is
+// bound by the bytes in flight up to five stages (E=128, ~2048 rows per
+// expert: 966 us with three stages, 845 with four, 791 with five; a sixth
+// measured the same, 806 vs 807-813 us), so the slots hold 32-column chunks
+// (32 KB for the four warps instead of 64) and the space goes to the operand
+// ring: six stages on pairs when the control block's expert arrays hold at
+// most 128 experts, five (instead of four) for up to 1024; a lone CTA's
+// 48 KB stages fit four times with 128 experts, three times (beside
+// 64-column slots) with 1024.
 using Shape1Dz = Shape<256, 3, 1, 0, 2>;
-using Shape2Dz = Shape<256, 4, 2, 0, 2>;
-// The same with a fifth operand stage, which fits beside the z slots when the
-// control block's expert arrays hold at most 128 experts.  Its operand feed
-// is bound by the bytes in flight (E=128, ~2048 rows per expert: 966 us with
-// three stages, 845 with four, 791 with five).
-using Shape2Dz5 = Shape<256, 5, 2, 0, 2, 1, 128>;
+using Shape1DzE128 = Shape<256, 4, 1, 0, 2, 1, 128, 32>;
+using Shape2Dz = Shape<256, 5, 2, 0, 2, 1, kMaxExperts, 32>;
+using Shape2DzE128 = Shape<256, 6, 2, 0, 2, 1, 128, 32>;
 
 // Whether a grouped GEMM runs on CTA pairs.  The pair's 256-row block is the
 // unit of rows for the forward and dlhs GEMMs; pairs pay off from ~256 rows
@@ -1724,17 +1767,18 @@ cudaError_t launch_grouped_gemm(const GemmCall& c, cudaStream_t s) {
     return launch_shape<Shape1>(c, s);
   const bool dz = (c.kind == GemmKind::kDlhsFc2 && c.aux != nullptr);
   const bool drhs = c.kind == GemmKind::kDrhsFc2 || c.kind == GemmKind::kDrhsFc1;
+  const bool e128 = d.E <= 128;  // the shapes whose control block holds 128 experts
   if (!use_pairs(c)) {
     if (drhs) return launch_shape<Shape1Drhs>(c, s);
-    return dz ? launch_shape<Shape1Dz>(c, s) : launch_shape<Shape1>(c, s);
+    if (dz) return e128 ? launch_shape<Shape1DzE128>(c, s) : launch_shape<Shape1Dz>(c, s);
+    return launch_shape<Shape1>(c, s);
   }
-  const bool e128 = d.E <= 128;  // the shapes whose control block holds 128 experts
   if (drhs) {
     if (wide_drhs(c)) return e128 ? launch_shape<Shape2DrhsE128>(c, s) : launch_shape<Shape2Drhs>(c, s);
     return e128 ? launch_shape<Shape2E128>(c, s) : launch_shape<Shape2>(c, s);
   }
   if (c.kind == GemmKind::kFc1) return launch_shape<Shape2Fc1>(c, s);
-  if (dz) return e128 ? launch_shape<Shape2Dz5>(c, s) : launch_shape<Shape2Dz>(c, s);
+  if (dz) return e128 ? launch_shape<Shape2DzE128>(c, s) : launch_shape<Shape2Dz>(c, s);
   return e128 ? launch_shape<Shape2E128>(c, s) : launch_shape<Shape2>(c, s);
 }
 
