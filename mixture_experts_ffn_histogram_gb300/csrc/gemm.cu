@@ -1710,9 +1710,10 @@ using Shape2DrhsE128 = Shape<256, 4, 2, 2, 0, 2, 128>;
 // measured the same, 806 vs 807-813 us), so the slots hold 32-column chunks
 // (32 KB for the four warps instead of 64) and the space goes to the operand
 // ring: six stages on pairs when the control block's expert arrays hold at
-// most 128 experts, five (instead of four) for up to 1024; a lone CTA's
-// 48 KB stages fit four times with 128 experts, three times (beside
-// 64-column slots) with 1024.
+// most 128 experts, five (instead of four) for up to 1024 (E=256, ~256 rows
+// per expert: 2095-2111 -> 1885-1890 us, same box); a lone CTA's 48 KB
+// stages fit four times with 128 experts, three times (beside 64-column
+// slots) with 1024.
 using Shape1Dz = Shape<256, 3, 1, 0, 2>;
 using Shape1DzE128 = Shape<256, 4, 1, 0, 2, 1, 128, 32>;
 using Shape2Dz = Shape<256, 5, 2, 0, 2, 1, kMaxExperts, 32>;
