@@ -314,6 +314,14 @@ __device__ __forceinline__ void sort_groups_desc(Ctl& s, int E) {
   }
 }
 
+// How many of the first n uses of a ring of S slots (taken in order 0, 1,
+// ..., S-1, 0, ...) fell on slot i.  The producer and MMA loops keep one
+// count instead of a per-slot array (which a run-time index would put in
+// local memory).
+__device__ __forceinline__ uint32_t ring_uses(uint32_t n, uint32_t i, uint32_t S) {
+  return n > i ? (n - i + S - 1) / S : 0u;
+}
+
 // One TMA load of a stage: for a pair, the bytes complete on the even CTA's
 // barrier (`bar` is then its shared::cluster address).
 template <int CG>
@@ -1109,10 +1117,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // tile is token row_src[r] / K) with one TMA gather of four 128-byte
     // rows, which lands in the 128-byte-swizzled layout the MMA reads.
     if constexpr (KIND == static_cast<int>(GemmKind::kFc1Gather) && CG == 1) {
-      uint32_t stage = 0, phase = 0;
-      uint32_t fills[kStages];
-#pragma unroll
-      for (int i = 0; i < kStages; ++i) fills[i] = 0;
+      uint32_t stage = 0, phase = 0, nfill = 0;  // stages filled so far
       bool aborted = false;
       while (!aborted) {
         const int t = tstat;
@@ -1142,7 +1147,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             issue_loads<KIND, BN, CG, NACC>(T, kb, rank, sa, sa + kAStageBytes,
                                             smem_u32(&s.full[stage]), &map_a, &map_b, &map_d, p);
           }
-          ++fills[stage];
+          ++nfill;
           __syncwarp();  // the stage is armed before any gather lands
           tma_gather4(sa + 512 * lane, &map_a, smem_u32(&s.full[stage]), kb * BK, tok[0], tok[1],
                       tok[2], tok[3]);
@@ -1150,8 +1155,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (aborted && lane == 0) {  // the copies of stages in flight land before the CTA exits
-        for (int i = 0; i < kStages; ++i)
-          if (fills[i] > 0) (void)mbar_wait_drain(&s.full[i], (fills[i] - 1u) & 1u, 100000000ull);
+        for (uint32_t i = 0; i < kStages; ++i) {
+          const uint32_t f = ring_uses(nfill, i, kStages);
+          if (f > 0) (void)mbar_wait_drain(&s.full[i], (f - 1u) & 1u, 100000000ull);
+        }
       }
     }
   } else if (warp == 0) {
@@ -1159,10 +1166,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       // For a pair, both CTAs' bytes complete on the even CTA's full barrier,
       // which the even CTA arms with the bytes of both.
-      uint32_t stage = 0, phase = 0;
-      uint32_t fills[kStages];
-#pragma unroll
-      for (int i = 0; i < kStages; ++i) fills[i] = 0;
+      uint32_t stage = 0, phase = 0, nfill = 0;  // stages filled so far
       const uint32_t full0 = (CG == 2) ? mapa_shared(smem_u32(&s.full[0]), 0) : smem_u32(&s.full[0]);
       bool aborted = false;
       // dynamic schedule: the even CTA claims the next tile a little before
@@ -1195,24 +1199,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           issue_loads<KIND, BN, CG, NACC>(T, kb, rank, sa, sa + kAStageBytes,
                                           full0 + stage * static_cast<uint32_t>(sizeof(uint64_t)),
                                           &map_a, &map_b, &map_d, p);
-          ++fills[stage];
+          ++nfill;
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
         if (!next_claimed) claimed = static_cast<int>(atomicAdd(p.tile_ctr, 1u));
       }
       if (aborted && leader) {  // let copies already in flight land before the CTA exits
-        for (int i = 0; i < kStages; ++i)
-          if (fills[i] > 0) (void)mbar_wait_drain(&s.full[i], (fills[i] - 1u) & 1u, 100000000ull);
+        for (uint32_t i = 0; i < kStages; ++i) {
+          const uint32_t f = ring_uses(nfill, i, kStages);
+          if (f > 0) (void)mbar_wait_drain(&s.full[i], (f - 1u) & 1u, 100000000ull);
+        }
       }
     }
   } else if (warp == 1) {
     if (CG == 1 || leader) {
       // ----------------------------------------------------------- MMA
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
-      uint32_t commits[kStages];
-#pragma unroll
-      for (int i = 0; i < kStages; ++i) commits[i] = 0;
-      int last_stage = -1;
+      uint32_t ncommit = 0;  // stages whose MMAs were committed so far
       bool aborted = false;
       while (!aborted) {
         int t;
@@ -1281,8 +1284,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             umma_commit<CG>(&s.empty[stage]);
           }
           __syncwarp();
-          ++commits[stage];
-          last_stage = static_cast<int>(stage);
+          ++ncommit;
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
         if (aborted) break;
@@ -1290,8 +1292,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (++acc == S::kAccSlots) { acc = 0; acc_phase ^= 1u; }
       }
-      if (aborted && last_stage >= 0) {  // let issued MMAs finish before TMEM is freed
-        (void)mbar_wait_drain(&s.empty[last_stage], (commits[last_stage] - 1u) & 1u,
+      if (aborted && ncommit > 0) {  // let issued MMAs finish before TMEM is freed
+        const uint32_t last = (ncommit - 1u) % kStages;
+        (void)mbar_wait_drain(&s.empty[last], (ring_uses(ncommit, last, kStages) - 1u) & 1u,
                               100000000ull);
       }
     }
