@@ -69,6 +69,13 @@ constexpr uint32_t kTxBytes = kAStage + kBStage + 512 + 1024;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSfStride = 16;               // scale slot per stage: A 4 + B 8 columns (16-aligned)
 
+// How many of the first n uses of a ring of S stages (taken in order) fell
+// on stage i: one counter per ring instead of a per-stage array, which a
+// run-time index would put in local memory.
+__device__ __forceinline__ uint32_t mx_ring_uses(uint32_t n, uint32_t i, uint32_t S) {
+  return n > i ? (n - i + S - 1) / S : 0u;
+}
+
 struct MxCtl {
   uint64_t full[kMaxStages];
   uint64_t empty[kMaxStages];
@@ -667,8 +674,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // -------------------------------------------------------- producer
     if (lane == 0) {
-      uint32_t stage = 0, phase = 0;
-      uint32_t fills[C::kStages] = {};
+      uint32_t stage = 0, phase = 0, nfill = 0;  // stages filled so far
       bool aborted = false;
       for (int t = blockIdx.x; t < ntiles && !aborted; t += gridDim.x) {
         const MxTile T = mx_decode<KIND>(t, p, s);
@@ -699,13 +705,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           bulk_load(st + kSfaOff, sfa + kb * sfa_step, 512, &s.full[stage]);
           bulk_load(st + kSfbOff, sfb + static_cast<size_t>(kb) * p.NBp * 512, 1024,
                     &s.full[stage]);
-          ++fills[stage];
+          ++nfill;
           if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
         }
       }
       if (aborted) {  // copies in flight land before the CTA exits
-        for (int i = 0; i < C::kStages; ++i)
-          if (fills[i] > 0) (void)mbar_wait_drain(&s.full[i], (fills[i] - 1u) & 1u, 100000000ull);
+        for (uint32_t i = 0; i < C::kStages; ++i) {
+          const uint32_t f = mx_ring_uses(nfill, i, C::kStages);
+          if (f > 0) (void)mbar_wait_drain(&s.full[i], (f - 1u) & 1u, 100000000ull);
+        }
       }
     }
   } else if (warp == 1) {
@@ -713,8 +721,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // one thread: waits, scale copies, MMAs and commits
     if (lane == 0) {
       uint32_t stage = 0, phase = 0, it = 0;
-      uint32_t commits[C::kStages] = {};
-      int last_stage = -1;
+      uint32_t ncommit = 0;  // stages whose MMAs were committed so far
       bool aborted = false;
       // descriptors of stage 0's A and scale blocks; stage i adds i * kStageBytes >> 4,
       // a k-step 2 (32 B >> 4)
@@ -760,15 +767,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           umma_commit<1>(&s.empty[stage]);
-          ++commits[stage];
-          last_stage = static_cast<int>(stage);
+          ++ncommit;
           if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
         }
         if (aborted) break;
         umma_commit<1>(&s.tfull[buf]);
       }
-      if (aborted && last_stage >= 0)  // issued MMAs finish before TMEM is freed
-        (void)mbar_wait_drain(&s.empty[last_stage], (commits[last_stage] - 1u) & 1u, 100000000ull);
+      if (aborted && ncommit > 0) {  // issued MMAs finish before TMEM is freed
+        const uint32_t last = (ncommit - 1u) % C::kStages;
+        (void)mbar_wait_drain(&s.empty[last], (mx_ring_uses(ncommit, last, C::kStages) - 1u) & 1u,
+                              100000000ull);
+      }
     }
   } else {
     // -------------------------------------------------------- epilogue
