@@ -554,16 +554,38 @@ def measure_mx(wl, inp, steps, pk, flushed, dev):
         "gpu_launches_per_step": len(MX_STEPS),
         "kernels": kern,
     }
-def mx_train_work(wl):
+def mx_train_work(wl, wgrad="mx"):
     """Per launch of the MXFP8 training step: (name, kind, amount) with kind
-    "tensor" (FLOPs of a block-scaled GEMM) or "hbm" (algorithmic bytes: bf16
-    read once, e4m3 codes and one scale byte per 32 elements written once)."""
+    "tensor" (FLOPs of a block-scaled GEMM), "tensor_bf16" (FLOPs of a bf16
+    grouped GEMM) or "hbm" (algorithmic bytes: bf16 read once, e4m3 codes and
+    one scale byte per 32 elements written once).  wgrad="bf16": the weight
+    gradients on the bf16 GEMM, with xs kept in bf16 by the forward and no
+    operand quantized along tokens."""
     T, D, E, K, F = wl.T, wl.D, wl.E, wl.K, wl.F
     R = T * K
 
     def quant(n_in, n_out):   # bf16 in, e4m3 + scales out
         return 2 * n_in + n_out + n_out // 32
 
+    if wgrad == "bf16":
+        return [
+            ("quantize_wi", "hbm", quant(E * D * 2 * F, 2 * E * D * 2 * F)),
+            ("quantize_wo", "hbm", quant(E * F * D, 2 * E * F * D)),
+            ("route", "hbm", hbm_bytes("route", T, D, E, K, F)),
+            ("permute_quantize", "hbm", mx_bytes("permute_quantize", T, D, E, K, F)),
+            ("permute_xs_bf16", "hbm", hbm_bytes("permute", T, D, E, K, F)),
+            ("fc1", "tensor", gemm_flops("fc1", R, D, F)),
+            ("fc2", "tensor", gemm_flops("fc2", R, D, F)),
+            ("combine", "hbm", hbm_bytes("combine", T, D, E, K, F)),
+            ("combine_bwd_quantize", "hbm",
+             hbm_bytes("combine_bwd", T, D, E, K, F) + R * D + R * D // 32),
+            ("fc2_dgrad", "tensor", gemm_flops("fc2_dlhs", R, D, F)),
+            ("fc2_wgrad_bf16", "tensor_bf16", gemm_flops("fc2_drhs", R, D, F)),
+            ("quantize_dz_rows", "hbm", quant(R * 2 * F, R * 2 * F)),
+            ("fc1_dgrad", "tensor", gemm_flops("fc1_dlhs", R, D, F)),
+            ("fc1_wgrad_bf16", "tensor_bf16", gemm_flops("fc1_drhs", R, D, F)),
+            ("permute_bwd", "hbm", hbm_bytes("permute_bwd", T, D, E, K, F)),
+        ]
     return [   # each weight read once for its two MX copies
         ("quantize_wi", "hbm", quant(E * D * 2 * F, 2 * E * D * 2 * F)),
         ("quantize_wo", "hbm", quant(E * F * D, 2 * E * F * D)),
@@ -587,15 +609,16 @@ def mx_train_work(wl):
     ]
 
 
-def measure_mx_train(wl, inp, steps, pk, flushed, dev):
+def measure_mx_train(wl, inp, steps, pk, flushed, dev, wgrad="mx"):
     """One MXFP8 training step per iteration through the C ABI: the weight
     quantizations (the weights change every step; one launch per weight
     writes its forward and dgrad copies), the MX forward
     with h and z kept in bf16, and the MX backward (see MoEBlockMX); an event
-    pair around every launch."""
+    pair around every launch.  wgrad="bf16": the weight gradients on the
+    bf16 grouped GEMM instead (MoEBlockMX(wgrad="bf16"))."""
     from mixture_experts_ffn_histogram_gb300 import binding as B
     from mixture_experts_ffn_histogram_gb300.block import MoEBlockMX
-    blk = MoEBlockMX(wl.T, wl.D, wl.E, wl.K, wl.F, wl.score_mode, train=True)
+    blk = MoEBlockMX(wl.T, wl.D, wl.E, wl.K, wl.F, wl.score_mode, train=True, wgrad=wgrad)
     d, D, F = blk.d, wl.D, wl.F
     offs = blk.group_offsets
     if wl.score_mode == B.SCORE_GIVEN:
@@ -636,7 +659,18 @@ def measure_mx_train(wl, inp, steps, pk, flushed, dev):
                                               blk.dztsc, offs, None, blk.dwi, blk.status, d),
         lambda: B.moe_permute_bwd(blk.dxs, blk.pos, blk.dx, d),
     ]
-    work = mx_train_work(wl)
+    if wgrad == "bf16":
+        calls = calls[:4] + [lambda: B.moe_permute(x, blk.pos, blk.xs, d)] + calls[4:8] + [
+            calls[10],
+            lambda: B.moe_grouped_gemm_fc2_bwd(blk.dys, blk.h, None, None, offs, None, blk.dwo,
+                                               blk.status, blk.ws, d),
+            calls[12],
+            calls[15],
+            lambda: B.moe_grouped_gemm_fc1_swiglu_bwd(blk.dz, None, blk.xs, None, offs, None,
+                                                      blk.dwi, blk.status, blk.ws, d),
+            calls[17],
+        ]
+    work = mx_train_work(wl, wgrad)
     assert len(work) == len(calls)
 
     def run(ev):
@@ -680,20 +714,27 @@ def measure_mx_train(wl, inp, steps, pk, flushed, dev):
             k["tflops"] = amount / avg / 1e12
             k["frac_tensor"] = amount / avg / 1e12 / fp8_peak
             gemm_s += avg
+        elif kind == "tensor_bf16":
+            k["tflops"] = amount / avg / 1e12
+            k["frac_tensor_bf16"] = amount / avg / 1e12 / bf16_peak
         else:
             k["gbs"] = amount / avg / 1e9
             k["frac_hbm"] = amount / avg / 1e9 / pk["hbm"]
         kern[n] = k
     flops = sum(a for _, kind, a in work if kind == "tensor")
+    mx_gemms = "all six GEMMs" if wgrad == "mx" else "the forward GEMMs and both dgrads"
     return {
-        "metric": "MoE block tokens/s (fwd+bwd, MXFP8)",
+        "metric": "MoE block tokens/s (fwd+bwd, MXFP8)" if wgrad == "mx" else
+                  "MoE block tokens/s (fwd+bwd, MXFP8 forward and dgrads, bf16 weight gradients)",
         "value": wl.T / step_s,
         "unit": "tokens/s",
         "ms_per_step": step_s * 1e3,
         "steps": steps,
-        "dtype": "e4m3 x e4m3 (E8M0 scales per 32) in all six GEMMs, fp32 accumulation, "
-                 "bf16 activations and gradients between them",
-        "step": "weights quantized (2 launches, both copies) + MX forward + MX backward",
+        "dtype": f"e4m3 x e4m3 (E8M0 scales per 32) in {mx_gemms}, fp32 accumulation, "
+                 "bf16 activations and gradients between them" +
+                 ("" if wgrad == "mx" else "; bf16 x bf16 weight gradients"),
+        "step": "weights quantized (2 launches, both copies) + MX forward + MX backward" +
+                ("" if wgrad == "mx" else " (weight gradients on the bf16 GEMM)"),
         "fp8_peak_tflops": fp8_peak,
         "fp8_peak_source": f"nominal 2 x bf16: {bf16_src}",
         "gemm_ms": gemm_s * 1e3,
@@ -913,11 +954,13 @@ def run_ours(args, dist, rank, world):
         del fstep
 
     # ---- the MXFP8 forward on the same inputs (a separate timed loop)
-    mx = mx_train = None
+    mx = mx_train = mx_train_bw = None
     if not args.no_mx:
         mx = measure_mx(wl_rank, inp, args.steps, pk, flushed, dev)
         if not fwd_only:
             mx_train = measure_mx_train(wl_rank, inp, args.steps, pk, flushed, dev)
+            mx_train_bw = measure_mx_train(wl_rank, inp, args.steps, pk, flushed, dev,
+                                           wgrad="bf16")
 
     # ---- end to end through the C ABI from pinned host buffers
     e2e = None
@@ -980,6 +1023,9 @@ def run_ours(args, dist, rank, world):
     if mx_train is not None:
         mx_train["value"] *= world
         line["mxfp8_train"] = mx_train
+    if mx_train_bw is not None:
+        mx_train_bw["value"] *= world
+        line["mxfp8_train_bf16_wgrad"] = mx_train_bw
     if configs is not None:
         line["configs"] = configs
     if rank == 0:

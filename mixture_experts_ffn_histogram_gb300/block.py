@@ -159,15 +159,23 @@ class MoEBlockMX:
     backward and the dwo wgrad, dz quantized along 2F and along tokens, x
     quantized along tokens straight from its token-major rows, the FC1
     dgrad and the dwi wgrad, and the permute backward.  Every buffer is
-    allocated once, in the library's MX layouts."""
+    allocated once, in the library's MX layouts.
+
+    ``wgrad="bf16"`` keeps the two weight gradients in bf16: the forward
+    also writes the sorted rows xs in bf16, and dwo = h^T dys, dwi = xs^T dz
+    run on the bf16 grouped GEMM, so no operand is quantized along tokens
+    (the forward and both dgrads stay in MXFP8)."""
 
     def __init__(self, T, D, E, K, F, score_mode=B.SCORE_SOFTMAX_TOPK, device="cuda",
-                 train=False):
+                 train=False, wgrad="mx"):
+        if wgrad not in ("mx", "bf16"):
+            raise ValueError(f"wgrad must be 'mx' or 'bf16', got {wgrad!r}")
         self.d = d = B.dims(T, D, E, K, F)
         self.T, self.D, self.E, self.K, self.F = T, D, E, K, F
         self.R = R = T * K
         self.mode = score_mode
         self.train = train
+        self.wgrad = wgrad
         dev = torch.device(device)
         i32, bf = torch.int32, torch.bfloat16
 
@@ -202,10 +210,13 @@ class MoEBlockMX:
             self.woq_b, self.wosc_b = u8(B.MX_WOQ_BWD), u8(B.MX_WOSC_BWD)
             self.dyq, self.dysc = u8(B.MX_DYQ), u8(B.MX_DYSC)
             self.dzq, self.dzsc = u8(B.MX_DZQ), u8(B.MX_DZSC)
-            self.xt, self.xtsc = u8(B.MX_XT), u8(B.MX_XTSC)
-            self.ht, self.htsc = u8(B.MX_HT), u8(B.MX_HTSC)
-            self.dyt, self.dytsc = u8(B.MX_DYT), u8(B.MX_DYTSC)
-            self.dzt, self.dztsc = u8(B.MX_DZT), u8(B.MX_DZTSC)
+            if wgrad == "mx":
+                self.xt, self.xtsc = u8(B.MX_XT), u8(B.MX_XTSC)
+                self.ht, self.htsc = u8(B.MX_HT), u8(B.MX_HTSC)
+                self.dyt, self.dytsc = u8(B.MX_DYT), u8(B.MX_DYTSC)
+                self.dzt, self.dztsc = u8(B.MX_DZT), u8(B.MX_DZTSC)
+            else:
+                self.xs = torch.empty((R, D), dtype=bf, device=dev)
         self.x = None
 
     def set_weights(self, wi, wo, stream=None):
@@ -224,6 +235,8 @@ class MoEBlockMX:
                               self.group_offsets, self.pos, self.row_src, self.status, self.ws,
                               d, stream)
         B.moe_mx_permute_quantize(x, self.pos, self.group_offsets, self.xq, self.xsc, d, stream)
+        if self.train and self.wgrad == "bf16":
+            B.moe_permute(x, self.pos, self.xs, d, stream)
         B.moe_mx_grouped_gemm_fc1_swiglu(self.xq, self.xsc, self.wiq, self.wisc,
                                          self.group_offsets, self.hq, self.hsc,
                                          self.h if self.train else None, self.status, d, stream,
@@ -243,6 +256,20 @@ class MoEBlockMX:
         offs = self.group_offsets
         B.moe_mx_combine_bwd(dy, self.ys, self.w, self.pos, offs, self.dys, self.dyq, self.dysc,
                              self.dw, d, stream)
+        if self.wgrad == "bf16":
+            B.moe_mx_grouped_gemm_fc2_bwd(self.dyq, self.dysc, self.woq_b, self.wosc_b, self.z,
+                                          None, None, None, None, offs, self.dz, None,
+                                          self.status, d, stream)
+            B.moe_grouped_gemm_fc2_bwd(self.dys, self.h, None, None, offs, None, self.dwo,
+                                       self.status, self.ws, d, stream)
+            B.moe_mx_quantize_rows(self.dz, 2 * F, offs, self.dzq, self.dzsc, d, stream)
+            B.moe_mx_grouped_gemm_fc1_bwd(self.dzq, self.dzsc, self.wiq_b, self.wisc_b, None,
+                                          None, None, None, offs, self.dxs, None, self.status,
+                                          d, stream)
+            B.moe_grouped_gemm_fc1_swiglu_bwd(self.dz, None, self.xs, None, offs, None, self.dwi,
+                                              self.status, self.ws, d, stream)
+            B.moe_permute_bwd(self.dxs, self.pos, self.dx, d, stream)
+            return self.dx
         B.moe_mx_quantize_tokens(self.dys, None, D, offs, self.dyt, self.dytsc, d, stream)
         B.moe_mx_quantize_tokens(self.h, None, F, offs, self.ht, self.htsc, d, stream)
         B.moe_mx_grouped_gemm_fc2_bwd(self.dyq, self.dysc, self.woq_b, self.wosc_b, self.z,

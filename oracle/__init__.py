@@ -453,13 +453,20 @@ def mx_block_forward(inp: dict) -> dict:
                 hsc=hsc, ys=ys, out=out)
 
 
-def mx_block_backward(inp: dict, fwd: dict) -> dict:
+def mx_block_backward(inp: dict, fwd: dict, wgrad: str = "mx") -> dict:
     """The MXFP8 backward in order, after :func:`mx_block_forward`: combine
     backward (bf16, as in the bf16 block); dys quantized along D and wo along
     D for the FC2 dgrad, whose output passes through the SwiGLU backward;
     dz quantized along 2F and wi along 2F for the FC1 dgrad; permute
     backward; then xs, h (both as the bf16 copies the block keeps), dys and
-    dz quantized along the tokens of each group for the two wgrads."""
+    dz quantized along the tokens of each group for the two wgrads.
+
+    ``wgrad="bf16"``: the two weight gradients instead take the same bf16
+    operands unquantized, dwo = h^T dys and dwi = xs^T dz per expert, as
+    :func:`fc2_bwd` and :func:`fc1_bwd` define them (the forward and the
+    dgrads unchanged)."""
+    if wgrad not in ("mx", "bf16"):
+        raise ValueError(f"wgrad must be 'mx' or 'bf16', got {wgrad!r}")
     wl = inp["workload"]
     T, D = wl.T, wl.D
     off = fwd["group_offsets"]
@@ -471,6 +478,11 @@ def mx_block_backward(inp: dict, fwd: dict) -> dict:
     dxs = mx_fc2(dzq, dzsc, iq, isc, off)
     dx = permute_bwd(dxs, fwd["pos"], T, D)
     hb = f32_to_bf16(fwd["h"])
+    if wgrad == "bf16":
+        _, dwo = fc2_bwd(dys, hb, inp["wo"], None, off, want_dlhs=False)
+        _, dwi = fc1_bwd(dz, fwd["xs"], inp["wi"], off, want_dlhs=False)
+        return dict(dys=dys, dw=dw, dq=dq, dsc=dsc, wiq_b=iq, wisc_b=isc, woq_b=oq, wosc_b=osc,
+                    dz=dz, dzq=dzq, dzsc=dzsc, dxs=dxs, dx=dx, hb=hb, dwo=dwo, dwi=dwi)
     xt = mx_quantize_tokens(bf16_to_f32(fwd["xs"]), off)
     ht = mx_quantize_tokens(bf16_to_f32(hb), off)
     dyt = mx_quantize_tokens(bf16_to_f32(dys), off)

@@ -618,6 +618,24 @@ def check_mx_block_backward(orc):
         got = g[name] if name == "dw" else bits_to_f64(g[name])
         r = rel(got, gr.numpy())
         assert r < 0.12, f"MX {name} vs dense autograd: relative error {r:.3f}"
+    # bf16 weight gradients: the dgrads unchanged, dwo = h^T dys and dwi =
+    # xs^T dz of the same bf16 operands per expert (float64 products rounded
+    # to bf16), and near the dense gradients like the MX ones
+    gb = orc.mx_block_backward(inp, f, wgrad="bf16")
+    for name in ("dys", "dz", "dxs", "dx", "dw"):
+        assert np.array_equal(gb[name], g[name]), f"bf16 weight gradients changed {name}"
+    off = f["group_offsets"]
+    H, DY, DZ, XS = (bits_to_f64(a) for a in (g["hb"], g["dys"], g["dz"], f["xs"]))
+    for e in range(4):
+        r0, r1 = off[e], off[e + 1]
+        want_o, want_i = H[r0:r1].T @ DY[r0:r1], XS[r0:r1].T @ DZ[r0:r1]
+        assert max_excess(bits_to_f64(gb["dwo"][e]), want_o, U / 2 + 1e-5,
+                          1e-5 * np.abs(want_o).max()) <= 0, "bf16 dwo differs from h^T dys"
+        assert max_excess(bits_to_f64(gb["dwi"][e]), want_i, U / 2 + 1e-5,
+                          1e-5 * np.abs(want_i).max()) <= 0, "bf16 dwi differs from xs^T dz"
+    for name, gr in (("dwi", WI.grad), ("dwo", WO.grad)):
+        r = rel(bits_to_f64(gb[name]), gr.numpy())
+        assert r < 0.12, f"bf16 {name} on MX activations vs dense autograd: {r:.3f}"
 
 
 ALL_CHECKS = [check_bf16_rounding, check_route, check_histogram, check_permute_combine,

@@ -86,3 +86,22 @@ def test_block_roofline_is_the_sum_of_kernel_rooflines():
     assert abs(kern["fc1"]["roofline_us"] - fl / 1924.2e12 * 1e6) < 1e-6
     assert abs(kern["permute"]["roofline_us"] -
                bench.hbm_bytes("permute", wl.T, wl.D, wl.E, wl.K, wl.F) / 6688.8e9 * 1e6) < 1e-6
+
+
+def test_mx_train_work_with_bf16_weight_gradients():
+    """The MX training step with bf16 weight gradients keeps the same six
+    GEMMs (two of them on the bf16 tensor peak), drops the four launches
+    that quantize along tokens and adds the bf16 permute of xs."""
+    wl = WORKLOADS["long_seq_train"]
+    mx = bench.mx_train_work(wl)
+    bw = bench.mx_train_work(wl, "bf16")
+    names_mx = [n for n, _, _ in mx]
+    names_bw = [n for n, _, _ in bw]
+    assert len(bw) == len(mx) - 3
+    assert not any("tokens" in n for n in names_bw)
+    assert "permute_xs_bf16" in names_bw and "permute_xs_bf16" not in names_mx
+    flops = lambda w: sum(a for _, k, a in w if k.startswith("tensor"))  # noqa: E731
+    assert flops(bw) == flops(mx)
+    assert [n for n, k, _ in bw if k == "tensor_bf16"] == ["fc2_wgrad_bf16", "fc1_wgrad_bf16"]
+    assert dict((n, a) for n, _, a in bw)["fc1_wgrad_bf16"] == dict(
+        (n, a) for n, _, a in mx)["fc1_wgrad"]

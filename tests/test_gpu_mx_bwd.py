@@ -263,9 +263,9 @@ def test_wgrads(case):
 
 
 # ------------------------------------------------------------ end to end
-def _mx_train_step(wl, inp):
+def _mx_train_step(wl, inp, wgrad="mx"):
     """Forward and backward through MoEBlockMX (the C ABI only)."""
-    blk = MoEBlockMX(wl.T, wl.D, wl.E, wl.K, wl.F, wl.score_mode, train=True)
+    blk = MoEBlockMX(wl.T, wl.D, wl.E, wl.K, wl.F, wl.score_mode, train=True, wgrad=wgrad)
     for t in (blk.dx, blk.dwi, blk.dwo, blk.dz, blk.dys, blk.out):
         t.fill_(float("nan"))
     blk.dw.fill_(float("nan"))
@@ -292,6 +292,29 @@ def test_train_step_end_to_end(case):
     _close("dx", to_host(blk.dx), refb["dx"], 2e-2, 2e-2)
     _close("dwo", to_host(blk.dwo), refb["dwo"], 2e-2, 2e-2)
     _close("dwi", to_host(blk.dwi), refb["dwi"], 2e-2, 2e-2)
+
+
+def test_train_step_bf16_wgrad(case):
+    """The MX block with bf16 weight gradients (wgrad="bf16"): the forward
+    and the dgrads are the same launches on the same inputs, so out, dys,
+    dz and dx equal the all-MX step's bit for bit; dwo = h^T dys and dwi =
+    xs^T dz on the bf16 grouped GEMM, against the oracle's bf16 products of
+    its own MX-path operands (end-to-end bar)."""
+    wl, inp, ref, refb = case
+    refw = oracle.mx_block_backward(inp, ref, wgrad="bf16")
+    mx = _mx_train_step(wl, inp)
+    blk = _mx_train_step(wl, inp, wgrad="bf16")
+    used = int(ref["group_offsets"][-1])
+    for name in ("out", "dx", "dw"):
+        assert_exact(name, to_host(getattr(blk, name)), to_host(getattr(mx, name)))
+    for name in ("dys", "dz"):
+        assert_exact(name, to_host(getattr(blk, name))[:used], to_host(getattr(mx, name))[:used])
+    assert_exact("xs", to_host(blk.xs)[:used], ref["xs"])
+    _close("dwo", to_host(blk.dwo), refw["dwo"], 2e-2, 2e-2)
+    _close("dwi", to_host(blk.dwi), refw["dwi"], 2e-2, 2e-2)
+    empty = np.flatnonzero(np.diff(ref["group_offsets"]) == 0)
+    if empty.size:
+        assert not to_host(blk.dwo)[empty].any() and not to_host(blk.dwi)[empty].any()
 
 
 def test_all_tokens_to_one_expert():
