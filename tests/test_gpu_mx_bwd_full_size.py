@@ -166,3 +166,78 @@ def test_weight_gradients_of_sampled_experts(run):
         want = oracle.mx_wgrad(xt, dzt, g1)[0]                     # [D, 2m]
         got = to_host(blk.dwi[e][:, torch.from_numpy(cols).long().cuda()])
         _close_bits(f"dwi[{e}] columns {cols.tolist()}", got, want)
+
+
+@pytest.fixture(scope="module")
+def run_bw():
+    """The same step with the weight gradients on the bf16 GEMM
+    (MoEBlockMX(wgrad="bf16"), as bench.py's mxfp8_train_bf16_wgrad)."""
+    need_gpu()
+    wl = WORKLOADS["long_seq_train"]
+    inp = make_inputs(wl, torch.device("cuda"), with_grad=True)
+    blk = MoEBlockMX(wl.T, wl.D, wl.E, wl.K, wl.F, wl.score_mode, train=True, wgrad="bf16")
+    for t in (blk.out, blk.h, blk.z, blk.dys, blk.dz, blk.dxs, blk.dx, blk.dwi, blk.dwo, blk.xs):
+        t.fill_(float("nan"))
+    blk.set_weights(inp["wi"], inp["wo"])
+    blk.forward(inp["x"], logits=inp["logits"], bias=inp["bias"])
+    blk.backward(inp["dy"])
+    torch.cuda.synchronize()
+    assert int(blk.status.item()) == 0
+    ids_ref, w_ref = oracle.route(to_host(inp["logits"]), to_host(inp["bias"]), wl.score_mode,
+                                  wl.T, wl.E, wl.K)
+    gs, off, pos, row_src, bad = oracle.histogram(ids_ref, wl.E)
+    rng = np.random.Generator(np.random.PCG64(29))
+    sizes = np.diff(off)
+    experts = sorted({int(np.argmax(sizes)), int(np.argmin(np.where(sizes > 0, sizes, 1 << 30))),
+                      int(rng.integers(0, wl.E))})
+    yield dict(wl=wl, inp=inp, blk=blk, w=w_ref, off=off, row_src=row_src, experts=experts,
+               rng=rng)
+    del blk, inp
+    torch.cuda.empty_cache()
+
+
+def test_bf16_weight_gradients_of_sampled_experts(run_bw):
+    """With bf16 weight gradients: every output written; dwo[e][f, :] =
+    h_f^T dys and dwi[e][:, n] = xs^T dz_n for a few f (n = f, F + f) of the
+    largest, the smallest and a random expert on their whole groups, with
+    h, dys and dz of those columns recomputed by the oracle's MX forward and
+    dgrad, the products by its bf16 fc2_bwd / fc1_bwd."""
+    wl, inp, blk, off, row_src = (run_bw[k] for k in ("wl", "inp", "blk", "off", "row_src"))
+    D, F, K = wl.D, wl.F, wl.K
+    R = int(off[-1])
+    for name, t in (("dwi", blk.dwi), ("dwo", blk.dwo), ("dx", blk.dx), ("xs", blk.xs[:R])):
+        assert bool(torch.isfinite(t).all()), f"{name}: elements left unwritten (NaN) or not finite"
+    for e in run_bw["experts"]:
+        n = int(off[e + 1] - off[e])
+        if n == 0:
+            continue
+        j = row_src[off[e]:off[e + 1]]
+        t, k = j // K, j % K
+        ti = torch.from_numpy(t).long().cuda()
+        sel = np.array(sorted({0, F - 1, int(run_bw["rng"].integers(0, F))}))
+        m = len(sel)
+        g1 = np.array([0, n], np.int32)
+        xs = to_host(inp["x"][ti])
+        dys, _ = oracle.combine_bwd(to_host(inp["dy"][ti]), np.zeros((n, D), np.uint16),
+                                    run_bw["w"][t, k][:, None],
+                                    np.arange(n, dtype=np.int32)[:, None])
+        wi_e = oracle.bf16_to_f32(to_host(inp["wi"][e]))          # [D, 2F]
+        cols = np.concatenate([sel, F + sel])
+        wq, wsc = oracle.mx_quantize(np.ascontiguousarray(wi_e[:, cols].T))
+        xq, xsc = oracle.mx_quantize(oracle.bf16_to_f32(xs))
+        h, z = oracle.mx_fc1_swiglu(xq, xsc, wq.reshape(1, 2 * m, D), wsc.reshape(1, 2 * m, -1),
+                                    g1, want_z=True)
+        hb = oracle.f32_to_bf16(h)                                 # [n, m]
+        wo_sub = to_host(inp["wo"][e][torch.from_numpy(sel).long().cuda()])[None]  # [1, m, D]
+        _, want = oracle.fc2_bwd(dys, hb, wo_sub, None, g1, want_dlhs=False)
+        got = to_host(blk.dwo[e][torch.from_numpy(sel).long().cuda()])
+        _close_bits(f"dwo[{e}] rows {sel.tolist()} (bf16)", got, want[0])
+        wo_e = oracle.bf16_to_f32(to_host(inp["wo"][e]))          # [F, D]
+        oq, osc = oracle.mx_quantize(np.ascontiguousarray(wo_e[sel]))
+        dq, dsc = oracle.mx_quantize(oracle.bf16_to_f32(dys))
+        dz = oracle.mx_fc2_dgrad_swiglu(dq, dsc, oq.reshape(1, m, D), osc.reshape(1, m, -1), z,
+                                        g1)                         # [n, 2m]
+        wi_sub = np.ascontiguousarray(to_host(inp["wi"][e])[:, cols])[None]        # [1, D, 2m]
+        _, want = oracle.fc1_bwd(dz, xs, wi_sub, g1, want_dlhs=False)
+        got = to_host(blk.dwi[e][:, torch.from_numpy(cols).long().cuda()])
+        _close_bits(f"dwi[{e}] columns {cols.tolist()} (bf16)", got, want[0])
